@@ -1,0 +1,214 @@
+"""Float64 CPU oracle for Hogwild! concurrent decode attention and block commit.
+
+TEST INFRASTRUCTURE ONLY.  The product path (the ``concurrent_shared_kv_gb300``
+package and its CUDA library) never imports this package; only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` do.  It shares
+no code with the CUDA path: the arithmetic lives in ``hwref.c`` (plain C, double
+precision) and the layout builder below is written independently of the
+library's own.
+
+Pages followed (title, section):
+  * "Hogwild! Inference: Parallel LLM Generation via Concurrent Attention"
+    (paper notes): key design 1 (the query-rotation equation), key design 2
+    (combined cache layout; step commit), implementation notes (block-local
+    positions, query rotation handles the real position).
+  * omica.com.cn article on Hogwild! Inference: section 2.1 (rotate_query),
+    section 3.2 (blockwise attention with one softmax across blocks).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+BUILD_DIR = os.path.join(HERE, "_build")
+SRC = os.path.join(HERE, "hwref.c")
+
+F32, BF16 = 0, 1
+
+
+def lib_path(mutant: int = 0) -> str:
+    name = "libhwref.so" if mutant == 0 else f"libhwref_mutant{mutant}.so"
+    return os.path.join(BUILD_DIR, name)
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    """Compile hwref.c with gcc (IEEE double, no fast-math)."""
+    out = lib_path(mutant)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(SRC):
+        return out
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-shared", "-fPIC",
+           "-pthread", f"-DHWREF_MUTANT={mutant}", SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+class HwrefDesc(ctypes.Structure):
+    _fields_ = [
+        ("n_rows", ctypes.c_int32),
+        ("n_q_heads", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("n_blocks", ctypes.c_int32),
+        ("max_view_blocks", ctypes.c_int32),
+        ("cache_capacity", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
+        ("rope_theta", ctypes.c_double),
+        ("scale", ctypes.c_double),
+    ]
+
+
+_P = ctypes.c_void_p
+
+
+class Oracle:
+    """ctypes handle on one build of hwref.c (the default, or a planted mutant)."""
+
+    def __init__(self, mutant: int = 0):
+        self.mutant = mutant
+        self.lib = ctypes.CDLL(build(mutant))
+        L = self.lib
+        L.hwref_rope.argtypes = [_P, ctypes.c_int, ctypes.c_double, ctypes.c_double, _P]
+        L.hwref_rope.restype = None
+        L.hwref_rope_freqs.argtypes = [ctypes.c_int, ctypes.c_double, _P]
+        L.hwref_rope_freqs.restype = None
+        L.hwref_attn_decode.argtypes = [ctypes.POINTER(HwrefDesc), _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P, _P, ctypes.c_int32, ctypes.c_int, _P, _P, ctypes.c_int]
+        L.hwref_attn_decode.restype = ctypes.c_int
+        L.hwref_block_commit.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
+                                         ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32,
+                                         ctypes.c_int32, _P]
+        L.hwref_block_commit.restype = ctypes.c_int
+        L.hwref_bf16_from_double.argtypes = [ctypes.c_double]
+        L.hwref_bf16_from_double.restype = ctypes.c_uint16
+
+    # -- RoPE ---------------------------------------------------------------
+    def rope(self, x, theta: float, pos: float) -> np.ndarray:
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        y = np.empty_like(x)
+        self.lib.hwref_rope(x.ctypes.data, x.shape[-1], float(theta), float(pos), y.ctypes.data)
+        return y
+
+    def freqs(self, D: int, theta: float) -> np.ndarray:
+        w = np.empty(D // 2, np.float64)
+        self.lib.hwref_rope_freqs(D, float(theta), w.ctypes.data)
+        return w
+
+    def bf16_from_double(self, x: float) -> int:
+        return int(self.lib.hwref_bf16_from_double(float(x)))
+
+    # -- decode -------------------------------------------------------------
+    def attn_decode(self, *, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
+                    q_pos, n_kv_heads: int, rope_theta: float, scale: float, dtype: int,
+                    q_to_kv=None, rows: Optional[Sequence[int]] = None, brute: bool = False,
+                    n_threads: Optional[int] = None):
+        """Returns (out [rows][Hq][D] float64, lse [rows][Hq] float64).
+
+        q, k_cache, v_cache hold storage values: float32 arrays for ``dtype=F32``,
+        uint16 bf16 bit patterns for ``dtype=BF16``.  k_cache/v_cache are
+        [Hkv][capacity][D].  Unselected rows of the outputs are NaN.
+        """
+        sd = np.float32 if dtype == F32 else np.uint16
+        q = np.ascontiguousarray(q, dtype=sd)
+        k_cache = np.ascontiguousarray(k_cache, dtype=sd)
+        v_cache = np.ascontiguousarray(v_cache, dtype=sd)
+        n_rows, Hq, D = q.shape
+        assert k_cache.shape[0] == n_kv_heads and k_cache.shape[2] == D
+        assert v_cache.shape == k_cache.shape
+        i32 = lambda a: np.ascontiguousarray(a, dtype=np.int32)
+        block_start, block_len = i32(block_start), i32(block_len)
+        view_block, view_offset, q_pos = i32(view_block), i32(view_offset), i32(q_pos)
+        assert view_block.shape == view_offset.shape and view_block.shape[0] == n_rows
+        qmap = None if q_to_kv is None else i32(q_to_kv)
+        sel = None if rows is None else i32(rows)
+        desc = HwrefDesc(n_rows, Hq, n_kv_heads, D, int(block_len.shape[0]),
+                         int(view_block.shape[1]), int(k_cache.shape[1]), dtype,
+                         float(rope_theta), float(scale))
+        out = np.full((n_rows, Hq, D), np.nan)
+        lse = np.full((n_rows, Hq), np.nan)
+        nt = n_threads or len(os.sched_getaffinity(0))
+        rc = self.lib.hwref_attn_decode(
+            ctypes.byref(desc), q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
+            block_start.ctypes.data, block_len.ctypes.data, view_block.ctypes.data,
+            view_offset.ctypes.data, q_pos.ctypes.data,
+            None if qmap is None else qmap.ctypes.data,
+            None if sel is None else sel.ctypes.data, 0 if sel is None else len(sel),
+            1 if brute else 0, out.ctypes.data, lse.ctypes.data, int(nt))
+        if rc != 0:
+            raise ValueError(f"hwref_attn_decode rejected its inputs (status {rc})")
+        return out, lse
+
+    # -- commit -------------------------------------------------------------
+    def block_commit(self, *, dtype: int, rope_theta: float, k_src, v_src, src_begin: int,
+                     n_tokens: int, k_dst, v_dst, dst_offset: int, pos_delta: int,
+                     want_exact: bool = False):
+        """In-place on copies of k_dst/v_dst ([Hkv][cap][D] storage values).
+
+        Returns (k_dst_new, v_dst_new[, k_exact [Hkv][n][D] float64]).
+        """
+        sd = np.float32 if dtype == F32 else np.uint16
+        k_src = np.ascontiguousarray(k_src, dtype=sd)
+        v_src = np.ascontiguousarray(v_src, dtype=sd)
+        kd = np.array(k_dst, dtype=sd, copy=True, order="C")
+        vd = np.array(v_dst, dtype=sd, copy=True, order="C")
+        Hkv, _, D = k_src.shape
+        exact = np.zeros((Hkv, n_tokens, D)) if want_exact else None
+        rc = self.lib.hwref_block_commit(
+            dtype, Hkv, D, float(rope_theta), k_src.ctypes.data, v_src.ctypes.data,
+            int(k_src.shape[1]) * D, int(src_begin), int(n_tokens), kd.ctypes.data,
+            vd.ctypes.data, int(kd.shape[1]) * D, int(dst_offset), int(pos_delta),
+            None if exact is None else exact.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"hwref_block_commit rejected its inputs (status {rc})")
+        return (kd, vd, exact) if want_exact else (kd, vd)
+
+
+_default: Optional[Oracle] = None
+
+
+def get(mutant: int = 0) -> Oracle:
+    global _default
+    if mutant:
+        return Oracle(mutant)
+    if _default is None:
+        _default = Oracle(0)
+    return _default
+
+
+# ---------------------------------------------------------------------------
+# Views: the combined layout, written out independently of the library.
+# ---------------------------------------------------------------------------
+
+def combined_views(block_len: Sequence[int], n_problems: int, n_workers: int):
+    """The combined cache layout of key design 2: each worker sees the common
+    block, then the other workers' in-progress blocks in worker order, then its
+    own block.  Problem p owns blocks p*(W+1) (common) and p*(W+1)+1+w (worker w).
+
+    Returns (view_block [rows][W+1], view_offset [rows][W+1], q_pos [rows]); the
+    offset of a block is the number of tokens before it in that worker's view and
+    the query sits right after the whole view (i_q = view length).
+    """
+    W = n_workers
+    rows = n_problems * W
+    vb = np.full((rows, W + 1), -1, np.int32)
+    vo = np.zeros((rows, W + 1), np.int32)
+    qp = np.zeros(rows, np.int32)
+    for p in range(n_problems):
+        base = p * (W + 1)
+        for w in range(W):
+            order = [base] + [base + 1 + o for o in range(W) if o != w] + [base + 1 + w]
+            pos = 0
+            for v, b in enumerate(order):
+                vb[p * W + w, v] = b
+                vo[p * W + w, v] = pos
+                pos += int(block_len[b])
+            qp[p * W + w] = pos
+    return vb, vo, qp
