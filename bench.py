@@ -1,0 +1,362 @@
+"""Benchmark: concurrent decode attention (Hogwild! Inference) on GB300.
+
+One step = one decode token for every worker through the whole layer stack:
+64 sequential hw_attn_decode calls (one per layer, each layer with its own K/V
+pools) on the 32B-shaped 4-worker 16K-context workload.  The metric is KV HBM
+GB/s (algorithmic bytes: every K and V row of the step read once, shared by all
+workers and query heads) and worker-tokens/s per layer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  --impl reference times the float64 CPU oracle on the
+same workload (a bounded sample of layers per step) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "concurrent decode attention: KV HBM GB/s vs 8 TB/s peak; worker-tokens/s per layer"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", default="C3", choices=["C2", "C3", "C4", "C5"])
+    p.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def reference_arm(args):
+    """The float64 oracle on the host cores, on the same workload and metric."""
+    import numpy as np
+    import oracle
+    from concurrent_shared_kv_gb300 import api
+    from concurrent_shared_kv_gb300 import workloads as wl
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = wl.ALL[args.config]()
+    o = oracle.get()
+    lens, starts = w.block_lengths(), w.block_starts()
+    vb, vo, qp = api.views_combined(lens, w.n_problems, w.n_workers)
+    cores = len(os.sched_getaffinity(0))
+    # each step: one full layer (all rows, all heads) of the workload; for the
+    # ragged serving shape, 2 of its 16 problems
+    rows = None if args.config != "C5" else list(range(0, 4)) + list(range(60, 64))
+    frac_rows = 1.0 if rows is None else len(rows) / w.n_rows
+    times = []
+    q, k, v = wl.draw_host(w, 0)
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        o.attn_decode(q=q, k_cache=k, v_cache=v, block_start=starts, block_len=lens,
+                      view_block=vb, view_offset=vo, q_pos=qp, n_kv_heads=w.n_kv_heads,
+                      rope_theta=w.rope_theta, scale=w.scale,
+                      dtype=oracle.F32 if w.dtype == "f32" else oracle.BF16, rows=rows,
+                      n_threads=cores)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t_layer = statistics.median(times) / frac_rows
+    gbs = w.kv_bytes_per_layer() / t_layer / 1e9
+    sample = (f"one layer per step ({'all rows' if rows is None else 'problems 0 and 15, scaled to 16'}),"
+              f" float64 oracle, {cores} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_layer * w.layers * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.layers},
+        "worker_tokens_per_s_per_layer": w.n_rows / t_layer,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from concurrent_shared_kv_gb300 import api, engine
+    from concurrent_shared_kv_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    w = wl.ALL[args.config]()
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    L = w.layers if args.config != "C5" else 1
+    lens, starts = w.block_lengths(), w.block_starts()
+    vb, vo, qp = api.views_combined(lens, w.n_problems, w.n_workers)
+    sess = engine.DecodeSession(n_rows=w.n_rows, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+                                head_dim=w.head_dim, n_blocks=w.n_blocks,
+                                max_view_blocks=w.n_workers + 1, capacity=w.capacity, dtype=tdt,
+                                rope_theta=w.rope_theta, scale=w.scale, device=dev)
+    sess.set_metadata(starts, lens, vb, vo, qp)
+    qs, ks, vs = [], [], []
+    for l in range(L):
+        q, k, v = wl.draw_device_layer(w, l, dev)
+        qs.append(q)
+        ks.append(k)
+        vs.append(v)
+    outs = [torch.empty_like(qs[0]) for _ in range(L)]
+    lses = [torch.empty((w.n_rows, w.n_q_heads), dtype=torch.float32, device=dev) for _ in range(L)]
+    calls_per_step = L if args.config != "C5" else 64  # C5: one layer timed x64
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for i in range(calls_per_step):
+            l = i % L
+            sess.decode(qs[l], ks[l], vs[l], out=outs[l], lse=lses[l], stream=stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        stream.synchronize()
+        for _ in range(2):
+            graph.replay()
+        stream.synchronize()
+    flags = sess.device_flags()
+    assert flags == 0, f"device flags {flags}"
+
+    def run_timed(n):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(n):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    step()
+            end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        return start.elapsed_time(end) / 1e3
+
+    with ClockSampler(local) as clk:
+        t = run_timed(args.steps)
+    if world > 1:
+        tt = torch.tensor([t], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+
+    step_bytes = w.kv_bytes_per_layer() * calls_per_step
+    per_step = t / args.steps
+    gbs_rank = step_bytes / per_step / 1e9
+    value = gbs_rank * world  # replicas: every rank streams its own copy
+    per_launch = per_step / calls_per_step
+    achieved = w.kv_bytes_per_layer() / per_launch / 1e9
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+
+    # end to end through the public API with host buffers: each step uploads
+    # every layer's query from pinned host memory and reads every layer's
+    # output and lse back; the KV pools are the resident cache state.
+    q_host = [q.cpu().pin_memory() for q in qs]
+    o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    l_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in lses]
+    qdev = [torch.empty_like(q) for q in qs]
+    meta_host = [torch.from_numpy(np.ascontiguousarray(x, np.int32)).pin_memory()
+                 for x in (starts, lens, vb, vo, qp)]
+    h2d = sum(q.numel() * q.element_size() for q in q_host) + sum(m.numel() * 4 for m in meta_host)
+    d2h = sum(o.numel() * o.element_size() for o in o_host) + sum(x.numel() * 4 for x in l_host)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for m, name in zip(meta_host, ("block_start", "block_len", "view_block", "view_offset", "q_pos")):
+                sess.meta[name].copy_(m, non_blocking=True)
+            for l in range(L):
+                qdev[l].copy_(q_host[l], non_blocking=True)
+            for i in range(calls_per_step):
+                l = i % L
+                sess.decode(qdev[l], ks[l], vs[l], out=outs[l], lse=lses[l], stream=stream)
+            for l in range(L):
+                o_host[l].copy_(outs[l], non_blocking=True)
+                l_host[l].copy_(lses[l], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    stream.synchronize()
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+        stream.synchronize()
+    t_e2e = (time.perf_counter() - t0) / e2e_steps
+    e2e_gbs = step_bytes / t_e2e / 1e9 * world
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {
+            "workload": w.name, "layers_per_step": calls_per_step, "problems": w.n_problems,
+            "workers": w.n_workers, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "kv_tokens_per_layer": w.kv_tokens(),
+            "kv_bytes_per_step": step_bytes, "parallelism": f"replicas x{world}",
+            "mode": "eager" if graph is None else "cuda-graph",
+            "l2": "inputs larger than L2: each step reads every layer's own KV pools "
+                  f"({step_bytes / 1e9:.2f} GB per step vs 0.13 GB of L2)",
+        },
+        "frac_of_8TBps": gbs_rank / NOMINAL_HBM_GBS,
+        "worker_tokens_per_s_per_layer": w.n_rows / per_launch,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "hw_attn_decode (decode_simt_kernel)"},
+        "gpu_launches": calls_per_step * args.steps,
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = timed_oracle(w, qs, ks, vs, starts, lens, vb, vo, qp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def timed_oracle(w, qs, ks, vs, starts, lens, vb, vo, qp, budget_s=12.0):
+    """The oracle, as it stands, over whole layers of the same workload on the
+    host cores for about budget_s seconds (at least one layer); GB/s of KV."""
+    import numpy as np
+    import torch
+    import oracle
+
+    def host(t):
+        t = t.detach().cpu().contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    cores = len(os.sched_getaffinity(0))
+    rows = None if w.n_problems == 1 else list(range(0, w.n_workers))  # one problem of the batch
+    done, spent = 0, 0.0
+    while True:
+        l = done % len(qs)
+        q, k, v = host(qs[l]), host(ks[l]), host(vs[l])
+        t0 = time.perf_counter()
+        oracle.get().attn_decode(q=q, k_cache=k, v_cache=v, block_start=starts, block_len=lens,
+                                 view_block=vb, view_offset=vo, q_pos=qp,
+                                 n_kv_heads=w.n_kv_heads, rope_theta=w.rope_theta, scale=w.scale,
+                                 dtype=oracle.F32 if w.dtype == "f32" else oracle.BF16, rows=rows,
+                                 n_threads=cores)
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent >= budget_s or done >= 64:
+            break
+    if rows is None:
+        nbytes = w.kv_bytes_per_layer() * done
+        what = f"{done} whole layer(s), all rows and heads"
+    else:
+        per_problem = (w.common_len[0] + sum(w.worker_len[0])) * w.n_kv_heads * w.head_dim * 2 * w.elem_bytes
+        nbytes = per_problem * done
+        what = f"{done} layer(s) of problem 0 only"
+    return {"value": nbytes / spent / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{what}, float64, {cores} threads, {spent:.1f} s"}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+"""Thin ctypes binding of libhogwild (include/hogwild.h): argument marshalling only.
+
+Every function maps one-to-one to a C entry point of the same name without the
+``hw_`` prefix.  Tensors are passed as device pointers (``tensor.data_ptr()``);
+all computation happens in the library's CUDA kernels.  If the library has not
+been built this module raises on first use: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libhogwild.so")
+
+HW_OK = 0
+HW_F32, HW_BF16 = 0, 1
+STATUS = {0: "HW_OK", -1: "HW_ERR_INVALID", -2: "HW_ERR_UNSUPPORTED", -3: "HW_ERR_WORKSPACE",
+          -4: "HW_ERR_CAPACITY", -5: "HW_ERR_OVERLAP", -6: "HW_ERR_CUDA", -7: "HW_ERR_DEVICE"}
+DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMAP",
+             8: "HW_DEV_TOO_MANY_REFS", 16: "HW_DEV_TIMEOUT"}
+
+# every symbol the header declares
+EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode",
+           "hw_block_commit", "hw_workspace_status", "hw_views_combined", "hw_last_cuda_error",
+           "hw_status_string"]
+
+
+class HwError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS.get(status, status)} ({status})")
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [
+        ("n_rows", ctypes.c_int32),
+        ("n_q_heads", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("n_blocks", ctypes.c_int32),
+        ("max_view_blocks", ctypes.c_int32),
+        ("cache_capacity", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
+        ("rope_theta", ctypes.c_double),
+        ("scale", ctypes.c_float),
+    ]
+
+
+_P = ctypes.c_void_p
+_lib = None
+
+
+def lib(path: Optional[str] = None):
+    """Load libhogwild.so (built by ``concurrent_shared_kv_gb300.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libhogwild.so not found at {p}: build it with "
+                           "`python -m concurrent_shared_kv_gb300.build` (no fallback path exists)")
+    L = ctypes.CDLL(p)
+    L.hw_attn_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_size_t)]
+    L.hw_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
+    L.hw_attn_decode.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12 + [ctypes.c_size_t, _P]
+    L.hw_block_commit.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
+                                  ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32,
+                                  ctypes.c_int32, _P]
+    L.hw_workspace_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
+    L.hw_views_combined.argtypes = [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
+    L.hw_last_cuda_error.argtypes = []
+    L.hw_status_string.argtypes = [ctypes.c_int]
+    L.hw_status_string.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        if name != "hw_status_string":
+            getattr(L, name).restype = ctypes.c_int
+    if path is None:
+        _lib = L
+    return L
+
+
+def _ptr(x) -> Optional[int]:
+    """Device/host pointer of a tensor, numpy array or int (None stays NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(type(x))
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        try:
+            import torch
+            return torch.cuda.current_stream().cuda_stream or None
+        except Exception:
+            return None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _check(fn: str, st: int):
+    if st != HW_OK:
+        raise HwError(fn, st)
+
+
+def make_desc(n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, max_view_blocks, cache_capacity,
+              dtype, rope_theta, scale) -> AttnDesc:
+    return AttnDesc(int(n_rows), int(n_q_heads), int(n_kv_heads), int(head_dim), int(n_blocks),
+                    int(max_view_blocks), int(cache_capacity), int(dtype), float(rope_theta),
+                    float(scale))
+
+
+def attn_decode_workspace_size(desc: AttnDesc) -> int:
+    n = ctypes.c_size_t(0)
+    _check("hw_attn_decode_workspace_size", lib().hw_attn_decode_workspace_size(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)
+
+
+def workspace_init(workspace, nbytes: int, stream=None):
+    _check("hw_workspace_init", lib().hw_workspace_init(_ptr(workspace), int(nbytes), _stream(stream)))
+
+
+def attn_decode(desc: AttnDesc, q, k_cache, v_cache, block_start, block_len, view_block,
+                view_offset, q_pos, out, lse, workspace, workspace_bytes: int, q_to_kv=None,
+                stream=None) -> int:
+    """hw_attn_decode; returns the status (raises on failure)."""
+    st = lib().hw_attn_decode(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(block_start), _ptr(block_len), _ptr(view_block),
+                              _ptr(view_offset), _ptr(q_pos), _ptr(q_to_kv), _ptr(out), _ptr(lse),
+                              _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check("hw_attn_decode", st)
+    return st
+
+
+def block_commit(dtype: int, n_layers: int, n_kv_heads: int, head_dim: int, rope_theta: float,
+                 k_src, v_src, src_capacity: int, src_begin: int, n_tokens: int, k_dst, v_dst,
+                 dst_capacity: int, dst_offset: int, pos_delta: int, stream=None) -> int:
+    st = lib().hw_block_commit(int(dtype), int(n_layers), int(n_kv_heads), int(head_dim),
+                               float(rope_theta), _ptr(k_src), _ptr(v_src), int(src_capacity),
+                               int(src_begin), int(n_tokens), _ptr(k_dst), _ptr(v_dst),
+                               int(dst_capacity), int(dst_offset), int(pos_delta), _stream(stream))
+    _check("hw_block_commit", st)
+    return st
+
+
+def workspace_status(workspace, stream=None) -> int:
+    """Device error bits (HW_DEV_*) since the last read; synchronises the stream."""
+    f = ctypes.c_int32(0)
+    _check("hw_workspace_status", lib().hw_workspace_status(_ptr(workspace), ctypes.byref(f), _stream(stream)))
+    return int(f.value)
+
+
+def views_combined(block_len, n_problems: int, n_workers: int):
+    """Host helper: (view_block, view_offset, q_pos) int32 arrays of the combined layout."""
+    bl = np.ascontiguousarray(block_len, dtype=np.int32)
+    rows, V = n_problems * n_workers, n_workers + 1
+    vb = np.empty((rows, V), np.int32)
+    vo = np.empty((rows, V), np.int32)
+    qp = np.empty(rows, np.int32)
+    _check("hw_views_combined", lib().hw_views_combined(int(n_problems), int(n_workers), bl.ctypes.data,
+                                                        vb.ctypes.data, vo.ctypes.data, qp.ctypes.data))
+    return vb, vo, qp
+
+
+def status_string(st: int) -> str:
+    return lib().hw_status_string(int(st)).decode()
+
+
+def last_cuda_error() -> int:
+    return int(lib().hw_last_cuda_error())

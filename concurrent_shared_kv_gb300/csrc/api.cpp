@@ -1,0 +1,290 @@
+// api.cpp - the C ABI of libhogwild (declared in include/hogwild.h): argument
+// checks on the host, workspace layout, RoPE phase tables, kernel selection.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "hogwild.h"
+#include "hw_internal.h"
+
+namespace hw {
+
+static thread_local int g_last_cuda_error = 0;
+
+static int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return HW_ERR_CUDA;
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// frac(w_i / 2pi) * 2^64 with w_i = theta^(-2i/D), in long double so that the
+// table is exact to well below one unit of its last place for positions up to
+// 2^31.
+void rope_phase_table(int head_dim, double theta, uint64_t *phase) {
+  const long double two_pi = 6.283185307179586476925286766559005768L;
+  for (int i = 0; i < 64; ++i) phase[i] = 0;
+  for (int i = 0; i < head_dim / 2 && i < 64; ++i) {
+    const long double w = powl(static_cast<long double>(theta),
+                               -2.0L * static_cast<long double>(i) / static_cast<long double>(head_dim));
+    long double f = w / two_pi;
+    f -= floorl(f);
+    long double x = ldexpl(f, 64) + 0.5L;
+    if (x >= 18446744073709551616.0L) x -= 18446744073709551616.0L;
+    phase[i] = static_cast<uint64_t>(x);
+  }
+}
+
+// Upper bound on the CTAs of any decode launch: slots are sized for it.
+static int max_decode_ctas() {
+  const int sms = device_sm_count();
+  return sms > 0 ? sms * 4 : -1;
+}
+
+WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  WorkspaceLayout L{};
+  L.err_off = 0;
+  L.counters_off = 256;
+  const size_t counters = static_cast<size_t>(d.n_rows) * d.n_kv_heads * sizeof(int32_t);
+  L.partials_off = L.counters_off + up(counters);
+  L.slots = static_cast<int64_t>(d.n_blocks) * d.n_kv_heads + max_ctas;
+  const size_t rec = static_cast<size_t>(kMaxQ) * (d.head_dim + 4) * sizeof(float);
+  L.total = L.partials_off + up(static_cast<size_t>(L.slots) * rec);
+  return L;
+}
+
+static int check_desc(const hw_attn_desc *d) {
+  if (!d) return HW_ERR_INVALID;
+  if (d->n_rows < 0 || d->n_blocks < 0 || d->max_view_blocks < 0 || d->cache_capacity < 0)
+    return HW_ERR_INVALID;
+  if (d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->n_q_heads % d->n_kv_heads != 0)
+    return HW_ERR_INVALID;
+  if (d->dtype != HW_F32 && d->dtype != HW_BF16) return HW_ERR_INVALID;
+  if (!(d->rope_theta > 1.0) || !std::isfinite(d->rope_theta)) return HW_ERR_INVALID;
+  if (!std::isfinite(d->scale)) return HW_ERR_INVALID;
+  if (d->head_dim != 64 && d->head_dim != 128) return HW_ERR_UNSUPPORTED;
+  if (d->n_blocks > HW_MAX_BLOCKS) return HW_ERR_UNSUPPORTED;
+  if (d->max_view_blocks > HW_MAX_VIEW_BLOCKS) return HW_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->n_rows) * d->max_view_blocks > HW_MAX_VIEW_ENTRIES)
+    return HW_ERR_UNSUPPORTED;
+  if (d->n_q_heads / d->n_kv_heads > kMaxQ) return HW_ERR_UNSUPPORTED;
+  if (d->cache_capacity > INT32_MAX) return HW_ERR_UNSUPPORTED;
+  return HW_OK;
+}
+
+}  // namespace hw
+
+using namespace hw;
+
+extern "C" {
+
+int hw_attn_decode_workspace_size(const hw_attn_desc *d, size_t *bytes) {
+  const int st = check_desc(d);
+  if (st != HW_OK) return st;
+  if (!bytes) return HW_ERR_INVALID;
+  const int ctas = max_decode_ctas();
+  if (ctas <= 0) return cuda_fail(cudaGetLastError());
+  *bytes = workspace_layout(*d, ctas).total;
+  return HW_OK;
+}
+
+int hw_workspace_init(void *workspace, size_t bytes, void *stream) {
+  if (!workspace || bytes < 256) return HW_ERR_WORKSPACE;
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HW_OK : cuda_fail(e);
+}
+
+int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_start, const int32_t *block_len,
+                   const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
+                   const int32_t *q_to_kv, void *out, float *lse, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+  int st = check_desc(d);
+  if (st != HW_OK) return st;
+  if (d->n_rows == 0) return HW_OK;
+  if (!q || !out || !q_pos) return HW_ERR_INVALID;
+  if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
+  if (d->n_blocks > 0 && (!block_start || !block_len || !k_cache || !v_cache)) return HW_ERR_INVALID;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return HW_ERR_WORKSPACE;
+  const int max_ctas = max_decode_ctas();
+  if (max_ctas <= 0) return cuda_fail(cudaGetLastError());
+  const WorkspaceLayout L = workspace_layout(*d, max_ctas);
+  if (workspace_bytes < L.total) return HW_ERR_WORKSPACE;
+
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.block_start = block_start;
+  a.block_len = block_len;
+  a.view_block = view_block;
+  a.view_offset = view_offset;
+  a.q_pos = q_pos;
+  a.q_to_kv = q_to_kv;
+  a.out = out;
+  a.lse = lse;
+  char *ws = static_cast<char *>(workspace);
+  a.err = reinterpret_cast<int32_t *>(ws + L.err_off);
+  a.counters = reinterpret_cast<int32_t *>(ws + L.counters_off);
+  a.partials = reinterpret_cast<float *>(ws + L.partials_off);
+  a.n_rows = d->n_rows;
+  a.n_q_heads = d->n_q_heads;
+  a.n_kv_heads = d->n_kv_heads;
+  a.head_dim = d->head_dim;
+  a.n_blocks = d->n_blocks;
+  a.n_view = d->max_view_blocks;
+  a.capacity = d->cache_capacity;
+  a.scale_log2 = static_cast<float>(static_cast<double>(d->scale) * 1.4426950408889634074);
+  rope_phase_table(d->head_dim, d->rope_theta, a.phase);
+
+  const int sms = device_sm_count();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int per_sm = decode_simt_ctas_per_sm(d->dtype, d->head_dim);
+  int ctas = sms * (per_sm > 4 ? 4 : per_sm);
+  if (ctas > max_ctas) ctas = max_ctas;
+  const cudaError_t e = launch_decode_simt(a, d->dtype, ctas, s);
+  return e == cudaSuccess ? HW_OK : cuda_fail(e);
+}
+
+int hw_block_commit(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                    double rope_theta, const void *k_src, const void *v_src, int64_t src_capacity,
+                    int32_t src_begin, int32_t n_tokens, void *k_dst, void *v_dst,
+                    int64_t dst_capacity, int32_t dst_offset, int32_t pos_delta, void *stream) {
+  if (dtype != HW_F32 && dtype != HW_BF16) return HW_ERR_INVALID;
+  if (n_layers < 0 || n_kv_heads <= 0 || n_tokens < 0 || src_begin < 0 || dst_offset < 0 ||
+      src_capacity < 0 || dst_capacity < 0)
+    return HW_ERR_INVALID;
+  if (!(rope_theta > 1.0) || !std::isfinite(rope_theta)) return HW_ERR_INVALID;
+  const int esz = dtype == HW_F32 ? 4 : 2;
+  const int epv = 16 / esz;
+  if (head_dim <= 0 || head_dim > 128 || head_dim % (2 * epv) != 0) return HW_ERR_UNSUPPORTED;
+  if (n_layers == 0 || n_tokens == 0) return HW_OK;
+  if (!k_src || !v_src || !k_dst || !v_dst) return HW_ERR_INVALID;
+  if (static_cast<int64_t>(src_begin) + n_tokens > src_capacity) return HW_ERR_CAPACITY;
+  if (static_cast<int64_t>(dst_offset) + n_tokens > dst_capacity) return HW_ERR_CAPACITY;
+  for (const void *p : {k_src, v_src, static_cast<const void *>(k_dst), static_cast<const void *>(v_dst)})
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return HW_ERR_INVALID;
+
+  // Overlap: the address spans of the pools; spans that meet are only allowed
+  // when they are the same pool (same base and capacity) and the token ranges
+  // are disjoint.
+  const int64_t row = static_cast<int64_t>(head_dim) * esz;
+  const int64_t src_span = static_cast<int64_t>(n_layers) * n_kv_heads * src_capacity * row;
+  const int64_t dst_span = static_cast<int64_t>(n_layers) * n_kv_heads * dst_capacity * row;
+  auto meets = [](const void *a, int64_t na, const void *b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
+  };
+  const bool tokens_disjoint =
+      src_begin + n_tokens <= dst_offset || dst_offset + n_tokens <= src_begin;
+  const struct { const void *s; } srcs[2] = {{k_src}, {v_src}};
+  const struct { const void *d; } dsts[2] = {{k_dst}, {v_dst}};
+  for (const auto &dd : dsts) {
+    for (const auto &ss : srcs) {
+      if (!meets(dd.d, dst_span, ss.s, src_span)) continue;
+      if (dd.d == ss.s && src_capacity == dst_capacity && tokens_disjoint) continue;
+      return HW_ERR_OVERLAP;
+    }
+  }
+  if (meets(k_dst, dst_span, v_dst, dst_span)) return HW_ERR_OVERLAP;
+
+  CommitArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.k_src = k_src;
+  a.v_src = v_src;
+  a.k_dst = k_dst;
+  a.v_dst = v_dst;
+  a.src_capacity = src_capacity;
+  a.dst_capacity = dst_capacity;
+  a.src_begin = src_begin;
+  a.dst_offset = dst_offset;
+  a.n_tokens = n_tokens;
+  a.n_layers = n_layers;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = head_dim;
+  a.delta = pos_delta;
+  rope_phase_table(head_dim, rope_theta, a.phase);
+  const cudaError_t e = launch_commit(a, dtype, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HW_OK : cuda_fail(e);
+}
+
+int hw_workspace_status(void *workspace, int32_t *flags, void *stream) {
+  if (!workspace) return HW_ERR_WORKSPACE;
+  if (!flags) return HW_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int32_t v = 0;
+  e = cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (v != 0) {
+    e = cudaMemset(workspace, 0, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  *flags = v;
+  return HW_OK;
+}
+
+int hw_views_combined(int32_t n_problems, int32_t n_workers, const int32_t *block_len,
+                      int32_t *view_block, int32_t *view_offset, int32_t *q_pos) {
+  if (n_problems < 0 || n_workers <= 0) return HW_ERR_INVALID;
+  if (n_problems == 0) return HW_OK;
+  if (!block_len || !view_block || !view_offset || !q_pos) return HW_ERR_INVALID;
+  const int W = n_workers, V = n_workers + 1;
+  for (int p = 0; p < n_problems; ++p) {
+    const int base = p * (W + 1);
+    for (int w = 0; w < W; ++w) {
+      const int row = p * W + w;
+      int v = 0;
+      int64_t pos = 0;
+      auto put = [&](int b) {
+        view_block[row * V + v] = b;
+        view_offset[row * V + v] = static_cast<int32_t>(pos);
+        pos += block_len[b];
+        ++v;
+      };
+      put(base);                                    // common cache
+      for (int o = 0; o < W; ++o)
+        if (o != w) put(base + 1 + o);              // others' unfinished steps, worker order
+      put(base + 1 + w);                            // own unfinished step
+      if (pos > INT32_MAX) return HW_ERR_INVALID;
+      q_pos[row] = static_cast<int32_t>(pos);
+    }
+  }
+  return HW_OK;
+}
+
+int hw_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *hw_status_string(int status) {
+  switch (status) {
+    case HW_OK: return "ok";
+    case HW_ERR_INVALID: return "invalid argument";
+    case HW_ERR_UNSUPPORTED: return "unsupported configuration";
+    case HW_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case HW_ERR_CAPACITY: return "range past the pool capacity";
+    case HW_ERR_OVERLAP: return "source and destination overlap";
+    case HW_ERR_CUDA: return "CUDA runtime error";
+    case HW_ERR_DEVICE: return "device-side metadata error";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// hw_internal.h - host-side declarations shared by the C ABI (api.cpp) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hogwild.h"
+
+namespace hw {
+
+// Tokens per scheduling unit (one tile of one block for one kv head).
+constexpr int kSimtTile = 64;
+constexpr int kTcTile = 128;
+// Query heads one tile serves at most (view references to a block x group).
+constexpr int kMaxQ = HW_MAX_QHEADS_PER_BLOCK;
+
+// Everything a decode kernel needs; passed by value as a kernel parameter.
+struct DecodeArgs {
+  const void *q;
+  const void *k;
+  const void *v;
+  const int32_t *block_start;
+  const int32_t *block_len;
+  const int32_t *view_block;
+  const int32_t *view_offset;
+  const int32_t *q_pos;
+  const int32_t *q_to_kv;
+  void *out;
+  float *lse;
+  int32_t *err;       // workspace error word (HW_DEV_* bits)
+  int32_t *counters;  // [n_rows][Hkv] merge arrival counters, zero between calls
+  float *partials;    // [slots][kMaxQ][D + 4]: o[0..D), m at D, l at D+1
+  int32_t n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
+  int64_t capacity;
+  float scale_log2;   // softmax scale * log2(e): scores live in the log2 domain
+  // RoPE phase increments: for pair i, the fraction of a turn per position,
+  // frac(w_i / 2pi), as an unsigned 0.64 fixed-point number.  The angle of
+  // position p is then (p * phase[i]) mod 2^64 turns, exact in integers.
+  uint64_t phase[64];
+};
+
+// Workspace layout helpers (bytes).
+struct WorkspaceLayout {
+  size_t err_off, counters_off, partials_off, total;
+  int64_t slots;
+};
+WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas);
+
+int device_sm_count();  // SMs of the current device, cached; <= 0 on failure
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_decode_simt(const DecodeArgs &a, int dtype, int ctas, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeArgs &a, int ctas, cudaStream_t s);
+int decode_simt_ctas_per_sm(int dtype, int head_dim);
+
+struct CommitArgs {
+  const void *k_src, *v_src;
+  void *k_dst, *v_dst;
+  int64_t src_capacity, dst_capacity;
+  int32_t src_begin, dst_offset, n_tokens, n_layers, n_kv_heads, head_dim;
+  uint64_t phase[64];
+  int64_t delta;  // pos_delta
+};
+cudaError_t launch_commit(const CommitArgs &a, int dtype, cudaStream_t s);
+
+// Fixed-point phase table for RoPE (host): frac(theta^(-2i/D) / 2pi) * 2^64.
+void rope_phase_table(int head_dim, double theta, uint64_t *phase);
+
+}  // namespace hw

@@ -1,0 +1,71 @@
+"""Torch-facing convenience layer over the C ABI: it owns a workspace and the
+device copies of the per-step metadata.  PyTorch only allocates memory and
+provides streams here; every step of the computation runs in libhogwild."""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import api
+
+DTYPES = {torch.float32: api.HW_F32, torch.bfloat16: api.HW_BF16}
+
+
+class DecodeSession:
+    """One decode configuration: shapes, pools, workspace and metadata."""
+
+    def __init__(self, *, n_rows: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                 n_blocks: int, max_view_blocks: int, capacity: int, dtype: torch.dtype,
+                 rope_theta: float, scale: Optional[float] = None, device="cuda"):
+        self.device = torch.device(device)
+        self.dtype = dtype
+        self.desc = api.make_desc(n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks,
+                                  max_view_blocks, capacity, DTYPES[dtype], rope_theta,
+                                  head_dim ** -0.5 if scale is None else scale)
+        self.ws_bytes = api.attn_decode_workspace_size(self.desc)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        api.workspace_init(self.workspace, self.ws_bytes)
+        self.meta = None
+
+    def set_metadata(self, block_start, block_len, view_block, view_offset, q_pos, q_to_kv=None,
+                     non_blocking: bool = False):
+        """Upload the step's metadata (shared by every layer of the step)."""
+        def dev(x):
+            if x is None:
+                return None
+            t = torch.as_tensor(np.ascontiguousarray(x, dtype=np.int32)) if not torch.is_tensor(x) else x
+            return t.to(self.device, dtype=torch.int32, non_blocking=non_blocking).contiguous()
+        self.meta = dict(block_start=dev(block_start), block_len=dev(block_len),
+                         view_block=dev(view_block), view_offset=dev(view_offset),
+                         q_pos=dev(q_pos), q_to_kv=dev(q_to_kv))
+
+    def decode(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               want_lse: bool = True, stream=None):
+        d = self.desc
+        if out is None:
+            out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
+        if lse is None and want_lse:
+            lse = torch.empty((d.n_rows, d.n_q_heads), dtype=torch.float32, device=self.device)
+        m = self.meta
+        api.attn_decode(d, q, k_cache, v_cache, m["block_start"], m["block_len"], m["view_block"],
+                        m["view_offset"], m["q_pos"], out, lse, self.workspace, self.ws_bytes,
+                        q_to_kv=m["q_to_kv"], stream=stream)
+        return out, lse
+
+    def device_flags(self) -> int:
+        return api.workspace_status(self.workspace)
+
+
+def block_commit(k_src: torch.Tensor, v_src: torch.Tensor, src_begin: int, n_tokens: int,
+                 k_dst: torch.Tensor, v_dst: torch.Tensor, dst_offset: int, pos_delta: int,
+                 rope_theta: float, stream=None):
+    """Pools shaped [layers][Hkv][cap][D] or [Hkv][cap][D]."""
+    def dims(t):
+        return (1,) + tuple(t.shape) if t.dim() == 3 else tuple(t.shape)
+    L, H, cs, D = dims(k_src)
+    _, _, cd, _ = dims(k_dst)
+    return api.block_commit(DTYPES[k_src.dtype], L, H, D, rope_theta, k_src, v_src, cs, src_begin,
+                            n_tokens, k_dst, v_dst, cd, dst_offset, pos_delta, stream=stream)

@@ -1,0 +1,190 @@
+/*
+ * hogwild.h - C ABI of libhogwild: concurrent decode attention over a KV cache
+ * that W workers share, and the block commit that moves a finished step into
+ * the shared history (Hogwild! Inference), for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (page title, then section / equation):
+ *  - "Hogwild! Inference: Parallel LLM Generation via Concurrent Attention"
+ *    (paper-notes page): key design 1 (shared KV cache; the query-rotation
+ *    equation rho(q,i_q)[rho(A,i_k^A) (+) rho(B,i_k^B) ...] =
+ *    rho(q,i_q-i_k^A)A (+) rho(q,i_q-i_k^B)B ...), key design 2 (combined cache
+ *    layout: common cache, other workers' unfinished steps in worker order,
+ *    the current worker's own step; a finished step is rotated and moved into
+ *    the shared history), implementation notes (a Flash-Decoding style kernel
+ *    over many cache blocks; each block stores its KV at block-local positions
+ *    and the query rotation supplies the real position).
+ *  - omica.com.cn article on Hogwild! Inference: section 2.1 (rotate_query:
+ *    frequencies 1/base^(2i/dim), q*cos + rotate_half(q)*sin), section 3.1
+ *    (a cache block carries its storage, start and current length), section
+ *    3.2 (blockwise scores q_rot.k/sqrt(dim), one softmax across all blocks;
+ *    KV work split evenly over the SMs, partial results merged).
+ *
+ * Conventions shared by every entry point
+ *  - The caller owns all memory.  No entry point allocates device memory.
+ *  - "dev" marks device pointers, "host" host pointers.  `stream` is a
+ *    cudaStream_t passed as void* (NULL = the legacy default stream).  Work is
+ *    enqueued on that stream; nothing synchronises unless stated.
+ *  - KV pool layout (one K pool and one V pool per layer): [Hkv][capacity][D],
+ *    D contiguous, element type `dtype`; a block is the token range
+ *    [block_start, block_start + block_len) of every head.  Keys are stored
+ *    already rotated by RoPE at block-local positions 0 .. len-1.
+ *  - RoPE pairs element i with element i + D/2 (rotate_half) at frequency
+ *    w_i = rope_theta^(-2i/D).
+ *  - Every call returns an hw_status.  Argument errors are found on the host
+ *    before anything is enqueued.  Errors in device-resident metadata are
+ *    recorded in the workspace (see hw_workspace_status) and the affected
+ *    blocks are skipped; no kernel traps, faults or waits without a bound.
+ */
+#ifndef HOGWILD_H
+#define HOGWILD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HW_OK = 0,
+  HW_ERR_INVALID = -1,     /* bad argument: null pointer, negative size, bad dtype */
+  HW_ERR_UNSUPPORTED = -2, /* valid but outside what the kernels handle (see limits) */
+  HW_ERR_WORKSPACE = -3,   /* workspace missing, too small or not 256-byte aligned */
+  HW_ERR_CAPACITY = -4,    /* commit would write past the destination capacity */
+  HW_ERR_OVERLAP = -5,     /* commit source and destination memory overlap */
+  HW_ERR_CUDA = -6,        /* a CUDA runtime call failed (hw_last_cuda_error) */
+  HW_ERR_DEVICE = -7       /* device-side metadata check failed (hw_workspace_status) */
+} hw_status;
+
+typedef enum { HW_F32 = 0, HW_BF16 = 1 } hw_dtype;
+
+/* Device-side error bits reported by hw_workspace_status. */
+enum {
+  HW_DEV_BAD_BLOCK = 1,     /* a view names a block id outside [-1, n_blocks) */
+  HW_DEV_BAD_RANGE = 2,     /* block_start/len negative or past the pool capacity */
+  HW_DEV_BAD_HEADMAP = 4,   /* q_to_kv entry out of range or groups of unequal size */
+  HW_DEV_TOO_MANY_REFS = 8, /* more than HW_MAX_QHEADS_PER_BLOCK query heads on a block */
+  HW_DEV_TIMEOUT = 16       /* a bounded in-kernel wait expired; results are invalid */
+};
+
+/* Limits of this build. */
+#define HW_MAX_BLOCKS 256          /* blocks per decode call */
+#define HW_MAX_VIEW_BLOCKS 64      /* max_view_blocks */
+#define HW_MAX_VIEW_ENTRIES 4096   /* n_rows * max_view_blocks */
+#define HW_MAX_QHEADS_PER_BLOCK 32 /* (view references to one block) x (Hq/Hkv) */
+
+/* Host-side description of one decode call (all scalars, host memory). */
+typedef struct {
+  int32_t n_rows;          /* query tokens: one per (problem, worker), >= 0 */
+  int32_t n_q_heads;       /* Hq */
+  int32_t n_kv_heads;      /* Hkv, Hq % Hkv == 0 */
+  int32_t head_dim;        /* D: 64 or 128 (bf16 tensor-core path: 128) */
+  int32_t n_blocks;        /* entries of block_start / block_len, <= HW_MAX_BLOCKS */
+  int32_t max_view_blocks; /* V: width of the per-row view tables */
+  int64_t cache_capacity;  /* tokens per head in the K and V pools */
+  int32_t dtype;           /* hw_dtype of q, pools and out */
+  double rope_theta;       /* RoPE base, > 1 */
+  float scale;             /* softmax scale, usually 1/sqrt(D) */
+} hw_attn_desc;
+
+/*
+ * Bytes of workspace hw_attn_decode needs for `d` on the current device.
+ * Writes the size to *bytes.  The workspace holds the error word, the merge
+ * arrival counters and the per-split partial results (max, sum of exp,
+ * unnormalised output) of the log-sum-exp merge.
+ */
+int hw_attn_decode_workspace_size(const hw_attn_desc *d, size_t *bytes);
+
+/*
+ * Zero a workspace (dev, `bytes` long) on `stream`.  Required once before the
+ * first hw_attn_decode that uses it; each decode leaves its counters at zero
+ * again for the next call.
+ */
+int hw_workspace_init(void *workspace, size_t bytes, void *stream);
+
+/*
+ * Concurrent decode attention, one layer, one launch.
+ *
+ * For every row r (a worker's current token) and query head hq with kv head
+ * g = q_to_kv ? q_to_kv[hq] : hq / (Hq/Hkv):
+ *   for each view entry v (view_block[r][v] = b >= 0, len_b = block_len[b] > 0):
+ *     q~ = rho(q[r][hq], q_pos[r] - view_offset[r][v])            (query rotation)
+ *     s_j = scale * q~ . K[g][block_start[b] + j],  j < len_b       (block scores)
+ *   out[r][hq] = sum_j softmax(s)_j V[g][block_start[b] + j]  over all entries
+ *   lse[r][hq] = log sum_j exp(s_j)   (natural log; -inf and out = 0 if empty)
+ *
+ *  d            host  description (above)
+ *  q            dev   [n_rows][Hq][D] dtype, un-rotated queries
+ *  k_cache      dev   [Hkv][capacity][D] dtype, keys rotated at block-local positions
+ *  v_cache      dev   [Hkv][capacity][D] dtype
+ *  block_start  dev   int32 [n_blocks], first pool token of each block
+ *  block_len    dev   int32 [n_blocks], tokens in each block
+ *  view_block   dev   int32 [n_rows][V], block ids in view order, -1 = unused slot
+ *  view_offset  dev   int32 [n_rows][V], i_k^block: tokens before that block in
+ *                     that row's view (any int32; the rotation uses i_q - offset)
+ *  q_pos        dev   int32 [n_rows], i_q: the query's position in its view
+ *  q_to_kv      dev   int32 [Hq] or NULL (grouped heads, hq / (Hq/Hkv))
+ *  out          dev   [n_rows][Hq][D] dtype
+ *  lse          dev   float [n_rows][Hq] or NULL
+ *  workspace    dev   >= hw_attn_decode_workspace_size bytes, 256-byte aligned,
+ *                     zeroed once with hw_workspace_init; one call at a time
+ *  stream       cudaStream_t as void*
+ * The same metadata arrays can serve every layer of a step.  Calls that share
+ * a workspace must be ordered on one stream.  Pool slots past a block's
+ * length are never used in the result, whatever they hold.
+ */
+int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_start, const int32_t *block_len,
+                   const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
+                   const int32_t *q_to_kv, void *out, float *lse, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * Block commit over n_layers layers in one launch (a finished step moves
+ * into the shared history; key design 2 of the Hogwild! notes):
+ *   K_dst[l][h][dst_offset + j] = rho(K_src[l][h][src_begin + j], pos_delta)
+ *   V_dst[l][h][dst_offset + j] = V_src[l][h][src_begin + j]        (bit copy)
+ * for l < n_layers, h < Hkv, j < n_tokens.  Pools are [n_layers][Hkv][cap][D]
+ * (layer stride Hkv*cap*D elements).  Keys are rotated in fp32 from the stored
+ * values and rounded once to dtype (nearest, ties to even); pos_delta may be
+ * negative; pos_delta = 0 is a bit copy.  Nothing outside the destination
+ * range is written.  Block lengths are the caller's to update.
+ *
+ *  k_src, v_src   dev  source pools, src_capacity tokens per head
+ *  k_dst, v_dst   dev  destination pools, dst_capacity tokens per head
+ * Errors: HW_ERR_CAPACITY if a range leaves its pool; HW_ERR_OVERLAP if any
+ * destination range shares memory with a source range or with the other
+ * destination.  head_dim must be a multiple of 16 bytes / element size * 2.
+ */
+int hw_block_commit(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                    double rope_theta, const void *k_src, const void *v_src, int64_t src_capacity,
+                    int32_t src_begin, int32_t n_tokens, void *k_dst, void *v_dst,
+                    int64_t dst_capacity, int32_t dst_offset, int32_t pos_delta, void *stream);
+
+/*
+ * Synchronises `stream`, reads and clears the device error bits of a
+ * workspace (HW_DEV_* flags, 0 = none) into *flags.
+ */
+int hw_workspace_status(void *workspace, int32_t *flags, void *stream);
+
+/*
+ * Host helper: the combined layout of key design 2 for n_problems problems of
+ * n_workers workers.  Block ids: problem p owns p*(W+1) (common) and
+ * p*(W+1)+1+w (worker w).  Worker w's view: common, the other workers in id
+ * order, itself; view_offset = tokens before each block in that view; q_pos =
+ * the view's total length.  All arrays host: block_len [n_problems*(W+1)],
+ * view_block and view_offset [n_problems*W][W+1], q_pos [n_problems*W].
+ */
+int hw_views_combined(int32_t n_problems, int32_t n_workers, const int32_t *block_len,
+                      int32_t *view_block, int32_t *view_offset, int32_t *q_pos);
+
+/* Last CUDA error code seen by this thread's library calls (cudaError_t). */
+int hw_last_cuda_error(void);
+
+/* Static description of a status code. */
+const char *hw_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HOGWILD_H */
