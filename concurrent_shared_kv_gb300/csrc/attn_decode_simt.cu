@@ -21,7 +21,12 @@ constexpr int kSimtThreads = 256;
 
 template <int D>
 struct SimtSmem {
-  PlanSmem plan;
+  PlanCore plan;
+  PlanScratch scratch;
+  SegMeta meta;
+  MergeScratch merge;
+  int32_t merge_list[kMaxQ];
+  int32_t n_merge;
   alignas(16) float q[kMaxQ][D + 4];
   alignas(16) float k[kSimtTile][D + 4];
   alignas(16) float v[kSimtTile][D + 4];
@@ -85,20 +90,23 @@ __device__ __forceinline__ void load_tile(const DecodeArgs &a, SimtSmem<D> &S, i
 template <typename T, int D>
 __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, int t0, int t1,
                              int64_t U, int C) {
-  PlanSmem &P = S.plan;
+  PlanCore &P = S.plan;
+  SegMeta &M = S.meta;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = a.n_q_heads / a.n_kv_heads;
-  gather_refs(a, P, b);
-  gather_qheads(a, P, h);
+  if (warp == 0) {
+    gather_refs(a, M, b, lane);
+    gather_qheads(a, M, h, lane);
+  }
   __syncthreads();
-  const int nq = P.n_ref * G;  // <= kMaxQ: blocks with more are skipped by the plan
+  const int nq = M.n_ref * G;  // <= kMaxQ: blocks with more are skipped by the plan
 
   // 1. rotated queries: q~ = rho(q, i_q - offset), fp32
   for (int idx = tid; idx < nq * (D / 2); idx += kSimtThreads) {
     const int qi = idx / (D / 2), i = idx % (D / 2);
-    const int e = P.ref_entry[qi / G];
+    const int e = M.ref_entry[qi / G];
     const int r = e / a.n_view;
-    const int hq = P.qhead[qi % G];
+    const int hq = M.qhead[qi % G];
     const int64_t rel = static_cast<int64_t>(a.q_pos[r]) - a.view_offset[e];
     const T *qp = reinterpret_cast<const T *>(a.q) + (static_cast<int64_t>(r) * a.n_q_heads + hq) * D;
     const float x0 = to_f32<T>(qp[i]), x1 = to_f32<T>(qp[i + D / 2]);
@@ -119,8 +127,8 @@ __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, 
   for (int k = 0; k < QPT; ++k) acc[k] = 0.f;
   __syncthreads();
 
-  const int len = P.len[b];
-  const int64_t row_base = P.start[b];
+  const int len = a.block_len[b];
+  const int64_t row_base = a.block_start[b];
   for (int t = t0; t < t1; ++t) {
     const int tok0 = t * kSimtTile;
     const int valid = min(kSimtTile, len - tok0);
@@ -195,41 +203,44 @@ __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, 
       }
     }
   }
-  arrive(a, P, b, h, U, C);
-  for (int i = 0; i < P.n_merge; ++i) merge_row<T>(a, P, P.merge_list[i], h, U, C);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) S.n_merge = arrive_rows(a, P, M, h, U, C, S.merge_list, 0, kMaxQ);
+  __syncthreads();
+  for (int i = 0; i < S.n_merge; ++i)
+    merge_row<T>(a, P, S.merge, M.qhead, S.merge_list[i] / a.n_kv_heads, h, U, C, tid,
+                 kSimtThreads, CtaSync());
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem<D> &S = *reinterpret_cast<SimtSmem<D> *>(smem_raw);
-  PlanSmem &P = S.plan;
-  build_plan<kSimtTile>(a, P);
-  const int C = gridDim.x, c = blockIdx.x;
+  PlanCore &P = S.plan;
+  build_plan<kSimtTile>(a, P, S.scratch);
+  const int c = blockIdx.x;
   const int64_t U = P.ubase[a.n_blocks];
+  const int C = static_cast<int>(U < gridDim.x ? U : gridDim.x);  // working CTAs
 
   // (row, kv head) pairs without any record: out = 0, lse = -inf
-  for (int rh = c; rh < a.n_rows * a.n_kv_heads; rh += C) {
+  for (int rh = c; rh < a.n_rows * a.n_kv_heads; rh += gridDim.x) {
     const int r = rh / a.n_kv_heads, h = rh % a.n_kv_heads;
     if (expected_records(a, P, r, h, U, C) == 0) {
-      gather_qheads(a, P, h);
+      if (threadIdx.x < 32) gather_qheads(a, S.meta, h, threadIdx.x);
       __syncthreads();
-      write_empty<T>(a, P, r);
+      write_empty<T>(a, S.meta.qhead, r, threadIdx.x, kSimtThreads);
       __syncthreads();
     }
   }
-  if (U == 0) return;
+  if (U == 0 || c >= C) return;
 
   int64_t u = cta_unit_begin(U, c, C);
   const int64_t u_end = cta_unit_begin(U, c + 1, C);
   while (u < u_end) {
-    const int b = block_of_unit(P, a.n_blocks, u);
-    const int tl = P.tiles[b];
-    const int h = static_cast<int>((u - P.ubase[b]) / tl);
-    const int64_t seg_first = P.ubase[b] + static_cast<int64_t>(h) * tl;
-    const int64_t seg_stop = min(seg_first + tl, u_end);
-    simt_segment<T, D>(a, S, b, h, static_cast<int>(u - seg_first),
-                       static_cast<int>(seg_stop - seg_first), U, C);
+    const UnitPos x = unit_pos(P, a.n_blocks, u);
+    const int64_t seg_stop = min(x.seg_first + x.tiles, u_end);
+    simt_segment<T, D>(a, S, x.b, x.h, static_cast<int>(u - x.seg_first),
+                       static_cast<int>(seg_stop - x.seg_first), U, C);
     u = seg_stop;
   }
 }

@@ -8,12 +8,18 @@
 //   units are ordered block-major, then kv head, then tile; only blocks that
 //   some view references take part.
 //   CTA c of C owns units [floor(c U / C), floor((c+1) U / C)), so every CTA
-//   streams the same number of tiles whatever the block lengths are.
+//   streams the same number of tiles whatever the block lengths are.  C is
+//   min(grid, U): every working CTA owns at least one unit, so the CTAs that
+//   touch a segment form one contiguous range.
 //   segment   = the units of one (block, kv head); a CTA emits one partial
 //   record per (segment it touched, query head served) into slot seg + c,
 //   which is unique because seg and c never both stay put as units advance.
 //   The last CTA to deliver a record for (row, kv head) - found with an
 //   arrival counter, no waiting - merges that row's records.
+//
+// Group-level helpers take (tid, nt) - the thread's index within the group
+// that runs them and the group's size - and a Sync functor that synchronises
+// exactly that group.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -56,7 +62,7 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
 
-// cos and sin of the RoPE angle for relative position `rel` and pair i.  The
+// cos and sin of the RoPE angle for relative position `rel` and one pair.  The
 // angle in turns is (rel * phase) mod 1, computed exactly in 64-bit integers;
 // its top bits become a float in [-0.5, 0.5) turns, and sincospif does the
 // rest (sin(pi x), cos(pi x) of x = 2 * turns).
@@ -66,25 +72,43 @@ __device__ __forceinline__ void rope_cos_sin(int64_t rel, uint64_t phase, float 
   sincospif(t, s, c);
 }
 
+struct CtaSync {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// Named barrier over COUNT threads (a multiple of 32).
+template <int ID, int COUNT>
+struct NamedSync {
+  __device__ __forceinline__ void operator()() const {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+  }
+};
+
 // ---------------------------------------------------------------------------
 // the plan: every CTA derives the same unit decomposition from the metadata
 // ---------------------------------------------------------------------------
 
-struct PlanSmem {
-  int32_t start[HW_MAX_BLOCKS];
-  int32_t len[HW_MAX_BLOCKS];
-  int32_t tiles[HW_MAX_BLOCKS];   // tiles per kv head (0: skipped)
-  int32_t refs[HW_MAX_BLOCKS];    // view references to the block
-  int64_t ubase[HW_MAX_BLOCKS + 1];
-  int32_t qhead[HW_MAX_QHEADS_PER_BLOCK * 4];  // scratch: q heads of a kv head
-  int32_t ref_entry[kMaxQ];       // view entries (r * V + v) referencing a block
-  int32_t n_ref;
-  int32_t merge_list[kMaxQ];      // rows this CTA has to merge
-  int32_t n_merge;
+struct PlanCore {
+  int32_t tiles[HW_MAX_BLOCKS];      // tiles per kv head (0: block skipped)
+  int64_t ubase[HW_MAX_BLOCKS + 1];  // first unit of each block
+};
+
+struct PlanScratch {  // only while the plan is built
+  int32_t refs[HW_MAX_BLOCKS];
   int32_t headmap_ok;
-  // merge scratch: per view entry of the row being merged
-  int32_t mv_qi[HW_MAX_VIEW_BLOCKS];  // rank of the entry among its block's references
-  int64_t mv_seg[HW_MAX_VIEW_BLOCKS]; // segment id b * Hkv + h, -1 = no records
+};
+
+// Per-segment metadata: the view entries referencing the block and the query
+// heads of the kv head.  Query head qi of the tile is (ref qi / G, head qi % G).
+struct SegMeta {
+  int32_t n_ref;
+  int32_t ref_entry[kMaxQ];  // view entries r * V + v, in entry order
+  int32_t qhead[kMaxQ];      // q heads of the kv head, in increasing order
+};
+
+struct MergeScratch {
+  int32_t mv_qi[HW_MAX_VIEW_BLOCKS];   // rank of the entry among its block's references
+  int64_t mv_seg[HW_MAX_VIEW_BLOCKS];  // segment id b * Hkv + h, -1 = no records
   int32_t mv_c0[HW_MAX_VIEW_BLOCKS], mv_c1[HW_MAX_VIEW_BLOCKS];
   float red[32];
 };
@@ -98,30 +122,22 @@ __device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int C) {
   return static_cast<int>(((u + 1) * C - 1) / U);
 }
 
+// Validates the metadata and builds the unit prefix.  Every thread of the CTA
+// takes part (blockDim.x threads, __syncthreads inside).
 template <int TILE>
-__device__ void build_plan(const DecodeArgs &a, PlanSmem &P) {
+__device__ void build_plan(const DecodeArgs &a, PlanCore &P, PlanScratch &S) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int G = a.n_q_heads / a.n_kv_heads;
-  for (int b = tid; b < a.n_blocks; b += nt) {
-    int32_t s = a.block_start[b], n = a.block_len[b];
-    if (s < 0 || n < 0 || static_cast<int64_t>(s) + n > a.capacity) {
-      flag_error(a.err, HW_DEV_BAD_RANGE);
-      s = 0;
-      n = 0;
-    }
-    P.start[b] = s;
-    P.len[b] = n;
-    P.refs[b] = 0;
-  }
-  if (tid == 0) P.headmap_ok = 1;
+  for (int b = tid; b < a.n_blocks; b += nt) S.refs[b] = 0;
+  if (tid == 0) S.headmap_ok = 1;
   __syncthreads();
   const int E = a.n_rows * a.n_view;
   for (int e = tid; e < E; e += nt) {
     const int b = a.view_block[e];
     if (b >= a.n_blocks || b < -1) {
-      flag_error(a.err, HW_DEV_BAD_BLOCK);
+      if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_BLOCK);
     } else if (b >= 0) {
-      atomicAdd(&P.refs[b], 1);
+      atomicAdd(&S.refs[b], 1);
     }
   }
   if (a.q_to_kv) {
@@ -129,25 +145,28 @@ __device__ void build_plan(const DecodeArgs &a, PlanSmem &P) {
     for (int h = tid; h < a.n_kv_heads; h += nt) {
       int cnt = 0;
       for (int hq = 0; hq < a.n_q_heads; ++hq) cnt += (a.q_to_kv[hq] == h);
-      if (cnt != G) P.headmap_ok = 0;
+      if (cnt != G) S.headmap_ok = 0;
     }
     for (int hq = tid; hq < a.n_q_heads; hq += nt) {
       const int g = a.q_to_kv[hq];
-      if (g < 0 || g >= a.n_kv_heads) P.headmap_ok = 0;
+      if (g < 0 || g >= a.n_kv_heads) S.headmap_ok = 0;
     }
   }
   __syncthreads();
-  if (!P.headmap_ok && tid == 0 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_HEADMAP);
+  if (!S.headmap_ok && tid == 0 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_HEADMAP);
   for (int b = tid; b < a.n_blocks; b += nt) {
+    const int32_t s = a.block_start[b], n = a.block_len[b];
     int t = 0;
-    if (P.refs[b] > 0 && P.len[b] > 0) {
-      if (P.refs[b] * G > kMaxQ) {
+    if (s < 0 || n < 0 || static_cast<int64_t>(s) + n > a.capacity) {
+      if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_RANGE);
+    } else if (S.refs[b] > 0 && n > 0) {
+      if (S.refs[b] * G > kMaxQ) {
         if (blockIdx.x == 0) flag_error(a.err, HW_DEV_TOO_MANY_REFS);
       } else {
-        t = (P.len[b] + TILE - 1) / TILE;
+        t = (n + TILE - 1) / TILE;
       }
     }
-    P.tiles[b] = P.headmap_ok ? t : 0;
+    P.tiles[b] = S.headmap_ok ? t : 0;
   }
   __syncthreads();
   if (tid < 32) {
@@ -155,7 +174,7 @@ __device__ void build_plan(const DecodeArgs &a, PlanSmem &P) {
     int64_t carry = 0;
     for (int base = 0; base < a.n_blocks; base += 32) {
       const int b = base + tid;
-      int64_t x = (b < a.n_blocks) ? static_cast<int64_t>(P.tiles[b]) * a.n_kv_heads : 0;
+      const int64_t x = (b < a.n_blocks) ? static_cast<int64_t>(P.tiles[b]) * a.n_kv_heads : 0;
       int64_t incl = x;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -171,7 +190,7 @@ __device__ void build_plan(const DecodeArgs &a, PlanSmem &P) {
 }
 
 // Block that holds unit u (ubase[b] <= u < ubase[b+1]), by binary search.
-__device__ __forceinline__ int block_of_unit(const PlanSmem &P, int n_blocks, int64_t u) {
+__device__ __forceinline__ int block_of_unit(const PlanCore &P, int n_blocks, int64_t u) {
   int lo = 0, hi = n_blocks - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -180,8 +199,24 @@ __device__ __forceinline__ int block_of_unit(const PlanSmem &P, int n_blocks, in
   return lo;
 }
 
+// The unit u decoded: block, kv head, tile, and the segment's first unit.
+struct UnitPos {
+  int b, h, t, tiles;
+  int64_t seg_first;
+};
+__device__ __forceinline__ UnitPos unit_pos(const PlanCore &P, int n_blocks, int64_t u) {
+  UnitPos x;
+  x.b = block_of_unit(P, n_blocks, u);
+  x.tiles = P.tiles[x.b];
+  const int64_t local = u - P.ubase[x.b];
+  x.h = static_cast<int>(local / x.tiles);
+  x.t = static_cast<int>(local - static_cast<int64_t>(x.h) * x.tiles);
+  x.seg_first = P.ubase[x.b] + static_cast<int64_t>(x.h) * x.tiles;
+  return x;
+}
+
 // Number of CTAs whose unit ranges touch segment (b, h).
-__device__ __forceinline__ int seg_ctas(const PlanSmem &P, int b, int h, int64_t U, int C) {
+__device__ __forceinline__ int seg_ctas(const PlanCore &P, int b, int h, int64_t U, int C) {
   const int tl = P.tiles[b];
   if (tl == 0) return 0;
   const int64_t s0 = P.ubase[b] + static_cast<int64_t>(h) * tl;
@@ -189,7 +224,7 @@ __device__ __forceinline__ int seg_ctas(const PlanSmem &P, int b, int h, int64_t
 }
 
 // Records expected for (row r, kv head h): one per (view entry, CTA) pair.
-__device__ __forceinline__ int expected_records(const DecodeArgs &a, const PlanSmem &P, int r,
+__device__ __forceinline__ int expected_records(const DecodeArgs &a, const PlanCore &P, int r,
                                                 int h, int64_t U, int C) {
   int n = 0;
   for (int v = 0; v < a.n_view; ++v) {
@@ -199,54 +234,50 @@ __device__ __forceinline__ int expected_records(const DecodeArgs &a, const PlanS
   return n;
 }
 
-// The query heads served by kv head h, in increasing order, into P.qhead.
-__device__ __forceinline__ void gather_qheads(const DecodeArgs &a, PlanSmem &P, int h) {
+// The query heads served by kv head h, in increasing order (one warp).
+__device__ __forceinline__ void gather_qheads(const DecodeArgs &a, SegMeta &M, int h, int lane) {
   const int G = a.n_q_heads / a.n_kv_heads;
-  if (threadIdx.x < 32) {
-    if (!a.q_to_kv) {
-      for (int i = threadIdx.x; i < G; i += 32) P.qhead[i] = h * G + i;
-    } else {
-      int cnt = 0;
-      for (int base = 0; base < a.n_q_heads; base += 32) {
-        const int hq = base + threadIdx.x;
-        const bool m = hq < a.n_q_heads && a.q_to_kv[hq] == h;
-        const unsigned mask = __ballot_sync(0xffffffffu, m);
-        const int pos = cnt + __popc(mask & ((1u << threadIdx.x) - 1u));
-        if (m && pos < G) P.qhead[pos] = hq;
-        cnt += __popc(mask);
-      }
+  if (!a.q_to_kv) {
+    for (int i = lane; i < G; i += 32) M.qhead[i] = h * G + i;
+  } else {
+    int cnt = 0;
+    for (int base = 0; base < a.n_q_heads; base += 32) {
+      const int hq = base + lane;
+      const bool m = hq < a.n_q_heads && a.q_to_kv[hq] == h;
+      const unsigned mask = __ballot_sync(0xffffffffu, m);
+      const int pos = cnt + __popc(mask & ((1u << lane) - 1u));
+      if (m && pos < G) M.qhead[pos] = hq;
+      cnt += __popc(mask);
     }
   }
 }
 
-// View entries referencing block b, in entry order, into P.ref_entry (warp 0).
-__device__ __forceinline__ void gather_refs(const DecodeArgs &a, PlanSmem &P, int b) {
-  if (threadIdx.x < 32) {
-    const int E = a.n_rows * a.n_view;
-    int cnt = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + threadIdx.x;
-      const bool m = e < E && a.view_block[e] == b;
-      const unsigned mask = __ballot_sync(0xffffffffu, m);
-      const int pos = cnt + __popc(mask & ((1u << threadIdx.x) - 1u));
-      if (m && pos < kMaxQ) P.ref_entry[pos] = e;
-      cnt += __popc(mask);
-    }
-    if (threadIdx.x == 0) P.n_ref = cnt;
+// View entries referencing block b, in entry order (one warp).
+__device__ __forceinline__ void gather_refs(const DecodeArgs &a, SegMeta &M, int b, int lane) {
+  const int E = a.n_rows * a.n_view;
+  int cnt = 0;
+  for (int base = 0; base < E; base += 32) {
+    const int e = base + lane;
+    const bool m = e < E && a.view_block[e] == b;
+    const unsigned mask = __ballot_sync(0xffffffffu, m);
+    const int pos = cnt + __popc(mask & ((1u << lane) - 1u));
+    if (m && pos < kMaxQ) M.ref_entry[pos] = e;
+    cnt += __popc(mask);
   }
+  if (lane == 0) M.n_ref = cnt;
 }
 
 __device__ __forceinline__ float *record_ptr(const DecodeArgs &a, int64_t slot, int qi) {
   return a.partials + (slot * kMaxQ + qi) * static_cast<int64_t>(a.head_dim + 4);
 }
 
-// Write out = 0, lse = -inf for every query head of (r, h): an empty view.
+// out = 0, lse = -inf for every query head of kv head h in row r (empty view).
 template <typename T>
-__device__ void write_empty(const DecodeArgs &a, const PlanSmem &P, int r) {
+__device__ void write_empty(const DecodeArgs &a, const int32_t *qhead, int r, int tid, int nt) {
   const int G = a.n_q_heads / a.n_kv_heads;
-  for (int i = threadIdx.x; i < G * a.head_dim; i += blockDim.x) {
+  for (int i = tid; i < G * a.head_dim; i += nt) {
     const int gi = i / a.head_dim, d = i % a.head_dim;
-    const int hq = P.qhead[gi];
+    const int hq = qhead[gi];
     reinterpret_cast<T *>(a.out)[(static_cast<int64_t>(r) * a.n_q_heads + hq) * a.head_dim + d] =
         from_f32<T>(0.f);
     if (d == 0 && a.lse) a.lse[static_cast<int64_t>(r) * a.n_q_heads + hq] = -INFINITY;
@@ -254,14 +285,15 @@ __device__ void write_empty(const DecodeArgs &a, const PlanSmem &P, int r) {
 }
 
 // Merge every record of (row r, kv head h) into out / lse, then re-arm the
-// counter.  All threads of the CTA call it; P.qhead must hold h's heads.
+// counter.  The whole group calls it; qhead must hold h's query heads.
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
 //   lse = (M + log2 L) ln 2     (m, l, o of each record in the log2 domain)
-template <typename T>
-__device__ void merge_row(const DecodeArgs &a, PlanSmem &P, int r, int h, int64_t U, int C) {
+template <typename T, typename Sync>
+__device__ void merge_row(const DecodeArgs &a, const PlanCore &P, MergeScratch &X,
+                          const int32_t *qhead, int r, int h, int64_t U, int C, int tid, int nt,
+                          Sync sync) {
   const int G = a.n_q_heads / a.n_kv_heads;
   const int D = a.head_dim;
-  const int tid = threadIdx.x, nt = blockDim.x;
   const int V = a.n_view;
   if (tid < 32) {
     // per view entry: its block's segment, the CTA range that wrote records,
@@ -269,13 +301,13 @@ __device__ void merge_row(const DecodeArgs &a, PlanSmem &P, int r, int h, int64_
     const int lane = tid;
     for (int v = lane; v < V; v += 32) {
       const int b = a.view_block[r * V + v];
-      P.mv_seg[v] = -1;
-      P.mv_qi[v] = 0;
+      X.mv_seg[v] = -1;
+      X.mv_qi[v] = 0;
       if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
         const int64_t s0 = P.ubase[b] + static_cast<int64_t>(h) * P.tiles[b];
-        P.mv_seg[v] = static_cast<int64_t>(b) * a.n_kv_heads + h;
-        P.mv_c0[v] = cta_of_unit(s0, U, C);
-        P.mv_c1[v] = cta_of_unit(s0 + P.tiles[b] - 1, U, C);
+        X.mv_seg[v] = static_cast<int64_t>(b) * a.n_kv_heads + h;
+        X.mv_c0[v] = cta_of_unit(s0, U, C);
+        X.mv_c1[v] = cta_of_unit(s0 + P.tiles[b] - 1, U, C);
       }
     }
     __syncwarp();
@@ -287,34 +319,34 @@ __device__ void merge_row(const DecodeArgs &a, PlanSmem &P, int r, int h, int64_
         const int e = r * V + v;
         const int b = a.view_block[e];
         const unsigned m = __ballot_sync(0xffffffffu, i < e && x == b);
-        if (lane == 0) P.mv_qi[v] += __popc(m);
+        if (lane == 0) X.mv_qi[v] += __popc(m);
       }
     }
   }
-  __syncthreads();
+  sync();
   for (int gi = 0; gi < G; ++gi) {
     // pass 1: M over every record, strided over threads
     float M = -INFINITY;
     for (int v = 0; v < V; ++v) {
-      if (P.mv_seg[v] < 0) continue;
-      const int qi = P.mv_qi[v] * G + gi;
-      for (int c = P.mv_c0[v] + tid; c <= P.mv_c1[v]; c += nt)
-        M = fmaxf(M, __ldcg(record_ptr(a, P.mv_seg[v] + c, qi) + D));
+      if (X.mv_seg[v] < 0) continue;
+      const int qi = X.mv_qi[v] * G + gi;
+      for (int c = X.mv_c0[v] + tid; c <= X.mv_c1[v]; c += nt)
+        M = fmaxf(M, __ldcg(record_ptr(a, X.mv_seg[v] + c, qi) + D));
     }
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if ((tid & 31) == 0) P.red[tid >> 5] = M;
-    __syncthreads();
-    M = P.red[0];
-    for (int w = 1; w < nt / 32; ++w) M = fmaxf(M, P.red[w]);
-    __syncthreads();
+    if ((tid & 31) == 0) X.red[tid >> 5] = M;
+    sync();
+    M = X.red[0];
+    for (int w = 1; w < nt / 32; ++w) M = fmaxf(M, X.red[w]);
+    sync();
     // pass 2: each thread owns elements d = tid + k * nt
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float L = 0.f;
     for (int v = 0; v < V; ++v) {
-      if (P.mv_seg[v] < 0) continue;
-      const int qi = P.mv_qi[v] * G + gi;
-      for (int c = P.mv_c0[v]; c <= P.mv_c1[v]; ++c) {
-        const float *rec = record_ptr(a, P.mv_seg[v] + c, qi);
+      if (X.mv_seg[v] < 0) continue;
+      const int qi = X.mv_qi[v] * G + gi;
+      for (int c = X.mv_c0[v]; c <= X.mv_c1[v]; ++c) {
+        const float *rec = record_ptr(a, X.mv_seg[v] + c, qi);
         const float w = ex2(__ldcg(rec + D) - M);
         L += w * __ldcg(rec + D + 1);
 #pragma unroll
@@ -324,7 +356,7 @@ __device__ void merge_row(const DecodeArgs &a, PlanSmem &P, int r, int h, int64_
         }
       }
     }
-    const int hq = P.qhead[gi];
+    const int hq = qhead[gi];
     const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
     const float inv = 1.f / L;
 #pragma unroll
@@ -335,27 +367,25 @@ __device__ void merge_row(const DecodeArgs &a, PlanSmem &P, int r, int h, int64_
     if (tid == 0 && a.lse) a.lse[ob] = (M + __log2f(L)) * 0.69314718055994530942f;
   }
   if (tid == 0) a.counters[r * a.n_kv_heads + h] = 0;  // re-armed for the next call
-  __syncthreads();
+  sync();
 }
 
-// After a CTA wrote its records for segment (b, h): count arrivals for every
-// row that references b and list the rows whose last record this was.
-// Must be called by all threads after the record stores.
-__device__ __forceinline__ void arrive(const DecodeArgs &a, PlanSmem &P, int b, int h, int64_t U,
-                                       int C) {
+// Count one arrival for every row that references block b (kv head h) and
+// append (r * Hkv + h) to `list` for the rows whose last record this was.  One
+// thread calls it, after the group's record stores were fenced and
+// synchronised.  Returns the new list length.
+__device__ __forceinline__ int arrive_rows(const DecodeArgs &a, const PlanCore &P,
+                                           const SegMeta &M, int h, int64_t U, int C,
+                                           int32_t *list, int n_list, int cap) {
   __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int nm = 0;
-    for (int j = 0; j < P.n_ref && j < kMaxQ; ++j) {
-      const int r = P.ref_entry[j] / a.n_view;
-      const int old = atomicAdd(&a.counters[r * a.n_kv_heads + h], 1);
-      if (old + 1 == expected_records(a, P, r, h, U, C)) P.merge_list[nm++] = r;
-    }
-    P.n_merge = nm;
-    __threadfence();
+  for (int j = 0; j < M.n_ref && j < kMaxQ; ++j) {
+    const int r = M.ref_entry[j] / a.n_view;
+    const int old = atomicAdd(&a.counters[r * a.n_kv_heads + h], 1);
+    if (old + 1 == expected_records(a, P, r, h, U, C) && n_list < cap)
+      list[n_list++] = r * a.n_kv_heads + h;
   }
-  __syncthreads();
+  __threadfence();
+  return n_list;
 }
 
 }  // namespace hw

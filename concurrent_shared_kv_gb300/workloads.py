@@ -174,7 +174,8 @@ def draw_host(w: Workload, layer: int = 0, poison: Optional[float] = None):
         v[:, s:s + n] = rng.standard_normal((Hkv, n, D))
     if w.sink:
         for p in range(w.n_problems):
-            k[:, int(starts[p * (w.n_workers + 1)])] *= 8.0
+            if lens[p * (w.n_workers + 1)] > 0:
+                k[:, int(starts[p * (w.n_workers + 1)])] *= 8.0
     return to_storage(q, w.dtype), to_storage(k, w.dtype), to_storage(v, w.dtype)
 
 
@@ -199,6 +200,7 @@ def draw_device_layer(w: Workload, layer: int, device, poison: float = 0.0):
         v[:, s:s + n] = torch.randn((Hkv, n, D), generator=g, device=device).to(tdt)
     if w.sink:
         for p in range(w.n_problems):
-            s0 = int(starts[p * (w.n_workers + 1)])
-            k[:, s0] = (k[:, s0].float() * 8.0).to(tdt)
+            if lens[p * (w.n_workers + 1)] > 0:
+                s0 = int(starts[p * (w.n_workers + 1)])
+                k[:, s0] = (k[:, s0].float() * 8.0).to(tdt)
     return q, k, v

@@ -11,6 +11,12 @@ from concurrent_shared_kv_gb300 import workloads as wl
 
 F32_TOL = 1e-5                     # max-abs, fp32 storage
 BF16_MAX, BF16_MEAN = 2e-2, 1e-2   # max-abs / mean-abs, bf16 storage, fp32 accumulation
+# Long views average many V rows, so |out| ~ 1/sqrt(L) and an absolute bar
+# alone is loose; the error is also bounded relative to the output's scale
+# (max-abs / max|ref| and rms error / rms ref).  bf16: the output's own
+# rounding is 2^-9 relative; bf16 queries and probabilities in the tensor-core
+# path add a few parts in 1e3.
+REL_TOL = {"f32": 1e-4, "bf16": 2e-2}
 LSE_TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 
@@ -108,6 +114,9 @@ def compare(w_dtype: str, out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what=""
     err = np.abs(g - r)
     mx, mean = float(err.max()), float(err.mean())
     rel = float(mx / max(np.abs(r).max(), 1e-30))
+    rms = float(np.sqrt(np.mean(err ** 2)) / max(np.sqrt(np.mean(r ** 2)), 1e-30))
+    assert rel <= REL_TOL[w_dtype] and rms <= REL_TOL[w_dtype] / 2, \
+        f"{what}: max-abs/max|ref| {rel:.3e}, rms rel {rms:.3e}"
     if w_dtype == "f32":
         assert mx <= F32_TOL, f"{what}: max-abs {mx}"
     else:

@@ -111,8 +111,15 @@ def test_qwen3_commit_all_layers_one_launch():
         mask[dst:dst + n] = True
         assert np.array_equal(kg[:, ~mask], kd[:, ~mask]), l
         got = wl.storage_to_f64(kg[:, mask], "bf16")
-        ulp = np.abs(exact) * 2.0 ** -8
-        assert np.all(np.abs(got - exact) <= ulp + 1e-30), l
+        # one bf16 unit in the last place of the exact value, plus the fp32
+        # rotation's own error where the two products cancel (a few fp32 ulps
+        # of the pair's magnitude)
+        src_pair = wl.storage_to_f64(k0[:, src:src + n], "bf16")
+        half = D // 2
+        mag = np.abs(src_pair) + np.abs(np.concatenate([src_pair[..., half:], src_pair[..., :half]], -1))
+        bound = np.abs(exact) * 2.0 ** -7 + mag * 2.0 ** -20
+        bad = np.abs(got - exact) > bound
+        assert not bad.any(), (l, got[bad][:5], exact[bad][:5], bound[bad][:5])
         # most values are the correctly rounded bf16 of the exact rotation
         assert np.mean(kg[:, mask] == kd[:, mask]) > 0.99
 
