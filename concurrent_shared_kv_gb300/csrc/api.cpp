@@ -1,5 +1,7 @@
 // api.cpp - the C ABI of libhogwild (declared in include/hogwild.h): argument
 // checks on the host, workspace layout, RoPE phase tables, kernel selection.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -48,6 +50,37 @@ void rope_phase_table(int head_dim, double theta, uint64_t *phase) {
     if (x >= 18446744073709551616.0L) x -= 18446744073709551616.0L;
     phase[i] = static_cast<uint64_t>(x);
   }
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// TMA map of one bf16 pool [Hkv][capacity][128]: boxes of 128 tokens x 64
+// elements (128 bytes, the 128-byte swizzle span), one head at a time.
+// Tokens past the capacity read as zeros.
+static bool make_pool_map(CUtensorMap *m, const void *pool, int64_t capacity, int n_kv_heads) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t cap = capacity > 0 ? static_cast<cuuint64_t>(capacity) : 1;
+  cuuint64_t dims[3] = {128, cap, static_cast<cuuint64_t>(n_kv_heads)};
+  cuuint64_t strides[2] = {128 * 2, cap * 128 * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTcTile), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Upper bound on the CTAs of any decode launch: slots are sized for it.
@@ -120,7 +153,9 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
   if (d->n_rows == 0) return HW_OK;
   if (!q || !out || !q_pos) return HW_ERR_INVALID;
   if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
-  if (d->n_blocks > 0 && (!block_start || !block_len || !k_cache || !v_cache)) return HW_ERR_INVALID;
+  if (d->n_blocks > 0 && (!block_start || !block_len)) return HW_ERR_INVALID;
+  // an empty pool (capacity 0) is never read and may be NULL
+  if (d->n_blocks > 0 && d->cache_capacity > 0 && (!k_cache || !v_cache)) return HW_ERR_INVALID;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return HW_ERR_WORKSPACE;
   const int max_ctas = max_decode_ctas();
   if (max_ctas <= 0) return cuda_fail(cudaGetLastError());
@@ -156,10 +191,27 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
 
   const int sms = device_sm_count();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int per_sm = decode_simt_ctas_per_sm(d->dtype, d->head_dim);
-  int ctas = sms * (per_sm > 4 ? 4 : per_sm);
-  if (ctas > max_ctas) ctas = max_ctas;
-  const cudaError_t e = launch_decode_simt(a, d->dtype, ctas, s);
+  cudaError_t e;
+  if (d->dtype == HW_BF16 && d->head_dim == 128) {
+    // tensor-core path: one persistent CTA per SM, K/V tiles by TMA
+    const bool have_pool = d->n_blocks > 0 && d->cache_capacity > 0;
+    if (have_pool && ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u))
+      return HW_ERR_INVALID;
+    CUtensorMap km, vm;
+    std::memset(&km, 0, sizeof km);
+    std::memset(&vm, 0, sizeof vm);
+    if (have_pool) {
+      if (!make_pool_map(&km, k_cache, d->cache_capacity, d->n_kv_heads) ||
+          !make_pool_map(&vm, v_cache, d->cache_capacity, d->n_kv_heads))
+        return cuda_fail(cudaErrorInvalidValue);
+    }
+    e = launch_decode_tc(a, km, vm, sms, s);
+  } else {
+    const int per_sm = decode_simt_ctas_per_sm(d->dtype, d->head_dim);
+    int ctas = sms * (per_sm > 4 ? 4 : per_sm);
+    if (ctas > max_ctas) ctas = max_ctas;
+    e = launch_decode_simt(a, d->dtype, ctas, s);
+  }
   return e == cudaSuccess ? HW_OK : cuda_fail(e);
 }
 

@@ -1,0 +1,616 @@
+// attn_decode_tc.cu - concurrent decode attention for bf16 caches with
+// head_dim 128 on the sm_100 tensor cores (tcgen05 + TMEM), K/V tiles staged
+// by TMA.
+//
+// The path is HBM-bound: every K/V tile is read once and serves every query
+// head that attends it (all workers' view references to the block times the
+// GQA group, up to 32).  At 16-20 flop per KV byte the CUDA cores would be
+// the ceiling, so the two small products run on the tensor cores:
+//   S^T [128 tokens x 32 heads] = K_tile [128 x 128] . Q~^T    (TMEM, fp32)
+//   O^T [128 d x 32 heads]     += V_tile^T [128 x 128 tokens] . P^T
+// with Q~ the rotated queries (Hogwild! notes, key design 1: the query is
+// rotated once per block by i_q - i_k^block; the keys stay as stored).
+//
+// One CTA per SM, persistent over its share of the units (hw_device.cuh).
+// Warp roles, all synchronised by mbarriers with bounded waits:
+//   warp 0     TMA producer: K and V tiles into a 3-stage ring
+//   warp 1     MMA issuer (one thread) and TMEM owner
+//   warps 2-5  softmax: S from TMEM, running max / sum, P (bf16) into smem;
+//              segment epilogue: O from TMEM -> partial records; merges
+//   warps 6-7  rotated queries of the next segment: fp32, scale folded in,
+//              split into bf16 hi + lo parts so that S keeps ~16 mantissa bits
+//              (QK runs as two MMA passes, hi then lo, into one accumulator)
+#include <cuda.h>
+
+#include "hw_device.cuh"
+#include "hw_sm100.cuh"
+
+namespace hw {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kStages = 3;
+constexpr int kT = kTcTile;                   // 128 tokens per tile
+constexpr int kN = kMaxQ;                     // 32 query heads per tile (MMA N)
+constexpr uint32_t kBox = 128 * 64 * 2;       // [128 rows][64 bf16], 128-B swizzled
+constexpr uint32_t kStageBytes = 4 * kBox;    // K lo, K hi, V lo, V hi
+constexpr uint32_t kQHalf = kN * 64 * 2;      // [32 heads][64 bf16], 128-B swizzled
+constexpr uint32_t kQPart = 2 * kQHalf;       // one part (hi or lo): d 0-63, d 64-127
+constexpr uint32_t kQBytes = 2 * kQPart;      // hi, lo
+constexpr uint32_t kPBytes = kT * kN * 2;     // [128 tokens][32 heads], 64-B swizzled
+constexpr uint32_t kTmemCols = 128;           // S0 [0,32)  S1 [32,64)  O [64,96)
+constexpr uint32_t kColO = 64;
+constexpr int kMergeCap = 64;
+constexpr float kLazy = 8.f;                  // rescale only when the max grows by > 2^8
+
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
+
+struct TcSmem {
+  alignas(1024) uint8_t stage[kStages][kStageBytes];
+  alignas(1024) uint8_t q[kQBytes];
+  alignas(1024) uint8_t p[kPBytes];  // also the plan scratch before the main loop
+  PlanCore plan;
+  SegMeta meta;        // handed from the query warps to the softmax warps
+  SegMeta qmeta;       // the query warps' working copy
+  SegMeta smeta;       // the softmax warps' copy for the segment epilogue
+  MergeScratch merge;
+  alignas(16) float red[2][kN][4];  // per tile: column maxima of the 4 softmax warps (read as float4)
+  alignas(16) float lsum[4][kN];    // per segment: column sums of the 4 softmax warps
+  int32_t merge_list[kMergeCap];
+  int32_t merge_qhead[kMaxQ];
+  int32_t n_merge;
+  int32_t abort_flag;
+  uint32_t tmem_base;
+  alignas(8) uint64_t k_full[kStages];
+  uint64_t v_full[kStages], kv_empty[kStages];
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full, p_empty, o_full, o_empty, mma_done;
+};
+
+__device__ __forceinline__ void set_abort(TcSmem &S, const DecodeArgs &a) {
+  if (atomicExch(&S.abort_flag, 1) == 0) flag_error(a.err, HW_DEV_TIMEOUT);
+}
+__device__ __forceinline__ bool aborted(TcSmem &S) {
+  return *reinterpret_cast<volatile int32_t *>(&S.abort_flag) != 0;
+}
+// Bounded wait; on timeout the CTA winds down.
+__device__ __forceinline__ bool wait_or_abort(TcSmem &S, const DecodeArgs &a, uint64_t *bar,
+                                              uint32_t parity) {
+  if (aborted(S)) return false;
+  if (mbar_wait(bar, parity)) return true;
+  set_abort(S, a);
+  return false;
+}
+
+__device__ __forceinline__ bool seg_first_unit(const UnitPos &x, int64_t u, int64_t u0) {
+  return u == u0 || u == x.seg_first;
+}
+__device__ __forceinline__ bool seg_last_unit(const UnitPos &x, int64_t u, int64_t u1) {
+  return u + 1 == u1 || u + 1 == x.seg_first + x.tiles;
+}
+
+// order-preserving float <-> int map for integer max reductions
+__device__ __forceinline__ int f2ord(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : i ^ 0x7fffffff;
+}
+__device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&p);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// ------------------------------------------------------------------ roles
+
+__device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
+                         const CUtensorMap *tv, int64_t u0, int64_t u1) {
+  tma_prefetch_desc(tk);
+  tma_prefetch_desc(tv);
+  const uint64_t pol = policy_evict_first();
+  int i = 0;
+  for (int64_t u = u0; u < u1; ++u, ++i) {
+    const int s = i % kStages;
+    if (!wait_or_abort(S, a, &S.kv_empty[s], ((i / kStages) & 1) ^ 1)) break;
+    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    const int row = a.block_start[x.b] + x.t * kT;
+    uint8_t *st = S.stage[s];
+    mbar_arrive_expect_tx(&S.k_full[s], 2 * kBox);
+    tma_load_3d(st, tk, &S.k_full[s], 0, row, x.h, pol);
+    tma_load_3d(st + kBox, tk, &S.k_full[s], 64, row, x.h, pol);
+    mbar_arrive_expect_tx(&S.v_full[s], 2 * kBox);
+    tma_load_3d(st + 2 * kBox, tv, &S.v_full[s], 0, row, x.h, pol);
+    tma_load_3d(st + 3 * kBox, tv, &S.v_full[s], 64, row, x.h, pol);
+  }
+  // no copy may still be landing in shared memory when the CTA retires
+  for (int j = (i > kStages ? i - kStages : 0); j < i; ++j) {
+    mbar_wait(&S.k_full[j % kStages], (j / kStages) & 1);
+    mbar_wait(&S.v_full[j % kStages], (j / kStages) & 1);
+  }
+}
+
+__device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0, int64_t u1) {
+  constexpr uint32_t idesc_qk = idesc_bf16(128, kN, 0, 0);  // K tile, Q~: both K-major
+  constexpr uint32_t idesc_pv = idesc_bf16(128, kN, 1, 1);  // V tile, P: both MN-major
+  const int n = static_cast<int>(u1 - u0);
+  int iq = 0, ip = 0, seg_q = -1, seg_p = -1;
+  long long last_progress = clock64();
+  while (ip < n) {
+    if (aborted(S)) break;
+    bool progressed = false;
+    if (iq < n && iq < ip + 2) {
+      const int64_t u = u0 + iq;
+      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+      const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
+      const int kseg = first ? seg_q + 1 : seg_q;
+      const int s = iq % kStages, sb = iq & 1;
+      if (mbar_test(&S.k_full[s], (iq / kStages) & 1) &&
+          mbar_test(&S.s_empty[sb], ((iq >> 1) & 1) ^ 1) &&
+          (!first || mbar_test(&S.q_full, kseg & 1))) {
+        seg_q = kseg;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(S.stage[s]), qbase = smem_u32(S.q);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {  // 8 k-steps against Q~ hi, then 8 against Q~ lo
+          const int k8 = kk & 7;
+          const uint64_t ad = smem_desc(kb + (k8 >> 2) * kBox + (k8 & 3) * 32, 16, 1024, kSw128);
+          const uint64_t bd = smem_desc(qbase + (kk >> 3) * kQPart + (k8 >> 2) * kQHalf + (k8 & 3) * 32,
+                                        16, 1024, kSw128);
+          mma_bf16(tmem + sb * kN, ad, bd, idesc_qk, kk > 0);
+        }
+        mma_commit(&S.s_full[sb]);
+        if (last) mma_commit(&S.q_empty);
+        ++iq;
+        progressed = true;
+      }
+    }
+    if (ip < iq) {
+      const int64_t u = u0 + ip;
+      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+      const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
+      const int kseg = first ? seg_p + 1 : seg_p;
+      const int s = ip % kStages;
+      if (mbar_test(&S.p_full, ip & 1) && mbar_test(&S.v_full[s], (ip / kStages) & 1) &&
+          (!first || kseg == 0 || mbar_test(&S.o_empty, (kseg - 1) & 1))) {
+        seg_p = kseg;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(S.stage[s]) + 2 * kBox, pb = smem_u32(S.p);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart,
+          // 8-token groups 1024 B apart.  P^T: MN-major, 32 heads = one 64-B atom,
+          // 8-token groups 512 B apart.
+          const uint64_t ad = smem_desc(vb + kk * 2048, kBox, 1024, kSw128);
+          const uint64_t bd = smem_desc(pb + kk * 1024, 512, 512, kSw64);
+          mma_bf16(tmem + kColO, ad, bd, idesc_pv, !(first && kk == 0));
+        }
+        mma_commit(&S.kv_empty[s]);
+        mma_commit(&S.p_empty);
+        if (last) mma_commit(&S.o_full);
+        ++ip;
+        progressed = true;
+      }
+    }
+    if (progressed) {
+      last_progress = clock64();
+    } else if (clock64() - last_progress > kWaitLimit) {
+      set_abort(S, a);
+      break;
+    }
+  }
+  mma_commit(&S.mma_done);
+  mbar_wait(&S.mma_done, 0);
+}
+
+// Rotated queries, one segment at a time: q~ = rho(q, i_q - offset) * scale *
+// log2(e) for every (view reference, q head) pair of the segment.  The values
+// of segment j are computed in registers while the tensor cores still work on
+// segment j - 1; they are written once the single Q~ buffer is released.
+__device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
+  const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
+  const int lane = threadIdx.x & 31;
+  const int G = a.n_q_heads / a.n_kv_heads;
+  NamedSync<2, 64> sync;
+  const uint32_t qbase = smem_u32(S.q);
+  int seg = -1;
+  for (int64_t u = u0; u < u1;) {
+    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    ++seg;
+    SegMeta &M = S.qmeta;
+    if (tq < 32) {
+      gather_refs(a, M, x.b, lane);
+      gather_qheads(a, M, x.h, lane);
+    }
+    sync();
+    const int nq = min(M.n_ref * G, kN);
+    // pair k of this thread: idx = tq + 64 k -> head qi = idx / 64, element i = idx % 64
+    float y[2 * kN];
+#pragma unroll
+    for (int k = 0; k < kN; ++k) {
+      const int idx = tq + 64 * k;
+      const int qi = idx >> 6, i = idx & 63;
+      float y0 = 0.f, y1 = 0.f;
+      if (qi < nq) {
+        const int e = M.ref_entry[qi / G];
+        const int r = e / a.n_view;
+        const int hq = M.qhead[qi % G];
+        const int64_t rel = static_cast<int64_t>(a.q_pos[r]) - a.view_offset[e];
+        const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
+                                  (static_cast<int64_t>(r) * a.n_q_heads + hq) * 128;
+        const float x0 = __bfloat162float(qp[i]), x1 = __bfloat162float(qp[i + 64]);
+        float cs, sn;
+        rope_cos_sin(rel, a.phase[i], &cs, &sn);
+        // scores leave the MMA already in log2 units: scale * log2(e) folded in
+        y0 = (x0 * cs - x1 * sn) * a.scale_log2;
+        y1 = (x1 * cs + x0 * sn) * a.scale_log2;
+      }
+      y[2 * k] = y0;
+      y[2 * k + 1] = y1;
+    }
+    // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
+    // warps keep the same control flow so the named barrier stays balanced.
+    // The Q~ buffer and the hand-off metadata are free once segment seg-1's QK
+    // products completed and the softmax warps took their copy.
+    if (seg > 0) wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
+    if (tq < 32) {
+      for (int j = lane; j < kMaxQ; j += 32) {
+        S.meta.ref_entry[j] = M.ref_entry[j];
+        S.meta.qhead[j] = M.qhead[j];
+      }
+      if (lane == 0) S.meta.n_ref = M.n_ref;
+    }
+#pragma unroll
+    for (int k = 0; k < kN; ++k) {
+      const int idx = tq + 64 * k;
+      const int qi = idx >> 6, i = idx & 63;
+      // element d of head qi: half d / 64, row qi (128 B), 16-B chunk swizzled by qi % 8
+      const uint32_t chunk = static_cast<uint32_t>(i >> 3), e2 = static_cast<uint32_t>(i & 7) * 2;
+      const uint32_t off = qi * 128 + ((chunk ^ (qi & 7)) << 4) + e2;
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {  // element i, then i + 64
+        const float v = y[2 * k + hv];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+        const uint32_t o = qbase + hv * kQHalf + off;
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(o), "h"(__bfloat16_as_ushort(hi)) : "memory");
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(o + kQPart), "h"(__bfloat16_as_ushort(lo)) : "memory");
+      }
+    }
+    fence_proxy_async_smem();
+    sync();
+    if (tq == 0) mbar_arrive(&S.q_full);
+    u = x.seg_first + x.tiles;
+  }
+}
+
+// Merges queued by this CTA (the rows whose last record it delivered).
+template <typename Sync>
+__device__ void run_merges(const DecodeArgs &a, TcSmem &S, int64_t U, int C, int ts, Sync sync) {
+  const int n = S.n_merge;
+  for (int m = 0; m < n; ++m) {
+    const int rh = S.merge_list[m];
+    const int r = rh / a.n_kv_heads, h = rh % a.n_kv_heads;
+    if (ts < 32) {
+      const int G = a.n_q_heads / a.n_kv_heads;
+      if (!a.q_to_kv) {
+        for (int i = ts; i < G; i += 32) S.merge_qhead[i] = h * G + i;
+      } else {
+        int cnt = 0;
+        for (int base = 0; base < a.n_q_heads; base += 32) {
+          const int hq = base + ts;
+          const bool mm = hq < a.n_q_heads && a.q_to_kv[hq] == h;
+          const unsigned mask = __ballot_sync(0xffffffffu, mm);
+          const int pos = cnt + __popc(mask & ((1u << ts) - 1u));
+          if (mm && pos < G) S.merge_qhead[pos] = hq;
+          cnt += __popc(mask);
+        }
+      }
+    }
+    sync();
+    merge_row<__nv_bfloat16>(a, S.plan, S.merge, S.merge_qhead, r, h, U, C, ts, 128, sync);
+  }
+  sync();
+  if (ts == 0) S.n_merge = 0;
+  sync();
+}
+
+__device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0,
+                             int64_t u1, int64_t U, int C) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ws = warp - kWarpSoft;              // 0..3
+  const int ts = threadIdx.x - kWarpSoft * 32;  // 0..127
+  const int qd = warp & 3;                      // TMEM lane quadrant of this warp
+  const int row = qd * 32 + lane;               // token of the tile (S) / element d (O)
+  const uint32_t tl = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+  const int G = a.n_q_heads / a.n_kv_heads;
+  const int n = static_cast<int>(u1 - u0);
+  NamedSync<1, 128> sync;
+  const uint32_t pb = smem_u32(S.p);
+
+  // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: every
+  // thread of the group keeps the same control flow, so the named barriers
+  // below are always reached by all 128 threads; after an abort no wait
+  // blocks any more and the CTA runs to its end on stale data.
+  float m_run[kN], l_part[kN];
+  int seg = -1, nq = 0;
+  for (int i = 0; i < n; ++i) {
+    const int64_t u = u0 + i;
+    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
+    if (first) {
+      ++seg;
+      wait_or_abort(S, a, &S.q_full, seg & 1);
+      nq = min(S.meta.n_ref * G, kN);
+      if (ws == 0) {  // private copy for the epilogue, then hand the buffer back
+        for (int j = lane; j < kMaxQ; j += 32) S.smeta.ref_entry[j] = S.meta.ref_entry[j];
+        if (lane == 0) S.smeta.n_ref = S.meta.n_ref;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.q_empty);
+#pragma unroll
+      for (int j = 0; j < kN; ++j) {
+        m_run[j] = -INFINITY;
+        l_part[j] = 0.f;
+      }
+    }
+    const int sb = i & 1, s = i % kStages;
+    wait_or_abort(S, a, &S.s_full[sb], (i >> 1) & 1);
+    tc_fence_after();
+    __syncwarp();
+    uint32_t r[32];
+    tmem_ld32(tl + sb * kN, r);
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.s_empty[sb]);
+
+    const int valid = min(kT, a.block_len[x.b] - x.t * kT);
+    const bool tok_ok = row < valid;
+    float sc[kN];
+#pragma unroll
+    for (int j = 0; j < kN; ++j) sc[j] = tok_ok ? __uint_as_float(r[j]) : -INFINITY;
+
+    // column maxima over the tile's 128 tokens
+    float(*red)[4] = S.red[i & 1];
+#pragma unroll
+    for (int j = 0; j < kN; ++j) {
+      if (j < nq) {
+        const int mk = __reduce_max_sync(0xffffffffu, f2ord(sc[j]));
+        if (lane == j) red[j][ws] = ord2f(mk);
+      }
+    }
+    sync();
+    float tmax[kN];
+#pragma unroll
+    for (int j = 0; j < kN; ++j) {
+      if (j < nq) {
+        const float4 v = *reinterpret_cast<const float4 *>(red[j]);
+        tmax[j] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+      } else {
+        tmax[j] = -INFINITY;
+      }
+    }
+    // lazy rescaling: the reference max moves only when a column's max grows
+    // by more than 2^kLazy, so p <= 2^kLazy and O is rarely touched
+    bool need = false;
+#pragma unroll
+    for (int j = 0; j < kN; ++j) need |= (j < nq) && (tmax[j] > m_run[j] + kLazy);
+    bool waited_p = false;
+    if (need) {
+      float alpha[kN];
+#pragma unroll
+      for (int j = 0; j < kN; ++j) {
+        alpha[j] = 1.f;
+        if (j < nq && tmax[j] > m_run[j] + kLazy) {
+          alpha[j] = ex2(m_run[j] - tmax[j]);  // 0 when m_run = -inf
+          m_run[j] = tmax[j];
+        }
+        l_part[j] *= alpha[j];
+      }
+      if (!first) {
+        // O must hold every earlier tile before it is rescaled
+        wait_or_abort(S, a, &S.p_empty, (i - 1) & 1);
+        waited_p = true;
+        tc_fence_after();
+        __syncwarp();
+        uint32_t o[32];
+        tmem_ld32(tl + kColO, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
+        tmem_st32(tl + kColO, o);
+        tmem_wait_st();
+        tc_fence_before();
+      }
+    }
+    uint32_t pk[kN / 2];
+#pragma unroll
+    for (int j = 0; j < kN; j += 2) {
+      const float p0 = (j < nq) ? ex2(sc[j] - m_run[j]) : 0.f;
+      const float p1 = (j + 1 < nq) ? ex2(sc[j + 1] - m_run[j + 1]) : 0.f;
+      pk[j / 2] = pack_bf16(p0, p1);
+      // the sum uses the same rounded weights the P.V product sees
+      l_part[j] += __uint_as_float(pk[j / 2] << 16);
+      l_part[j + 1] += __uint_as_float(pk[j / 2] & 0xffff0000u);
+    }
+    // the single P buffer is free once PV of the previous tile has completed
+    if (i > 0 && !waited_p) wait_or_abort(S, a, &S.p_empty, (i - 1) & 1);
+    if (valid < kT) {
+      // V rows past the block end may hold anything: zero them (p = 0 there,
+      // but 0 * NaN would still poison the sum)
+      wait_or_abort(S, a, &S.v_full[s], (i / kStages) & 1);
+      if (!tok_ok) {
+        const uint32_t v0 = smem_u32(S.stage[s]) + 2 * kBox + row * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          st_shared_v4(v0 + c * 16, 0, 0, 0, 0);
+          st_shared_v4(v0 + kBox + c * 16, 0, 0, 0, 0);
+        }
+      }
+    }
+    // P row of this token: 32 heads = four 16-B chunks, 64-B swizzle
+    const uint32_t prow = pb + row * 64;
+    const uint32_t swz = (row >> 1) & 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      st_shared_v4(prow + ((c ^ swz) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.p_full);
+
+    if (last) {
+      // ---- segment epilogue: O -> records, arrivals
+      wait_or_abort(S, a, &S.o_full, seg & 1);
+      tc_fence_after();
+      __syncwarp();
+      uint32_t o[32];
+      tmem_ld32(tl + kColO, o);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.o_empty);
+      // column sums of l: transpose-reduce inside the warp, lane j ends with column j
+      float v[kN];
+#pragma unroll
+      for (int j = 0; j < kN; ++j) v[j] = l_part[j];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+        for (int k = 0; k < off; ++k) {
+          const bool up = (lane & off) != 0;
+          const float mine = up ? v[k + off] : v[k];
+          const float other = up ? v[k] : v[k + off];
+          v[k] = mine + __shfl_xor_sync(0xffffffffu, other, off);
+        }
+      }
+      S.lsum[ws][lane] = v[0];
+      float mcol = 0.f;
+#pragma unroll
+      for (int j = 0; j < kN; ++j)
+        if (j == lane) mcol = m_run[j];
+      sync();
+      const int64_t slot = static_cast<int64_t>(x.b) * a.n_kv_heads + x.h + blockIdx.x;
+#pragma unroll
+      for (int j = 0; j < kN; ++j)
+        if (j < nq) record_ptr(a, slot, j)[row] = __uint_as_float(o[j]);
+      if (ws == 0 && lane < nq) {
+        float *rec = record_ptr(a, slot, lane);
+        rec[128] = mcol;
+        rec[129] = S.lsum[0][lane] + S.lsum[1][lane] + S.lsum[2][lane] + S.lsum[3][lane];
+      }
+      __threadfence();
+      sync();
+      // keep room in the merge list: merge what is pending when it could overflow
+      if (S.n_merge + S.smeta.n_ref > kMergeCap) run_merges(a, S, U, C, ts, sync);
+      if (ts == 0)
+        S.n_merge = arrive_rows(a, S.plan, S.smeta, x.h, U, C, S.merge_list, S.n_merge, kMergeCap);
+      sync();
+    }
+  }
+  run_merges(a, S, U, C, ts, sync);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ uint8_t smem_raw[];
+  TcSmem &S = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.k_full[s], 1);
+      mbar_init(&S.v_full[s], 1);
+      mbar_init(&S.kv_empty[s], 1);
+    }
+    mbar_init(&S.q_full, 1);
+    mbar_init(&S.q_empty, 5);  // last QK of the segment + each softmax warp's read
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.s_full[b], 1);
+      mbar_init(&S.s_empty[b], 4);  // one per softmax warp
+    }
+    mbar_init(&S.p_full, 4);
+    mbar_init(&S.p_empty, 1);
+    mbar_init(&S.o_full, 1);
+    mbar_init(&S.o_empty, 4);
+    mbar_init(&S.mma_done, 1);
+    S.abort_flag = 0;
+    S.n_merge = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  build_plan<kT>(a, S.plan, *reinterpret_cast<PlanScratch *>(S.p));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  const int c = blockIdx.x;
+  const int64_t U = S.plan.ubase[a.n_blocks];
+  const int C = static_cast<int>(U < gridDim.x ? U : gridDim.x);
+
+  // (row, kv head) pairs without any record: out = 0, lse = -inf
+  for (int rh = c; rh < a.n_rows * a.n_kv_heads; rh += gridDim.x) {
+    const int r = rh / a.n_kv_heads, h = rh % a.n_kv_heads;
+    if (expected_records(a, S.plan, r, h, U, C) == 0) {
+      if (warp == 0) gather_qheads(a, S.meta, h, lane);
+      __syncthreads();
+      write_empty<__nv_bfloat16>(a, S.meta.qhead, r, tid, kThreads);
+      __syncthreads();
+    }
+  }
+
+  if (U > 0 && c < C) {
+    const int64_t u0 = cta_unit_begin(U, c, C), u1 = cta_unit_begin(U, c + 1, C);
+    if (warp == kWarpTma) {
+      if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1);
+    } else if (warp == kWarpMma) {
+      if (lane == 0) mma_issuer(a, S, tmem, u0, u1);
+    } else if (warp < kWarpQ) {
+      softmax_role(a, S, tmem, u0, u1, U, C);
+    } else {
+      qprep(a, S, u0, u1);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t decode_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
+
+cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                             int ctas, cudaStream_t s) {
+  const size_t smem = decode_tc_smem_bytes();
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  decode_tc_kernel<<<ctas, kThreads, smem, s>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace hw

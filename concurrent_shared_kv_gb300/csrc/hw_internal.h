@@ -2,6 +2,7 @@
 // kernel translation units.  Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,7 +52,9 @@ int device_sm_count();  // SMs of the current device, cached; <= 0 on failure
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_decode_simt(const DecodeArgs &a, int dtype, int ctas, cudaStream_t s);
-cudaError_t launch_decode_tc(const DecodeArgs &a, int ctas, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &k_map,
+                             const CUtensorMap &v_map, int ctas, cudaStream_t s);
+size_t decode_tc_smem_bytes();
 int decode_simt_ctas_per_sm(int dtype, int head_dim);
 
 struct CommitArgs {

@@ -115,8 +115,9 @@ int hw_workspace_init(void *workspace, size_t bytes, void *stream);
  *
  *  d            host  description (above)
  *  q            dev   [n_rows][Hq][D] dtype, un-rotated queries
- *  k_cache      dev   [Hkv][capacity][D] dtype, keys rotated at block-local positions
- *  v_cache      dev   [Hkv][capacity][D] dtype
+ *  k_cache      dev   [Hkv][capacity][D] dtype, keys rotated at block-local positions;
+ *                     16-byte aligned; may be NULL when capacity is 0
+ *  v_cache      dev   [Hkv][capacity][D] dtype, same rules
  *  block_start  dev   int32 [n_blocks], first pool token of each block
  *  block_len    dev   int32 [n_blocks], tokens in each block
  *  view_block   dev   int32 [n_rows][V], block ids in view order, -1 = unused slot
