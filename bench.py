@@ -38,6 +38,9 @@ def parse():
     p.add_argument("--config", default="C3", choices=["C2", "C3", "C4", "C5"])
     p.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--layers", type=int, default=0,
+                   help="time only the first N layers (profiling of a small case); 0 = all")
     return p.parse_args()
 
 
@@ -177,6 +180,8 @@ def main():
     w = wl.ALL[args.config]()
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     L = w.layers if args.config != "C5" else 1
+    if args.layers > 0:
+        L = min(L, args.layers)
     lens, starts = w.block_lengths(), w.block_starts()
     vb, vo, qp = api.views_combined(lens, w.n_problems, w.n_workers)
     sess = engine.DecodeSession(n_rows=w.n_rows, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
@@ -193,6 +198,7 @@ def main():
     outs = [torch.empty_like(qs[0]) for _ in range(L)]
     lses = [torch.empty((w.n_rows, w.n_q_heads), dtype=torch.float32, device=dev) for _ in range(L)]
     calls_per_step = L if args.config != "C5" else 64  # C5: one layer timed x64
+    kernel = "decode_tc_kernel" if (w.dtype == "bf16" and w.head_dim == 128) else "decode_simt_kernel"
     stream = torch.cuda.Stream(device=dev)
 
     def step():
@@ -252,42 +258,49 @@ def main():
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["hbm_gbs"])
 
-    # end to end through the public API with host buffers: each step uploads
-    # every layer's query from pinned host memory and reads every layer's
-    # output and lse back; the KV pools are the resident cache state.
-    q_host = [q.cpu().pin_memory() for q in qs]
-    o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    l_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in lses]
-    qdev = [torch.empty_like(q) for q in qs]
-    meta_host = [torch.from_numpy(np.ascontiguousarray(x, np.int32)).pin_memory()
-                 for x in (starts, lens, vb, vo, qp)]
-    h2d = sum(q.numel() * q.element_size() for q in q_host) + sum(m.numel() * 4 for m in meta_host)
-    d2h = sum(o.numel() * o.element_size() for o in o_host) + sum(x.numel() * 4 for x in l_host)
+    def run_e2e():
+        # end to end through the public API with host buffers: each step uploads
+        # every layer's query from pinned host memory and reads every layer's
+        # output and lse back; the KV pools are the resident cache state.
+        q_host = [q.cpu().pin_memory() for q in qs]
+        o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        l_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in lses]
+        qdev = [torch.empty_like(q) for q in qs]
+        meta_host = [torch.from_numpy(np.ascontiguousarray(x, np.int32)).pin_memory()
+                     for x in (starts, lens, vb, vo, qp)]
+        h2d = sum(q.numel() * q.element_size() for q in q_host) + sum(m.numel() * 4 for m in meta_host)
+        d2h = sum(o.numel() * o.element_size() for o in o_host) + sum(x.numel() * 4 for x in l_host)
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for m, name in zip(meta_host, ("block_start", "block_len", "view_block", "view_offset", "q_pos")):
-                sess.meta[name].copy_(m, non_blocking=True)
-            for l in range(L):
-                qdev[l].copy_(q_host[l], non_blocking=True)
-            for i in range(calls_per_step):
-                l = i % L
-                sess.decode(qdev[l], ks[l], vs[l], out=outs[l], lse=lses[l], stream=stream)
-            for l in range(L):
-                o_host[l].copy_(outs[l], non_blocking=True)
-                l_host[l].copy_(lses[l], non_blocking=True)
+        def e2e_step():  # noqa: E306
+            with torch.cuda.stream(stream):
+                for m, name in zip(meta_host, ("block_start", "block_len", "view_block", "view_offset", "q_pos")):
+                    sess.meta[name].copy_(m, non_blocking=True)
+                for l in range(L):
+                    qdev[l].copy_(q_host[l], non_blocking=True)
+                for i in range(calls_per_step):
+                    l = i % L
+                    sess.decode(qdev[l], ks[l], vs[l], out=outs[l], lse=lses[l], stream=stream)
+                for l in range(L):
+                    o_host[l].copy_(outs[l], non_blocking=True)
+                    l_host[l].copy_(lses[l], non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    stream.synchronize()
-    e2e_steps = max(3, min(args.steps, 10))
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+        for _ in range(2):
+            e2e_step()
         stream.synchronize()
-    t_e2e = (time.perf_counter() - t0) / e2e_steps
-    e2e_gbs = step_bytes / t_e2e / 1e9 * world
+        e2e_steps = max(3, min(args.steps, 10))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+            stream.synchronize()
+        t_e2e = (time.perf_counter() - t0) / e2e_steps
+        e2e_gbs = step_bytes / t_e2e / 1e9 * world
+        return {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e()
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -306,11 +319,10 @@ def main():
         "worker_tokens_per_s_per_layer": w.n_rows / per_launch,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "hw_attn_decode (decode_simt_kernel)"},
+                     "kernel": f"hw_attn_decode ({kernel})"},
         "gpu_launches": calls_per_step * args.steps,
         "clocks": clk.summary(),
-        "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
+        "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = timed_oracle(w, qs, ks, vs, starts, lens, vb, vo, qp)
