@@ -10,9 +10,9 @@
 //   2. K and V tiles of 64 tokens are read from HBM once for all of them;
 //   3. scores and an online softmax in the log2 domain; P.V accumulates in
 //      registers;
-//   4. a partial record (m, l, o) per query head goes to the workspace and the
-//      last arriving CTA per (row, kv head) merges (omica.com.cn article,
-//      section 3.2: split over SMs, partial results merged).
+//   4. a partial record (m, l, o) per query head goes to the workspace; after
+//      its units every CTA takes part in the merge phase (omica.com.cn
+//      article, section 3.2: split over SMs, partial results merged).
 #include "hw_device.cuh"
 
 namespace hw {
@@ -25,8 +25,8 @@ struct SimtSmem {
   PlanScratch scratch;
   SegMeta meta;
   MergeScratch merge;
-  int32_t merge_list[kMaxQ];
-  int32_t n_merge;
+  int32_t merge_qhead[kMaxQ];
+  int32_t merge_flag;
   alignas(16) float q[kMaxQ][D + 4];
   alignas(16) float k[kSimtTile][D + 4];
   alignas(16) float v[kSimtTile][D + 4];
@@ -205,11 +205,8 @@ __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, 
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) S.n_merge = arrive_rows(a, P, M, h, U, C, S.merge_list, 0, kMaxQ);
-  __syncthreads();
-  for (int i = 0; i < S.n_merge; ++i)
-    merge_row<T>(a, P, S.merge, M.qhead, S.merge_list[i] / a.n_kv_heads, h, U, C, tid,
-                 kSimtThreads, CtaSync());
+  if (tid == 0) arrive_segment(a, M, h);
+  __syncthreads();  // the segment metadata is rewritten by the next segment
 }
 
 template <typename T, int D>
@@ -232,17 +229,20 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
       __syncthreads();
     }
   }
-  if (U == 0 || c >= C) return;
-
-  int64_t u = cta_unit_begin(U, c, C);
-  const int64_t u_end = cta_unit_begin(U, c + 1, C);
-  while (u < u_end) {
-    const UnitPos x = unit_pos(P, a.n_blocks, u);
-    const int64_t seg_stop = min(x.seg_first + x.tiles, u_end);
-    simt_segment<T, D>(a, S, x.b, x.h, static_cast<int>(u - x.seg_first),
-                       static_cast<int>(seg_stop - x.seg_first), U, C);
-    u = seg_stop;
+  if (U > 0 && c < C) {
+    int64_t u = cta_unit_begin(U, c, C);
+    const int64_t u_end = cta_unit_begin(U, c + 1, C);
+    while (u < u_end) {
+      const UnitPos x = unit_pos(P, a.n_blocks, u);
+      const int64_t seg_stop = min(x.seg_first + x.tiles, u_end);
+      simt_segment<T, D>(a, S, x.b, x.h, static_cast<int>(u - x.seg_first),
+                         static_cast<int>(seg_stop - x.seg_first), U, C);
+      u = seg_stop;
+    }
   }
+  __syncthreads();
+  merge_phase<T, D>(a, P, S.merge, S.merge_qhead, &S.merge_flag, U, C, threadIdx.x, kSimtThreads,
+                    CtaSync(), 2000000000ll);
 }
 
 template <typename T, int D>
@@ -256,8 +256,18 @@ static cudaError_t launch_simt(const DecodeArgs &a, int ctas, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  decode_simt_kernel<T, D><<<ctas, kSimtThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  // cooperative: the merge phase waits on other CTAs, so all must be resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kSimtThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_simt_kernel<T, D>, a);
 }
 
 template <typename T, int D>

@@ -16,7 +16,8 @@
 //   warp 0     TMA producer: K and V tiles into a 3-stage ring
 //   warp 1     MMA issuer (one thread) and TMEM owner
 //   warps 2-5  softmax: S from TMEM, running max / sum, P (bf16) into smem;
-//              segment epilogue: O from TMEM -> partial records; merges
+//              segment epilogue: O from TMEM -> partial records
+// then all eight warps take part in the grid-wide merge phase (hw_device.cuh).
 //   warps 6-7  rotated queries of the next segment: fp32, scale folded in,
 //              split into bf16 hi + lo parts so that S keeps ~16 mantissa bits
 //              (QK runs as two MMA passes, hi then lo, into one accumulator)
@@ -43,7 +44,6 @@ constexpr uint32_t kQBytes = 2 * kQPart;      // hi, lo
 constexpr uint32_t kPBytes = kT * kN * 2;     // [128 tokens][32 heads], 64-B swizzled
 constexpr uint32_t kTmemCols = 128;           // S0 [0,32)  S1 [32,64)  O [64,96)
 constexpr uint32_t kColO = 64;
-constexpr int kMergeCap = 64;
 constexpr float kLazy = 8.f;                  // rescale only when the max grows by > 2^8
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
@@ -59,9 +59,8 @@ struct TcSmem {
   MergeScratch merge;
   alignas(16) float red[2][kN][4];  // per tile: column maxima of the 4 softmax warps (read as float4)
   alignas(16) float lsum[4][kN];    // per segment: column sums of the 4 softmax warps
-  int32_t merge_list[kMergeCap];
   int32_t merge_qhead[kMaxQ];
-  int32_t n_merge;
+  int32_t merge_flag;
   int32_t abort_flag;
   uint32_t tmem_base;
   alignas(8) uint64_t k_full[kStages];
@@ -294,39 +293,8 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   }
 }
 
-// Merges queued by this CTA (the rows whose last record it delivered).
-template <typename Sync>
-__device__ void run_merges(const DecodeArgs &a, TcSmem &S, int64_t U, int C, int ts, Sync sync) {
-  const int n = S.n_merge;
-  for (int m = 0; m < n; ++m) {
-    const int rh = S.merge_list[m];
-    const int r = rh / a.n_kv_heads, h = rh % a.n_kv_heads;
-    if (ts < 32) {
-      const int G = a.n_q_heads / a.n_kv_heads;
-      if (!a.q_to_kv) {
-        for (int i = ts; i < G; i += 32) S.merge_qhead[i] = h * G + i;
-      } else {
-        int cnt = 0;
-        for (int base = 0; base < a.n_q_heads; base += 32) {
-          const int hq = base + ts;
-          const bool mm = hq < a.n_q_heads && a.q_to_kv[hq] == h;
-          const unsigned mask = __ballot_sync(0xffffffffu, mm);
-          const int pos = cnt + __popc(mask & ((1u << ts) - 1u));
-          if (mm && pos < G) S.merge_qhead[pos] = hq;
-          cnt += __popc(mask);
-        }
-      }
-    }
-    sync();
-    merge_row<__nv_bfloat16>(a, S.plan, S.merge, S.merge_qhead, r, h, U, C, ts, 128, sync);
-  }
-  sync();
-  if (ts == 0) S.n_merge = 0;
-  sync();
-}
-
 __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0,
-                             int64_t u1, int64_t U, int C) {
+                             int64_t u1) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ws = warp - kWarpSoft;              // 0..3
   const int ts = threadIdx.x - kWarpSoft * 32;  // 0..127
@@ -511,14 +479,9 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       }
       __threadfence();
       sync();
-      // keep room in the merge list: merge what is pending when it could overflow
-      if (S.n_merge + S.smeta.n_ref > kMergeCap) run_merges(a, S, U, C, ts, sync);
-      if (ts == 0)
-        S.n_merge = arrive_rows(a, S.plan, S.smeta, x.h, U, C, S.merge_list, S.n_merge, kMergeCap);
-      sync();
+      if (ts == 0) arrive_segment(a, S.smeta, x.h);
     }
   }
-  run_merges(a, S, U, C, ts, sync);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -547,7 +510,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&S.o_empty, 4);
     mbar_init(&S.mma_done, 1);
     S.abort_flag = 0;
-    S.n_merge = 0;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -581,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma) {
       if (lane == 0) mma_issuer(a, S, tmem, u0, u1);
     } else if (warp < kWarpQ) {
-      softmax_role(a, S, tmem, u0, u1, U, C);
+      softmax_role(a, S, tmem, u0, u1);
     } else {
       qprep(a, S, u0, u1);
     }
@@ -592,6 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  merge_phase<__nv_bfloat16, 128>(a, S.plan, S.merge, S.merge_qhead, &S.merge_flag, U, C, tid,
+                                  kThreads, CtaSync(), kWaitLimit);
 }
 
 }  // namespace
@@ -609,8 +573,18 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const C
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  decode_tc_kernel<<<ctas, kThreads, smem, s>>>(a, tk, tv);
-  return cudaGetLastError();
+  // cooperative: the merge phase waits on other CTAs, so all must be resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a, tk, tv);
 }
 
 }  // namespace hw

@@ -14,8 +14,12 @@
 //   segment   = the units of one (block, kv head); a CTA emits one partial
 //   record per (segment it touched, query head served) into slot seg + c,
 //   which is unique because seg and c never both stay put as units advance.
-//   The last CTA to deliver a record for (row, kv head) - found with an
-//   arrival counter, no waiting - merges that row's records.
+//   Every delivered record bumps the arrival counter of its (row, kv head).
+//   The launch is cooperative (all CTAs resident at once): after its own
+//   units, CTA c merges the (row, kv head) pairs c, c + grid, ... - it waits,
+//   with a bound, until the pair's counter shows every record, then combines
+//   them with one warp per query head.  Spreading the merges over the grid
+//   keeps them off any single CTA's critical path.
 //
 // Group-level helpers take (tid, nt) - the thread's index within the group
 // that runs them and the group's size - and a Sync functor that synchronises
@@ -284,108 +288,179 @@ __device__ void write_empty(const DecodeArgs &a, const int32_t *qhead, int r, in
   }
 }
 
-// Merge every record of (row r, kv head h) into out / lse, then re-arm the
-// counter.  The whole group calls it; qhead must hold h's query heads.
-//   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
-//   lse = (M + log2 L) ln 2     (m, l, o of each record in the log2 domain)
-template <typename T, typename Sync>
-__device__ void merge_row(const DecodeArgs &a, const PlanCore &P, MergeScratch &X,
-                          const int32_t *qhead, int r, int h, int64_t U, int C, int tid, int nt,
-                          Sync sync) {
-  const int G = a.n_q_heads / a.n_kv_heads;
-  const int D = a.head_dim;
-  const int V = a.n_view;
-  if (tid < 32) {
-    // per view entry: its block's segment, the CTA range that wrote records,
-    // and its rank among the entries that reference the same block
-    const int lane = tid;
-    for (int v = lane; v < V; v += 32) {
-      const int b = a.view_block[r * V + v];
-      X.mv_seg[v] = -1;
-      X.mv_qi[v] = 0;
-      if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
-        const int64_t s0 = P.ubase[b] + static_cast<int64_t>(h) * P.tiles[b];
-        X.mv_seg[v] = static_cast<int64_t>(b) * a.n_kv_heads + h;
-        X.mv_c0[v] = cta_of_unit(s0, U, C);
-        X.mv_c1[v] = cta_of_unit(s0 + P.tiles[b] - 1, U, C);
-      }
-    }
-    __syncwarp();
-    const int E = r * V + V;
-    for (int base = 0; base < E; base += 32) {
-      const int i = base + lane;
-      const int x = (i < E) ? a.view_block[i] : -2;
-      for (int v = 0; v < V; ++v) {
-        const int e = r * V + v;
-        const int b = a.view_block[e];
-        const unsigned m = __ballot_sync(0xffffffffu, i < e && x == b);
-        if (lane == 0) X.mv_qi[v] += __popc(m);
-      }
-    }
-  }
-  sync();
-  for (int gi = 0; gi < G; ++gi) {
-    // pass 1: M over every record, strided over threads
-    float M = -INFINITY;
-    for (int v = 0; v < V; ++v) {
-      if (X.mv_seg[v] < 0) continue;
-      const int qi = X.mv_qi[v] * G + gi;
-      for (int c = X.mv_c0[v] + tid; c <= X.mv_c1[v]; c += nt)
-        M = fmaxf(M, __ldcg(record_ptr(a, X.mv_seg[v] + c, qi) + D));
-    }
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if ((tid & 31) == 0) X.red[tid >> 5] = M;
-    sync();
-    M = X.red[0];
-    for (int w = 1; w < nt / 32; ++w) M = fmaxf(M, X.red[w]);
-    sync();
-    // pass 2: each thread owns elements d = tid + k * nt
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float L = 0.f;
-    for (int v = 0; v < V; ++v) {
-      if (X.mv_seg[v] < 0) continue;
-      const int qi = X.mv_qi[v] * G + gi;
-      for (int c = X.mv_c0[v]; c <= X.mv_c1[v]; ++c) {
-        const float *rec = record_ptr(a, X.mv_seg[v] + c, qi);
-        const float w = ex2(__ldcg(rec + D) - M);
-        L += w * __ldcg(rec + D + 1);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int d = tid + k * nt;
-          if (d < D) acc[k] += w * __ldcg(rec + d);
-        }
-      }
-    }
-    const int hq = qhead[gi];
-    const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
-    const float inv = 1.f / L;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int d = tid + k * nt;
-      if (d < D) reinterpret_cast<T *>(a.out)[ob * D + d] = from_f32<T>(acc[k] * inv);
-    }
-    if (tid == 0 && a.lse) a.lse[ob] = (M + __log2f(L)) * 0.69314718055994530942f;
-  }
-  if (tid == 0) a.counters[r * a.n_kv_heads + h] = 0;  // re-armed for the next call
-  sync();
+// ---------------------------------------------------------------------------
+// arrivals and the merge phase
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
-// Count one arrival for every row that references block b (kv head h) and
-// append (r * Hkv + h) to `list` for the rows whose last record this was.  One
-// thread calls it, after the group's record stores were fenced and
-// synchronised.  Returns the new list length.
-__device__ __forceinline__ int arrive_rows(const DecodeArgs &a, const PlanCore &P,
-                                           const SegMeta &M, int h, int64_t U, int C,
-                                           int32_t *list, int n_list, int cap) {
+// One arrival on (row, kv head h) for every view entry referencing the
+// segment's block.  One thread calls it, after the group's record stores were
+// fenced (__threadfence by each writer) and synchronised.
+__device__ __forceinline__ void arrive_segment(const DecodeArgs &a, const SegMeta &M, int h) {
   __threadfence();
   for (int j = 0; j < M.n_ref && j < kMaxQ; ++j) {
     const int r = M.ref_entry[j] / a.n_view;
-    const int old = atomicAdd(&a.counters[r * a.n_kv_heads + h], 1);
-    if (old + 1 == expected_records(a, P, r, h, U, C) && n_list < cap)
-      list[n_list++] = r * a.n_kv_heads + h;
+    atomicAdd(&a.counters[r * a.n_kv_heads + h], 1);
   }
-  __threadfence();
-  return n_list;
+}
+
+// (m, l) of two partial softmaxes in the log2 domain, combined.
+__device__ __forceinline__ void lse_combine(float &M, float &L, float m, float l) {
+  if (m == -INFINITY) return;  // nothing to add (and -inf - -inf would be NaN)
+  if (m > M) {
+    L = L * ex2(M - m) + l;  // ex2(-inf) = 0 when M is still -inf
+    M = m;
+  } else {
+    L += l * ex2(m - M);
+  }
+}
+
+// One warp merges every record of (row r, q head gi of kv head h):
+//   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
+//   lse = (M + log2 L) ln 2     (m, l, o of each record in the log2 domain)
+// Lane j owns elements [j * D/32, (j+1) * D/32).
+template <typename T, int D>
+__device__ void merge_head(const DecodeArgs &a, const MergeScratch &X, int r, int gi, int hq,
+                           int lane) {
+  constexpr int EPL = D / 32;
+  const int G = a.n_q_heads / a.n_kv_heads;
+  const int V = a.n_view;
+  float Mx = -INFINITY, Lx = 0.f;
+  for (int v = 0; v < V; ++v) {
+    if (X.mv_seg[v] < 0) continue;
+    const int qi = X.mv_qi[v] * G + gi;
+    for (int c = X.mv_c0[v] + lane; c <= X.mv_c1[v]; c += 32) {
+      const float *rec = record_ptr(a, X.mv_seg[v] + c, qi);
+      lse_combine(Mx, Lx, __ldcg(rec + D), __ldcg(rec + D + 1));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, Mx, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, Lx, o);
+    lse_combine(Mx, Lx, m2, l2);
+  }
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  for (int v = 0; v < V; ++v) {
+    if (X.mv_seg[v] < 0) continue;
+    const int qi = X.mv_qi[v] * G + gi;
+    const int c1 = X.mv_c1[v];
+    for (int base = X.mv_c0[v]; base <= c1; base += 32) {
+      const int c = base + lane;
+      const float wl = (c <= c1) ? ex2(__ldcg(record_ptr(a, X.mv_seg[v] + c, qi) + D) - Mx) : 0.f;
+      const int n = min(32, c1 - base + 1);
+#pragma unroll 8
+      for (int k = 0; k < 32; ++k) {
+        if (k < n) {
+          const float w = __shfl_sync(0xffffffffu, wl, k);
+          const float *o = record_ptr(a, X.mv_seg[v] + base + k, qi) + lane * EPL;
+          if constexpr (EPL == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
+            acc[0] += w * x.x;
+            acc[1] += w * x.y;
+            acc[2] += w * x.z;
+            acc[3] += w * x.w;
+          } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
+            acc[0] += w * x.x;
+            acc[1] += w * x.y;
+          }
+        }
+      }
+    }
+  }
+  const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
+  const float inv = 1.f / Lx;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e)
+    reinterpret_cast<T *>(a.out)[ob * D + lane * EPL + e] = from_f32<T>(acc[e] * inv);
+  if (lane == 0 && a.lse) a.lse[ob] = (Mx + __log2f(Lx)) * 0.69314718055994530942f;
+}
+
+// The merge phase: every thread of the CTA calls it after the CTA's own
+// units.  qhead_s and flag_s are shared scratch.  Pairs without records were
+// written as empty at the start and are skipped here.
+template <typename T, int D, typename Sync>
+__device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch &X,
+                            int32_t *qhead_s, int32_t *flag_s, int64_t U, int C, int tid, int nt,
+                            Sync sync, long long wait_limit) {
+  const int V = a.n_view;
+  const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
+  const int G = a.n_q_heads / a.n_kv_heads;
+  const int items = a.n_rows * a.n_kv_heads;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int r = it / a.n_kv_heads, h = it % a.n_kv_heads;
+    const int expected = expected_records(a, P, r, h, U, C);
+    if (expected == 0) continue;
+    if (tid == 0) {
+      // every record of the pair is delivered (bounded wait: co-resident CTAs)
+      const int32_t *ctr = a.counters + it;
+      bool ok = ld_acquire_gpu(ctr) >= expected;
+      if (!ok) {
+        const long long t0 = clock64();
+        while (!(ok = ld_acquire_gpu(ctr) >= expected)) {
+          if (clock64() - t0 > wait_limit) break;
+          __nanosleep(32);
+        }
+      }
+      if (!ok) flag_error(a.err, HW_DEV_TIMEOUT);
+      *flag_s = ok ? 1 : 0;
+    }
+    if (warp == 0) {
+      // per view entry: its block's segment, the CTA range that wrote records,
+      // and its rank among the entries that reference the same block
+      for (int v = lane; v < V; v += 32) {
+        const int b = a.view_block[r * V + v];
+        X.mv_seg[v] = -1;
+        X.mv_qi[v] = 0;
+        if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
+          const int64_t s0 = P.ubase[b] + static_cast<int64_t>(h) * P.tiles[b];
+          X.mv_seg[v] = static_cast<int64_t>(b) * a.n_kv_heads + h;
+          X.mv_c0[v] = cta_of_unit(s0, U, C);
+          X.mv_c1[v] = cta_of_unit(s0 + P.tiles[b] - 1, U, C);
+        }
+      }
+      __syncwarp();
+      const int E = r * V + V;
+      for (int base = 0; base < E; base += 32) {
+        const int i = base + lane;
+        const int x = (i < E) ? a.view_block[i] : -2;
+        for (int v = 0; v < V; ++v) {
+          const int e = r * V + v;
+          const int b = a.view_block[e];
+          const unsigned m = __ballot_sync(0xffffffffu, i < e && x == b);
+          if (lane == 0) X.mv_qi[v] += __popc(m);
+        }
+      }
+      // the q heads of kv head h
+      if (!a.q_to_kv) {
+        for (int i = lane; i < G; i += 32) qhead_s[i] = h * G + i;
+      } else {
+        int cnt = 0;
+        for (int base = 0; base < a.n_q_heads; base += 32) {
+          const int hq = base + lane;
+          const bool mm = hq < a.n_q_heads && a.q_to_kv[hq] == h;
+          const unsigned mask = __ballot_sync(0xffffffffu, mm);
+          const int pos = cnt + __popc(mask & ((1u << lane) - 1u));
+          if (mm && pos < G) qhead_s[pos] = hq;
+          cnt += __popc(mask);
+        }
+      }
+    }
+    sync();
+    if (*flag_s) {
+      for (int gi = warp; gi < G; gi += nwarps) merge_head<T, D>(a, X, r, gi, qhead_s[gi], lane);
+    }
+    sync();
+    if (tid == 0) a.counters[it] = 0;  // re-armed for the next call
+  }
 }
 
 }  // namespace hw
