@@ -86,7 +86,10 @@ static bool make_pool_map(CUtensorMap *m, const void *pool, int64_t capacity, in
 // Upper bound on the CTAs of any decode launch: slots are sized for it.
 static int max_decode_ctas() {
   const int sms = device_sm_count();
-  return sms > 0 ? sms * 4 : -1;
+  if (sms <= 0) return -1;
+  // a merge gathers at most max_view_blocks + grid - 1 records
+  const int cap = kMaxRecords - HW_MAX_VIEW_BLOCKS;
+  return sms * 4 < cap ? sms * 4 : cap;
 }
 
 WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {

@@ -41,33 +41,45 @@ constexpr uint32_t kStageBytes = 4 * kBox;    // K lo, K hi, V lo, V hi
 constexpr uint32_t kQHalf = kN * 64 * 2;      // [32 heads][64 bf16], 128-B swizzled
 constexpr uint32_t kQPart = 2 * kQHalf;       // one part (hi or lo): d 0-63, d 64-127
 constexpr uint32_t kQBytes = 2 * kQPart;      // hi, lo
-constexpr uint32_t kPBytes = kT * kN * 2;     // [128 tokens][32 heads], 64-B swizzled
+constexpr uint32_t kPBytes = kT * kN * 2;     // [128 tokens][32 heads], 64-B swizzled; it
+                                              // lives in the stage's K region, free once
+                                              // the tile's QK product has completed
 constexpr uint32_t kTmemCols = 128;           // S0 [0,32)  S1 [32,64)  O [64,96)
 constexpr uint32_t kColO = 64;
 constexpr float kLazy = 8.f;                  // rescale only when the max grows by > 2^8
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
+constexpr int kPre = 4;  // segments whose metadata the prologue prepares
+
+// A segment's query-side metadata: view references, q heads, and for each
+// reference its row and relative rotation i_q - offset.
+struct SegPre {
+  SegMeta m;
+  int32_t qrow[kMaxQ];
+  int64_t qrel[kMaxQ];
+};
 
 struct TcSmem {
   alignas(1024) uint8_t stage[kStages][kStageBytes];
   alignas(1024) uint8_t q[kQBytes];
-  alignas(1024) uint8_t p[kPBytes];  // also the plan scratch before the main loop
   PlanCore plan;
   SegMeta meta;        // handed from the query warps to the softmax warps
-  SegMeta qmeta;       // the query warps' working copy
   SegMeta smeta;       // the softmax warps' copy for the segment epilogue
+  SegPre pre[kPre];    // query-side metadata of segments j (j < kPre) or j % kPre
   MergeScratch merge;
   alignas(16) float red[2][kN][4];  // per tile: column maxima of the 4 softmax warps (read as float4)
   alignas(16) float lsum[4][kN];    // per segment: column sums of the 4 softmax warps
   int32_t merge_qhead[kMaxQ];
-  int32_t merge_flag;
+  int32_t merge_flag[2];
+  int32_t merge_list[kMaxRecords];
   int32_t abort_flag;
   uint32_t tmem_base;
   alignas(8) uint64_t k_full[kStages];
   uint64_t v_full[kStages], kv_empty[kStages];
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, p_empty, o_full, o_empty, mma_done;
+  uint64_t p_full[kStages];  // P of the stage's tile written (the softmax may run ahead)
+  uint64_t p_empty, o_full, o_empty, mma_done;
 };
 
 __device__ __forceinline__ void set_abort(TcSmem &S, const DecodeArgs &a) {
@@ -98,6 +110,20 @@ __device__ __forceinline__ int f2ord(float f) {
   return i >= 0 ? i : i ^ 0x7fffffff;
 }
 __device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
+
+// Named barrier 1 over the 128 softmax threads, returning the OR of `pred`.
+__device__ __forceinline__ bool bar_red_or_128(bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return out != 0;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
@@ -148,6 +174,35 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
   while (ip < n) {
     if (aborted(S)) break;
     bool progressed = false;
+    // P.V first: it releases a stage and the O accumulator; QK of a later
+    // tile is not needed until the softmax warps are done with this one
+    if (ip < iq) {
+      const int64_t u = u0 + ip;
+      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+      const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
+      const int kseg = first ? seg_p + 1 : seg_p;
+      const int s = ip % kStages;
+      if (mbar_test(&S.p_full[s], (ip / kStages) & 1) && mbar_test(&S.v_full[s], (ip / kStages) & 1) &&
+          (!first || kseg == 0 || mbar_test(&S.o_empty, (kseg - 1) & 1))) {
+        seg_p = kseg;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(S.stage[s]) + 2 * kBox, pb = smem_u32(S.stage[s]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart,
+          // 8-token groups 1024 B apart.  P^T: MN-major, 32 heads = one 64-B atom,
+          // 8-token groups 512 B apart.
+          const uint64_t ad = smem_desc(vb + kk * 2048, kBox, 1024, kSw128);
+          const uint64_t bd = smem_desc(pb + kk * 1024, 512, 512, kSw64);
+          mma_bf16(tmem + kColO, ad, bd, idesc_pv, !(first && kk == 0));
+        }
+        mma_commit(&S.kv_empty[s]);
+        mma_commit(&S.p_empty);
+        if (last) mma_commit(&S.o_full);
+        ++ip;
+        progressed = true;
+      }
+    }
     if (iq < n && iq < ip + 2) {
       const int64_t u = u0 + iq;
       const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
@@ -174,33 +229,6 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
         progressed = true;
       }
     }
-    if (ip < iq) {
-      const int64_t u = u0 + ip;
-      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-      const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
-      const int kseg = first ? seg_p + 1 : seg_p;
-      const int s = ip % kStages;
-      if (mbar_test(&S.p_full, ip & 1) && mbar_test(&S.v_full[s], (ip / kStages) & 1) &&
-          (!first || kseg == 0 || mbar_test(&S.o_empty, (kseg - 1) & 1))) {
-        seg_p = kseg;
-        tc_fence_after();
-        const uint32_t vb = smem_u32(S.stage[s]) + 2 * kBox, pb = smem_u32(S.p);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart,
-          // 8-token groups 1024 B apart.  P^T: MN-major, 32 heads = one 64-B atom,
-          // 8-token groups 512 B apart.
-          const uint64_t ad = smem_desc(vb + kk * 2048, kBox, 1024, kSw128);
-          const uint64_t bd = smem_desc(pb + kk * 1024, 512, 512, kSw64);
-          mma_bf16(tmem + kColO, ad, bd, idesc_pv, !(first && kk == 0));
-        }
-        mma_commit(&S.kv_empty[s]);
-        mma_commit(&S.p_empty);
-        if (last) mma_commit(&S.o_full);
-        ++ip;
-        progressed = true;
-      }
-    }
     if (progressed) {
       last_progress = clock64();
     } else if (clock64() - last_progress > kWaitLimit) {
@@ -212,79 +240,154 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
   mbar_wait(&S.mma_done, 0);
 }
 
-// Rotated queries, one segment at a time: q~ = rho(q, i_q - offset) * scale *
-// log2(e) for every (view reference, q head) pair of the segment.  The values
-// of segment j are computed in registers while the tensor cores still work on
-// segment j - 1; they are written once the single Q~ buffer is released.
+// Query-side metadata of segment (b, h) into X, by one warp.
+__device__ void seg_pre(const DecodeArgs &a, SegPre &X, int b, int h, int lane) {
+  gather_refs(a, X.m, b, lane);
+  gather_qheads(a, X.m, h, lane);
+  __syncwarp();
+  for (int j = lane; j < X.m.n_ref && j < kMaxQ; j += 32) {
+    const int e = X.m.ref_entry[j];
+    const int r = e / a.n_view;
+    X.qrow[j] = r;
+    X.qrel[j] = static_cast<int64_t>(a.q_pos[r]) - a.view_offset[e];
+  }
+  __syncwarp();
+}
+
+// Rotated query element i (and i + 64) of head qi of a segment, scaled by
+// scale * log2(e) so that scores leave the MMA in log2 units.
+__device__ __forceinline__ float2 rot_pair(const DecodeArgs &a, uint32_t xq, float cs, float sn) {
+  const float x0 = __uint_as_float(xq << 16), x1 = __uint_as_float(xq & 0xffff0000u);
+  return make_float2((x0 * cs - x1 * sn) * a.scale_log2, (x1 * cs + x0 * sn) * a.scale_log2);
+}
+
+// Store element i (hv = 0) or i + 64 (hv = 1) of head qi as bf16 hi and lo
+// into the Q~ buffer: half d / 64, row qi (128 B), 16-B chunk swizzled by qi % 8.
+__device__ __forceinline__ void store_q(uint32_t qbase, int qi, int i, int hv, float v) {
+  const uint32_t chunk = static_cast<uint32_t>(i >> 3), e2 = static_cast<uint32_t>(i & 7) * 2;
+  const uint32_t o = qbase + hv * kQHalf + qi * 128 + ((chunk ^ (qi & 7)) << 4) + e2;
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(o), "h"(__bfloat16_as_ushort(hi)) : "memory");
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(o + kQPart), "h"(__bfloat16_as_ushort(lo)) : "memory");
+}
+
+__device__ __forceinline__ const __nv_bfloat16 *q_row(const DecodeArgs &a, const SegPre &X, int qi,
+                                                      int G) {
+  return reinterpret_cast<const __nv_bfloat16 *>(a.q) +
+         (static_cast<int64_t>(X.qrow[qi / G]) * a.n_q_heads + X.m.qhead[qi % G]) * 128;
+}
+
+// Prologue, all threads, before any K/V copy is issued (so that these small
+// loads do not queue behind the tile stream): the metadata of the CTA's first
+// kPre segments (one warp each) and the rotated queries of segment 0.
+__device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.n_q_heads / a.n_kv_heads;
+  if (warp < kPre) {
+    int64_t u = u0;
+    for (int k = 0; k < warp && u < u1; ++k) {
+      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+      u = x.seg_first + x.tiles;
+    }
+    if (u < u1) {
+      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+      seg_pre(a, S.pre[warp], x.b, x.h, lane);
+    }
+  }
+  __syncthreads();
+  const SegPre &X = S.pre[0];
+  const int nq = min(X.m.n_ref * G, kN);
+  const uint32_t qbase = smem_u32(S.q);
+  for (int idx = tid; idx < kN * 64; idx += kThreads) {
+    const int qi = idx >> 6, i = idx & 63;
+    float2 y = make_float2(0.f, 0.f);
+    if (qi < nq) {
+      const __nv_bfloat16 *qp = q_row(a, X, qi, G);
+      const uint32_t xq = static_cast<uint32_t>(__bfloat16_as_ushort(qp[i])) |
+                          (static_cast<uint32_t>(__bfloat16_as_ushort(qp[i + 64])) << 16);
+      float cs, sn;
+      rope_cos_sin(X.qrel[qi / G], a.phase[i], &cs, &sn);
+      y = rot_pair(a, xq, cs, sn);
+    }
+    store_q(qbase, qi, i, 0, y.x);
+    store_q(qbase, qi, i, 1, y.y);
+  }
+  for (int j = tid; j < kMaxQ; j += kThreads) {
+    S.meta.ref_entry[j] = X.m.ref_entry[j];
+    S.meta.qhead[j] = X.m.qhead[j];
+  }
+  if (tid == 0) S.meta.n_ref = X.m.n_ref;
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) mbar_arrive(&S.q_full);  // phase 0: segment 0
+}
+
+// Rotated queries of segments 1, 2, ... (segment 0 came from the prologue).
+// The values of segment j are loaded and computed in registers while the
+// tensor cores still work on segment j - 1; they are written once the single
+// Q~ buffer is released.
 __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
   const int lane = threadIdx.x & 31;
   const int G = a.n_q_heads / a.n_kv_heads;
   NamedSync<2, 64> sync;
   const uint32_t qbase = smem_u32(S.q);
-  int seg = -1;
-  for (int64_t u = u0; u < u1;) {
+  int64_t u = u0;
+  {
     const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-    ++seg;
-    SegMeta &M = S.qmeta;
-    if (tq < 32) {
-      gather_refs(a, M, x.b, lane);
-      gather_qheads(a, M, x.h, lane);
+    u = x.seg_first + x.tiles;  // segment 0 is done
+  }
+  for (int seg = 1; u < u1; ++seg) {
+    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    SegPre &X = S.pre[seg % kPre];
+    if (seg >= kPre) {
+      if (tq < 32) seg_pre(a, X, x.b, x.h, lane);
+      sync();
     }
-    sync();
-    const int nq = min(M.n_ref * G, kN);
-    // pair k of this thread: idx = tq + 64 k -> head qi = idx / 64, element i = idx % 64
-    float y[2 * kN];
+    const int nq = min(X.m.n_ref * G, kN);
+    // this thread owns element i = tq (and tq + 64) of every query head qi:
+    // all 2 x 32 loads go out first (64 consecutive bf16 per head across the
+    // two warps: coalesced), then the rotation
+    uint32_t xq[kN];
 #pragma unroll
     for (int k = 0; k < kN; ++k) {
-      const int idx = tq + 64 * k;
-      const int qi = idx >> 6, i = idx & 63;
-      float y0 = 0.f, y1 = 0.f;
-      if (qi < nq) {
-        const int e = M.ref_entry[qi / G];
-        const int r = e / a.n_view;
-        const int hq = M.qhead[qi % G];
-        const int64_t rel = static_cast<int64_t>(a.q_pos[r]) - a.view_offset[e];
-        const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
-                                  (static_cast<int64_t>(r) * a.n_q_heads + hq) * 128;
-        const float x0 = __bfloat162float(qp[i]), x1 = __bfloat162float(qp[i + 64]);
-        float cs, sn;
-        rope_cos_sin(rel, a.phase[i], &cs, &sn);
-        // scores leave the MMA already in log2 units: scale * log2(e) folded in
-        y0 = (x0 * cs - x1 * sn) * a.scale_log2;
-        y1 = (x1 * cs + x0 * sn) * a.scale_log2;
+      xq[k] = 0;
+      if (k < nq) {
+        const __nv_bfloat16 *qp = q_row(a, X, k, G);
+        xq[k] = static_cast<uint32_t>(__bfloat16_as_ushort(qp[tq])) |
+                (static_cast<uint32_t>(__bfloat16_as_ushort(qp[tq + 64])) << 16);
       }
-      y[2 * k] = y0;
-      y[2 * k + 1] = y1;
+    }
+    float y[2 * kN];
+    float cs = 1.f, sn = 0.f;
+#pragma unroll
+    for (int k = 0; k < kN; ++k) {
+      float2 v = make_float2(0.f, 0.f);
+      if (k < nq) {
+        // cos/sin depend on the reference (k / G) and the pair (tq) only
+        if (k % G == 0) rope_cos_sin(X.qrel[k / G], a.phase[tq], &cs, &sn);
+        v = rot_pair(a, xq[k], cs, sn);
+      }
+      y[2 * k] = v.x;
+      y[2 * k + 1] = v.y;
     }
     // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
     // warps keep the same control flow so the named barrier stays balanced.
     // The Q~ buffer and the hand-off metadata are free once segment seg-1's QK
     // products completed and the softmax warps took their copy.
-    if (seg > 0) wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
+    wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
     if (tq < 32) {
       for (int j = lane; j < kMaxQ; j += 32) {
-        S.meta.ref_entry[j] = M.ref_entry[j];
-        S.meta.qhead[j] = M.qhead[j];
+        S.meta.ref_entry[j] = X.m.ref_entry[j];
+        S.meta.qhead[j] = X.m.qhead[j];
       }
-      if (lane == 0) S.meta.n_ref = M.n_ref;
+      if (lane == 0) S.meta.n_ref = X.m.n_ref;
     }
 #pragma unroll
     for (int k = 0; k < kN; ++k) {
-      const int idx = tq + 64 * k;
-      const int qi = idx >> 6, i = idx & 63;
-      // element d of head qi: half d / 64, row qi (128 B), 16-B chunk swizzled by qi % 8
-      const uint32_t chunk = static_cast<uint32_t>(i >> 3), e2 = static_cast<uint32_t>(i & 7) * 2;
-      const uint32_t off = qi * 128 + ((chunk ^ (qi & 7)) << 4) + e2;
-#pragma unroll
-      for (int hv = 0; hv < 2; ++hv) {  // element i, then i + 64
-        const float v = y[2 * k + hv];
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-        const uint32_t o = qbase + hv * kQHalf + off;
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(o), "h"(__bfloat16_as_ushort(hi)) : "memory");
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(o + kQPart), "h"(__bfloat16_as_ushort(lo)) : "memory");
-      }
+      store_q(qbase, k, tq, 0, y[2 * k]);
+      store_q(qbase, k, tq, 1, y[2 * k + 1]);
     }
     fence_proxy_async_smem();
     sync();
@@ -304,7 +407,6 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   const int G = a.n_q_heads / a.n_kv_heads;
   const int n = static_cast<int>(u1 - u0);
   NamedSync<1, 128> sync;
-  const uint32_t pb = smem_u32(S.p);
 
   // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: every
   // thread of the group keeps the same control flow, so the named barriers
@@ -349,47 +451,41 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
 #pragma unroll
     for (int j = 0; j < kN; ++j) sc[j] = tok_ok ? __uint_as_float(r[j]) : -INFINITY;
 
-    // column maxima over the tile's 128 tokens
-    float(*red)[4] = S.red[i & 1];
+    // Lazy rescaling: the reference max m_run moves only when some score
+    // exceeds it by more than kLazy (log2 units), so p <= 2^kLazy and O is
+    // rarely touched.  The common case needs only this one CTA-group vote;
+    // exact column maxima are taken on the rare tiles that need them (the
+    // first tile of a segment always does: m_run starts at -inf).
+    bool exceed = false;
 #pragma unroll
-    for (int j = 0; j < kN; ++j) {
-      if (j < nq) {
-        const int mk = __reduce_max_sync(0xffffffffu, f2ord(sc[j]));
-        if (lane == j) red[j][ws] = ord2f(mk);
+    for (int j = 0; j < kN; ++j) exceed |= (j < nq) && (sc[j] > m_run[j] + kLazy);
+    if (bar_red_or_128(exceed)) {
+      float(*red)[4] = S.red[i & 1];
+#pragma unroll
+      for (int j = 0; j < kN; ++j) {
+        if (j < nq) {
+          const int mk = __reduce_max_sync(0xffffffffu, f2ord(sc[j]));
+          if (lane == j) red[j][ws] = ord2f(mk);
+        }
       }
-    }
-    sync();
-    float tmax[kN];
-#pragma unroll
-    for (int j = 0; j < kN; ++j) {
-      if (j < nq) {
-        const float4 v = *reinterpret_cast<const float4 *>(red[j]);
-        tmax[j] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-      } else {
-        tmax[j] = -INFINITY;
-      }
-    }
-    // lazy rescaling: the reference max moves only when a column's max grows
-    // by more than 2^kLazy, so p <= 2^kLazy and O is rarely touched
-    bool need = false;
-#pragma unroll
-    for (int j = 0; j < kN; ++j) need |= (j < nq) && (tmax[j] > m_run[j] + kLazy);
-    bool waited_p = false;
-    if (need) {
+      sync();
       float alpha[kN];
 #pragma unroll
       for (int j = 0; j < kN; ++j) {
         alpha[j] = 1.f;
-        if (j < nq && tmax[j] > m_run[j] + kLazy) {
-          alpha[j] = ex2(m_run[j] - tmax[j]);  // 0 when m_run = -inf
-          m_run[j] = tmax[j];
+        if (j < nq) {
+          const float4 v = *reinterpret_cast<const float4 *>(red[j]);
+          const float tmax = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+          if (tmax > m_run[j] + kLazy) {
+            alpha[j] = ex2(m_run[j] - tmax);  // 0 when m_run = -inf
+            m_run[j] = tmax;
+          }
         }
         l_part[j] *= alpha[j];
       }
       if (!first) {
         // O must hold every earlier tile before it is rescaled
         wait_or_abort(S, a, &S.p_empty, (i - 1) & 1);
-        waited_p = true;
         tc_fence_after();
         __syncwarp();
         uint32_t o[32];
@@ -412,8 +508,6 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       l_part[j] += __uint_as_float(pk[j / 2] << 16);
       l_part[j + 1] += __uint_as_float(pk[j / 2] & 0xffff0000u);
     }
-    // the single P buffer is free once PV of the previous tile has completed
-    if (i > 0 && !waited_p) wait_or_abort(S, a, &S.p_empty, (i - 1) & 1);
     if (valid < kT) {
       // V rows past the block end may hold anything: zero them (p = 0 there,
       // but 0 * NaN would still poison the sum)
@@ -427,15 +521,16 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
         }
       }
     }
-    // P row of this token: 32 heads = four 16-B chunks, 64-B swizzle
-    const uint32_t prow = pb + row * 64;
+    // P row of this token: 32 heads = four 16-B chunks, 64-B swizzle, in the
+    // K region of the tile's stage (QK of this tile has completed: s_full)
+    const uint32_t prow = smem_u32(S.stage[s]) + row * 64;
     const uint32_t swz = (row >> 1) & 3;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       st_shared_v4(prow + ((c ^ swz) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.p_full);
+    if (lane == 0) mbar_arrive(&S.p_full[s]);
 
     if (last) {
       // ---- segment epilogue: O -> records, arrivals
@@ -494,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.p_full[s], 4);  // one per softmax warp
       mbar_init(&S.k_full[s], 1);
       mbar_init(&S.v_full[s], 1);
       mbar_init(&S.kv_empty[s], 1);
@@ -504,7 +600,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.s_full[b], 1);
       mbar_init(&S.s_empty[b], 4);  // one per softmax warp
     }
-    mbar_init(&S.p_full, 4);
     mbar_init(&S.p_empty, 1);
     mbar_init(&S.o_full, 1);
     mbar_init(&S.o_empty, 4);
@@ -516,7 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&S.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  build_plan<kT>(a, S.plan, *reinterpret_cast<PlanScratch *>(S.p));
+  // the plan scratch borrows stage 0, which no copy has touched yet
+  build_plan<kT>(a, S.plan, *reinterpret_cast<PlanScratch *>(S.stage[0]));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -538,6 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (U > 0 && c < C) {
     const int64_t u0 = cta_unit_begin(U, c, C), u1 = cta_unit_begin(U, c + 1, C);
+    query_prologue(a, S, u0, u1);
     if (warp == kWarpTma) {
       if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1);
     } else if (warp == kWarpMma) {
@@ -554,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  merge_phase<__nv_bfloat16, 128>(a, S.plan, S.merge, S.merge_qhead, &S.merge_flag, U, C, tid,
-                                  kThreads, CtaSync(), kWaitLimit);
+  merge_phase<__nv_bfloat16, 128>(a, S.plan, S.merge, S.merge_qhead, S.merge_flag, S.merge_list,
+                                  U, C, tid, kThreads, CtaSync(), kWaitLimit);
 }
 
 }  // namespace

@@ -320,24 +320,21 @@ __device__ __forceinline__ void lse_combine(float &M, float &L, float m, float l
   }
 }
 
-// One warp merges every record of (row r, q head gi of kv head h):
+// One warp merges every record of (row r, q head gi) - the records listed in
+// `list` (record index without the head: slot * 32 + rank * G):
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
 //   lse = (M + log2 L) ln 2     (m, l, o of each record in the log2 domain)
-// Lane j owns elements [j * D/32, (j+1) * D/32).
+// Lane j owns elements [j * D/32, (j+1) * D/32).  All loads of a pass are
+// independent of each other, so they overlap instead of queueing.
 template <typename T, int D>
-__device__ void merge_head(const DecodeArgs &a, const MergeScratch &X, int r, int gi, int hq,
-                           int lane) {
+__device__ void merge_head(const DecodeArgs &a, const int32_t *list, int n_rec, int r, int gi,
+                           int hq, int lane) {
   constexpr int EPL = D / 32;
-  const int G = a.n_q_heads / a.n_kv_heads;
-  const int V = a.n_view;
+  constexpr int64_t RS = D + 4;  // record stride in floats
   float Mx = -INFINITY, Lx = 0.f;
-  for (int v = 0; v < V; ++v) {
-    if (X.mv_seg[v] < 0) continue;
-    const int qi = X.mv_qi[v] * G + gi;
-    for (int c = X.mv_c0[v] + lane; c <= X.mv_c1[v]; c += 32) {
-      const float *rec = record_ptr(a, X.mv_seg[v] + c, qi);
-      lse_combine(Mx, Lx, __ldcg(rec + D), __ldcg(rec + D + 1));
-    }
+  for (int k = lane; k < n_rec; k += 32) {
+    const float *rec = a.partials + static_cast<int64_t>(list[k] + gi) * RS;
+    lse_combine(Mx, Lx, __ldcg(rec + D), __ldcg(rec + D + 1));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -348,30 +345,26 @@ __device__ void merge_head(const DecodeArgs &a, const MergeScratch &X, int r, in
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  for (int v = 0; v < V; ++v) {
-    if (X.mv_seg[v] < 0) continue;
-    const int qi = X.mv_qi[v] * G + gi;
-    const int c1 = X.mv_c1[v];
-    for (int base = X.mv_c0[v]; base <= c1; base += 32) {
-      const int c = base + lane;
-      const float wl = (c <= c1) ? ex2(__ldcg(record_ptr(a, X.mv_seg[v] + c, qi) + D) - Mx) : 0.f;
-      const int n = min(32, c1 - base + 1);
-#pragma unroll 8
-      for (int k = 0; k < 32; ++k) {
-        if (k < n) {
-          const float w = __shfl_sync(0xffffffffu, wl, k);
-          const float *o = record_ptr(a, X.mv_seg[v] + base + k, qi) + lane * EPL;
-          if constexpr (EPL == 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
-            acc[0] += w * x.x;
-            acc[1] += w * x.y;
-            acc[2] += w * x.z;
-            acc[3] += w * x.w;
-          } else {
-            const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
-            acc[0] += w * x.x;
-            acc[1] += w * x.y;
-          }
+  for (int base = 0; base < n_rec; base += 32) {
+    const int k = base + lane;
+    const float wl =
+        (k < n_rec) ? ex2(__ldcg(a.partials + static_cast<int64_t>(list[k] + gi) * RS + D) - Mx) : 0.f;
+    const int n = min(32, n_rec - base);
+#pragma unroll 16
+    for (int kk = 0; kk < 32; ++kk) {
+      if (kk < n) {
+        const float w = __shfl_sync(0xffffffffu, wl, kk);
+        const float *o = a.partials + static_cast<int64_t>(list[base + kk] + gi) * RS + lane * EPL;
+        if constexpr (EPL == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
+          acc[0] += w * x.x;
+          acc[1] += w * x.y;
+          acc[2] += w * x.z;
+          acc[3] += w * x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
+          acc[0] += w * x.x;
+          acc[1] += w * x.y;
         }
       }
     }
@@ -385,12 +378,13 @@ __device__ void merge_head(const DecodeArgs &a, const MergeScratch &X, int r, in
 }
 
 // The merge phase: every thread of the CTA calls it after the CTA's own
-// units.  qhead_s and flag_s are shared scratch.  Pairs without records were
-// written as empty at the start and are skipped here.
+// units.  qhead_s, flag_s (2 ints) and list (kMaxRecords ints) are shared
+// scratch.  Pairs without records were written as empty at the start and are
+// skipped here.
 template <typename T, int D, typename Sync>
 __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch &X,
-                            int32_t *qhead_s, int32_t *flag_s, int64_t U, int C, int tid, int nt,
-                            Sync sync, long long wait_limit) {
+                            int32_t *qhead_s, int32_t *flag_s, int32_t *list, int64_t U, int C,
+                            int tid, int nt, Sync sync, long long wait_limit) {
   const int V = a.n_view;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
   const int G = a.n_q_heads / a.n_kv_heads;
@@ -399,20 +393,6 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch
     const int r = it / a.n_kv_heads, h = it % a.n_kv_heads;
     const int expected = expected_records(a, P, r, h, U, C);
     if (expected == 0) continue;
-    if (tid == 0) {
-      // every record of the pair is delivered (bounded wait: co-resident CTAs)
-      const int32_t *ctr = a.counters + it;
-      bool ok = ld_acquire_gpu(ctr) >= expected;
-      if (!ok) {
-        const long long t0 = clock64();
-        while (!(ok = ld_acquire_gpu(ctr) >= expected)) {
-          if (clock64() - t0 > wait_limit) break;
-          __nanosleep(32);
-        }
-      }
-      if (!ok) flag_error(a.err, HW_DEV_TIMEOUT);
-      *flag_s = ok ? 1 : 0;
-    }
     if (warp == 0) {
       // per view entry: its block's segment, the CTA range that wrote records,
       // and its rank among the entries that reference the same block
@@ -434,10 +414,30 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch
         const int x = (i < E) ? a.view_block[i] : -2;
         for (int v = 0; v < V; ++v) {
           const int e = r * V + v;
-          const int b = a.view_block[e];
-          const unsigned m = __ballot_sync(0xffffffffu, i < e && x == b);
+          const int b = __shfl_sync(0xffffffffu, x, (e - base) & 31);  // valid when e in chunk
+          const int bb = (e >= base && e < base + 32) ? b : a.view_block[e];
+          const unsigned m = __ballot_sync(0xffffffffu, i < e && x == bb);
           if (lane == 0) X.mv_qi[v] += __popc(m);
         }
+      }
+      __syncwarp();
+      // the flat record list: (view entry, CTA) pairs in view order
+      int off = 0;
+      for (int v = 0; v < V; ++v) {
+        if (X.mv_seg[v] < 0) continue;
+        const int c0 = X.mv_c0[v], cnt = X.mv_c1[v] - c0 + 1;
+        const int base_rec = X.mv_qi[v] * G;
+        for (int j = lane; j < cnt; j += 32)
+          if (off + j < kMaxRecords)
+            list[off + j] = static_cast<int32_t>((X.mv_seg[v] + c0 + j) * kMaxQ + base_rec);
+        off += cnt;
+      }
+      if (lane == 0) {
+        if (off > kMaxRecords) {
+          flag_error(a.err, HW_DEV_TOO_MANY_REFS);
+          off = kMaxRecords;
+        }
+        flag_s[1] = off;
       }
       // the q heads of kv head h
       if (!a.q_to_kv) {
@@ -455,8 +455,25 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch
       }
     }
     sync();
-    if (*flag_s) {
-      for (int gi = warp; gi < G; gi += nwarps) merge_head<T, D>(a, X, r, gi, qhead_s[gi], lane);
+    // the setup above only needs metadata; now wait for the records
+    if (tid == 0) {
+      // every record of the pair is delivered (bounded wait: co-resident CTAs)
+      const int32_t *ctr = a.counters + it;
+      bool ok = ld_acquire_gpu(ctr) >= expected;
+      if (!ok) {
+        const long long t0 = clock64();
+        while (!(ok = ld_acquire_gpu(ctr) >= expected)) {
+          if (clock64() - t0 > wait_limit) break;
+          __nanosleep(32);
+        }
+      }
+      if (!ok) flag_error(a.err, HW_DEV_TIMEOUT);
+      flag_s[0] = ok ? 1 : 0;
+    }
+    sync();
+    if (flag_s[0]) {
+      const int n_rec = flag_s[1];
+      for (int gi = warp; gi < G; gi += nwarps) merge_head<T, D>(a, list, n_rec, r, gi, qhead_s[gi], lane);
     }
     sync();
     if (tid == 0) a.counters[it] = 0;  // re-armed for the next call

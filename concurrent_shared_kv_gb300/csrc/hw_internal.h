@@ -15,6 +15,9 @@ constexpr int kSimtTile = 64;
 constexpr int kTcTile = 128;
 // Query heads one tile serves at most (view references to a block x group).
 constexpr int kMaxQ = HW_MAX_QHEADS_PER_BLOCK;
+// Partial records one (row, kv head) merge can gather: at most one per (view
+// entry, CTA) pair whose ranges meet, i.e. <= max_view_blocks + grid - 1.
+constexpr int kMaxRecords = 1024;
 
 // Everything a decode kernel needs; passed by value as a kernel parameter.
 struct DecodeArgs {
