@@ -198,6 +198,7 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
   if (d->dtype == HW_BF16 && d->head_dim == 128) {
     // tensor-core path: one persistent CTA per SM, K/V tiles by TMA
     const bool have_pool = d->n_blocks > 0 && d->cache_capacity > 0;
+    if (reinterpret_cast<uintptr_t>(q) & 15u) return HW_ERR_INVALID;  // 16-byte query loads
     if (have_pool && ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u))
       return HW_ERR_INVALID;
     CUtensorMap km, vm;

@@ -44,8 +44,8 @@ constexpr uint32_t kQBytes = 2 * kQPart;      // hi, lo
 constexpr uint32_t kPBytes = kT * kN * 2;     // [128 tokens][32 heads], 64-B swizzled; it
                                               // lives in the stage's K region, free once
                                               // the tile's QK product has completed
-constexpr uint32_t kTmemCols = 128;           // S0 [0,32)  S1 [32,64)  O [64,96)
-constexpr uint32_t kColO = 64;
+constexpr uint32_t kTmemCols = 128;           // S0 [0,32)  S1 [32,64)  O0 [64,96)  O1 [96,128)
+constexpr uint32_t kColO = 64;                // segment k accumulates in O[k & 1]
 constexpr float kLazy = 8.f;                  // rescale only when the max grows by > 2^8
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
@@ -79,7 +79,8 @@ struct TcSmem {
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[kStages];  // P of the stage's tile written (the softmax may run ahead)
-  uint64_t p_empty, o_full, o_empty, mma_done;
+  uint64_t p_empty, mma_done;
+  uint64_t o_full[2], o_empty[2];  // per O buffer: segment done / epilogue read it
 };
 
 __device__ __forceinline__ void set_abort(TcSmem &S, const DecodeArgs &a) {
@@ -183,7 +184,7 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
       const int kseg = first ? seg_p + 1 : seg_p;
       const int s = ip % kStages;
       if (mbar_test(&S.p_full[s], (ip / kStages) & 1) && mbar_test(&S.v_full[s], (ip / kStages) & 1) &&
-          (!first || kseg == 0 || mbar_test(&S.o_empty, (kseg - 1) & 1))) {
+          (!first || mbar_test(&S.o_empty[kseg & 1], ((kseg >> 1) & 1) ^ 1))) {
         seg_p = kseg;
         tc_fence_after();
         const uint32_t vb = smem_u32(S.stage[s]) + 2 * kBox, pb = smem_u32(S.stage[s]);
@@ -194,11 +195,11 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
           // 8-token groups 512 B apart.
           const uint64_t ad = smem_desc(vb + kk * 2048, kBox, 1024, kSw128);
           const uint64_t bd = smem_desc(pb + kk * 1024, 512, 512, kSw64);
-          mma_bf16(tmem + kColO, ad, bd, idesc_pv, !(first && kk == 0));
+          mma_bf16(tmem + kColO + (kseg & 1) * kN, ad, bd, idesc_pv, !(first && kk == 0));
         }
         mma_commit(&S.kv_empty[s]);
         mma_commit(&S.p_empty);
-        if (last) mma_commit(&S.o_full);
+        if (last) mma_commit(&S.o_full[kseg & 1]);
         ++ip;
         progressed = true;
       }
@@ -254,73 +255,98 @@ __device__ void seg_pre(const DecodeArgs &a, SegPre &X, int b, int h, int lane) 
   __syncwarp();
 }
 
-// Rotated query element i (and i + 64) of head qi of a segment, scaled by
-// scale * log2(e) so that scores leave the MMA in log2 units.
-__device__ __forceinline__ float2 rot_pair(const DecodeArgs &a, uint32_t xq, float cs, float sn) {
-  const float x0 = __uint_as_float(xq << 16), x1 = __uint_as_float(xq & 0xffff0000u);
-  return make_float2((x0 * cs - x1 * sn) * a.scale_log2, (x1 * cs + x0 * sn) * a.scale_log2);
+// One item of the rotated queries: head qi, elements 8c..8c+7 and their
+// RoPE partners 64+8c..64+8c+7, rotated by the reference's i_q - offset and
+// scaled by scale * log2(e) (scores leave the MMA in log2 units), then split
+// into bf16 hi and lo parts.  out[0..3]: hi of d 8c.., hi of d 64+8c.., lo of
+// d 8c.., lo of d 64+8c.. (16 bytes each).
+__device__ __forceinline__ void rot_item(const DecodeArgs &a, const SegPre &X, int qi, int c,
+                                         int nq, int G, uint4 (&out)[4]) {
+  uint32_t w[4][4];
+  if (qi < nq) {
+    const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
+                              (static_cast<int64_t>(X.qrow[qi / G]) * a.n_q_heads + X.m.qhead[qi % G]) * 128;
+    const uint4 xl = __ldg(reinterpret_cast<const uint4 *>(qp + 8 * c));
+    const uint4 xh = __ldg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * c));
+    const uint32_t lo32[4] = {xl.x, xl.y, xl.z, xl.w}, hi32[4] = {xh.x, xh.y, xh.z, xh.w};
+    const int64_t rel = X.qrel[qi / G];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      float ylo[2], yhi[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const float x0 = __uint_as_float(h2 ? (lo32[e2] & 0xffff0000u) : (lo32[e2] << 16));
+        const float x1 = __uint_as_float(h2 ? (hi32[e2] & 0xffff0000u) : (hi32[e2] << 16));
+        float cs, sn;
+        rope_cos_sin(rel, a.phase[8 * c + 2 * e2 + h2], &cs, &sn);
+        ylo[h2] = (x0 * cs - x1 * sn) * a.scale_log2;
+        yhi[h2] = (x1 * cs + x0 * sn) * a.scale_log2;
+      }
+      const __nv_bfloat162 hl = __floats2bfloat162_rn(ylo[0], ylo[1]);
+      const __nv_bfloat162 hh = __floats2bfloat162_rn(yhi[0], yhi[1]);
+      const __nv_bfloat162 ll = __floats2bfloat162_rn(ylo[0] - __low2float(hl), ylo[1] - __high2float(hl));
+      const __nv_bfloat162 lh = __floats2bfloat162_rn(yhi[0] - __low2float(hh), yhi[1] - __high2float(hh));
+      w[0][e2] = *reinterpret_cast<const uint32_t *>(&hl);
+      w[1][e2] = *reinterpret_cast<const uint32_t *>(&hh);
+      w[2][e2] = *reinterpret_cast<const uint32_t *>(&ll);
+      w[3][e2] = *reinterpret_cast<const uint32_t *>(&lh);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) w[k][e2] = 0;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) out[k] = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
 }
 
-// Store element i (hv = 0) or i + 64 (hv = 1) of head qi as bf16 hi and lo
-// into the Q~ buffer: half d / 64, row qi (128 B), 16-B chunk swizzled by qi % 8.
-__device__ __forceinline__ void store_q(uint32_t qbase, int qi, int i, int hv, float v) {
-  const uint32_t chunk = static_cast<uint32_t>(i >> 3), e2 = static_cast<uint32_t>(i & 7) * 2;
-  const uint32_t o = qbase + hv * kQHalf + qi * 128 + ((chunk ^ (qi & 7)) << 4) + e2;
-  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-  asm volatile("st.shared.b16 [%0], %1;" ::"r"(o), "h"(__bfloat16_as_ushort(hi)) : "memory");
-  asm volatile("st.shared.b16 [%0], %1;" ::"r"(o + kQPart), "h"(__bfloat16_as_ushort(lo)) : "memory");
+// Store one item into the Q~ buffer: row qi (128 B per half), 16-B chunk c
+// swizzled by qi % 8 (the 128-byte swizzle the MMA descriptor expects).
+__device__ __forceinline__ void store_item(uint32_t qbase, int qi, int c, const uint4 (&v)[4]) {
+  const uint32_t off = qi * 128 + ((static_cast<uint32_t>(c) ^ (qi & 7)) << 4);
+  st_shared_v4(qbase + off, v[0].x, v[0].y, v[0].z, v[0].w);
+  st_shared_v4(qbase + kQHalf + off, v[1].x, v[1].y, v[1].z, v[1].w);
+  st_shared_v4(qbase + kQPart + off, v[2].x, v[2].y, v[2].z, v[2].w);
+  st_shared_v4(qbase + kQPart + kQHalf + off, v[3].x, v[3].y, v[3].z, v[3].w);
 }
 
-__device__ __forceinline__ const __nv_bfloat16 *q_row(const DecodeArgs &a, const SegPre &X, int qi,
-                                                      int G) {
-  return reinterpret_cast<const __nv_bfloat16 *>(a.q) +
-         (static_cast<int64_t>(X.qrow[qi / G]) * a.n_q_heads + X.m.qhead[qi % G]) * 128;
-}
-
-// Prologue, all threads, before any K/V copy is issued (so that these small
-// loads do not queue behind the tile stream): the metadata of the CTA's first
-// kPre segments (one warp each) and the rotated queries of segment 0.
+// Prologue of warps 2-7 (the TMA and MMA warps start at once): the metadata
+// of the CTA's first kPre segments (one warp each) and the rotated queries of
+// segment 0.
 __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = threadIdx.x - kWarpSoft * 32;  // 0..191
+  const int w = t >> 5, lane = t & 31;
   const int G = a.n_q_heads / a.n_kv_heads;
-  if (warp < kPre) {
+  NamedSync<3, 192> sync;
+  if (w < kPre) {
     int64_t u = u0;
-    for (int k = 0; k < warp && u < u1; ++k) {
+    for (int k = 0; k < w && u < u1; ++k) {
       const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
       u = x.seg_first + x.tiles;
     }
     if (u < u1) {
       const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-      seg_pre(a, S.pre[warp], x.b, x.h, lane);
+      seg_pre(a, S.pre[w], x.b, x.h, lane);
     }
   }
-  __syncthreads();
+  sync();
   const SegPre &X = S.pre[0];
   const int nq = min(X.m.n_ref * G, kN);
   const uint32_t qbase = smem_u32(S.q);
-  for (int idx = tid; idx < kN * 64; idx += kThreads) {
-    const int qi = idx >> 6, i = idx & 63;
-    float2 y = make_float2(0.f, 0.f);
-    if (qi < nq) {
-      const __nv_bfloat16 *qp = q_row(a, X, qi, G);
-      const uint32_t xq = static_cast<uint32_t>(__bfloat16_as_ushort(qp[i])) |
-                          (static_cast<uint32_t>(__bfloat16_as_ushort(qp[i + 64])) << 16);
-      float cs, sn;
-      rope_cos_sin(X.qrel[qi / G], a.phase[i], &cs, &sn);
-      y = rot_pair(a, xq, cs, sn);
-    }
-    store_q(qbase, qi, i, 0, y.x);
-    store_q(qbase, qi, i, 1, y.y);
+  for (int item = t; item < kN * 8; item += 192) {
+    uint4 v[4];
+    rot_item(a, X, item >> 3, item & 7, nq, G, v);
+    store_item(qbase, item >> 3, item & 7, v);
   }
-  for (int j = tid; j < kMaxQ; j += kThreads) {
+  for (int j = t; j < kMaxQ; j += 192) {
     S.meta.ref_entry[j] = X.m.ref_entry[j];
     S.meta.qhead[j] = X.m.qhead[j];
   }
-  if (tid == 0) S.meta.n_ref = X.m.n_ref;
+  if (t == 0) S.meta.n_ref = X.m.n_ref;
   fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) mbar_arrive(&S.q_full);  // phase 0: segment 0
+  sync();
+  if (t == 0) mbar_arrive(&S.q_full);  // phase 0: segment 0
 }
 
 // Rotated queries of segments 1, 2, ... (segment 0 came from the prologue).
@@ -346,32 +372,10 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
       sync();
     }
     const int nq = min(X.m.n_ref * G, kN);
-    // this thread owns element i = tq (and tq + 64) of every query head qi:
-    // all 2 x 32 loads go out first (64 consecutive bf16 per head across the
-    // two warps: coalesced), then the rotation
-    uint32_t xq[kN];
+    // items tq + 64 k: head (tq >> 3) + 8 k, chunk tq & 7
+    uint4 v[4][4];
 #pragma unroll
-    for (int k = 0; k < kN; ++k) {
-      xq[k] = 0;
-      if (k < nq) {
-        const __nv_bfloat16 *qp = q_row(a, X, k, G);
-        xq[k] = static_cast<uint32_t>(__bfloat16_as_ushort(qp[tq])) |
-                (static_cast<uint32_t>(__bfloat16_as_ushort(qp[tq + 64])) << 16);
-      }
-    }
-    float y[2 * kN];
-    float cs = 1.f, sn = 0.f;
-#pragma unroll
-    for (int k = 0; k < kN; ++k) {
-      float2 v = make_float2(0.f, 0.f);
-      if (k < nq) {
-        // cos/sin depend on the reference (k / G) and the pair (tq) only
-        if (k % G == 0) rope_cos_sin(X.qrel[k / G], a.phase[tq], &cs, &sn);
-        v = rot_pair(a, xq[k], cs, sn);
-      }
-      y[2 * k] = v.x;
-      y[2 * k + 1] = v.y;
-    }
+    for (int k = 0; k < 4; ++k) rot_item(a, X, (tq >> 3) + 8 * k, tq & 7, nq, G, v[k]);
     // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
     // warps keep the same control flow so the named barrier stays balanced.
     // The Q~ buffer and the hand-off metadata are free once segment seg-1's QK
@@ -385,10 +389,7 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
       if (lane == 0) S.meta.n_ref = X.m.n_ref;
     }
 #pragma unroll
-    for (int k = 0; k < kN; ++k) {
-      store_q(qbase, k, tq, 0, y[2 * k]);
-      store_q(qbase, k, tq, 1, y[2 * k + 1]);
-    }
+    for (int k = 0; k < 4; ++k) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
     fence_proxy_async_smem();
     sync();
     if (tq == 0) mbar_arrive(&S.q_full);
@@ -489,11 +490,11 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
         tc_fence_after();
         __syncwarp();
         uint32_t o[32];
-        tmem_ld32(tl + kColO, o);
+        tmem_ld32(tl + kColO + (seg & 1) * kN, o);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
-        tmem_st32(tl + kColO, o);
+        tmem_st32(tl + kColO + (seg & 1) * kN, o);
         tmem_wait_st();
         tc_fence_before();
       }
@@ -534,15 +535,15 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
 
     if (last) {
       // ---- segment epilogue: O -> records, arrivals
-      wait_or_abort(S, a, &S.o_full, seg & 1);
+      wait_or_abort(S, a, &S.o_full[seg & 1], (seg >> 1) & 1);
       tc_fence_after();
       __syncwarp();
       uint32_t o[32];
-      tmem_ld32(tl + kColO, o);
+      tmem_ld32(tl + kColO + (seg & 1) * kN, o);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.o_empty);
+      if (lane == 0) mbar_arrive(&S.o_empty[seg & 1]);
       // column sums of l: transpose-reduce inside the warp, lane j ends with column j
       float v[kN];
 #pragma unroll
@@ -572,7 +573,8 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
         rec[128] = mcol;
         rec[129] = S.lsum[0][lane] + S.lsum[1][lane] + S.lsum[2][lane] + S.lsum[3][lane];
       }
-      __threadfence();
+      // the records of all 128 threads are ordered before the arrivals by the
+      // barrier plus the release fence thread 0 issues in arrive_segment
       sync();
       if (ts == 0) arrive_segment(a, S.smeta, x.h);
     }
@@ -601,8 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.s_empty[b], 4);  // one per softmax warp
     }
     mbar_init(&S.p_empty, 1);
-    mbar_init(&S.o_full, 1);
-    mbar_init(&S.o_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.o_full[b], 1);
+      mbar_init(&S.o_empty[b], 4);  // one per softmax warp
+    }
     mbar_init(&S.mma_done, 1);
     S.abort_flag = 0;
     fence_mbar_init();
@@ -634,15 +638,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (U > 0 && c < C) {
     const int64_t u0 = cta_unit_begin(U, c, C), u1 = cta_unit_begin(U, c + 1, C);
-    query_prologue(a, S, u0, u1);
     if (warp == kWarpTma) {
       if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1);
     } else if (warp == kWarpMma) {
       if (lane == 0) mma_issuer(a, S, tmem, u0, u1);
-    } else if (warp < kWarpQ) {
-      softmax_role(a, S, tmem, u0, u1);
     } else {
-      qprep(a, S, u0, u1);
+      query_prologue(a, S, u0, u1);
+      if (warp < kWarpQ)
+        softmax_role(a, S, tmem, u0, u1);
+      else
+        qprep(a, S, u0, u1);
     }
   }
   tc_fence_before();

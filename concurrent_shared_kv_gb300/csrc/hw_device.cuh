@@ -331,10 +331,14 @@ __device__ void merge_head(const DecodeArgs &a, const int32_t *list, int n_rec, 
                            int hq, int lane) {
   constexpr int EPL = D / 32;
   constexpr int64_t RS = D + 4;  // record stride in floats
+  // pass A: (M, L) over the records; the first 64 maxima stay in registers
   float Mx = -INFINITY, Lx = 0.f;
+  float mreg[2] = {-INFINITY, -INFINITY};
   for (int k = lane; k < n_rec; k += 32) {
     const float *rec = a.partials + static_cast<int64_t>(list[k] + gi) * RS;
-    lse_combine(Mx, Lx, __ldcg(rec + D), __ldcg(rec + D + 1));
+    const float m = __ldcg(rec + D);
+    if (k < 64) mreg[k >> 5] = m;
+    lse_combine(Mx, Lx, m, __ldcg(rec + D + 1));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -342,15 +346,20 @@ __device__ void merge_head(const DecodeArgs &a, const int32_t *list, int n_rec, 
     const float l2 = __shfl_xor_sync(0xffffffffu, Lx, o);
     lse_combine(Mx, Lx, m2, l2);
   }
+  // pass B: out = sum_i w_i o_i, every load of a chunk in flight at once
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   for (int base = 0; base < n_rec; base += 32) {
     const int k = base + lane;
-    const float wl =
-        (k < n_rec) ? ex2(__ldcg(a.partials + static_cast<int64_t>(list[k] + gi) * RS + D) - Mx) : 0.f;
+    float wl = 0.f;
+    if (k < n_rec) {
+      const float m = (base < 64) ? mreg[base >> 5]
+                                  : __ldcg(a.partials + static_cast<int64_t>(list[k] + gi) * RS + D);
+      wl = ex2(m - Mx);
+    }
     const int n = min(32, n_rec - base);
-#pragma unroll 16
+#pragma unroll
     for (int kk = 0; kk < 32; ++kk) {
       if (kk < n) {
         const float w = __shfl_sync(0xffffffffu, wl, kk);

@@ -114,7 +114,7 @@ int hw_workspace_init(void *workspace, size_t bytes, void *stream);
  *   lse[r][hq] = log sum_j exp(s_j)   (natural log; -inf and out = 0 if empty)
  *
  *  d            host  description (above)
- *  q            dev   [n_rows][Hq][D] dtype, un-rotated queries
+ *  q            dev   [n_rows][Hq][D] dtype, un-rotated queries, 16-byte aligned
  *  k_cache      dev   [Hkv][capacity][D] dtype, keys rotated at block-local positions;
  *                     16-byte aligned; may be NULL when capacity is 0
  *  v_cache      dev   [Hkv][capacity][D] dtype, same rules
