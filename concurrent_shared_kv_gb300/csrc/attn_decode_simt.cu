@@ -128,8 +128,8 @@ __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, 
   for (int k = 0; k < QPT; ++k) acc[k] = 0.f;
   __syncthreads();
 
-  const int len = a.block_len[b];
-  const int64_t row_base = a.block_start[b];
+  const int len = P.len[b];
+  const int64_t row_base = P.start[b];
   for (int t = t0; t < t1; ++t) {
     const int tok0 = t * kSimtTile;
     const int valid = min(kSimtTile, len - tok0);

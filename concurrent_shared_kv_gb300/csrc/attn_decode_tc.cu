@@ -64,11 +64,12 @@ struct TcSmem {
   alignas(1024) uint8_t q[kQBytes];
   PlanCore plan;
   SegMeta meta;        // handed from the query warps to the softmax warps
-  SegMeta smeta;       // the softmax warps' copy for the segment epilogue
+  SegMeta smeta[2];    // the softmax warps' copy per segment parity, for the arrivals
   SegPre pre[kPre];    // query-side metadata of segments j (j < kPre) or j % kPre
   MergeScratch merge;
   alignas(16) float red[2][kN][4];  // per tile: column maxima of the 4 softmax warps (read as float4)
-  alignas(16) float lsum[4][kN];    // per segment: column sums of the 4 softmax warps
+  float lsave[2][4][kN];  // per segment parity: column sums of l of the 4 softmax warps
+  float msave[2][kN];     // per segment parity: the reference maxima
   int32_t merge_qhead[kMaxQ];
   int32_t merge_flag[2];
   int32_t merge_list[kMaxRecords];
@@ -81,6 +82,7 @@ struct TcSmem {
   uint64_t p_full[kStages];  // P of the stage's tile written (the softmax may run ahead)
   uint64_t p_empty, mma_done;
   uint64_t o_full[2], o_empty[2];  // per O buffer: segment done / epilogue read it
+  uint64_t rec_ready[2];           // per segment parity: records written, arrivals due
 };
 
 __device__ __forceinline__ void set_abort(TcSmem &S, const DecodeArgs &a) {
@@ -150,7 +152,7 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
     const int s = i % kStages;
     if (!wait_or_abort(S, a, &S.kv_empty[s], ((i / kStages) & 1) ^ 1)) break;
     const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-    const int row = a.block_start[x.b] + x.t * kT;
+    const int row = S.plan.start[x.b] + x.t * kT;
     uint8_t *st = S.stage[s];
     mbar_arrive_expect_tx(&S.k_full[s], 2 * kBox);
     tma_load_3d(st, tk, &S.k_full[s], 0, row, x.h, pol);
@@ -349,10 +351,13 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
   if (t == 0) mbar_arrive(&S.q_full);  // phase 0: segment 0
 }
 
-// Rotated queries of segments 1, 2, ... (segment 0 came from the prologue).
-// The values of segment j are loaded and computed in registers while the
-// tensor cores still work on segment j - 1; they are written once the single
-// Q~ buffer is released.
+// Rotated queries of segments 1, 2, ... (segment 0 came from the prologue),
+// and the arrivals of finished segments.  The values of segment j are loaded
+// and computed in registers while the tensor cores still work on segment
+// j - 1; they are written once the single Q~ buffer is released.  After
+// handing over segment j the warps wait for segment j - 1's records and
+// count them (fence + one atomic per view reference), so that the softmax
+// warps never wait on global memory ordering.
 __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
   const int lane = threadIdx.x & 31;
@@ -360,48 +365,106 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   NamedSync<2, 64> sync;
   const uint32_t qbase = smem_u32(S.q);
   int64_t u = u0;
+  int prev_h;
   {
     const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
     u = x.seg_first + x.tiles;  // segment 0 is done
+    prev_h = x.h;
   }
-  for (int seg = 1; u < u1; ++seg) {
-    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-    SegPre &X = S.pre[seg % kPre];
-    if (seg >= kPre) {
-      if (tq < 32) seg_pre(a, X, x.b, x.h, lane);
-      sync();
-    }
-    const int nq = min(X.m.n_ref * G, kN);
-    // items tq + 64 k: head (tq >> 3) + 8 k, chunk tq & 7
-    uint4 v[4][4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) rot_item(a, X, (tq >> 3) + 8 * k, tq & 7, nq, G, v[k]);
-    // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
-    // warps keep the same control flow so the named barrier stays balanced.
-    // The Q~ buffer and the hand-off metadata are free once segment seg-1's QK
-    // products completed and the softmax warps took their copy.
-    wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
-    if (tq < 32) {
-      for (int j = lane; j < kMaxQ; j += 32) {
-        S.meta.ref_entry[j] = X.m.ref_entry[j];
-        S.meta.qhead[j] = X.m.qhead[j];
+  for (int seg = 1;; ++seg) {
+    const bool more = u < u1;
+    UnitPos x = {0, 0, 0, 0, 0};
+    if (more) {
+      x = unit_pos(S.plan, a.n_blocks, u);
+      SegPre &X = S.pre[seg % kPre];
+      if (seg >= kPre) {
+        if (tq < 32) seg_pre(a, X, x.b, x.h, lane);
+        sync();
       }
-      if (lane == 0) S.meta.n_ref = X.m.n_ref;
-    }
+      const int nq = min(X.m.n_ref * G, kN);
+      // items tq + 64 k: head (tq >> 3) + 8 k, chunk tq & 7
+      uint4 v[4][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
-    fence_proxy_async_smem();
-    sync();
-    if (tq == 0) mbar_arrive(&S.q_full);
+      for (int k = 0; k < 4; ++k) rot_item(a, X, (tq >> 3) + 8 * k, tq & 7, nq, G, v[k]);
+      // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
+      // warps keep the same control flow so the named barrier stays balanced.
+      // The Q~ buffer and the hand-off metadata are free once segment seg-1's
+      // QK products completed and the softmax warps took their copy.
+      wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
+      if (tq < 32) {
+        for (int j = lane; j < kMaxQ; j += 32) {
+          S.meta.ref_entry[j] = X.m.ref_entry[j];
+          S.meta.qhead[j] = X.m.qhead[j];
+        }
+        if (lane == 0) S.meta.n_ref = X.m.n_ref;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
+      fence_proxy_async_smem();
+      sync();
+      if (tq == 0) mbar_arrive(&S.q_full);
+    }
+    // arrivals of segment seg - 1 (its records are written one tile after it ends)
+    const int done = seg - 1;
+    wait_or_abort(S, a, &S.rec_ready[done & 1], (done >> 1) & 1);
+    if (tq == 0) arrive_segment(a, S.smeta[done & 1], prev_h);
+    if (!more) break;
+    prev_h = x.h;
     u = x.seg_first + x.tiles;
   }
+}
+
+// Butterfly transpose-reduce over the warp: on entry v[j] is this lane's
+// value of column j; on exit lane j holds op over all 32 lanes of column j
+// in v[0] (31 shuffles for 32 columns).
+template <bool MAX>
+__device__ __forceinline__ void transpose_reduce(float (&v)[kN], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+    for (int k = 0; k < off; ++k) {
+      const bool up = (lane & off) != 0;
+      const float mine = up ? v[k + off] : v[k];
+      const float other = __shfl_xor_sync(0xffffffffu, up ? v[k] : v[k + off], off);
+      v[k] = MAX ? fmaxf(mine, other) : mine + other;
+    }
+  }
+}
+
+// Records of a finished segment: O (TMEM buffer seg & 1) and the handed-over
+// (m, l) of each query head -> partial records in the workspace.  Runs one
+// tile after the segment's end, when its last P.V product has (nearly always)
+// completed; the arrivals are left to the query warps.
+__device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int seg, int b, int h,
+                                int nq, int ws, int lane, int row, NamedSync<1, 128> sync) {
+  wait_or_abort(S, a, &S.o_full[seg & 1], (seg >> 1) & 1);
+  tc_fence_after();
+  __syncwarp();
+  uint32_t o[32];
+  tmem_ld32(tl + kColO + (seg & 1) * kN, o);
+  tmem_wait_ld();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&S.o_empty[seg & 1]);
+  sync();  // every warp's lsave of this segment is in place
+  const int64_t slot = static_cast<int64_t>(b) * a.n_kv_heads + h + blockIdx.x;
+#pragma unroll
+  for (int j = 0; j < kN; ++j)
+    if (j < nq) record_ptr(a, slot, j)[row] = __uint_as_float(o[j]);
+  if (ws == 0 && lane < nq) {
+    float *rec = record_ptr(a, slot, lane);
+    const float(*ls)[kN] = S.lsave[seg & 1];
+    rec[128] = S.msave[seg & 1][lane];
+    rec[129] = ls[0][lane] + ls[1][lane] + ls[2][lane] + ls[3][lane];
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&S.rec_ready[seg & 1]);
 }
 
 __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0,
                              int64_t u1) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ws = warp - kWarpSoft;              // 0..3
-  const int ts = threadIdx.x - kWarpSoft * 32;  // 0..127
   const int qd = warp & 3;                      // TMEM lane quadrant of this warp
   const int row = qd * 32 + lane;               // token of the tile (S) / element d (O)
   const uint32_t tl = tmem + (static_cast<uint32_t>(qd * 32) << 16);
@@ -415,6 +478,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   // blocks any more and the CTA runs to its end on stale data.
   float m_run[kN], l_part[kN];
   int seg = -1, nq = 0;
+  int pend = -1, pend_b = 0, pend_h = 0, pend_nq = 0;  // segment whose records are due
   for (int i = 0; i < n; ++i) {
     const int64_t u = u0 + i;
     const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
@@ -423,9 +487,10 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       ++seg;
       wait_or_abort(S, a, &S.q_full, seg & 1);
       nq = min(S.meta.n_ref * G, kN);
-      if (ws == 0) {  // private copy for the epilogue, then hand the buffer back
-        for (int j = lane; j < kMaxQ; j += 32) S.smeta.ref_entry[j] = S.meta.ref_entry[j];
-        if (lane == 0) S.smeta.n_ref = S.meta.n_ref;
+      if (ws == 0) {  // copy for the arrivals, then hand the buffer back
+        SegMeta &sm = S.smeta[seg & 1];
+        for (int j = lane; j < kMaxQ; j += 32) sm.ref_entry[j] = S.meta.ref_entry[j];
+        if (lane == 0) sm.n_ref = S.meta.n_ref;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.q_empty);
@@ -446,7 +511,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.s_empty[sb]);
 
-    const int valid = min(kT, a.block_len[x.b] - x.t * kT);
+    const int valid = min(kT, S.plan.len[x.b] - x.t * kT);
     const bool tok_ok = row < valid;
     float sc[kN];
 #pragma unroll
@@ -462,21 +527,19 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     for (int j = 0; j < kN; ++j) exceed |= (j < nq) && (sc[j] > m_run[j] + kLazy);
     if (bar_red_or_128(exceed)) {
       float(*red)[4] = S.red[i & 1];
+      float v[kN];
 #pragma unroll
-      for (int j = 0; j < kN; ++j) {
-        if (j < nq) {
-          const int mk = __reduce_max_sync(0xffffffffu, f2ord(sc[j]));
-          if (lane == j) red[j][ws] = ord2f(mk);
-        }
-      }
+      for (int j = 0; j < kN; ++j) v[j] = sc[j];
+      transpose_reduce<true>(v, lane);
+      red[lane][ws] = v[0];
       sync();
       float alpha[kN];
 #pragma unroll
       for (int j = 0; j < kN; ++j) {
         alpha[j] = 1.f;
         if (j < nq) {
-          const float4 v = *reinterpret_cast<const float4 *>(red[j]);
-          const float tmax = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+          const float4 t4 = *reinterpret_cast<const float4 *>(red[j]);
+          const float tmax = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
           if (tmax > m_run[j] + kLazy) {
             alpha[j] = ex2(m_run[j] - tmax);  // 0 when m_run = -inf
             m_run[j] = tmax;
@@ -533,52 +596,31 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.p_full[s]);
 
+    if (pend >= 0) {  // records of the previous segment, one tile late
+      segment_records(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync);
+      pend = -1;
+    }
     if (last) {
-      // ---- segment epilogue: O -> records, arrivals
-      wait_or_abort(S, a, &S.o_full[seg & 1], (seg >> 1) & 1);
-      tc_fence_after();
-      __syncwarp();
-      uint32_t o[32];
-      tmem_ld32(tl + kColO + (seg & 1) * kN, o);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.o_empty[seg & 1]);
-      // column sums of l: transpose-reduce inside the warp, lane j ends with column j
+      // hand over (m, l) of every query head; the records follow one tile later
       float v[kN];
 #pragma unroll
       for (int j = 0; j < kN; ++j) v[j] = l_part[j];
+      transpose_reduce<false>(v, lane);
+      S.lsave[seg & 1][ws][lane] = v[0];
+      if (ws == 0) {
+        float mcol = 0.f;
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-#pragma unroll
-        for (int k = 0; k < off; ++k) {
-          const bool up = (lane & off) != 0;
-          const float mine = up ? v[k + off] : v[k];
-          const float other = up ? v[k] : v[k + off];
-          v[k] = mine + __shfl_xor_sync(0xffffffffu, other, off);
-        }
+        for (int j = 0; j < kN; ++j)
+          if (j == lane) mcol = m_run[j];
+        S.msave[seg & 1][lane] = mcol;
       }
-      S.lsum[ws][lane] = v[0];
-      float mcol = 0.f;
-#pragma unroll
-      for (int j = 0; j < kN; ++j)
-        if (j == lane) mcol = m_run[j];
-      sync();
-      const int64_t slot = static_cast<int64_t>(x.b) * a.n_kv_heads + x.h + blockIdx.x;
-#pragma unroll
-      for (int j = 0; j < kN; ++j)
-        if (j < nq) record_ptr(a, slot, j)[row] = __uint_as_float(o[j]);
-      if (ws == 0 && lane < nq) {
-        float *rec = record_ptr(a, slot, lane);
-        rec[128] = mcol;
-        rec[129] = S.lsum[0][lane] + S.lsum[1][lane] + S.lsum[2][lane] + S.lsum[3][lane];
-      }
-      // the records of all 128 threads are ordered before the arrivals by the
-      // barrier plus the release fence thread 0 issues in arrive_segment
-      sync();
-      if (ts == 0) arrive_segment(a, S.smeta, x.h);
+      pend = seg;
+      pend_b = x.b;
+      pend_h = x.h;
+      pend_nq = nq;
     }
   }
+  if (pend >= 0) segment_records(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -605,7 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&S.p_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.o_full[b], 1);
-      mbar_init(&S.o_empty[b], 4);  // one per softmax warp
+      mbar_init(&S.o_empty[b], 4);    // one per softmax warp
+      mbar_init(&S.rec_ready[b], 4);  // one per softmax warp
     }
     mbar_init(&S.mma_done, 1);
     S.abort_flag = 0;

@@ -94,6 +94,8 @@ struct NamedSync {
 
 struct PlanCore {
   int32_t tiles[HW_MAX_BLOCKS];      // tiles per kv head (0: block skipped)
+  int32_t start[HW_MAX_BLOCKS];      // first pool token (valid where tiles > 0)
+  int32_t len[HW_MAX_BLOCKS];        // tokens (valid where tiles > 0)
   int64_t ubase[HW_MAX_BLOCKS + 1];  // first unit of each block
 };
 
@@ -171,6 +173,8 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, PlanScratch &S) {
       }
     }
     P.tiles[b] = S.headmap_ok ? t : 0;
+    P.start[b] = s;
+    P.len[b] = n;
   }
   __syncthreads();
   if (tid < 32) {
