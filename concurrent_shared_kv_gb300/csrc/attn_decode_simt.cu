@@ -191,7 +191,7 @@ __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, 
   }
 
   // 4. partial records into slot seg + c, then arrival and merges
-  const int64_t slot = static_cast<int64_t>(b) * a.n_kv_heads + h + blockIdx.x;
+  const int64_t slot = seg_id(a.n_blocks, b, h) + blockIdx.x;
 #pragma unroll
   for (int k = 0; k < QPT; ++k) {
     const int qi = qbase + k * QSTEP;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
   PlanCore &P = S.plan;
   build_plan<kSimtTile>(a, P, S.scratch);
   const int c = blockIdx.x;
-  const int64_t U = P.ubase[a.n_blocks];
+  const int64_t U = total_units(P, a);
   const int C = static_cast<int>(U < gridDim.x ? U : gridDim.x);  // working CTAs
 
   // (row, kv head) pairs without any record: out = 0, lse = -inf

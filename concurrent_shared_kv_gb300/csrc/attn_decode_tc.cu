@@ -55,6 +55,7 @@ constexpr int kPre = 4;  // segments whose metadata the prologue prepares
 // reference its row and relative rotation i_q - offset.
 struct SegPre {
   SegMeta m;
+  int32_t h;  // kv head of the segment
   int32_t qrow[kMaxQ];
   int64_t qrel[kMaxQ];
 };
@@ -64,7 +65,6 @@ struct TcSmem {
   alignas(1024) uint8_t q[kQBytes];
   PlanCore plan;
   SegMeta meta;        // handed from the query warps to the softmax warps
-  SegMeta smeta[2];    // the softmax warps' copy per segment parity, for the arrivals
   SegPre pre[kPre];    // query-side metadata of segments j (j < kPre) or j % kPre
   MergeScratch merge;
   alignas(16) float red[2][kN][4];  // per tile: column maxima of the 4 softmax warps (read as float4)
@@ -82,7 +82,7 @@ struct TcSmem {
   uint64_t p_full[kStages];  // P of the stage's tile written (the softmax may run ahead)
   uint64_t p_empty, mma_done;
   uint64_t o_full[2], o_empty[2];  // per O buffer: segment done / epilogue read it
-  uint64_t rec_ready[2];           // per segment parity: records written, arrivals due
+  uint64_t rec_ready[4];           // per segment mod 4: records written, arrivals due
 };
 
 __device__ __forceinline__ void set_abort(TcSmem &S, const DecodeArgs &a) {
@@ -245,6 +245,7 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
 
 // Query-side metadata of segment (b, h) into X, by one warp.
 __device__ void seg_pre(const DecodeArgs &a, SegPre &X, int b, int h, int lane) {
+  if (lane == 0) X.h = h;
   gather_refs(a, X.m, b, lane);
   gather_qheads(a, X.m, h, lane);
   __syncwarp();
@@ -354,62 +355,62 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
 // Rotated queries of segments 1, 2, ... (segment 0 came from the prologue),
 // and the arrivals of finished segments.  The values of segment j are loaded
 // and computed in registers while the tensor cores still work on segment
-// j - 1; they are written once the single Q~ buffer is released.  After
-// handing over segment j the warps wait for segment j - 1's records and
-// count them (fence + one atomic per view reference), so that the softmax
-// warps never wait on global memory ordering.
+// j - 1; they are written once the single Q~ buffer is released.  Then the
+// warps count segment j - 2's records (fence + one atomic per view
+// reference): two segments late, so that neither these global-memory
+// operations nor the softmax warps' record stores sit on the path of the
+// next rotated queries.  Segment k's metadata stays in pre[k % kPre] until
+// segment k + kPre is prepared, well after its arrivals.
 __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
   const int lane = threadIdx.x & 31;
   const int G = a.n_q_heads / a.n_kv_heads;
   NamedSync<2, 64> sync;
   const uint32_t qbase = smem_u32(S.q);
+  auto arrivals = [&](int done) {
+    // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
+    // warps keep the same control flow so the named barrier stays balanced.
+    wait_or_abort(S, a, &S.rec_ready[done & 3], (done >> 2) & 1);
+    if (tq == 0) arrive_segment(a, S.pre[done % kPre].m, S.pre[done % kPre].h);
+  };
   int64_t u = u0;
-  int prev_h;
   {
     const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-    u = x.seg_first + x.tiles;  // segment 0 is done
-    prev_h = x.h;
+    u = x.seg_first + x.tiles;  // segment 0 came from the prologue
   }
   for (int seg = 1;; ++seg) {
-    const bool more = u < u1;
-    UnitPos x = {0, 0, 0, 0, 0};
-    if (more) {
-      x = unit_pos(S.plan, a.n_blocks, u);
-      SegPre &X = S.pre[seg % kPre];
-      if (seg >= kPre) {
-        if (tq < 32) seg_pre(a, X, x.b, x.h, lane);
-        sync();
-      }
-      const int nq = min(X.m.n_ref * G, kN);
-      // items tq + 64 k: head (tq >> 3) + 8 k, chunk tq & 7
-      uint4 v[4][4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) rot_item(a, X, (tq >> 3) + 8 * k, tq & 7, nq, G, v[k]);
-      // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
-      // warps keep the same control flow so the named barrier stays balanced.
-      // The Q~ buffer and the hand-off metadata are free once segment seg-1's
-      // QK products completed and the softmax warps took their copy.
-      wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
-      if (tq < 32) {
-        for (int j = lane; j < kMaxQ; j += 32) {
-          S.meta.ref_entry[j] = X.m.ref_entry[j];
-          S.meta.qhead[j] = X.m.qhead[j];
-        }
-        if (lane == 0) S.meta.n_ref = X.m.n_ref;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
-      fence_proxy_async_smem();
-      sync();
-      if (tq == 0) mbar_arrive(&S.q_full);
+    if (u >= u1) {  // no segment seg: the last arrivals
+      if (seg >= 2) arrivals(seg - 2);
+      arrivals(seg - 1);
+      break;
     }
-    // arrivals of segment seg - 1 (its records are written one tile after it ends)
-    const int done = seg - 1;
-    wait_or_abort(S, a, &S.rec_ready[done & 1], (done >> 1) & 1);
-    if (tq == 0) arrive_segment(a, S.smeta[done & 1], prev_h);
-    if (!more) break;
-    prev_h = x.h;
+    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    SegPre &X = S.pre[seg % kPre];
+    if (seg >= kPre) {
+      if (tq < 32) seg_pre(a, X, x.b, x.h, lane);
+      sync();
+    }
+    const int nq = min(X.m.n_ref * G, kN);
+    // items tq + 64 k: head (tq >> 3) + 8 k, chunk tq & 7
+    uint4 v[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) rot_item(a, X, (tq >> 3) + 8 * k, tq & 7, nq, G, v[k]);
+    // The Q~ buffer and the hand-off metadata are free once segment seg-1's
+    // QK products completed and every softmax warp read the hand-off.
+    wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
+    if (tq < 32) {
+      for (int j = lane; j < kMaxQ; j += 32) {
+        S.meta.ref_entry[j] = X.m.ref_entry[j];
+        S.meta.qhead[j] = X.m.qhead[j];
+      }
+      if (lane == 0) S.meta.n_ref = X.m.n_ref;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
+    fence_proxy_async_smem();
+    sync();
+    if (tq == 0) mbar_arrive(&S.q_full);
+    if (seg >= 2) arrivals(seg - 2);
     u = x.seg_first + x.tiles;
   }
 }
@@ -447,7 +448,7 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
   __syncwarp();
   if (lane == 0) mbar_arrive(&S.o_empty[seg & 1]);
   sync();  // every warp's lsave of this segment is in place
-  const int64_t slot = static_cast<int64_t>(b) * a.n_kv_heads + h + blockIdx.x;
+  const int64_t slot = seg_id(a.n_blocks, b, h) + blockIdx.x;
 #pragma unroll
   for (int j = 0; j < kN; ++j)
     if (j < nq) record_ptr(a, slot, j)[row] = __uint_as_float(o[j]);
@@ -458,7 +459,7 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
     rec[129] = ls[0][lane] + ls[1][lane] + ls[2][lane] + ls[3][lane];
   }
   __syncwarp();
-  if (lane == 0) mbar_arrive(&S.rec_ready[seg & 1]);
+  if (lane == 0) mbar_arrive(&S.rec_ready[seg & 3]);
 }
 
 __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0,
@@ -487,13 +488,8 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       ++seg;
       wait_or_abort(S, a, &S.q_full, seg & 1);
       nq = min(S.meta.n_ref * G, kN);
-      if (ws == 0) {  // copy for the arrivals, then hand the buffer back
-        SegMeta &sm = S.smeta[seg & 1];
-        for (int j = lane; j < kMaxQ; j += 32) sm.ref_entry[j] = S.meta.ref_entry[j];
-        if (lane == 0) sm.n_ref = S.meta.n_ref;
-      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.q_empty);
+      if (lane == 0) mbar_arrive(&S.q_empty);  // this warp has read the hand-off
 #pragma unroll
       for (int j = 0; j < kN; ++j) {
         m_run[j] = -INFINITY;
@@ -648,8 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.o_full[b], 1);
       mbar_init(&S.o_empty[b], 4);    // one per softmax warp
-      mbar_init(&S.rec_ready[b], 4);  // one per softmax warp
     }
+    for (int b = 0; b < 4; ++b) mbar_init(&S.rec_ready[b], 4);  // one per softmax warp
     mbar_init(&S.mma_done, 1);
     S.abort_flag = 0;
     fence_mbar_init();
@@ -665,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   const int c = blockIdx.x;
-  const int64_t U = S.plan.ubase[a.n_blocks];
+  const int64_t U = total_units(S.plan, a);
   const int C = static_cast<int>(U < gridDim.x ? U : gridDim.x);
 
   // (row, kv head) pairs without any record: out = 0, lse = -inf

@@ -5,15 +5,18 @@
 // Scheduling (omica.com.cn article, section 3.2: the KV cache is split evenly
 // over the SMs and the partial results are merged):
 //   unit      = one tile of `TILE` tokens of one block for one kv head;
-//   units are ordered block-major, then kv head, then tile; only blocks that
-//   some view references take part.
+//   units are ordered kv-head-major, then block, then tile (UH units per
+//   head); only blocks that some view references take part.  Head-major
+//   order keeps each head's short worker blocks next to its long common
+//   block, instead of stacking every head's short blocks on the last CTAs.
 //   CTA c of C owns units [floor(c U / C), floor((c+1) U / C)), so every CTA
 //   streams the same number of tiles whatever the block lengths are.  C is
 //   min(grid, U): every working CTA owns at least one unit, so the CTAs that
 //   touch a segment form one contiguous range.
-//   segment   = the units of one (block, kv head); a CTA emits one partial
-//   record per (segment it touched, query head served) into slot seg + c,
-//   which is unique because seg and c never both stay put as units advance.
+//   segment   = the units of one (block, kv head), id seg = h * n_blocks + b,
+//   increasing along the unit order; a CTA emits one partial record per
+//   (segment it touched, query head served) into slot seg + c, which is
+//   unique because seg and c never both stay put as units advance.
 //   Every delivered record bumps the arrival counter of its (row, kv head).
 //   The launch is cooperative (all CTAs resident at once): after its own
 //   units, CTA c merges the (row, kv head) pairs c, c + grid, ... - it waits,
@@ -96,7 +99,7 @@ struct PlanCore {
   int32_t tiles[HW_MAX_BLOCKS];      // tiles per kv head (0: block skipped)
   int32_t start[HW_MAX_BLOCKS];      // first pool token (valid where tiles > 0)
   int32_t len[HW_MAX_BLOCKS];        // tokens (valid where tiles > 0)
-  int64_t ubase[HW_MAX_BLOCKS + 1];  // first unit of each block
+  int64_t ubase[HW_MAX_BLOCKS + 1];  // first unit of each block within a head; [n] = UH
 };
 
 struct PlanScratch {  // only while the plan is built
@@ -178,11 +181,11 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, PlanScratch &S) {
   }
   __syncthreads();
   if (tid < 32) {
-    // exclusive prefix over blocks of Hkv * tiles, one warp
+    // exclusive prefix over blocks of tiles (units of one kv head), one warp
     int64_t carry = 0;
     for (int base = 0; base < a.n_blocks; base += 32) {
       const int b = base + tid;
-      const int64_t x = (b < a.n_blocks) ? static_cast<int64_t>(P.tiles[b]) * a.n_kv_heads : 0;
+      const int64_t x = (b < a.n_blocks) ? static_cast<int64_t>(P.tiles[b]) : 0;
       int64_t incl = x;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -197,7 +200,12 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, PlanScratch &S) {
   __syncthreads();
 }
 
-// Block that holds unit u (ubase[b] <= u < ubase[b+1]), by binary search.
+// Total units: UH per kv head.
+__device__ __forceinline__ int64_t total_units(const PlanCore &P, const DecodeArgs &a) {
+  return P.ubase[a.n_blocks] * a.n_kv_heads;
+}
+
+// Block that holds in-head unit u (ubase[b] <= u < ubase[b+1]), by binary search.
 __device__ __forceinline__ int block_of_unit(const PlanCore &P, int n_blocks, int64_t u) {
   int lo = 0, hi = n_blocks - 1;
   while (lo < hi) {
@@ -214,20 +222,30 @@ struct UnitPos {
 };
 __device__ __forceinline__ UnitPos unit_pos(const PlanCore &P, int n_blocks, int64_t u) {
   UnitPos x;
-  x.b = block_of_unit(P, n_blocks, u);
+  const int64_t UH = P.ubase[n_blocks];
+  x.h = static_cast<int>(u / UH);
+  const int64_t local = u - static_cast<int64_t>(x.h) * UH;
+  x.b = block_of_unit(P, n_blocks, local);
   x.tiles = P.tiles[x.b];
-  const int64_t local = u - P.ubase[x.b];
-  x.h = static_cast<int>(local / x.tiles);
-  x.t = static_cast<int>(local - static_cast<int64_t>(x.h) * x.tiles);
-  x.seg_first = P.ubase[x.b] + static_cast<int64_t>(x.h) * x.tiles;
+  x.t = static_cast<int>(local - P.ubase[x.b]);
+  x.seg_first = static_cast<int64_t>(x.h) * UH + P.ubase[x.b];
   return x;
 }
 
+// First unit of segment (b, h) and its id.
+__device__ __forceinline__ int64_t seg_first_unit_of(const PlanCore &P, int n_blocks, int b, int h) {
+  return static_cast<int64_t>(h) * P.ubase[n_blocks] + P.ubase[b];
+}
+__device__ __forceinline__ int64_t seg_id(int n_blocks, int b, int h) {
+  return static_cast<int64_t>(h) * n_blocks + b;
+}
+
 // Number of CTAs whose unit ranges touch segment (b, h).
-__device__ __forceinline__ int seg_ctas(const PlanCore &P, int b, int h, int64_t U, int C) {
+__device__ __forceinline__ int seg_ctas(const PlanCore &P, int n_blocks, int b, int h, int64_t U,
+                                        int C) {
   const int tl = P.tiles[b];
   if (tl == 0) return 0;
-  const int64_t s0 = P.ubase[b] + static_cast<int64_t>(h) * tl;
+  const int64_t s0 = seg_first_unit_of(P, n_blocks, b, h);
   return cta_of_unit(s0 + tl - 1, U, C) - cta_of_unit(s0, U, C) + 1;
 }
 
@@ -237,7 +255,7 @@ __device__ __forceinline__ int expected_records(const DecodeArgs &a, const PlanC
   int n = 0;
   for (int v = 0; v < a.n_view; ++v) {
     const int b = a.view_block[r * a.n_view + v];
-    if (b >= 0 && b < a.n_blocks) n += seg_ctas(P, b, h, U, C);
+    if (b >= 0 && b < a.n_blocks) n += seg_ctas(P, a.n_blocks, b, h, U, C);
   }
   return n;
 }
@@ -414,8 +432,8 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch
         X.mv_seg[v] = -1;
         X.mv_qi[v] = 0;
         if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
-          const int64_t s0 = P.ubase[b] + static_cast<int64_t>(h) * P.tiles[b];
-          X.mv_seg[v] = static_cast<int64_t>(b) * a.n_kv_heads + h;
+          const int64_t s0 = seg_first_unit_of(P, a.n_blocks, b, h);
+          X.mv_seg[v] = seg_id(a.n_blocks, b, h);
           X.mv_c0[v] = cta_of_unit(s0, U, C);
           X.mv_c1[v] = cta_of_unit(s0 + P.tiles[b] - 1, U, C);
         }
