@@ -25,6 +25,7 @@ DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMA
 
 # every symbol the header declares
 EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode",
+           "hw_attn_decode_noalloc",
            "hw_block_commit", "hw_workspace_status", "hw_views_combined", "hw_last_cuda_error",
            "hw_status_string"]
 
@@ -67,6 +68,7 @@ def lib(path: Optional[str] = None):
     L.hw_attn_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_size_t)]
     L.hw_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
     L.hw_attn_decode.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12 + [ctypes.c_size_t, _P]
+    L.hw_attn_decode_noalloc.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12
     L.hw_block_commit.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
                                   ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32,
@@ -140,6 +142,18 @@ def attn_decode(desc: AttnDesc, q, k_cache, v_cache, block_start, block_len, vie
                               _ptr(view_offset), _ptr(q_pos), _ptr(q_to_kv), _ptr(out), _ptr(lse),
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check("hw_attn_decode", st)
+    return st
+
+
+def attn_decode_noalloc(desc: AttnDesc, q, k_cache, v_cache, block_start, block_len, view_block,
+                        view_offset, q_pos, out, lse, q_to_kv=None, stream=None) -> int:
+    """hw_attn_decode_noalloc: the decode without a caller workspace, for code
+    that cannot allocate device memory (it uses the library's fixed scratch)."""
+    st = lib().hw_attn_decode_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(block_start), _ptr(block_len), _ptr(view_block),
+                                      _ptr(view_offset), _ptr(q_pos), _ptr(q_to_kv), _ptr(out),
+                                      _ptr(lse), _stream(stream))
+    _check("hw_attn_decode_noalloc", st)
     return st
 
 

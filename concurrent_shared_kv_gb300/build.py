@@ -19,7 +19,8 @@ BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libhogwild.so")
 
-SOURCES = ["api.cpp", "attn_decode_simt.cu", "attn_decode_tc.cu", "block_commit.cu"]
+SOURCES = ["api.cpp", "attn_decode_simt.cu", "attn_decode_tc.cu", "block_commit.cu",
+           "attn_decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

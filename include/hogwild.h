@@ -141,6 +141,40 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
                    size_t workspace_bytes, void *stream);
 
 /*
+ * Size of the fixed scratch array hw_attn_decode_noalloc uses (32 MiB): it
+ * covers descriptions whose hw_attn_decode_workspace_size is at most this,
+ * e.g. up to about 1300 (block, kv head) pairs with head_dim 128.
+ */
+#define HW_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * hw_attn_decode for callers that cannot allocate device memory - code that
+ * runs inside an allocator or memory pool, plugins whose host runtime owns
+ * every device buffer, processes that forbid allocation after start-up.  The
+ * pages describe no such variant; it has no counterpart there.
+ *
+ * Same arguments, meaning and result as hw_attn_decode, without the
+ * workspace: the call uses a scratch array of HW_NOALLOC_SCRATCH_BYTES that
+ * the library itself holds on every GPU that loads it, until the process
+ * exits.  No call allocates or frees memory.
+ *  - The first call on a device finds the array's device address and zeroes
+ *    it with a synchronous cudaMemset; make that first call before any stream
+ *    capture.  Each call then clears the scratch's counters on `stream`.
+ *  - Every call shares the one array: calls whose work overlaps on the GPU
+ *    (other streams, other host threads) race and give wrong results.
+ *    Order them on one stream.
+ *  - Returns HW_ERR_WORKSPACE, before enqueuing anything, when `d` needs more
+ *    scratch than HW_NOALLOC_SCRATCH_BYTES; use hw_attn_decode then.
+ *  - Device-side metadata errors (HW_DEV_*) are not reported: there is no
+ *    workspace to read them from.
+ */
+int hw_attn_decode_noalloc(const hw_attn_desc *d, const void *q, const void *k_cache,
+                           const void *v_cache, const int32_t *block_start,
+                           const int32_t *block_len, const int32_t *view_block,
+                           const int32_t *view_offset, const int32_t *q_pos,
+                           const int32_t *q_to_kv, void *out, float *lse, void *stream);
+
+/*
  * Block commit over n_layers layers in one launch (a finished step moves
  * into the shared history; key design 2 of the Hogwild! notes):
  *   K_dst[l][h][dst_offset + j] = rho(K_src[l][h][src_begin + j], pos_delta)

@@ -1,0 +1,59 @@
+"""hw_attn_decode_noalloc: decode attention for callers that cannot allocate.
+
+Code running inside a memory pool or allocator, plugins whose host runtime owns
+every device buffer, and processes that forbid allocation after start-up cannot
+hand hw_attn_decode a freshly allocated workspace.  The no-allocation entry
+point runs the same kernels on a fixed scratch array the library holds.  These
+tests call it through the C ABI and check it against the workspace entry point,
+twice in a row (the scratch keeps the previous call's contents), within the
+tolerances of the parity tests.  The file sorts last so that a run stopping at
+its first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from concurrent_shared_kv_gb300 import api
+from concurrent_shared_kv_gb300 import workloads as wl
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _tolerances(dtype):
+    return (H.F32_TOL, H.F32_TOL) if dtype == "f32" else (H.BF16_MAX, H.BF16_MEAN)
+
+
+@pytest.mark.parametrize("make", [wl.tiny_f32, wl.qwq32b_w4], ids=["tiny-f32", "qwq32b-w4"])
+def test_noalloc_matches_workspace_entry_point(make):
+    w = make()
+    c = H.host_case(w) if w.dtype == "f32" else H.device_case(w, 0)
+    s = c.session()
+    ref_out, ref_lse = s.decode(c.q, c.k, c.v)  # hw_attn_decode with a workspace
+    torch.cuda.synchronize()
+    m = s.meta
+    max_tol, mean_tol = _tolerances(w.dtype)
+    for call in range(2):  # the scratch keeps the last call's contents
+        out = torch.full_like(ref_out, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        api.attn_decode_noalloc(s.desc, c.q, c.k, c.v, m["block_start"], m["block_len"],
+                                m["view_block"], m["view_offset"], m["q_pos"], out, lse,
+                                q_to_kv=m["q_to_kv"])
+        torch.cuda.synchronize()
+        err = (out.double() - ref_out.double()).abs()
+        assert torch.isfinite(out).all(), call
+        assert err.max().item() <= max_tol and err.mean().item() <= mean_tol, (call, err.max().item())
+        lerr = (lse.double() - ref_lse.double()).abs().max().item()
+        assert lerr <= H.LSE_TOL[w.dtype], (call, lerr)
+
+
+def test_noalloc_rejects_descriptions_beyond_the_scratch():
+    # 256 blocks x 8 kv heads of partial-record slots need more than 32 MiB
+    d = api.make_desc(4, 40, 8, 128, 256, 5, 1 << 20, api.HW_BF16, 1e6, 128 ** -0.5)
+    need = api.attn_decode_workspace_size(d)
+    assert need > (32 << 20)
+    dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
+    st = api.lib().hw_attn_decode_noalloc(ctypes.byref(d), *([dummy.data_ptr()] * 12), None)
+    assert st == -3  # HW_ERR_WORKSPACE, nothing enqueued
