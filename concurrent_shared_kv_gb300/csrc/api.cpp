@@ -97,7 +97,7 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
   WorkspaceLayout L{};
   L.err_off = 0;
   L.counters_off = 256;
-  const size_t counters = static_cast<size_t>(d.n_rows) * d.n_kv_heads * sizeof(int32_t);
+  const size_t counters = static_cast<size_t>(d.n_rows) * d.n_q_heads * sizeof(int32_t);
   L.partials_off = L.counters_off + up(counters);
   L.slots = static_cast<int64_t>(d.n_blocks) * d.n_kv_heads + max_ctas;
   const size_t rec = static_cast<size_t>(kMaxQ) * (d.head_dim + 4) * sizeof(float);

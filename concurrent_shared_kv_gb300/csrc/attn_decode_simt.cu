@@ -24,10 +24,7 @@ struct SimtSmem {
   PlanCore plan;
   PlanScratch scratch;
   SegMeta meta;
-  MergeScratch merge;
-  int32_t merge_qhead[kMaxQ];
-  int32_t merge_flag[2];
-  int32_t merge_list[kMaxRecords];
+  MergeSmem merge;
   alignas(16) float q[kMaxQ][D + 4];
   alignas(16) float k[kSimtTile][D + 4];
   alignas(16) float v[kSimtTile][D + 4];
@@ -242,8 +239,7 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
     }
   }
   __syncthreads();
-  merge_phase<T, D>(a, P, S.merge, S.merge_qhead, S.merge_flag, S.merge_list, U, C, threadIdx.x,
-                    kSimtThreads, CtaSync(), 2000000000ll);
+  merge_phase<T, D>(a, P, S.merge, U, C, threadIdx.x, kSimtThreads, CtaSync(), 2000000000ll);
 }
 
 template <typename T, int D>

@@ -66,13 +66,9 @@ struct TcSmem {
   PlanCore plan;
   SegMeta meta;        // handed from the query warps to the softmax warps
   SegPre pre[kPre];    // query-side metadata of segments j (j < kPre) or j % kPre
-  MergeScratch merge;
   alignas(16) float red[2][kN][4];  // per tile: column maxima of the 4 softmax warps (read as float4)
   float lsave[2][4][kN];  // per segment parity: column sums of l of the 4 softmax warps
   float msave[2][kN];     // per segment parity: the reference maxima
-  int32_t merge_qhead[kMaxQ];
-  int32_t merge_flag[2];
-  int32_t merge_list[kMaxRecords];
   int32_t abort_flag;
   uint32_t tmem_base;
   alignas(8) uint64_t k_full[kStages];
@@ -695,8 +691,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  merge_phase<__nv_bfloat16, 128>(a, S.plan, S.merge, S.merge_qhead, S.merge_flag, S.merge_list,
-                                  U, C, tid, kThreads, CtaSync(), kWaitLimit);
+  // the merge scratch lives in the tile buffers: every copy and MMA is done
+  static_assert(sizeof(MergeSmem) <= kStageBytes, "merge scratch must fit in a stage");
+  merge_phase<__nv_bfloat16, 128>(a, S.plan, *reinterpret_cast<MergeSmem *>(S.stage[0]), U, C, tid,
+                                  kThreads, CtaSync(), kWaitLimit);
 }
 
 }  // namespace

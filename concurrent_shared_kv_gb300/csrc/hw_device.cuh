@@ -320,14 +320,17 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
   return v;
 }
 
-// One arrival on (row, kv head h) for every view entry referencing the
-// segment's block.  One thread calls it, after the group's record stores were
-// fenced (__threadfence by each writer) and synchronised.
+// One arrival on (row, q head) for every view entry referencing the
+// segment's block and every q head of kv head h (M.qhead).  One thread calls
+// it, after the group's record stores were ordered before it (a barrier the
+// writers took part in, or an mbarrier they arrived on).
 __device__ __forceinline__ void arrive_segment(const DecodeArgs &a, const SegMeta &M, int h) {
+  (void)h;
+  const int G = a.n_q_heads / a.n_kv_heads;
   __threadfence();
   for (int j = 0; j < M.n_ref && j < kMaxQ; ++j) {
     const int r = M.ref_entry[j] / a.n_view;
-    atomicAdd(&a.counters[r * a.n_kv_heads + h], 1);
+    for (int gi = 0; gi < G; ++gi) atomicAdd(&a.counters[r * a.n_q_heads + M.qhead[gi]], 1);
   }
 }
 
@@ -342,88 +345,97 @@ __device__ __forceinline__ void lse_combine(float &M, float &L, float m, float l
   }
 }
 
-// One warp merges every record of (row r, q head gi) - the records listed in
-// `list` (record index without the head: slot * 32 + rank * G):
-//   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
-//   lse = (M + log2 L) ln 2     (m, l, o of each record in the log2 domain)
-// Lane j owns elements [j * D/32, (j+1) * D/32).  All loads of a pass are
-// independent of each other, so they overlap instead of queueing.
-template <typename T, int D>
-__device__ void merge_head(const DecodeArgs &a, const int32_t *list, int n_rec, int r, int gi,
-                           int hq, int lane) {
-  constexpr int EPL = D / 32;
-  constexpr int64_t RS = D + 4;  // record stride in floats
-  // pass A: (M, L) over the records; the first 64 maxima stay in registers
-  float Mx = -INFINITY, Lx = 0.f;
-  float mreg[2] = {-INFINITY, -INFINITY};
-  for (int k = lane; k < n_rec; k += 32) {
-    const float *rec = a.partials + static_cast<int64_t>(list[k] + gi) * RS;
-    const float m = __ldcg(rec + D);
-    if (k < 64) mreg[k >> 5] = m;
-    lse_combine(Mx, Lx, m, __ldcg(rec + D + 1));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, Mx, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, Lx, o);
-    lse_combine(Mx, Lx, m2, l2);
-  }
-  // pass B: out = sum_i w_i o_i, every load of a chunk in flight at once
-  float acc[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  for (int base = 0; base < n_rec; base += 32) {
-    const int k = base + lane;
-    float wl = 0.f;
-    if (k < n_rec) {
-      const float m = (base < 64) ? mreg[base >> 5]
-                                  : __ldcg(a.partials + static_cast<int64_t>(list[k] + gi) * RS + D);
-      wl = ex2(m - Mx);
-    }
-    const int n = min(32, n_rec - base);
-#pragma unroll
-    for (int kk = 0; kk < 32; ++kk) {
-      if (kk < n) {
-        const float w = __shfl_sync(0xffffffffu, wl, kk);
-        const float *o = a.partials + static_cast<int64_t>(list[base + kk] + gi) * RS + lane * EPL;
-        if constexpr (EPL == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
-          acc[0] += w * x.x;
-          acc[1] += w * x.y;
-          acc[2] += w * x.z;
-          acc[3] += w * x.w;
-        } else {
-          const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
-          acc[0] += w * x.x;
-          acc[1] += w * x.y;
-        }
-      }
-    }
-  }
-  const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
-  const float inv = 1.f / Lx;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e)
-    reinterpret_cast<T *>(a.out)[ob * D + lane * EPL + e] = from_f32<T>(acc[e] * inv);
-  if (lane == 0 && a.lse) a.lse[ob] = (Mx + __log2f(Lx)) * 0.69314718055994530942f;
+// Shared scratch of the merge phase (at most ~20 KB; the tensor-core kernel
+// places it in its tile buffers, idle by then).
+struct MergeSmem {
+  MergeScratch X;
+  int32_t list[kMaxRecords];  // record index of each partial: slot * 32 + rank * G + gi
+  float mlist[kMaxRecords];   // its max m (log2 domain)
+  float acc[8][128];          // per warp partial sums of the output row
+  int32_t nb_before[HW_MAX_BLOCKS];  // blocks with tiles before b (segment ordinals)
+  int32_t rank_part[8];
+  int32_t n_rec, ok, rank;
+  float M, L;
+};
+
+// Ordinal of the segment that holds unit u, in unit order.
+__device__ __forceinline__ int seg_ordinal(const PlanCore &P, const MergeSmem &Z, int n_blocks,
+                                           int nb_total, int64_t u) {
+  const int64_t UH = P.ubase[n_blocks];
+  const int h = static_cast<int>(u / UH);
+  const int b = block_of_unit(P, n_blocks, u - static_cast<int64_t>(h) * UH);
+  return h * nb_total + Z.nb_before[b];
 }
 
-// The merge phase: every thread of the CTA calls it after the CTA's own
-// units.  qhead_s, flag_s (2 ints) and list (kMaxRecords ints) are shared
-// scratch.  Pairs without records were written as empty at the start and are
-// skipped here.
+// The merge phase.  Every thread of every CTA of the (cooperative) grid calls
+// it once its own units are done.  Work item = (row r, q head hq): all the
+// partial records of that output row, each from one (view entry, CTA) pair.
+// Items go to CTAs in order of how many segments they processed (idle and
+// lightly loaded CTAs first), so the merges do not queue behind the slowest
+// CTAs.  An item's owner prepares the record list, waits (bounded) until the
+// item's arrival counter shows every record, then merges with the whole CTA:
+//   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
+//   lse = (M + log2 L) ln 2.
 template <typename T, int D, typename Sync>
-__device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch &X,
-                            int32_t *qhead_s, int32_t *flag_s, int32_t *list, int64_t U, int C,
-                            int tid, int nt, Sync sync, long long wait_limit) {
+__device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeSmem &Z, int64_t U,
+                            int C, int tid, int nt, Sync sync, long long wait_limit) {
+  constexpr int EPL = D / 32;
+  constexpr int64_t RS = D + 4;  // record stride in floats
   const int V = a.n_view;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
   const int G = a.n_q_heads / a.n_kv_heads;
-  const int items = a.n_rows * a.n_kv_heads;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    const int r = it / a.n_kv_heads, h = it % a.n_kv_heads;
+  const int items = a.n_rows * a.n_q_heads;
+  const int grid = static_cast<int>(gridDim.x);
+  MergeScratch &X = Z.X;
+
+  // ---- this CTA's rank among the grid: fewer segments first, then index
+  if (tid < 32) {
+    int cnt = 0;
+    for (int base = 0; base < a.n_blocks; base += 32) {
+      const int b = base + lane;
+      const bool ne = b < a.n_blocks && P.tiles[b] > 0;
+      const unsigned m = __ballot_sync(0xffffffffu, ne);
+      if (b < a.n_blocks) Z.nb_before[b] = cnt + __popc(m & ((1u << lane) - 1u));
+      cnt += __popc(m);
+    }
+    if (lane == 0) Z.n_rec = cnt;  // number of non-empty blocks, for the ordinals
+  }
+  sync();
+  const int nb_total = Z.n_rec;
+  auto nseg_of = [&](int c) -> int {
+    if (U == 0 || c >= C) return 0;
+    const int64_t u0 = cta_unit_begin(U, c, C), u1 = cta_unit_begin(U, c + 1, C);
+    return seg_ordinal(P, Z, a.n_blocks, nb_total, u1 - 1) - seg_ordinal(P, Z, a.n_blocks, nb_total, u0) + 1;
+  };
+  const int me = blockIdx.x;
+  const int my_n = nseg_of(me);
+  int before = 0;
+  for (int c = tid; c < grid; c += nt) {
+    const int nc = nseg_of(c);
+    before += (nc < my_n || (nc == my_n && c < me)) ? 1 : 0;
+  }
+  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+  if (lane == 0) Z.rank_part[warp] = before;
+  sync();
+  if (tid == 0) {
+    int rk = 0;
+    for (int w2 = 0; w2 < nwarps; ++w2) rk += Z.rank_part[w2];
+    Z.rank = rk;
+  }
+  sync();
+  const int rank = Z.rank;
+
+  for (int it = rank; it < items; it += grid) {
+    const int r = it / a.n_q_heads, hq = it % a.n_q_heads;
+    int h = hq / G, gi = hq % G;
+    if (a.q_to_kv) {
+      h = a.q_to_kv[hq];
+      gi = 0;
+      for (int q2 = 0; q2 < hq; ++q2) gi += (a.q_to_kv[q2] == h);
+      if (h < 0 || h >= a.n_kv_heads || gi >= G) continue;  // flagged by the plan
+    }
     const int expected = expected_records(a, P, r, h, U, C);
-    if (expected == 0) continue;
+    if (expected == 0) continue;  // written as empty at the start
     if (warp == 0) {
       // per view entry: its block's segment, the CTA range that wrote records,
       // and its rank among the entries that reference the same block
@@ -445,7 +457,7 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch
         const int x = (i < E) ? a.view_block[i] : -2;
         for (int v = 0; v < V; ++v) {
           const int e = r * V + v;
-          const int b = __shfl_sync(0xffffffffu, x, (e - base) & 31);  // valid when e in chunk
+          const int b = __shfl_sync(0xffffffffu, x, (e - base) & 31);
           const int bb = (e >= base && e < base + 32) ? b : a.view_block[e];
           const unsigned m = __ballot_sync(0xffffffffu, i < e && x == bb);
           if (lane == 0) X.mv_qi[v] += __popc(m);
@@ -457,10 +469,10 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch
       for (int v = 0; v < V; ++v) {
         if (X.mv_seg[v] < 0) continue;
         const int c0 = X.mv_c0[v], cnt = X.mv_c1[v] - c0 + 1;
-        const int base_rec = X.mv_qi[v] * G;
+        const int base_rec = X.mv_qi[v] * G + gi;
         for (int j = lane; j < cnt; j += 32)
           if (off + j < kMaxRecords)
-            list[off + j] = static_cast<int32_t>((X.mv_seg[v] + c0 + j) * kMaxQ + base_rec);
+            Z.list[off + j] = static_cast<int32_t>((X.mv_seg[v] + c0 + j) * kMaxQ + base_rec);
         off += cnt;
       }
       if (lane == 0) {
@@ -468,27 +480,11 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch
           flag_error(a.err, HW_DEV_TOO_MANY_REFS);
           off = kMaxRecords;
         }
-        flag_s[1] = off;
-      }
-      // the q heads of kv head h
-      if (!a.q_to_kv) {
-        for (int i = lane; i < G; i += 32) qhead_s[i] = h * G + i;
-      } else {
-        int cnt = 0;
-        for (int base = 0; base < a.n_q_heads; base += 32) {
-          const int hq = base + lane;
-          const bool mm = hq < a.n_q_heads && a.q_to_kv[hq] == h;
-          const unsigned mask = __ballot_sync(0xffffffffu, mm);
-          const int pos = cnt + __popc(mask & ((1u << lane) - 1u));
-          if (mm && pos < G) qhead_s[pos] = hq;
-          cnt += __popc(mask);
-        }
+        Z.n_rec = off;
       }
     }
-    sync();
-    // the setup above only needs metadata; now wait for the records
     if (tid == 0) {
-      // every record of the pair is delivered (bounded wait: co-resident CTAs)
+      // every record of the item is delivered (bounded wait: co-resident CTAs)
       const int32_t *ctr = a.counters + it;
       bool ok = ld_acquire_gpu(ctr) >= expected;
       if (!ok) {
@@ -499,12 +495,63 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeScratch
         }
       }
       if (!ok) flag_error(a.err, HW_DEV_TIMEOUT);
-      flag_s[0] = ok ? 1 : 0;
+      Z.ok = ok ? 1 : 0;
     }
     sync();
-    if (flag_s[0]) {
-      const int n_rec = flag_s[1];
-      for (int gi = warp; gi < G; gi += nwarps) merge_head<T, D>(a, list, n_rec, r, gi, qhead_s[gi], lane);
+    const int n_rec = Z.n_rec;
+    if (Z.ok) {
+      if (warp == 0) {  // pass A: the maxima and the normaliser
+        float Mx = -INFINITY, Lx = 0.f;
+        for (int k = lane; k < n_rec; k += 32) {
+          const float *rec = a.partials + static_cast<int64_t>(Z.list[k]) * RS;
+          const float m = __ldcg(rec + D);
+          Z.mlist[k] = m;
+          lse_combine(Mx, Lx, m, __ldcg(rec + D + 1));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, Mx, o);
+          const float l2 = __shfl_xor_sync(0xffffffffu, Lx, o);
+          lse_combine(Mx, Lx, m2, l2);
+        }
+        if (lane == 0) {
+          Z.M = Mx;
+          Z.L = Lx;
+        }
+      }
+      sync();
+      // pass B: warp w takes records w, w + nwarps, ...; lane j owns elements
+      // [j * EPL, (j+1) * EPL) of the row
+      const float Mx = Z.M;
+      float acc[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
+      for (int k = warp; k < n_rec; k += nwarps) {
+        const float w = ex2(Z.mlist[k] - Mx);
+        const float *o = a.partials + static_cast<int64_t>(Z.list[k]) * RS + lane * EPL;
+        if constexpr (EPL == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
+          acc[0] += w * x.x;
+          acc[1] += w * x.y;
+          acc[2] += w * x.z;
+          acc[3] += w * x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
+          acc[0] += w * x.x;
+          acc[1] += w * x.y;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) Z.acc[warp][lane * EPL + e] = acc[e];
+      sync();
+      if (tid < D) {
+        float sum = 0.f;
+        for (int w2 = 0; w2 < nwarps; ++w2) sum += Z.acc[w2][tid];
+        const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
+        reinterpret_cast<T *>(a.out)[ob * D + tid] = from_f32<T>(sum / Z.L);
+        if (tid == 0 && a.lse) a.lse[ob] = (Z.M + __log2f(Z.L)) * 0.69314718055994530942f;
+      }
     }
     sync();
     if (tid == 0) a.counters[it] = 0;  // re-armed for the next call

@@ -33,7 +33,7 @@ struct DecodeArgs {
   void *out;
   float *lse;
   int32_t *err;       // workspace error word (HW_DEV_* bits)
-  int32_t *counters;  // [n_rows][Hkv] merge arrival counters, zero between calls
+  int32_t *counters;  // [n_rows][Hq] merge arrival counters, zero between calls
   float *partials;    // [slots][kMaxQ][D + 4]: o[0..D), m at D, l at D+1
   int32_t n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
   int64_t capacity;
