@@ -116,6 +116,7 @@ static int check_desc(const hw_attn_desc *d) {
   if (!std::isfinite(d->scale)) return HW_ERR_INVALID;
   if (d->head_dim != 64 && d->head_dim != 128) return HW_ERR_UNSUPPORTED;
   if (d->n_blocks > HW_MAX_BLOCKS) return HW_ERR_UNSUPPORTED;
+  if (d->n_q_heads > HW_MAX_Q_HEADS) return HW_ERR_UNSUPPORTED;
   if (d->max_view_blocks > HW_MAX_VIEW_BLOCKS) return HW_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->n_rows) * d->max_view_blocks > HW_MAX_VIEW_ENTRIES)
     return HW_ERR_UNSUPPORTED;

@@ -22,6 +22,7 @@ constexpr int kSimtThreads = 256;
 template <int D>
 struct SimtSmem {
   PlanCore plan;
+  MetaCache cache;
   PlanScratch scratch;
   SegMeta meta;
   MergeSmem merge;
@@ -86,15 +87,14 @@ __device__ __forceinline__ void load_tile(const DecodeArgs &a, SimtSmem<D> &S, i
 }
 
 template <typename T, int D>
-__device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, int t0, int t1,
-                             int64_t U, int C) {
+__device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, int t0, int t1) {
   PlanCore &P = S.plan;
   SegMeta &M = S.meta;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = a.n_q_heads / a.n_kv_heads;
   if (warp == 0) {
-    gather_refs(a, M, b, lane);
-    gather_qheads(a, M, h, lane);
+    gather_refs(a, S.cache, M, b, lane);
+    gather_qheads(a, S.cache, M, h, lane);
   }
   __syncthreads();
   const int nq = M.n_ref * G;  // <= kMaxQ: blocks with more are skipped by the plan
@@ -105,7 +105,7 @@ __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, 
     const int e = M.ref_entry[qi / G];
     const int r = e / a.n_view;
     const int hq = M.qhead[qi % G];
-    const int64_t rel = static_cast<int64_t>(a.q_pos[r]) - a.view_offset[e];
+    const int64_t rel = entry_rel(a, S.cache, e);
     const T *qp = reinterpret_cast<const T *>(a.q) + (static_cast<int64_t>(r) * a.n_q_heads + hq) * D;
     const float x0 = to_f32<T>(qp[i]), x1 = to_f32<T>(qp[i + D / 2]);
     float cs, sn;
@@ -203,7 +203,7 @@ __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, 
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) arrive_segment(a, M, h);
+  if (tid == 0) arrive_segment(a, M);
   __syncthreads();  // the segment metadata is rewritten by the next segment
 }
 
@@ -212,34 +212,19 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem<D> &S = *reinterpret_cast<SimtSmem<D> *>(smem_raw);
   PlanCore &P = S.plan;
-  build_plan<kSimtTile>(a, P, S.scratch);
+  build_plan<kSimtTile>(a, P, S.cache, S.scratch);
   const int c = blockIdx.x;
-  const int64_t U = total_units(P, a);
-  const int C = static_cast<int>(U < gridDim.x ? U : gridDim.x);  // working CTAs
-
-  // (row, kv head) pairs without any record: out = 0, lse = -inf
-  for (int rh = c; rh < a.n_rows * a.n_kv_heads; rh += gridDim.x) {
-    const int r = rh / a.n_kv_heads, h = rh % a.n_kv_heads;
-    if (expected_records(a, P, r, h, U, C) == 0) {
-      if (threadIdx.x < 32) gather_qheads(a, S.meta, h, threadIdx.x);
-      __syncthreads();
-      write_empty<T>(a, S.meta.qhead, r, threadIdx.x, kSimtThreads);
-      __syncthreads();
-    }
-  }
-  if (U > 0 && c < C) {
-    int64_t u = cta_unit_begin(U, c, C);
-    const int64_t u_end = cta_unit_begin(U, c + 1, C);
-    while (u < u_end) {
-      const UnitPos x = unit_pos(P, a.n_blocks, u);
-      const int64_t seg_stop = min(x.seg_first + x.tiles, u_end);
-      simt_segment<T, D>(a, S, x.b, x.h, static_cast<int>(u - x.seg_first),
-                         static_cast<int>(seg_stop - x.seg_first), U, C);
-      u = seg_stop;
-    }
+  int64_t u = cta_unit_begin(P, a.n_blocks, c);
+  const int64_t u_end = cta_unit_begin(P, a.n_blocks, c + 1);
+  while (u < u_end) {
+    const UnitPos x = unit_pos(P, a.n_blocks, u);
+    const int64_t seg_stop = min(x.seg_first + x.tiles, u_end);
+    simt_segment<T, D>(a, S, x.b, x.h, static_cast<int>(u - x.seg_first),
+                       static_cast<int>(seg_stop - x.seg_first));
+    u = seg_stop;
   }
   __syncthreads();
-  merge_phase<T, D>(a, P, S.merge, U, C, threadIdx.x, kSimtThreads, CtaSync(), 2000000000ll);
+  merge_phase<T, D>(a, P, S.cache, S.merge, threadIdx.x, kSimtThreads, CtaSync(), 2000000000ll);
 }
 
 template <typename T, int D>

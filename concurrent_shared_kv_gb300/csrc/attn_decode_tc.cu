@@ -50,22 +50,19 @@ constexpr float kLazy = 8.f;                  // rescale only when the max grows
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
 constexpr int kPre = 4;  // segments whose metadata the prologue prepares
-
-// A segment's query-side metadata: view references, q heads, and for each
-// reference its row and relative rotation i_q - offset.
-struct SegPre {
-  SegMeta m;
-  int32_t h;  // kv head of the segment
-  int32_t qrow[kMaxQ];
-  int64_t qrel[kMaxQ];
-};
+// Named barriers: 1 softmax warps, 2 query warps, 3 prologue warps,
+// 4 prologue warps + TMA warp (the queries of segment 0 are requested before
+// the first K/V tile, so that they do not queue behind the tile stream).
+constexpr int kBarQIssued = 4;
 
 struct TcSmem {
   alignas(1024) uint8_t stage[kStages][kStageBytes];
   alignas(1024) uint8_t q[kQBytes];
   PlanCore plan;
+  MetaCache cache;
   SegMeta meta;        // handed from the query warps to the softmax warps
-  SegPre pre[kPre];    // query-side metadata of segments j (j < kPre) or j % kPre
+  SegMeta pre[kPre];   // query-side metadata of segment j in pre[j % kPre]
+  int32_t pre_count;   // segments among the first kPre that exist
   alignas(16) float red[2][kN][4];  // per tile: column maxima of the 4 softmax warps (read as float4)
   float lsave[2][4][kN];  // per segment parity: column sums of l of the 4 softmax warps
   float msave[2][kN];     // per segment parity: the reference maxima
@@ -239,62 +236,72 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
   mbar_wait(&S.mma_done, 0);
 }
 
-// Query-side metadata of segment (b, h) into X, by one warp.
-__device__ void seg_pre(const DecodeArgs &a, SegPre &X, int b, int h, int lane) {
-  if (lane == 0) X.h = h;
-  gather_refs(a, X.m, b, lane);
-  gather_qheads(a, X.m, h, lane);
-  __syncwarp();
-  for (int j = lane; j < X.m.n_ref && j < kMaxQ; j += 32) {
-    const int e = X.m.ref_entry[j];
-    const int r = e / a.n_view;
-    X.qrow[j] = r;
-    X.qrel[j] = static_cast<int64_t>(a.q_pos[r]) - a.view_offset[e];
-  }
+// Query-side metadata of segment (b, h) into X, by one warp (shared memory only).
+__device__ void seg_pre(const DecodeArgs &a, const TcSmem &S, SegMeta &X, int b, int h, int lane) {
+  gather_refs(a, S.cache, X, b, lane);
+  gather_qheads(a, S.cache, X, h, lane);
   __syncwarp();
 }
 
-// One item of the rotated queries: head qi, elements 8c..8c+7 and their
-// RoPE partners 64+8c..64+8c+7, rotated by the reference's i_q - offset and
-// scaled by scale * log2(e) (scores leave the MMA in log2 units), then split
-// into bf16 hi and lo parts.  out[0..3]: hi of d 8c.., hi of d 64+8c.., lo of
-// d 8c.., lo of d 64+8c.. (16 bytes each).
-__device__ __forceinline__ void rot_item(const DecodeArgs &a, const SegPre &X, int qi, int c,
-                                         int nq, int G, uint4 (&out)[4]) {
-  uint32_t w[4][4];
-  if (qi < nq) {
+// Warms L2 with the queries of segment X (one warp, one 256-byte row each).
+__device__ __forceinline__ void prefetch_q(const DecodeArgs &a, const SegMeta &X, int lane) {
+  const int G = a.n_q_heads / a.n_kv_heads;
+  if (lane < X.n_ref * G && lane < kN) {
+    const int r = X.ref_entry[lane / G] / a.n_view;
     const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
-                              (static_cast<int64_t>(X.qrow[qi / G]) * a.n_q_heads + X.m.qhead[qi % G]) * 128;
-    const uint4 xl = __ldg(reinterpret_cast<const uint4 *>(qp + 8 * c));
-    const uint4 xh = __ldg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * c));
-    const uint32_t lo32[4] = {xl.x, xl.y, xl.z, xl.w}, hi32[4] = {xh.x, xh.y, xh.z, xh.w};
-    const int64_t rel = X.qrel[qi / G];
+                              (static_cast<int64_t>(r) * a.n_q_heads + X.qhead[lane % G]) * 128;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" ::"l"(qp) : "memory");
+  }
+}
+
+// One item of the rotated queries: head qi, elements 8c..8c+7 and their RoPE
+// partners 64+8c..64+8c+7, and the reference's rotation i_q - offset.
+// Columns past nq load nothing and rotate to zeros.
+struct QItem {
+  uint4 lo, hi;
+  int64_t rel;
+};
+__device__ __forceinline__ void load_item(const DecodeArgs &a, const TcSmem &S, const SegMeta &X,
+                                          int qi, int c, int nq, int G, QItem &it) {
+  it.lo = it.hi = make_uint4(0, 0, 0, 0);
+  it.rel = 0;
+  if (qi < nq) {
+    const int e = X.ref_entry[qi / G];
+    const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
+                              (static_cast<int64_t>(e / a.n_view) * a.n_q_heads + X.qhead[qi % G]) * 128;
+    it.lo = __ldg(reinterpret_cast<const uint4 *>(qp + 8 * c));
+    it.hi = __ldg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * c));
+    it.rel = entry_rel(a, S.cache, e);
+  }
+}
+
+// The item rotated and scaled by scale * log2(e) (scores leave the MMA in
+// log2 units), then split into bf16 hi and lo parts.  out[0..3]: hi of d
+// 8c.., hi of d 64+8c.., lo of d 8c.., lo of d 64+8c.. (16 bytes each).
+__device__ __forceinline__ void rot_item(const DecodeArgs &a, const QItem &it, int c, uint4 (&out)[4]) {
+  const uint32_t lo32[4] = {it.lo.x, it.lo.y, it.lo.z, it.lo.w};
+  const uint32_t hi32[4] = {it.hi.x, it.hi.y, it.hi.z, it.hi.w};
+  uint32_t w[4][4];
 #pragma unroll
-    for (int e2 = 0; e2 < 4; ++e2) {
-      float ylo[2], yhi[2];
+  for (int e2 = 0; e2 < 4; ++e2) {
+    float ylo[2], yhi[2];
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const float x0 = __uint_as_float(h2 ? (lo32[e2] & 0xffff0000u) : (lo32[e2] << 16));
-        const float x1 = __uint_as_float(h2 ? (hi32[e2] & 0xffff0000u) : (hi32[e2] << 16));
-        float cs, sn;
-        rope_cos_sin(rel, a.phase[8 * c + 2 * e2 + h2], &cs, &sn);
-        ylo[h2] = (x0 * cs - x1 * sn) * a.scale_log2;
-        yhi[h2] = (x1 * cs + x0 * sn) * a.scale_log2;
-      }
-      const __nv_bfloat162 hl = __floats2bfloat162_rn(ylo[0], ylo[1]);
-      const __nv_bfloat162 hh = __floats2bfloat162_rn(yhi[0], yhi[1]);
-      const __nv_bfloat162 ll = __floats2bfloat162_rn(ylo[0] - __low2float(hl), ylo[1] - __high2float(hl));
-      const __nv_bfloat162 lh = __floats2bfloat162_rn(yhi[0] - __low2float(hh), yhi[1] - __high2float(hh));
-      w[0][e2] = *reinterpret_cast<const uint32_t *>(&hl);
-      w[1][e2] = *reinterpret_cast<const uint32_t *>(&hh);
-      w[2][e2] = *reinterpret_cast<const uint32_t *>(&ll);
-      w[3][e2] = *reinterpret_cast<const uint32_t *>(&lh);
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const float x0 = __uint_as_float(h2 ? (lo32[e2] & 0xffff0000u) : (lo32[e2] << 16));
+      const float x1 = __uint_as_float(h2 ? (hi32[e2] & 0xffff0000u) : (hi32[e2] << 16));
+      float cs, sn;
+      rope_cos_sin(it.rel, a.phase[8 * c + 2 * e2 + h2], &cs, &sn);
+      ylo[h2] = (x0 * cs - x1 * sn) * a.scale_log2;
+      yhi[h2] = (x1 * cs + x0 * sn) * a.scale_log2;
     }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-      for (int e2 = 0; e2 < 4; ++e2) w[k][e2] = 0;
+    const __nv_bfloat162 hl = __floats2bfloat162_rn(ylo[0], ylo[1]);
+    const __nv_bfloat162 hh = __floats2bfloat162_rn(yhi[0], yhi[1]);
+    const __nv_bfloat162 ll = __floats2bfloat162_rn(ylo[0] - __low2float(hl), ylo[1] - __high2float(hl));
+    const __nv_bfloat162 lh = __floats2bfloat162_rn(yhi[0] - __low2float(hh), yhi[1] - __high2float(hh));
+    w[0][e2] = *reinterpret_cast<const uint32_t *>(&hl);
+    w[1][e2] = *reinterpret_cast<const uint32_t *>(&hh);
+    w[2][e2] = *reinterpret_cast<const uint32_t *>(&ll);
+    w[3][e2] = *reinterpret_cast<const uint32_t *>(&lh);
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) out[k] = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
@@ -310,9 +317,16 @@ __device__ __forceinline__ void store_item(uint32_t qbase, int qi, int c, const 
   st_shared_v4(qbase + kQPart + kQHalf + off, v[3].x, v[3].y, v[3].z, v[3].w);
 }
 
+// First unit after the segment that holds unit u.
+__device__ __forceinline__ int64_t next_segment(const TcSmem &S, int n_blocks, int64_t u) {
+  const UnitPos x = unit_pos(S.plan, n_blocks, u);
+  return x.seg_first + x.tiles;
+}
+
 // Prologue of warps 2-7 (the TMA and MMA warps start at once): the metadata
-// of the CTA's first kPre segments (one warp each) and the rotated queries of
-// segment 0.
+// of the CTA's first kPre segments (one warp each), then the queries of
+// segment 0 - requested before the TMA warp starts the K/V stream - rotated
+// into the Q~ buffer.
 __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int t = threadIdx.x - kWarpSoft * 32;  // 0..191
   const int w = t >> 5, lane = t & 31;
@@ -320,29 +334,38 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
   NamedSync<3, 192> sync;
   if (w < kPre) {
     int64_t u = u0;
-    for (int k = 0; k < w && u < u1; ++k) {
-      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-      u = x.seg_first + x.tiles;
-    }
+    for (int k = 0; k < w && u < u1; ++k) u = next_segment(S, a.n_blocks, u);
     if (u < u1) {
       const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-      seg_pre(a, S.pre[w], x.b, x.h, lane);
+      seg_pre(a, S, S.pre[w], x.b, x.h, lane);
     }
+    if (lane == 0 && u < u1) atomicMax(&S.pre_count, w + 1);
   }
   sync();
-  const SegPre &X = S.pre[0];
-  const int nq = min(X.m.n_ref * G, kN);
+  const SegMeta &X = S.pre[0];
+  const int nq = min(X.n_ref * G, kN);
+  // items t and t + 192 of the kN * 8 (head, 16-byte chunk) items
+  QItem q0, q1;
+  load_item(a, S, X, t >> 3, t & 7, nq, G, q0);
+  const bool two = t + 192 < kN * 8;
+  if (two) load_item(a, S, X, (t + 192) >> 3, (t + 192) & 7, nq, G, q1);
+  asm volatile("bar.arrive %0, %1;" ::"n"(kBarQIssued), "n"(224) : "memory");
   const uint32_t qbase = smem_u32(S.q);
-  for (int item = t; item < kN * 8; item += 192) {
+  {
     uint4 v[4];
-    rot_item(a, X, item >> 3, item & 7, nq, G, v);
-    store_item(qbase, item >> 3, item & 7, v);
+    rot_item(a, q0, t & 7, v);
+    store_item(qbase, t >> 3, t & 7, v);
+  }
+  if (two) {
+    uint4 v[4];
+    rot_item(a, q1, (t + 192) & 7, v);
+    store_item(qbase, (t + 192) >> 3, (t + 192) & 7, v);
   }
   for (int j = t; j < kMaxQ; j += 192) {
-    S.meta.ref_entry[j] = X.m.ref_entry[j];
-    S.meta.qhead[j] = X.m.qhead[j];
+    S.meta.ref_entry[j] = X.ref_entry[j];
+    S.meta.qhead[j] = X.qhead[j];
   }
-  if (t == 0) S.meta.n_ref = X.m.n_ref;
+  if (t == 0) S.meta.n_ref = X.n_ref;
   fence_proxy_async_smem();
   sync();
   if (t == 0) mbar_arrive(&S.q_full);  // phase 0: segment 0
@@ -350,16 +373,17 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
 
 // Rotated queries of segments 1, 2, ... (segment 0 came from the prologue),
 // and the arrivals of finished segments.  The values of segment j are loaded
-// and computed in registers while the tensor cores still work on segment
-// j - 1; they are written once the single Q~ buffer is released.  Then the
-// warps count segment j - 2's records (fence + one atomic per view
-// reference): two segments late, so that neither these global-memory
-// operations nor the softmax warps' record stores sit on the path of the
-// next rotated queries.  Segment k's metadata stays in pre[k % kPre] until
-// segment k + kPre is prepared, well after its arrivals.
+// (from L2: prefetched two segments ahead) and computed in registers while
+// the tensor cores still work on segment j - 1; they are written once the
+// single Q~ buffer is released.  Then the warps count segment j - 2's
+// records (fence + one atomic per view reference and q head): two segments
+// late, so that neither these global-memory operations nor the softmax
+// warps' record stores sit on the path of the next rotated queries.  Last,
+// the metadata of segment j + 2 goes into the slot segment j - 2 vacated,
+// and its queries are prefetched into L2.
 __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wq = tq >> 5;
   const int G = a.n_q_heads / a.n_kv_heads;
   NamedSync<2, 64> sync;
   const uint32_t qbase = smem_u32(S.q);
@@ -367,47 +391,57 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
     // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
     // warps keep the same control flow so the named barrier stays balanced.
     wait_or_abort(S, a, &S.rec_ready[done & 3], (done >> 2) & 1);
-    if (tq == 0) arrive_segment(a, S.pre[done % kPre].m, S.pre[done % kPre].h);
+    if (tq == 0) arrive_segment(a, S.pre[done % kPre]);
   };
-  int64_t u = u0;
-  {
-    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-    u = x.seg_first + x.tiles;  // segment 0 came from the prologue
-  }
+  for (int k = 1 + wq; k < S.pre_count; k += 2) prefetch_q(a, S.pre[k], lane);
+  int64_t u = next_segment(S, a.n_blocks, u0);  // segment 1
+  int64_t u_prep = u;                            // segment kPre: the next to prepare
+  for (int k = 1; k < kPre && u_prep < u1; ++k) u_prep = next_segment(S, a.n_blocks, u_prep);
   for (int seg = 1;; ++seg) {
     if (u >= u1) {  // no segment seg: the last arrivals
       if (seg >= 2) arrivals(seg - 2);
       arrivals(seg - 1);
       break;
     }
-    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-    SegPre &X = S.pre[seg % kPre];
-    if (seg >= kPre) {
-      if (tq < 32) seg_pre(a, X, x.b, x.h, lane);
-      sync();
-    }
-    const int nq = min(X.m.n_ref * G, kN);
+    const SegMeta &X = S.pre[seg % kPre];
+    const int nq = min(X.n_ref * G, kN);
     // items tq + 64 k: head (tq >> 3) + 8 k, chunk tq & 7
+    QItem raw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) load_item(a, S, X, (tq >> 3) + 8 * k, tq & 7, nq, G, raw[k]);
     uint4 v[4][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) rot_item(a, X, (tq >> 3) + 8 * k, tq & 7, nq, G, v[k]);
+    for (int k = 0; k < 4; ++k) rot_item(a, raw[k], tq & 7, v[k]);
     // The Q~ buffer and the hand-off metadata are free once segment seg-1's
     // QK products completed and every softmax warp read the hand-off.
     wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
     if (tq < 32) {
       for (int j = lane; j < kMaxQ; j += 32) {
-        S.meta.ref_entry[j] = X.m.ref_entry[j];
-        S.meta.qhead[j] = X.m.qhead[j];
+        S.meta.ref_entry[j] = X.ref_entry[j];
+        S.meta.qhead[j] = X.qhead[j];
       }
-      if (lane == 0) S.meta.n_ref = X.m.n_ref;
+      if (lane == 0) S.meta.n_ref = X.n_ref;
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
     fence_proxy_async_smem();
     sync();
     if (tq == 0) mbar_arrive(&S.q_full);
-    if (seg >= 2) arrivals(seg - 2);
-    u = x.seg_first + x.tiles;
+    if (seg >= 2) {
+      arrivals(seg - 2);
+      sync();  // the slot of segment seg - 2 is read; it now takes segment seg + 2
+      if (u_prep < u1) {
+        const UnitPos x = unit_pos(S.plan, a.n_blocks, u_prep);
+        SegMeta &N = S.pre[(seg + 2) % kPre];
+        if (wq == 0) {
+          seg_pre(a, S, N, x.b, x.h, lane);
+          prefetch_q(a, N, lane);
+        }
+        u_prep = x.seg_first + x.tiles;
+      }
+      sync();
+    }
+    u = next_segment(S, a.n_blocks, u);
   }
 }
 
@@ -473,7 +507,9 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   // thread of the group keeps the same control flow, so the named barriers
   // below are always reached by all 128 threads; after an abort no wait
   // blocks any more and the CTA runs to its end on stale data.
-  float m_run[kN], l_part[kN];
+  // m_run[j]: reference max of column j (the same in every lane); m_mine:
+  // the one of column `lane`, from which the others are broadcast
+  float m_run[kN], l_part[kN], m_mine = -INFINITY;
   int seg = -1, nq = 0;
   int pend = -1, pend_b = 0, pend_h = 0, pend_nq = 0;  // segment whose records are due
   for (int i = 0; i < n; ++i) {
@@ -491,6 +527,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
         m_run[j] = -INFINITY;
         l_part[j] = 0.f;
       }
+      m_mine = -INFINITY;
     }
     const int sb = i & 1, s = i % kStages;
     wait_or_abort(S, a, &S.s_full[sb], (i >> 1) & 1);
@@ -525,18 +562,19 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       transpose_reduce<true>(v, lane);
       red[lane][ws] = v[0];
       sync();
+      // lane j: the tile maximum of column j over the four warps, the new
+      // reference and its rescale factor (0 when the old one was -inf);
+      // then every lane takes all 32 by shuffles
+      const float4 t4 = *reinterpret_cast<const float4 *>(red[lane]);
+      const float tmax = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
+      const float m_old = m_mine;
+      if (lane < nq && tmax > m_old + kLazy) m_mine = tmax;
+      const float a_mine = (m_mine == m_old) ? 1.f : ex2(m_old - m_mine);
       float alpha[kN];
 #pragma unroll
       for (int j = 0; j < kN; ++j) {
-        alpha[j] = 1.f;
-        if (j < nq) {
-          const float4 t4 = *reinterpret_cast<const float4 *>(red[j]);
-          const float tmax = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
-          if (tmax > m_run[j] + kLazy) {
-            alpha[j] = ex2(m_run[j] - tmax);  // 0 when m_run = -inf
-            m_run[j] = tmax;
-          }
-        }
+        m_run[j] = __shfl_sync(0xffffffffu, m_mine, j);
+        alpha[j] = __shfl_sync(0xffffffffu, a_mine, j);
         l_part[j] *= alpha[j];
       }
       if (!first) {
@@ -599,13 +637,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       for (int j = 0; j < kN; ++j) v[j] = l_part[j];
       transpose_reduce<false>(v, lane);
       S.lsave[seg & 1][ws][lane] = v[0];
-      if (ws == 0) {
-        float mcol = 0.f;
-#pragma unroll
-        for (int j = 0; j < kN; ++j)
-          if (j == lane) mcol = m_run[j];
-        S.msave[seg & 1][lane] = mcol;
-      }
+      if (ws == 0) S.msave[seg & 1][lane] = m_mine;
       pend = seg;
       pend_b = x.b;
       pend_h = x.h;
@@ -644,6 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 4; ++b) mbar_init(&S.rec_ready[b], 4);  // one per softmax warp
     mbar_init(&S.mma_done, 1);
     S.abort_flag = 0;
+    S.pre_count = 0;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -651,29 +684,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   // the plan scratch borrows stage 0, which no copy has touched yet
-  build_plan<kT>(a, S.plan, *reinterpret_cast<PlanScratch *>(S.stage[0]));
+  build_plan<kT>(a, S.plan, S.cache, *reinterpret_cast<PlanScratch *>(S.stage[0]));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   const int c = blockIdx.x;
-  const int64_t U = total_units(S.plan, a);
-  const int C = static_cast<int>(U < gridDim.x ? U : gridDim.x);
-
-  // (row, kv head) pairs without any record: out = 0, lse = -inf
-  for (int rh = c; rh < a.n_rows * a.n_kv_heads; rh += gridDim.x) {
-    const int r = rh / a.n_kv_heads, h = rh % a.n_kv_heads;
-    if (expected_records(a, S.plan, r, h, U, C) == 0) {
-      if (warp == 0) gather_qheads(a, S.meta, h, lane);
-      __syncthreads();
-      write_empty<__nv_bfloat16>(a, S.meta.qhead, r, tid, kThreads);
-      __syncthreads();
-    }
-  }
-
-  if (U > 0 && c < C) {
-    const int64_t u0 = cta_unit_begin(U, c, C), u1 = cta_unit_begin(U, c + 1, C);
+  const int64_t u0 = cta_unit_begin(S.plan, a.n_blocks, c);
+  const int64_t u1 = cta_unit_begin(S.plan, a.n_blocks, c + 1);
+  if (u0 < u1) {
     if (warp == kWarpTma) {
+      // the first K/V tiles go out behind the queries of segment 0
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarQIssued), "n"(224) : "memory");
       if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1);
     } else if (warp == kWarpMma) {
       if (lane == 0) mma_issuer(a, S, tmem, u0, u1);
@@ -693,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // the merge scratch lives in the tile buffers: every copy and MMA is done
   static_assert(sizeof(MergeSmem) <= kStageBytes, "merge scratch must fit in a stage");
-  merge_phase<__nv_bfloat16, 128>(a, S.plan, *reinterpret_cast<MergeSmem *>(S.stage[0]), U, C, tid,
-                                  kThreads, CtaSync(), kWaitLimit);
+  merge_phase<__nv_bfloat16, 128>(a, S.plan, S.cache, *reinterpret_cast<MergeSmem *>(S.stage[0]),
+                                  tid, kThreads, CtaSync(), kWaitLimit);
 }
 
 }  // namespace

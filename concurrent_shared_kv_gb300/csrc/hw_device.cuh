@@ -1,5 +1,5 @@
-// hw_device.cuh - device code shared by the decode kernels: the work plan
-// (KV split evenly over the CTAs), query rotation, partial records and the
+// hw_device.cuh - device code shared by the decode kernels: the metadata
+// cache, the work plan (KV split over the CTAs), partial records and the
 // log-sum-exp merge.
 //
 // Scheduling (omica.com.cn article, section 3.2: the KV cache is split evenly
@@ -9,20 +9,32 @@
 //   head); only blocks that some view references take part.  Head-major
 //   order keeps each head's short worker blocks next to its long common
 //   block, instead of stacking every head's short blocks on the last CTAs.
-//   CTA c of C owns units [floor(c U / C), floor((c+1) U / C)), so every CTA
-//   streams the same number of tiles whatever the block lengths are.  C is
-//   min(grid, U): every working CTA owns at least one unit, so the CTAs that
-//   touch a segment form one contiguous range.
 //   segment   = the units of one (block, kv head), id seg = h * n_blocks + b,
-//   increasing along the unit order; a CTA emits one partial record per
-//   (segment it touched, query head served) into slot seg + c, which is
-//   unique because seg and c never both stay put as units advance.
-//   Every delivered record bumps the arrival counter of its (row, kv head).
-//   The launch is cooperative (all CTAs resident at once): after its own
-//   units, CTA c merges the (row, kv head) pairs c, c + grid, ... - it waits,
-//   with a bound, until the pair's counter shows every record, then combines
-//   them with one warp per query head.  Spreading the merges over the grid
-//   keeps them off any single CTA's critical path.
+//   increasing along the unit order.
+//   The split is stream-K over a weighted line: every unit weighs 1 and every
+//   segment start kSegW more (a segment switch costs a record epilogue and a
+//   new set of rotated queries), so a CTA that crosses several short worker
+//   blocks streams fewer tiles than one inside the long common block.  Unit
+//   (h, b, t) sits at weight h WH + ubase[b] + kSegW (sord[b] + 1) + t, where
+//   sord[b] counts the non-empty blocks before b and WH = UH + kSegW NB.  CTA
+//   c of C takes the units whose weight lies in [floor(c W / C),
+//   floor((c+1) W / C)).  C = min(grid, W / (kSegW + 1)): any kSegW + 1
+//   consecutive weights hold a unit, so every working CTA owns at least one
+//   unit and the CTAs touching a segment form one contiguous range.
+//   A CTA emits one partial record per (segment it touched, query head
+//   served) into slot seg + c, unique because seg and c never both stay put
+//   as units advance.  Every delivered record bumps the arrival counter of
+//   its (row, q head).  The launch is cooperative (all CTAs resident): after
+//   its own units, each CTA merges the (row, q head) items given to it - it
+//   waits, with a bound, until the item's counter shows every record, then
+//   combines them with the whole CTA.
+//
+// The view tables, positions and head map are read from global memory once,
+// in one round of independent loads, into a shared-memory cache (MetaCache);
+// everything later (plan, per-segment metadata, merge lists) reads the cache,
+// so no chain of dependent global loads sits on the path once the K/V tiles
+// are streaming.  Views with more than kCacheEntries entries fall back to
+// global reads.
 //
 // Group-level helpers take (tid, nt) - the thread's index within the group
 // that runs them and the group's size - and a Sync functor that synchronises
@@ -91,80 +103,181 @@ struct NamedSync {
   }
 };
 
+__device__ __forceinline__ unsigned lanemask_lt(int lane) { return (1u << lane) - 1u; }
+
+// ---------------------------------------------------------------------------
+// the metadata cache
+// ---------------------------------------------------------------------------
+
+constexpr int kCacheEntries = 384;  // view entries (rows x view blocks) held in shared memory
+constexpr int kCacheRows = 384;     // q_pos entries held in shared memory
+
+struct MetaCache {
+  int32_t vb[kCacheEntries];    // view_block
+  int32_t voff[kCacheEntries];  // view_offset
+  int32_t qpos[kCacheRows];     // q_pos
+  uint8_t rank[kCacheEntries];  // the entry's position among the references to its block
+  uint8_t kv_of[HW_MAX_Q_HEADS];  // q head -> kv head
+  uint8_t gi_of[HW_MAX_Q_HEADS];  // q head -> its index among the kv head's q heads
+  int32_t entries_cached, rows_cached;
+};
+
+__device__ __forceinline__ int vb_at(const DecodeArgs &a, const MetaCache &M, int e) {
+  return M.entries_cached ? M.vb[e] : __ldg(a.view_block + e);
+}
+__device__ __forceinline__ int voff_at(const DecodeArgs &a, const MetaCache &M, int e) {
+  return M.entries_cached ? M.voff[e] : __ldg(a.view_offset + e);
+}
+__device__ __forceinline__ int qpos_at(const DecodeArgs &a, const MetaCache &M, int r) {
+  return M.rows_cached ? M.qpos[r] : __ldg(a.q_pos + r);
+}
+// i_q - offset of view entry e (row e / V): the rotation of its queries.
+__device__ __forceinline__ int64_t entry_rel(const DecodeArgs &a, const MetaCache &M, int e) {
+  return static_cast<int64_t>(qpos_at(a, M, e / a.n_view)) - voff_at(a, M, e);
+}
+
+// Rank of entry e among the entries referencing the same block, for views
+// too large for the cache: one warp counts the matching earlier entries.
+__device__ __forceinline__ int entry_rank_scan(const DecodeArgs &a, int e, int lane) {
+  const int b = __ldg(a.view_block + e);
+  int cnt = 0;
+  for (int base = 0; base < e; base += 32) {
+    const int i = base + lane;
+    cnt += __popc(__ballot_sync(0xffffffffu, i < e && __ldg(a.view_block + i) == b));
+  }
+  return cnt;
+}
+
 // ---------------------------------------------------------------------------
 // the plan: every CTA derives the same unit decomposition from the metadata
 // ---------------------------------------------------------------------------
 
+constexpr int kSegW = 1;  // weight of a segment start, in tiles
+
 struct PlanCore {
   int32_t tiles[HW_MAX_BLOCKS];      // tiles per kv head (0: block skipped)
-  int32_t start[HW_MAX_BLOCKS];      // first pool token (valid where tiles > 0)
-  int32_t len[HW_MAX_BLOCKS];        // tokens (valid where tiles > 0)
+  int32_t start[HW_MAX_BLOCKS];      // first pool token
+  int32_t len[HW_MAX_BLOCKS];        // tokens
   int64_t ubase[HW_MAX_BLOCKS + 1];  // first unit of each block within a head; [n] = UH
+  uint8_t sord[HW_MAX_BLOCKS];       // non-empty blocks before b
+  int64_t UH, U, WH, W;              // units per head and in all; weights likewise
+  int32_t NB, C;                     // non-empty blocks; working CTAs
 };
 
 struct PlanScratch {  // only while the plan is built
   int32_t refs[HW_MAX_BLOCKS];
+  int32_t kv_cnt[HW_MAX_Q_HEADS];
   int32_t headmap_ok;
 };
 
-// Per-segment metadata: the view entries referencing the block and the query
-// heads of the kv head.  Query head qi of the tile is (ref qi / G, head qi % G).
+// Per-segment metadata: the view entries that reference the block and the
+// query heads of the kv head.  Query column qi of the tile is (reference
+// qi / G, q head qi % G).
 struct SegMeta {
   int32_t n_ref;
   int32_t ref_entry[kMaxQ];  // view entries r * V + v, in entry order
   int32_t qhead[kMaxQ];      // q heads of the kv head, in increasing order
 };
 
-struct MergeScratch {
-  int32_t mv_qi[HW_MAX_VIEW_BLOCKS];   // rank of the entry among its block's references
-  int64_t mv_seg[HW_MAX_VIEW_BLOCKS];  // segment id b * Hkv + h, -1 = no records
-  int32_t mv_c0[HW_MAX_VIEW_BLOCKS], mv_c1[HW_MAX_VIEW_BLOCKS];
-  float red[32];
-};
-
-// Unit range of CTA c.
-__device__ __forceinline__ int64_t cta_unit_begin(int64_t U, int c, int C) {
-  return (U * c) / C;
-}
-// The CTA that owns unit u: the largest c with floor(c U / C) <= u.
-__device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int C) {
-  return static_cast<int>(((u + 1) * C - 1) / U);
-}
-
-// Validates the metadata and builds the unit prefix.  Every thread of the CTA
-// takes part (blockDim.x threads, __syncthreads inside).
+// Loads the metadata into the cache (one round of independent loads), checks
+// it and builds the unit prefix.  Every thread of the CTA takes part
+// (blockDim.x == 256, __syncthreads inside).
 template <int TILE>
-__device__ void build_plan(const DecodeArgs &a, PlanCore &P, PlanScratch &S) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int G = a.n_q_heads / a.n_kv_heads;
-  for (int b = tid; b < a.n_blocks; b += nt) S.refs[b] = 0;
-  if (tid == 0) S.headmap_ok = 1;
-  __syncthreads();
+__device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanScratch &S) {
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads;
   const int E = a.n_rows * a.n_view;
-  for (int e = tid; e < E; e += nt) {
-    const int b = a.view_block[e];
-    if (b >= a.n_blocks || b < -1) {
-      if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_BLOCK);
-    } else if (b >= 0) {
-      atomicAdd(&S.refs[b], 1);
-    }
+  const bool ecached = E <= kCacheEntries, rcached = a.n_rows <= kCacheRows;
+
+  // 1. every metadata word this CTA needs, as one batch of loads
+  int r_vb[2], r_vo[2], r_qp[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int e = tid + k * nt;
+    const bool le = ecached && e < E, lr = rcached && e < a.n_rows;
+    r_vb[k] = le ? __ldg(a.view_block + e) : 0;
+    r_vo[k] = le ? __ldg(a.view_offset + e) : 0;
+    r_qp[k] = lr ? __ldg(a.q_pos + e) : 0;
   }
-  if (a.q_to_kv) {
-    // every kv head must serve exactly G query heads
-    for (int h = tid; h < a.n_kv_heads; h += nt) {
-      int cnt = 0;
-      for (int hq = 0; hq < a.n_q_heads; ++hq) cnt += (a.q_to_kv[hq] == h);
-      if (cnt != G) S.headmap_ok = 0;
+  const bool lb = tid < a.n_blocks, lh = tid < Hq;
+  const int r_bs = lb ? __ldg(a.block_start + tid) : 0;
+  const int r_bl = lb ? __ldg(a.block_len + tid) : 0;
+  const int r_kv = lh ? (a.q_to_kv ? __ldg(a.q_to_kv + tid) : tid / G) : 0;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int e = tid + k * nt;
+    if (ecached && e < E) {
+      M.vb[e] = r_vb[k];
+      M.voff[e] = r_vo[k];
     }
-    for (int hq = tid; hq < a.n_q_heads; hq += nt) {
-      const int g = a.q_to_kv[hq];
-      if (g < 0 || g >= a.n_kv_heads) S.headmap_ok = 0;
+    if (rcached && e < a.n_rows) M.qpos[e] = r_qp[k];
+  }
+  if (tid == 0) {
+    M.entries_cached = ecached;
+    M.rows_cached = rcached;
+    S.headmap_ok = 1;
+  }
+  if (lb) {
+    P.start[tid] = r_bs;
+    P.len[tid] = r_bl;
+    S.refs[tid] = 0;
+  }
+  if (lh) {
+    S.kv_cnt[tid] = 0;
+    const bool ok = r_kv >= 0 && r_kv < a.n_kv_heads;
+    M.kv_of[tid] = static_cast<uint8_t>(ok ? r_kv : 0);
+  }
+  __syncthreads();
+  if (lh && (r_kv < 0 || r_kv >= a.n_kv_heads)) S.headmap_ok = 0;
+
+  if (warp == 0) {
+    // references per block, and each entry's rank among its block's references
+    if (ecached) {
+      for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        const int b = e < E ? M.vb[e] : -1;
+        const bool valid = b >= 0 && b < a.n_blocks;
+        if (e < E && !valid && b != -1 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_BLOCK);
+        const unsigned m = __match_any_sync(0xffffffffu, valid ? b : -2 - lane);
+        const int before = valid ? S.refs[b] : 0;
+        const int rk = before + __popc(m & lanemask_lt(lane));
+        if (e < E) M.rank[e] = static_cast<uint8_t>(rk < 255 ? rk : 255);
+        __syncwarp();
+        if (valid && lane == 31 - __clz(m)) S.refs[b] = before + __popc(m);
+        __syncwarp();
+      }
+    } else {
+      for (int e = lane; e < E; e += 32) {
+        const int b = __ldg(a.view_block + e);
+        if (b >= a.n_blocks || b < -1) {
+          if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_BLOCK);
+        } else if (b >= 0) {
+          atomicAdd(&S.refs[b], 1);
+        }
+      }
     }
+  } else if (warp == 1) {
+    // each q head's index within its kv head's group; every group must have G
+    for (int base = 0; base < Hq; base += 32) {
+      const int hq = base + lane;
+      const int g = hq < Hq ? M.kv_of[hq] : 0;
+      const unsigned m = __match_any_sync(0xffffffffu, hq < Hq ? g : -2 - lane);
+      const int before = hq < Hq ? S.kv_cnt[g] : 0;
+      if (hq < Hq) {
+        const int gi = before + __popc(m & lanemask_lt(lane));
+        M.gi_of[hq] = static_cast<uint8_t>(gi < 255 ? gi : 255);
+      }
+      __syncwarp();
+      if (hq < Hq && lane == 31 - __clz(m)) S.kv_cnt[g] = before + __popc(m);
+      __syncwarp();
+    }
+    for (int h = lane; h < a.n_kv_heads; h += 32)
+      if (S.kv_cnt[h] != G) S.headmap_ok = 0;
   }
   __syncthreads();
   if (!S.headmap_ok && tid == 0 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_HEADMAP);
   for (int b = tid; b < a.n_blocks; b += nt) {
-    const int32_t s = a.block_start[b], n = a.block_len[b];
+    const int32_t s = P.start[b], n = P.len[b];
     int t = 0;
     if (s < 0 || n < 0 || static_cast<int64_t>(s) + n > a.capacity) {
       if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_RANGE);
@@ -176,33 +289,41 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, PlanScratch &S) {
       }
     }
     P.tiles[b] = S.headmap_ok ? t : 0;
-    P.start[b] = s;
-    P.len[b] = n;
   }
   __syncthreads();
-  if (tid < 32) {
-    // exclusive prefix over blocks of tiles (units of one kv head), one warp
+  if (warp == 0) {
+    // exclusive prefixes over blocks: tiles (ubase) and non-empty blocks (sord)
     int64_t carry = 0;
+    int ncarry = 0;
     for (int base = 0; base < a.n_blocks; base += 32) {
-      const int b = base + tid;
+      const int b = base + lane;
       const int64_t x = (b < a.n_blocks) ? static_cast<int64_t>(P.tiles[b]) : 0;
       int64_t incl = x;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (tid >= o) incl += y;
+        if (lane >= o) incl += y;
       }
-      if (b < a.n_blocks) P.ubase[b] = carry + incl - x;
+      const unsigned ne = __ballot_sync(0xffffffffu, x > 0);
+      if (b < a.n_blocks) {
+        P.ubase[b] = carry + incl - x;
+        P.sord[b] = static_cast<uint8_t>(ncarry + __popc(ne & lanemask_lt(lane)));
+      }
       carry += __shfl_sync(0xffffffffu, incl, 31);
+      ncarry += __popc(ne);
     }
-    if (tid == 0) P.ubase[a.n_blocks] = carry;
+    if (lane == 0) {
+      P.ubase[a.n_blocks] = carry;
+      P.UH = carry;
+      P.U = carry * a.n_kv_heads;
+      P.NB = ncarry;
+      P.WH = carry + static_cast<int64_t>(kSegW) * ncarry;
+      P.W = P.WH * a.n_kv_heads;
+      const int64_t cmax = P.W / (kSegW + 1);
+      P.C = static_cast<int>(cmax < static_cast<int64_t>(gridDim.x) ? cmax : gridDim.x);
+    }
   }
   __syncthreads();
-}
-
-// Total units: UH per kv head.
-__device__ __forceinline__ int64_t total_units(const PlanCore &P, const DecodeArgs &a) {
-  return P.ubase[a.n_blocks] * a.n_kv_heads;
 }
 
 // Block that holds in-head unit u (ubase[b] <= u < ubase[b+1]), by binary search.
@@ -222,92 +343,82 @@ struct UnitPos {
 };
 __device__ __forceinline__ UnitPos unit_pos(const PlanCore &P, int n_blocks, int64_t u) {
   UnitPos x;
-  const int64_t UH = P.ubase[n_blocks];
-  x.h = static_cast<int>(u / UH);
-  const int64_t local = u - static_cast<int64_t>(x.h) * UH;
+  x.h = static_cast<int>(u / P.UH);
+  const int64_t local = u - static_cast<int64_t>(x.h) * P.UH;
   x.b = block_of_unit(P, n_blocks, local);
   x.tiles = P.tiles[x.b];
   x.t = static_cast<int>(local - P.ubase[x.b]);
-  x.seg_first = static_cast<int64_t>(x.h) * UH + P.ubase[x.b];
+  x.seg_first = static_cast<int64_t>(x.h) * P.UH + P.ubase[x.b];
   return x;
 }
 
-// First unit of segment (b, h) and its id.
-__device__ __forceinline__ int64_t seg_first_unit_of(const PlanCore &P, int n_blocks, int b, int h) {
-  return static_cast<int64_t>(h) * P.ubase[n_blocks] + P.ubase[b];
+// Weight of unit u (strictly increasing in u).
+__device__ __forceinline__ int64_t unit_weight(const PlanCore &P, int n_blocks, int64_t u) {
+  const int h = static_cast<int>(u / P.UH);
+  const int64_t local = u - static_cast<int64_t>(h) * P.UH;
+  const int b = block_of_unit(P, n_blocks, local);
+  return static_cast<int64_t>(h) * P.WH + local + static_cast<int64_t>(kSegW) * (P.sord[b] + 1);
 }
+
+// The CTA that owns unit u: the largest c with floor(c W / C) <= weight(u).
+__device__ __forceinline__ int cta_of_unit(const PlanCore &P, int n_blocks, int64_t u) {
+  return static_cast<int>(((unit_weight(P, n_blocks, u) + 1) * P.C - 1) / P.W);
+}
+
+// First unit of CTA c: the first unit whose weight is >= floor(c W / C).
+__device__ __forceinline__ int64_t cta_unit_begin(const PlanCore &P, int n_blocks, int c) {
+  if (c >= P.C) return P.U;
+  const int64_t w = (P.W * c) / P.C;
+  const int h = static_cast<int>(w / P.WH);
+  const int64_t l = w - static_cast<int64_t>(h) * P.WH;
+  // the last block whose weight region [ubase + kSegW sord, ...) starts at or before l
+  int lo = 0, hi = n_blocks - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.ubase[mid] + static_cast<int64_t>(kSegW) * P.sord[mid] <= l) lo = mid; else hi = mid - 1;
+  }
+  const int64_t off = l - (P.ubase[lo] + static_cast<int64_t>(kSegW) * P.sord[lo]);
+  return static_cast<int64_t>(h) * P.UH + P.ubase[lo] + (off > kSegW ? off - kSegW : 0);
+}
+
 __device__ __forceinline__ int64_t seg_id(int n_blocks, int b, int h) {
   return static_cast<int64_t>(h) * n_blocks + b;
 }
 
-// Number of CTAs whose unit ranges touch segment (b, h).
-__device__ __forceinline__ int seg_ctas(const PlanCore &P, int n_blocks, int b, int h, int64_t U,
-                                        int C) {
-  const int tl = P.tiles[b];
-  if (tl == 0) return 0;
-  const int64_t s0 = seg_first_unit_of(P, n_blocks, b, h);
-  return cta_of_unit(s0 + tl - 1, U, C) - cta_of_unit(s0, U, C) + 1;
-}
-
-// Records expected for (row r, kv head h): one per (view entry, CTA) pair.
-__device__ __forceinline__ int expected_records(const DecodeArgs &a, const PlanCore &P, int r,
-                                                int h, int64_t U, int C) {
-  int n = 0;
-  for (int v = 0; v < a.n_view; ++v) {
-    const int b = a.view_block[r * a.n_view + v];
-    if (b >= 0 && b < a.n_blocks) n += seg_ctas(P, a.n_blocks, b, h, U, C);
-  }
-  return n;
-}
-
-// The query heads served by kv head h, in increasing order (one warp).
-__device__ __forceinline__ void gather_qheads(const DecodeArgs &a, SegMeta &M, int h, int lane) {
-  const int G = a.n_q_heads / a.n_kv_heads;
-  if (!a.q_to_kv) {
-    for (int i = lane; i < G; i += 32) M.qhead[i] = h * G + i;
-  } else {
-    int cnt = 0;
-    for (int base = 0; base < a.n_q_heads; base += 32) {
-      const int hq = base + lane;
-      const bool m = hq < a.n_q_heads && a.q_to_kv[hq] == h;
-      const unsigned mask = __ballot_sync(0xffffffffu, m);
-      const int pos = cnt + __popc(mask & ((1u << lane) - 1u));
-      if (m && pos < G) M.qhead[pos] = hq;
-      cnt += __popc(mask);
-    }
-  }
-}
-
-// View entries referencing block b, in entry order (one warp).
-__device__ __forceinline__ void gather_refs(const DecodeArgs &a, SegMeta &M, int b, int lane) {
+// The view entries referencing block b, in entry order (one warp).
+__device__ __forceinline__ void gather_refs(const DecodeArgs &a, const MetaCache &C, SegMeta &M,
+                                            int b, int lane) {
   const int E = a.n_rows * a.n_view;
   int cnt = 0;
-  for (int base = 0; base < E; base += 32) {
-    const int e = base + lane;
-    const bool m = e < E && a.view_block[e] == b;
-    const unsigned mask = __ballot_sync(0xffffffffu, m);
-    const int pos = cnt + __popc(mask & ((1u << lane) - 1u));
-    if (m && pos < kMaxQ) M.ref_entry[pos] = e;
-    cnt += __popc(mask);
+  if (C.entries_cached) {
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const bool m = e < E && C.vb[e] == b;
+      if (m && C.rank[e] < kMaxQ) M.ref_entry[C.rank[e]] = e;
+      cnt += __popc(__ballot_sync(0xffffffffu, m));
+    }
+  } else {
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const bool m = e < E && __ldg(a.view_block + e) == b;
+      const unsigned mask = __ballot_sync(0xffffffffu, m);
+      const int pos = cnt + __popc(mask & lanemask_lt(lane));
+      if (m && pos < kMaxQ) M.ref_entry[pos] = e;
+      cnt += __popc(mask);
+    }
   }
   if (lane == 0) M.n_ref = cnt;
 }
 
-__device__ __forceinline__ float *record_ptr(const DecodeArgs &a, int64_t slot, int qi) {
-  return a.partials + (slot * kMaxQ + qi) * static_cast<int64_t>(a.head_dim + 4);
+// The q heads of kv head h, in increasing order (one warp).
+__device__ __forceinline__ void gather_qheads(const DecodeArgs &a, const MetaCache &C, SegMeta &M,
+                                              int h, int lane) {
+  for (int hq = lane; hq < a.n_q_heads; hq += 32)
+    if (C.kv_of[hq] == h && C.gi_of[hq] < kMaxQ) M.qhead[C.gi_of[hq]] = hq;
 }
 
-// out = 0, lse = -inf for every query head of kv head h in row r (empty view).
-template <typename T>
-__device__ void write_empty(const DecodeArgs &a, const int32_t *qhead, int r, int tid, int nt) {
-  const int G = a.n_q_heads / a.n_kv_heads;
-  for (int i = tid; i < G * a.head_dim; i += nt) {
-    const int gi = i / a.head_dim, d = i % a.head_dim;
-    const int hq = qhead[gi];
-    reinterpret_cast<T *>(a.out)[(static_cast<int64_t>(r) * a.n_q_heads + hq) * a.head_dim + d] =
-        from_f32<T>(0.f);
-    if (d == 0 && a.lse) a.lse[static_cast<int64_t>(r) * a.n_q_heads + hq] = -INFINITY;
-  }
+__device__ __forceinline__ float *record_ptr(const DecodeArgs &a, int64_t slot, int qi) {
+  return a.partials + (slot * kMaxQ + qi) * static_cast<int64_t>(a.head_dim + 4);
 }
 
 // ---------------------------------------------------------------------------
@@ -321,11 +432,10 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
 }
 
 // One arrival on (row, q head) for every view entry referencing the
-// segment's block and every q head of kv head h (M.qhead).  One thread calls
-// it, after the group's record stores were ordered before it (a barrier the
-// writers took part in, or an mbarrier they arrived on).
-__device__ __forceinline__ void arrive_segment(const DecodeArgs &a, const SegMeta &M, int h) {
-  (void)h;
+// segment's block and every q head of its kv head (M.qhead).  One thread
+// calls it, after the group's record stores were ordered before it (a
+// barrier the writers took part in, or an mbarrier they arrived on).
+__device__ __forceinline__ void arrive_segment(const DecodeArgs &a, const SegMeta &M) {
   const int G = a.n_q_heads / a.n_kv_heads;
   __threadfence();
   for (int j = 0; j < M.n_ref && j < kMaxQ; ++j) {
@@ -345,135 +455,77 @@ __device__ __forceinline__ void lse_combine(float &M, float &L, float m, float l
   }
 }
 
-// Shared scratch of the merge phase (at most ~20 KB; the tensor-core kernel
-// places it in its tile buffers, idle by then).
+// Shared scratch of the merge phase (~17 KB; the tensor-core kernel places
+// it in its tile buffers, idle by then).
 struct MergeSmem {
-  MergeScratch X;
   int32_t list[kMaxRecords];  // record index of each partial: slot * 32 + rank * G + gi
   float mlist[kMaxRecords];   // its max m (log2 domain)
   float acc[8][128];          // per warp partial sums of the output row
-  int32_t nb_before[HW_MAX_BLOCKS];  // blocks with tiles before b (segment ordinals)
-  int32_t rank_part[8];
-  int32_t n_rec, ok, rank;
+  int32_t rank_tmp[HW_MAX_VIEW_BLOCKS];  // entry ranks of one row (views beyond the cache)
+  int32_t n_rec, ok;
   float M, L;
 };
-
-// Ordinal of the segment that holds unit u, in unit order.
-__device__ __forceinline__ int seg_ordinal(const PlanCore &P, const MergeSmem &Z, int n_blocks,
-                                           int nb_total, int64_t u) {
-  const int64_t UH = P.ubase[n_blocks];
-  const int h = static_cast<int>(u / UH);
-  const int b = block_of_unit(P, n_blocks, u - static_cast<int64_t>(h) * UH);
-  return h * nb_total + Z.nb_before[b];
-}
 
 // The merge phase.  Every thread of every CTA of the (cooperative) grid calls
 // it once its own units are done.  Work item = (row r, q head hq): all the
 // partial records of that output row, each from one (view entry, CTA) pair.
-// Items go to CTAs in order of how many segments they processed (idle and
-// lightly loaded CTAs first), so the merges do not queue behind the slowest
-// CTAs.  An item's owner prepares the record list, waits (bounded) until the
-// item's arrival counter shows every record, then merges with the whole CTA:
+// Items go round-robin over the CTAs, those without units first.  An item's
+// owner lists its records from the plan, waits (bounded) until the item's
+// arrival counter shows every record, then merges with the whole CTA:
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
-//   lse = (M + log2 L) ln 2.
+//   lse = (M + log2 L) ln 2;
+// an item without records gets out = 0, lse = -inf.
 template <typename T, int D, typename Sync>
-__device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeSmem &Z, int64_t U,
-                            int C, int tid, int nt, Sync sync, long long wait_limit) {
+__device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCache &MC,
+                            MergeSmem &Z, int tid, int nt, Sync sync, long long wait_limit) {
   constexpr int EPL = D / 32;
   constexpr int64_t RS = D + 4;  // record stride in floats
   const int V = a.n_view;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
   const int G = a.n_q_heads / a.n_kv_heads;
   const int items = a.n_rows * a.n_q_heads;
-  const int grid = static_cast<int>(gridDim.x);
-  MergeScratch &X = Z.X;
-
-  // ---- this CTA's rank among the grid: fewer segments first, then index
-  if (tid < 32) {
-    int cnt = 0;
-    for (int base = 0; base < a.n_blocks; base += 32) {
-      const int b = base + lane;
-      const bool ne = b < a.n_blocks && P.tiles[b] > 0;
-      const unsigned m = __ballot_sync(0xffffffffu, ne);
-      if (b < a.n_blocks) Z.nb_before[b] = cnt + __popc(m & ((1u << lane) - 1u));
-      cnt += __popc(m);
-    }
-    if (lane == 0) Z.n_rec = cnt;  // number of non-empty blocks, for the ordinals
-  }
-  sync();
-  const int nb_total = Z.n_rec;
-  auto nseg_of = [&](int c) -> int {
-    if (U == 0 || c >= C) return 0;
-    const int64_t u0 = cta_unit_begin(U, c, C), u1 = cta_unit_begin(U, c + 1, C);
-    return seg_ordinal(P, Z, a.n_blocks, nb_total, u1 - 1) - seg_ordinal(P, Z, a.n_blocks, nb_total, u0) + 1;
-  };
-  const int me = blockIdx.x;
-  const int my_n = nseg_of(me);
-  int before = 0;
-  for (int c = tid; c < grid; c += nt) {
-    const int nc = nseg_of(c);
-    before += (nc < my_n || (nc == my_n && c < me)) ? 1 : 0;
-  }
-  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
-  if (lane == 0) Z.rank_part[warp] = before;
-  sync();
-  if (tid == 0) {
-    int rk = 0;
-    for (int w2 = 0; w2 < nwarps; ++w2) rk += Z.rank_part[w2];
-    Z.rank = rk;
-  }
-  sync();
-  const int rank = Z.rank;
+  const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int rank = c >= P.C ? c - P.C : c + (grid - P.C);
 
   for (int it = rank; it < items; it += grid) {
     const int r = it / a.n_q_heads, hq = it % a.n_q_heads;
-    int h = hq / G, gi = hq % G;
-    if (a.q_to_kv) {
-      h = a.q_to_kv[hq];
-      gi = 0;
-      for (int q2 = 0; q2 < hq; ++q2) gi += (a.q_to_kv[q2] == h);
-      if (h < 0 || h >= a.n_kv_heads || gi >= G) continue;  // flagged by the plan
-    }
-    const int expected = expected_records(a, P, r, h, U, C);
-    if (expected == 0) continue;  // written as empty at the start
+    const int h = MC.kv_of[hq], gi = MC.gi_of[hq];
     if (warp == 0) {
-      // per view entry: its block's segment, the CTA range that wrote records,
-      // and its rank among the entries that reference the same block
-      for (int v = lane; v < V; v += 32) {
-        const int b = a.view_block[r * V + v];
-        X.mv_seg[v] = -1;
-        X.mv_qi[v] = 0;
-        if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
-          const int64_t s0 = seg_first_unit_of(P, a.n_blocks, b, h);
-          X.mv_seg[v] = seg_id(a.n_blocks, b, h);
-          X.mv_c0[v] = cta_of_unit(s0, U, C);
-          X.mv_c1[v] = cta_of_unit(s0 + P.tiles[b] - 1, U, C);
-        }
-      }
-      __syncwarp();
-      const int E = r * V + V;
-      for (int base = 0; base < E; base += 32) {
-        const int i = base + lane;
-        const int x = (i < E) ? a.view_block[i] : -2;
+      if (!MC.entries_cached) {
         for (int v = 0; v < V; ++v) {
-          const int e = r * V + v;
-          const int b = __shfl_sync(0xffffffffu, x, (e - base) & 31);
-          const int bb = (e >= base && e < base + 32) ? b : a.view_block[e];
-          const unsigned m = __ballot_sync(0xffffffffu, i < e && x == bb);
-          if (lane == 0) X.mv_qi[v] += __popc(m);
+          const int rk = entry_rank_scan(a, r * V + v, lane);
+          if (lane == 0) Z.rank_tmp[v] = rk;
         }
+        __syncwarp();
       }
-      __syncwarp();
-      // the flat record list: (view entry, CTA) pairs in view order
+      // per view entry: the CTAs c0..c1 that wrote records of segment (b, h),
+      // and the record column rank * G + gi; then the flat list in view order
       int off = 0;
-      for (int v = 0; v < V; ++v) {
-        if (X.mv_seg[v] < 0) continue;
-        const int c0 = X.mv_c0[v], cnt = X.mv_c1[v] - c0 + 1;
-        const int base_rec = X.mv_qi[v] * G + gi;
-        for (int j = lane; j < cnt; j += 32)
-          if (off + j < kMaxRecords)
-            Z.list[off + j] = static_cast<int32_t>((X.mv_seg[v] + c0 + j) * kMaxQ + base_rec);
-        off += cnt;
+      for (int v0 = 0; v0 < V; v0 += 32) {
+        const int v = v0 + lane;
+        int cnt = 0, col = 0;
+        int64_t slot0 = 0;
+        if (v < V) {
+          const int e = r * V + v;
+          const int b = vb_at(a, MC, e);
+          if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
+            const int64_t s0 = static_cast<int64_t>(h) * P.UH + P.ubase[b];
+            const int c0 = cta_of_unit(P, a.n_blocks, s0);
+            cnt = cta_of_unit(P, a.n_blocks, s0 + P.tiles[b] - 1) - c0 + 1;
+            slot0 = seg_id(a.n_blocks, b, h) + c0;
+            col = (MC.entries_cached ? MC.rank[e] : Z.rank_tmp[v]) * G + gi;
+          }
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int my = off + incl - cnt;
+        for (int j = 0; j < cnt; ++j)
+          if (my + j < kMaxRecords) Z.list[my + j] = static_cast<int32_t>((slot0 + j) * kMaxQ + col);
+        off += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (lane == 0) {
         if (off > kMaxRecords) {
@@ -483,13 +535,23 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeSmem &Z
         Z.n_rec = off;
       }
     }
+    sync();
+    const int n_rec = Z.n_rec;
+    const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
+    if (n_rec == 0) {
+      // no block of the view has tokens
+      if (tid < D) reinterpret_cast<T *>(a.out)[ob * D + tid] = from_f32<T>(0.f);
+      if (tid == 0 && a.lse) a.lse[ob] = -INFINITY;
+      sync();
+      continue;
+    }
     if (tid == 0) {
       // every record of the item is delivered (bounded wait: co-resident CTAs)
       const int32_t *ctr = a.counters + it;
-      bool ok = ld_acquire_gpu(ctr) >= expected;
+      bool ok = ld_acquire_gpu(ctr) >= n_rec;
       if (!ok) {
         const long long t0 = clock64();
-        while (!(ok = ld_acquire_gpu(ctr) >= expected)) {
+        while (!(ok = ld_acquire_gpu(ctr) >= n_rec)) {
           if (clock64() - t0 > wait_limit) break;
           __nanosleep(32);
         }
@@ -498,7 +560,6 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeSmem &Z
       Z.ok = ok ? 1 : 0;
     }
     sync();
-    const int n_rec = Z.n_rec;
     if (Z.ok) {
       if (warp == 0) {  // pass A: the maxima and the normaliser
         float Mx = -INFINITY, Lx = 0.f;
@@ -548,7 +609,6 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, MergeSmem &Z
       if (tid < D) {
         float sum = 0.f;
         for (int w2 = 0; w2 < nwarps; ++w2) sum += Z.acc[w2][tid];
-        const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
         reinterpret_cast<T *>(a.out)[ob * D + tid] = from_f32<T>(sum / Z.L);
         if (tid == 0 && a.lse) a.lse[ob] = (Z.M + __log2f(Z.L)) * 0.69314718055994530942f;
       }

@@ -72,11 +72,12 @@ enum {
 #define HW_MAX_VIEW_BLOCKS 64      /* max_view_blocks */
 #define HW_MAX_VIEW_ENTRIES 4096   /* n_rows * max_view_blocks */
 #define HW_MAX_QHEADS_PER_BLOCK 32 /* (view references to one block) x (Hq/Hkv) */
+#define HW_MAX_Q_HEADS 256         /* n_q_heads */
 
 /* Host-side description of one decode call (all scalars, host memory). */
 typedef struct {
   int32_t n_rows;          /* query tokens: one per (problem, worker), >= 0 */
-  int32_t n_q_heads;       /* Hq */
+  int32_t n_q_heads;       /* Hq, <= HW_MAX_Q_HEADS */
   int32_t n_kv_heads;      /* Hkv, Hq % Hkv == 0 */
   int32_t head_dim;        /* D: 64 or 128 (bf16 tensor-core path: 128) */
   int32_t n_blocks;        /* entries of block_start / block_len, <= HW_MAX_BLOCKS */
