@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
   SimtSmem<D> &S = *reinterpret_cast<SimtSmem<D> *>(smem_raw);
   PlanCore &P = S.plan;
   build_plan<kSimtTile>(a, P, S.cache, S.scratch);
-  const int c = blockIdx.x;
-  int64_t u = cta_unit_begin(P, a.n_blocks, c);
-  const int64_t u_end = cta_unit_begin(P, a.n_blocks, c + 1);
+  plan_ranks(a, S.cache, threadIdx.x >> 5, threadIdx.x & 31, 0, 1);  // read by the merge
+  int64_t u = P.u0;
+  const int64_t u_end = P.u1;
   while (u < u_end) {
     const UnitPos x = unit_pos(P, a.n_blocks, u);
     const int64_t seg_stop = min(x.seg_first + x.tiles, u_end);
@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
     u = seg_stop;
   }
   __syncthreads();
-  merge_phase<T, D>(a, P, S.cache, S.merge, threadIdx.x, kSimtThreads, CtaSync(), 2000000000ll);
+  merge_phase<T, D>(a, P, S.cache, S.merge, nullptr, -1, threadIdx.x, kSimtThreads, CtaSync(),
+                    2000000000ll);
 }
 
 template <typename T, int D>

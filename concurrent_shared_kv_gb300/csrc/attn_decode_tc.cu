@@ -49,24 +49,33 @@ constexpr uint32_t kColO = 64;                // segment k accumulates in O[k & 
 constexpr float kLazy = 8.f;                  // rescale only when the max grows by > 2^8
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
-constexpr int kPre = 4;  // segments whose metadata the prologue prepares
-// Named barriers: 1 softmax warps, 2 query warps, 3 prologue warps,
-// 4 prologue warps + TMA warp (the queries of segment 0 are requested before
-// the first K/V tile, so that they do not queue behind the tile stream).
-constexpr int kBarQIssued = 4;
+constexpr int kPre = 4;  // slots of query-side segment metadata
+constexpr int kPreList = 64;  // records of a merge list built ahead of the merge
+// Named barriers: 1 softmax warps, 2 query warps, 3 prologue warps.
+
+// Query-side metadata of a segment: its view references and q heads, and per
+// query column qi = (reference qi / G, q head qi % G) the q row to read and
+// the rotation i_q - offset of its reference.
+struct SegQ {
+  SegMeta m;
+  int32_t qrow[kMaxQ];  // row * Hq + q head
+  int64_t rel[kMaxQ];
+};
 
 struct TcSmem {
   alignas(1024) uint8_t stage[kStages][kStageBytes];
   alignas(1024) uint8_t q[kQBytes];
   PlanCore plan;
   MetaCache cache;
-  SegMeta meta;        // handed from the query warps to the softmax warps
-  SegMeta pre[kPre];   // query-side metadata of segment j in pre[j % kPre]
-  int32_t pre_count;   // segments among the first kPre that exist
+  int32_t meta_nref;   // references of the current segment, handed to the softmax warps
+  SegQ pre[kPre];      // query-side metadata of segment j in pre[j % kPre]
+  int32_t mpre[kPreList];  // record list of the CTA's first merge item, built while tiles stream
+  int32_t mpre_n;          // its length, or -1 (not built)
   alignas(16) float red[2][kN][4];  // per tile: column maxima of the 4 softmax warps (read as float4)
   float lsave[2][4][kN];  // per segment parity: column sums of l of the 4 softmax warps
   float msave[2][kN];     // per segment parity: the reference maxima
   int32_t abort_flag;
+  int32_t tiles_done;  // tiles whose P the softmax warps have written (progress only)
   uint32_t tmem_base;
   alignas(8) uint64_t k_full[kStages];
   uint64_t v_full[kStages], kv_empty[kStages];
@@ -161,124 +170,107 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
   }
 }
 
+// Issues the products in a fixed order - QK(0), QK(1), then PV(i), QK(i+2) -
+// each after a blocking (bounded) wait on its inputs.  QK(i+2) is not needed
+// before the softmax warps are done with tile i+1, so issuing PV(i) first
+// costs nothing, and the thread sleeps instead of polling.
 __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0, int64_t u1) {
   constexpr uint32_t idesc_qk = idesc_bf16(128, kN, 0, 0);  // K tile, Q~: both K-major
   constexpr uint32_t idesc_pv = idesc_bf16(128, kN, 1, 1);  // V tile, P: both MN-major
   const int n = static_cast<int>(u1 - u0);
-  int iq = 0, ip = 0, seg_q = -1, seg_p = -1;
-  long long last_progress = clock64();
-  while (ip < n) {
-    if (aborted(S)) break;
-    bool progressed = false;
-    // P.V first: it releases a stage and the O accumulator; QK of a later
-    // tile is not needed until the softmax warps are done with this one
-    if (ip < iq) {
-      const int64_t u = u0 + ip;
-      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-      const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
-      const int kseg = first ? seg_p + 1 : seg_p;
-      const int s = ip % kStages;
-      if (mbar_test(&S.p_full[s], (ip / kStages) & 1) && mbar_test(&S.v_full[s], (ip / kStages) & 1) &&
-          (!first || mbar_test(&S.o_empty[kseg & 1], ((kseg >> 1) & 1) ^ 1))) {
-        seg_p = kseg;
-        tc_fence_after();
-        const uint32_t vb = smem_u32(S.stage[s]) + 2 * kBox, pb = smem_u32(S.stage[s]);
+  int seg_q = -1, seg_p = -1;
+  auto qk = [&](int i) {
+    const int64_t u = u0 + i;
+    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
+    if (first) ++seg_q;
+    const int s = i % kStages, sb = i & 1;
+    if (!wait_or_abort(S, a, &S.k_full[s], (i / kStages) & 1)) return;
+    if (!wait_or_abort(S, a, &S.s_empty[sb], ((i >> 1) & 1) ^ 1)) return;
+    if (first && !wait_or_abort(S, a, &S.q_full, seg_q & 1)) return;
+    tc_fence_after();
+    const uint32_t kb = smem_u32(S.stage[s]), qbase = smem_u32(S.q);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart,
-          // 8-token groups 1024 B apart.  P^T: MN-major, 32 heads = one 64-B atom,
-          // 8-token groups 512 B apart.
-          const uint64_t ad = smem_desc(vb + kk * 2048, kBox, 1024, kSw128);
-          const uint64_t bd = smem_desc(pb + kk * 1024, 512, 512, kSw64);
-          mma_bf16(tmem + kColO + (kseg & 1) * kN, ad, bd, idesc_pv, !(first && kk == 0));
-        }
-        mma_commit(&S.kv_empty[s]);
-        mma_commit(&S.p_empty);
-        if (last) mma_commit(&S.o_full[kseg & 1]);
-        ++ip;
-        progressed = true;
-      }
+    for (int kk = 0; kk < 16; ++kk) {  // 8 k-steps against Q~ hi, then 8 against Q~ lo
+      const int k8 = kk & 7;
+      const uint64_t ad = smem_desc(kb + (k8 >> 2) * kBox + (k8 & 3) * 32, 16, 1024, kSw128);
+      const uint64_t bd = smem_desc(qbase + (kk >> 3) * kQPart + (k8 >> 2) * kQHalf + (k8 & 3) * 32,
+                                    16, 1024, kSw128);
+      mma_bf16(tmem + sb * kN, ad, bd, idesc_qk, kk > 0);
     }
-    if (iq < n && iq < ip + 2) {
-      const int64_t u = u0 + iq;
-      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-      const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
-      const int kseg = first ? seg_q + 1 : seg_q;
-      const int s = iq % kStages, sb = iq & 1;
-      if (mbar_test(&S.k_full[s], (iq / kStages) & 1) &&
-          mbar_test(&S.s_empty[sb], ((iq >> 1) & 1) ^ 1) &&
-          (!first || mbar_test(&S.q_full, kseg & 1))) {
-        seg_q = kseg;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(S.stage[s]), qbase = smem_u32(S.q);
+    mma_commit(&S.s_full[sb]);
+    if (last) mma_commit(&S.q_empty);
+  };
+  auto pv = [&](int i) {
+    const int64_t u = u0 + i;
+    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
+    if (first) ++seg_p;
+    const int s = i % kStages;
+    if (!wait_or_abort(S, a, &S.p_full[s], (i / kStages) & 1)) return;
+    if (!wait_or_abort(S, a, &S.v_full[s], (i / kStages) & 1)) return;
+    if (first && !wait_or_abort(S, a, &S.o_empty[seg_p & 1], ((seg_p >> 1) & 1) ^ 1)) return;
+    tc_fence_after();
+    const uint32_t vb = smem_u32(S.stage[s]) + 2 * kBox, pb = smem_u32(S.stage[s]);
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {  // 8 k-steps against Q~ hi, then 8 against Q~ lo
-          const int k8 = kk & 7;
-          const uint64_t ad = smem_desc(kb + (k8 >> 2) * kBox + (k8 & 3) * 32, 16, 1024, kSw128);
-          const uint64_t bd = smem_desc(qbase + (kk >> 3) * kQPart + (k8 >> 2) * kQHalf + (k8 & 3) * 32,
-                                        16, 1024, kSw128);
-          mma_bf16(tmem + sb * kN, ad, bd, idesc_qk, kk > 0);
-        }
-        mma_commit(&S.s_full[sb]);
-        if (last) mma_commit(&S.q_empty);
-        ++iq;
-        progressed = true;
-      }
+    for (int kk = 0; kk < 8; ++kk) {
+      // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart,
+      // 8-token groups 1024 B apart.  P^T: MN-major, 32 heads = one 64-B atom,
+      // 8-token groups 512 B apart.
+      const uint64_t ad = smem_desc(vb + kk * 2048, kBox, 1024, kSw128);
+      const uint64_t bd = smem_desc(pb + kk * 1024, 512, 512, kSw64);
+      mma_bf16(tmem + kColO + (seg_p & 1) * kN, ad, bd, idesc_pv, !(first && kk == 0));
     }
-    if (progressed) {
-      last_progress = clock64();
-    } else if (clock64() - last_progress > kWaitLimit) {
-      set_abort(S, a);
-      break;
-    }
+    mma_commit(&S.kv_empty[s]);
+    mma_commit(&S.p_empty);
+    if (last) mma_commit(&S.o_full[seg_p & 1]);
+  };
+  // one call site each: QK(0), QK(1), PV(0), QK(2), PV(1), ...
+  for (int j = 0; j < n + 2 && !aborted(S); ++j) {
+    if (j >= 2) pv(j - 2);
+    if (j < n) qk(j);
   }
   mma_commit(&S.mma_done);
   mbar_wait(&S.mma_done, 0);
 }
 
-// Query-side metadata of segment (b, h) into X, by one warp (shared memory only).
-__device__ void seg_pre(const DecodeArgs &a, const TcSmem &S, SegMeta &X, int b, int h, int lane) {
-  gather_refs(a, S.cache, X, b, lane);
-  gather_qheads(a, S.cache, X, h, lane);
+// Query-side metadata of segment (b, h) into X, by one warp (shared memory
+// only, except for views beyond the metadata cache).
+__device__ void seg_pre(const DecodeArgs &a, const TcSmem &S, SegQ &X, int b, int h, int lane) {
+  const int G = a.n_q_heads / a.n_kv_heads;
+  gather_refs(a, S.cache, X.m, b, lane);
+  gather_qheads(a, S.cache, X.m, h, lane);
+  __syncwarp();
+  if (lane < X.m.n_ref * G) {
+    const int e = X.m.ref_entry[lane / G];
+    X.qrow[lane] = (e / a.n_view) * a.n_q_heads + X.m.qhead[lane % G];
+    X.rel[lane] = entry_rel(a, S.cache, e);
+  }
   __syncwarp();
 }
 
-// Warms L2 with the queries of segment X (one warp, one 256-byte row each).
-__device__ __forceinline__ void prefetch_q(const DecodeArgs &a, const SegMeta &X, int lane) {
-  const int G = a.n_q_heads / a.n_kv_heads;
-  if (lane < X.n_ref * G && lane < kN) {
-    const int r = X.ref_entry[lane / G] / a.n_view;
-    const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
-                              (static_cast<int64_t>(r) * a.n_q_heads + X.qhead[lane % G]) * 128;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" ::"l"(qp) : "memory");
-  }
-}
-
-// One item of the rotated queries: head qi, elements 8c..8c+7 and their RoPE
-// partners 64+8c..64+8c+7, and the reference's rotation i_q - offset.
-// Columns past nq load nothing and rotate to zeros.
+// One item of the rotated queries: column qi, elements 8c..8c+7 and their
+// RoPE partners 64+8c..64+8c+7, and the column's rotation i_q - offset.  Only
+// columns below nq are rotated: the rows of Q~ past them feed S columns that
+// the softmax neither reads nor lets into P (their P is zero).
 struct QItem {
   uint4 lo, hi;
   int64_t rel;
 };
-__device__ __forceinline__ void load_item(const DecodeArgs &a, const TcSmem &S, const SegMeta &X,
-                                          int qi, int c, int nq, int G, QItem &it) {
-  it.lo = it.hi = make_uint4(0, 0, 0, 0);
-  it.rel = 0;
-  if (qi < nq) {
-    const int e = X.ref_entry[qi / G];
-    const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
-                              (static_cast<int64_t>(e / a.n_view) * a.n_q_heads + X.qhead[qi % G]) * 128;
-    it.lo = __ldg(reinterpret_cast<const uint4 *>(qp + 8 * c));
-    it.hi = __ldg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * c));
-    it.rel = entry_rel(a, S.cache, e);
-  }
+__device__ __forceinline__ void load_item(const DecodeArgs &a, const SegQ &X, int qi, int c,
+                                          QItem &it) {
+  const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
+                            static_cast<int64_t>(X.qrow[qi]) * 128;
+  it.lo = __ldg(reinterpret_cast<const uint4 *>(qp + 8 * c));
+  it.hi = __ldg(reinterpret_cast<const uint4 *>(qp + 64 + 8 * c));
+  it.rel = X.rel[qi];
 }
 
 // The item rotated and scaled by scale * log2(e) (scores leave the MMA in
 // log2 units), then split into bf16 hi and lo parts.  out[0..3]: hi of d
 // 8c.., hi of d 64+8c.., lo of d 8c.., lo of d 64+8c.. (16 bytes each).
-__device__ __forceinline__ void rot_item(const DecodeArgs &a, const QItem &it, int c, uint4 (&out)[4]) {
+__device__ __forceinline__ void rot_item(const DecodeArgs &a, const TcSmem &S, const QItem &it, int c,
+                                        uint4 (&out)[4]) {
   const uint32_t lo32[4] = {it.lo.x, it.lo.y, it.lo.z, it.lo.w};
   const uint32_t hi32[4] = {it.hi.x, it.hi.y, it.hi.z, it.hi.w};
   uint32_t w[4][4];
@@ -290,7 +282,7 @@ __device__ __forceinline__ void rot_item(const DecodeArgs &a, const QItem &it, i
       const float x0 = __uint_as_float(h2 ? (lo32[e2] & 0xffff0000u) : (lo32[e2] << 16));
       const float x1 = __uint_as_float(h2 ? (hi32[e2] & 0xffff0000u) : (hi32[e2] << 16));
       float cs, sn;
-      rope_cos_sin(it.rel, a.phase[8 * c + 2 * e2 + h2], &cs, &sn);
+      rope_cos_sin_fast(it.rel, S.cache.phase[8 * c + 2 * e2 + h2], &cs, &sn);
       ylo[h2] = (x0 * cs - x1 * sn) * a.scale_log2;
       yhi[h2] = (x1 * cs + x0 * sn) * a.scale_log2;
     }
@@ -324,48 +316,37 @@ __device__ __forceinline__ int64_t next_segment(const TcSmem &S, int n_blocks, i
 }
 
 // Prologue of warps 2-7 (the TMA and MMA warps start at once): the metadata
-// of the CTA's first kPre segments (one warp each), then the queries of
-// segment 0 - requested before the TMA warp starts the K/V stream - rotated
-// into the Q~ buffer.
+// of segment 0 (warp 2), then its queries rotated into the Q~ buffer (all six
+// warps).
 __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int t = threadIdx.x - kWarpSoft * 32;  // 0..191
   const int w = t >> 5, lane = t & 31;
   const int G = a.n_q_heads / a.n_kv_heads;
   NamedSync<3, 192> sync;
-  if (w < kPre) {
-    int64_t u = u0;
-    for (int k = 0; k < w && u < u1; ++k) u = next_segment(S, a.n_blocks, u);
-    if (u < u1) {
-      const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-      seg_pre(a, S, S.pre[w], x.b, x.h, lane);
-    }
-    if (lane == 0 && u < u1) atomicMax(&S.pre_count, w + 1);
+  if (w == 0) {
+    const UnitPos x = unit_pos(S.plan, a.n_blocks, u0);
+    seg_pre(a, S, S.pre[0], x.b, x.h, lane);
   }
   sync();
-  const SegMeta &X = S.pre[0];
-  const int nq = min(X.n_ref * G, kN);
-  // items t and t + 192 of the kN * 8 (head, 16-byte chunk) items
-  QItem q0, q1;
-  load_item(a, S, X, t >> 3, t & 7, nq, G, q0);
-  const bool two = t + 192 < kN * 8;
-  if (two) load_item(a, S, X, (t + 192) >> 3, (t + 192) & 7, nq, G, q1);
-  asm volatile("bar.arrive %0, %1;" ::"n"(kBarQIssued), "n"(224) : "memory");
+  const SegQ &X = S.pre[0];
+  const int nq = min(X.m.n_ref * G, kN);
+  // items t and t + 192 of the nq * 8 (column, 16-byte chunk) items
+  const int n_items = nq * 8;
   const uint32_t qbase = smem_u32(S.q);
-  {
+  QItem q0, q1;
+  if (t < n_items) load_item(a, X, t >> 3, t & 7, q0);
+  if (t + 192 < n_items) load_item(a, X, (t + 192) >> 3, (t + 192) & 7, q1);
+  if (t < n_items) {
     uint4 v[4];
-    rot_item(a, q0, t & 7, v);
+    rot_item(a, S, q0, t & 7, v);
     store_item(qbase, t >> 3, t & 7, v);
   }
-  if (two) {
+  if (t + 192 < n_items) {
     uint4 v[4];
-    rot_item(a, q1, (t + 192) & 7, v);
+    rot_item(a, S, q1, (t + 192) & 7, v);
     store_item(qbase, (t + 192) >> 3, (t + 192) & 7, v);
   }
-  for (int j = t; j < kMaxQ; j += 192) {
-    S.meta.ref_entry[j] = X.ref_entry[j];
-    S.meta.qhead[j] = X.qhead[j];
-  }
-  if (t == 0) S.meta.n_ref = X.n_ref;
+  if (t == 0) S.meta_nref = X.m.n_ref;
   fence_proxy_async_smem();
   sync();
   if (t == 0) mbar_arrive(&S.q_full);  // phase 0: segment 0
@@ -391,39 +372,74 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
     // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
     // warps keep the same control flow so the named barrier stays balanced.
     wait_or_abort(S, a, &S.rec_ready[done & 3], (done >> 2) & 1);
-    if (tq == 0) arrive_segment(a, S.pre[done % kPre]);
+    if (tq == 0) arrive_segment(a, S.pre[done % kPre].m);
   };
-  for (int k = 1 + wq; k < S.pre_count; k += 2) prefetch_q(a, S.pre[k], lane);
-  int64_t u = next_segment(S, a.n_blocks, u0);  // segment 1
-  int64_t u_prep = u;                            // segment kPre: the next to prepare
-  for (int k = 1; k < kPre && u_prep < u1; ++k) u_prep = next_segment(S, a.n_blocks, u_prep);
+  // metadata of segments 1 .. kPre-1 (warp k & 1)
+  int64_t us[kPre];
+  us[0] = u0;
+#pragma unroll
+  for (int k = 1; k < kPre; ++k) us[k] = us[k - 1] < u1 ? next_segment(S, a.n_blocks, us[k - 1]) : u1;
+#pragma unroll
+  for (int k = 1; k < kPre; ++k) {
+    if ((k & 1) == wq && us[k] < u1) {
+      const UnitPos x = unit_pos(S.plan, a.n_blocks, us[k]);
+      seg_pre(a, S, S.pre[k], x.b, x.h, lane);
+    }
+  }
+  sync();
+  int64_t u = us[1];                                                   // segment 1
+  int64_t u_prep = us[kPre - 1] < u1 ? next_segment(S, a.n_blocks, us[kPre - 1]) : u1;  // segment kPre
   for (int seg = 1;; ++seg) {
-    if (u >= u1) {  // no segment seg: the last arrivals
+    if (u >= u1) {
+      // no segment seg.  Until the last records arrive, prepare the merge:
+      // ranks and group indices, and the list of the CTA's first item - once
+      // the softmax warps are past their first tiles, so as not to slow them
+      {
+        // tiles_done only grows; the wait is bounded like every other
+        const int want = static_cast<int>(u1 - u0) < 3 ? static_cast<int>(u1 - u0) : 3;
+        const long long t0 = clock64();
+        while (*reinterpret_cast<volatile int32_t *>(&S.tiles_done) < want && !aborted(S)) {
+          if (clock64() - t0 > kWaitLimit) {
+            set_abort(S, a);
+            break;
+          }
+          __nanosleep(256);
+        }
+      }
+      plan_ranks(a, S.cache, wq, lane, 0, 1);
+      sync();
+      if (wq == 0 && S.cache.entries_cached) {
+        const int first = merge_rank(S.plan, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
+        int n = -1;
+        if (first < a.n_rows * a.n_q_heads) {
+          n = merge_list(a, S.plan, S.cache, first / a.n_q_heads, first % a.n_q_heads, S.mpre,
+                         kPreList, nullptr, lane);
+          if (n > kPreList) n = -1;
+        }
+        if (lane == 0) S.mpre_n = n;
+      }
       if (seg >= 2) arrivals(seg - 2);
       arrivals(seg - 1);
       break;
     }
-    const SegMeta &X = S.pre[seg % kPre];
-    const int nq = min(X.n_ref * G, kN);
-    // items tq + 64 k: head (tq >> 3) + 8 k, chunk tq & 7
+    const SegQ &X = S.pre[seg % kPre];
+    const int nq = min(X.m.n_ref * G, kN);
+    // items tq + 64 k of the nq * 8: column (tq >> 3) + 8 k, chunk tq & 7
     QItem raw[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) load_item(a, S, X, (tq >> 3) + 8 * k, tq & 7, nq, G, raw[k]);
+    for (int k = 0; k < 4; ++k)
+      if ((tq >> 3) + 8 * k < nq) load_item(a, X, (tq >> 3) + 8 * k, tq & 7, raw[k]);
     uint4 v[4][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) rot_item(a, raw[k], tq & 7, v[k]);
+    for (int k = 0; k < 4; ++k)
+      if ((tq >> 3) + 8 * k < nq) rot_item(a, S, raw[k], tq & 7, v[k]);
     // The Q~ buffer and the hand-off metadata are free once segment seg-1's
     // QK products completed and every softmax warp read the hand-off.
     wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
-    if (tq < 32) {
-      for (int j = lane; j < kMaxQ; j += 32) {
-        S.meta.ref_entry[j] = X.ref_entry[j];
-        S.meta.qhead[j] = X.qhead[j];
-      }
-      if (lane == 0) S.meta.n_ref = X.n_ref;
-    }
+    if (tq == 0) S.meta_nref = X.m.n_ref;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
+    for (int k = 0; k < 4; ++k)
+      if ((tq >> 3) + 8 * k < nq) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
     fence_proxy_async_smem();
     sync();
     if (tq == 0) mbar_arrive(&S.q_full);
@@ -432,11 +448,8 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
       sync();  // the slot of segment seg - 2 is read; it now takes segment seg + 2
       if (u_prep < u1) {
         const UnitPos x = unit_pos(S.plan, a.n_blocks, u_prep);
-        SegMeta &N = S.pre[(seg + 2) % kPre];
-        if (wq == 0) {
-          seg_pre(a, S, N, x.b, x.h, lane);
-          prefetch_q(a, N, lane);
-        }
+        SegQ &N = S.pre[(seg + 2) % kPre];
+        if (wq == 0) seg_pre(a, S, N, x.b, x.h, lane);
         u_prep = x.seg_first + x.tiles;
       }
       sync();
@@ -519,7 +532,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     if (first) {
       ++seg;
       wait_or_abort(S, a, &S.q_full, seg & 1);
-      nq = min(S.meta.n_ref * G, kN);
+      nq = min(S.meta_nref * G, kN);
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.q_empty);  // this warp has read the hand-off
 #pragma unroll
@@ -625,6 +638,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.p_full[s]);
+    if (threadIdx.x == kWarpSoft * 32) *reinterpret_cast<volatile int32_t *>(&S.tiles_done) = i + 1;
 
     if (pend >= 0) {  // records of the previous segment, one tile late
       segment_records(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync);
@@ -654,6 +668,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   TcSmem &S = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 32) {
+    // Every CTA warms L2 with its share of q before any K/V tile is asked
+    // for: query loads then hit L2 instead of queueing behind the tile
+    // stream.  q is [n_rows][Hq][128] bf16, a multiple of 256 bytes.
+    const uint64_t total = static_cast<uint64_t>(a.n_rows) * a.n_q_heads * 256;
+    const uint64_t per = ((total + gridDim.x - 1) / gridDim.x + 255) & ~static_cast<uint64_t>(255);
+    const uint64_t off = per * blockIdx.x;
+    if (off < total) {
+      const uint32_t n = static_cast<uint32_t>(total - off < per ? total - off : per);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       reinterpret_cast<const uint8_t *>(a.q) + off), "r"(n)
+                   : "memory");
+    }
+  }
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -676,7 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 4; ++b) mbar_init(&S.rec_ready[b], 4);  // one per softmax warp
     mbar_init(&S.mma_done, 1);
     S.abort_flag = 0;
-    S.pre_count = 0;
+    S.tiles_done = 0;
+    S.mpre_n = -1;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -689,13 +718,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  const int c = blockIdx.x;
-  const int64_t u0 = cta_unit_begin(S.plan, a.n_blocks, c);
-  const int64_t u1 = cta_unit_begin(S.plan, a.n_blocks, c + 1);
+  const int64_t u0 = S.plan.u0, u1 = S.plan.u1;
   if (u0 < u1) {
     if (warp == kWarpTma) {
-      // the first K/V tiles go out behind the queries of segment 0
-      asm volatile("bar.sync %0, %1;" ::"n"(kBarQIssued), "n"(224) : "memory");
       if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1);
     } else if (warp == kWarpMma) {
       if (lane == 0) mma_issuer(a, S, tmem, u0, u1);
@@ -706,6 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         qprep(a, S, u0, u1);
     }
+  } else {
+    plan_ranks(a, S.cache, warp, lane, 0, 1);  // a CTA without units: ranks for the merge
   }
   tc_fence_before();
   __syncthreads();
@@ -716,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the merge scratch lives in the tile buffers: every copy and MMA is done
   static_assert(sizeof(MergeSmem) <= kStageBytes, "merge scratch must fit in a stage");
   merge_phase<__nv_bfloat16, 128>(a, S.plan, S.cache, *reinterpret_cast<MergeSmem *>(S.stage[0]),
-                                  tid, kThreads, CtaSync(), kWaitLimit);
+                                  S.mpre, S.mpre_n, tid, kThreads, CtaSync(), kWaitLimit);
 }
 
 }  // namespace

@@ -91,6 +91,22 @@ __device__ __forceinline__ void rope_cos_sin(int64_t rel, uint64_t phase, float 
   sincospif(t, s, c);
 }
 
+// The same from the exactly reduced angle through the fast hardware sine and
+// cosine: pi * t lies in [-pi, pi), where their absolute error is at most
+// 2^-21.41 (CUDA math documentation) - far below the 16 bits that the
+// tensor-core path keeps of a rotated query.
+__device__ __forceinline__ void rope_cos_sin_fast(int64_t rel, uint64_t phase, float *c, float *s) {
+  const uint64_t turns = static_cast<uint64_t>(rel) * phase;  // mod 2^64
+  const float t = static_cast<float>(static_cast<int64_t>(turns)) * 0x1p-63f;
+  __sincosf(t * 3.14159265358979323846f, s, c);
+}
+
+// a / b for a >= 0, b > 0, in 32 bits when both fit.
+__device__ __forceinline__ int64_t div_nn(int64_t a, int64_t b) {
+  if (((a | b) >> 32) == 0) return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
+}
+
 struct CtaSync {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
 };
@@ -113,12 +129,16 @@ constexpr int kCacheEntries = 384;  // view entries (rows x view blocks) held in
 constexpr int kCacheRows = 384;     // q_pos entries held in shared memory
 
 struct MetaCache {
+  uint64_t phase[64];           // RoPE phase increments (the kernel argument's table)
   int32_t vb[kCacheEntries];    // view_block
   int32_t voff[kCacheEntries];  // view_offset
   int32_t qpos[kCacheRows];     // q_pos
-  uint8_t rank[kCacheEntries];  // the entry's position among the references to its block
   uint8_t kv_of[HW_MAX_Q_HEADS];  // q head -> kv head
+  // For the merge only, filled by plan_ranks() while the tiles stream:
+  uint8_t rank[kCacheEntries];    // the entry's position among the references to its block
   uint8_t gi_of[HW_MAX_Q_HEADS];  // q head -> its index among the kv head's q heads
+  uint8_t rcount[HW_MAX_BLOCKS];  // scratch of plan_ranks
+  uint8_t gcount[HW_MAX_Q_HEADS];
   int32_t entries_cached, rows_cached;
 };
 
@@ -161,6 +181,7 @@ struct PlanCore {
   int64_t ubase[HW_MAX_BLOCKS + 1];  // first unit of each block within a head; [n] = UH
   uint8_t sord[HW_MAX_BLOCKS];       // non-empty blocks before b
   int64_t UH, U, WH, W;              // units per head and in all; weights likewise
+  int64_t u0, u1;                    // this CTA's units
   int32_t NB, C;                     // non-empty blocks; working CTAs
 };
 
@@ -179,9 +200,26 @@ struct SegMeta {
   int32_t qhead[kMaxQ];      // q heads of the kv head, in increasing order
 };
 
+// First unit of CTA c: the first unit whose weight is >= floor(c W / C).
+__device__ __forceinline__ int64_t cta_unit_begin(const PlanCore &P, int n_blocks, int c) {
+  if (c >= P.C) return P.U;
+  const int64_t w = div_nn(P.W * c, P.C);
+  const int h = static_cast<int>(div_nn(w, P.WH));
+  const int64_t l = w - static_cast<int64_t>(h) * P.WH;
+  // the last block whose weight region [ubase + kSegW sord, ...) starts at or before l
+  int lo = 0, hi = n_blocks - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.ubase[mid] + static_cast<int64_t>(kSegW) * P.sord[mid] <= l) lo = mid; else hi = mid - 1;
+  }
+  const int64_t off = l - (P.ubase[lo] + static_cast<int64_t>(kSegW) * P.sord[lo]);
+  return static_cast<int64_t>(h) * P.UH + P.ubase[lo] + (off > kSegW ? off - kSegW : 0);
+}
+
 // Loads the metadata into the cache (one round of independent loads), checks
-// it and builds the unit prefix.  Every thread of the CTA takes part
-// (blockDim.x == 256, __syncthreads inside).
+// it and builds the unit prefix and this CTA's unit range.  Every thread of
+// the CTA takes part (blockDim.x == 256, three __syncthreads inside); one
+// warp does the serial part in a single pass.
 template <int TILE>
 __device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanScratch &S) {
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
@@ -203,6 +241,7 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanS
   const int r_bs = lb ? __ldg(a.block_start + tid) : 0;
   const int r_bl = lb ? __ldg(a.block_len + tid) : 0;
   const int r_kv = lh ? (a.q_to_kv ? __ldg(a.q_to_kv + tid) : tid / G) : 0;
+  if (tid < 64) M.phase[tid] = a.phase[tid];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int e = tid + k * nt;
@@ -222,97 +261,69 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanS
     P.len[tid] = r_bl;
     S.refs[tid] = 0;
   }
+  const bool kv_ok = r_kv >= 0 && r_kv < a.n_kv_heads;
   if (lh) {
     S.kv_cnt[tid] = 0;
-    const bool ok = r_kv >= 0 && r_kv < a.n_kv_heads;
-    M.kv_of[tid] = static_cast<uint8_t>(ok ? r_kv : 0);
+    M.kv_of[tid] = static_cast<uint8_t>(kv_ok ? r_kv : 0);
   }
   __syncthreads();
-  if (lh && (r_kv < 0 || r_kv >= a.n_kv_heads)) S.headmap_ok = 0;
 
+  // 2. references per block and q heads per kv head
+  for (int e = tid; e < E; e += nt) {
+    const int b = ecached ? M.vb[e] : __ldg(a.view_block + e);
+    if (b >= a.n_blocks || b < -1) {
+      if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_BLOCK);
+    } else if (b >= 0) {
+      atomicAdd(&S.refs[b], 1);
+    }
+  }
+  if (lh) {
+    if (kv_ok) atomicAdd(&S.kv_cnt[r_kv], 1);
+    else S.headmap_ok = 0;
+  }
+  __syncthreads();
+
+  // 3. one warp: tiles per block, the prefixes, the totals, this CTA's range
   if (warp == 0) {
-    // references per block, and each entry's rank among its block's references
-    if (ecached) {
-      for (int base = 0; base < E; base += 32) {
-        const int e = base + lane;
-        const int b = e < E ? M.vb[e] : -1;
-        const bool valid = b >= 0 && b < a.n_blocks;
-        if (e < E && !valid && b != -1 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_BLOCK);
-        const unsigned m = __match_any_sync(0xffffffffu, valid ? b : -2 - lane);
-        const int before = valid ? S.refs[b] : 0;
-        const int rk = before + __popc(m & lanemask_lt(lane));
-        if (e < E) M.rank[e] = static_cast<uint8_t>(rk < 255 ? rk : 255);
-        __syncwarp();
-        if (valid && lane == 31 - __clz(m)) S.refs[b] = before + __popc(m);
-        __syncwarp();
-      }
-    } else {
-      for (int e = lane; e < E; e += 32) {
-        const int b = __ldg(a.view_block + e);
-        if (b >= a.n_blocks || b < -1) {
-          if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_BLOCK);
-        } else if (b >= 0) {
-          atomicAdd(&S.refs[b], 1);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // each q head's index within its kv head's group; every group must have G
-    for (int base = 0; base < Hq; base += 32) {
-      const int hq = base + lane;
-      const int g = hq < Hq ? M.kv_of[hq] : 0;
-      const unsigned m = __match_any_sync(0xffffffffu, hq < Hq ? g : -2 - lane);
-      const int before = hq < Hq ? S.kv_cnt[g] : 0;
-      if (hq < Hq) {
-        const int gi = before + __popc(m & lanemask_lt(lane));
-        M.gi_of[hq] = static_cast<uint8_t>(gi < 255 ? gi : 255);
-      }
-      __syncwarp();
-      if (hq < Hq && lane == 31 - __clz(m)) S.kv_cnt[g] = before + __popc(m);
-      __syncwarp();
-    }
     for (int h = lane; h < a.n_kv_heads; h += 32)
       if (S.kv_cnt[h] != G) S.headmap_ok = 0;
-  }
-  __syncthreads();
-  if (!S.headmap_ok && tid == 0 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_HEADMAP);
-  for (int b = tid; b < a.n_blocks; b += nt) {
-    const int32_t s = P.start[b], n = P.len[b];
-    int t = 0;
-    if (s < 0 || n < 0 || static_cast<int64_t>(s) + n > a.capacity) {
-      if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_RANGE);
-    } else if (S.refs[b] > 0 && n > 0) {
-      if (S.refs[b] * G > kMaxQ) {
-        if (blockIdx.x == 0) flag_error(a.err, HW_DEV_TOO_MANY_REFS);
-      } else {
-        t = (n + TILE - 1) / TILE;
-      }
-    }
-    P.tiles[b] = S.headmap_ok ? t : 0;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // exclusive prefixes over blocks: tiles (ubase) and non-empty blocks (sord)
+    __syncwarp();
+    const bool hm_ok = S.headmap_ok != 0;
     int64_t carry = 0;
     int ncarry = 0;
     for (int base = 0; base < a.n_blocks; base += 32) {
       const int b = base + lane;
-      const int64_t x = (b < a.n_blocks) ? static_cast<int64_t>(P.tiles[b]) : 0;
-      int64_t incl = x;
+      int t = 0;
+      if (b < a.n_blocks) {
+        const int32_t st = P.start[b], n = P.len[b], refs = S.refs[b];
+        if (st < 0 || n < 0 || static_cast<int64_t>(st) + n > a.capacity) {
+          if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_RANGE);
+        } else if (refs > 0 && n > 0) {
+          if (refs * G > kMaxQ) {
+            if (blockIdx.x == 0) flag_error(a.err, HW_DEV_TOO_MANY_REFS);
+          } else {
+            t = (n + TILE - 1) / TILE;
+          }
+        }
+        if (!hm_ok) t = 0;
+        P.tiles[b] = t;
+      }
+      int64_t incl = t;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      const unsigned ne = __ballot_sync(0xffffffffu, x > 0);
+      const unsigned ne = __ballot_sync(0xffffffffu, t > 0);
       if (b < a.n_blocks) {
-        P.ubase[b] = carry + incl - x;
+        P.ubase[b] = carry + incl - t;
         P.sord[b] = static_cast<uint8_t>(ncarry + __popc(ne & lanemask_lt(lane)));
       }
       carry += __shfl_sync(0xffffffffu, incl, 31);
       ncarry += __popc(ne);
     }
     if (lane == 0) {
+      if (!hm_ok && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_HEADMAP);
       P.ubase[a.n_blocks] = carry;
       P.UH = carry;
       P.U = carry * a.n_kv_heads;
@@ -322,8 +333,62 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanS
       const int64_t cmax = P.W / (kSegW + 1);
       P.C = static_cast<int>(cmax < static_cast<int64_t>(gridDim.x) ? cmax : gridDim.x);
     }
+    __syncwarp();
+    // lanes 0 and 1: the two ends of this CTA's unit range, side by side
+    if (lane < 2) {
+      const int64_t u = cta_unit_begin(P, a.n_blocks, blockIdx.x + lane);
+      if (lane == 0) P.u0 = u; else P.u1 = u;
+    }
   }
   __syncthreads();
+}
+
+// Entry ranks and q-head group indices for the merge (cached views only):
+// warp `wr` ranks the view entries, warp `wg` the q heads.  Called by two
+// warps that are idle while the tiles stream; the results are read after a
+// later CTA-wide barrier.
+__device__ __forceinline__ void plan_ranks(const DecodeArgs &a, MetaCache &M, int warp, int lane,
+                                           int wr, int wg) {
+  const int E = a.n_rows * a.n_view;
+  if (warp == wr && M.entries_cached) {
+    for (int b = lane; b < a.n_blocks; b += 32) M.rcount[b] = 0;
+    __syncwarp();
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int b = e < E ? M.vb[e] : -1;
+      const bool valid = b >= 0 && b < a.n_blocks;
+      const unsigned m = __match_any_sync(0xffffffffu, valid ? b : -2 - lane);
+      const int before = valid ? M.rcount[b] : 0;
+      const int rk = before + __popc(m & lanemask_lt(lane));
+      if (e < E) M.rank[e] = static_cast<uint8_t>(rk < 255 ? rk : 255);
+      __syncwarp();
+      if (valid && lane == 31 - __clz(m)) {
+        const int n = before + __popc(m);
+        M.rcount[b] = static_cast<uint8_t>(n < 255 ? n : 255);
+      }
+      __syncwarp();
+    }
+  } else if (warp == wg) {
+    const int Hq = a.n_q_heads;
+    for (int h = lane; h < a.n_kv_heads; h += 32) M.gcount[h] = 0;
+    __syncwarp();
+    for (int base = 0; base < Hq; base += 32) {
+      const int hq = base + lane;
+      const int g = hq < Hq ? M.kv_of[hq] : 0;
+      const unsigned m = __match_any_sync(0xffffffffu, hq < Hq ? g : -2 - lane);
+      const int before = hq < Hq ? M.gcount[g] : 0;
+      if (hq < Hq) {
+        const int gi = before + __popc(m & lanemask_lt(lane));
+        M.gi_of[hq] = static_cast<uint8_t>(gi < 255 ? gi : 255);
+      }
+      __syncwarp();
+      if (hq < Hq && lane == 31 - __clz(m)) {
+        const int n = before + __popc(m);
+        M.gcount[g] = static_cast<uint8_t>(n < 255 ? n : 255);
+      }
+      __syncwarp();
+    }
+  }
 }
 
 // Block that holds in-head unit u (ubase[b] <= u < ubase[b+1]), by binary search.
@@ -343,7 +408,7 @@ struct UnitPos {
 };
 __device__ __forceinline__ UnitPos unit_pos(const PlanCore &P, int n_blocks, int64_t u) {
   UnitPos x;
-  x.h = static_cast<int>(u / P.UH);
+  x.h = static_cast<int>(div_nn(u, P.UH));
   const int64_t local = u - static_cast<int64_t>(x.h) * P.UH;
   x.b = block_of_unit(P, n_blocks, local);
   x.tiles = P.tiles[x.b];
@@ -354,7 +419,7 @@ __device__ __forceinline__ UnitPos unit_pos(const PlanCore &P, int n_blocks, int
 
 // Weight of unit u (strictly increasing in u).
 __device__ __forceinline__ int64_t unit_weight(const PlanCore &P, int n_blocks, int64_t u) {
-  const int h = static_cast<int>(u / P.UH);
+  const int h = static_cast<int>(div_nn(u, P.UH));
   const int64_t local = u - static_cast<int64_t>(h) * P.UH;
   const int b = block_of_unit(P, n_blocks, local);
   return static_cast<int64_t>(h) * P.WH + local + static_cast<int64_t>(kSegW) * (P.sord[b] + 1);
@@ -362,59 +427,43 @@ __device__ __forceinline__ int64_t unit_weight(const PlanCore &P, int n_blocks, 
 
 // The CTA that owns unit u: the largest c with floor(c W / C) <= weight(u).
 __device__ __forceinline__ int cta_of_unit(const PlanCore &P, int n_blocks, int64_t u) {
-  return static_cast<int>(((unit_weight(P, n_blocks, u) + 1) * P.C - 1) / P.W);
-}
-
-// First unit of CTA c: the first unit whose weight is >= floor(c W / C).
-__device__ __forceinline__ int64_t cta_unit_begin(const PlanCore &P, int n_blocks, int c) {
-  if (c >= P.C) return P.U;
-  const int64_t w = (P.W * c) / P.C;
-  const int h = static_cast<int>(w / P.WH);
-  const int64_t l = w - static_cast<int64_t>(h) * P.WH;
-  // the last block whose weight region [ubase + kSegW sord, ...) starts at or before l
-  int lo = 0, hi = n_blocks - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.ubase[mid] + static_cast<int64_t>(kSegW) * P.sord[mid] <= l) lo = mid; else hi = mid - 1;
-  }
-  const int64_t off = l - (P.ubase[lo] + static_cast<int64_t>(kSegW) * P.sord[lo]);
-  return static_cast<int64_t>(h) * P.UH + P.ubase[lo] + (off > kSegW ? off - kSegW : 0);
+  return static_cast<int>(div_nn((unit_weight(P, n_blocks, u) + 1) * P.C - 1, P.W));
 }
 
 __device__ __forceinline__ int64_t seg_id(int n_blocks, int b, int h) {
   return static_cast<int64_t>(h) * n_blocks + b;
 }
 
-// The view entries referencing block b, in entry order (one warp).
+// The view entries referencing block b, in entry order (one warp); an
+// entry's position here is its rank among the block's references.
 __device__ __forceinline__ void gather_refs(const DecodeArgs &a, const MetaCache &C, SegMeta &M,
                                             int b, int lane) {
   const int E = a.n_rows * a.n_view;
   int cnt = 0;
-  if (C.entries_cached) {
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const bool m = e < E && C.vb[e] == b;
-      if (m && C.rank[e] < kMaxQ) M.ref_entry[C.rank[e]] = e;
-      cnt += __popc(__ballot_sync(0xffffffffu, m));
-    }
-  } else {
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const bool m = e < E && __ldg(a.view_block + e) == b;
-      const unsigned mask = __ballot_sync(0xffffffffu, m);
-      const int pos = cnt + __popc(mask & lanemask_lt(lane));
-      if (m && pos < kMaxQ) M.ref_entry[pos] = e;
-      cnt += __popc(mask);
-    }
+  for (int base = 0; base < E; base += 32) {
+    const int e = base + lane;
+    const bool m = e < E && vb_at(a, C, e) == b;
+    const unsigned mask = __ballot_sync(0xffffffffu, m);
+    const int pos = cnt + __popc(mask & lanemask_lt(lane));
+    if (m && pos < kMaxQ) M.ref_entry[pos] = e;
+    cnt += __popc(mask);
   }
   if (lane == 0) M.n_ref = cnt;
 }
 
-// The q heads of kv head h, in increasing order (one warp).
+// The q heads of kv head h, in increasing order (one warp); a q head's
+// position here is its group index gi.
 __device__ __forceinline__ void gather_qheads(const DecodeArgs &a, const MetaCache &C, SegMeta &M,
                                               int h, int lane) {
-  for (int hq = lane; hq < a.n_q_heads; hq += 32)
-    if (C.kv_of[hq] == h && C.gi_of[hq] < kMaxQ) M.qhead[C.gi_of[hq]] = hq;
+  int cnt = 0;
+  for (int base = 0; base < a.n_q_heads; base += 32) {
+    const int hq = base + lane;
+    const bool m = hq < a.n_q_heads && C.kv_of[hq] == h;
+    const unsigned mask = __ballot_sync(0xffffffffu, m);
+    const int pos = cnt + __popc(mask & lanemask_lt(lane));
+    if (m && pos < kMaxQ) M.qhead[pos] = hq;
+    cnt += __popc(mask);
+  }
 }
 
 __device__ __forceinline__ float *record_ptr(const DecodeArgs &a, int64_t slot, int qi) {
@@ -459,82 +508,102 @@ __device__ __forceinline__ void lse_combine(float &M, float &L, float m, float l
 // it in its tile buffers, idle by then).
 struct MergeSmem {
   int32_t list[kMaxRecords];  // record index of each partial: slot * 32 + rank * G + gi
-  float mlist[kMaxRecords];   // its max m (log2 domain)
   float acc[8][128];          // per warp partial sums of the output row
+  float wm[8], wl[8];         // per warp running max and normaliser
   int32_t rank_tmp[HW_MAX_VIEW_BLOCKS];  // entry ranks of one row (views beyond the cache)
   int32_t n_rec, ok;
-  float M, L;
 };
+
+// Position of CTA c in the order items are dealt: CTAs without units first.
+__device__ __forceinline__ int merge_rank(const PlanCore &P, int c, int grid) {
+  return c >= P.C ? c - P.C : c + (grid - P.C);
+}
+
+// The record list of merge item (row r, q head hq) in view order, built by
+// one warp: for every view entry, the records that the CTAs c0..c1 touching
+// segment (block, kv head) wrote at column rank * G + gi.  Returns the number
+// of records (in every lane); entries at or past `cap` are not written.
+// rank_tmp (HW_MAX_VIEW_BLOCKS ints) is scratch for views beyond the cache.
+__device__ __forceinline__ int merge_list(const DecodeArgs &a, const PlanCore &P,
+                                          const MetaCache &MC, int r, int hq, int32_t *list,
+                                          int cap, int32_t *rank_tmp, int lane) {
+  const int V = a.n_view, G = a.n_q_heads / a.n_kv_heads;
+  const int h = MC.kv_of[hq], gi = MC.gi_of[hq];
+  if (!MC.entries_cached) {
+    for (int v = 0; v < V; ++v) {
+      const int rk = entry_rank_scan(a, r * V + v, lane);
+      if (lane == 0) rank_tmp[v] = rk;
+    }
+    __syncwarp();
+  }
+  int off = 0;
+  for (int v0 = 0; v0 < V; v0 += 32) {
+    const int v = v0 + lane;
+    int cnt = 0, col = 0;
+    int64_t slot0 = 0;
+    if (v < V) {
+      const int e = r * V + v;
+      const int b = vb_at(a, MC, e);
+      if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
+        const int64_t s0 = static_cast<int64_t>(h) * P.UH + P.ubase[b];
+        const int c0 = cta_of_unit(P, a.n_blocks, s0);
+        cnt = cta_of_unit(P, a.n_blocks, s0 + P.tiles[b] - 1) - c0 + 1;
+        slot0 = seg_id(a.n_blocks, b, h) + c0;
+        col = (MC.entries_cached ? MC.rank[e] : rank_tmp[v]) * G + gi;
+      }
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int my = off + incl - cnt;
+    for (int j = 0; j < cnt; ++j)
+      if (my + j < cap) list[my + j] = static_cast<int32_t>((slot0 + j) * kMaxQ + col);
+    off += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return off;
+}
 
 // The merge phase.  Every thread of every CTA of the (cooperative) grid calls
 // it once its own units are done.  Work item = (row r, q head hq): all the
 // partial records of that output row, each from one (view entry, CTA) pair.
 // Items go round-robin over the CTAs, those without units first.  An item's
-// owner lists its records from the plan, waits (bounded) until the item's
-// arrival counter shows every record, then merges with the whole CTA:
+// owner lists its records from the plan (the first item's list may come
+// ready-made in pre_list / pre_n, else pre_n < 0), waits (bounded) until the
+// item's arrival counter shows every record, then merges with the whole CTA:
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
 //   lse = (M + log2 L) ln 2;
 // an item without records gets out = 0, lse = -inf.
 template <typename T, int D, typename Sync>
 __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCache &MC,
-                            MergeSmem &Z, int tid, int nt, Sync sync, long long wait_limit) {
+                            MergeSmem &Z, const int32_t *pre_list, int pre_n, int tid, int nt,
+                            Sync sync, long long wait_limit) {
   constexpr int EPL = D / 32;
   constexpr int64_t RS = D + 4;  // record stride in floats
-  const int V = a.n_view;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
-  const int G = a.n_q_heads / a.n_kv_heads;
   const int items = a.n_rows * a.n_q_heads;
-  const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  const int rank = c >= P.C ? c - P.C : c + (grid - P.C);
+  const int grid = static_cast<int>(gridDim.x);
+  const int rank = merge_rank(P, static_cast<int>(blockIdx.x), grid);
 
   for (int it = rank; it < items; it += grid) {
     const int r = it / a.n_q_heads, hq = it % a.n_q_heads;
-    const int h = MC.kv_of[hq], gi = MC.gi_of[hq];
-    if (warp == 0) {
-      if (!MC.entries_cached) {
-        for (int v = 0; v < V; ++v) {
-          const int rk = entry_rank_scan(a, r * V + v, lane);
-          if (lane == 0) Z.rank_tmp[v] = rk;
-        }
-        __syncwarp();
-      }
-      // per view entry: the CTAs c0..c1 that wrote records of segment (b, h),
-      // and the record column rank * G + gi; then the flat list in view order
-      int off = 0;
-      for (int v0 = 0; v0 < V; v0 += 32) {
-        const int v = v0 + lane;
-        int cnt = 0, col = 0;
-        int64_t slot0 = 0;
-        if (v < V) {
-          const int e = r * V + v;
-          const int b = vb_at(a, MC, e);
-          if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
-            const int64_t s0 = static_cast<int64_t>(h) * P.UH + P.ubase[b];
-            const int c0 = cta_of_unit(P, a.n_blocks, s0);
-            cnt = cta_of_unit(P, a.n_blocks, s0 + P.tiles[b] - 1) - c0 + 1;
-            slot0 = seg_id(a.n_blocks, b, h) + c0;
-            col = (MC.entries_cached ? MC.rank[e] : Z.rank_tmp[v]) * G + gi;
-          }
-        }
-        int incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const int my = off + incl - cnt;
-        for (int j = 0; j < cnt; ++j)
-          if (my + j < kMaxRecords) Z.list[my + j] = static_cast<int32_t>((slot0 + j) * kMaxQ + col);
-        off += __shfl_sync(0xffffffffu, incl, 31);
-      }
+    // the first item's list may have been built while the tiles streamed
+    const bool pre = it == rank && pre_n >= 0;
+    if (pre) {
+      if (tid == 0) Z.n_rec = pre_n;
+    } else if (warp == 0) {
+      int n = merge_list(a, P, MC, r, hq, Z.list, kMaxRecords, Z.rank_tmp, lane);
       if (lane == 0) {
-        if (off > kMaxRecords) {
+        if (n > kMaxRecords) {
           flag_error(a.err, HW_DEV_TOO_MANY_REFS);
-          off = kMaxRecords;
+          n = kMaxRecords;
         }
-        Z.n_rec = off;
+        Z.n_rec = n;
       }
     }
+    const int32_t *list = pre ? pre_list : Z.list;
     sync();
     const int n_rec = Z.n_rec;
     const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
@@ -561,56 +630,50 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
     }
     sync();
     if (Z.ok) {
-      if (warp == 0) {  // pass A: the maxima and the normaliser
-        float Mx = -INFINITY, Lx = 0.f;
-        for (int k = lane; k < n_rec; k += 32) {
-          const float *rec = a.partials + static_cast<int64_t>(Z.list[k]) * RS;
-          const float m = __ldcg(rec + D);
-          Z.mlist[k] = m;
-          lse_combine(Mx, Lx, m, __ldcg(rec + D + 1));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float m2 = __shfl_xor_sync(0xffffffffu, Mx, o);
-          const float l2 = __shfl_xor_sync(0xffffffffu, Lx, o);
-          lse_combine(Mx, Lx, m2, l2);
-        }
-        if (lane == 0) {
-          Z.M = Mx;
-          Z.L = Lx;
-        }
-      }
-      sync();
-      // pass B: warp w takes records w, w + nwarps, ...; lane j owns elements
-      // [j * EPL, (j+1) * EPL) of the row
-      const float Mx = Z.M;
-      float acc[EPL];
+      // one pass: warp w folds records w, w + nwarps, ... into a running
+      // (m, l, o) - lane j owns elements [j * EPL, (j+1) * EPL) of the row -
+      // then the warps' partials are combined through shared memory
+      float Mw = -INFINITY, Lw = 0.f, acc[EPL];
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-#pragma unroll 4
       for (int k = warp; k < n_rec; k += nwarps) {
-        const float w = ex2(Z.mlist[k] - Mx);
-        const float *o = a.partials + static_cast<int64_t>(Z.list[k]) * RS + lane * EPL;
+        const float *rec = a.partials + static_cast<int64_t>(list[k]) * RS;
+        const float m = __ldcg(rec + D), l = __ldcg(rec + D + 1);
+        float x[EPL];
         if constexpr (EPL == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
-          acc[0] += w * x.x;
-          acc[1] += w * x.y;
-          acc[2] += w * x.z;
-          acc[3] += w * x.w;
+          const float4 v = __ldcg(reinterpret_cast<const float4 *>(rec + lane * EPL));
+          x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
         } else {
-          const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
-          acc[0] += w * x.x;
-          acc[1] += w * x.y;
+          const float2 v = __ldcg(reinterpret_cast<const float2 *>(rec + lane * EPL));
+          x[0] = v.x; x[1] = v.y;
         }
+        if (m == -INFINITY) continue;  // an empty partial adds nothing
+        const float Mn = fmaxf(Mw, m);
+        const float sa = ex2(Mw - Mn), sb = ex2(m - Mn);  // sa = 0 while Mw = -inf
+        Lw = Lw * sa + l * sb;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * sa + x[e] * sb;
+        Mw = Mn;
       }
 #pragma unroll
       for (int e = 0; e < EPL; ++e) Z.acc[warp][lane * EPL + e] = acc[e];
+      if (lane == 0) {
+        Z.wm[warp] = Mw;
+        Z.wl[warp] = Lw;
+      }
       sync();
       if (tid < D) {
-        float sum = 0.f;
-        for (int w2 = 0; w2 < nwarps; ++w2) sum += Z.acc[w2][tid];
-        reinterpret_cast<T *>(a.out)[ob * D + tid] = from_f32<T>(sum / Z.L);
-        if (tid == 0 && a.lse) a.lse[ob] = (Z.M + __log2f(Z.L)) * 0.69314718055994530942f;
+        float Mx = -INFINITY;
+        for (int w2 = 0; w2 < nwarps; ++w2) Mx = fmaxf(Mx, Z.wm[w2]);
+        float sum = 0.f, L = 0.f;
+        for (int w2 = 0; w2 < nwarps; ++w2) {
+          if (Z.wm[w2] == -INFINITY) continue;
+          const float f = ex2(Z.wm[w2] - Mx);
+          sum += Z.acc[w2][tid] * f;
+          L += Z.wl[w2] * f;
+        }
+        reinterpret_cast<T *>(a.out)[ob * D + tid] = from_f32<T>(sum / L);
+        if (tid == 0 && a.lse) a.lse[ob] = (Mx + __log2f(L)) * 0.69314718055994530942f;
       }
     }
     sync();
