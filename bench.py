@@ -37,6 +37,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--config", default="C3", choices=["C2", "C3", "C4", "C5"])
     p.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph")
+    p.add_argument("--unplanned", action="store_true",
+                   help="one hw_attn_decode per layer instead of hw_attn_plan once per step "
+                        "plus hw_attn_decode_planned per layer")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     p.add_argument("--layers", type=int, default=0,
@@ -201,10 +204,21 @@ def main():
     kernel = "decode_tc_kernel" if (w.dtype == "bf16" and w.head_dim == 128) else "decode_simt_kernel"
     stream = torch.cuda.Stream(device=dev)
 
-    def step():
+    planned = not args.unplanned
+
+    def layer_calls(qsrc):
+        # a decode step: the views are planned once, then every layer runs
+        if planned:
+            sess.plan(stream=stream)
         for i in range(calls_per_step):
             l = i % L
-            sess.decode(qs[l], ks[l], vs[l], out=outs[l], lse=lses[l], stream=stream)
+            if planned:
+                sess.decode_planned(qsrc[l], ks[l], vs[l], out=outs[l], lse=lses[l], stream=stream)
+            else:
+                sess.decode(qsrc[l], ks[l], vs[l], out=outs[l], lse=lses[l], stream=stream)
+
+    def step():
+        layer_calls(qs)
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -277,9 +291,7 @@ def main():
                     sess.meta[name].copy_(m, non_blocking=True)
                 for l in range(L):
                     qdev[l].copy_(q_host[l], non_blocking=True)
-                for i in range(calls_per_step):
-                    l = i % L
-                    sess.decode(qdev[l], ks[l], vs[l], out=outs[l], lse=lses[l], stream=stream)
+                layer_calls(qdev)
                 for l in range(L):
                     o_host[l].copy_(outs[l], non_blocking=True)
                     l_host[l].copy_(lses[l], non_blocking=True)
@@ -312,6 +324,8 @@ def main():
             "head_dim": w.head_dim, "kv_tokens_per_layer": w.kv_tokens(),
             "kv_bytes_per_step": step_bytes, "parallelism": f"replicas x{world}",
             "mode": "eager" if graph is None else "cuda-graph",
+            "calls": ("hw_attn_plan once per step + hw_attn_decode_planned per layer" if planned
+                      else "hw_attn_decode per layer"),
             "l2": "inputs larger than L2: each step reads every layer's own KV pools "
                   f"({step_bytes / 1e9:.2f} GB per step vs 0.13 GB of L2)",
         },
@@ -319,8 +333,9 @@ def main():
         "worker_tokens_per_s_per_layer": w.n_rows / per_launch,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
-                     "kernel": f"hw_attn_decode ({kernel})"},
-        "gpu_launches": calls_per_step * args.steps,
+                     "kernel": f"{'hw_attn_decode_planned' if planned else 'hw_attn_decode'} ({kernel})",
+                     "per_launch": "step time / layers per step (the plan launch included)"},
+        "gpu_launches": (calls_per_step + (1 if planned else 0)) * args.steps,
         "clocks": clk.summary(),
         "e2e": e2e,
     }

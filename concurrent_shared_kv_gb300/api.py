@@ -21,11 +21,11 @@ HW_F32, HW_BF16 = 0, 1
 STATUS = {0: "HW_OK", -1: "HW_ERR_INVALID", -2: "HW_ERR_UNSUPPORTED", -3: "HW_ERR_WORKSPACE",
           -4: "HW_ERR_CAPACITY", -5: "HW_ERR_OVERLAP", -6: "HW_ERR_CUDA", -7: "HW_ERR_DEVICE"}
 DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMAP",
-             8: "HW_DEV_TOO_MANY_REFS", 16: "HW_DEV_TIMEOUT"}
+             8: "HW_DEV_TOO_MANY_REFS", 16: "HW_DEV_TIMEOUT", 32: "HW_DEV_BAD_PLAN"}
 
 # every symbol the header declares
 EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode",
-           "hw_attn_decode_noalloc",
+           "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_decode_noalloc",
            "hw_block_commit", "hw_workspace_status", "hw_views_combined", "hw_last_cuda_error",
            "hw_status_string"]
 
@@ -68,6 +68,8 @@ def lib(path: Optional[str] = None):
     L.hw_attn_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_size_t)]
     L.hw_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
     L.hw_attn_decode.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12 + [ctypes.c_size_t, _P]
+    L.hw_attn_plan.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 7 + [ctypes.c_size_t, _P]
+    L.hw_attn_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 6 + [ctypes.c_size_t, _P]
     L.hw_attn_decode_noalloc.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12
     L.hw_block_commit.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
@@ -142,6 +144,26 @@ def attn_decode(desc: AttnDesc, q, k_cache, v_cache, block_start, block_len, vie
                               _ptr(view_offset), _ptr(q_pos), _ptr(q_to_kv), _ptr(out), _ptr(lse),
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check("hw_attn_decode", st)
+    return st
+
+
+def attn_plan(desc: AttnDesc, block_start, block_len, view_block, view_offset, q_pos, workspace,
+              workspace_bytes: int, q_to_kv=None, stream=None) -> int:
+    """hw_attn_plan: the step's metadata planned once into the workspace."""
+    st = lib().hw_attn_plan(ctypes.byref(desc), _ptr(block_start), _ptr(block_len), _ptr(view_block),
+                            _ptr(view_offset), _ptr(q_pos), _ptr(q_to_kv), _ptr(workspace),
+                            int(workspace_bytes), _stream(stream))
+    _check("hw_attn_plan", st)
+    return st
+
+
+def attn_decode_planned(desc: AttnDesc, q, k_cache, v_cache, out, lse, workspace,
+                        workspace_bytes: int, stream=None) -> int:
+    """hw_attn_decode_planned: one layer against the plan in the workspace."""
+    st = lib().hw_attn_decode_planned(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                                      _stream(stream))
+    _check("hw_attn_decode_planned", st)
     return st
 
 

@@ -101,8 +101,35 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
   L.partials_off = L.counters_off + up(counters);
   L.slots = static_cast<int64_t>(d.n_blocks) * d.n_kv_heads + max_ctas;
   const size_t rec = static_cast<size_t>(kMaxQ) * (d.head_dim + 4) * sizeof(float);
-  L.total = L.partials_off + up(static_cast<size_t>(L.slots) * rec);
+  L.meta_off = L.partials_off + up(static_cast<size_t>(L.slots) * rec);
+  // metadata copies: view_block, view_offset (rows x V), q_pos, q_to_kv, block_start, block_len
+  const size_t entries = static_cast<size_t>(d.n_rows) * d.max_view_blocks;
+  const size_t meta = (2 * entries + d.n_rows + d.n_q_heads + 2 * static_cast<size_t>(d.n_blocks)) *
+                      sizeof(int32_t);
+  L.plan_off = L.meta_off + up(meta);
+  // the tensor-core plan: one record per CTA of its grid (one per SM)
+  const int sms = device_sm_count();
+  const size_t plan = kPlanHeaderBytes + plan_shared_bytes() +
+                      static_cast<size_t>(sms > 0 ? sms : 0) * plan_cta_bytes();
+  L.total = L.plan_off + up(plan);
   return L;
+}
+
+// The metadata copies of a workspace (written by hw_attn_plan).
+struct MetaCopies {
+  int32_t *view_block, *view_offset, *q_pos, *q_to_kv, *block_start, *block_len;
+};
+static MetaCopies meta_copies(const hw_attn_desc &d, const WorkspaceLayout &L, void *workspace) {
+  int32_t *m = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.meta_off);
+  const size_t entries = static_cast<size_t>(d.n_rows) * d.max_view_blocks;
+  MetaCopies c;
+  c.view_block = m;
+  c.view_offset = c.view_block + entries;
+  c.q_pos = c.view_offset + entries;
+  c.q_to_kv = c.q_pos + d.n_rows;
+  c.block_start = c.q_to_kv + d.n_q_heads;
+  c.block_len = c.block_start + d.n_blocks;
+  return c;
 }
 
 static int check_desc(const hw_attn_desc *d) {
@@ -147,38 +174,24 @@ int hw_workspace_init(void *workspace, size_t bytes, void *stream) {
   return e == cudaSuccess ? HW_OK : cuda_fail(e);
 }
 
-int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, const void *v_cache,
-                   const int32_t *block_start, const int32_t *block_len,
-                   const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
-                   const int32_t *q_to_kv, void *out, float *lse, void *workspace,
-                   size_t workspace_bytes, void *stream) {
-  int st = check_desc(d);
-  if (st != HW_OK) return st;
-  if (d->n_rows == 0) return HW_OK;
-  if (!q || !out || !q_pos) return HW_ERR_INVALID;
-  if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
-  if (d->n_blocks > 0 && (!block_start || !block_len)) return HW_ERR_INVALID;
-  // an empty pool (capacity 0) is never read and may be NULL
-  if (d->n_blocks > 0 && d->cache_capacity > 0 && (!k_cache || !v_cache)) return HW_ERR_INVALID;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return HW_ERR_WORKSPACE;
-  const int max_ctas = max_decode_ctas();
-  if (max_ctas <= 0) return cuda_fail(cudaGetLastError());
-  const WorkspaceLayout L = workspace_layout(*d, max_ctas);
-  if (workspace_bytes < L.total) return HW_ERR_WORKSPACE;
+}  // extern "C"
 
-  DecodeArgs a;
+namespace hw {
+
+// Workspace checks shared by hw_attn_decode, hw_attn_decode_planned and
+// hw_attn_plan (after the description and argument checks); fills the layout.
+static int check_workspace(const hw_attn_desc *d, void *workspace, size_t workspace_bytes,
+                           WorkspaceLayout *L, int *max_ctas) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return HW_ERR_WORKSPACE;
+  *max_ctas = max_decode_ctas();
+  if (*max_ctas <= 0) return cuda_fail(cudaGetLastError());
+  *L = workspace_layout(*d, *max_ctas);
+  if (workspace_bytes < L->total) return HW_ERR_WORKSPACE;
+  return HW_OK;
+}
+
+static void fill_args(DecodeArgs &a, const hw_attn_desc *d, const WorkspaceLayout &L, void *workspace) {
   std::memset(&a, 0, sizeof a);
-  a.q = q;
-  a.k = k_cache;
-  a.v = v_cache;
-  a.block_start = block_start;
-  a.block_len = block_len;
-  a.view_block = view_block;
-  a.view_offset = view_offset;
-  a.q_pos = q_pos;
-  a.q_to_kv = q_to_kv;
-  a.out = out;
-  a.lse = lse;
   char *ws = static_cast<char *>(workspace);
   a.err = reinterpret_cast<int32_t *>(ws + L.err_off);
   a.counters = reinterpret_cast<int32_t *>(ws + L.counters_off);
@@ -192,12 +205,40 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
   a.capacity = d->cache_capacity;
   a.scale_log2 = static_cast<float>(static_cast<double>(d->scale) * 1.4426950408889634074);
   rope_phase_table(d->head_dim, d->rope_theta, a.phase);
+}
+
+static bool tensor_core_path(const hw_attn_desc *d) {
+  return d->dtype == HW_BF16 && d->head_dim == 128;
+}
+
+// One decode launch: metadata from the caller (plan null) or from the
+// workspace copies with the step's plan.
+static int decode_common(const hw_attn_desc *d, const void *q, const void *k_cache,
+                         const void *v_cache, const int32_t *block_start, const int32_t *block_len,
+                         const int32_t *view_block, const int32_t *view_offset,
+                         const int32_t *q_pos, const int32_t *q_to_kv, const uint8_t *plan,
+                         void *out, float *lse, void *workspace, const WorkspaceLayout &L,
+                         int max_ctas, void *stream) {
+  DecodeArgs a;
+  fill_args(a, d, L, workspace);
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.block_start = block_start;
+  a.block_len = block_len;
+  a.view_block = view_block;
+  a.view_offset = view_offset;
+  a.q_pos = q_pos;
+  a.q_to_kv = q_to_kv;
+  a.out = out;
+  a.lse = lse;
 
   const int sms = device_sm_count();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (d->dtype == HW_BF16 && d->head_dim == 128) {
+  if (tensor_core_path(d)) {
     // tensor-core path: one persistent CTA per SM, K/V tiles by TMA
+    a.plan = plan;
     const bool have_pool = d->n_blocks > 0 && d->cache_capacity > 0;
     if (reinterpret_cast<uintptr_t>(q) & 15u) return HW_ERR_INVALID;  // 16-byte query loads
     if (have_pool && ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u))
@@ -218,6 +259,84 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
     e = launch_decode_simt(a, d->dtype, ctas, s);
   }
   return e == cudaSuccess ? HW_OK : cuda_fail(e);
+}
+
+}  // namespace hw
+
+extern "C" {
+
+int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_start, const int32_t *block_len,
+                   const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
+                   const int32_t *q_to_kv, void *out, float *lse, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+  int st = check_desc(d);
+  if (st != HW_OK) return st;
+  if (d->n_rows == 0) return HW_OK;
+  if (!q || !out || !q_pos) return HW_ERR_INVALID;
+  if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
+  if (d->n_blocks > 0 && (!block_start || !block_len)) return HW_ERR_INVALID;
+  // an empty pool (capacity 0) is never read and may be NULL
+  if (d->n_blocks > 0 && d->cache_capacity > 0 && (!k_cache || !v_cache)) return HW_ERR_INVALID;
+  WorkspaceLayout L;
+  int max_ctas = 0;
+  st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
+  if (st != HW_OK) return st;
+  return decode_common(d, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
+                       q_pos, q_to_kv, nullptr, out, lse, workspace, L, max_ctas, stream);
+}
+
+int hw_attn_plan(const hw_attn_desc *d, const int32_t *block_start, const int32_t *block_len,
+                 const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
+                 const int32_t *q_to_kv, void *workspace, size_t workspace_bytes, void *stream) {
+  int st = check_desc(d);
+  if (st != HW_OK) return st;
+  if (d->n_rows == 0) return HW_OK;
+  if (!q_pos) return HW_ERR_INVALID;
+  if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
+  if (d->n_blocks > 0 && (!block_start || !block_len)) return HW_ERR_INVALID;
+  WorkspaceLayout L;
+  int max_ctas = 0;
+  st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
+  if (st != HW_OK) return st;
+  DecodeArgs a;
+  fill_args(a, d, L, workspace);
+  a.block_start = block_start;
+  a.block_len = block_len;
+  a.view_block = view_block;
+  a.view_offset = view_offset;
+  a.q_pos = q_pos;
+  a.q_to_kv = q_to_kv;
+  const MetaCopies m = meta_copies(*d, L, workspace);
+  PlanOut o;
+  o.plan = tensor_core_path(d) ? static_cast<uint8_t *>(workspace) + L.plan_off : nullptr;
+  o.view_block = m.view_block;
+  o.view_offset = m.view_offset;
+  o.q_pos = m.q_pos;
+  o.q_to_kv = m.q_to_kv;
+  o.block_start = m.block_start;
+  o.block_len = m.block_len;
+  const cudaError_t e = launch_plan(a, o, device_sm_count(), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HW_OK : cuda_fail(e);
+}
+
+int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_cache,
+                           const void *v_cache, void *out, float *lse, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  int st = check_desc(d);
+  if (st != HW_OK) return st;
+  if (d->n_rows == 0) return HW_OK;
+  if (!q || !out) return HW_ERR_INVALID;
+  if (d->n_blocks > 0 && d->cache_capacity > 0 && (!k_cache || !v_cache)) return HW_ERR_INVALID;
+  WorkspaceLayout L;
+  int max_ctas = 0;
+  st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
+  if (st != HW_OK) return st;
+  const MetaCopies m = meta_copies(*d, L, workspace);
+  const uint8_t *plan = static_cast<const uint8_t *>(workspace) + L.plan_off;
+  return decode_common(d, q, k_cache, v_cache, m.block_start, m.block_len, m.view_block,
+                       m.view_offset, m.q_pos, m.q_to_kv, plan, out, lse, workspace, L, max_ctas,
+                       stream);
 }
 
 int hw_block_commit(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,

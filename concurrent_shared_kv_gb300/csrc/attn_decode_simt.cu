@@ -24,6 +24,7 @@ struct SimtSmem {
   PlanCore plan;
   MetaCache cache;
   PlanScratch scratch;
+  int64_t u_range[2];
   SegMeta meta;
   MergeSmem merge;
   alignas(16) float q[kMaxQ][D + 4];
@@ -212,10 +213,10 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem<D> &S = *reinterpret_cast<SimtSmem<D> *>(smem_raw);
   PlanCore &P = S.plan;
-  build_plan<kSimtTile>(a, P, S.cache, S.scratch);
+  build_plan<kSimtTile>(a, P, S.cache, S.scratch, S.u_range);
   plan_ranks(a, S.cache, threadIdx.x >> 5, threadIdx.x & 31, 0, 1);  // read by the merge
-  int64_t u = P.u0;
-  const int64_t u_end = P.u1;
+  int64_t u = S.u_range[0];
+  const int64_t u_end = S.u_range[1];
   while (u < u_end) {
     const UnitPos x = unit_pos(P, a.n_blocks, u);
     const int64_t seg_stop = min(x.seg_first + x.tiles, u_end);

@@ -62,20 +62,28 @@ struct SegQ {
   int64_t rel[kMaxQ];
 };
 
+// What the plan derives for one CTA (copied as one block).
+struct alignas(16) CtaPlan {
+  int64_t u0, u1;          // its units
+  int64_t us[kPre];        // first unit of its segments 0 .. kPre-1 (u1 where none)
+  SegQ pre[kPre];          // query-side metadata of segment j in pre[j % kPre]
+  int32_t mpre[kPreList];  // record list of its first merge item
+  int32_t mpre_n;          // its length, or -1 (not built)
+  int32_t pad[3];
+};
+
 struct TcSmem {
   alignas(1024) uint8_t stage[kStages][kStageBytes];
   alignas(1024) uint8_t q[kQBytes];
-  PlanCore plan;
-  MetaCache cache;
+  PlanShared ps;
+  CtaPlan cp;
   int32_t meta_nref;   // references of the current segment, handed to the softmax warps
-  SegQ pre[kPre];      // query-side metadata of segment j in pre[j % kPre]
-  int32_t mpre[kPreList];  // record list of the CTA's first merge item, built while tiles stream
-  int32_t mpre_n;          // its length, or -1 (not built)
   alignas(16) float red[2][kN][4];  // per tile: column maxima of the 4 softmax warps (read as float4)
   float lsave[2][4][kN];  // per segment parity: column sums of l of the 4 softmax warps
   float msave[2][kN];     // per segment parity: the reference maxima
   int32_t abort_flag;
   int32_t tiles_done;  // tiles whose P the softmax warps have written (progress only)
+  int32_t plan_ok;     // the plan (own or loaded) is usable
   uint32_t tmem_base;
   alignas(8) uint64_t k_full[kStages];
   uint64_t v_full[kStages], kv_empty[kStages];
@@ -85,7 +93,41 @@ struct TcSmem {
   uint64_t p_empty, mma_done;
   uint64_t o_full[2], o_empty[2];  // per O buffer: segment done / epilogue read it
   uint64_t rec_ready[4];           // per segment mod 4: records written, arrivals due
+  uint64_t plan_bar;               // a loaded plan has landed
 };
+
+// ------------------------------------------------------------------- plans
+//
+// hw_attn_plan runs plan_kernel once per decode step: it copies the metadata
+// into the workspace and, for this kernel, writes what every launch of the
+// step would otherwise derive again - a header, the shared plan (PlanShared:
+// unit prefix and metadata cache with ranks) and one CtaPlan per CTA (unit
+// range, first segments' query metadata, first merge list).  A planned
+// launch copies the shared part and its own record into shared memory with
+// two bulk copies and starts streaming at once.
+
+constexpr uint32_t kPlanMagic = 0x4c505748u;  // "HWPL"
+
+struct PlanHeader {
+  uint32_t magic;
+  int32_t grid, n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
+  int64_t capacity;
+};
+static_assert(sizeof(PlanHeader) <= kPlanHeaderBytes, "plan header");
+static_assert(sizeof(PlanShared) % 16 == 0 && sizeof(CtaPlan) % 16 == 0, "bulk copy sizes");
+
+__device__ __forceinline__ const uint8_t *plan_cta_record(const uint8_t *plan, int c) {
+  return plan + kPlanHeaderBytes + sizeof(PlanShared) + static_cast<size_t>(c) * sizeof(CtaPlan);
+}
+
+// Does the plan in global memory describe this launch?
+__device__ __forceinline__ bool plan_matches(const DecodeArgs &a, const uint8_t *plan) {
+  const PlanHeader &h = *reinterpret_cast<const PlanHeader *>(plan);
+  return h.magic == kPlanMagic && h.grid == static_cast<int32_t>(gridDim.x) &&
+         h.n_rows == a.n_rows && h.n_q_heads == a.n_q_heads && h.n_kv_heads == a.n_kv_heads &&
+         h.head_dim == a.head_dim && h.n_blocks == a.n_blocks && h.n_view == a.n_view &&
+         h.capacity == a.capacity;
+}
 
 __device__ __forceinline__ void set_abort(TcSmem &S, const DecodeArgs &a) {
   if (atomicExch(&S.abort_flag, 1) == 0) flag_error(a.err, HW_DEV_TIMEOUT);
@@ -153,8 +195,8 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
   for (int64_t u = u0; u < u1; ++u, ++i) {
     const int s = i % kStages;
     if (!wait_or_abort(S, a, &S.kv_empty[s], ((i / kStages) & 1) ^ 1)) break;
-    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
-    const int row = S.plan.start[x.b] + x.t * kT;
+    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
+    const int row = S.ps.plan.start[x.b] + x.t * kT;
     uint8_t *st = S.stage[s];
     mbar_arrive_expect_tx(&S.k_full[s], 2 * kBox);
     tma_load_3d(st, tk, &S.k_full[s], 0, row, x.h, pol);
@@ -181,7 +223,7 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
   int seg_q = -1, seg_p = -1;
   auto qk = [&](int i) {
     const int64_t u = u0 + i;
-    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
     const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
     if (first) ++seg_q;
     const int s = i % kStages, sb = i & 1;
@@ -203,7 +245,7 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
   };
   auto pv = [&](int i) {
     const int64_t u = u0 + i;
-    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
     const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
     if (first) ++seg_p;
     const int s = i % kStages;
@@ -236,15 +278,15 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
 
 // Query-side metadata of segment (b, h) into X, by one warp (shared memory
 // only, except for views beyond the metadata cache).
-__device__ void seg_pre(const DecodeArgs &a, const TcSmem &S, SegQ &X, int b, int h, int lane) {
+__device__ void seg_pre(const DecodeArgs &a, const MetaCache &C, SegQ &X, int b, int h, int lane) {
   const int G = a.n_q_heads / a.n_kv_heads;
-  gather_refs(a, S.cache, X.m, b, lane);
-  gather_qheads(a, S.cache, X.m, h, lane);
+  gather_refs(a, C, X.m, b, lane);
+  gather_qheads(a, C, X.m, h, lane);
   __syncwarp();
   if (lane < X.m.n_ref * G) {
     const int e = X.m.ref_entry[lane / G];
     X.qrow[lane] = (e / a.n_view) * a.n_q_heads + X.m.qhead[lane % G];
-    X.rel[lane] = entry_rel(a, S.cache, e);
+    X.rel[lane] = entry_rel(a, C, e);
   }
   __syncwarp();
 }
@@ -282,7 +324,7 @@ __device__ __forceinline__ void rot_item(const DecodeArgs &a, const TcSmem &S, c
       const float x0 = __uint_as_float(h2 ? (lo32[e2] & 0xffff0000u) : (lo32[e2] << 16));
       const float x1 = __uint_as_float(h2 ? (hi32[e2] & 0xffff0000u) : (hi32[e2] << 16));
       float cs, sn;
-      rope_cos_sin_fast(it.rel, S.cache.phase[8 * c + 2 * e2 + h2], &cs, &sn);
+      rope_cos_sin_fast(it.rel, S.ps.cache.phase[8 * c + 2 * e2 + h2], &cs, &sn);
       ylo[h2] = (x0 * cs - x1 * sn) * a.scale_log2;
       yhi[h2] = (x1 * cs + x0 * sn) * a.scale_log2;
     }
@@ -310,8 +352,8 @@ __device__ __forceinline__ void store_item(uint32_t qbase, int qi, int c, const 
 }
 
 // First unit after the segment that holds unit u.
-__device__ __forceinline__ int64_t next_segment(const TcSmem &S, int n_blocks, int64_t u) {
-  const UnitPos x = unit_pos(S.plan, n_blocks, u);
+__device__ __forceinline__ int64_t next_segment(const PlanCore &P, int n_blocks, int64_t u) {
+  const UnitPos x = unit_pos(P, n_blocks, u);
   return x.seg_first + x.tiles;
 }
 
@@ -323,12 +365,12 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
   const int w = t >> 5, lane = t & 31;
   const int G = a.n_q_heads / a.n_kv_heads;
   NamedSync<3, 192> sync;
-  if (w == 0) {
-    const UnitPos x = unit_pos(S.plan, a.n_blocks, u0);
-    seg_pre(a, S, S.pre[0], x.b, x.h, lane);
+  if (w == 0 && !a.plan) {  // a plan brings it ready-made
+    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u0);
+    seg_pre(a, S.ps.cache, S.cp.pre[0], x.b, x.h, lane);
   }
   sync();
-  const SegQ &X = S.pre[0];
+  const SegQ &X = S.cp.pre[0];
   const int nq = min(X.m.n_ref * G, kN);
   // items t and t + 192 of the nq * 8 (column, 16-byte chunk) items
   const int n_items = nq * 8;
@@ -372,57 +414,66 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
     // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
     // warps keep the same control flow so the named barrier stays balanced.
     wait_or_abort(S, a, &S.rec_ready[done & 3], (done >> 2) & 1);
-    if (tq == 0) arrive_segment(a, S.pre[done % kPre].m);
+    if (tq == 0) arrive_segment(a, S.cp.pre[done % kPre].m);
   };
-  // metadata of segments 1 .. kPre-1 (warp k & 1)
-  int64_t us[kPre];
-  us[0] = u0;
-#pragma unroll
-  for (int k = 1; k < kPre; ++k) us[k] = us[k - 1] < u1 ? next_segment(S, a.n_blocks, us[k - 1]) : u1;
-#pragma unroll
-  for (int k = 1; k < kPre; ++k) {
-    if ((k & 1) == wq && us[k] < u1) {
-      const UnitPos x = unit_pos(S.plan, a.n_blocks, us[k]);
-      seg_pre(a, S, S.pre[k], x.b, x.h, lane);
+  if (!a.plan) {
+    // first units and metadata of segments 1 .. kPre-1 (a plan brings them)
+    if (tq == 0) {
+      int64_t u = u0;
+      for (int k = 0; k < kPre; ++k) {
+        S.cp.us[k] = u;
+        if (u < u1) u = next_segment(S.ps.plan, a.n_blocks, u);
+      }
     }
+    sync();
+#pragma unroll
+    for (int k = 1; k < kPre; ++k) {
+      if ((k & 1) == wq && S.cp.us[k] < u1) {
+        const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, S.cp.us[k]);
+        seg_pre(a, S.ps.cache, S.cp.pre[k], x.b, x.h, lane);
+      }
+    }
+    sync();
   }
-  sync();
-  int64_t u = us[1];                                                   // segment 1
-  int64_t u_prep = us[kPre - 1] < u1 ? next_segment(S, a.n_blocks, us[kPre - 1]) : u1;  // segment kPre
+  int64_t u = S.cp.us[1];  // segment 1
+  int64_t u_prep = S.cp.us[kPre - 1] < u1 ? next_segment(S.ps.plan, a.n_blocks, S.cp.us[kPre - 1]) : u1;  // segment kPre
   for (int seg = 1;; ++seg) {
     if (u >= u1) {
-      // no segment seg.  Until the last records arrive, prepare the merge:
-      // ranks and group indices, and the list of the CTA's first item - once
-      // the softmax warps are past their first tiles, so as not to slow them
-      {
-        // tiles_done only grows; the wait is bounded like every other
-        const int want = static_cast<int>(u1 - u0) < 3 ? static_cast<int>(u1 - u0) : 3;
-        const long long t0 = clock64();
-        while (*reinterpret_cast<volatile int32_t *>(&S.tiles_done) < want && !aborted(S)) {
-          if (clock64() - t0 > kWaitLimit) {
-            set_abort(S, a);
-            break;
+      // no segment seg.  Until the last records arrive, prepare the merge
+      // (a plan brings it): ranks and group indices, and the list of the
+      // CTA's first item - once the softmax warps are past their first
+      // tiles, so as not to slow them
+      if (!a.plan) {
+        {
+          // tiles_done only grows; the wait is bounded like every other
+          const int want = static_cast<int>(u1 - u0) < 3 ? static_cast<int>(u1 - u0) : 3;
+          const long long t0 = clock64();
+          while (*reinterpret_cast<volatile int32_t *>(&S.tiles_done) < want && !aborted(S)) {
+            if (clock64() - t0 > kWaitLimit) {
+              set_abort(S, a);
+              break;
+            }
+            __nanosleep(256);
           }
-          __nanosleep(256);
         }
-      }
-      plan_ranks(a, S.cache, wq, lane, 0, 1);
-      sync();
-      if (wq == 0 && S.cache.entries_cached) {
-        const int first = merge_rank(S.plan, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
-        int n = -1;
-        if (first < a.n_rows * a.n_q_heads) {
-          n = merge_list(a, S.plan, S.cache, first / a.n_q_heads, first % a.n_q_heads, S.mpre,
-                         kPreList, nullptr, lane);
-          if (n > kPreList) n = -1;
+        plan_ranks(a, S.ps.cache, wq, lane, 0, 1);
+        sync();
+        if (wq == 0 && S.ps.cache.entries_cached) {
+          const int first = merge_rank(S.ps.plan, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
+          int n = -1;
+          if (first < a.n_rows * a.n_q_heads) {
+            n = merge_list(a, S.ps.plan, S.ps.cache, first / a.n_q_heads, first % a.n_q_heads,
+                           S.cp.mpre, kPreList, nullptr, lane);
+            if (n > kPreList) n = -1;
+          }
+          if (lane == 0) S.cp.mpre_n = n;
         }
-        if (lane == 0) S.mpre_n = n;
       }
       if (seg >= 2) arrivals(seg - 2);
       arrivals(seg - 1);
       break;
     }
-    const SegQ &X = S.pre[seg % kPre];
+    const SegQ &X = S.cp.pre[seg % kPre];
     const int nq = min(X.m.n_ref * G, kN);
     // items tq + 64 k of the nq * 8: column (tq >> 3) + 8 k, chunk tq & 7
     QItem raw[4];
@@ -447,14 +498,14 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
       arrivals(seg - 2);
       sync();  // the slot of segment seg - 2 is read; it now takes segment seg + 2
       if (u_prep < u1) {
-        const UnitPos x = unit_pos(S.plan, a.n_blocks, u_prep);
-        SegQ &N = S.pre[(seg + 2) % kPre];
-        if (wq == 0) seg_pre(a, S, N, x.b, x.h, lane);
+        const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u_prep);
+        SegQ &N = S.cp.pre[(seg + 2) % kPre];
+        if (wq == 0) seg_pre(a, S.ps.cache, N, x.b, x.h, lane);
         u_prep = x.seg_first + x.tiles;
       }
       sync();
     }
-    u = next_segment(S, a.n_blocks, u);
+    u = next_segment(S.ps.plan, a.n_blocks, u);
   }
 }
 
@@ -527,7 +578,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   int pend = -1, pend_b = 0, pend_h = 0, pend_nq = 0;  // segment whose records are due
   for (int i = 0; i < n; ++i) {
     const int64_t u = u0 + i;
-    const UnitPos x = unit_pos(S.plan, a.n_blocks, u);
+    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
     const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
     if (first) {
       ++seg;
@@ -553,7 +604,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.s_empty[sb]);
 
-    const int valid = min(kT, S.plan.len[x.b] - x.t * kT);
+    const int valid = min(kT, S.ps.plan.len[x.b] - x.t * kT);
     const bool tok_ok = row < valid;
     float sc[kN];
 #pragma unroll
@@ -703,22 +754,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 4; ++b) mbar_init(&S.rec_ready[b], 4);  // one per softmax warp
     mbar_init(&S.mma_done, 1);
+    mbar_init(&S.plan_bar, 1);
     S.abort_flag = 0;
     S.tiles_done = 0;
-    S.mpre_n = -1;
+    S.plan_ok = 1;
+    S.cp.mpre_n = -1;
     fence_mbar_init();
+    if (a.plan) {
+      // the step's plan: the shared part and this CTA's record
+      mbar_arrive_expect_tx(&S.plan_bar, sizeof(PlanShared) + sizeof(CtaPlan));
+      bulk_g2s(&S.ps, a.plan + kPlanHeaderBytes, sizeof(PlanShared), &S.plan_bar);
+      bulk_g2s(&S.cp, plan_cta_record(a.plan, blockIdx.x), sizeof(CtaPlan), &S.plan_bar);
+      if (!plan_matches(a, a.plan)) S.plan_ok = 0;
+    }
   }
   if (warp == kWarpMma) {
     tmem_alloc(&S.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  // the plan scratch borrows stage 0, which no copy has touched yet
-  build_plan<kT>(a, S.plan, S.cache, *reinterpret_cast<PlanScratch *>(S.stage[0]));
+  if (!a.plan) {
+    // the plan scratch borrows stage 0, which no copy has touched yet
+    build_plan<kT>(a, S.ps.plan, S.ps.cache, *reinterpret_cast<PlanScratch *>(S.stage[0]),
+                   *reinterpret_cast<int64_t(*)[2]>(&S.cp.u0));
+  } else {
+    __syncthreads();  // the barrier is initialised
+    if (!mbar_wait(&S.plan_bar, 0)) {
+      flag_error(a.err, HW_DEV_TIMEOUT);
+      S.plan_ok = 0;
+    }
+    __syncthreads();  // every thread's wait is over: the table may be refreshed
+    if (tid < 64) S.ps.cache.phase[tid] = a.phase[tid];  // this launch's RoPE table
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  const int64_t u0 = S.plan.u0, u1 = S.plan.u1;
+  const bool ok = S.plan_ok != 0;
+  if (!ok && tid == 0 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_PLAN);
+  const int64_t u0 = ok ? S.cp.u0 : 0, u1 = ok ? S.cp.u1 : 0;
   if (u0 < u1) {
     if (warp == kWarpTma) {
       if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1);
@@ -731,8 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         qprep(a, S, u0, u1);
     }
-  } else {
-    plan_ranks(a, S.cache, warp, lane, 0, 1);  // a CTA without units: ranks for the merge
+  } else if (!a.plan) {
+    plan_ranks(a, S.ps.cache, warp, lane, 0, 1);  // a CTA without units: ranks for the merge
   }
   tc_fence_before();
   __syncthreads();
@@ -742,13 +815,110 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // the merge scratch lives in the tile buffers: every copy and MMA is done
   static_assert(sizeof(MergeSmem) <= kStageBytes, "merge scratch must fit in a stage");
-  merge_phase<__nv_bfloat16, 128>(a, S.plan, S.cache, *reinterpret_cast<MergeSmem *>(S.stage[0]),
-                                  S.mpre, S.mpre_n, tid, kThreads, CtaSync(), kWaitLimit);
+  if (ok)
+    merge_phase<__nv_bfloat16, 128>(a, S.ps.plan, S.ps.cache,
+                                    *reinterpret_cast<MergeSmem *>(S.stage[0]), S.cp.mpre,
+                                    S.cp.mpre_n, tid, kThreads, CtaSync(), kWaitLimit);
+}
+
+// The plan of one decode step (see "plans" above).  Any grid: CTA c writes
+// the record of decode CTA c, CTA 0 also the metadata copies, the shared part
+// and the header.  With o.plan null only the metadata is copied.
+struct PlanSmem {
+  PlanShared ps;
+  CtaPlan cp;
+  PlanScratch scratch;
+  int32_t rank_tmp[HW_MAX_VIEW_BLOCKS];
+};
+
+__device__ __forceinline__ void copy16(uint8_t *dst, const void *src, size_t bytes, int tid, int nt) {
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+  for (size_t i = tid; i < bytes / 16; i += nt) d4[i] = s4[i];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    plan_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ PlanOut o) {
+  extern __shared__ uint8_t smem_raw[];
+  PlanSmem &S = *reinterpret_cast<PlanSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 15) &
+                                              ~static_cast<uintptr_t>(15));
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.n_rows * a.n_view, G = a.n_q_heads / a.n_kv_heads;
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < E; i += nt) {
+      o.view_block[i] = a.view_block[i];
+      o.view_offset[i] = a.view_offset[i];
+    }
+    for (int i = tid; i < a.n_rows; i += nt) o.q_pos[i] = a.q_pos[i];
+    for (int i = tid; i < a.n_blocks; i += nt) {
+      o.block_start[i] = a.block_start[i];
+      o.block_len[i] = a.block_len[i];
+    }
+    for (int i = tid; i < a.n_q_heads; i += nt) o.q_to_kv[i] = a.q_to_kv ? a.q_to_kv[i] : i / G;
+  }
+  if (!o.plan) return;
+  PlanCore &P = S.ps.plan;
+  build_plan<kT>(a, P, S.ps.cache, S.scratch, *reinterpret_cast<int64_t(*)[2]>(&S.cp.u0));
+  plan_ranks(a, S.ps.cache, warp, lane, 0, 1);
+  if (tid == 0) {
+    int64_t u = S.cp.u0;
+    for (int k = 0; k < kPre; ++k) {
+      S.cp.us[k] = u;
+      if (u < S.cp.u1) u = next_segment(P, a.n_blocks, u);
+    }
+  }
+  __syncthreads();
+  if (warp < kPre && S.cp.us[warp] < S.cp.u1) {
+    const UnitPos x = unit_pos(P, a.n_blocks, S.cp.us[warp]);
+    seg_pre(a, S.ps.cache, S.cp.pre[warp], x.b, x.h, lane);
+  } else if (warp == kPre) {
+    const int first = merge_rank(P, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
+    int n = -1;
+    if (first < a.n_rows * a.n_q_heads) {
+      n = merge_list(a, P, S.ps.cache, first / a.n_q_heads, first % a.n_q_heads, S.cp.mpre,
+                     kPreList, S.rank_tmp, lane);
+      if (n > kPreList) n = -1;
+    }
+    if (lane == 0) S.cp.mpre_n = n;
+  }
+  __syncthreads();
+  copy16(const_cast<uint8_t *>(plan_cta_record(o.plan, blockIdx.x)), &S.cp, sizeof(CtaPlan), tid, nt);
+  if (blockIdx.x == 0) {
+    copy16(o.plan + kPlanHeaderBytes, &S.ps, sizeof(PlanShared), tid, nt);
+    if (tid == 0) {
+      PlanHeader h;
+      h.magic = kPlanMagic;
+      h.grid = static_cast<int32_t>(gridDim.x);
+      h.n_rows = a.n_rows;
+      h.n_q_heads = a.n_q_heads;
+      h.n_kv_heads = a.n_kv_heads;
+      h.head_dim = a.head_dim;
+      h.n_blocks = a.n_blocks;
+      h.n_view = a.n_view;
+      h.capacity = a.capacity;
+      *reinterpret_cast<PlanHeader *>(o.plan) = h;
+    }
+  }
 }
 
 }  // namespace
 
 size_t decode_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
+size_t plan_shared_bytes() { return sizeof(PlanShared); }
+size_t plan_cta_bytes() { return sizeof(CtaPlan); }
+
+cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s) {
+  const size_t smem = sizeof(PlanSmem) + 16;
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  plan_kernel<<<o.plan ? ctas : 1, kThreads, smem, s>>>(a, o);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                              int ctas, cudaStream_t s) {

@@ -181,8 +181,13 @@ struct PlanCore {
   int64_t ubase[HW_MAX_BLOCKS + 1];  // first unit of each block within a head; [n] = UH
   uint8_t sord[HW_MAX_BLOCKS];       // non-empty blocks before b
   int64_t UH, U, WH, W;              // units per head and in all; weights likewise
-  int64_t u0, u1;                    // this CTA's units
   int32_t NB, C;                     // non-empty blocks; working CTAs
+};
+
+// Everything the plan derives that every CTA shares (copied as one block).
+struct alignas(16) PlanShared {
+  PlanCore plan;
+  MetaCache cache;
 };
 
 struct PlanScratch {  // only while the plan is built
@@ -217,11 +222,13 @@ __device__ __forceinline__ int64_t cta_unit_begin(const PlanCore &P, int n_block
 }
 
 // Loads the metadata into the cache (one round of independent loads), checks
-// it and builds the unit prefix and this CTA's unit range.  Every thread of
+// it and builds the unit prefix and this CTA's unit range [u_range[0],
+// u_range[1]).  Every thread of
 // the CTA takes part (blockDim.x == 256, three __syncthreads inside); one
 // warp does the serial part in a single pass.
 template <int TILE>
-__device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanScratch &S) {
+__device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanScratch &S,
+                           int64_t (&u_range)[2]) {
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads;
   const int E = a.n_rows * a.n_view;
@@ -337,7 +344,7 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanS
     // lanes 0 and 1: the two ends of this CTA's unit range, side by side
     if (lane < 2) {
       const int64_t u = cta_unit_begin(P, a.n_blocks, blockIdx.x + lane);
-      if (lane == 0) P.u0 = u; else P.u1 = u;
+      u_range[lane] = u;
     }
   }
   __syncthreads();

@@ -37,6 +37,7 @@ struct DecodeArgs {
   float *partials;    // [slots][kMaxQ][D + 4]: o[0..D), m at D, l at D+1
   int32_t n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
   int64_t capacity;
+  const uint8_t *plan;  // precomputed plan of the tensor-core kernel (hw_attn_plan), or null
   float scale_log2;   // softmax scale * log2(e): scores live in the log2 domain
   // RoPE phase increments: for pair i, the fraction of a turn per position,
   // frac(w_i / 2pi), as an unsigned 0.64 fixed-point number.  The angle of
@@ -44,11 +45,15 @@ struct DecodeArgs {
   uint64_t phase[64];
 };
 
-// Workspace layout helpers (bytes).
+// Workspace layout helpers (bytes).  The metadata copies and the plan are
+// written by hw_attn_plan and read by hw_attn_decode_planned.
 struct WorkspaceLayout {
-  size_t err_off, counters_off, partials_off, total;
+  size_t err_off, counters_off, partials_off, meta_off, plan_off, total;
   int64_t slots;
 };
+constexpr size_t kPlanHeaderBytes = 256;
+size_t plan_shared_bytes();  // the part of a plan every CTA reads
+size_t plan_cta_bytes();     // the part each CTA reads for itself
 WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas);
 
 int device_sm_count();  // SMs of the current device, cached; <= 0 on failure
@@ -58,6 +63,14 @@ cudaError_t launch_decode_simt(const DecodeArgs &a, int dtype, int ctas, cudaStr
 cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &k_map,
                              const CUtensorMap &v_map, int ctas, cudaStream_t s);
 size_t decode_tc_smem_bytes();
+
+// Destinations of hw_attn_plan: metadata copies (int32) and, for the
+// tensor-core kernel, the plan (header, shared part, one record per CTA).
+struct PlanOut {
+  uint8_t *plan;  // null: copy the metadata only
+  int32_t *view_block, *view_offset, *q_pos, *q_to_kv, *block_start, *block_len;
+};
+cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s);
 int decode_simt_ctas_per_sm(int dtype, int head_dim);
 
 struct CommitArgs {

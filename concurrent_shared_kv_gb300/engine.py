@@ -55,6 +55,27 @@ class DecodeSession:
                         q_to_kv=m["q_to_kv"], stream=stream)
         return out, lse
 
+    def plan(self, stream=None):
+        """hw_attn_plan on the uploaded metadata: once per step, before the
+        layers' decode_planned calls."""
+        m = self.meta
+        api.attn_plan(self.desc, m["block_start"], m["block_len"], m["view_block"],
+                      m["view_offset"], m["q_pos"], self.workspace, self.ws_bytes,
+                      q_to_kv=m["q_to_kv"], stream=stream)
+
+    def decode_planned(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                       want_lse: bool = True, stream=None):
+        """One layer against the step's plan (see plan())."""
+        d = self.desc
+        if out is None:
+            out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
+        if lse is None and want_lse:
+            lse = torch.empty((d.n_rows, d.n_q_heads), dtype=torch.float32, device=self.device)
+        api.attn_decode_planned(d, q, k_cache, v_cache, out, lse, self.workspace, self.ws_bytes,
+                                stream=stream)
+        return out, lse
+
     def device_flags(self) -> int:
         return api.workspace_status(self.workspace)
 

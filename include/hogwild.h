@@ -64,7 +64,8 @@ enum {
   HW_DEV_BAD_RANGE = 2,     /* block_start/len negative or past the pool capacity */
   HW_DEV_BAD_HEADMAP = 4,   /* q_to_kv entry out of range or groups of unequal size */
   HW_DEV_TOO_MANY_REFS = 8, /* more than HW_MAX_QHEADS_PER_BLOCK query heads on a block */
-  HW_DEV_TIMEOUT = 16       /* a bounded in-kernel wait expired; results are invalid */
+  HW_DEV_TIMEOUT = 16,      /* a bounded in-kernel wait expired; results are invalid */
+  HW_DEV_BAD_PLAN = 32      /* hw_attn_decode_planned found no plan for this description */
 };
 
 /* Limits of this build. */
@@ -140,6 +141,34 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
                    const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
                    const int32_t *q_to_kv, void *out, float *lse, void *workspace,
                    size_t workspace_bytes, void *stream);
+
+/*
+ * The metadata of a decode step, planned once for every layer of the step.
+ *
+ * In a decode step every layer attends the same views: the block table,
+ * the views and positions are per step, only q, K and V change per layer.
+ * hw_attn_plan copies the metadata (same arguments and layouts as
+ * hw_attn_decode) into `workspace` and, for the bf16 head_dim-128 kernel,
+ * precomputes the work split, each CTA's first segments and the merge lists
+ * there.  hw_attn_decode_planned then runs one layer against that plan, with
+ * results identical to hw_attn_decode on the same metadata.  The plan holds a
+ * copy of the metadata: the caller may change its own arrays after planning.
+ * A plan stays valid until the next hw_attn_plan on the workspace; planned
+ * calls must use the same description (checked on the device: a mismatch or
+ * a missing plan sets HW_DEV_BAD_PLAN, see hw_workspace_status, and leaves
+ * out and lse untouched).  Both enqueue work on `stream` only; the plan is
+ * seen by calls enqueued after it on the same stream.
+ *
+ * Not in the Hogwild! notes, which describe one attention call per layer:
+ * this is the usual split of a decode kernel's scheduling from its runs.
+ */
+int hw_attn_plan(const hw_attn_desc *d, const int32_t *block_start, const int32_t *block_len,
+                 const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
+                 const int32_t *q_to_kv, void *workspace, size_t workspace_bytes, void *stream);
+
+int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_cache,
+                           const void *v_cache, void *out, float *lse, void *workspace,
+                           size_t workspace_bytes, void *stream);
 
 /*
  * Size of the fixed scratch array hw_attn_decode_noalloc uses (32 MiB): it
