@@ -225,8 +225,8 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
     u = seg_stop;
   }
   __syncthreads();
-  merge_phase<T, D>(a, P, S.cache, S.merge, nullptr, -1, threadIdx.x, kSimtThreads, CtaSync(),
-                    2000000000ll);
+  merge_phase<T, D>(a, P, S.cache, S.merge, nullptr, nullptr, 0, 0, threadIdx.x, kSimtThreads,
+                    CtaSync(), 2000000000ll);
 }
 
 template <typename T, int D>

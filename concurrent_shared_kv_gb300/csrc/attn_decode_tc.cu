@@ -51,6 +51,7 @@ constexpr float kLazy = 8.f;                  // rescale only when the max grows
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
 constexpr int kPre = 4;  // slots of query-side segment metadata
 constexpr int kPreList = 64;  // records of a merge list built ahead of the merge
+constexpr int kPreItems = 2;  // merge items of a CTA whose lists a plan builds
 // Named barriers: 1 softmax warps, 2 query warps, 3 prologue warps.
 
 // Query-side metadata of a segment: its view references and q heads, and per
@@ -67,9 +68,9 @@ struct alignas(16) CtaPlan {
   int64_t u0, u1;          // its units
   int64_t us[kPre];        // first unit of its segments 0 .. kPre-1 (u1 where none)
   SegQ pre[kPre];          // query-side metadata of segment j in pre[j % kPre]
-  int32_t mpre[kPreList];  // record list of its first merge item
-  int32_t mpre_n;          // its length, or -1 (not built)
-  int32_t pad[3];
+  int32_t mpre[kPreItems][kPreList];  // record lists of its first merge items
+  int32_t mpre_n[kPreItems];          // their lengths, or -1 (not built)
+  int32_t pad[2];
 };
 
 struct TcSmem {
@@ -463,10 +464,10 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
           int n = -1;
           if (first < a.n_rows * a.n_q_heads) {
             n = merge_list(a, S.ps.plan, S.ps.cache, first / a.n_q_heads, first % a.n_q_heads,
-                           S.cp.mpre, kPreList, nullptr, lane);
+                           S.cp.mpre[0], kPreList, nullptr, lane);
             if (n > kPreList) n = -1;
           }
-          if (lane == 0) S.cp.mpre_n = n;
+          if (lane == 0) S.cp.mpre_n[0] = n;
         }
       }
       if (seg >= 2) arrivals(seg - 2);
@@ -758,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.abort_flag = 0;
     S.tiles_done = 0;
     S.plan_ok = 1;
-    S.cp.mpre_n = -1;
+    for (int k = 0; k < kPreItems; ++k) S.cp.mpre_n[k] = -1;
     fence_mbar_init();
     if (a.plan) {
       // the step's plan: the shared part and this CTA's record
@@ -817,8 +818,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(sizeof(MergeSmem) <= kStageBytes, "merge scratch must fit in a stage");
   if (ok)
     merge_phase<__nv_bfloat16, 128>(a, S.ps.plan, S.ps.cache,
-                                    *reinterpret_cast<MergeSmem *>(S.stage[0]), S.cp.mpre,
-                                    S.cp.mpre_n, tid, kThreads, CtaSync(), kWaitLimit);
+                                    *reinterpret_cast<MergeSmem *>(S.stage[0]), &S.cp.mpre[0][0],
+                                    S.cp.mpre_n, kPreItems, kPreList, tid, kThreads, CtaSync(),
+                                    kWaitLimit);
 }
 
 // The plan of one decode step (see "plans" above).  Any grid: CTA c writes
@@ -828,7 +830,7 @@ struct PlanSmem {
   PlanShared ps;
   CtaPlan cp;
   PlanScratch scratch;
-  int32_t rank_tmp[HW_MAX_VIEW_BLOCKS];
+  int32_t rank_tmp[kPreItems][HW_MAX_VIEW_BLOCKS];
 };
 
 __device__ __forceinline__ void copy16(uint8_t *dst, const void *src, size_t bytes, int tid, int nt) {
@@ -871,15 +873,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kPre && S.cp.us[warp] < S.cp.u1) {
     const UnitPos x = unit_pos(P, a.n_blocks, S.cp.us[warp]);
     seg_pre(a, S.ps.cache, S.cp.pre[warp], x.b, x.h, lane);
-  } else if (warp == kPre) {
-    const int first = merge_rank(P, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
+  } else if (warp >= kPre && warp < kPre + kPreItems) {
+    // the record lists of the CTA's first merge items (item k: first + k * grid)
+    const int k = warp - kPre;
+    const int it = merge_rank(P, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x)) +
+                   k * static_cast<int>(gridDim.x);
     int n = -1;
-    if (first < a.n_rows * a.n_q_heads) {
-      n = merge_list(a, P, S.ps.cache, first / a.n_q_heads, first % a.n_q_heads, S.cp.mpre,
-                     kPreList, S.rank_tmp, lane);
+    if (it < a.n_rows * a.n_q_heads) {
+      n = merge_list(a, P, S.ps.cache, it / a.n_q_heads, it % a.n_q_heads, S.cp.mpre[k], kPreList,
+                     S.rank_tmp[k], lane);
       if (n > kPreList) n = -1;
     }
-    if (lane == 0) S.cp.mpre_n = n;
+    if (lane == 0) S.cp.mpre_n[k] = n;
   }
   __syncthreads();
   copy16(const_cast<uint8_t *>(plan_cta_record(o.plan, blockIdx.x)), &S.cp, sizeof(CtaPlan), tid, nt);

@@ -577,16 +577,18 @@ __device__ __forceinline__ int merge_list(const DecodeArgs &a, const PlanCore &P
 // it once its own units are done.  Work item = (row r, q head hq): all the
 // partial records of that output row, each from one (view entry, CTA) pair.
 // Items go round-robin over the CTAs, those without units first.  An item's
-// owner lists its records from the plan (the first item's list may come
-// ready-made in pre_list / pre_n, else pre_n < 0), waits (bounded) until the
+// owner lists its records from the plan (the k-th item's list, k < n_pre, may
+// come ready-made at pre_list + k * pre_stride with length pre_n[k] >= 0),
+// waits (bounded) until the
 // item's arrival counter shows every record, then merges with the whole CTA:
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
 //   lse = (M + log2 L) ln 2;
 // an item without records gets out = 0, lse = -inf.
 template <typename T, int D, typename Sync>
 __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCache &MC,
-                            MergeSmem &Z, const int32_t *pre_list, int pre_n, int tid, int nt,
-                            Sync sync, long long wait_limit) {
+                            MergeSmem &Z, const int32_t *pre_list, const int32_t *pre_n,
+                            int n_pre, int pre_stride, int tid, int nt, Sync sync,
+                            long long wait_limit) {
   constexpr int EPL = D / 32;
   constexpr int64_t RS = D + 4;  // record stride in floats
   const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
@@ -594,12 +596,13 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
   const int grid = static_cast<int>(gridDim.x);
   const int rank = merge_rank(P, static_cast<int>(blockIdx.x), grid);
 
-  for (int it = rank; it < items; it += grid) {
+  for (int it = rank, k = 0; it < items; it += grid, ++k) {
     const int r = it / a.n_q_heads, hq = it % a.n_q_heads;
-    // the first item's list may have been built while the tiles streamed
-    const bool pre = it == rank && pre_n >= 0;
+    // the first items' lists may have been built ahead (a plan, or while the
+    // tiles streamed)
+    const bool pre = k < n_pre && pre_n[k] >= 0;
     if (pre) {
-      if (tid == 0) Z.n_rec = pre_n;
+      if (tid == 0) Z.n_rec = pre_n[k];
     } else if (warp == 0) {
       int n = merge_list(a, P, MC, r, hq, Z.list, kMaxRecords, Z.rank_tmp, lane);
       if (lane == 0) {
@@ -610,7 +613,7 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
         Z.n_rec = n;
       }
     }
-    const int32_t *list = pre ? pre_list : Z.list;
+    const int32_t *list = pre ? pre_list + k * pre_stride : Z.list;
     sync();
     const int n_rec = Z.n_rec;
     const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
