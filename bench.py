@@ -112,6 +112,31 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def measured_traffic(kernel: str, workload_key: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's sources changed since the counters were taken (or none exist)."""
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    path = os.path.join(root, "profiles", f"{kernel}_{workload_key}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if line.startswith("#") or ":" not in line:
+            continue
+        k, v = line.split(":", 1)
+        kv[k.strip()] = v.strip()
+    h = hashlib.sha256()
+    try:
+        for src in kv["sources"].split():
+            h.update(open(os.path.join(root, src), "rb").read())
+    except (KeyError, OSError):
+        return None
+    if h.hexdigest()[:16] != kv.get("sources_sha256_16"):
+        return None
+    return int(kv["dram_bytes_per_launch"])
+
+
 def reference_arm(args):
     """The float64 oracle on the host cores, on the same workload and metric."""
     import numpy as np
@@ -193,8 +218,18 @@ def main():
                                 rope_theta=w.rope_theta, scale=w.scale, device=dev)
     sess.set_metadata(starts, lens, vb, vo, qp)
     qs, ks, vs = [], [], []
+    commit = w.commit_tokens > 0 and args.config == "C4"
+    if commit:
+        # one [layers][Hkv][cap][D] pool per K and V, so that one commit launch
+        # covers every layer
+        k_all = torch.empty((L, w.n_kv_heads, w.capacity, w.head_dim), dtype=tdt, device=dev)
+        v_all = torch.empty_like(k_all)
     for l in range(L):
         q, k, v = wl.draw_device_layer(w, l, dev)
+        if commit:
+            k_all[l].copy_(k)
+            v_all[l].copy_(v)
+            k, v = k_all[l], v_all[l]
         qs.append(q)
         ks.append(k)
         vs.append(v)
@@ -217,8 +252,24 @@ def main():
             else:
                 sess.decode(qsrc[l], ks[l], vs[l], out=outs[l], lse=lses[l], stream=stream)
 
+    step_no = [0]
+
+    def commit_call():
+        # a worker's finished step joins the common history: its block is
+        # rotated by the position change and written after the common tokens
+        # (the decode's views keep reading [0, common_len), so every rep times
+        # the same work)
+        wk = step_no[0] % w.n_workers
+        step_no[0] += 1
+        src = int(starts[1 + wk])
+        engine.block_commit(k_all, v_all, src, w.commit_tokens, k_all, v_all,
+                            int(starts[0]) + int(w.common_len[0]), int(w.common_len[0]),
+                            w.rope_theta, stream=stream)
+
     def step():
         layer_calls(qs)
+        if commit:
+            commit_call()
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -263,7 +314,8 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t = float(tt.item())
 
-    step_bytes = w.kv_bytes_per_layer() * calls_per_step
+    commit_bytes = w.commit_bytes_per_layer() * L if commit else 0
+    step_bytes = w.kv_bytes_per_layer() * calls_per_step + commit_bytes
     per_step = t / args.steps
     gbs_rank = step_bytes / per_step / 1e9
     value = gbs_rank * world  # replicas: every rank streams its own copy
@@ -292,6 +344,8 @@ def main():
                 for l in range(L):
                     qdev[l].copy_(q_host[l], non_blocking=True)
                 layer_calls(qdev)
+                if commit:
+                    commit_call()
                 for l in range(L):
                     o_host[l].copy_(outs[l], non_blocking=True)
                     l_host[l].copy_(lses[l], non_blocking=True)
@@ -322,7 +376,8 @@ def main():
             "workload": w.name, "layers_per_step": calls_per_step, "problems": w.n_problems,
             "workers": w.n_workers, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
             "head_dim": w.head_dim, "kv_tokens_per_layer": w.kv_tokens(),
-            "kv_bytes_per_step": step_bytes, "parallelism": f"replicas x{world}",
+            "kv_bytes_per_step": step_bytes, "commit_bytes_per_step": commit_bytes,
+            "parallelism": f"replicas x{world}",
             "mode": "eager" if graph is None else "cuda-graph",
             "calls": ("hw_attn_plan once per step + hw_attn_decode_planned per layer" if planned
                       else "hw_attn_decode per layer"),
@@ -332,7 +387,10 @@ def main():
         "frac_of_8TBps": gbs_rank / NOMINAL_HBM_GBS,
         "worker_tokens_per_s_per_layer": w.n_rows / per_launch,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / peak,
+                     "traffic": (measured_traffic(kernel, "qwq32b_w4")
+                                 if args.config == "C3" and planned else None),
+                     "peak_kind": peak_kind,
                      "kernel": f"{'hw_attn_decode_planned' if planned else 'hw_attn_decode'} ({kernel})",
                      "per_launch": "step time / layers per step (the plan launch included)"},
         "gpu_launches": (calls_per_step + (1 if planned else 0)) * args.steps,

@@ -6,7 +6,7 @@
 // head that attends it (all workers' view references to the block times the
 // GQA group, up to 32).  At 16-20 flop per KV byte the CUDA cores would be
 // the ceiling, so the two small products run on the tensor cores:
-//   S^T [128 tokens x 32 heads] = K_tile [128 x 128] . Q~^T    (TMEM, fp32)
+//   S^T [128 tokens x 64]      = K_tile [128 x 128] . [Q~hi; Q~lo]^T   (TMEM, fp32)
 //   O^T [128 d x 32 heads]     += V_tile^T [128 x 128 tokens] . P^T
 // with Q~ the rotated queries (Hogwild! notes, key design 1: the query is
 // rotated once per block by i_q - i_k^block; the keys stay as stored).
@@ -19,8 +19,11 @@
 //              segment epilogue: O from TMEM -> partial records
 // then all eight warps take part in the grid-wide merge phase (hw_device.cuh).
 //   warps 6-7  rotated queries of the next segment: fp32, scale folded in,
-//              split into bf16 hi + lo parts so that S keeps ~16 mantissa bits
-//              (QK runs as two MMA passes, hi then lo, into one accumulator)
+//              split into bf16 hi + lo parts so that S keeps ~16 mantissa bits.
+// QK multiplies the K tile with hi and lo stacked as one 64-column operand:
+// one pass of 8 MMAs reads each K slice once, S_hi and S_lo land in separate
+// TMEM columns and the softmax adds them in fp32.  (Each tcgen05.mma of this
+// kernel costs stream time whatever its N, so fewer, wider products pay.)
 #include <cuda.h>
 
 #include "hw_device.cuh"
@@ -38,14 +41,18 @@ constexpr int kT = kTcTile;                   // 128 tokens per tile
 constexpr int kN = kMaxQ;                     // 32 query heads per tile (MMA N)
 constexpr uint32_t kBox = 128 * 64 * 2;       // [128 rows][64 bf16], 128-B swizzled
 constexpr uint32_t kStageBytes = 4 * kBox;    // K lo, K hi, V lo, V hi
-constexpr uint32_t kQHalf = kN * 64 * 2;      // [32 heads][64 bf16], 128-B swizzled
-constexpr uint32_t kQPart = 2 * kQHalf;       // one part (hi or lo): d 0-63, d 64-127
-constexpr uint32_t kQBytes = 2 * kQPart;      // hi, lo
+// Q~ buffer: [d half (0-63, 64-127)][part (hi, lo)][32 columns][64 bf16],
+// 128-byte swizzled: per d half, 64 rows (hi columns, then lo columns) at a
+// 128-byte stride - the B operand of one N = 64 product.
+constexpr uint32_t kQPart = kN * 64 * 2;      // one part of one d half: 4 KB
+constexpr uint32_t kQHalf = 2 * kQPart;       // hi + lo of one d half: 8 KB
+constexpr uint32_t kQBytes = 2 * kQHalf;
 constexpr uint32_t kPBytes = kT * kN * 2;     // [128 tokens][32 heads], 64-B swizzled; it
                                               // lives in the stage's K region, free once
                                               // the tile's QK product has completed
-constexpr uint32_t kTmemCols = 128;           // S0 [0,32)  S1 [32,64)  O0 [64,96)  O1 [96,128)
-constexpr uint32_t kColO = 64;                // segment k accumulates in O[k & 1]
+constexpr uint32_t kSCols = 2 * kN;           // S buffer: S_hi [0,32), S_lo [32,64)
+constexpr uint32_t kTmemCols = 256;           // S0 [0,64)  S1 [64,128)  O0 [128,160)  O1 [160,192)
+constexpr uint32_t kColO = 2 * kSCols;        // segment k accumulates in O[k & 1]
 constexpr float kLazy = 8.f;                  // rescale only when the max grows by > 2^8
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
@@ -187,6 +194,23 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // ------------------------------------------------------------------ roles
 
+// Spin (bounded) until the phase with this parity completes: the producer
+// re-issues a stage the moment it is released, without the wake-up delay of
+// a suspended wait.
+__device__ __forceinline__ bool spin_or_abort(TcSmem &S, const DecodeArgs &a, uint64_t *bar,
+                                              uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity)) {
+    if (aborted(S)) return false;
+    if (clock64() - t0 > kWaitLimit) {
+      set_abort(S, a);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
                          const CUtensorMap *tv, int64_t u0, int64_t u1) {
   tma_prefetch_desc(tk);
@@ -195,10 +219,11 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
   int i = 0;
   for (int64_t u = u0; u < u1; ++u, ++i) {
     const int s = i % kStages;
-    if (!wait_or_abort(S, a, &S.kv_empty[s], ((i / kStages) & 1) ^ 1)) break;
+    // the tile's coordinates first, so that only the copy waits for the stage
     const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
     const int row = S.ps.plan.start[x.b] + x.t * kT;
     uint8_t *st = S.stage[s];
+    if (i >= kStages && !spin_or_abort(S, a, &S.kv_empty[s], ((i / kStages) & 1) ^ 1)) break;
     mbar_arrive_expect_tx(&S.k_full[s], 2 * kBox);
     tma_load_3d(st, tk, &S.k_full[s], 0, row, x.h, pol);
     tma_load_3d(st + kBox, tk, &S.k_full[s], 64, row, x.h, pol);
@@ -218,7 +243,7 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
 // before the softmax warps are done with tile i+1, so issuing PV(i) first
 // costs nothing, and the thread sleeps instead of polling.
 __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0, int64_t u1) {
-  constexpr uint32_t idesc_qk = idesc_bf16(128, kN, 0, 0);  // K tile, Q~: both K-major
+  constexpr uint32_t idesc_qk = idesc_bf16(128, kSCols, 0, 0);  // K tile, [Q~hi; Q~lo]: K-major
   constexpr uint32_t idesc_pv = idesc_bf16(128, kN, 1, 1);  // V tile, P: both MN-major
   const int n = static_cast<int>(u1 - u0);
   int seg_q = -1, seg_p = -1;
@@ -234,12 +259,10 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
     tc_fence_after();
     const uint32_t kb = smem_u32(S.stage[s]), qbase = smem_u32(S.q);
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {  // 8 k-steps against Q~ hi, then 8 against Q~ lo
-      const int k8 = kk & 7;
+    for (int k8 = 0; k8 < 8; ++k8) {  // 8 k-steps of 16 over d
       const uint64_t ad = smem_desc(kb + (k8 >> 2) * kBox + (k8 & 3) * 32, 16, 1024, kSw128);
-      const uint64_t bd = smem_desc(qbase + (kk >> 3) * kQPart + (k8 >> 2) * kQHalf + (k8 & 3) * 32,
-                                    16, 1024, kSw128);
-      mma_bf16(tmem + sb * kN, ad, bd, idesc_qk, kk > 0);
+      const uint64_t bd = smem_desc(qbase + (k8 >> 2) * kQHalf + (k8 & 3) * 32, 16, 1024, kSw128);
+      mma_bf16(tmem + sb * kSCols, ad, bd, idesc_qk, k8 > 0);
     }
     mma_commit(&S.s_full[sb]);
     if (last) mma_commit(&S.q_empty);
@@ -342,14 +365,15 @@ __device__ __forceinline__ void rot_item(const DecodeArgs &a, const TcSmem &S, c
   for (int k = 0; k < 4; ++k) out[k] = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
 }
 
-// Store one item into the Q~ buffer: row qi (128 B per half), 16-B chunk c
-// swizzled by qi % 8 (the 128-byte swizzle the MMA descriptor expects).
+// Store one item into the Q~ buffer: column qi of the hi and lo parts of both
+// d halves (128 B per row), 16-B chunk c swizzled by qi % 8 (the 128-byte
+// swizzle the MMA descriptor expects; lo row 32 + qi has the same pattern).
 __device__ __forceinline__ void store_item(uint32_t qbase, int qi, int c, const uint4 (&v)[4]) {
   const uint32_t off = qi * 128 + ((static_cast<uint32_t>(c) ^ (qi & 7)) << 4);
-  st_shared_v4(qbase + off, v[0].x, v[0].y, v[0].z, v[0].w);
-  st_shared_v4(qbase + kQHalf + off, v[1].x, v[1].y, v[1].z, v[1].w);
-  st_shared_v4(qbase + kQPart + off, v[2].x, v[2].y, v[2].z, v[2].w);
-  st_shared_v4(qbase + kQPart + kQHalf + off, v[3].x, v[3].y, v[3].z, v[3].w);
+  st_shared_v4(qbase + off, v[0].x, v[0].y, v[0].z, v[0].w);                     // hi, d 0-63
+  st_shared_v4(qbase + kQHalf + off, v[1].x, v[1].y, v[1].z, v[1].w);            // hi, d 64-127
+  st_shared_v4(qbase + kQPart + off, v[2].x, v[2].y, v[2].z, v[2].w);            // lo, d 0-63
+  st_shared_v4(qbase + kQHalf + kQPart + off, v[3].x, v[3].y, v[3].z, v[3].w);   // lo, d 64-127
 }
 
 // First unit after the segment that holds unit u.
@@ -598,12 +622,15 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     wait_or_abort(S, a, &S.s_full[sb], (i >> 1) & 1);
     tc_fence_after();
     __syncwarp();
-    uint32_t r[32];
-    tmem_ld32(tl + sb * kN, r);
+    uint32_t r[32], r2[32];
+    tmem_ld32(tl + sb * kSCols, r);        // S_hi
+    tmem_ld32(tl + sb * kSCols + kN, r2);  // S_lo
     tmem_wait_ld();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.s_empty[sb]);
+#pragma unroll
+    for (int j = 0; j < kN; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
 
     const int valid = min(kT, S.ps.plan.len[x.b] - x.t * kT);
     const bool tok_ok = row < valid;
