@@ -91,6 +91,7 @@ struct TcSmem {
   float msave[2][kN];     // per segment parity: the reference maxima
   int32_t abort_flag;
   int32_t tiles_done;  // tiles whose P the softmax warps have written (progress only)
+  uint8_t tflags[kStages];  // per stage: the tile starts (1) / ends (2) its segment
   int32_t plan_ok;     // the plan (own or loaded) is usable
   uint32_t tmem_base;
   alignas(8) uint64_t k_full[kStages];
@@ -222,8 +223,12 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
     // the tile's coordinates first, so that only the copy waits for the stage
     const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
     const int row = S.ps.plan.start[x.b] + x.t * kT;
+    const uint8_t flags = (seg_first_unit(x, u, u0) ? 1 : 0) | (seg_last_unit(x, u, u1) ? 2 : 0);
     uint8_t *st = S.stage[s];
     if (i >= kStages && !spin_or_abort(S, a, &S.kv_empty[s], ((i / kStages) & 1) ^ 1)) break;
+    // read by the MMA thread once the stage's copies are seen complete (the
+    // arrive below releases this store)
+    S.tflags[s] = flags;
     mbar_arrive_expect_tx(&S.k_full[s], 2 * kBox);
     tma_load_3d(st, tk, &S.k_full[s], 0, row, x.h, pol);
     tma_load_3d(st + kBox, tk, &S.k_full[s], 64, row, x.h, pol);
@@ -239,57 +244,60 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
 }
 
 // Issues the products in a fixed order - QK(0), QK(1), then PV(i), QK(i+2) -
-// each after a blocking (bounded) wait on its inputs.  QK(i+2) is not needed
-// before the softmax warps are done with tile i+1, so issuing PV(i) first
-// costs nothing, and the thread sleeps instead of polling.
+// each after a (bounded) spin on its inputs.  QK(i+2) is not needed before
+// the softmax warps are done with tile i+1, so issuing PV(i) first costs
+// nothing.  The thread is on the critical path of every stage's release, so
+// it does no more than wait and issue: the tile's segment flags come from
+// the producer (tflags), and the operand descriptors are a base plus a
+// constant offset per k-step (the start address is the descriptor's low
+// field, 14 bits of address >> 4: shared addresses stay below 2^18).
 __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0, int64_t u1) {
   constexpr uint32_t idesc_qk = idesc_bf16(128, kSCols, 0, 0);  // K tile, [Q~hi; Q~lo]: K-major
-  constexpr uint32_t idesc_pv = idesc_bf16(128, kN, 1, 1);  // V tile, P: both MN-major
+  constexpr uint32_t idesc_pv = idesc_bf16(128, kN, 1, 1);      // V tile, P: both MN-major
   const int n = static_cast<int>(u1 - u0);
+  const uint32_t stage0 = smem_u32(S.stage[0]), qbase = smem_u32(S.q);
+  const uint64_t a_qk = smem_desc(stage0, 16, 1024, kSw128);    // + (stage, k-step) offset >> 4
+  const uint64_t b_qk = smem_desc(qbase, 16, 1024, kSw128);
+  const uint64_t a_pv = smem_desc(stage0 + 2 * kBox, kBox, 1024, kSw128);
+  const uint64_t b_pv = smem_desc(stage0, 512, 512, kSw64);
   int seg_q = -1, seg_p = -1;
   auto qk = [&](int i) {
-    const int64_t u = u0 + i;
-    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
-    const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
-    if (first) ++seg_q;
     const int s = i % kStages, sb = i & 1;
-    if (!wait_or_abort(S, a, &S.k_full[s], (i / kStages) & 1)) return;
-    if (!wait_or_abort(S, a, &S.s_empty[sb], ((i >> 1) & 1) ^ 1)) return;
-    if (first && !wait_or_abort(S, a, &S.q_full, seg_q & 1)) return;
+    if (!spin_or_abort(S, a, &S.k_full[s], (i / kStages) & 1)) return;
+    const uint32_t flags = S.tflags[s];
+    if (flags & 1) ++seg_q;
+    if (!spin_or_abort(S, a, &S.s_empty[sb], ((i >> 1) & 1) ^ 1)) return;
+    if ((flags & 1) && !spin_or_abort(S, a, &S.q_full, seg_q & 1)) return;
     tc_fence_after();
-    const uint32_t kb = smem_u32(S.stage[s]), qbase = smem_u32(S.q);
+    const uint64_t as = a_qk + ((s * kStageBytes) >> 4);
 #pragma unroll
     for (int k8 = 0; k8 < 8; ++k8) {  // 8 k-steps of 16 over d
-      const uint64_t ad = smem_desc(kb + (k8 >> 2) * kBox + (k8 & 3) * 32, 16, 1024, kSw128);
-      const uint64_t bd = smem_desc(qbase + (k8 >> 2) * kQHalf + (k8 & 3) * 32, 16, 1024, kSw128);
-      mma_bf16(tmem + sb * kSCols, ad, bd, idesc_qk, k8 > 0);
+      const uint32_t ao = (k8 >> 2) * kBox + (k8 & 3) * 32, bo = (k8 >> 2) * kQHalf + (k8 & 3) * 32;
+      mma_bf16(tmem + sb * kSCols, as + (ao >> 4), b_qk + (bo >> 4), idesc_qk, k8 > 0);
     }
     mma_commit(&S.s_full[sb]);
-    if (last) mma_commit(&S.q_empty);
+    if (flags & 2) mma_commit(&S.q_empty);
   };
   auto pv = [&](int i) {
-    const int64_t u = u0 + i;
-    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
-    const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
-    if (first) ++seg_p;
     const int s = i % kStages;
-    if (!wait_or_abort(S, a, &S.p_full[s], (i / kStages) & 1)) return;
-    if (!wait_or_abort(S, a, &S.v_full[s], (i / kStages) & 1)) return;
-    if (first && !wait_or_abort(S, a, &S.o_empty[seg_p & 1], ((seg_p >> 1) & 1) ^ 1)) return;
+    if (!spin_or_abort(S, a, &S.p_full[s], (i / kStages) & 1)) return;
+    if (!spin_or_abort(S, a, &S.v_full[s], (i / kStages) & 1)) return;
+    const uint32_t flags = S.tflags[s];
+    const bool first = flags & 1;
+    if (first) ++seg_p;
+    if (first && !spin_or_abort(S, a, &S.o_empty[seg_p & 1], ((seg_p >> 1) & 1) ^ 1)) return;
     tc_fence_after();
-    const uint32_t vb = smem_u32(S.stage[s]) + 2 * kBox, pb = smem_u32(S.stage[s]);
+    // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart,
+    // 8-token groups 1024 B apart.  P^T: MN-major, 32 heads = one 64-B atom,
+    // 8-token groups 512 B apart, in the stage's K region.
+    const uint64_t as = a_pv + ((s * kStageBytes) >> 4), bs = b_pv + ((s * kStageBytes) >> 4);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart,
-      // 8-token groups 1024 B apart.  P^T: MN-major, 32 heads = one 64-B atom,
-      // 8-token groups 512 B apart.
-      const uint64_t ad = smem_desc(vb + kk * 2048, kBox, 1024, kSw128);
-      const uint64_t bd = smem_desc(pb + kk * 1024, 512, 512, kSw64);
-      mma_bf16(tmem + kColO + (seg_p & 1) * kN, ad, bd, idesc_pv, !(first && kk == 0));
-    }
+    for (int kk = 0; kk < 8; ++kk)
+      mma_bf16(tmem + kColO + (seg_p & 1) * kN, as + ((kk * 2048) >> 4), bs + ((kk * 1024) >> 4),
+               idesc_pv, !(first && kk == 0));
     mma_commit(&S.kv_empty[s]);
     mma_commit(&S.p_empty);
-    if (last) mma_commit(&S.o_full[seg_p & 1]);
+    if (flags & 2) mma_commit(&S.o_full[seg_p & 1]);
   };
   // one call site each: QK(0), QK(1), PV(0), QK(2), PV(1), ...
   for (int j = 0; j < n + 2 && !aborted(S); ++j) {
