@@ -794,7 +794,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.abort_flag = 0;
     S.tiles_done = 0;
     S.plan_ok = 1;
-    for (int k = 0; k < kPreItems; ++k) S.cp.mpre_n[k] = -1;
+    // (with a plan, the bulk copy brings these: no generic store may race it)
+    if (!a.plan)
+      for (int k = 0; k < kPreItems; ++k) S.cp.mpre_n[k] = -1;
     fence_mbar_init();
     if (a.plan) {
       // the step's plan: the shared part and this CTA's record

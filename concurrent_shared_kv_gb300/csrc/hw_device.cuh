@@ -172,7 +172,7 @@ __device__ __forceinline__ int entry_rank_scan(const DecodeArgs &a, int e, int l
 // the plan: every CTA derives the same unit decomposition from the metadata
 // ---------------------------------------------------------------------------
 
-constexpr int kSegW = 1;  // weight of a segment start, in tiles
+constexpr int kSegW = 3;  // weight of a segment start, in tiles
 
 struct PlanCore {
   int32_t tiles[HW_MAX_BLOCKS];      // tiles per kv head (0: block skipped)
