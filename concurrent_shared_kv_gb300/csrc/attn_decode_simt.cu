@@ -26,7 +26,7 @@ struct SimtSmem {
   PlanScratch scratch;
   int64_t u_range[2];
   SegMeta meta;
-  MergeSmem merge;
+  MergeSmem<1> merge;
   alignas(16) float q[kMaxQ][D + 4];
   alignas(16) float k[kSimtTile][D + 4];
   alignas(16) float v[kSimtTile][D + 4];
@@ -204,7 +204,7 @@ __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, 
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) arrive_segment(a, M);
+  if (tid < 32) arrive_segment(a, M, tid);
   __syncthreads();  // the segment metadata is rewritten by the next segment
 }
 
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
     u = seg_stop;
   }
   __syncthreads();
-  merge_phase<T, D>(a, P, S.cache, S.merge, nullptr, nullptr, 0, 0, threadIdx.x, kSimtThreads,
+  merge_phase<T, D, 1>(a, P, S.cache, S.merge, nullptr, nullptr, 0, 0, threadIdx.x, kSimtThreads,
                     CtaSync(), 2000000000ll);
 }
 

@@ -447,7 +447,7 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
     // A wait that gives up (HW_DEV_TIMEOUT) does not leave the loop: both
     // warps keep the same control flow so the named barrier stays balanced.
     wait_or_abort(S, a, &S.rec_ready[done & 3], (done >> 2) & 1);
-    if (tq == 0) arrive_segment(a, S.cp.pre[done % kPre].m);
+    if (wq == 0) arrive_segment(a, S.cp.pre[done % kPre].m, lane);
   };
   if (!a.plan) {
     // first units and metadata of segments 1 .. kPre-1 (a plan brings them)
@@ -852,12 +852,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
   // the merge scratch lives in the tile buffers: every copy and MMA is done
-  static_assert(sizeof(MergeSmem) <= kStageBytes, "merge scratch must fit in a stage");
+  static_assert(sizeof(MergeSmem<8>) <= kStageBytes, "merge scratch must fit in a stage");
   if (ok)
-    merge_phase<__nv_bfloat16, 128>(a, S.ps.plan, S.ps.cache,
-                                    *reinterpret_cast<MergeSmem *>(S.stage[0]), &S.cp.mpre[0][0],
-                                    S.cp.mpre_n, kPreItems, kPreList, tid, kThreads, CtaSync(),
-                                    kWaitLimit);
+    merge_phase<__nv_bfloat16, 128, 8>(a, S.ps.plan, S.ps.cache,
+                                       *reinterpret_cast<MergeSmem<8> *>(S.stage[0]),
+                                       &S.cp.mpre[0][0], S.cp.mpre_n, kPreItems, kPreList, tid,
+                                       kThreads, CtaSync(), kWaitLimit);
 }
 
 // The plan of one decode step (see "plans" above).  Any grid: CTA c writes

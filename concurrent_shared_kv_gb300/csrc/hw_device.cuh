@@ -488,15 +488,18 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
 }
 
 // One arrival on (row, q head) for every view entry referencing the
-// segment's block and every q head of its kv head (M.qhead).  One thread
-// calls it, after the group's record stores were ordered before it (a
-// barrier the writers took part in, or an mbarrier they arrived on).
-__device__ __forceinline__ void arrive_segment(const DecodeArgs &a, const SegMeta &M) {
+// segment's block and every q head of its kv head (M.qhead), one per lane:
+// the whole warp calls it, after the group's record stores were ordered
+// before it (a barrier the writers took part in, or an mbarrier they arrived
+// on).  The plan skips blocks with more than kMaxQ columns, so one warp
+// covers every arrival; issued together, they cost one trip to L2 instead
+// of one each.
+__device__ __forceinline__ void arrive_segment(const DecodeArgs &a, const SegMeta &M, int lane) {
   const int G = a.n_q_heads / a.n_kv_heads;
   __threadfence();
-  for (int j = 0; j < M.n_ref && j < kMaxQ; ++j) {
-    const int r = M.ref_entry[j] / a.n_view;
-    for (int gi = 0; gi < G; ++gi) atomicAdd(&a.counters[r * a.n_q_heads + M.qhead[gi]], 1);
+  if (lane < M.n_ref * G && lane < kMaxQ) {
+    const int r = M.ref_entry[lane / G] / a.n_view;
+    atomicAdd(&a.counters[r * a.n_q_heads + M.qhead[lane % G]], 1);
   }
 }
 
@@ -511,14 +514,15 @@ __device__ __forceinline__ void lse_combine(float &M, float &L, float m, float l
   }
 }
 
-// Shared scratch of the merge phase (~17 KB; the tensor-core kernel places
-// it in its tile buffers, idle by then).
+// Shared scratch of the merge phase, for NL items merged side by side (the
+// tensor-core kernel places it in its tile buffers, idle by then).
+template <int NL>
 struct MergeSmem {
-  int32_t list[kMaxRecords];  // record index of each partial: slot * 32 + rank * G + gi
-  float acc[8][128];          // per warp partial sums of the output row
-  float wm[8], wl[8];         // per warp running max and normaliser
-  int32_t rank_tmp[HW_MAX_VIEW_BLOCKS];  // entry ranks of one row (views beyond the cache)
-  int32_t n_rec, ok;
+  int32_t list[NL][kMaxRecords];  // record index of each partial: slot * 32 + rank * G + gi
+  float acc[8][128];              // per warp partial sums of the output row
+  float wm[8], wl[8];             // per warp running max and normaliser
+  int32_t rank_tmp[NL][HW_MAX_VIEW_BLOCKS];  // entry ranks of one row (views beyond the cache)
+  int32_t n_rec[NL], ok[NL];
 };
 
 // Position of CTA c in the order items are dealt: CTAs without units first.
@@ -576,118 +580,153 @@ __device__ __forceinline__ int merge_list(const DecodeArgs &a, const PlanCore &P
 // The merge phase.  Every thread of every CTA of the (cooperative) grid calls
 // it once its own units are done.  Work item = (row r, q head hq): all the
 // partial records of that output row, each from one (view entry, CTA) pair.
-// Items go round-robin over the CTAs, those without units first.  An item's
-// owner lists its records from the plan (the k-th item's list, k < n_pre, may
-// come ready-made at pre_list + k * pre_stride with length pre_n[k] >= 0),
-// waits (bounded) until the
-// item's arrival counter shows every record, then merges with the whole CTA:
+// Items go round-robin over the CTAs, those without units first.  A CTA
+// merges up to NL of its items side by side, its warps split evenly between
+// them.  The first warp of an item's group lists the item's records from the
+// plan (the k-th item of the CTA, k < n_pre, may come with its list
+// ready-made at pre_list + k * pre_stride, length pre_n[k] >= 0) and waits
+// (bounded) until the item's arrival counter shows every record; the group
+// then folds the records, each warp a strided share with kMergeBatch loads
+// in flight, and its first warp combines the warps' partials:
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i o_i 2^(m_i - M) / L,
 //   lse = (M + log2 L) ln 2;
 // an item without records gets out = 0, lse = -inf.
-template <typename T, int D, typename Sync>
+constexpr int kMergeBatch = 4;
+
+template <typename T, int D, int NL, typename Sync>
 __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCache &MC,
-                            MergeSmem &Z, const int32_t *pre_list, const int32_t *pre_n,
+                            MergeSmem<NL> &Z, const int32_t *pre_list, const int32_t *pre_n,
                             int n_pre, int pre_stride, int tid, int nt, Sync sync,
                             long long wait_limit) {
   constexpr int EPL = D / 32;
   constexpr int64_t RS = D + 4;  // record stride in floats
+  constexpr int B = kMergeBatch;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
   const int items = a.n_rows * a.n_q_heads;
   const int grid = static_cast<int>(gridDim.x);
   const int rank = merge_rank(P, static_cast<int>(blockIdx.x), grid);
+  const int mine = rank < items ? (items - rank + grid - 1) / grid : 0;
 
-  for (int it = rank, k = 0; it < items; it += grid, ++k) {
-    const int r = it / a.n_q_heads, hq = it % a.n_q_heads;
-    // the first items' lists may have been built ahead (a plan, or while the
-    // tiles streamed)
-    const bool pre = k < n_pre && pre_n[k] >= 0;
-    if (pre) {
-      if (tid == 0) Z.n_rec = pre_n[k];
-    } else if (warp == 0) {
-      int n = merge_list(a, P, MC, r, hq, Z.list, kMaxRecords, Z.rank_tmp, lane);
-      if (lane == 0) {
+  for (int k0 = 0; k0 < mine; k0 += NL) {
+    const int np = min(mine - k0, NL);  // items merged side by side
+    const int g = nwarps / np;          // warps per item (np <= NL <= nwarps)
+    const int p = warp / g, wi = warp - p * g;
+    const bool active = p < np;
+    const int k = k0 + p;
+    const int it = rank + k * grid;
+    const int r = it / a.n_q_heads, hq = it - r * a.n_q_heads;
+    const bool pre = active && k < n_pre && pre_n[k] >= 0;
+    if (active && wi == 0) {
+      int n;
+      if (pre) {
+        n = pre_n[k];
+      } else {
+        n = merge_list(a, P, MC, r, hq, Z.list[p], kMaxRecords, Z.rank_tmp[p], lane);
         if (n > kMaxRecords) {
-          flag_error(a.err, HW_DEV_TOO_MANY_REFS);
+          if (lane == 0) flag_error(a.err, HW_DEV_TOO_MANY_REFS);
           n = kMaxRecords;
         }
-        Z.n_rec = n;
       }
-    }
-    const int32_t *list = pre ? pre_list + k * pre_stride : Z.list;
-    sync();
-    const int n_rec = Z.n_rec;
-    const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
-    if (n_rec == 0) {
-      // no block of the view has tokens
-      if (tid < D) reinterpret_cast<T *>(a.out)[ob * D + tid] = from_f32<T>(0.f);
-      if (tid == 0 && a.lse) a.lse[ob] = -INFINITY;
-      sync();
-      continue;
-    }
-    if (tid == 0) {
-      // every record of the item is delivered (bounded wait: co-resident CTAs)
-      const int32_t *ctr = a.counters + it;
-      bool ok = ld_acquire_gpu(ctr) >= n_rec;
-      if (!ok) {
-        const long long t0 = clock64();
-        while (!(ok = ld_acquire_gpu(ctr) >= n_rec)) {
-          if (clock64() - t0 > wait_limit) break;
-          __nanosleep(32);
+      if (lane == 0) {
+        // every record of the item is delivered (bounded wait: co-resident CTAs)
+        bool ok = true;
+        if (n > 0) {
+          const int32_t *ctr = a.counters + it;
+          ok = ld_acquire_gpu(ctr) >= n;
+          if (!ok) {
+            const long long t0 = clock64();
+            while (!(ok = ld_acquire_gpu(ctr) >= n)) {
+              if (clock64() - t0 > wait_limit) break;
+              __nanosleep(32);
+            }
+          }
+          if (!ok) flag_error(a.err, HW_DEV_TIMEOUT);
         }
+        Z.n_rec[p] = n;
+        Z.ok[p] = ok ? 1 : 0;
       }
-      if (!ok) flag_error(a.err, HW_DEV_TIMEOUT);
-      Z.ok = ok ? 1 : 0;
     }
     sync();
-    if (Z.ok) {
-      // one pass: warp w folds records w, w + nwarps, ... into a running
-      // (m, l, o) - lane j owns elements [j * EPL, (j+1) * EPL) of the row -
-      // then the warps' partials are combined through shared memory
-      float Mw = -INFINITY, Lw = 0.f, acc[EPL];
+    const int n_rec = active ? Z.n_rec[p] : 0;
+    const bool ok = active && Z.ok[p] != 0;
+    const int32_t *list = pre ? pre_list + k * pre_stride : Z.list[active ? p : 0];
+    // fold: lane j owns elements [j * EPL, (j+1) * EPL) of the row
+    float Mw = -INFINITY, Lw = 0.f, acc[EPL];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-      for (int k = warp; k < n_rec; k += nwarps) {
-        const float *rec = a.partials + static_cast<int64_t>(list[k]) * RS;
-        const float m = __ldcg(rec + D), l = __ldcg(rec + D + 1);
-        float x[EPL];
-        if constexpr (EPL == 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4 *>(rec + lane * EPL));
-          x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2 *>(rec + lane * EPL));
-          x[0] = v.x; x[1] = v.y;
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    if (ok) {
+      for (int kb = wi; kb < n_rec; kb += B * g) {
+        float m[B], l[B], x[B][EPL];
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          const int kk = kb + b * g;
+          m[b] = -INFINITY;
+          l[b] = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) x[b][e] = 0.f;
+          if (kk < n_rec) {
+            const float *rec = a.partials + static_cast<int64_t>(list[kk]) * RS;
+            m[b] = __ldcg(rec + D);
+            l[b] = __ldcg(rec + D + 1);
+            if constexpr (EPL == 4) {
+              const float4 v = __ldcg(reinterpret_cast<const float4 *>(rec + lane * EPL));
+              x[b][0] = v.x; x[b][1] = v.y; x[b][2] = v.z; x[b][3] = v.w;
+            } else {
+              const float2 v = __ldcg(reinterpret_cast<const float2 *>(rec + lane * EPL));
+              x[b][0] = v.x; x[b][1] = v.y;
+            }
+          }
         }
-        if (m == -INFINITY) continue;  // an empty partial adds nothing
-        const float Mn = fmaxf(Mw, m);
-        const float sa = ex2(Mw - Mn), sb = ex2(m - Mn);  // sa = 0 while Mw = -inf
-        Lw = Lw * sa + l * sb;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * sa + x[e] * sb;
-        Mw = Mn;
+        for (int b = 0; b < B; ++b) {
+          if (m[b] == -INFINITY) continue;  // an empty partial (or none) adds nothing
+          const float Mn = fmaxf(Mw, m[b]);
+          const float sa = ex2(Mw - Mn), sb = ex2(m[b] - Mn);  // sa = 0 while Mw = -inf
+          Lw = Lw * sa + l[b] * sb;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * sa + x[b][e] * sb;
+          Mw = Mn;
+        }
       }
+    }
+    if (active) {
 #pragma unroll
       for (int e = 0; e < EPL; ++e) Z.acc[warp][lane * EPL + e] = acc[e];
       if (lane == 0) {
         Z.wm[warp] = Mw;
         Z.wl[warp] = Lw;
       }
-      sync();
-      if (tid < D) {
-        float Mx = -INFINITY;
-        for (int w2 = 0; w2 < nwarps; ++w2) Mx = fmaxf(Mx, Z.wm[w2]);
-        float sum = 0.f, L = 0.f;
-        for (int w2 = 0; w2 < nwarps; ++w2) {
-          if (Z.wm[w2] == -INFINITY) continue;
-          const float f = ex2(Z.wm[w2] - Mx);
-          sum += Z.acc[w2][tid] * f;
-          L += Z.wl[w2] * f;
-        }
-        reinterpret_cast<T *>(a.out)[ob * D + tid] = from_f32<T>(sum / L);
-        if (tid == 0 && a.lse) a.lse[ob] = (Mx + __log2f(L)) * 0.69314718055994530942f;
-      }
     }
     sync();
-    if (tid == 0) a.counters[it] = 0;  // re-armed for the next call
+    if (active && wi == 0) {
+      const int64_t ob = static_cast<int64_t>(r) * a.n_q_heads + hq;
+      T *orow = reinterpret_cast<T *>(a.out) + ob * D + lane * EPL;
+      if (n_rec == 0) {
+        // no block of the view has tokens
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) orow[e] = from_f32<T>(0.f);
+        if (lane == 0 && a.lse) a.lse[ob] = -INFINITY;
+      } else if (ok) {
+        const int w0 = p * g;
+        float Mx = -INFINITY;
+        for (int w2 = 0; w2 < g; ++w2) Mx = fmaxf(Mx, Z.wm[w0 + w2]);
+        float L = 0.f, sum[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) sum[e] = 0.f;
+        for (int w2 = 0; w2 < g; ++w2) {
+          if (Z.wm[w0 + w2] == -INFINITY) continue;
+          const float f = ex2(Z.wm[w0 + w2] - Mx);
+          L += Z.wl[w0 + w2] * f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) sum[e] += Z.acc[w0 + w2][lane * EPL + e] * f;
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) orow[e] = from_f32<T>(sum[e] / L);
+        if (lane == 0 && a.lse) a.lse[ob] = (Mx + __log2f(L)) * 0.69314718055994530942f;
+      }
+      if (lane == 0) a.counters[it] = 0;  // re-armed for the next call
+    }
+    sync();  // the scratch is rewritten by the next round
   }
 }
 
