@@ -214,8 +214,6 @@ __device__ __forceinline__ bool spin_or_abort(TcSmem &S, const DecodeArgs &a, ui
 
 __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
                          const CUtensorMap *tv, int64_t u0, int64_t u1) {
-  tma_prefetch_desc(tk);
-  tma_prefetch_desc(tv);
   const uint64_t pol = policy_evict_first();
   int i = 0;
   for (int64_t u = u0; u < u1; ++u, ++i) {
@@ -393,12 +391,13 @@ __device__ __forceinline__ int64_t next_segment(const PlanCore &P, int n_blocks,
 // Prologue of warps 2-7 (the TMA and MMA warps start at once): the metadata
 // of segment 0 (warp 2), then its queries rotated into the Q~ buffer (all six
 // warps).
+template <bool kPlanned>
 __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int t = threadIdx.x - kWarpSoft * 32;  // 0..191
   const int w = t >> 5, lane = t & 31;
   const int G = a.n_q_heads / a.n_kv_heads;
   NamedSync<3, 192> sync;
-  if (w == 0 && !a.plan) {  // a plan brings it ready-made
+  if (w == 0 && !kPlanned) {  // a plan brings it ready-made
     const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u0);
     seg_pre(a, S.ps.cache, S.cp.pre[0], x.b, x.h, lane);
   }
@@ -437,6 +436,7 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
 // warps' record stores sit on the path of the next rotated queries.  Last,
 // the metadata of segment j + 2 goes into the slot segment j - 2 vacated,
 // and its queries are prefetched into L2.
+template <bool kPlanned>
 __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
   const int lane = threadIdx.x & 31, wq = tq >> 5;
@@ -449,7 +449,7 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
     wait_or_abort(S, a, &S.rec_ready[done & 3], (done >> 2) & 1);
     if (wq == 0) arrive_segment(a, S.cp.pre[done % kPre].m, lane);
   };
-  if (!a.plan) {
+  if (!kPlanned) {
     // first units and metadata of segments 1 .. kPre-1 (a plan brings them)
     if (tq == 0) {
       int64_t u = u0;
@@ -476,7 +476,7 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
       // (a plan brings it): ranks and group indices, and the list of the
       // CTA's first item - once the softmax warps are past their first
       // tiles, so as not to slow them
-      if (!a.plan) {
+      if (!kPlanned) {
         {
           // tiles_done only grows; the wait is bounded like every other
           const int want = static_cast<int>(u1 - u0) < 3 ? static_cast<int>(u1 - u0) : 3;
@@ -748,6 +748,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   if (pend >= 0) segment_records(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync);
 }
 
+template <bool kPlanned>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
@@ -755,22 +756,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   TcSmem &S = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 32) {
-    // Every CTA warms L2 with its share of q before any K/V tile is asked
-    // for: query loads then hit L2 instead of queueing behind the tile
-    // stream.  q is [n_rows][Hq][128] bf16, a multiple of 256 bytes.
-    const uint64_t total = static_cast<uint64_t>(a.n_rows) * a.n_q_heads * 256;
-    const uint64_t per = ((total + gridDim.x - 1) / gridDim.x + 255) & ~static_cast<uint64_t>(255);
-    const uint64_t off = per * blockIdx.x;
-    if (off < total) {
-      const uint32_t n = static_cast<uint32_t>(total - off < per ? total - off : per);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                       reinterpret_cast<const uint8_t *>(a.q) + off), "r"(n)
-                   : "memory");
-    }
-  }
-
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream: this CTA may start while that grid's last CTAs still run (an SM
+  // holds one CTA of this kernel, so only SMs they left), and the next
+  // launch may be placed likewise.  Until griddepcontrol.wait nothing here
+  // touches global memory: the previous grid may have written q, the plan,
+  // the caches or this workspace.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
+    tma_prefetch_desc(&tm_k);  // (kernel parameters)
+    tma_prefetch_desc(&tm_v);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.p_full[s], 4);  // one per softmax warp
       mbar_init(&S.k_full[s], 1);
@@ -795,10 +790,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.tiles_done = 0;
     S.plan_ok = 1;
     // (with a plan, the bulk copy brings these: no generic store may race it)
-    if (!a.plan)
+    if (!kPlanned)
       for (int k = 0; k < kPreItems; ++k) S.cp.mpre_n[k] = -1;
     fence_mbar_init();
-    if (a.plan) {
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid is complete
+  if (tid == 32) {
+    // Every CTA warms L2 with its share of q before any K/V tile is asked
+    // for: query loads then hit L2 instead of queueing behind the tile
+    // stream.  q is [n_rows][Hq][128] bf16, a multiple of 256 bytes.
+    const uint64_t total = static_cast<uint64_t>(a.n_rows) * a.n_q_heads * 256;
+    const uint64_t per = ((total + gridDim.x - 1) / gridDim.x + 255) & ~static_cast<uint64_t>(255);
+    const uint64_t off = per * blockIdx.x;
+    if (off < total) {
+      const uint32_t n = static_cast<uint32_t>(total - off < per ? total - off : per);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       reinterpret_cast<const uint8_t *>(a.q) + off), "r"(n)
+                   : "memory");
+    }
+  }
+
+  if (tid == 0) {
+    if (kPlanned) {
       // the step's plan: the shared part and this CTA's record
       mbar_arrive_expect_tx(&S.plan_bar, sizeof(PlanShared) + sizeof(CtaPlan));
       bulk_g2s(&S.ps, a.plan + kPlanHeaderBytes, sizeof(PlanShared), &S.plan_bar);
@@ -806,11 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!plan_matches(a, a.plan)) S.plan_ok = 0;
     }
   }
-  if (warp == kWarpMma) {
-    tmem_alloc(&S.tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  if (!a.plan) {
+  if (!kPlanned) {
     // the plan scratch borrows stage 0, which no copy has touched yet
     build_plan<kT>(a, S.ps.plan, S.ps.cache, *reinterpret_cast<PlanScratch *>(S.stage[0]),
                    *reinterpret_cast<int64_t(*)[2]>(&S.cp.u0));
@@ -836,13 +849,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma) {
       if (lane == 0) mma_issuer(a, S, tmem, u0, u1);
     } else {
-      query_prologue(a, S, u0, u1);
+      query_prologue<kPlanned>(a, S, u0, u1);
       if (warp < kWarpQ)
         softmax_role(a, S, tmem, u0, u1);
       else
-        qprep(a, S, u0, u1);
+        qprep<kPlanned>(a, S, u0, u1);
     }
-  } else if (!a.plan) {
+  } else if (!kPlanned) {
     plan_ranks(a, S.ps.cache, warp, lane, 0, 1);  // a CTA without units: ranks for the merge
   }
   tc_fence_before();
@@ -965,26 +978,33 @@ cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStr
 cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                              int ctas, cudaStream_t s) {
   const size_t smem = decode_tc_smem_bytes();
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // a planned launch runs its own instantiation: without the plan-building
+  // code the kernel is far smaller, which matters for instruction fetch
+  void (*kernel)(DecodeArgs, CUtensorMap, CUtensorMap) =
+      a.plan ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+  static bool configured[2] = {false, false};
+  if (!configured[a.plan ? 1 : 0]) {
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[a.plan ? 1 : 0] = true;
   }
-  // cooperative: the merge phase waits on other CTAs, so all must be resident
+  // cooperative: the merge phase waits on other CTAs, so all must be
+  // resident; a programmatic dependent of the previous kernel (see the
+  // kernel's entry)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a, tk, tv);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, a, tk, tv);
 }
 
 }  // namespace hw
