@@ -77,7 +77,10 @@ struct alignas(16) CtaPlan {
   SegQ pre[kPre];          // query-side metadata of segment j in pre[j % kPre]
   int32_t mpre[kPreItems][kPreList];  // record lists of its first merge items
   int32_t mpre_n[kPreItems];          // their lengths, or -1 (not built)
-  int32_t pad[2];
+  int32_t trow[kStages];   // its first tiles (the ring's first fill): first cache row,
+  uint8_t th[kStages];     // kv head,
+  uint8_t tfl[kStages];    // segment flags (see TileRef)
+  uint8_t n_first;         // how many (min(kStages, u1 - u0)); 0 without a plan
 };
 
 struct TcSmem {
@@ -212,27 +215,52 @@ __device__ __forceinline__ bool spin_or_abort(TcSmem &S, const DecodeArgs &a, ui
   return true;
 }
 
+// The tile of unit u in a CTA's range [u0, u1): its first cache row, its kv
+// head, and whether it starts (1) / ends (2) its segment within the range.
+struct TileRef {
+  int row, h;
+  uint8_t flags;
+};
+__device__ __forceinline__ TileRef tile_ref(const PlanCore &P, int n_blocks, int64_t u, int64_t u0,
+                                            int64_t u1) {
+  const UnitPos x = unit_pos(P, n_blocks, u);
+  TileRef t;
+  t.row = P.start[x.b] + x.t * kT;
+  t.h = x.h;
+  t.flags = (seg_first_unit(x, u, u0) ? 1 : 0) | (seg_last_unit(x, u, u1) ? 2 : 0);
+  return t;
+}
+
+// Streams the CTA's tiles through the ring.  The first n_first come decoded
+// from the plan, so that the ring fills without waiting on the unit
+// arithmetic; the others are decoded while their stage is still busy.
 __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
                          const CUtensorMap *tv, int64_t u0, int64_t u1) {
   const uint64_t pol = policy_evict_first();
+  const int n_first = S.cp.n_first;
   int i = 0;
   for (int64_t u = u0; u < u1; ++u, ++i) {
     const int s = i % kStages;
     // the tile's coordinates first, so that only the copy waits for the stage
-    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
-    const int row = S.ps.plan.start[x.b] + x.t * kT;
-    const uint8_t flags = (seg_first_unit(x, u, u0) ? 1 : 0) | (seg_last_unit(x, u, u1) ? 2 : 0);
+    TileRef t;
+    if (i < n_first) {
+      t.row = S.cp.trow[i];
+      t.h = S.cp.th[i];
+      t.flags = S.cp.tfl[i];
+    } else {
+      t = tile_ref(S.ps.plan, a.n_blocks, u, u0, u1);
+    }
     uint8_t *st = S.stage[s];
     if (i >= kStages && !spin_or_abort(S, a, &S.kv_empty[s], ((i / kStages) & 1) ^ 1)) break;
     // read by the MMA thread once the stage's copies are seen complete (the
     // arrive below releases this store)
-    S.tflags[s] = flags;
+    S.tflags[s] = t.flags;
     mbar_arrive_expect_tx(&S.k_full[s], 2 * kBox);
-    tma_load_3d(st, tk, &S.k_full[s], 0, row, x.h, pol);
-    tma_load_3d(st + kBox, tk, &S.k_full[s], 64, row, x.h, pol);
+    tma_load_3d(st, tk, &S.k_full[s], 0, t.row, t.h, pol);
+    tma_load_3d(st + kBox, tk, &S.k_full[s], 64, t.row, t.h, pol);
     mbar_arrive_expect_tx(&S.v_full[s], 2 * kBox);
-    tma_load_3d(st + 2 * kBox, tv, &S.v_full[s], 0, row, x.h, pol);
-    tma_load_3d(st + 3 * kBox, tv, &S.v_full[s], 64, row, x.h, pol);
+    tma_load_3d(st + 2 * kBox, tv, &S.v_full[s], 0, t.row, t.h, pol);
+    tma_load_3d(st + 3 * kBox, tv, &S.v_full[s], 64, t.row, t.h, pol);
   }
   // no copy may still be landing in shared memory when the CTA retires
   for (int j = (i > kStages ? i - kStages : 0); j < i; ++j) {
@@ -790,8 +818,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.tiles_done = 0;
     S.plan_ok = 1;
     // (with a plan, the bulk copy brings these: no generic store may race it)
-    if (!kPlanned)
+    if (!kPlanned) {
       for (int k = 0; k < kPreItems; ++k) S.cp.mpre_n[k] = -1;
+      S.cp.n_first = 0;
+    }
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -917,6 +947,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < kPre; ++k) {
       S.cp.us[k] = u;
       if (u < S.cp.u1) u = next_segment(P, a.n_blocks, u);
+    }
+    const int64_t nf = min(static_cast<int64_t>(kStages), S.cp.u1 - S.cp.u0);
+    S.cp.n_first = static_cast<uint8_t>(nf > 0 ? nf : 0);
+    for (int i = 0; i < kStages; ++i) {
+      TileRef t = {0, 0, 0};
+      if (i < nf) t = tile_ref(P, a.n_blocks, S.cp.u0 + i, S.cp.u0, S.cp.u1);
+      S.cp.trow[i] = t.row;
+      S.cp.th[i] = static_cast<uint8_t>(t.h);
+      S.cp.tfl[i] = t.flags;
     }
   }
   __syncthreads();

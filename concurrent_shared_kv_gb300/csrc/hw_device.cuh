@@ -11,16 +11,17 @@
 //   block, instead of stacking every head's short blocks on the last CTAs.
 //   segment   = the units of one (block, kv head), id seg = h * n_blocks + b,
 //   increasing along the unit order.
-//   The split is stream-K over a weighted line: every unit weighs 1 and every
-//   segment start kSegW more (a segment switch costs a record epilogue and a
-//   new set of rotated queries), so a CTA that crosses several short worker
-//   blocks streams fewer tiles than one inside the long common block.  Unit
-//   (h, b, t) sits at weight h WH + ubase[b] + kSegW (sord[b] + 1) + t, where
-//   sord[b] counts the non-empty blocks before b and WH = UH + kSegW NB.  CTA
-//   c of C takes the units whose weight lies in [floor(c W / C),
-//   floor((c+1) W / C)).  C = min(grid, W / (kSegW + 1)): any kSegW + 1
-//   consecutive weights hold a unit, so every working CTA owns at least one
-//   unit and the CTAs touching a segment form one contiguous range.
+//   The split is stream-K over a weighted line: every unit weighs kTileW and
+//   every segment start kSegW more (a segment switch costs a record epilogue
+//   and a new set of rotated queries), so a CTA that crosses several short
+//   worker blocks streams fewer tiles than one inside the long common block.
+//   Unit (h, b, t) starts at weight h WH + kTileW (ubase[b] + t) +
+//   kSegW (sord[b] + 1), where sord[b] counts the non-empty blocks before b
+//   and WH = kTileW UH + kSegW NB.  CTA c of C takes the units whose start
+//   lies in [floor(c W / C), floor((c+1) W / C)).  C = min(grid,
+//   W / (kSegW + kTileW)): unit starts are at most kSegW + kTileW apart, so
+//   every working CTA owns at least one unit and the CTAs touching a segment
+//   form one contiguous range.
 //   A CTA emits one partial record per (segment it touched, query head
 //   served) into slot seg + c, unique because seg and c never both stay put
 //   as units advance.  Every delivered record bumps the arrival counter of
@@ -172,7 +173,12 @@ __device__ __forceinline__ int entry_rank_scan(const DecodeArgs &a, int e, int l
 // the plan: every CTA derives the same unit decomposition from the metadata
 // ---------------------------------------------------------------------------
 
-constexpr int kSegW = 3;  // weight of a segment start, in tiles
+// Weights of a unit (one tile) and of a segment start.  Measured on the 40/8
+// head, 16K-token-common workload, a segment start costs about as much as
+// three tiles once the records, arrivals and merge wait are counted; the
+// ratio can be made finer through kTileW.
+constexpr int kTileW = 1;
+constexpr int kSegW = 3;
 
 struct PlanCore {
   int32_t tiles[HW_MAX_BLOCKS];      // tiles per kv head (0: block skipped)
@@ -211,14 +217,16 @@ __device__ __forceinline__ int64_t cta_unit_begin(const PlanCore &P, int n_block
   const int64_t w = div_nn(P.W * c, P.C);
   const int h = static_cast<int>(div_nn(w, P.WH));
   const int64_t l = w - static_cast<int64_t>(h) * P.WH;
-  // the last block whose weight region [ubase + kSegW sord, ...) starts at or before l
+  // the last block whose weight region [kTileW ubase + kSegW sord, ...) starts
+  // at or before l, then its first unit starting at or after l (one past its
+  // last unit is the next block's first, or the next head's)
   int lo = 0, hi = n_blocks - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (P.ubase[mid] + static_cast<int64_t>(kSegW) * P.sord[mid] <= l) lo = mid; else hi = mid - 1;
+    if (kTileW * P.ubase[mid] + static_cast<int64_t>(kSegW) * P.sord[mid] <= l) lo = mid; else hi = mid - 1;
   }
-  const int64_t off = l - (P.ubase[lo] + static_cast<int64_t>(kSegW) * P.sord[lo]);
-  return static_cast<int64_t>(h) * P.UH + P.ubase[lo] + (off > kSegW ? off - kSegW : 0);
+  const int64_t off = l - (kTileW * P.ubase[lo] + static_cast<int64_t>(kSegW) * P.sord[lo]) - kSegW;
+  return static_cast<int64_t>(h) * P.UH + P.ubase[lo] + (off > 0 ? (off + kTileW - 1) / kTileW : 0);
 }
 
 // Loads the metadata into the cache (one round of independent loads), checks
@@ -335,9 +343,9 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanS
       P.UH = carry;
       P.U = carry * a.n_kv_heads;
       P.NB = ncarry;
-      P.WH = carry + static_cast<int64_t>(kSegW) * ncarry;
+      P.WH = kTileW * carry + static_cast<int64_t>(kSegW) * ncarry;
       P.W = P.WH * a.n_kv_heads;
-      const int64_t cmax = P.W / (kSegW + 1);
+      const int64_t cmax = P.W / (kSegW + kTileW);
       P.C = static_cast<int>(cmax < static_cast<int64_t>(gridDim.x) ? cmax : gridDim.x);
     }
     __syncwarp();
@@ -424,12 +432,12 @@ __device__ __forceinline__ UnitPos unit_pos(const PlanCore &P, int n_blocks, int
   return x;
 }
 
-// Weight of unit u (strictly increasing in u).
+// Start weight of unit u (strictly increasing in u).
 __device__ __forceinline__ int64_t unit_weight(const PlanCore &P, int n_blocks, int64_t u) {
   const int h = static_cast<int>(div_nn(u, P.UH));
   const int64_t local = u - static_cast<int64_t>(h) * P.UH;
   const int b = block_of_unit(P, n_blocks, local);
-  return static_cast<int64_t>(h) * P.WH + local + static_cast<int64_t>(kSegW) * (P.sord[b] + 1);
+  return static_cast<int64_t>(h) * P.WH + kTileW * local + static_cast<int64_t>(kSegW) * (P.sord[b] + 1);
 }
 
 // The CTA that owns unit u: the largest c with floor(c W / C) <= weight(u).
