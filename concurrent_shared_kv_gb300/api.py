@@ -26,8 +26,12 @@ DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMA
 # every symbol the header declares
 EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode",
            "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_decode_noalloc",
-           "hw_block_commit", "hw_workspace_status", "hw_views_combined", "hw_last_cuda_error",
-           "hw_status_string"]
+           "hw_block_commit", "hw_block_commit_many", "hw_workspace_status", "hw_views_combined",
+           "hw_views", "hw_last_cuda_error", "hw_status_string"]
+HW_LAYOUT_COMBINED, HW_LAYOUT_INTERLEAVED, HW_LAYOUT_CONTIGUOUS = 0, 1, 2
+LAYOUTS = {"combined": HW_LAYOUT_COMBINED, "interleaved": HW_LAYOUT_INTERLEAVED,
+           "contiguous": HW_LAYOUT_CONTIGUOUS}
+HW_MAX_COMMITS = 64
 
 
 class HwError(RuntimeError):
@@ -75,8 +79,12 @@ def lib(path: Optional[str] = None):
                                   ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
                                   ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32,
                                   ctypes.c_int32, _P]
+    L.hw_block_commit_many.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_double, _P, _P, ctypes.c_int64, _P, _P,
+                                       ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P]
     L.hw_workspace_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
     L.hw_views_combined.argtypes = [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
+    L.hw_views.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
     L.hw_last_cuda_error.argtypes = []
     L.hw_status_string.argtypes = [ctypes.c_int]
     L.hw_status_string.restype = ctypes.c_char_p
@@ -190,6 +198,22 @@ def block_commit(dtype: int, n_layers: int, n_kv_heads: int, head_dim: int, rope
     return st
 
 
+def block_commit_many(dtype: int, n_layers: int, n_kv_heads: int, head_dim: int, rope_theta: float,
+                      k_src, v_src, src_capacity: int, k_dst, v_dst, dst_capacity: int,
+                      src_begin, n_tokens, dst_offset, pos_delta, stream=None) -> int:
+    """Several commits in one launch; the four per-commit sequences are host ints."""
+    arrs = [np.ascontiguousarray(x, dtype=np.int32) for x in (src_begin, n_tokens, dst_offset, pos_delta)]
+    n = len(arrs[0])
+    if any(len(x) != n for x in arrs):
+        raise ValueError("per-commit sequences of different lengths")
+    st = lib().hw_block_commit_many(int(dtype), int(n_layers), int(n_kv_heads), int(head_dim),
+                                    float(rope_theta), _ptr(k_src), _ptr(v_src), int(src_capacity),
+                                    _ptr(k_dst), _ptr(v_dst), int(dst_capacity), int(n),
+                                    *[x.ctypes.data for x in arrs], _stream(stream))
+    _check("hw_block_commit_many", st)
+    return st
+
+
 def workspace_status(workspace, stream=None) -> int:
     """Device error bits (HW_DEV_*) since the last read; synchronises the stream."""
     f = ctypes.c_int32(0)
@@ -206,6 +230,20 @@ def views_combined(block_len, n_problems: int, n_workers: int):
     qp = np.empty(rows, np.int32)
     _check("hw_views_combined", lib().hw_views_combined(int(n_problems), int(n_workers), bl.ctypes.data,
                                                         vb.ctypes.data, vo.ctypes.data, qp.ctypes.data))
+    return vb, vo, qp
+
+
+def views(layout, block_len, n_problems: int, n_workers: int):
+    """Host helper: (view_block, view_offset, q_pos) of a cache layout ("combined",
+    "interleaved", "contiguous" or its HW_LAYOUT_* value)."""
+    lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    bl = np.ascontiguousarray(block_len, dtype=np.int32)
+    rows, V = n_problems * n_workers, n_workers + 1
+    vb = np.empty((rows, V), np.int32)
+    vo = np.empty((rows, V), np.int32)
+    qp = np.empty(rows, np.int32)
+    _check("hw_views", lib().hw_views(lay, int(n_problems), int(n_workers), bl.ctypes.data,
+                                      vb.ctypes.data, vo.ctypes.data, qp.ctypes.data))
     return vb, vo, qp
 
 

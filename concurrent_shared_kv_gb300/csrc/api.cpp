@@ -339,28 +339,49 @@ int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_c
                        stream);
 }
 
-int hw_block_commit(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
-                    double rope_theta, const void *k_src, const void *v_src, int64_t src_capacity,
-                    int32_t src_begin, int32_t n_tokens, void *k_dst, void *v_dst,
-                    int64_t dst_capacity, int32_t dst_offset, int32_t pos_delta, void *stream) {
+static_assert(kMaxCommits == HW_MAX_COMMITS, "commit table size");
+
+// Checks and launch of n commits (hw_block_commit: n = 1).
+static int commit_impl(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                       double rope_theta, const void *k_src, const void *v_src,
+                       int64_t src_capacity, void *k_dst, void *v_dst, int64_t dst_capacity,
+                       int32_t n, const int32_t *src_begin, const int32_t *n_tokens,
+                       const int32_t *dst_offset, const int32_t *pos_delta, void *stream) {
   if (dtype != HW_F32 && dtype != HW_BF16) return HW_ERR_INVALID;
-  if (n_layers < 0 || n_kv_heads <= 0 || n_tokens < 0 || src_begin < 0 || dst_offset < 0 ||
-      src_capacity < 0 || dst_capacity < 0)
-    return HW_ERR_INVALID;
+  if (n < 0 || n > HW_MAX_COMMITS) return HW_ERR_INVALID;
+  if (n > 0 && (!src_begin || !n_tokens || !dst_offset || !pos_delta)) return HW_ERR_INVALID;
+  if (n_layers < 0 || n_kv_heads <= 0 || src_capacity < 0 || dst_capacity < 0) return HW_ERR_INVALID;
+  for (int c = 0; c < n; ++c)
+    if (n_tokens[c] < 0 || src_begin[c] < 0 || dst_offset[c] < 0) return HW_ERR_INVALID;
   if (!(rope_theta > 1.0) || !std::isfinite(rope_theta)) return HW_ERR_INVALID;
   const int esz = dtype == HW_F32 ? 4 : 2;
   const int epv = 16 / esz;
   if (head_dim <= 0 || head_dim > 128 || head_dim % (2 * epv) != 0) return HW_ERR_UNSUPPORTED;
-  if (n_layers == 0 || n_tokens == 0) return HW_OK;
+  int64_t tokens = 0;
+  for (int c = 0; c < n; ++c) tokens += n_tokens[c];
+  if (n_layers == 0 || tokens == 0) return HW_OK;
   if (!k_src || !v_src || !k_dst || !v_dst) return HW_ERR_INVALID;
-  if (static_cast<int64_t>(src_begin) + n_tokens > src_capacity) return HW_ERR_CAPACITY;
-  if (static_cast<int64_t>(dst_offset) + n_tokens > dst_capacity) return HW_ERR_CAPACITY;
+  for (int c = 0; c < n; ++c) {
+    if (static_cast<int64_t>(src_begin[c]) + n_tokens[c] > src_capacity) return HW_ERR_CAPACITY;
+    if (static_cast<int64_t>(dst_offset[c]) + n_tokens[c] > dst_capacity) return HW_ERR_CAPACITY;
+  }
   for (const void *p : {k_src, v_src, static_cast<const void *>(k_dst), static_cast<const void *>(v_dst)})
     if (reinterpret_cast<uintptr_t>(p) & 15u) return HW_ERR_INVALID;
 
   // Overlap: the address spans of the pools; spans that meet are only allowed
-  // when they are the same pool (same base and capacity) and the token ranges
-  // are disjoint.
+  // when they are the same pool (same base and capacity) and every destination
+  // token range is disjoint from every source range.  Destination ranges never
+  // meet one another.
+  auto disjoint = [](int64_t a0, int64_t na, int64_t b0, int64_t nb) {
+    return na == 0 || nb == 0 || a0 + na <= b0 || b0 + nb <= a0;
+  };
+  for (int c = 0; c < n; ++c)
+    for (int e = c + 1; e < n; ++e)
+      if (!disjoint(dst_offset[c], n_tokens[c], dst_offset[e], n_tokens[e])) return HW_ERR_OVERLAP;
+  bool tokens_disjoint = true;
+  for (int c = 0; c < n; ++c)
+    for (int e = 0; e < n; ++e)
+      if (!disjoint(dst_offset[c], n_tokens[c], src_begin[e], n_tokens[e])) tokens_disjoint = false;
   const int64_t row = static_cast<int64_t>(head_dim) * esz;
   const int64_t src_span = static_cast<int64_t>(n_layers) * n_kv_heads * src_capacity * row;
   const int64_t dst_span = static_cast<int64_t>(n_layers) * n_kv_heads * dst_capacity * row;
@@ -368,14 +389,10 @@ int hw_block_commit(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
   };
-  const bool tokens_disjoint =
-      src_begin + n_tokens <= dst_offset || dst_offset + n_tokens <= src_begin;
-  const struct { const void *s; } srcs[2] = {{k_src}, {v_src}};
-  const struct { const void *d; } dsts[2] = {{k_dst}, {v_dst}};
-  for (const auto &dd : dsts) {
-    for (const auto &ss : srcs) {
-      if (!meets(dd.d, dst_span, ss.s, src_span)) continue;
-      if (dd.d == ss.s && src_capacity == dst_capacity && tokens_disjoint) continue;
+  for (const void *d : {static_cast<const void *>(k_dst), static_cast<const void *>(v_dst)}) {
+    for (const void *sp : {k_src, v_src}) {
+      if (!meets(d, dst_span, sp, src_span)) continue;
+      if (d == sp && src_capacity == dst_capacity && tokens_disjoint) continue;
       return HW_ERR_OVERLAP;
     }
   }
@@ -389,16 +406,38 @@ int hw_block_commit(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t
   a.v_dst = v_dst;
   a.src_capacity = src_capacity;
   a.dst_capacity = dst_capacity;
-  a.src_begin = src_begin;
-  a.dst_offset = dst_offset;
-  a.n_tokens = n_tokens;
   a.n_layers = n_layers;
   a.n_kv_heads = n_kv_heads;
   a.head_dim = head_dim;
-  a.delta = pos_delta;
+  a.n_commits = n;
+  for (int c = 0; c < n; ++c) {
+    a.src_begin[c] = src_begin[c];
+    a.dst_offset[c] = dst_offset[c];
+    a.n_tokens[c] = n_tokens[c];
+    a.delta[c] = pos_delta[c];
+  }
   rope_phase_table(head_dim, rope_theta, a.phase);
   const cudaError_t e = launch_commit(a, dtype, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? HW_OK : cuda_fail(e);
+}
+
+int hw_block_commit(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                    double rope_theta, const void *k_src, const void *v_src, int64_t src_capacity,
+                    int32_t src_begin, int32_t n_tokens, void *k_dst, void *v_dst,
+                    int64_t dst_capacity, int32_t dst_offset, int32_t pos_delta, void *stream) {
+  return commit_impl(dtype, n_layers, n_kv_heads, head_dim, rope_theta, k_src, v_src,
+                     src_capacity, k_dst, v_dst, dst_capacity, 1, &src_begin, &n_tokens,
+                     &dst_offset, &pos_delta, stream);
+}
+
+int hw_block_commit_many(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                         double rope_theta, const void *k_src, const void *v_src,
+                         int64_t src_capacity, void *k_dst, void *v_dst, int64_t dst_capacity,
+                         int32_t n_commits, const int32_t *src_begin, const int32_t *n_tokens,
+                         const int32_t *dst_offset, const int32_t *pos_delta, void *stream) {
+  return commit_impl(dtype, n_layers, n_kv_heads, head_dim, rope_theta, k_src, v_src,
+                     src_capacity, k_dst, v_dst, dst_capacity, n_commits, src_begin, n_tokens,
+                     dst_offset, pos_delta, stream);
 }
 
 int hw_workspace_status(void *workspace, int32_t *flags, void *stream) {
@@ -418,12 +457,16 @@ int hw_workspace_status(void *workspace, int32_t *flags, void *stream) {
   return HW_OK;
 }
 
-int hw_views_combined(int32_t n_problems, int32_t n_workers, const int32_t *block_len,
-                      int32_t *view_block, int32_t *view_offset, int32_t *q_pos) {
+int hw_views(int32_t layout, int32_t n_problems, int32_t n_workers, const int32_t *block_len,
+             int32_t *view_block, int32_t *view_offset, int32_t *q_pos) {
+  if (layout != HW_LAYOUT_COMBINED && layout != HW_LAYOUT_INTERLEAVED &&
+      layout != HW_LAYOUT_CONTIGUOUS)
+    return HW_ERR_INVALID;
   if (n_problems < 0 || n_workers <= 0) return HW_ERR_INVALID;
   if (n_problems == 0) return HW_OK;
   if (!block_len || !view_block || !view_offset || !q_pos) return HW_ERR_INVALID;
   const int W = n_workers, V = n_workers + 1;
+  const bool others = layout != HW_LAYOUT_INTERLEAVED;
   for (int p = 0; p < n_problems; ++p) {
     const int base = p * (W + 1);
     for (int w = 0; w < W; ++w) {
@@ -437,14 +480,25 @@ int hw_views_combined(int32_t n_problems, int32_t n_workers, const int32_t *bloc
         ++v;
       };
       put(base);                                    // common cache
-      for (int o = 0; o < W; ++o)
-        if (o != w) put(base + 1 + o);              // others' unfinished steps, worker order
+      if (others)
+        for (int o = 0; o < W; ++o)
+          if (o != w) put(base + 1 + o);            // others' unfinished steps, worker order
       put(base + 1 + w);                            // own unfinished step
+      for (; v < V; ++v) {                          // unused entries
+        view_block[row * V + v] = -1;
+        view_offset[row * V + v] = 0;
+      }
       if (pos > INT32_MAX) return HW_ERR_INVALID;
       q_pos[row] = static_cast<int32_t>(pos);
     }
   }
   return HW_OK;
+}
+
+int hw_views_combined(int32_t n_problems, int32_t n_workers, const int32_t *block_len,
+                      int32_t *view_block, int32_t *view_offset, int32_t *q_pos) {
+  return hw_views(HW_LAYOUT_COMBINED, n_problems, n_workers, block_len, view_block, view_offset,
+                  q_pos);
 }
 
 int hw_last_cuda_error(void) { return g_last_cuda_error; }

@@ -1,9 +1,9 @@
-// block_commit.cu - move a finished step into the shared history (Hogwild!
+// block_commit.cu - move finished steps into the shared history (Hogwild!
 // notes, key design 2: a finished step's KV is rotated and moved into the
-// common cache).
+// common cache).  For each commit c of the launch:
 //
-//   K_dst[l][h][dst_offset + j] = rho(K_src[l][h][src_begin + j], delta)
-//   V_dst[l][h][dst_offset + j] = V_src[l][h][src_begin + j]
+//   K_dst[l][h][dst_offset_c + j] = rho(K_src[l][h][src_begin_c + j], delta_c)
+//   V_dst[l][h][dst_offset_c + j] = V_src[l][h][src_begin_c + j]
 //
 // HBM-bound: every byte is read once and written once.  A thread owns one
 // 16-byte chunk of the first half of a key row and the matching chunk of the
@@ -60,24 +60,29 @@ __device__ __forceinline__ uint4 rotate16<__nv_bfloat16>(const uint4 &lo, const 
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// Grid row c (blockIdx.y) commits range c; its CTAs stride over the range's
+// (layer, head, token, chunk) items.
 template <typename T>
 __global__ void __launch_bounds__(kCommitThreads) block_commit_kernel(const __grid_constant__ CommitArgs a) {
   constexpr int EPV = 16 / sizeof(T);
   __shared__ float cs[64], sn[64];
-  const int D = a.head_dim;
-  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) rope_cos_sin(a.delta, a.phase[i], &cs[i], &sn[i]);
+  const int c = blockIdx.y;
+  const int D = a.head_dim, n_tokens = a.n_tokens[c];
+  const int64_t delta = a.delta[c];
+  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) rope_cos_sin(delta, a.phase[i], &cs[i], &sn[i]);
   __syncthreads();
   const int half_chunks = (D / 2) / EPV;
-  const int64_t rows = static_cast<int64_t>(a.n_layers) * a.n_kv_heads * a.n_tokens;
+  const int64_t rows = static_cast<int64_t>(a.n_layers) * a.n_kv_heads * n_tokens;
   const int64_t total = rows * half_chunks;
-  const bool copy_only = (a.delta == 0);
+  const bool copy_only = (delta == 0);
+  const int64_t src_begin = a.src_begin[c], dst_offset = a.dst_offset[c];
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t row = idx / half_chunks;
     const int ch = static_cast<int>(idx % half_chunks);
-    const int64_t j = row % a.n_tokens, lh = row / a.n_tokens;  // lh = layer * Hkv + h
-    const int64_t so = (lh * a.src_capacity + a.src_begin + j) * D + ch * EPV;
-    const int64_t dof = (lh * a.dst_capacity + a.dst_offset + j) * D + ch * EPV;
+    const int64_t j = row % n_tokens, lh = row / n_tokens;  // lh = layer * Hkv + h
+    const int64_t so = (lh * a.src_capacity + src_begin + j) * D + ch * EPV;
+    const int64_t dof = (lh * a.dst_capacity + dst_offset + j) * D + ch * EPV;
     const T *ks = reinterpret_cast<const T *>(a.k_src);
     const T *vs = reinterpret_cast<const T *>(a.v_src);
     T *kd = reinterpret_cast<T *>(a.k_dst);
@@ -100,17 +105,21 @@ __global__ void __launch_bounds__(kCommitThreads) block_commit_kernel(const __gr
 
 cudaError_t launch_commit(const CommitArgs &a, int dtype, cudaStream_t s) {
   const int epv = dtype == HW_F32 ? 4 : 8;
-  const int64_t work = static_cast<int64_t>(a.n_layers) * a.n_kv_heads * a.n_tokens *
-                       ((a.head_dim / 2) / epv);
+  int64_t work = 0;
+  for (int c = 0; c < a.n_commits; ++c)
+    work += static_cast<int64_t>(a.n_layers) * a.n_kv_heads * a.n_tokens[c] * ((a.head_dim / 2) / epv);
   if (work == 0) return cudaSuccess;
+  // about eight CTAs per SM in all, shared evenly by the commits
   const int sms = device_sm_count();
   int64_t ctas = (work + kCommitThreads - 1) / kCommitThreads;
   const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
   if (ctas > cap) ctas = cap;
+  const int64_t per = (ctas + a.n_commits - 1) / a.n_commits;
+  const dim3 grid(static_cast<unsigned>(per > 0 ? per : 1), static_cast<unsigned>(a.n_commits));
   if (dtype == HW_F32)
-    block_commit_kernel<float><<<static_cast<int>(ctas), kCommitThreads, 0, s>>>(a);
+    block_commit_kernel<float><<<grid, kCommitThreads, 0, s>>>(a);
   else
-    block_commit_kernel<__nv_bfloat16><<<static_cast<int>(ctas), kCommitThreads, 0, s>>>(a);
+    block_commit_kernel<__nv_bfloat16><<<grid, kCommitThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

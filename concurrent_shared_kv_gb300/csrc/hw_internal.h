@@ -73,13 +73,16 @@ struct PlanOut {
 cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s);
 int decode_simt_ctas_per_sm(int dtype, int head_dim);
 
+// One launch commits n_commits ranges (kernel grid row c = commit c).
+constexpr int kMaxCommits = 64;  // HW_MAX_COMMITS
 struct CommitArgs {
   const void *k_src, *v_src;
   void *k_dst, *v_dst;
   int64_t src_capacity, dst_capacity;
-  int32_t src_begin, dst_offset, n_tokens, n_layers, n_kv_heads, head_dim;
+  int32_t n_layers, n_kv_heads, head_dim, n_commits;
   uint64_t phase[64];
-  int64_t delta;  // pos_delta
+  int32_t src_begin[kMaxCommits], dst_offset[kMaxCommits], n_tokens[kMaxCommits];
+  int32_t delta[kMaxCommits];  // pos_delta
 };
 cudaError_t launch_commit(const CommitArgs &a, int dtype, cudaStream_t s);
 

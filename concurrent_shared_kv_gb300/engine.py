@@ -90,3 +90,16 @@ def block_commit(k_src: torch.Tensor, v_src: torch.Tensor, src_begin: int, n_tok
     _, _, cd, _ = dims(k_dst)
     return api.block_commit(DTYPES[k_src.dtype], L, H, D, rope_theta, k_src, v_src, cs, src_begin,
                             n_tokens, k_dst, v_dst, cd, dst_offset, pos_delta, stream=stream)
+
+
+def block_commit_many(k_src: torch.Tensor, v_src: torch.Tensor, commits, k_dst: torch.Tensor,
+                      v_dst: torch.Tensor, rope_theta: float, stream=None):
+    """Several finished steps in one launch.  `commits`: (src_begin, n_tokens,
+    dst_offset, pos_delta) tuples; pools as in block_commit."""
+    def dims(t):
+        return (1,) + tuple(t.shape) if t.dim() == 3 else tuple(t.shape)
+    L, H, cs, D = dims(k_src)
+    _, _, cd, _ = dims(k_dst)
+    cols = list(zip(*commits)) if commits else [(), (), (), ()]
+    return api.block_commit_many(DTYPES[k_src.dtype], L, H, D, rope_theta, k_src, v_src, cs, k_dst,
+                                 v_dst, cd, *cols, stream=stream)

@@ -227,6 +227,25 @@ int hw_block_commit(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t
                     int64_t dst_capacity, int32_t dst_offset, int32_t pos_delta, void *stream);
 
 /*
+ * Several finished steps committed in one launch (workers that finish a step
+ * together join the shared history in one go, in the caller's order).
+ * Commit c applies the hw_block_commit formula to its own range:
+ *   K_dst[l][h][dst_offset[c] + j] = rho(K_src[l][h][src_begin[c] + j], pos_delta[c])
+ *   V_dst[l][h][dst_offset[c] + j] = V_src[l][h][src_begin[c] + j]
+ * for j < n_tokens[c], with the pools, rounding and layer stride of
+ * hw_block_commit.  src_begin, n_tokens, dst_offset, pos_delta: host arrays of
+ * n_commits entries, 0 <= n_commits <= HW_MAX_COMMITS.
+ * Errors: those of hw_block_commit for each commit, and HW_ERR_OVERLAP when
+ * two destination ranges meet.
+ */
+#define HW_MAX_COMMITS 64
+int hw_block_commit_many(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                         double rope_theta, const void *k_src, const void *v_src,
+                         int64_t src_capacity, void *k_dst, void *v_dst, int64_t dst_capacity,
+                         int32_t n_commits, const int32_t *src_begin, const int32_t *n_tokens,
+                         const int32_t *dst_offset, const int32_t *pos_delta, void *stream);
+
+/*
  * Synchronises `stream`, reads and clears the device error bits of a
  * workspace (HW_DEV_* flags, 0 = none) into *flags.
  */
@@ -242,6 +261,27 @@ int hw_workspace_status(void *workspace, int32_t *flags, void *stream);
  */
 int hw_views_combined(int32_t n_problems, int32_t n_workers, const int32_t *block_len,
                       int32_t *view_block, int32_t *view_offset, int32_t *q_pos);
+
+/*
+ * Host helper: the views of one of the three cache layouts the Hogwild! notes
+ * compare in their layout ablation, with the block ids of hw_views_combined.
+ *  HW_LAYOUT_COMBINED     common, the other workers in id order, itself
+ *                         (token-level visibility and the step history);
+ *  HW_LAYOUT_INTERLEAVED  common, itself: only finished steps, committed into
+ *                         the common history, are shared (step-level only);
+ *                         the other W-1 entries are -1;
+ *  HW_LAYOUT_CONTIGUOUS   the combined order over blocks that hold each
+ *                         worker's whole generation: nothing is ever
+ *                         committed, so the common block stays the prompt
+ *                         (token-level only).  The views are the combined
+ *                         ones; the difference is the caller's commit policy.
+ * view_offset = tokens before each block in the view; q_pos = the view's
+ * total length.  Arrays as in hw_views_combined.  HW_ERR_INVALID for an
+ * unknown layout.
+ */
+typedef enum { HW_LAYOUT_COMBINED = 0, HW_LAYOUT_INTERLEAVED = 1, HW_LAYOUT_CONTIGUOUS = 2 } hw_layout;
+int hw_views(int32_t layout, int32_t n_problems, int32_t n_workers, const int32_t *block_len,
+             int32_t *view_block, int32_t *view_offset, int32_t *q_pos);
 
 /* Last CUDA error code seen by this thread's library calls (cudaError_t). */
 int hw_last_cuda_error(void);

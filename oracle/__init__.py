@@ -212,3 +212,44 @@ def combined_views(block_len: Sequence[int], n_problems: int, n_workers: int):
                 pos += int(block_len[b])
             qp[p * W + w] = pos
     return vb, vo, qp
+
+
+def interleaved_views(block_len: Sequence[int], n_problems: int, n_workers: int):
+    """The interleaved cache layout of the notes' layout ablation (step-level
+    synchronisation only): a worker sees the common history - the prompt and
+    every finished step committed into it - then its own unfinished step; the
+    other workers' unfinished steps stay invisible until they are committed.
+    Same block ids and return values as combined_views; unused view entries
+    are -1 with offset 0.
+    """
+    W = n_workers
+    rows = n_problems * W
+    vb = np.full((rows, W + 1), -1, np.int32)
+    vo = np.zeros((rows, W + 1), np.int32)
+    qp = np.zeros(rows, np.int32)
+    for p in range(n_problems):
+        common = p * (W + 1)
+        for w in range(W):
+            own = common + 1 + w
+            r = p * W + w
+            vb[r, 0], vo[r, 0] = common, 0
+            vb[r, 1], vo[r, 1] = own, int(block_len[common])
+            qp[r] = int(block_len[common]) + int(block_len[own])
+    return vb, vo, qp
+
+
+def contiguous_views(block_len: Sequence[int], n_problems: int, n_workers: int):
+    """The contiguous cache layout of the notes' layout ablation (token-level
+    synchronisation only): every worker's whole generation is one growing
+    block that is never committed, so the common block holds only the prompt;
+    a worker sees the prompt, the other workers' generations in worker order,
+    then its own - the combined order, over blocks that are never moved.
+    """
+    return combined_views(block_len, n_problems, n_workers)
+
+
+def layout_views(layout: str, block_len: Sequence[int], n_problems: int, n_workers: int):
+    """Views of a layout by name: "combined", "interleaved" or "contiguous"."""
+    return {"combined": combined_views, "interleaved": interleaved_views,
+            "contiguous": contiguous_views}[layout](block_len, n_problems, n_workers)
+
