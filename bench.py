@@ -14,6 +14,7 @@ same workload (a bounded sample of layers per step) on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -37,6 +38,11 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--config", default="C3", choices=["C2", "C3", "C4", "C5"])
     p.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph")
+    p.add_argument("--layout", default="combined", choices=["combined", "interleaved", "contiguous"],
+                   help="views of the cache layout (the combined layout is the method's own)")
+    p.add_argument("--commit-all", action="store_true",
+                   help="C4: every worker's finished block joins the history each step, all in "
+                        "one hw_block_commit_many launch (the common block gets room for them)")
     p.add_argument("--unplanned", action="store_true",
                    help="one hw_attn_decode per layer instead of hw_attn_plan once per step "
                         "plus hw_attn_decode_planned per layer")
@@ -206,12 +212,16 @@ def main():
     dev = torch.device("cuda", local)
 
     w = wl.ALL[args.config]()
+    commit_all = args.commit_all and args.config == "C4"
+    if commit_all:
+        w = dataclasses.replace(w, name=w.name + ", all 4 workers' blocks committed per step",
+                                common_extra=w.n_workers * w.commit_tokens)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     L = w.layers if args.config != "C5" else 1
     if args.layers > 0:
         L = min(L, args.layers)
     lens, starts = w.block_lengths(), w.block_starts()
-    vb, vo, qp = api.views_combined(lens, w.n_problems, w.n_workers)
+    vb, vo, qp = api.views(args.layout, lens, w.n_problems, w.n_workers)
     sess = engine.DecodeSession(n_rows=w.n_rows, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
                                 head_dim=w.head_dim, n_blocks=w.n_blocks,
                                 max_view_blocks=w.n_workers + 1, capacity=w.capacity, dtype=tdt,
@@ -259,6 +269,12 @@ def main():
         # rotated by the position change and written after the common tokens
         # (the decode's views keep reading [0, common_len), so every rep times
         # the same work)
+        if commit_all:
+            n, c0 = w.commit_tokens, int(w.common_len[0])
+            commits = [(int(starts[1 + k]), n, int(starts[0]) + c0 + k * n, c0 + k * n)
+                       for k in range(w.n_workers)]
+            engine.block_commit_many(k_all, v_all, commits, k_all, v_all, w.rope_theta, stream=stream)
+            return
         wk = step_no[0] % w.n_workers
         step_no[0] += 1
         src = int(starts[1 + wk])
@@ -314,7 +330,7 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t = float(tt.item())
 
-    commit_bytes = w.commit_bytes_per_layer() * L if commit else 0
+    commit_bytes = w.commit_bytes_per_layer() * L * (w.n_workers if commit_all else 1) if commit else 0
     step_bytes = w.kv_bytes_per_layer() * calls_per_step + commit_bytes
     per_step = t / args.steps
     gbs_rank = step_bytes / per_step / 1e9
@@ -401,7 +417,7 @@ def main():
             "workers": w.n_workers, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
             "head_dim": w.head_dim, "kv_tokens_per_layer": w.kv_tokens(),
             "kv_bytes_per_step": step_bytes, "commit_bytes_per_step": commit_bytes,
-            "parallelism": f"replicas x{world}",
+            "parallelism": f"replicas x{world}", "layout": args.layout,
             "mode": "eager" if graph is None else "cuda-graph",
             "calls": ("hw_attn_plan once per step + hw_attn_decode_planned per layer" if planned
                       else "hw_attn_decode per layer"),
@@ -417,7 +433,7 @@ def main():
                      "peak_kind": peak_kind,
                      "kernel": f"{'hw_attn_decode_planned' if planned else 'hw_attn_decode'} ({kernel})",
                      "per_launch": "step time / layers per step (the plan launch included)"},
-        "gpu_launches": (calls_per_step + (1 if planned else 0)) * args.steps,
+        "gpu_launches": (calls_per_step + (1 if planned else 0) + (1 if commit else 0)) * args.steps,
         "clocks": clk.summary(),
         "e2e": e2e,
     }
