@@ -25,7 +25,8 @@ DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMA
 
 # every symbol the header declares
 EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode",
-           "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_decode_noalloc",
+           "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_plan_append",
+           "hw_attn_append_decode_planned", "hw_attn_decode_noalloc",
            "hw_block_commit", "hw_block_commit_many", "hw_workspace_status", "hw_views_combined",
            "hw_views", "hw_last_cuda_error", "hw_status_string"]
 HW_LAYOUT_COMBINED, HW_LAYOUT_INTERLEAVED, HW_LAYOUT_CONTIGUOUS = 0, 1, 2
@@ -74,6 +75,8 @@ def lib(path: Optional[str] = None):
     L.hw_attn_decode.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12 + [ctypes.c_size_t, _P]
     L.hw_attn_plan.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 7 + [ctypes.c_size_t, _P]
     L.hw_attn_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 6 + [ctypes.c_size_t, _P]
+    L.hw_attn_plan_append.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]
+    L.hw_attn_append_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]
     L.hw_attn_decode_noalloc.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12
     L.hw_block_commit.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
@@ -172,6 +175,30 @@ def attn_decode_planned(desc: AttnDesc, q, k_cache, v_cache, out, lse, workspace
                                       _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                                       _stream(stream))
     _check("hw_attn_decode_planned", st)
+    return st
+
+
+def attn_plan_append(desc: AttnDesc, block_start, block_len, view_block, view_offset, q_pos,
+                     append_block, append_pos, workspace, workspace_bytes: int, q_to_kv=None,
+                     stream=None) -> int:
+    """hw_attn_plan_append: the step planned with each row's new token
+    (append_block[r], append_pos[r]; -1 = none)."""
+    st = lib().hw_attn_plan_append(ctypes.byref(desc), _ptr(block_start), _ptr(block_len),
+                                   _ptr(view_block), _ptr(view_offset), _ptr(q_pos), _ptr(q_to_kv),
+                                   _ptr(append_block), _ptr(append_pos), _ptr(workspace),
+                                   int(workspace_bytes), _stream(stream))
+    _check("hw_attn_plan_append", st)
+    return st
+
+
+def attn_append_decode_planned(desc: AttnDesc, q, k_new, v_new, k_cache, v_cache, out, lse,
+                               workspace, workspace_bytes: int, stream=None) -> int:
+    """hw_attn_append_decode_planned: the layer's new tokens written, then the
+    layer decoded, in one launch."""
+    st = lib().hw_attn_append_decode_planned(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                             _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse),
+                                             _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check("hw_attn_append_decode_planned", st)
     return st
 
 

@@ -102,9 +102,11 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
   L.slots = static_cast<int64_t>(d.n_blocks) * d.n_kv_heads + max_ctas;
   const size_t rec = static_cast<size_t>(kMaxQ) * (d.head_dim + 4) * sizeof(float);
   L.meta_off = L.partials_off + up(static_cast<size_t>(L.slots) * rec);
-  // metadata copies: view_block, view_offset (rows x V), q_pos, q_to_kv, block_start, block_len
+  // metadata copies: view_block, view_offset (rows x V), q_pos, q_to_kv, block_start, block_len,
+  // append_block, append_pos
   const size_t entries = static_cast<size_t>(d.n_rows) * d.max_view_blocks;
-  const size_t meta = (2 * entries + d.n_rows + d.n_q_heads + 2 * static_cast<size_t>(d.n_blocks)) *
+  const size_t meta = (2 * entries + 3 * static_cast<size_t>(d.n_rows) + d.n_q_heads +
+                       2 * static_cast<size_t>(d.n_blocks)) *
                       sizeof(int32_t);
   L.plan_off = L.meta_off + up(meta);
   // the tensor-core plan: one record per CTA of its grid (one per SM)
@@ -118,6 +120,7 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
 // The metadata copies of a workspace (written by hw_attn_plan).
 struct MetaCopies {
   int32_t *view_block, *view_offset, *q_pos, *q_to_kv, *block_start, *block_len;
+  int32_t *append_block, *append_pos;
 };
 static MetaCopies meta_copies(const hw_attn_desc &d, const WorkspaceLayout &L, void *workspace) {
   int32_t *m = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.meta_off);
@@ -129,6 +132,8 @@ static MetaCopies meta_copies(const hw_attn_desc &d, const WorkspaceLayout &L, v
   c.q_to_kv = c.q_pos + d.n_rows;
   c.block_start = c.q_to_kv + d.n_q_heads;
   c.block_len = c.block_start + d.n_blocks;
+  c.append_block = c.block_len + d.n_blocks;
+  c.append_pos = c.append_block + d.n_rows;
   return c;
 }
 
@@ -218,9 +223,15 @@ static int decode_common(const hw_attn_desc *d, const void *q, const void *k_cac
                          const int32_t *view_block, const int32_t *view_offset,
                          const int32_t *q_pos, const int32_t *q_to_kv, const uint8_t *plan,
                          void *out, float *lse, void *workspace, const WorkspaceLayout &L,
-                         int max_ctas, void *stream) {
+                         int max_ctas, void *stream, const int32_t *append_block = nullptr,
+                         const int32_t *append_pos = nullptr, const void *k_new = nullptr,
+                         const void *v_new = nullptr) {
   DecodeArgs a;
   fill_args(a, d, L, workspace);
+  a.append_block = append_block;
+  a.append_pos = append_pos;
+  a.k_new = k_new;
+  a.v_new = v_new;
   a.q = q;
   a.k = k_cache;
   a.v = v_cache;
@@ -286,15 +297,18 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
                        q_pos, q_to_kv, nullptr, out, lse, workspace, L, max_ctas, stream);
 }
 
-int hw_attn_plan(const hw_attn_desc *d, const int32_t *block_start, const int32_t *block_len,
-                 const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
-                 const int32_t *q_to_kv, void *workspace, size_t workspace_bytes, void *stream) {
+static int plan_impl(const hw_attn_desc *d, const int32_t *block_start, const int32_t *block_len,
+                     const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
+                     const int32_t *q_to_kv, const int32_t *append_block,
+                     const int32_t *append_pos, void *workspace, size_t workspace_bytes,
+                     void *stream) {
   int st = check_desc(d);
   if (st != HW_OK) return st;
   if (d->n_rows == 0) return HW_OK;
   if (!q_pos) return HW_ERR_INVALID;
   if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
   if (d->n_blocks > 0 && (!block_start || !block_len)) return HW_ERR_INVALID;
+  if (append_block && !tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
   WorkspaceLayout L;
   int max_ctas = 0;
   st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
@@ -307,6 +321,8 @@ int hw_attn_plan(const hw_attn_desc *d, const int32_t *block_start, const int32_
   a.view_offset = view_offset;
   a.q_pos = q_pos;
   a.q_to_kv = q_to_kv;
+  a.append_block = append_block;
+  a.append_pos = append_pos;
   const MetaCopies m = meta_copies(*d, L, workspace);
   PlanOut o;
   o.plan = tensor_core_path(d) ? static_cast<uint8_t *>(workspace) + L.plan_off : nullptr;
@@ -316,8 +332,27 @@ int hw_attn_plan(const hw_attn_desc *d, const int32_t *block_start, const int32_
   o.q_to_kv = m.q_to_kv;
   o.block_start = m.block_start;
   o.block_len = m.block_len;
+  o.append_block = m.append_block;
+  o.append_pos = m.append_pos;
   const cudaError_t e = launch_plan(a, o, device_sm_count(), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? HW_OK : cuda_fail(e);
+}
+
+int hw_attn_plan(const hw_attn_desc *d, const int32_t *block_start, const int32_t *block_len,
+                 const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
+                 const int32_t *q_to_kv, void *workspace, size_t workspace_bytes, void *stream) {
+  return plan_impl(d, block_start, block_len, view_block, view_offset, q_pos, q_to_kv, nullptr,
+                   nullptr, workspace, workspace_bytes, stream);
+}
+
+int hw_attn_plan_append(const hw_attn_desc *d, const int32_t *block_start,
+                        const int32_t *block_len, const int32_t *view_block,
+                        const int32_t *view_offset, const int32_t *q_pos, const int32_t *q_to_kv,
+                        const int32_t *append_block, const int32_t *append_pos, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+  if (d && d->n_rows > 0 && (!append_block || !append_pos)) return HW_ERR_INVALID;
+  return plan_impl(d, block_start, block_len, view_block, view_offset, q_pos, q_to_kv,
+                   append_block, append_pos, workspace, workspace_bytes, stream);
 }
 
 int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_cache,
@@ -337,6 +372,29 @@ int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_c
   return decode_common(d, q, k_cache, v_cache, m.block_start, m.block_len, m.view_block,
                        m.view_offset, m.q_pos, m.q_to_kv, plan, out, lse, workspace, L, max_ctas,
                        stream);
+}
+
+int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const void *k_new,
+                                  const void *v_new, void *k_cache, void *v_cache, void *out,
+                                  float *lse, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+  int st = check_desc(d);
+  if (st != HW_OK) return st;
+  if (d->n_rows == 0) return HW_OK;
+  if (!tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
+  if (!q || !out || !k_new || !v_new) return HW_ERR_INVALID;
+  if (d->n_blocks > 0 && d->cache_capacity > 0 && (!k_cache || !v_cache)) return HW_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
+    return HW_ERR_INVALID;  // 16-byte loads of the new rows
+  WorkspaceLayout L;
+  int max_ctas = 0;
+  st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
+  if (st != HW_OK) return st;
+  const MetaCopies m = meta_copies(*d, L, workspace);
+  const uint8_t *plan = static_cast<const uint8_t *>(workspace) + L.plan_off;
+  return decode_common(d, q, k_cache, v_cache, m.block_start, m.block_len, m.view_block,
+                       m.view_offset, m.q_pos, m.q_to_kv, plan, out, lse, workspace, L, max_ctas,
+                       stream, m.append_block, m.append_pos, k_new, v_new);
 }
 
 static_assert(kMaxCommits == HW_MAX_COMMITS, "commit table size");

@@ -26,6 +26,8 @@
 // kernel costs stream time whatever its N, so fewer, wider products pay.)
 #include <cuda.h>
 
+#include <climits>
+
 #include "hw_device.cuh"
 #include "hw_sm100.cuh"
 
@@ -81,6 +83,8 @@ struct alignas(16) CtaPlan {
   uint8_t th[kStages];     // kv head,
   uint8_t tfl[kStages];    // segment flags (see TileRef)
   uint8_t n_first;         // how many (min(kStages, u1 - u0)); 0 without a plan
+  int32_t app_n;           // new tokens this CTA writes (hw_attn_plan_append), 0: none
+  int32_t app_tile;        // its first tile (from u0) that holds one of them
 };
 
 struct TcSmem {
@@ -106,6 +110,7 @@ struct TcSmem {
   uint64_t o_full[2], o_empty[2];  // per O buffer: segment done / epilogue read it
   uint64_t rec_ready[4];           // per segment mod 4: records written, arrivals due
   uint64_t plan_bar;               // a loaded plan has landed
+  uint64_t app_bar;                // this CTA's new tokens are written (and fenced)
 };
 
 // ------------------------------------------------------------------- plans
@@ -235,9 +240,12 @@ __device__ __forceinline__ TileRef tile_ref(const PlanCore &P, int n_blocks, int
 // from the plan, so that the ring fills without waiting on the unit
 // arithmetic; the others are decoded while their stage is still busy.
 __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
-                         const CUtensorMap *tv, int64_t u0, int64_t u1) {
+                         const CUtensorMap *tv, int64_t u0, int64_t u1, bool appending) {
   const uint64_t pol = policy_evict_first();
   const int n_first = S.cp.n_first;
+  // the first tile holding a new token is loaded only once the tokens are
+  // written (and fenced for the copy engine)
+  const int app_tile = appending ? S.cp.app_tile : -1;
   int i = 0;
   for (int64_t u = u0; u < u1; ++u, ++i) {
     const int s = i % kStages;
@@ -252,6 +260,7 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
     }
     uint8_t *st = S.stage[s];
     if (i >= kStages && !spin_or_abort(S, a, &S.kv_empty[s], ((i / kStages) & 1) ^ 1)) break;
+    if (i == app_tile && !spin_or_abort(S, a, &S.app_bar, 0)) break;
     // read by the MMA thread once the stage's copies are seen complete (the
     // arrive below releases this store)
     S.tflags[s] = t.flags;
@@ -416,15 +425,15 @@ __device__ __forceinline__ int64_t next_segment(const PlanCore &P, int n_blocks,
   return x.seg_first + x.tiles;
 }
 
-// Prologue of warps 2-7 (the TMA and MMA warps start at once): the metadata
-// of segment 0 (warp 2), then its queries rotated into the Q~ buffer (all six
-// warps).
+// Prologue of warps 2-7, or of warps 2-5 alone (nt = 128) while warps 6-7
+// write the CTA's new tokens: the metadata of segment 0 (warp 2), then its
+// queries rotated into the Q~ buffer.
 template <bool kPlanned>
-__device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
-  const int t = threadIdx.x - kWarpSoft * 32;  // 0..191
+__device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1, int nt) {
+  const int t = threadIdx.x - kWarpSoft * 32;  // 0 .. nt-1
   const int w = t >> 5, lane = t & 31;
   const int G = a.n_q_heads / a.n_kv_heads;
-  NamedSync<3, 192> sync;
+  auto sync = [nt]() { asm volatile("bar.sync 3, %0;" ::"r"(nt) : "memory"); };
   if (w == 0 && !kPlanned) {  // a plan brings it ready-made
     const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u0);
     seg_pre(a, S.ps.cache, S.cp.pre[0], x.b, x.h, lane);
@@ -432,26 +441,86 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
   sync();
   const SegQ &X = S.cp.pre[0];
   const int nq = min(X.m.n_ref * G, kN);
-  // items t and t + 192 of the nq * 8 (column, 16-byte chunk) items
+  // items t and t + nt of the nq * 8 <= 256 (column, 16-byte chunk) items
   const int n_items = nq * 8;
+  const int t1 = t + nt;
   const uint32_t qbase = smem_u32(S.q);
   QItem q0, q1;
   if (t < n_items) load_item(a, X, t >> 3, t & 7, q0);
-  if (t + 192 < n_items) load_item(a, X, (t + 192) >> 3, (t + 192) & 7, q1);
+  if (t1 < n_items) load_item(a, X, t1 >> 3, t1 & 7, q1);
   if (t < n_items) {
     uint4 v[4];
     rot_item(a, S, q0, t & 7, v);
     store_item(qbase, t >> 3, t & 7, v);
   }
-  if (t + 192 < n_items) {
+  if (t1 < n_items) {
     uint4 v[4];
-    rot_item(a, S, q1, (t + 192) & 7, v);
-    store_item(qbase, (t + 192) >> 3, (t + 192) & 7, v);
+    rot_item(a, S, q1, t1 & 7, v);
+    store_item(qbase, t1 >> 3, t1 & 7, v);
   }
   if (t == 0) S.meta_nref = X.m.n_ref;
   fence_proxy_async_smem();
   sync();
   if (t == 0) mbar_arrive(&S.q_full);  // phase 0: segment 0
+}
+
+// The CTA's new tokens (hw_attn_append_decode_planned), by warps 6-7: for
+// every (row, kv head) whose appended token lies in a tile of this CTA, the
+// key rotated at its block-local position - in fp32 from the stored values,
+// rounded once to bf16, the block commit's arithmetic - and the value copied,
+// into the cache rows that tile's copies will read.  The writes are fenced
+// for the async proxy before the producer is released.
+__device__ void append_tokens(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
+  const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
+  const int lane = tq & 31, wq = tq >> 5;
+  const PlanCore &P = S.ps.plan;
+  const int Hkv = a.n_kv_heads, npairs = a.n_rows * Hkv;
+  const __nv_bfloat16 *kn = static_cast<const __nv_bfloat16 *>(a.k_new);
+  const __nv_bfloat16 *vn = static_cast<const __nv_bfloat16 *>(a.v_new);
+  __nv_bfloat16 *kc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.k));
+  __nv_bfloat16 *vc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.v));
+  for (int base = wq * 32; base < npairs; base += 64) {
+    // lane: one (row, kv head) pair; the warp then writes the ones it owns
+    const int pr = base + lane;
+    int r = 0, h = 0, pos = 0, row = 0;
+    bool mine = false;
+    if (pr < npairs) {
+      r = pr / Hkv;
+      h = pr - r * Hkv;
+      const int b = __ldg(a.append_block + r);
+      if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
+        pos = __ldg(a.append_pos + r);
+        if (pos >= 0 && pos < P.len[b]) {
+          const int64_t u = static_cast<int64_t>(h) * P.UH + P.ubase[b] + pos / kT;
+          mine = u >= u0 && u < u1;
+          row = P.start[b] + pos;
+        }
+      }
+    }
+    unsigned m = __ballot_sync(0xffffffffu, mine);
+    while (m) {
+      const int src = __ffs(m) - 1;
+      m &= m - 1;
+      const int rr = __shfl_sync(0xffffffffu, r, src), hh = __shfl_sync(0xffffffffu, h, src);
+      const int pp = __shfl_sync(0xffffffffu, pos, src), ro = __shfl_sync(0xffffffffu, row, src);
+      const int64_t s_off = (static_cast<int64_t>(rr) * Hkv + hh) * 128;
+      const int64_t d_off = (static_cast<int64_t>(hh) * a.capacity + ro) * 128;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int i = lane + 32 * half;  // pair (i, i + 64)
+        const float x0 = __bfloat162float(kn[s_off + i]), x1 = __bfloat162float(kn[s_off + i + 64]);
+        float cs, sn;
+        rope_cos_sin(pp, a.phase[i], &cs, &sn);
+        kc[d_off + i] = __float2bfloat16_rn(__fmaf_rn(x0, cs, -__fmul_rn(x1, sn)));
+        kc[d_off + i + 64] = __float2bfloat16_rn(__fmaf_rn(x1, cs, __fmul_rn(x0, sn)));
+        vc[d_off + i] = vn[s_off + i];
+        vc[d_off + i + 64] = vn[s_off + i + 64];
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  NamedSync<2, 64>()();
+  if (tq == 0) mbar_arrive(&S.app_bar);
 }
 
 // Rotated queries of segments 1, 2, ... (segment 0 came from the prologue),
@@ -814,6 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 4; ++b) mbar_init(&S.rec_ready[b], 4);  // one per softmax warp
     mbar_init(&S.mma_done, 1);
     mbar_init(&S.plan_bar, 1);
+    mbar_init(&S.app_bar, 1);
     S.abort_flag = 0;
     S.tiles_done = 0;
     S.plan_ok = 1;
@@ -821,6 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!kPlanned) {
       for (int k = 0; k < kPreItems; ++k) S.cp.mpre_n[k] = -1;
       S.cp.n_first = 0;
+      S.cp.app_n = 0;
     }
     fence_mbar_init();
   }
@@ -874,12 +945,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ok && tid == 0 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_PLAN);
   const int64_t u0 = ok ? S.cp.u0 : 0, u1 = ok ? S.cp.u1 : 0;
   if (u0 < u1) {
+    const bool appending = kPlanned && a.k_new != nullptr && S.cp.app_n > 0;
     if (warp == kWarpTma) {
-      if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1);
+      if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1, appending);
     } else if (warp == kWarpMma) {
       if (lane == 0) mma_issuer(a, S, tmem, u0, u1);
     } else {
-      query_prologue<kPlanned>(a, S, u0, u1);
+      if (appending && warp >= kWarpQ)
+        append_tokens(a, S, u0, u1);
+      else
+        query_prologue<kPlanned>(a, S, u0, u1, appending ? 128 : 192);
       if (warp < kWarpQ)
         softmax_role(a, S, tmem, u0, u1);
       else
@@ -937,6 +1012,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       o.block_len[i] = a.block_len[i];
     }
     for (int i = tid; i < a.n_q_heads; i += nt) o.q_to_kv[i] = a.q_to_kv ? a.q_to_kv[i] : i / G;
+    for (int i = tid; i < a.n_rows; i += nt) {
+      o.append_block[i] = a.append_block ? a.append_block[i] : -1;
+      o.append_pos[i] = a.append_block ? a.append_pos[i] : 0;
+    }
   }
   if (!o.plan) return;
   PlanCore &P = S.ps.plan;
@@ -948,6 +1027,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       S.cp.us[k] = u;
       if (u < S.cp.u1) u = next_segment(P, a.n_blocks, u);
     }
+    S.cp.app_n = 0;
+    S.cp.app_tile = INT_MAX;
     const int64_t nf = min(static_cast<int64_t>(kStages), S.cp.u1 - S.cp.u0);
     S.cp.n_first = static_cast<uint8_t>(nf > 0 ? nf : 0);
     for (int i = 0; i < kStages; ++i) {
@@ -959,6 +1040,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  if (a.append_block) {
+    // the step's new tokens that lie in this CTA's tiles: how many, and the
+    // first such tile (a token outside its block is an error and skipped)
+    const int Hkv = a.n_kv_heads;
+    for (int pr = tid; pr < a.n_rows * Hkv; pr += nt) {
+      const int r = pr / Hkv, h = pr - r * Hkv;
+      const int b = a.append_block[r];
+      if (b < 0) continue;
+      const int pos = a.append_pos[r];
+      if (b >= a.n_blocks || pos < 0 || pos >= P.len[b]) {
+        if (blockIdx.x == 0 && h == 0) flag_error(a.err, HW_DEV_BAD_RANGE);
+        continue;
+      }
+      if (P.tiles[b] == 0) continue;  // a block no view reads takes no part
+      const int64_t u = static_cast<int64_t>(h) * P.UH + P.ubase[b] + pos / kT;
+      if (u >= S.cp.u0 && u < S.cp.u1) {
+        atomicAdd(&S.cp.app_n, 1);
+        atomicMin(&S.cp.app_tile, static_cast<int>(u - S.cp.u0));
+      }
+    }
+    __syncthreads();
+  }
   if (warp < kPre && S.cp.us[warp] < S.cp.u1) {
     const UnitPos x = unit_pos(P, a.n_blocks, S.cp.us[warp]);
     seg_pre(a, S.ps.cache, S.cp.pre[warp], x.b, x.h, lane);

@@ -38,6 +38,11 @@ struct DecodeArgs {
   int32_t n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
   int64_t capacity;
   const uint8_t *plan;  // precomputed plan of the tensor-core kernel (hw_attn_plan), or null
+  // The step's appends: at plan time the caller's arrays (null: none); at
+  // decode time the plan's copies.  k_new / v_new: this layer's new tokens,
+  // [n_rows][Hkv][D], or null (nothing is written; k and v are then only read).
+  const int32_t *append_block, *append_pos;
+  const void *k_new, *v_new;
   float scale_log2;   // softmax scale * log2(e): scores live in the log2 domain
   // RoPE phase increments: for pair i, the fraction of a turn per position,
   // frac(w_i / 2pi), as an unsigned 0.64 fixed-point number.  The angle of
@@ -69,6 +74,7 @@ size_t decode_tc_smem_bytes();
 struct PlanOut {
   uint8_t *plan;  // null: copy the metadata only
   int32_t *view_block, *view_offset, *q_pos, *q_to_kv, *block_start, *block_len;
+  int32_t *append_block, *append_pos;  // -1 / 0 for every row without an append
 };
 cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s);
 int decode_simt_ctas_per_sm(int dtype, int head_dim);

@@ -63,6 +63,33 @@ class DecodeSession:
                       m["view_offset"], m["q_pos"], self.workspace, self.ws_bytes,
                       q_to_kv=m["q_to_kv"], stream=stream)
 
+    def plan_append(self, append_block, append_pos, stream=None):
+        """hw_attn_plan_append: plan the step with each row's new token
+        (append_block[r] = its block or -1, append_pos[r] = its block-local
+        position; block_len of the uploaded metadata must count it)."""
+        m = self.meta
+        def dev(x):
+            t = torch.as_tensor(np.ascontiguousarray(x, dtype=np.int32)) if not torch.is_tensor(x) else x
+            return t.to(self.device, dtype=torch.int32).contiguous()
+        self.append = (dev(append_block), dev(append_pos))
+        api.attn_plan_append(self.desc, m["block_start"], m["block_len"], m["view_block"],
+                             m["view_offset"], m["q_pos"], self.append[0], self.append[1],
+                             self.workspace, self.ws_bytes, q_to_kv=m["q_to_kv"], stream=stream)
+
+    def append_decode_planned(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                              k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                              want_lse: bool = True, stream=None):
+        """One layer: its new tokens ([rows][Hkv][D]) written, then decoded."""
+        d = self.desc
+        if out is None:
+            out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
+        if lse is None and want_lse:
+            lse = torch.empty((d.n_rows, d.n_q_heads), dtype=torch.float32, device=self.device)
+        api.attn_append_decode_planned(d, q, k_new, v_new, k_cache, v_cache, out, lse,
+                                       self.workspace, self.ws_bytes, stream=stream)
+        return out, lse
+
     def decode_planned(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                        want_lse: bool = True, stream=None):

@@ -171,6 +171,43 @@ int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_c
                            size_t workspace_bytes, void *stream);
 
 /*
+ * The step's new tokens written and the layer decoded in one launch.  Every
+ * layer of a decode step first appends each worker's new token to its own
+ * block - the key stored rotated at its block-local position, like every
+ * key of the cache (the Hogwild! notes: keys are kept at positions
+ * 0..len-1 of their block) - then attends.
+ *
+ * hw_attn_plan_append is hw_attn_plan with the step's appends:
+ *  append_block  dev  int32 [n_rows], the block row r appends to, -1 = none
+ *  append_pos    dev  int32 [n_rows], the block-local position of its token;
+ *                     the plan's block_len must already count it:
+ *                     0 <= append_pos[r] < block_len[append_block[r]]
+ * (copied into the plan like the rest of the metadata; a row whose append
+ * falls outside its block sets HW_DEV_BAD_RANGE and is not appended).
+ * hw_attn_append_decode_planned then, for every row r with an append and
+ * every kv head h,
+ *   K[h][block_start[b] + p] = rho(k_new[r][h], p)     (b, p = append_block[r], append_pos[r])
+ *   V[h][block_start[b] + p] = v_new[r][h]
+ * with k_new, v_new dev [n_rows][Hkv][D] in the cache dtype, the key rotated
+ * in fp32 and rounded once to the dtype (nearest, ties to even), and then
+ * decodes as hw_attn_decode_planned does, the new tokens included.  Each
+ * token is written by the CTA that streams the tile holding it, before that
+ * tile is loaded.  A plan from hw_attn_plan has no appends (nothing is
+ * written); hw_attn_decode_planned on a plan with appends writes nothing
+ * either.  bf16 with head_dim 128 only (HW_ERR_UNSUPPORTED otherwise).
+ */
+int hw_attn_plan_append(const hw_attn_desc *d, const int32_t *block_start,
+                        const int32_t *block_len, const int32_t *view_block,
+                        const int32_t *view_offset, const int32_t *q_pos, const int32_t *q_to_kv,
+                        const int32_t *append_block, const int32_t *append_pos, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const void *k_new,
+                                  const void *v_new, void *k_cache, void *v_cache, void *out,
+                                  float *lse, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
  * Size of the fixed scratch array hw_attn_decode_noalloc uses (32 MiB): it
  * covers descriptions whose hw_attn_decode_workspace_size is at most this,
  * e.g. up to about 1300 (block, kv head) pairs with head_dim 128.

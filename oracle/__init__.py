@@ -171,6 +171,37 @@ class Oracle:
         return (kd, vd, exact) if want_exact else (kd, vd)
 
 
+    def append_tokens(self, *, dtype: int, rope_theta: float, k_cache, v_cache, k_new, v_new,
+                      block_start, append_block, append_pos, want_exact: bool = False):
+        """Each row's new token into its block, the step before every layer's
+        attention: the key is stored like every key of the cache, rotated at
+        its block-local position p (keys sit at 0..len-1 of their block), the
+        value as it is.  For row r with b = append_block[r] >= 0 and
+        p = append_pos[r], every kv head h:
+            K[h][block_start[b] + p] = rho(k_new[r][h], p),  V[...] = v_new[r][h]
+        which is the block commit of a one-token source by delta = p.
+        k_new, v_new: [rows][Hkv][D] storage values; caches [Hkv][cap][D].
+        Returns (k, v[, exact keys {row: [Hkv][D] float64}]) on copies.
+        """
+        sd = np.float32 if dtype == F32 else np.uint16
+        kd = np.array(k_cache, dtype=sd, copy=True, order="C")
+        vd = np.array(v_cache, dtype=sd, copy=True, order="C")
+        exact = {}
+        for r in range(len(append_block)):
+            b = int(append_block[r])
+            if b < 0:
+                continue
+            p = int(append_pos[r])
+            ks = np.ascontiguousarray(np.asarray(k_new[r], dtype=sd)[:, None, :])
+            vs = np.ascontiguousarray(np.asarray(v_new[r], dtype=sd)[:, None, :])
+            kd, vd, ex = self.block_commit(dtype=dtype, rope_theta=rope_theta, k_src=ks, v_src=vs,
+                                           src_begin=0, n_tokens=1, k_dst=kd, v_dst=vd,
+                                           dst_offset=int(block_start[b]) + p, pos_delta=p,
+                                           want_exact=True)
+            exact[r] = ex[:, 0, :]
+        return (kd, vd, exact) if want_exact else (kd, vd)
+
+
 _default: Optional[Oracle] = None
 
 
