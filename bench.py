@@ -40,6 +40,9 @@ def parse():
     p.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph")
     p.add_argument("--layout", default="combined", choices=["combined", "interleaved", "contiguous"],
                    help="views of the cache layout (the combined layout is the method's own)")
+    p.add_argument("--append", action="store_true",
+                   help="each layer first writes every worker's new token (the last position of "
+                        "its block) and then decodes, in one hw_attn_append_decode_planned launch")
     p.add_argument("--commit-all", action="store_true",
                    help="C4: every worker's finished block joins the history each step, all in "
                         "one hw_block_commit_many launch (the common block gets room for them)")
@@ -251,13 +254,38 @@ def main():
 
     planned = not args.unplanned
 
+    append = args.append and planned and kernel == "decode_tc_kernel"
+    if append:
+        # every worker's new token at the last position of its own block (the
+        # block lengths count it); the same rows are rewritten every step
+        ab = np.full(w.n_rows, -1, np.int32)
+        ap = np.zeros(w.n_rows, np.int32)
+        for r in range(w.n_rows):
+            pb, wk = divmod(r, w.n_workers)
+            b = pb * (w.n_workers + 1) + 1 + wk
+            if lens[b] > 0:
+                ab[r], ap[r] = b, lens[b] - 1
+        ab = torch.from_numpy(ab).to(dev)  # uploaded once (the graph replays the plan)
+        ap = torch.from_numpy(ap).to(dev)
+        gn = torch.Generator(device=dev)
+        gn.manual_seed(4321)
+        new_k = [torch.randn((w.n_rows, w.n_kv_heads, w.head_dim), generator=gn, device=dev).to(tdt)
+                 for _ in range(L)]
+        new_v = [torch.randn((w.n_rows, w.n_kv_heads, w.head_dim), generator=gn, device=dev).to(tdt)
+                 for _ in range(L)]
+
     def layer_calls(qsrc, osrc=outs, lsrc=lses):
         # a decode step: the views are planned once, then every layer runs
-        if planned:
+        if planned and append:
+            sess.plan_append(ab, ap, stream=stream)
+        elif planned:
             sess.plan(stream=stream)
         for i in range(calls_per_step):
             l = i % L
-            if planned:
+            if append:
+                sess.append_decode_planned(qsrc[l], new_k[l], new_v[l], ks[l], vs[l], out=osrc[l],
+                                           lse=lsrc[l], stream=stream)
+            elif planned:
                 sess.decode_planned(qsrc[l], ks[l], vs[l], out=osrc[l], lse=lsrc[l], stream=stream)
             else:
                 sess.decode(qsrc[l], ks[l], vs[l], out=osrc[l], lse=lsrc[l], stream=stream)
@@ -419,7 +447,9 @@ def main():
             "kv_bytes_per_step": step_bytes, "commit_bytes_per_step": commit_bytes,
             "parallelism": f"replicas x{world}", "layout": args.layout,
             "mode": "eager" if graph is None else "cuda-graph",
-            "calls": ("hw_attn_plan once per step + hw_attn_decode_planned per layer" if planned
+            "calls": ("hw_attn_plan_append once per step + hw_attn_append_decode_planned per layer "
+                      "(each worker's new token written, then decoded)" if append else
+                      "hw_attn_plan once per step + hw_attn_decode_planned per layer" if planned
                       else "hw_attn_decode per layer"),
             "l2": "inputs larger than L2: each step reads every layer's own KV pools "
                   f"({step_bytes / 1e9:.2f} GB per step vs 0.13 GB of L2)",

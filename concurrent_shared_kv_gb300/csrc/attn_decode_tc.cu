@@ -61,6 +61,7 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
 constexpr int kPre = 4;  // slots of query-side segment metadata
 constexpr int kPreList = 64;  // records of a merge list built ahead of the merge
 constexpr int kPreItems = 2;  // merge items of a CTA whose lists a plan builds
+constexpr int kAppList = 8;   // new tokens of a CTA a plan lists (more: found by a scan)
 // Named barriers: 1 softmax warps, 2 query warps, 3 prologue warps.
 
 // Query-side metadata of a segment: its view references and q heads, and per
@@ -85,6 +86,8 @@ struct alignas(16) CtaPlan {
   uint8_t n_first;         // how many (min(kStages, u1 - u0)); 0 without a plan
   int32_t app_n;           // new tokens this CTA writes (hw_attn_plan_append), 0: none
   int32_t app_tile;        // its first tile (from u0) that holds one of them
+  // the first kAppList of them: (row * Hkv + kv head), cache row, block-local position
+  int32_t app_pair[kAppList], app_row[kAppList], app_pos[kAppList];
 };
 
 struct TcSmem {
@@ -479,42 +482,51 @@ __device__ void append_tokens(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_
   const __nv_bfloat16 *vn = static_cast<const __nv_bfloat16 *>(a.v_new);
   __nv_bfloat16 *kc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.k));
   __nv_bfloat16 *vc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.v));
-  for (int base = wq * 32; base < npairs; base += 64) {
-    // lane: one (row, kv head) pair; the warp then writes the ones it owns
-    const int pr = base + lane;
-    int r = 0, h = 0, pos = 0, row = 0;
-    bool mine = false;
-    if (pr < npairs) {
-      r = pr / Hkv;
-      h = pr - r * Hkv;
-      const int b = __ldg(a.append_block + r);
-      if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
-        pos = __ldg(a.append_pos + r);
-        if (pos >= 0 && pos < P.len[b]) {
-          const int64_t u = static_cast<int64_t>(h) * P.UH + P.ubase[b] + pos / kT;
-          mine = u >= u0 && u < u1;
-          row = P.start[b] + pos;
+  // one (row, kv head) token by the whole warp: lane l the pairs (l, l + 64)
+  // and (l + 32, l + 96)
+  auto write_token = [&](int pr, int pos, int row) {
+    const int r = pr / Hkv, h = pr - r * Hkv;
+    const int64_t s_off = (static_cast<int64_t>(r) * Hkv + h) * 128;
+    const int64_t d_off = (static_cast<int64_t>(h) * a.capacity + row) * 128;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int i = lane + 32 * half;
+      const float x0 = __bfloat162float(kn[s_off + i]), x1 = __bfloat162float(kn[s_off + i + 64]);
+      float cs, sn;
+      rope_cos_sin(pos, a.phase[i], &cs, &sn);
+      kc[d_off + i] = __float2bfloat16_rn(__fmaf_rn(x0, cs, -__fmul_rn(x1, sn)));
+      kc[d_off + i + 64] = __float2bfloat16_rn(__fmaf_rn(x1, cs, __fmul_rn(x0, sn)));
+      vc[d_off + i] = vn[s_off + i];
+      vc[d_off + i + 64] = vn[s_off + i + 64];
+    }
+  };
+  if (S.cp.app_n <= kAppList) {
+    // the plan lists them
+    for (int e = wq; e < S.cp.app_n; e += 2) write_token(S.cp.app_pair[e], S.cp.app_pos[e], S.cp.app_row[e]);
+  } else {
+    // more than the plan lists: every (row, kv head) pair is checked
+    for (int base = wq * 32; base < npairs; base += 64) {
+      const int pr = base + lane;
+      int pos = 0, row = 0;
+      bool mine = false;
+      if (pr < npairs) {
+        const int r = pr / Hkv, h = pr - r * Hkv;
+        const int b = __ldg(a.append_block + r);
+        if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
+          pos = __ldg(a.append_pos + r);
+          if (pos >= 0 && pos < P.len[b]) {
+            const int64_t u = static_cast<int64_t>(h) * P.UH + P.ubase[b] + pos / kT;
+            mine = u >= u0 && u < u1;
+            row = P.start[b] + pos;
+          }
         }
       }
-    }
-    unsigned m = __ballot_sync(0xffffffffu, mine);
-    while (m) {
-      const int src = __ffs(m) - 1;
-      m &= m - 1;
-      const int rr = __shfl_sync(0xffffffffu, r, src), hh = __shfl_sync(0xffffffffu, h, src);
-      const int pp = __shfl_sync(0xffffffffu, pos, src), ro = __shfl_sync(0xffffffffu, row, src);
-      const int64_t s_off = (static_cast<int64_t>(rr) * Hkv + hh) * 128;
-      const int64_t d_off = (static_cast<int64_t>(hh) * a.capacity + ro) * 128;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int i = lane + 32 * half;  // pair (i, i + 64)
-        const float x0 = __bfloat162float(kn[s_off + i]), x1 = __bfloat162float(kn[s_off + i + 64]);
-        float cs, sn;
-        rope_cos_sin(pp, a.phase[i], &cs, &sn);
-        kc[d_off + i] = __float2bfloat16_rn(__fmaf_rn(x0, cs, -__fmul_rn(x1, sn)));
-        kc[d_off + i + 64] = __float2bfloat16_rn(__fmaf_rn(x1, cs, __fmul_rn(x0, sn)));
-        vc[d_off + i] = vn[s_off + i];
-        vc[d_off + i + 64] = vn[s_off + i + 64];
+      unsigned m = __ballot_sync(0xffffffffu, mine);
+      while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        write_token(__shfl_sync(0xffffffffu, pr, src), __shfl_sync(0xffffffffu, pos, src),
+                    __shfl_sync(0xffffffffu, row, src));
       }
     }
   }
@@ -914,6 +926,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : "memory");
     }
   }
+  if (kPlanned && tid == 64 && a.k_new) {
+    // likewise the layer's new tokens (k_new, v_new: [n_rows][Hkv][128] bf16),
+    // which the CTAs that write them read early, under the first tiles
+    const uint64_t total = static_cast<uint64_t>(a.n_rows) * a.n_kv_heads * 256;
+    const uint64_t per = ((total + gridDim.x - 1) / gridDim.x + 255) & ~static_cast<uint64_t>(255);
+    const uint64_t off = per * blockIdx.x;
+    if (off < total) {
+      const uint32_t n = static_cast<uint32_t>(total - off < per ? total - off : per);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       reinterpret_cast<const uint8_t *>(a.k_new) + off), "r"(n)
+                   : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       reinterpret_cast<const uint8_t *>(a.v_new) + off), "r"(n)
+                   : "memory");
+    }
+  }
 
   if (tid == 0) {
     if (kPlanned) {
@@ -1056,8 +1084,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (P.tiles[b] == 0) continue;  // a block no view reads takes no part
       const int64_t u = static_cast<int64_t>(h) * P.UH + P.ubase[b] + pos / kT;
       if (u >= S.cp.u0 && u < S.cp.u1) {
-        atomicAdd(&S.cp.app_n, 1);
+        const int k = atomicAdd(&S.cp.app_n, 1);
         atomicMin(&S.cp.app_tile, static_cast<int>(u - S.cp.u0));
+        if (k < kAppList) {
+          S.cp.app_pair[k] = pr;
+          S.cp.app_row[k] = P.start[b] + pos;
+          S.cp.app_pos[k] = pos;
+        }
       }
     }
     __syncthreads();
@@ -1100,6 +1133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory of one CTA per SM");
 size_t decode_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 size_t plan_shared_bytes() { return sizeof(PlanShared); }
 size_t plan_cta_bytes() { return sizeof(CtaPlan); }

@@ -117,3 +117,25 @@ def test_append_position_outside_its_block_is_reported_and_skipped():
     assert np.array_equal(kg[:, bad_row], k0[:, bad_row])  # not written
     good_row = c.block_start[ab[0]] + ap[0]
     assert not np.array_equal(kg[:, good_row], k0[:, good_row])  # the others were
+
+
+def test_append_decode_serving_ragged_uses_the_scan_beyond_the_plan_list():
+    # 16 problems x 4 workers: CTAs that cross many short worker blocks own
+    # more new tokens than the plan lists and find the rest by scanning
+    w = wl.serve_ragged()
+    c = H.device_case(w)
+    ab, ap = last_position_appends(c)
+    kn, vn = new_tokens(w, 8)
+    check_append_decode(c, ab, ap, kn, vn, "append serving ragged", rows=list(range(0, 4)) + list(range(60, 64)))
+
+
+def test_append_decode_beyond_the_plan_list():
+    # a long common block makes each CTA's share of the split large, so the
+    # CTAs that cross the 30 one-to-three-token worker blocks own up to 11 new
+    # tokens (host replica of the split: four CTAs above the plan's list of 8)
+    w = wl.Workload("scan", "bf16", 1, 30, 2, 2, 128, 1e6, 1, [400000],
+                    [[1 + (i % 3) for i in range(30)]], seed=21)
+    c = H.device_case(w)
+    ab, ap = last_position_appends(c)
+    kn, vn = new_tokens(w, 9)
+    check_append_decode(c, ab, ap, kn, vn, "append beyond the list", rows=[0, 13, 29])
