@@ -428,7 +428,7 @@ __device__ __forceinline__ int64_t next_segment(const PlanCore &P, int n_blocks,
   return x.seg_first + x.tiles;
 }
 
-// Prologue of warps 2-7, or of warps 2-5 alone (nt = 128) while warps 6-7
+// Prologue of warps 2-7 (nt = 192), or of warps 2-5 alone (nt = 128) while warps 6-7
 // write the CTA's new tokens: the metadata of segment 0 (warp 2), then its
 // queries rotated into the Q~ buffer.
 template <bool kPlanned>
@@ -436,7 +436,12 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
   const int t = threadIdx.x - kWarpSoft * 32;  // 0 .. nt-1
   const int w = t >> 5, lane = t & 31;
   const int G = a.n_q_heads / a.n_kv_heads;
-  auto sync = [nt]() { asm volatile("bar.sync 3, %0;" ::"r"(nt) : "memory"); };
+  auto sync = [nt]() {
+    if (nt == 192)
+      asm volatile("bar.sync 3, 192;" ::: "memory");
+    else
+      asm volatile("bar.sync 3, 128;" ::: "memory");
+  };
   if (w == 0 && !kPlanned) {  // a plan brings it ready-made
     const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u0);
     seg_pre(a, S.ps.cache, S.cp.pre[0], x.b, x.h, lane);
@@ -857,7 +862,10 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   if (pend >= 0) segment_records(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync);
 }
 
-template <bool kPlanned>
+// kPlanned: the step's plan is loaded (else built in-kernel); kAppend (with a
+// plan): the layer's new tokens are written first.  Each combination is its
+// own kernel, so that no path carries another's code.
+template <bool kPlanned, bool kAppend>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
@@ -926,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : "memory");
     }
   }
-  if (kPlanned && tid == 64 && a.k_new) {
+  if (kAppend && tid == 64) {
     // likewise the layer's new tokens (k_new, v_new: [n_rows][Hkv][128] bf16),
     // which the CTAs that write them read early, under the first tiles
     const uint64_t total = static_cast<uint64_t>(a.n_rows) * a.n_kv_heads * 256;
@@ -973,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ok && tid == 0 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_PLAN);
   const int64_t u0 = ok ? S.cp.u0 : 0, u1 = ok ? S.cp.u1 : 0;
   if (u0 < u1) {
-    const bool appending = kPlanned && a.k_new != nullptr && S.cp.app_n > 0;
+    const bool appending = kAppend && S.cp.app_n > 0;
     if (warp == kWarpTma) {
       if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1, appending);
     } else if (warp == kWarpMma) {
@@ -1154,16 +1162,18 @@ cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStr
 cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                              int ctas, cudaStream_t s) {
   const size_t smem = decode_tc_smem_bytes();
-  // a planned launch runs its own instantiation: without the plan-building
-  // code the kernel is far smaller, which matters for instruction fetch
+  // planned launches run their own instantiations: without the plan-building
+  // (and, without appends, the append) code the kernel is far smaller
+  const int which = !a.plan ? 0 : !a.k_new ? 1 : 2;
   void (*kernel)(DecodeArgs, CUtensorMap, CUtensorMap) =
-      a.plan ? decode_tc_kernel<true> : decode_tc_kernel<false>;
-  static bool configured[2] = {false, false};
-  if (!configured[a.plan ? 1 : 0]) {
+      which == 0 ? decode_tc_kernel<false, false>
+                 : which == 1 ? decode_tc_kernel<true, false> : decode_tc_kernel<true, true>;
+  static bool configured[3] = {false, false, false};
+  if (!configured[which]) {
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    configured[a.plan ? 1 : 0] = true;
+    configured[which] = true;
   }
   // cooperative: the merge phase waits on other CTAs, so all must be
   // resident; a programmatic dependent of the previous kernel (see the
