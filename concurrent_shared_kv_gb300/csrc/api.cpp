@@ -100,7 +100,7 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
   const size_t counters = static_cast<size_t>(d.n_rows) * d.n_q_heads * sizeof(int32_t);
   L.partials_off = L.counters_off + up(counters);
   L.slots = static_cast<int64_t>(d.n_blocks) * d.n_kv_heads + max_ctas;
-  const size_t rec = static_cast<size_t>(kMaxQ) * (d.head_dim + 4) * sizeof(float);
+  const size_t rec = static_cast<size_t>(kMaxQ) * (d.head_dim + kRecPad) * sizeof(float);
   L.meta_off = L.partials_off + up(static_cast<size_t>(L.slots) * rec);
   // metadata copies: view_block, view_offset (rows x V), q_pos, q_to_kv, block_start, block_len,
   // append_block, append_pos

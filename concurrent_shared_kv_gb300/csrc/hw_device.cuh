@@ -482,7 +482,7 @@ __device__ __forceinline__ void gather_qheads(const DecodeArgs &a, const MetaCac
 }
 
 __device__ __forceinline__ float *record_ptr(const DecodeArgs &a, int64_t slot, int qi) {
-  return a.partials + (slot * kMaxQ + qi) * static_cast<int64_t>(a.head_dim + 4);
+  return a.partials + (slot * kMaxQ + qi) * static_cast<int64_t>(a.head_dim + kRecPad);
 }
 
 // ---------------------------------------------------------------------------
@@ -607,7 +607,7 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
                             int n_pre, int pre_stride, int tid, int nt, Sync sync,
                             long long wait_limit) {
   constexpr int EPL = D / 32;
-  constexpr int64_t RS = D + 4;  // record stride in floats
+  constexpr int64_t RS = D + kRecPad;  // record stride in floats
   constexpr int B = kMergeBatch;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
   const int items = a.n_rows * a.n_q_heads;

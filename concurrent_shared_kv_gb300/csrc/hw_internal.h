@@ -20,6 +20,10 @@ constexpr int kMaxQ = HW_MAX_QHEADS_PER_BLOCK;
 constexpr int kMaxRecords = 1024;
 
 // Everything a decode kernel needs; passed by value as a kernel parameter.
+// A partial record is o[0..D), m, l and padding to whole 128-byte lines: a
+// record's stores and loads then touch D / 32 + 1 lines, not one more.
+constexpr int kRecPad = 32;
+
 struct DecodeArgs {
   const void *q;
   const void *k;
@@ -34,7 +38,7 @@ struct DecodeArgs {
   float *lse;
   int32_t *err;       // workspace error word (HW_DEV_* bits)
   int32_t *counters;  // [n_rows][Hq] merge arrival counters, zero between calls
-  float *partials;    // [slots][kMaxQ][D + 4]: o[0..D), m at D, l at D+1
+  float *partials;    // [slots][kMaxQ][D + kRecPad]: o[0..D), m at D, l at D+1
   int32_t n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
   int64_t capacity;
   const uint8_t *plan;  // precomputed plan of the tensor-core kernel (hw_attn_plan), or null

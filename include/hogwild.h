@@ -210,7 +210,7 @@ int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const vo
 /*
  * Size of the fixed scratch array hw_attn_decode_noalloc uses (32 MiB): it
  * covers descriptions whose hw_attn_decode_workspace_size is at most this,
- * e.g. up to about 1300 (block, kv head) pairs with head_dim 128.
+ * e.g. up to about 1450 (block, kv head) pairs with head_dim 128.
  */
 #define HW_NOALLOC_SCRATCH_BYTES (32u << 20)
 
