@@ -26,7 +26,7 @@ DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMA
 # every symbol the header declares
 EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode",
            "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_plan_append",
-           "hw_attn_append_decode_planned", "hw_attn_decode_noalloc",
+           "hw_attn_append_decode_planned", "hw_plan_export", "hw_attn_decode_noalloc",
            "hw_block_commit", "hw_block_commit_many", "hw_workspace_status", "hw_views_combined",
            "hw_views", "hw_last_cuda_error", "hw_status_string"]
 HW_LAYOUT_COMBINED, HW_LAYOUT_INTERLEAVED, HW_LAYOUT_CONTIGUOUS = 0, 1, 2
@@ -77,6 +77,8 @@ def lib(path: Optional[str] = None):
     L.hw_attn_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 6 + [ctypes.c_size_t, _P]
     L.hw_attn_plan_append.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]
     L.hw_attn_append_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]
+    L.hw_plan_export.argtypes = [ctypes.POINTER(AttnDesc), _P, ctypes.c_size_t, _P, ctypes.c_int32,
+                                 ctypes.POINTER(ctypes.c_int32), _P]
     L.hw_attn_decode_noalloc.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12
     L.hw_block_commit.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
@@ -200,6 +202,17 @@ def attn_append_decode_planned(desc: AttnDesc, q, k_new, v_new, k_cache, v_cache
                                              _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check("hw_attn_append_decode_planned", st)
     return st
+
+
+def plan_export(desc: AttnDesc, workspace, workspace_bytes: int, max_ctas: int = 1024, stream=None):
+    """hw_plan_export: the plan's per-CTA work split as an int64 array [ctas][12]
+    (u0, u1, n_first, first rows x3, kv heads x3, segment flags x3)."""
+    out = np.zeros((max_ctas, 12), np.int64)
+    n = ctypes.c_int32(0)
+    st = lib().hw_plan_export(ctypes.byref(desc), _ptr(workspace), int(workspace_bytes),
+                              out.ctypes.data, int(max_ctas), ctypes.byref(n), _stream(stream))
+    _check("hw_plan_export", st)
+    return out[:n.value]
 
 
 def attn_decode_noalloc(desc: AttnDesc, q, k_cache, v_cache, block_start, block_len, view_block,

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <vector>
 #include <mutex>
 
 #include "hogwild.h"
@@ -372,6 +373,31 @@ int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_c
   return decode_common(d, q, k_cache, v_cache, m.block_start, m.block_len, m.view_block,
                        m.view_offset, m.q_pos, m.q_to_kv, plan, out, lse, workspace, L, max_ctas,
                        stream);
+}
+
+int hw_plan_export(const hw_attn_desc *d, const void *workspace, size_t workspace_bytes,
+                   int64_t *out, int32_t max_ctas, int32_t *n_ctas, void *stream) {
+  int st = check_desc(d);
+  if (st != HW_OK) return st;
+  if (!out || !n_ctas || max_ctas <= 0) return HW_ERR_INVALID;
+  if (!tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
+  WorkspaceLayout L;
+  int max_grid = 0;
+  st = check_workspace(d, const_cast<void *>(workspace), workspace_bytes, &L, &max_grid);
+  if (st != HW_OK) return st;
+  const size_t bytes = kPlanHeaderBytes + plan_shared_bytes() +
+                       static_cast<size_t>(device_sm_count()) * plan_cta_bytes();
+  std::vector<uint8_t> host(bytes);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(host.data(), static_cast<const uint8_t *>(workspace) + L.plan_off, bytes,
+                   cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int grid = plan_export_records(host.data(), out, max_ctas);
+  if (grid < 0) return HW_ERR_INVALID;
+  *n_ctas = grid;
+  return HW_OK;
 }
 
 int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const void *k_new,

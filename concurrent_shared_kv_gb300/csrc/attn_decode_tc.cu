@@ -1146,6 +1146,25 @@ size_t decode_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 size_t plan_shared_bytes() { return sizeof(PlanShared); }
 size_t plan_cta_bytes() { return sizeof(CtaPlan); }
 
+int plan_export_records(const uint8_t *plan_host, int64_t *out, int max_ctas) {
+  const PlanHeader &h = *reinterpret_cast<const PlanHeader *>(plan_host);
+  if (h.magic != kPlanMagic || h.grid <= 0 || h.grid > max_ctas) return -1;
+  for (int c = 0; c < h.grid; ++c) {
+    const CtaPlan &cp = *reinterpret_cast<const CtaPlan *>(
+        plan_host + kPlanHeaderBytes + sizeof(PlanShared) + static_cast<size_t>(c) * sizeof(CtaPlan));
+    int64_t *o = out + static_cast<int64_t>(c) * kPlanExportFields;
+    o[0] = cp.u0;
+    o[1] = cp.u1;
+    o[2] = cp.n_first;
+    for (int i = 0; i < kStages; ++i) {
+      o[3 + i] = cp.trow[i];
+      o[6 + i] = cp.th[i];
+      o[9 + i] = cp.tfl[i];
+    }
+  }
+  return h.grid;
+}
+
 cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s) {
   const size_t smem = sizeof(PlanSmem) + 16;
   static bool configured = false;

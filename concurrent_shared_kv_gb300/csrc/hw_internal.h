@@ -63,6 +63,11 @@ struct WorkspaceLayout {
 constexpr size_t kPlanHeaderBytes = 256;
 size_t plan_shared_bytes();  // the part of a plan every CTA reads
 size_t plan_cta_bytes();     // the part each CTA reads for itself
+// From a host copy of a plan region: kPlanExportFields int64 per CTA (unit
+// range, number of first tiles, their rows, kv heads and segment flags).
+// Returns the plan's grid, or -1 when there is no plan (or it exceeds max_ctas).
+constexpr int kPlanExportFields = 12;
+int plan_export_records(const uint8_t *plan_host, int64_t *out, int max_ctas);
 WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas);
 
 int device_sm_count();  // SMs of the current device, cached; <= 0 on failure

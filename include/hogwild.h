@@ -208,6 +208,19 @@ int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const vo
                                   void *stream);
 
 /*
+ * For tests: the work split of the plan in `workspace` (bf16 head_dim-128
+ * kernel; synchronises `stream`).  Per CTA c < *n_ctas, 12 int64 at
+ * out[12 c ..]: its unit range [u0, u1) (units: 128-token tiles of one
+ * (block, kv head), kv-head-major, then block, then tile), the number of
+ * first tiles the plan decodes (min(3, u1 - u0)), their first cache rows,
+ * kv heads and segment flags (1: starts its segment within the range, 2:
+ * ends it), 3 each.  out holds max_ctas records.  HW_ERR_INVALID when the
+ * workspace holds no plan.
+ */
+int hw_plan_export(const hw_attn_desc *d, const void *workspace, size_t workspace_bytes,
+                   int64_t *out, int32_t max_ctas, int32_t *n_ctas, void *stream);
+
+/*
  * Size of the fixed scratch array hw_attn_decode_noalloc uses (32 MiB): it
  * covers descriptions whose hw_attn_decode_workspace_size is at most this,
  * e.g. up to about 1450 (block, kv head) pairs with head_dim 128.
