@@ -82,6 +82,10 @@ class Oracle:
         L.hwref_attn_decode.argtypes = [ctypes.POINTER(HwrefDesc), _P, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P, ctypes.c_int32, ctypes.c_int, _P, _P, ctypes.c_int]
         L.hwref_attn_decode.restype = ctypes.c_int
+        L.hwref_attn_decode_limited.argtypes = [ctypes.POINTER(HwrefDesc), _P, _P, _P, _P, _P, _P, _P,
+                                                _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int, _P, _P,
+                                                ctypes.c_int]
+        L.hwref_attn_decode_limited.restype = ctypes.c_int
         L.hwref_block_commit.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
                                          ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32,
@@ -109,8 +113,11 @@ class Oracle:
     def attn_decode(self, *, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
                     q_pos, n_kv_heads: int, rope_theta: float, scale: float, dtype: int,
                     q_to_kv=None, rows: Optional[Sequence[int]] = None, brute: bool = False,
-                    n_threads: Optional[int] = None):
+                    n_threads: Optional[int] = None, view_limit=None):
         """Returns (out [rows][Hq][D] float64, lse [rows][Hq] float64).
+
+        view_limit [rows][V] (optional): an entry with a limit >= 0 attends
+        only the first min(limit, len) tokens of its block.
 
         q, k_cache, v_cache hold storage values: float32 arrays for ``dtype=F32``,
         uint16 bf16 bit patterns for ``dtype=BF16``.  k_cache/v_cache are
@@ -135,11 +142,15 @@ class Oracle:
         out = np.full((n_rows, Hq, D), np.nan)
         lse = np.full((n_rows, Hq), np.nan)
         nt = n_threads or len(os.sched_getaffinity(0))
-        rc = self.lib.hwref_attn_decode(
+        vlim = None if view_limit is None else i32(view_limit)
+        if vlim is not None:
+            assert vlim.shape == view_block.shape
+        rc = self.lib.hwref_attn_decode_limited(
             ctypes.byref(desc), q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
             block_start.ctypes.data, block_len.ctypes.data, view_block.ctypes.data,
             view_offset.ctypes.data, q_pos.ctypes.data,
             None if qmap is None else qmap.ctypes.data,
+            None if vlim is None else vlim.ctypes.data,
             None if sel is None else sel.ctypes.data, 0 if sel is None else len(sel),
             1 if brute else 0, out.ctypes.data, lse.ctypes.data, int(nt))
         if rc != 0:

@@ -173,6 +173,7 @@ typedef struct {
   const hwref_desc *d;
   const void *q, *k, *v;
   const int32_t *block_start, *block_len, *view_block, *view_offset, *q_pos, *q_to_kv;
+  const int32_t *view_limit; /* [rows][V] or NULL: tokens of the entry's block the row sees */
   const int32_t *rows; /* rows to compute, n_items = n_sel * Hq */
   int32_t n_sel;
   int brute; /* 0: block form (the method), 1: brute-force re-encoding */
@@ -187,6 +188,15 @@ static int kv_head_of(const hwref_desc *d, const int32_t *q_to_kv, int h) {
   int group = d->n_q_heads / d->n_kv_heads;
   if (MUTANT(6)) return h % d->n_kv_heads; /* strided instead of grouped */
   return h / group;
+}
+
+/* Tokens of view entry (row, v) the row attends: the block's first
+ * min(limit, len) when the entry has a limit >= 0, else all len. */
+static int entry_len(const decode_job *J, int32_t row, int v, int len) {
+  if (!J->view_limit) return len;
+  const int32_t lim = J->view_limit[(int64_t)row * J->d->max_view_blocks + v];
+  if (MUTANT(9) && lim > 0 && lim < len) return lim - 1; /* the limit's own token left out */
+  return lim >= 0 && lim < len ? lim : len;
 }
 
 /* One (row, q-head) item.  Returns 0 or an error code. */
@@ -211,7 +221,7 @@ static int decode_item(decode_job *J, int32_t row, int32_t h, double *scratch_q,
     if (len < 0) return HWREF_EINVAL;
     if ((int64_t)J->block_start[b] + len > d->cache_capacity || J->block_start[b] < 0)
       return HWREF_EINVAL;
-    n_tok += len;
+    n_tok += entry_len(J, row, v, len);
   }
   double *s = (double *)malloc(sizeof(double) * (size_t)(n_tok > 0 ? n_tok : 1));
   if (!s) return HWREF_ENOMEM;
@@ -221,7 +231,7 @@ static int decode_item(decode_job *J, int32_t row, int32_t h, double *scratch_q,
   for (int v = 0; v < V; ++v) {
     int b = J->view_block[(int64_t)row * V + v];
     if (b < 0) continue;
-    int len = J->block_len[b];
+    int len = entry_len(J, row, v, J->block_len[b]);
     if (len == 0) continue;
     int32_t off = J->view_offset[(int64_t)row * V + v];
     if (!J->brute) {
@@ -264,7 +274,7 @@ static int decode_item(decode_job *J, int32_t row, int32_t h, double *scratch_q,
   for (int v = 0; v < V; ++v) {
     int b = J->view_block[(int64_t)row * V + v];
     if (b < 0) continue;
-    int len = J->block_len[b];
+    int len = entry_len(J, row, v, J->block_len[b]);
     for (int j = 0; j < len; ++j) {
       double p = exp(s[t++] - M);
       Z += p;
@@ -315,11 +325,15 @@ static int valid_desc(const hwref_desc *d) {
  * (rows == NULL: all rows, n_sel ignored).  Entries of unselected rows are not
  * touched.  brute = 0 computes the method (query rotated once per block);
  * brute = 1 re-encodes every key at its absolute view position instead.
+ * view_limit [rows][V] or NULL: an entry with a limit >= 0 attends only the
+ * first min(limit, len) tokens of its block (a chunk's causal order within
+ * its own block).
  */
-int hwref_attn_decode(const hwref_desc *d, const void *q, const void *k_cache, const void *v_cache,
+int hwref_attn_decode_limited(const hwref_desc *d, const void *q, const void *k_cache, const void *v_cache,
                       const int32_t *block_start, const int32_t *block_len,
                       const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
-                      const int32_t *q_to_kv, const int32_t *rows, int32_t n_sel, int brute,
+                      const int32_t *q_to_kv, const int32_t *view_limit, const int32_t *rows,
+                      int32_t n_sel, int brute,
                       double *out, double *lse, int n_threads) {
   if (!valid_desc(d) || !out || !lse) return HWREF_EINVAL;
   decode_job J;
@@ -334,6 +348,7 @@ int hwref_attn_decode(const hwref_desc *d, const void *q, const void *k_cache, c
   J.view_offset = view_offset;
   J.q_pos = q_pos;
   J.q_to_kv = q_to_kv;
+  J.view_limit = view_limit;
   J.rows = rows;
   J.n_sel = rows ? n_sel : d->n_rows;
   J.brute = brute;
@@ -350,6 +365,17 @@ int hwref_attn_decode(const hwref_desc *d, const void *q, const void *k_cache, c
   for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
   pthread_mutex_destroy(&J.mu);
   return J.status;
+}
+
+/* hwref_attn_decode_limited without limits: every entry sees its whole block. */
+int hwref_attn_decode(const hwref_desc *d, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_start, const int32_t *block_len,
+                      const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
+                      const int32_t *q_to_kv, const int32_t *rows, int32_t n_sel, int brute,
+                      double *out, double *lse, int n_threads) {
+  return hwref_attn_decode_limited(d, q, k_cache, v_cache, block_start, block_len, view_block,
+                                   view_offset, q_pos, q_to_kv, NULL, rows, n_sel, brute, out, lse,
+                                   n_threads);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -381,9 +381,53 @@ def pin_bf16_rounding(o: O.Oracle):
     assert np.array_equal(got, want)
 
 
+def pin_view_limits(o: O.Oracle):
+    """Per-entry limits (a chunk's causal order within its block): limits at or
+    past the block's length change nothing; a limit of 0 is the entry dropped;
+    T query rows of one worker over one block at offset 0, row t at position
+    P + t seeing the block's first P + t + 1 tokens, are textbook causal
+    attention (scipy), row by row."""
+    c = case_tiny()
+    base_out, base_lse = o.attn_decode(**c)
+    vb = c["view_block"]
+    none = np.full(vb.shape, -1, np.int32)
+    past = np.array([[c["block_len"][b] + 5 for b in row] for row in vb], np.int32)
+    for lim in (none, past):
+        out, lse = o.attn_decode(**c, view_limit=lim)
+        assert np.array_equal(out, base_out) and np.array_equal(lse, base_lse)
+    lim = none.copy()
+    lim[0, 1] = 0
+    out1, lse1 = o.attn_decode(**c, view_limit=lim)
+    dropped = dict(c)
+    dropped["view_block"] = vb.copy()
+    dropped["view_block"][0, 1] = -1
+    out2, lse2 = o.attn_decode(**dropped)
+    assert np.array_equal(out1[0], out2[0]) and np.array_equal(lse1[0], lse2[0])
+    assert not np.allclose(out1[0], base_out[0])  # the limit did hide tokens
+    rng = np.random.default_rng(13)
+    D, P, T, Hq, Hkv, theta = 16, 37, 3, 4, 2, 1e4
+    n = P + T
+    q = rng.standard_normal((T, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((Hkv, n, D)).astype(np.float32)
+    v = rng.standard_normal((Hkv, n, D)).astype(np.float32)
+    out, lse = o.attn_decode(q=q, k_cache=k, v_cache=v, block_start=[0], block_len=[n],
+                             view_block=[[0]] * T, view_offset=[[0]] * T,
+                             q_pos=[P + t for t in range(T)], n_kv_heads=Hkv, rope_theta=theta,
+                             scale=D ** -0.5, dtype=O.F32, view_limit=[[P + t + 1] for t in range(T)])
+    w = o.freqs(D, theta)
+    for t in range(T):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            qa = complex_rope(q[t, h].astype(np.float64), w, P + t)
+            s_ = (k[g, :P + t + 1].astype(np.float64) @ qa) * D ** -0.5
+            want = softmax(s_) @ v[g, :P + t + 1].astype(np.float64)
+            assert np.max(np.abs(out[t, h] - want)) < 1e-12, (t, h)
+            assert abs(lse[t, h] - logsumexp(s_)) < 1e-12, (t, h)
+
+
 ALL_PINS = [
     pin_rope_golden_freqs, pin_rope_complex, pin_rope_group, pin_textbook_single_block,
     pin_identity_block_vs_brute, pin_q_zero_mean, pin_permutation_invariance, pin_one_hot_exact,
     pin_gqa_mapping, pin_empty_view, pin_combined_layout, pin_commit_placement_and_copy,
-    pin_commit_rotation, pin_commit_single_worker_invariance, pin_bf16_rounding,
+    pin_commit_rotation, pin_commit_single_worker_invariance, pin_bf16_rounding, pin_view_limits,
 ]

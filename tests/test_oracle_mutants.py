@@ -14,6 +14,7 @@ MUTANTS = {
     6: "strided GQA head mapping",
     7: "commit places tokens in reverse order",
     8: "commit rotates by -delta",
+    9: "a limited entry leaves out its last visible token",
 }
 
 
