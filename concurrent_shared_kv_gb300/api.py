@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libhogwild.so")
 
 HW_OK = 0
 HW_F32, HW_BF16 = 0, 1
+HW_DESC_VIEW_LIMITS = 1
 STATUS = {0: "HW_OK", -1: "HW_ERR_INVALID", -2: "HW_ERR_UNSUPPORTED", -3: "HW_ERR_WORKSPACE",
           -4: "HW_ERR_CAPACITY", -5: "HW_ERR_OVERLAP", -6: "HW_ERR_CUDA", -7: "HW_ERR_DEVICE"}
 DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMAP",
@@ -25,10 +26,10 @@ DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMA
 
 # every symbol the header declares
 EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode",
-           "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_plan_append",
+           "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_plan_limited", "hw_attn_plan_append",
            "hw_attn_append_decode_planned", "hw_plan_export", "hw_attn_decode_noalloc",
            "hw_block_commit", "hw_block_commit_many", "hw_workspace_status", "hw_views_combined",
-           "hw_views", "hw_last_cuda_error", "hw_status_string"]
+           "hw_views", "hw_views_chunked", "hw_last_cuda_error", "hw_status_string"]
 HW_LAYOUT_COMBINED, HW_LAYOUT_INTERLEAVED, HW_LAYOUT_CONTIGUOUS = 0, 1, 2
 LAYOUTS = {"combined": HW_LAYOUT_COMBINED, "interleaved": HW_LAYOUT_INTERLEAVED,
            "contiguous": HW_LAYOUT_CONTIGUOUS}
@@ -53,6 +54,7 @@ class AttnDesc(ctypes.Structure):
         ("dtype", ctypes.c_int32),
         ("rope_theta", ctypes.c_double),
         ("scale", ctypes.c_float),
+        ("flags", ctypes.c_int32),
     ]
 
 
@@ -75,6 +77,7 @@ def lib(path: Optional[str] = None):
     L.hw_attn_decode.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12 + [ctypes.c_size_t, _P]
     L.hw_attn_plan.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 7 + [ctypes.c_size_t, _P]
     L.hw_attn_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 6 + [ctypes.c_size_t, _P]
+    L.hw_attn_plan_limited.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]
     L.hw_attn_plan_append.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]
     L.hw_attn_append_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]
     L.hw_plan_export.argtypes = [ctypes.POINTER(AttnDesc), _P, ctypes.c_size_t, _P, ctypes.c_int32,
@@ -90,6 +93,7 @@ def lib(path: Optional[str] = None):
     L.hw_workspace_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
     L.hw_views_combined.argtypes = [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
     L.hw_views.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
+    L.hw_views_chunked.argtypes = [ctypes.c_int32] * 4 + [_P] * 5
     L.hw_last_cuda_error.argtypes = []
     L.hw_status_string.argtypes = [ctypes.c_int]
     L.hw_status_string.restype = ctypes.c_char_p
@@ -132,10 +136,10 @@ def _check(fn: str, st: int):
 
 
 def make_desc(n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, max_view_blocks, cache_capacity,
-              dtype, rope_theta, scale) -> AttnDesc:
+              dtype, rope_theta, scale, flags=0) -> AttnDesc:
     return AttnDesc(int(n_rows), int(n_q_heads), int(n_kv_heads), int(head_dim), int(n_blocks),
                     int(max_view_blocks), int(cache_capacity), int(dtype), float(rope_theta),
-                    float(scale))
+                    float(scale), int(flags))
 
 
 def attn_decode_workspace_size(desc: AttnDesc) -> int:
@@ -177,6 +181,19 @@ def attn_decode_planned(desc: AttnDesc, q, k_cache, v_cache, out, lse, workspace
                                       _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                                       _stream(stream))
     _check("hw_attn_decode_planned", st)
+    return st
+
+
+def attn_plan_limited(desc: AttnDesc, block_start, block_len, view_block, view_offset, view_limit,
+                      q_pos, workspace, workspace_bytes: int, q_to_kv=None, stream=None) -> int:
+    """hw_attn_plan_limited: the step planned with a token limit per view
+    entry (view_limit[r][v]: row r attends the first view_limit[r][v] tokens
+    of block view_block[r][v]; negative = all of them)."""
+    st = lib().hw_attn_plan_limited(ctypes.byref(desc), _ptr(block_start), _ptr(block_len),
+                                    _ptr(view_block), _ptr(view_offset), _ptr(view_limit),
+                                    _ptr(q_pos), _ptr(q_to_kv), _ptr(workspace),
+                                    int(workspace_bytes), _stream(stream))
+    _check("hw_attn_plan_limited", st)
     return st
 
 
@@ -285,6 +302,23 @@ def views(layout, block_len, n_problems: int, n_workers: int):
     _check("hw_views", lib().hw_views(lay, int(n_problems), int(n_workers), bl.ctypes.data,
                                       vb.ctypes.data, vo.ctypes.data, qp.ctypes.data))
     return vb, vo, qp
+
+
+def views_chunked(layout, block_len, n_problems: int, n_workers: int, chunk: int):
+    """Host helper: (view_block, view_offset, view_limit, q_pos) of T-token
+    query chunks (T = chunk) in a cache layout; row (p, w, t) at index
+    (p*W + w)*T + t."""
+    lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    bl = np.ascontiguousarray(block_len, dtype=np.int32)
+    rows, V = n_problems * n_workers * chunk, n_workers + 1
+    vb = np.empty((rows, V), np.int32)
+    vo = np.empty((rows, V), np.int32)
+    vl = np.empty((rows, V), np.int32)
+    qp = np.empty(rows, np.int32)
+    _check("hw_views_chunked", lib().hw_views_chunked(lay, int(n_problems), int(n_workers), int(chunk),
+                                                      bl.ctypes.data, vb.ctypes.data, vo.ctypes.data,
+                                                      vl.ctypes.data, qp.ctypes.data))
+    return vb, vo, vl, qp
 
 
 def status_string(st: int) -> str:

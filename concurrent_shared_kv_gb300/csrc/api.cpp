@@ -104,9 +104,9 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
   const size_t rec = static_cast<size_t>(kMaxQ) * (d.head_dim + kRecPad) * sizeof(float);
   L.meta_off = L.partials_off + up(static_cast<size_t>(L.slots) * rec);
   // metadata copies: view_block, view_offset (rows x V), q_pos, q_to_kv, block_start, block_len,
-  // append_block, append_pos
+  // append_block, append_pos, view_limit (rows x V)
   const size_t entries = static_cast<size_t>(d.n_rows) * d.max_view_blocks;
-  const size_t meta = (2 * entries + 3 * static_cast<size_t>(d.n_rows) + d.n_q_heads +
+  const size_t meta = (3 * entries + 3 * static_cast<size_t>(d.n_rows) + d.n_q_heads +
                        2 * static_cast<size_t>(d.n_blocks)) *
                       sizeof(int32_t);
   L.plan_off = L.meta_off + up(meta);
@@ -121,7 +121,7 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
 // The metadata copies of a workspace (written by hw_attn_plan).
 struct MetaCopies {
   int32_t *view_block, *view_offset, *q_pos, *q_to_kv, *block_start, *block_len;
-  int32_t *append_block, *append_pos;
+  int32_t *append_block, *append_pos, *view_limit;
 };
 static MetaCopies meta_copies(const hw_attn_desc &d, const WorkspaceLayout &L, void *workspace) {
   int32_t *m = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.meta_off);
@@ -135,6 +135,7 @@ static MetaCopies meta_copies(const hw_attn_desc &d, const WorkspaceLayout &L, v
   c.block_len = c.block_start + d.n_blocks;
   c.append_block = c.block_len + d.n_blocks;
   c.append_pos = c.append_block + d.n_rows;
+  c.view_limit = c.append_pos + d.n_rows;
   return c;
 }
 
@@ -155,8 +156,13 @@ static int check_desc(const hw_attn_desc *d) {
     return HW_ERR_UNSUPPORTED;
   if (d->n_q_heads / d->n_kv_heads > kMaxQ) return HW_ERR_UNSUPPORTED;
   if (d->cache_capacity > INT32_MAX) return HW_ERR_UNSUPPORTED;
+  if (d->flags & ~HW_DESC_VIEW_LIMITS) return HW_ERR_INVALID;
+  if ((d->flags & HW_DESC_VIEW_LIMITS) && !(d->dtype == HW_BF16 && d->head_dim == 128))
+    return HW_ERR_UNSUPPORTED;
   return HW_OK;
 }
+
+static bool limited(const hw_attn_desc *d) { return (d->flags & HW_DESC_VIEW_LIMITS) != 0; }
 
 }  // namespace hw
 
@@ -226,9 +232,10 @@ static int decode_common(const hw_attn_desc *d, const void *q, const void *k_cac
                          void *out, float *lse, void *workspace, const WorkspaceLayout &L,
                          int max_ctas, void *stream, const int32_t *append_block = nullptr,
                          const int32_t *append_pos = nullptr, const void *k_new = nullptr,
-                         const void *v_new = nullptr) {
+                         const void *v_new = nullptr, const int32_t *view_limit = nullptr) {
   DecodeArgs a;
   fill_args(a, d, L, workspace);
+  a.view_limit = view_limit;
   a.append_block = append_block;
   a.append_pos = append_pos;
   a.k_new = k_new;
@@ -284,6 +291,7 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
                    size_t workspace_bytes, void *stream) {
   int st = check_desc(d);
   if (st != HW_OK) return st;
+  if (limited(d)) return HW_ERR_UNSUPPORTED;  // limits come with a plan
   if (d->n_rows == 0) return HW_OK;
   if (!q || !out || !q_pos) return HW_ERR_INVALID;
   if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
@@ -302,14 +310,15 @@ static int plan_impl(const hw_attn_desc *d, const int32_t *block_start, const in
                      const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
                      const int32_t *q_to_kv, const int32_t *append_block,
                      const int32_t *append_pos, void *workspace, size_t workspace_bytes,
-                     void *stream) {
+                     void *stream, const int32_t *view_limit = nullptr) {
   int st = check_desc(d);
   if (st != HW_OK) return st;
   if (d->n_rows == 0) return HW_OK;
   if (!q_pos) return HW_ERR_INVALID;
   if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
   if (d->n_blocks > 0 && (!block_start || !block_len)) return HW_ERR_INVALID;
-  if (append_block && !tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
+  if ((append_block || view_limit) && !tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
+  if (limited(d) != (view_limit != nullptr)) return view_limit ? HW_ERR_INVALID : HW_ERR_UNSUPPORTED;
   WorkspaceLayout L;
   int max_ctas = 0;
   st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
@@ -324,6 +333,7 @@ static int plan_impl(const hw_attn_desc *d, const int32_t *block_start, const in
   a.q_to_kv = q_to_kv;
   a.append_block = append_block;
   a.append_pos = append_pos;
+  a.view_limit = view_limit;
   const MetaCopies m = meta_copies(*d, L, workspace);
   PlanOut o;
   o.plan = tensor_core_path(d) ? static_cast<uint8_t *>(workspace) + L.plan_off : nullptr;
@@ -335,6 +345,7 @@ static int plan_impl(const hw_attn_desc *d, const int32_t *block_start, const in
   o.block_len = m.block_len;
   o.append_block = m.append_block;
   o.append_pos = m.append_pos;
+  o.view_limit = m.view_limit;
   const cudaError_t e = launch_plan(a, o, device_sm_count(), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? HW_OK : cuda_fail(e);
 }
@@ -344,6 +355,17 @@ int hw_attn_plan(const hw_attn_desc *d, const int32_t *block_start, const int32_
                  const int32_t *q_to_kv, void *workspace, size_t workspace_bytes, void *stream) {
   return plan_impl(d, block_start, block_len, view_block, view_offset, q_pos, q_to_kv, nullptr,
                    nullptr, workspace, workspace_bytes, stream);
+}
+
+int hw_attn_plan_limited(const hw_attn_desc *d, const int32_t *block_start,
+                         const int32_t *block_len, const int32_t *view_block,
+                         const int32_t *view_offset, const int32_t *view_limit,
+                         const int32_t *q_pos, const int32_t *q_to_kv, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  if (d && !(d->flags & HW_DESC_VIEW_LIMITS)) return HW_ERR_INVALID;
+  if (d && d->n_rows > 0 && d->max_view_blocks > 0 && !view_limit) return HW_ERR_INVALID;
+  return plan_impl(d, block_start, block_len, view_block, view_offset, q_pos, q_to_kv, nullptr,
+                   nullptr, workspace, workspace_bytes, stream, view_limit);
 }
 
 int hw_attn_plan_append(const hw_attn_desc *d, const int32_t *block_start,
@@ -372,7 +394,8 @@ int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_c
   const uint8_t *plan = static_cast<const uint8_t *>(workspace) + L.plan_off;
   return decode_common(d, q, k_cache, v_cache, m.block_start, m.block_len, m.view_block,
                        m.view_offset, m.q_pos, m.q_to_kv, plan, out, lse, workspace, L, max_ctas,
-                       stream);
+                       stream, nullptr, nullptr, nullptr, nullptr,
+                       limited(d) ? m.view_limit : nullptr);
 }
 
 int hw_plan_export(const hw_attn_desc *d, const void *workspace, size_t workspace_bytes,
@@ -406,6 +429,7 @@ int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const vo
                                   void *stream) {
   int st = check_desc(d);
   if (st != HW_OK) return st;
+  if (limited(d)) return HW_ERR_UNSUPPORTED;
   if (d->n_rows == 0) return HW_OK;
   if (!tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
   if (!q || !out || !k_new || !v_new) return HW_ERR_INVALID;
@@ -574,6 +598,42 @@ int hw_views(int32_t layout, int32_t n_problems, int32_t n_workers, const int32_
       }
       if (pos > INT32_MAX) return HW_ERR_INVALID;
       q_pos[row] = static_cast<int32_t>(pos);
+    }
+  }
+  return HW_OK;
+}
+
+int hw_views_chunked(int32_t layout, int32_t n_problems, int32_t n_workers, int32_t chunk,
+                     const int32_t *block_len, int32_t *view_block, int32_t *view_offset,
+                     int32_t *view_limit, int32_t *q_pos) {
+  if (chunk <= 0 || n_problems < 0 || n_workers <= 0) return HW_ERR_INVALID;
+  if (n_problems == 0) return HW_OK;
+  if (!block_len || !view_block || !view_offset || !view_limit || !q_pos) return HW_ERR_INVALID;
+  const int W = n_workers, V = n_workers + 1, T = chunk;
+  for (int p = 0; p < n_problems; ++p)
+    for (int w = 0; w < W; ++w)
+      if (block_len[p * (W + 1) + 1 + w] < T) return HW_ERR_INVALID;
+  // each problem's one-row-per-worker views, then T rows per worker
+  std::vector<int32_t> vb(W * V), vo(W * V), qp(W);
+  for (int p = 0; p < n_problems; ++p) {
+    const int base = p * (W + 1);
+    const int st = hw_views(layout, 1, W, block_len + base, vb.data(), vo.data(), qp.data());
+    if (st != HW_OK) return st;
+    for (int w = 0; w < W; ++w) {
+      const int n = block_len[base + 1 + w];
+      for (int t = 0; t < T; ++t) {
+        const int64_t r = (static_cast<int64_t>(p) * W + w) * T + t;
+        for (int v = 0; v < V; ++v) {
+          const int b = vb[w * V + v];
+          view_block[r * V + v] = b < 0 ? -1 : base + b;
+          view_offset[r * V + v] = vo[w * V + v];
+          view_limit[r * V + v] = -1;
+          if (b == 1 + w) {  // its own block: up to its own token
+            view_limit[r * V + v] = n - T + t + 1;
+            q_pos[r] = vo[w * V + v] + n - T + t;
+          }
+        }
+      }
     }
   }
   return HW_OK;

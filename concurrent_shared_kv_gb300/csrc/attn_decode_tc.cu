@@ -26,6 +26,7 @@
 // kernel costs stream time whatever its N, so fewer, wider products pay.)
 #include <cuda.h>
 
+#include <cfloat>
 #include <climits>
 
 #include "hw_device.cuh"
@@ -70,6 +71,7 @@ constexpr int kAppList = 8;   // new tokens of a CTA a plan lists (more: found b
 struct SegQ {
   SegMeta m;
   int32_t qrow[kMaxQ];  // row * Hq + q head
+  int32_t minlim;       // fewest tokens of the block a column attends (view limits), <= len
   int64_t rel[kMaxQ];
 };
 
@@ -132,6 +134,7 @@ struct PlanHeader {
   uint32_t magic;
   int32_t grid, n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
   int64_t capacity;
+  int32_t limited;  // planned with view limits: decoded by the limited kernel only
 };
 static_assert(sizeof(PlanHeader) <= kPlanHeaderBytes, "plan header");
 static_assert(sizeof(PlanShared) % 16 == 0 && sizeof(CtaPlan) % 16 == 0, "bulk copy sizes");
@@ -146,7 +149,7 @@ __device__ __forceinline__ bool plan_matches(const DecodeArgs &a, const uint8_t 
   return h.magic == kPlanMagic && h.grid == static_cast<int32_t>(gridDim.x) &&
          h.n_rows == a.n_rows && h.n_q_heads == a.n_q_heads && h.n_kv_heads == a.n_kv_heads &&
          h.head_dim == a.head_dim && h.n_blocks == a.n_blocks && h.n_view == a.n_view &&
-         h.capacity == a.capacity;
+         h.capacity == a.capacity && (h.limited != 0) == (a.view_limit != nullptr);
 }
 
 __device__ __forceinline__ void set_abort(TcSmem &S, const DecodeArgs &a) {
@@ -346,18 +349,37 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
   mbar_wait(&S.mma_done, 0);
 }
 
+// The tokens of its block that view entry e attends: all len, or fewer under
+// a view limit.
+__device__ __forceinline__ int entry_limit(const int32_t *view_limit, int e, int len) {
+  if (!view_limit) return len;
+  const int v = __ldg(view_limit + e);
+  return v >= 0 && v < len ? v : len;
+}
+
 // Query-side metadata of segment (b, h) into X, by one warp (shared memory
-// only, except for views beyond the metadata cache).
-__device__ void seg_pre(const DecodeArgs &a, const MetaCache &C, SegQ &X, int b, int h, int lane) {
+// only, except for views beyond the metadata cache), with the fewest tokens
+// any of its columns attends (len when no view limit cuts the block).
+template <bool kLimit>
+__device__ void seg_pre(const DecodeArgs &a, const PlanCore &P, const MetaCache &C, SegQ &X, int b,
+                        int h, int lane) {
+  const int len = P.len[b];
   const int G = a.n_q_heads / a.n_kv_heads;
   gather_refs(a, C, X.m, b, lane);
   gather_qheads(a, C, X.m, h, lane);
   __syncwarp();
+  int lim = len;
   if (lane < X.m.n_ref * G) {
     const int e = X.m.ref_entry[lane / G];
     X.qrow[lane] = (e / a.n_view) * a.n_q_heads + X.m.qhead[lane % G];
     X.rel[lane] = entry_rel(a, C, e);
+    if (kLimit) lim = entry_limit(a.view_limit, e, len);
   }
+  if (kLimit) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) lim = min(lim, __shfl_xor_sync(0xffffffffu, lim, o));
+  }
+  if (lane == 0) X.minlim = lim;
   __syncwarp();
 }
 
@@ -444,7 +466,7 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
   };
   if (w == 0 && !kPlanned) {  // a plan brings it ready-made
     const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u0);
-    seg_pre(a, S.ps.cache, S.cp.pre[0], x.b, x.h, lane);
+    seg_pre<false>(a, S.ps.plan, S.ps.cache, S.cp.pre[0], x.b, x.h, lane);
   }
   sync();
   const SegQ &X = S.cp.pre[0];
@@ -550,7 +572,7 @@ __device__ void append_tokens(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_
 // warps' record stores sit on the path of the next rotated queries.  Last,
 // the metadata of segment j + 2 goes into the slot segment j - 2 vacated,
 // and its queries are prefetched into L2.
-template <bool kPlanned>
+template <bool kPlanned, bool kLimit>
 __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
   const int lane = threadIdx.x & 31, wq = tq >> 5;
@@ -577,7 +599,7 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
     for (int k = 1; k < kPre; ++k) {
       if ((k & 1) == wq && S.cp.us[k] < u1) {
         const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, S.cp.us[k]);
-        seg_pre(a, S.ps.cache, S.cp.pre[k], x.b, x.h, lane);
+        seg_pre<kLimit>(a, S.ps.plan, S.ps.cache, S.cp.pre[k], x.b, x.h, lane);
       }
     }
     sync();
@@ -647,7 +669,7 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
       if (u_prep < u1) {
         const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u_prep);
         SegQ &N = S.cp.pre[(seg + 2) % kPre];
-        if (wq == 0) seg_pre(a, S.ps.cache, N, x.b, x.h, lane);
+        if (wq == 0) seg_pre<kLimit>(a, S.ps.plan, S.ps.cache, N, x.b, x.h, lane);
         u_prep = x.seg_first + x.tiles;
       }
       sync();
@@ -703,6 +725,9 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
   if (lane == 0) mbar_arrive(&S.rec_ready[seg & 3]);
 }
 
+// kLimit: the plan carries view limits, so a column may attend only part of
+// a block.
+template <bool kLimit>
 __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0,
                              int64_t u1) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -719,9 +744,15 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   // below are always reached by all 128 threads; after an abort no wait
   // blocks any more and the CTA runs to its end on stale data.
   // m_run[j]: reference max of column j (the same in every lane); m_mine:
-  // the one of column `lane`, from which the others are broadcast
-  float m_run[kN], l_part[kN], m_mine = -INFINITY;
+  // the one of column `lane`, from which the others are broadcast.  They
+  // start at -FLT_MAX, not -inf: a column that a view limit keeps from every
+  // token of its segment then gets p = 2^(-inf) = 0 (l = 0, an empty record)
+  // where -inf - -inf would give NaN.
+  float m_run[kN], l_part[kN], m_mine = -FLT_MAX;
   int seg = -1, nq = 0;
+  // view limits of the segment: the fewest tokens a column attends, and the
+  // count of column `lane` (broadcast to the others on the tiles that need it)
+  int minlim = INT_MAX, lim_mine = INT_MAX;
   int pend = -1, pend_b = 0, pend_h = 0, pend_nq = 0;  // segment whose records are due
   for (int i = 0; i < n; ++i) {
     const int64_t u = u0 + i;
@@ -731,14 +762,23 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       ++seg;
       wait_or_abort(S, a, &S.q_full, seg & 1);
       nq = min(S.meta_nref * G, kN);
+      if constexpr (kLimit) {
+        // the segment's metadata stays in its slot until its records are out
+        const SegQ &X = S.cp.pre[seg % kPre];
+        const int len = S.ps.plan.len[x.b];
+        minlim = X.minlim;
+        lim_mine = len;
+        if (minlim < len && lane < nq)
+          lim_mine = entry_limit(a.view_limit, X.m.ref_entry[lane / G], len);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.q_empty);  // this warp has read the hand-off
 #pragma unroll
       for (int j = 0; j < kN; ++j) {
-        m_run[j] = -INFINITY;
+        m_run[j] = -FLT_MAX;
         l_part[j] = 0.f;
       }
-      m_mine = -INFINITY;
+      m_mine = -FLT_MAX;
     }
     const int sb = i & 1, s = i % kStages;
     wait_or_abort(S, a, &S.s_full[sb], (i >> 1) & 1);
@@ -754,11 +794,22 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
 #pragma unroll
     for (int j = 0; j < kN; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
 
-    const int valid = min(kT, S.ps.plan.len[x.b] - x.t * kT);
+    const int base = x.t * kT;  // the tile's first token in its block
+    const int valid = min(kT, S.ps.plan.len[x.b] - base);
     const bool tok_ok = row < valid;
     float sc[kN];
+    if (!kLimit || base + kT <= minlim) {
 #pragma unroll
-    for (int j = 0; j < kN; ++j) sc[j] = tok_ok ? __uint_as_float(r[j]) : -INFINITY;
+      for (int j = 0; j < kN; ++j) sc[j] = tok_ok ? __uint_as_float(r[j]) : -INFINITY;
+    } else {
+      // some column's view limit ends in this tile (a chunk's own tokens);
+      // limits never exceed the block, so they cover valid too
+#pragma unroll
+      for (int j = 0; j < kN; ++j) {
+        const int lim = __shfl_sync(0xffffffffu, lim_mine, j);
+        sc[j] = (tok_ok && base + row < lim) ? __uint_as_float(r[j]) : -INFINITY;
+      }
+    }
 
     // Lazy rescaling: the reference max m_run moves only when some score
     // exceeds it by more than kLazy (log2 units), so p <= 2^kLazy and O is
@@ -863,9 +914,11 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
 }
 
 // kPlanned: the step's plan is loaded (else built in-kernel); kAppend (with a
-// plan): the layer's new tokens are written first.  Each combination is its
-// own kernel, so that no path carries another's code.
-template <bool kPlanned, bool kAppend>
+// plan): the layer's new tokens are written first; kLimit (with a plan, no
+// appends): the plan carries view limits.  Each combination is its own
+// kernel, so that no path carries another's code (a second softmax loop in
+// the same kernel, even one never entered, cost the plain path 8 %).
+template <bool kPlanned, bool kAppend, bool kLimit>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
@@ -992,9 +1045,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         query_prologue<kPlanned>(a, S, u0, u1, appending ? 128 : 192);
       if (warp < kWarpQ)
-        softmax_role(a, S, tmem, u0, u1);
+        softmax_role<kLimit>(a, S, tmem, u0, u1);
       else
-        qprep<kPlanned>(a, S, u0, u1);
+        qprep<kPlanned, kLimit>(a, S, u0, u1);
     }
   } else if (!kPlanned) {
     plan_ranks(a, S.ps.cache, warp, lane, 0, 1);  // a CTA without units: ranks for the merge
@@ -1052,6 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       o.append_block[i] = a.append_block ? a.append_block[i] : -1;
       o.append_pos[i] = a.append_block ? a.append_pos[i] : 0;
     }
+    for (int i = tid; i < E; i += nt) o.view_limit[i] = a.view_limit ? a.view_limit[i] : -1;
   }
   if (!o.plan) return;
   PlanCore &P = S.ps.plan;
@@ -1105,7 +1159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp < kPre && S.cp.us[warp] < S.cp.u1) {
     const UnitPos x = unit_pos(P, a.n_blocks, S.cp.us[warp]);
-    seg_pre(a, S.ps.cache, S.cp.pre[warp], x.b, x.h, lane);
+    seg_pre<true>(a, P, S.ps.cache, S.cp.pre[warp], x.b, x.h, lane);
   } else if (warp >= kPre && warp < kPre + kPreItems) {
     // the record lists of the CTA's first merge items (item k: first + k * grid)
     const int k = warp - kPre;
@@ -1134,6 +1188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       h.n_blocks = a.n_blocks;
       h.n_view = a.n_view;
       h.capacity = a.capacity;
+      h.limited = a.view_limit != nullptr;
       *reinterpret_cast<PlanHeader *>(o.plan) = h;
     }
   }
@@ -1183,11 +1238,12 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const C
   const size_t smem = decode_tc_smem_bytes();
   // planned launches run their own instantiations: without the plan-building
   // (and, without appends, the append) code the kernel is far smaller
-  const int which = !a.plan ? 0 : !a.k_new ? 1 : 2;
-  void (*kernel)(DecodeArgs, CUtensorMap, CUtensorMap) =
-      which == 0 ? decode_tc_kernel<false, false>
-                 : which == 1 ? decode_tc_kernel<true, false> : decode_tc_kernel<true, true>;
-  static bool configured[3] = {false, false, false};
+  const int which = !a.plan ? 0 : a.k_new ? 2 : a.view_limit ? 3 : 1;
+  void (*const kernels[4])(DecodeArgs, CUtensorMap, CUtensorMap) = {
+      decode_tc_kernel<false, false, false>, decode_tc_kernel<true, false, false>,
+      decode_tc_kernel<true, true, false>, decode_tc_kernel<true, false, true>};
+  void (*kernel)(DecodeArgs, CUtensorMap, CUtensorMap) = kernels[which];
+  static bool configured[4] = {false, false, false, false};
   if (!configured[which]) {
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));

@@ -728,9 +728,12 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
 #pragma unroll
           for (int e = 0; e < EPL; ++e) sum[e] += Z.acc[w0 + w2][lane * EPL + e] * f;
         }
+        // L = 0: view limits left the row no token (its partials are empty)
+        const bool any = L > 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) orow[e] = from_f32<T>(sum[e] / L);
-        if (lane == 0 && a.lse) a.lse[ob] = (Mx + __log2f(L)) * 0.69314718055994530942f;
+        for (int e = 0; e < EPL; ++e) orow[e] = from_f32<T>(any ? sum[e] / L : 0.f);
+        if (lane == 0 && a.lse)
+          a.lse[ob] = any ? (Mx + __log2f(L)) * 0.69314718055994530942f : -INFINITY;
       }
       if (lane == 0) a.counters[it] = 0;  // re-armed for the next call
     }

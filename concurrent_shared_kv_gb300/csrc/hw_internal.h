@@ -47,6 +47,10 @@ struct DecodeArgs {
   // [n_rows][Hkv][D], or null (nothing is written; k and v are then only read).
   const int32_t *append_block, *append_pos;
   const void *k_new, *v_new;
+  // Per view entry, the tokens of its block the row attends (negative: all),
+  // or null: every entry sees its whole block.  At plan time the caller's
+  // array, at decode time the plan's copy.
+  const int32_t *view_limit;
   float scale_log2;   // softmax scale * log2(e): scores live in the log2 domain
   // RoPE phase increments: for pair i, the fraction of a turn per position,
   // frac(w_i / 2pi), as an unsigned 0.64 fixed-point number.  The angle of
@@ -84,6 +88,7 @@ struct PlanOut {
   uint8_t *plan;  // null: copy the metadata only
   int32_t *view_block, *view_offset, *q_pos, *q_to_kv, *block_start, *block_len;
   int32_t *append_block, *append_pos;  // -1 / 0 for every row without an append
+  int32_t *view_limit;                 // -1 for every entry without a limit
 };
 cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s);
 int decode_simt_ctas_per_sm(int dtype, int head_dim);

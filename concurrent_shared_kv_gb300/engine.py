@@ -18,12 +18,16 @@ class DecodeSession:
 
     def __init__(self, *, n_rows: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
                  n_blocks: int, max_view_blocks: int, capacity: int, dtype: torch.dtype,
-                 rope_theta: float, scale: Optional[float] = None, device="cuda"):
+                 rope_theta: float, scale: Optional[float] = None, device="cuda",
+                 view_limits: bool = False):
+        """view_limits: the steps are planned with per-view-entry token limits
+        (plan_limited; decode_planned then applies them)."""
         self.device = torch.device(device)
         self.dtype = dtype
         self.desc = api.make_desc(n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks,
                                   max_view_blocks, capacity, DTYPES[dtype], rope_theta,
-                                  head_dim ** -0.5 if scale is None else scale)
+                                  head_dim ** -0.5 if scale is None else scale,
+                                  flags=api.HW_DESC_VIEW_LIMITS if view_limits else 0)
         self.ws_bytes = api.attn_decode_workspace_size(self.desc)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         api.workspace_init(self.workspace, self.ws_bytes)
@@ -62,6 +66,18 @@ class DecodeSession:
         api.attn_plan(self.desc, m["block_start"], m["block_len"], m["view_block"],
                       m["view_offset"], m["q_pos"], self.workspace, self.ws_bytes,
                       q_to_kv=m["q_to_kv"], stream=stream)
+
+    def plan_limited(self, view_limit, stream=None):
+        """hw_attn_plan_limited: plan the step with a token limit per view
+        entry ([rows][V]; negative = the whole block), e.g. the causal order
+        of a chunk of queries within its own block."""
+        m = self.meta
+        t = torch.as_tensor(np.ascontiguousarray(view_limit, dtype=np.int32)) \
+            if not torch.is_tensor(view_limit) else view_limit
+        self.view_limit = t.to(self.device, dtype=torch.int32).contiguous()
+        api.attn_plan_limited(self.desc, m["block_start"], m["block_len"], m["view_block"],
+                              m["view_offset"], self.view_limit, m["q_pos"], self.workspace,
+                              self.ws_bytes, q_to_kv=m["q_to_kv"], stream=stream)
 
     def plan_append(self, append_block, append_pos, stream=None):
         """hw_attn_plan_append: plan the step with each row's new token

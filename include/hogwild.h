@@ -87,7 +87,18 @@ typedef struct {
   int32_t dtype;           /* hw_dtype of q, pools and out */
   double rope_theta;       /* RoPE base, > 1 */
   float scale;             /* softmax scale, usually 1/sqrt(D) */
+  int32_t flags;           /* HW_DESC_* bits, 0 for none */
 } hw_attn_desc;
+
+/*
+ * The step's plan carries per-view-entry token limits.  A descriptor with this
+ * flag is planned by hw_attn_plan_limited and decoded by
+ * hw_attn_decode_planned only (bf16, head_dim 128): the other decode and plan
+ * calls return HW_ERR_UNSUPPORTED for it, and hw_attn_plan_limited returns
+ * HW_ERR_INVALID without it.  (The limits run in their own kernel, so that
+ * steps without limits pay nothing for them.)
+ */
+#define HW_DESC_VIEW_LIMITS 1
 
 /*
  * Bytes of workspace hw_attn_decode needs for `d` on the current device.
@@ -196,6 +207,24 @@ int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_c
  * written); hw_attn_decode_planned on a plan with appends writes nothing
  * either.  bf16 with head_dim 128 only (HW_ERR_UNSUPPORTED otherwise).
  */
+/*
+ * Chunked multi-token queries: a worker's chunk of T query tokens is T rows
+ * with the same view, row t at position q_pos + t, and within the worker's
+ * own block - which holds the chunk's own tokens - each row sees only the
+ * tokens up to its own (causal order).  hw_attn_plan_limited is hw_attn_plan
+ * with a per-view-entry limit:
+ *  view_limit  dev  int32 [n_rows][V]: row r attends only the first
+ *                   min(view_limit[r][v], len) tokens of block view_block[r][v];
+ *                   a negative value: the whole block
+ * (copied into the plan).  hw_attn_decode_planned then applies the limits.
+ * bf16 with head_dim 128 only (HW_ERR_UNSUPPORTED otherwise).
+ */
+int hw_attn_plan_limited(const hw_attn_desc *d, const int32_t *block_start,
+                         const int32_t *block_len, const int32_t *view_block,
+                         const int32_t *view_offset, const int32_t *view_limit,
+                         const int32_t *q_pos, const int32_t *q_to_kv, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
 int hw_attn_plan_append(const hw_attn_desc *d, const int32_t *block_start,
                         const int32_t *block_len, const int32_t *view_block,
                         const int32_t *view_offset, const int32_t *q_pos, const int32_t *q_to_kv,
@@ -332,6 +361,22 @@ int hw_views_combined(int32_t n_problems, int32_t n_workers, const int32_t *bloc
 typedef enum { HW_LAYOUT_COMBINED = 0, HW_LAYOUT_INTERLEAVED = 1, HW_LAYOUT_CONTIGUOUS = 2 } hw_layout;
 int hw_views(int32_t layout, int32_t n_problems, int32_t n_workers, const int32_t *block_len,
              int32_t *view_block, int32_t *view_offset, int32_t *q_pos);
+
+/*
+ * Host helper: the views of T-token query chunks (T = chunk > 0), for
+ * hw_attn_plan_limited.  Each worker's last T tokens are already in its own
+ * block and are queried at once, one row per token: row (p, w, t), index
+ * (p*W + w)*T + t, sees the blocks of worker w's view in `layout` (as
+ * hw_views), every other block whole and its own block up to its own token -
+ * block-local position len - T + t, so view_limit = len - T + t + 1 on that
+ * entry and -1 (whole block) on the others; q_pos = that token's position in
+ * the view.  All arrays host: view_block, view_offset, view_limit
+ * [n_problems*W*T][W+1], q_pos [n_problems*W*T].  HW_ERR_INVALID for an
+ * unknown layout or a worker block shorter than T.
+ */
+int hw_views_chunked(int32_t layout, int32_t n_problems, int32_t n_workers, int32_t chunk,
+                     const int32_t *block_len, int32_t *view_block, int32_t *view_offset,
+                     int32_t *view_limit, int32_t *q_pos);
 
 /* Last CUDA error code seen by this thread's library calls (cudaError_t). */
 int hw_last_cuda_error(void);

@@ -296,6 +296,37 @@ def layout_views(layout: str, block_len: Sequence[int], n_problems: int, n_worke
             "contiguous": contiguous_views}[layout](block_len, n_problems, n_workers)
 
 
+def chunk_views(layout: str, block_len: Sequence[int], n_problems: int, n_workers: int,
+                chunk: int):
+    """Views of T-token query chunks (T = chunk): each worker's last T tokens,
+    already in its own block, are queried at once, one row per token.  Row
+    (p, w, t), index (p*W + w)*T + t, sees the blocks of worker w's view in
+    the layout's order; every other block whole, its own block only up to its
+    own token (causal order inside the chunk): own block position
+    len - T + t, so the first len - T + t + 1 tokens, and q_pos is that
+    token's position in the view.  Returns (view_block, view_offset,
+    view_limit, q_pos); view_limit is -1 (whole block) except on the own
+    entry."""
+    vb1, vo1, _ = layout_views(layout, block_len, n_problems, n_workers)
+    W, T = n_workers, chunk
+    rows = n_problems * W * T
+    vb = np.repeat(vb1, T, axis=0)
+    vo = np.repeat(vo1, T, axis=0)
+    lim = np.full(vb.shape, -1, np.int32)
+    qp = np.zeros(rows, np.int32)
+    for p in range(n_problems):
+        for w in range(W):
+            own = p * (W + 1) + 1 + w
+            n = int(block_len[own])
+            assert n >= T, "each own block holds its chunk"
+            for t in range(T):
+                r = (p * W + w) * T + t
+                v = int(np.where(vb[r] == own)[0][0])
+                lim[r, v] = n - T + t + 1
+                qp[r] = vo[r, v] + n - T + t
+    return vb, vo, lim, qp
+
+
 
 # ---------------------------------------------------------------------------
 # The tensor-core kernel's work split, written out from its definition (for

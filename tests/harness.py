@@ -60,13 +60,13 @@ class Case:
     def capacity(self):
         return int(self.k.shape[1])
 
-    def session(self) -> engine.DecodeSession:
+    def session(self, view_limits: bool = False) -> engine.DecodeSession:
         w = self.w
         s = engine.DecodeSession(n_rows=self.q.shape[0], n_q_heads=w.n_q_heads,
                                  n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
                                  n_blocks=len(self.block_len), max_view_blocks=self.view_block.shape[1],
                                  capacity=self.capacity, dtype=torch_dtype(w), rope_theta=w.rope_theta,
-                                 scale=w.scale)
+                                 scale=w.scale, view_limits=view_limits)
         s.set_metadata(self.block_start, self.block_len, self.view_block, self.view_offset,
                        self.q_pos, self.q_to_kv)
         return s
