@@ -43,6 +43,9 @@ def parse():
     p.add_argument("--append", action="store_true",
                    help="each layer first writes every worker's new token (the last position of "
                         "its block) and then decodes, in one hw_attn_append_decode_planned launch")
+    p.add_argument("--chunk", type=int, default=0,
+                   help="T > 0: T query tokens per worker, each seeing its own block up to its own "
+                        "token (hw_views_chunked + hw_attn_plan_limited)")
     p.add_argument("--commit-all", action="store_true",
                    help="C4: every worker's finished block joins the history each step, all in "
                         "one hw_block_commit_many launch (the common block gets room for them)")
@@ -224,11 +227,19 @@ def main():
     if args.layers > 0:
         L = min(L, args.layers)
     lens, starts = w.block_lengths(), w.block_starts()
-    vb, vo, qp = api.views(args.layout, lens, w.n_problems, w.n_workers)
-    sess = engine.DecodeSession(n_rows=w.n_rows, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+    chunk = args.chunk
+    if chunk > 0:
+        assert not (args.append or args.unplanned), "--chunk runs planned decodes without appends"
+        vb, vo, vl, qp = api.views_chunked(args.layout, lens, w.n_problems, w.n_workers, chunk)
+        vl_dev = torch.from_numpy(vl).to(dev)  # uploaded once (the graph replays the plan)
+    else:
+        vb, vo, qp = api.views(args.layout, lens, w.n_problems, w.n_workers)
+    n_rows = vb.shape[0]
+    sess = engine.DecodeSession(n_rows=n_rows, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
                                 head_dim=w.head_dim, n_blocks=w.n_blocks,
                                 max_view_blocks=w.n_workers + 1, capacity=w.capacity, dtype=tdt,
-                                rope_theta=w.rope_theta, scale=w.scale, device=dev)
+                                rope_theta=w.rope_theta, scale=w.scale, device=dev,
+                                view_limits=chunk > 0)
     sess.set_metadata(starts, lens, vb, vo, qp)
     qs, ks, vs = [], [], []
     commit = w.commit_tokens > 0 and args.config == "C4"
@@ -239,6 +250,10 @@ def main():
         v_all = torch.empty_like(k_all)
     for l in range(L):
         q, k, v = wl.draw_device_layer(w, l, dev)
+        if chunk > 0:  # one query per chunk token
+            gq = torch.Generator(device=dev)
+            gq.manual_seed(7000 + l)
+            q = torch.randn((n_rows, w.n_q_heads, w.head_dim), generator=gq, device=dev).to(tdt)
         if commit:
             k_all[l].copy_(k)
             v_all[l].copy_(v)
@@ -247,7 +262,7 @@ def main():
         ks.append(k)
         vs.append(v)
     outs = [torch.empty_like(qs[0]) for _ in range(L)]
-    lses = [torch.empty((w.n_rows, w.n_q_heads), dtype=torch.float32, device=dev) for _ in range(L)]
+    lses = [torch.empty((n_rows, w.n_q_heads), dtype=torch.float32, device=dev) for _ in range(L)]
     calls_per_step = L if args.config != "C5" else 64  # C5: one layer timed x64
     kernel = "decode_tc_kernel" if (w.dtype == "bf16" and w.head_dim == 128) else "decode_simt_kernel"
     stream = torch.cuda.Stream(device=dev)
@@ -278,6 +293,8 @@ def main():
         # a decode step: the views are planned once, then every layer runs
         if planned and append:
             sess.plan_append(ab, ap, stream=stream)
+        elif chunk > 0:
+            sess.plan_limited(vl_dev, stream=stream)
         elif planned:
             sess.plan(stream=stream)
         for i in range(calls_per_step):
@@ -384,6 +401,11 @@ def main():
         l_host = torch.empty(lses_all.shape, dtype=lses_all.dtype, pin_memory=True)
         meta_host = [torch.from_numpy(np.ascontiguousarray(x, np.int32)).pin_memory()
                      for x in (starts, lens, vb, vo, qp)]
+        meta_dev = [sess.meta[name] for name in ("block_start", "block_len", "view_block",
+                                                 "view_offset", "q_pos")]
+        if chunk > 0:
+            meta_host.append(torch.from_numpy(np.ascontiguousarray(vl, np.int32)).pin_memory())
+            meta_dev.append(vl_dev)
         h2d = q_host.numel() * q_host.element_size() + sum(m.numel() * 4 for m in meta_host)
         d2h = o_host.numel() * o_host.element_size() + l_host.numel() * 4
 
@@ -404,8 +426,8 @@ def main():
 
         def e2e_step():  # noqa: E306
             with torch.cuda.stream(stream):
-                for m, name in zip(meta_host, ("block_start", "block_len", "view_block", "view_offset", "q_pos")):
-                    sess.meta[name].copy_(m, non_blocking=True)
+                for m, md in zip(meta_host, meta_dev):
+                    md.copy_(m, non_blocking=True)
                 qdev_all.copy_(q_host, non_blocking=True)
                 if g_e2e is not None:
                     g_e2e.replay()
@@ -446,16 +468,19 @@ def main():
             "head_dim": w.head_dim, "kv_tokens_per_layer": w.kv_tokens(),
             "kv_bytes_per_step": step_bytes, "commit_bytes_per_step": commit_bytes,
             "parallelism": f"replicas x{world}", "layout": args.layout,
+            "query_rows": n_rows, "chunk": chunk if chunk > 0 else None,
             "mode": "eager" if graph is None else "cuda-graph",
             "calls": ("hw_attn_plan_append once per step + hw_attn_append_decode_planned per layer "
                       "(each worker's new token written, then decoded)" if append else
+                      f"hw_attn_plan_limited once per step + hw_attn_decode_planned per layer "
+                      f"({chunk}-token chunks, causal within each worker's own block)" if chunk > 0 else
                       "hw_attn_plan once per step + hw_attn_decode_planned per layer" if planned
                       else "hw_attn_decode per layer"),
             "l2": "inputs larger than L2: each step reads every layer's own KV pools "
                   f"({step_bytes / 1e9:.2f} GB per step vs 0.13 GB of L2)",
         },
         "frac_of_8TBps": gbs_rank / NOMINAL_HBM_GBS,
-        "worker_tokens_per_s_per_layer": w.n_rows / per_launch,
+        "worker_tokens_per_s_per_layer": n_rows / per_launch,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": (measured_traffic(kernel, "qwq32b_w4")
@@ -467,7 +492,7 @@ def main():
         "clocks": clk.summary(),
         "e2e": e2e,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and chunk == 0:
         line["cpu_baseline"] = timed_oracle(w, qs, ks, vs, starts, lens, vb, vo, qp)
     if rank == 0:
         print(json.dumps(line), flush=True)
