@@ -28,7 +28,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD_DIR = os.path.join(HERE, "_build")
 SRC = os.path.join(HERE, "hwref.c")
 
-F32, BF16 = 0, 1
+F32, BF16, FP8 = 0, 1, 2  # FP8: bf16 queries, E4M3 K and V with per-kv-head scales
 
 
 def lib_path(mutant: int = 0) -> str:
@@ -86,6 +86,13 @@ class Oracle:
                                                 _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int, _P, _P,
                                                 ctypes.c_int]
         L.hwref_attn_decode_limited.restype = ctypes.c_int
+        L.hwref_attn_decode_scaled.argtypes = [ctypes.POINTER(HwrefDesc)] + [_P] * 13 + [
+            ctypes.c_int32, ctypes.c_int, _P, _P, ctypes.c_int]
+        L.hwref_attn_decode_scaled.restype = ctypes.c_int
+        L.hwref_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.hwref_e4m3_to_double.restype = ctypes.c_double
+        L.hwref_e4m3_from_double.argtypes = [ctypes.c_double]
+        L.hwref_e4m3_from_double.restype = ctypes.c_uint8
         L.hwref_block_commit.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
                                          ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32,
@@ -109,24 +116,38 @@ class Oracle:
     def bf16_from_double(self, x: float) -> int:
         return int(self.lib.hwref_bf16_from_double(float(x)))
 
+    def e4m3_to_double(self, code: int) -> float:
+        return float(self.lib.hwref_e4m3_to_double(int(code)))
+
+    def e4m3_from_double(self, x: float) -> int:
+        return int(self.lib.hwref_e4m3_from_double(float(x)))
+
     # -- decode -------------------------------------------------------------
     def attn_decode(self, *, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
                     q_pos, n_kv_heads: int, rope_theta: float, scale: float, dtype: int,
                     q_to_kv=None, rows: Optional[Sequence[int]] = None, brute: bool = False,
-                    n_threads: Optional[int] = None, view_limit=None):
+                    n_threads: Optional[int] = None, view_limit=None, k_scale=None,
+                    v_scale=None):
         """Returns (out [rows][Hq][D] float64, lse [rows][Hq] float64).
 
         view_limit [rows][V] (optional): an entry with a limit >= 0 attends
         only the first min(limit, len) tokens of its block.
 
         q, k_cache, v_cache hold storage values: float32 arrays for ``dtype=F32``,
-        uint16 bf16 bit patterns for ``dtype=BF16``.  k_cache/v_cache are
-        [Hkv][capacity][D].  Unselected rows of the outputs are NaN.
+        uint16 bf16 bit patterns for ``dtype=BF16``; for ``dtype=FP8`` q is bf16
+        and the caches hold uint8 E4M3 codes, a cached element being its value
+        times its kv head's k_scale / v_scale (float32 [Hkv]).  k_cache/v_cache
+        are [Hkv][capacity][D].  Unselected rows of the outputs are NaN.
         """
         sd = np.float32 if dtype == F32 else np.uint16
+        cd = np.uint8 if dtype == FP8 else sd
         q = np.ascontiguousarray(q, dtype=sd)
-        k_cache = np.ascontiguousarray(k_cache, dtype=sd)
-        v_cache = np.ascontiguousarray(v_cache, dtype=sd)
+        k_cache = np.ascontiguousarray(k_cache, dtype=cd)
+        v_cache = np.ascontiguousarray(v_cache, dtype=cd)
+        if dtype == FP8:
+            k_scale = np.ascontiguousarray(k_scale, dtype=np.float32)
+            v_scale = np.ascontiguousarray(v_scale, dtype=np.float32)
+            assert k_scale.shape == (n_kv_heads,) and v_scale.shape == (n_kv_heads,)
         n_rows, Hq, D = q.shape
         assert k_cache.shape[0] == n_kv_heads and k_cache.shape[2] == D
         assert v_cache.shape == k_cache.shape
@@ -145,8 +166,10 @@ class Oracle:
         vlim = None if view_limit is None else i32(view_limit)
         if vlim is not None:
             assert vlim.shape == view_block.shape
-        rc = self.lib.hwref_attn_decode_limited(
+        rc = self.lib.hwref_attn_decode_scaled(
             ctypes.byref(desc), q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
+            k_scale.ctypes.data if dtype == FP8 else None,
+            v_scale.ctypes.data if dtype == FP8 else None,
             block_start.ctypes.data, block_len.ctypes.data, view_block.ctypes.data,
             view_offset.ctypes.data, q_pos.ctypes.data,
             None if qmap is None else qmap.ctypes.data,
@@ -164,8 +187,9 @@ class Oracle:
         """In-place on copies of k_dst/v_dst ([Hkv][cap][D] storage values).
 
         Returns (k_dst_new, v_dst_new[, k_exact [Hkv][n][D] float64]).
+        FP8: uint8 E4M3 codes, no scale (a rotation carries a head's scale over).
         """
-        sd = np.float32 if dtype == F32 else np.uint16
+        sd = np.float32 if dtype == F32 else np.uint8 if dtype == FP8 else np.uint16
         k_src = np.ascontiguousarray(k_src, dtype=sd)
         v_src = np.ascontiguousarray(v_src, dtype=sd)
         kd = np.array(k_dst, dtype=sd, copy=True, order="C")

@@ -33,7 +33,11 @@
  *    worker's own view; the query is rotated by i_q - i_k^block;
  *  - one max-subtracted softmax over the concatenation of all view blocks;
  *    an empty view gives out = 0 and lse = -inf;
- *  - GQA: q head h reads kv head h / (Hq/Hkv) unless a map is given.
+ *  - GQA: q head h reads kv head h / (Hq/Hkv) unless a map is given;
+ *  - FP8 caches (the survey's next steps name E4M3 storage with per-head
+ *    scales; the pages only mention FP8 attention as future work): K and V
+ *    hold E4M3 codes, a cached element is its decoded value times its kv
+ *    head's scale, queries stay bf16.
  *
  * Everything is computed in double, elementwise, with no blocking, fusion or
  * reordering beyond what the definitions state.  Work is spread over POSIX
@@ -54,7 +58,7 @@
 #endif
 #define MUTANT(n) (HWREF_MUTANT == (n))
 
-enum { HWREF_F32 = 0, HWREF_BF16 = 1 };
+enum { HWREF_F32 = 0, HWREF_BF16 = 1, HWREF_FP8 = 2 };
 enum { HWREF_OK = 0, HWREF_EINVAL = -1, HWREF_ENOMEM = -2 };
 
 /* ------------------------------------------------------------------------ */
@@ -62,8 +66,11 @@ enum { HWREF_OK = 0, HWREF_EINVAL = -1, HWREF_ENOMEM = -2 };
 /* ------------------------------------------------------------------------ */
 
 /* A bf16 value is the float whose upper 16 bits are the stored bits. */
+static double e4m3_to_double(uint8_t b);
+
 static double load_elem(const void *base, int dtype, int64_t idx) {
   if (dtype == HWREF_F32) return (double)((const float *)base)[idx];
+  if (dtype == HWREF_FP8) return e4m3_to_double(((const uint8_t *)base)[idx]);
   uint32_t u = (uint32_t)((const uint16_t *)base)[idx] << 16;
   float f;
   memcpy(&f, &u, sizeof f);
@@ -94,9 +101,48 @@ static uint16_t bf16_from_double(double x) {
   return (uint16_t)(sign | ((u >> 16) & 0x7fff));
 }
 
+/* FP8 E4M3 (the "fn" variant of the OCP 8-bit floating point formats): sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is subnormal
+ * (m * 2^-9), S.1111.111 is NaN, there is no infinity, the largest finite
+ * value is S.1111.110 = 448. */
+static double e4m3_to_double(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(8.0 + m, e - (MUTANT(10) ? 11 : 10)); /* (1 + m/8) * 2^(e - 7) */
+  return sign ? -v : v;
+}
+
+/* Round a double to E4M3, ties to even, directly from the double; magnitudes
+ * beyond 448 saturate to 448 (no infinity to round to). */
+static uint8_t e4m3_from_double(double x) {
+  if (isnan(x)) return 0x7f;
+  const uint8_t sign = signbit(x) ? 0x80 : 0;
+  const double a = fabs(x);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e); /* a in [2^(e-1), 2^e) */
+  int k = e - 1;
+  if (k < -6) k = -6; /* below 2^-6 the subnormal grid keeps the step 2^-9 */
+  double q = nearbyint(ldexp(a, 3 - k)); /* a on the grid of step 2^(k-3), in steps */
+  q = ldexp(q, k - 3);
+  if (q > 448.0) q = 448.0;
+  if (q == 0.0) return sign;
+  if (q < 0x1p-6) return sign | (uint8_t)ldexp(q, 9); /* subnormal: m * 2^-9 */
+  frexp(q, &e); /* q may have rounded up into the next binade */
+  k = e - 1;
+  const int m = (int)ldexp(q, 3 - k) - 8;
+  return sign | (uint8_t)(((k + 7) << 3) | m);
+}
+
 static void store_elem(void *base, int dtype, int64_t idx, double v) {
   if (dtype == HWREF_F32)
     ((float *)base)[idx] = (float)v; /* round to nearest even */
+  else if (dtype == HWREF_FP8)
+    ((uint8_t *)base)[idx] = e4m3_from_double(v);
   else
     ((uint16_t *)base)[idx] = bf16_from_double(v);
 }
@@ -104,6 +150,8 @@ static void store_elem(void *base, int dtype, int64_t idx, double v) {
 static void copy_elem(void *dst, const void *src, int dtype, int64_t di, int64_t si) {
   if (dtype == HWREF_F32)
     memcpy((float *)dst + di, (const float *)src + si, 4);
+  else if (dtype == HWREF_FP8)
+    memcpy((uint8_t *)dst + di, (const uint8_t *)src + si, 1);
   else
     memcpy((uint16_t *)dst + di, (const uint16_t *)src + si, 2);
 }
@@ -164,7 +212,7 @@ typedef struct {
   int32_t n_blocks;        /* blocks in the cache pool */
   int32_t max_view_blocks; /* width of the per-row view tables */
   int64_t cache_capacity;  /* tokens per head in the pool */
-  int32_t dtype;           /* HWREF_F32 or HWREF_BF16 */
+  int32_t dtype;           /* HWREF_F32, HWREF_BF16, or HWREF_FP8 (bf16 q, E4M3 K and V) */
   double rope_theta;
   double scale;
 } hwref_desc;
@@ -174,6 +222,7 @@ typedef struct {
   const void *q, *k, *v;
   const int32_t *block_start, *block_len, *view_block, *view_offset, *q_pos, *q_to_kv;
   const int32_t *view_limit; /* [rows][V] or NULL: tokens of the entry's block the row sees */
+  const float *k_scale, *v_scale; /* HWREF_FP8: [Hkv], a stored value times its head's scale */
   const int32_t *rows; /* rows to compute, n_items = n_sel * Hq */
   int32_t n_sel;
   int brute; /* 0: block form (the method), 1: brute-force re-encoding */
@@ -207,7 +256,11 @@ static int decode_item(decode_job *J, int32_t row, int32_t h, double *scratch_q,
   const int g = kv_head_of(d, J->q_to_kv, h);
   if (g < 0 || g >= d->n_kv_heads) return HWREF_EINVAL;
   const int64_t qbase = ((int64_t)row * d->n_q_heads + h) * D;
-  for (int i = 0; i < D; ++i) scratch_q[i] = load_elem(J->q, d->dtype, qbase + i);
+  const int qdt = d->dtype == HWREF_FP8 ? HWREF_BF16 : d->dtype;
+  for (int i = 0; i < D; ++i) scratch_q[i] = load_elem(J->q, qdt, qbase + i);
+  /* a cached K or V element is its stored value times the head's scale (E4M3) */
+  const double ks = d->dtype == HWREF_FP8 ? (double)J->k_scale[MUTANT(11) ? g ^ 1 : g] : 1.0;
+  const double vs = d->dtype == HWREF_FP8 ? (double)J->v_scale[g] : 1.0;
   const int64_t head_base = (int64_t)g * d->cache_capacity * D;
   const int32_t iq = J->q_pos[row];
 
@@ -244,11 +297,11 @@ static int decode_item(decode_job *J, int32_t row, int32_t h, double *scratch_q,
       int64_t kb = head_base + ((int64_t)J->block_start[b] + j) * D;
       double dot = 0.0;
       if (!J->brute) {
-        for (int i = 0; i < D; ++i) dot += qt[i] * load_elem(J->k, d->dtype, kb + i);
+        for (int i = 0; i < D; ++i) dot += qt[i] * (ks * load_elem(J->k, d->dtype, kb + i));
       } else {
         /* stored key sits at block-local position j: undo that, then encode
          * it at its absolute position in this view, off + j */
-        for (int i = 0; i < D; ++i) kk[i] = load_elem(J->k, d->dtype, kb + i);
+        for (int i = 0; i < D; ++i) kk[i] = ks * load_elem(J->k, d->dtype, kb + i);
         rope_with(kk, D, w, -(double)j, kk);
         rope_with(kk, D, w, (double)off + (double)j, ka);
         for (int i = 0; i < D; ++i) dot += qt[i] * ka[i];
@@ -279,7 +332,7 @@ static int decode_item(decode_job *J, int32_t row, int32_t h, double *scratch_q,
       double p = exp(s[t++] - M);
       Z += p;
       int64_t vb = head_base + ((int64_t)J->block_start[b] + j) * D;
-      for (int i = 0; i < D; ++i) o[i] += p * load_elem(J->v, d->dtype, vb + i);
+      for (int i = 0; i < D; ++i) o[i] += p * (vs * load_elem(J->v, d->dtype, vb + i));
     }
   }
   for (int i = 0; i < D; ++i) J->out[obase * D + i] = o[i] / Z;
@@ -316,7 +369,7 @@ static int valid_desc(const hwref_desc *d) {
   if (d->head_dim <= 0 || d->head_dim % 2 || d->head_dim > 1024) return 0;
   if (d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->n_q_heads % d->n_kv_heads) return 0;
   if (d->n_rows < 0 || d->n_blocks < 0 || d->max_view_blocks < 0) return 0;
-  if (d->dtype != HWREF_F32 && d->dtype != HWREF_BF16) return 0;
+  if (d->dtype != HWREF_F32 && d->dtype != HWREF_BF16 && d->dtype != HWREF_FP8) return 0;
   return 1;
 }
 
@@ -329,13 +382,15 @@ static int valid_desc(const hwref_desc *d) {
  * first min(limit, len) tokens of its block (a chunk's causal order within
  * its own block).
  */
-int hwref_attn_decode_limited(const hwref_desc *d, const void *q, const void *k_cache, const void *v_cache,
-                      const int32_t *block_start, const int32_t *block_len,
-                      const int32_t *view_block, const int32_t *view_offset, const int32_t *q_pos,
-                      const int32_t *q_to_kv, const int32_t *view_limit, const int32_t *rows,
-                      int32_t n_sel, int brute,
-                      double *out, double *lse, int n_threads) {
+int hwref_attn_decode_scaled(const hwref_desc *d, const void *q, const void *k_cache,
+                             const void *v_cache, const float *k_scale, const float *v_scale,
+                             const int32_t *block_start, const int32_t *block_len,
+                             const int32_t *view_block, const int32_t *view_offset,
+                             const int32_t *q_pos, const int32_t *q_to_kv,
+                             const int32_t *view_limit, const int32_t *rows, int32_t n_sel,
+                             int brute, double *out, double *lse, int n_threads) {
   if (!valid_desc(d) || !out || !lse) return HWREF_EINVAL;
+  if (d->dtype == HWREF_FP8 && (!k_scale || !v_scale)) return HWREF_EINVAL;
   decode_job J;
   memset(&J, 0, sizeof J);
   J.d = d;
@@ -349,6 +404,8 @@ int hwref_attn_decode_limited(const hwref_desc *d, const void *q, const void *k_
   J.q_pos = q_pos;
   J.q_to_kv = q_to_kv;
   J.view_limit = view_limit;
+  J.k_scale = k_scale;
+  J.v_scale = v_scale;
   J.rows = rows;
   J.n_sel = rows ? n_sel : d->n_rows;
   J.brute = brute;
@@ -365,6 +422,20 @@ int hwref_attn_decode_limited(const hwref_desc *d, const void *q, const void *k_
   for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
   pthread_mutex_destroy(&J.mu);
   return J.status;
+}
+
+/* hwref_attn_decode_scaled for bf16 or fp32 caches (no scales). */
+int hwref_attn_decode_limited(const hwref_desc *d, const void *q, const void *k_cache,
+                              const void *v_cache, const int32_t *block_start,
+                              const int32_t *block_len, const int32_t *view_block,
+                              const int32_t *view_offset, const int32_t *q_pos,
+                              const int32_t *q_to_kv, const int32_t *view_limit,
+                              const int32_t *rows, int32_t n_sel, int brute, double *out,
+                              double *lse, int n_threads) {
+  if (d && d->dtype == HWREF_FP8) return HWREF_EINVAL;
+  return hwref_attn_decode_scaled(d, q, k_cache, v_cache, NULL, NULL, block_start, block_len,
+                                  view_block, view_offset, q_pos, q_to_kv, view_limit, rows,
+                                  n_sel, brute, out, lse, n_threads);
 }
 
 /* hwref_attn_decode_limited without limits: every entry sees its whole block. */
@@ -387,7 +458,9 @@ int hwref_attn_decode(const hwref_desc *d, const void *q, const void *k_cache, c
  *   K_dst[h][dst_offset + j] = rho(K_src[h][src_begin + j], pos_delta)
  *   V_dst[h][dst_offset + j] = V_src[h][src_begin + j]          (bit copy)
  * for h < Hkv, j < n.  The rotated key is computed in double and rounded once
- * to the storage type (round to nearest, ties to even).  Destination entries
+ * to the storage type (round to nearest, ties to even; E4M3 saturates at
+ * +-448).  E4M3 pools take no scale here: a rotation is linear, so the key's
+ * head scale carries over unchanged when both pools share it.  Destination entries
  * outside [dst_offset, dst_offset + n) are left as they are.  If k_exact is
  * not NULL it receives the unrounded keys, [Hkv][n][D].
  * Heads are strided by *_head_stride elements.  src and dst must not overlap
@@ -400,7 +473,7 @@ int hwref_block_commit(int dtype, int32_t n_kv_heads, int32_t head_dim, double r
                        double *k_exact) {
   if (head_dim <= 0 || head_dim % 2 || head_dim > 1024 || n_kv_heads <= 0 || n_tokens < 0)
     return HWREF_EINVAL;
-  if (dtype != HWREF_F32 && dtype != HWREF_BF16) return HWREF_EINVAL;
+  if (dtype != HWREF_F32 && dtype != HWREF_BF16 && dtype != HWREF_FP8) return HWREF_EINVAL;
   const int D = head_dim;
   double w[512], x[1024], y[1024];
   hwref_rope_freqs(D, rope_theta, w);
@@ -422,5 +495,8 @@ int hwref_block_commit(int dtype, int32_t n_kv_heads, int32_t head_dim, double r
   return HWREF_OK;
 }
 
-/* Exposed for the tests: the oracle's own double -> bf16 rounding. */
+/* Exposed for the tests: the oracle's own double -> bf16 rounding, and its
+ * E4M3 decoding and rounding. */
 uint16_t hwref_bf16_from_double(double x) { return bf16_from_double(x); }
+double hwref_e4m3_to_double(uint8_t b) { return e4m3_to_double(b); }
+uint8_t hwref_e4m3_from_double(double x) { return e4m3_from_double(x); }

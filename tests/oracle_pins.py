@@ -425,9 +425,103 @@ def pin_view_limits(o: O.Oracle):
             assert abs(lse[t, h] - logsumexp(s_)) < 1e-12, (t, h)
 
 
+def pin_e4m3_codes(o: O.Oracle):
+    """E4M3 decoding against torch's float8_e4m3fn for all 256 codes (the two
+    NaN codes included), and rounding: values exactly representable in
+    float32 against torch's cast, hand-worked ties and saturation, and every
+    finite code back to itself."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    mine = np.array([o.e4m3_to_double(c) for c in codes])
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(mine[fin], ref[fin])
+    for c in codes[fin]:
+        got = o.e4m3_from_double(o.e4m3_to_double(c))
+        assert got == c or (mine[c] == 0 and got & 0x7f == 0), c
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(4000) * np.exp2(rng.integers(-12, 9, 4000))).astype(np.float32)
+    x = x[np.abs(x) < 440]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([o.e4m3_from_double(float(v)) for v in x], np.uint8)
+    assert np.array_equal(got, want)
+    # ties to even: 17 between 16 and 18, 2^-10 between 0 and 2^-9, 3 * 2^-10
+    # between 2^-9 and 2^-8; beyond 448 everything saturates
+    for v, c in ((17.0, 0x58), (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (448.0, 0x7E),
+                 (465.0, 0x7E), (1e9, 0x7E), (-500.0, 0xFE), (0.0, 0x00)):
+        assert o.e4m3_from_double(v) == c, (v, c)
+
+
+def fp8_case(seed=3, D=16, Hq=4, Hkv=2, lens=(23, 5, 9)):
+    """case_tiny with E4M3 caches (random codes, NaN codes avoided) and
+    power-of-two head scales, different per head."""
+    c = case_tiny(dtype=O.BF16, seed=seed, D=D, Hq=Hq, Hkv=Hkv, lens=lens)
+    rng = np.random.default_rng(seed + 100)
+    shape = c["k_cache"].shape
+    k = rng.integers(0, 256, size=shape).astype(np.uint8)
+    v = rng.integers(0, 256, size=shape).astype(np.uint8)
+    for a in (k, v):
+        a[(a & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    c.update(k_cache=k, v_cache=v, dtype=O.FP8)
+    c["k_scale"] = np.exp2(rng.integers(-6, 3, Hkv)).astype(np.float32)
+    c["v_scale"] = np.exp2(rng.integers(-6, 3, Hkv)).astype(np.float32)
+    return c
+
+
+def pin_fp8_decode_is_the_decode_of_the_scaled_values(o: O.Oracle):
+    """A cache of E4M3 codes with power-of-two head scales is the fp32 cache
+    of the decoded values times the scales (exact in fp32): the same outputs
+    bit for bit; a head scale doubled doubles that head's outputs (V) or
+    equals a query doubled (K)."""
+    import torch
+    c = fp8_case()
+    out, lse = o.attn_decode(**c)
+    dec = lambda a: torch.from_numpy(a).view(torch.float8_e4m3fn).float().numpy()
+    f = dict(c)
+    f.pop("k_scale"), f.pop("v_scale")
+    f.update(dtype=O.F32, q=wl.storage_to_f64(c["q"], "bf16").astype(np.float32),
+             k_cache=dec(c["k_cache"]) * c["k_scale"][:, None, None],
+             v_cache=dec(c["v_cache"]) * c["v_scale"][:, None, None])
+    out32, lse32 = o.attn_decode(**f)
+    assert np.array_equal(out, out32) and np.array_equal(lse, lse32)
+    g = dict(c, v_scale=c["v_scale"] * 2)
+    out2, lse2 = o.attn_decode(**g)
+    assert np.array_equal(out2, 2 * out) and np.array_equal(lse2, lse)
+
+
+def pin_fp8_commit(o: O.Oracle):
+    """E4M3 commit: delta 0 keeps every key value, values are copied as codes, and
+    a rotated key is the E4M3 neighbour of the exact rotation (of the decoded
+    key) nearest to it."""
+    c = fp8_case(D=16)
+    k, v = c["k_cache"], c["v_cache"]
+    for delta in (0, 37):
+        kd, vd, ex = o.block_commit(dtype=O.FP8, rope_theta=1e4, k_src=k, v_src=v, src_begin=0,
+                                    n_tokens=5, k_dst=k, v_dst=v, dst_offset=40, pos_delta=delta,
+                                    want_exact=True)
+        assert np.array_equal(vd[:, 40:45], v[:, 0:5])
+        dec = np.vectorize(o.e4m3_to_double)
+        if delta == 0:  # the same values (a zero may change its sign: -0 - -0 = +0)
+            assert np.array_equal(dec(kd[:, 40:45]), dec(k[:, 0:5]))
+            nz = dec(k[:, 0:5]) != 0
+            assert np.array_equal(kd[:, 40:45][nz], k[:, 0:5][nz])
+        x = np.stack([np.stack([o.rope(dec(k[h, j]), 1e4, float(delta)) for j in range(5)])
+                      for h in range(k.shape[0])])
+        assert np.array_equal(x, ex)
+        got = dec(kd[:, 40:45])
+        # the nearest code: no finite code is closer to the exact value
+        grid = np.array(sorted({o.e4m3_to_double(b) for b in range(256)
+                                if not np.isnan(o.e4m3_to_double(b))}))
+        xs = np.clip(x, -448, 448)
+        best = np.min(np.abs(grid[None, :] - xs.reshape(-1, 1)), axis=1).reshape(xs.shape)
+        assert np.all(np.abs(got - xs) <= best + 0.0)
+
+
 ALL_PINS = [
     pin_rope_golden_freqs, pin_rope_complex, pin_rope_group, pin_textbook_single_block,
     pin_identity_block_vs_brute, pin_q_zero_mean, pin_permutation_invariance, pin_one_hot_exact,
     pin_gqa_mapping, pin_empty_view, pin_combined_layout, pin_commit_placement_and_copy,
     pin_commit_rotation, pin_commit_single_worker_invariance, pin_bf16_rounding, pin_view_limits,
+    pin_e4m3_codes, pin_fp8_decode_is_the_decode_of_the_scaled_values, pin_fp8_commit,
 ]

@@ -15,6 +15,8 @@ MUTANTS = {
     7: "commit places tokens in reverse order",
     8: "commit rotates by -delta",
     9: "a limited entry leaves out its last visible token",
+    10: "E4M3 exponent bias off by one",
+    11: "E4M3 keys scaled by another head's scale",
 }
 
 
