@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--chunk", type=int, default=0,
                    help="T > 0: T query tokens per worker, each seeing its own block up to its own "
                         "token (hw_views_chunked + hw_attn_plan_limited)")
+    p.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                   help="fp8: the K/V pools as E4M3 codes with per-kv-head scales "
+                        "(hw_attn_decode_planned_fp8)")
     p.add_argument("--commit-all", action="store_true",
                    help="C4: every worker's finished block joins the history each step, all in "
                         "one hw_block_commit_many launch (the common block gets room for them)")
@@ -228,6 +231,10 @@ def main():
         L = min(L, args.layers)
     lens, starts = w.block_lengths(), w.block_starts()
     chunk = args.chunk
+    fp8 = args.kv == "fp8"
+    if fp8:
+        assert not (args.append or args.unplanned or chunk), "--kv fp8 runs planned decodes"
+        assert w.dtype == "bf16" and w.head_dim == 128, "E4M3 caches: the bf16 head_dim-128 shapes"
     if chunk > 0:
         assert not (args.append or args.unplanned), "--chunk runs planned decodes without appends"
         vb, vo, vl, qp = api.views_chunked(args.layout, lens, w.n_problems, w.n_workers, chunk)
@@ -239,17 +246,24 @@ def main():
                                 head_dim=w.head_dim, n_blocks=w.n_blocks,
                                 max_view_blocks=w.n_workers + 1, capacity=w.capacity, dtype=tdt,
                                 rope_theta=w.rope_theta, scale=w.scale, device=dev,
-                                view_limits=chunk > 0)
+                                view_limits=chunk > 0, kv_fp8=fp8)
     sess.set_metadata(starts, lens, vb, vo, qp)
     qs, ks, vs = [], [], []
+    kscale, vscale = [], []  # E4M3: per layer, the per-kv-head scales
     commit = w.commit_tokens > 0 and args.config == "C4"
     if commit:
         # one [layers][Hkv][cap][D] pool per K and V, so that one commit launch
         # covers every layer
-        k_all = torch.empty((L, w.n_kv_heads, w.capacity, w.head_dim), dtype=tdt, device=dev)
+        k_all = torch.empty((L, w.n_kv_heads, w.capacity, w.head_dim),
+                            dtype=torch.uint8 if fp8 else tdt, device=dev)
         v_all = torch.empty_like(k_all)
     for l in range(L):
         q, k, v = wl.draw_device_layer(w, l, dev)
+        if fp8:  # the layer's pools packed as E4M3 codes, one scale per kv head
+            k, ksc = wl.e4m3_pack(k, lens, starts)
+            v, vsc = wl.e4m3_pack(v, lens, starts)
+            kscale.append(ksc)
+            vscale.append(vsc)
         if chunk > 0:  # one query per chunk token
             gq = torch.Generator(device=dev)
             gq.manual_seed(7000 + l)
@@ -302,6 +316,9 @@ def main():
             if append:
                 sess.append_decode_planned(qsrc[l], new_k[l], new_v[l], ks[l], vs[l], out=osrc[l],
                                            lse=lsrc[l], stream=stream)
+            elif planned and fp8:
+                sess.decode_planned_fp8(qsrc[l], ks[l], vs[l], kscale[l], vscale[l], out=osrc[l],
+                                        lse=lsrc[l], stream=stream)
             elif planned:
                 sess.decode_planned(qsrc[l], ks[l], vs[l], out=osrc[l], lse=lsrc[l], stream=stream)
             else:
@@ -375,13 +392,17 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t = float(tt.item())
 
-    commit_bytes = w.commit_bytes_per_layer() * L * (w.n_workers if commit_all else 1) if commit else 0
-    step_bytes = w.kv_bytes_per_layer() * calls_per_step + commit_bytes
+    # algorithmic bytes: E4M3 codes are one byte where bf16 takes two
+    div = 2 if fp8 else 1
+    kv_layer = w.kv_bytes_per_layer() // div
+    commit_bytes = (w.commit_bytes_per_layer() // div * L * (w.n_workers if commit_all else 1)
+                    if commit else 0)
+    step_bytes = kv_layer * calls_per_step + commit_bytes
     per_step = t / args.steps
     gbs_rank = step_bytes / per_step / 1e9
     value = gbs_rank * world  # replicas: every rank streams its own copy
     per_launch = per_step / calls_per_step
-    achieved = w.kv_bytes_per_layer() / per_launch / 1e9
+    achieved = kv_layer / per_launch / 1e9
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["hbm_gbs"])
 
@@ -461,19 +482,22 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 kv, bf16 q" if fp8 else w.dtype,
+        "data": "synthetic",
         "config": {
             "workload": w.name, "layers_per_step": calls_per_step, "problems": w.n_problems,
             "workers": w.n_workers, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
             "head_dim": w.head_dim, "kv_tokens_per_layer": w.kv_tokens(),
             "kv_bytes_per_step": step_bytes, "commit_bytes_per_step": commit_bytes,
-            "parallelism": f"replicas x{world}", "layout": args.layout,
+            "parallelism": f"replicas x{world}", "layout": args.layout, "kv": args.kv,
             "query_rows": n_rows, "chunk": chunk if chunk > 0 else None,
             "mode": "eager" if graph is None else "cuda-graph",
             "calls": ("hw_attn_plan_append once per step + hw_attn_append_decode_planned per layer "
                       "(each worker's new token written, then decoded)" if append else
                       f"hw_attn_plan_limited once per step + hw_attn_decode_planned per layer "
                       f"({chunk}-token chunks, causal within each worker's own block)" if chunk > 0 else
+                      "hw_attn_plan once per step + hw_attn_decode_planned_fp8 per layer (E4M3 "
+                      "K/V codes, per-kv-head scales)" if fp8 else
                       "hw_attn_plan once per step + hw_attn_decode_planned per layer" if planned
                       else "hw_attn_decode per layer"),
             "l2": "inputs larger than L2: each step reads every layer's own KV pools "
@@ -484,7 +508,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": (measured_traffic(kernel, "qwq32b_w4")
-                                 if args.config == "C3" and planned else None),
+                                 if args.config == "C3" and planned and not fp8 else None),
                      "peak_kind": peak_kind,
                      "kernel": f"{'hw_attn_decode_planned' if planned else 'hw_attn_decode'} ({kernel})",
                      "per_launch": "step time / layers per step (the plan launch included)"},
@@ -492,7 +516,7 @@ def main():
         "clocks": clk.summary(),
         "e2e": e2e,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and chunk == 0:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and chunk == 0 and not fp8:
         line["cpu_baseline"] = timed_oracle(w, qs, ks, vs, starts, lens, vb, vo, qp)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libhogwild.so")
 
 HW_OK = 0
-HW_F32, HW_BF16 = 0, 1
+HW_F32, HW_BF16, HW_FP8_E4M3 = 0, 1, 2
 HW_DESC_VIEW_LIMITS = 1
 STATUS = {0: "HW_OK", -1: "HW_ERR_INVALID", -2: "HW_ERR_UNSUPPORTED", -3: "HW_ERR_WORKSPACE",
           -4: "HW_ERR_CAPACITY", -5: "HW_ERR_OVERLAP", -6: "HW_ERR_CUDA", -7: "HW_ERR_DEVICE"}
@@ -26,7 +26,7 @@ DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMA
 
 # every symbol the header declares
 EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode",
-           "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_plan_limited", "hw_attn_plan_append",
+           "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_decode_planned_fp8", "hw_attn_plan_limited", "hw_attn_plan_append",
            "hw_attn_append_decode_planned", "hw_plan_export", "hw_attn_decode_noalloc",
            "hw_block_commit", "hw_block_commit_many", "hw_workspace_status", "hw_views_combined",
            "hw_views", "hw_views_chunked", "hw_last_cuda_error", "hw_status_string"]
@@ -77,6 +77,7 @@ def lib(path: Optional[str] = None):
     L.hw_attn_decode.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12 + [ctypes.c_size_t, _P]
     L.hw_attn_plan.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 7 + [ctypes.c_size_t, _P]
     L.hw_attn_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 6 + [ctypes.c_size_t, _P]
+    L.hw_attn_decode_planned_fp8.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]
     L.hw_attn_plan_limited.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]
     L.hw_attn_plan_append.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]
     L.hw_attn_append_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]
@@ -181,6 +182,17 @@ def attn_decode_planned(desc: AttnDesc, q, k_cache, v_cache, out, lse, workspace
                                       _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                                       _stream(stream))
     _check("hw_attn_decode_planned", st)
+    return st
+
+
+def attn_decode_planned_fp8(desc: AttnDesc, q, k_cache, v_cache, k_scale, v_scale, out, lse,
+                            workspace, workspace_bytes: int, stream=None) -> int:
+    """hw_attn_decode_planned_fp8: one layer over E4M3 caches with per-kv-head
+    scales, against the plan in the workspace."""
+    st = lib().hw_attn_decode_planned_fp8(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse),
+                                          _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check("hw_attn_decode_planned_fp8", st)
     return st
 
 

@@ -71,17 +71,22 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 // TMA map of one bf16 pool [Hkv][capacity][128]: boxes of 128 tokens x 64
 // elements (128 bytes, the 128-byte swizzle span), one head at a time.
 // Tokens past the capacity read as zeros.
-static bool make_pool_map(CUtensorMap *m, const void *pool, int64_t capacity, int n_kv_heads) {
+// A [Hkv][capacity][128] pool as 128-token tiles of 128 bytes per row,
+// 128-byte swizzled: bf16 in two boxes of 64 elements, E4M3 in one of 128.
+static bool make_pool_map(CUtensorMap *m, const void *pool, int64_t capacity, int n_kv_heads,
+                          bool e4m3 = false) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t cap = capacity > 0 ? static_cast<cuuint64_t>(capacity) : 1;
+  const cuuint64_t esz = e4m3 ? 1 : 2;
   cuuint64_t dims[3] = {128, cap, static_cast<cuuint64_t>(n_kv_heads)};
-  cuuint64_t strides[2] = {128 * 2, cap * 128 * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTcTile), 1};
+  cuuint64_t strides[2] = {128 * esz, cap * 128 * esz};
+  cuuint32_t box[3] = {e4m3 ? 128u : 64u, static_cast<cuuint32_t>(kTcTile), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Upper bound on the CTAs of any decode launch: slots are sized for it.
@@ -145,10 +150,11 @@ static int check_desc(const hw_attn_desc *d) {
     return HW_ERR_INVALID;
   if (d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->n_q_heads % d->n_kv_heads != 0)
     return HW_ERR_INVALID;
-  if (d->dtype != HW_F32 && d->dtype != HW_BF16) return HW_ERR_INVALID;
+  if (d->dtype != HW_F32 && d->dtype != HW_BF16 && d->dtype != HW_FP8_E4M3) return HW_ERR_INVALID;
   if (!(d->rope_theta > 1.0) || !std::isfinite(d->rope_theta)) return HW_ERR_INVALID;
   if (!std::isfinite(d->scale)) return HW_ERR_INVALID;
   if (d->head_dim != 64 && d->head_dim != 128) return HW_ERR_UNSUPPORTED;
+  if (d->dtype == HW_FP8_E4M3 && d->head_dim != 128) return HW_ERR_UNSUPPORTED;
   if (d->n_blocks > HW_MAX_BLOCKS) return HW_ERR_UNSUPPORTED;
   if (d->n_q_heads > HW_MAX_Q_HEADS) return HW_ERR_UNSUPPORTED;
   if (d->max_view_blocks > HW_MAX_VIEW_BLOCKS) return HW_ERR_UNSUPPORTED;
@@ -220,8 +226,9 @@ static void fill_args(DecodeArgs &a, const hw_attn_desc *d, const WorkspaceLayou
 }
 
 static bool tensor_core_path(const hw_attn_desc *d) {
-  return d->dtype == HW_BF16 && d->head_dim == 128;
+  return (d->dtype == HW_BF16 || d->dtype == HW_FP8_E4M3) && d->head_dim == 128;
 }
+static bool e4m3(const hw_attn_desc *d) { return d->dtype == HW_FP8_E4M3; }
 
 // One decode launch: metadata from the caller (plan null) or from the
 // workspace copies with the step's plan.
@@ -232,10 +239,13 @@ static int decode_common(const hw_attn_desc *d, const void *q, const void *k_cac
                          void *out, float *lse, void *workspace, const WorkspaceLayout &L,
                          int max_ctas, void *stream, const int32_t *append_block = nullptr,
                          const int32_t *append_pos = nullptr, const void *k_new = nullptr,
-                         const void *v_new = nullptr, const int32_t *view_limit = nullptr) {
+                         const void *v_new = nullptr, const int32_t *view_limit = nullptr,
+                         const float *k_scale = nullptr, const float *v_scale = nullptr) {
   DecodeArgs a;
   fill_args(a, d, L, workspace);
   a.view_limit = view_limit;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.append_block = append_block;
   a.append_pos = append_pos;
   a.k_new = k_new;
@@ -266,8 +276,8 @@ static int decode_common(const hw_attn_desc *d, const void *q, const void *k_cac
     std::memset(&km, 0, sizeof km);
     std::memset(&vm, 0, sizeof vm);
     if (have_pool) {
-      if (!make_pool_map(&km, k_cache, d->cache_capacity, d->n_kv_heads) ||
-          !make_pool_map(&vm, v_cache, d->cache_capacity, d->n_kv_heads))
+      if (!make_pool_map(&km, k_cache, d->cache_capacity, d->n_kv_heads, e4m3(d)) ||
+          !make_pool_map(&vm, v_cache, d->cache_capacity, d->n_kv_heads, e4m3(d)))
         return cuda_fail(cudaErrorInvalidValue);
     }
     e = launch_decode_tc(a, km, vm, sms, s);
@@ -278,6 +288,25 @@ static int decode_common(const hw_attn_desc *d, const void *q, const void *k_cac
     e = launch_decode_simt(a, d->dtype, ctas, s);
   }
   return e == cudaSuccess ? HW_OK : cuda_fail(e);
+}
+
+// hw_attn_decode_planned and its E4M3 form, after their own checks.
+static int planned_impl(const hw_attn_desc *d, const void *q, const void *k_cache,
+                        const void *v_cache, const float *k_scale, const float *v_scale, void *out,
+                        float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+  if (d->n_rows == 0) return HW_OK;
+  if (!q || !out) return HW_ERR_INVALID;
+  if (d->n_blocks > 0 && d->cache_capacity > 0 && (!k_cache || !v_cache)) return HW_ERR_INVALID;
+  WorkspaceLayout L;
+  int max_ctas = 0;
+  const int st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
+  if (st != HW_OK) return st;
+  const MetaCopies m = meta_copies(*d, L, workspace);
+  const uint8_t *plan = static_cast<const uint8_t *>(workspace) + L.plan_off;
+  return decode_common(d, q, k_cache, v_cache, m.block_start, m.block_len, m.view_block,
+                       m.view_offset, m.q_pos, m.q_to_kv, plan, out, lse, workspace, L, max_ctas,
+                       stream, nullptr, nullptr, nullptr, nullptr,
+                       limited(d) ? m.view_limit : nullptr, k_scale, v_scale);
 }
 
 }  // namespace hw
@@ -292,6 +321,7 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
   int st = check_desc(d);
   if (st != HW_OK) return st;
   if (limited(d)) return HW_ERR_UNSUPPORTED;  // limits come with a plan
+  if (e4m3(d)) return HW_ERR_UNSUPPORTED;     // E4M3 caches: planned, with their scales
   if (d->n_rows == 0) return HW_OK;
   if (!q || !out || !q_pos) return HW_ERR_INVALID;
   if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
@@ -318,6 +348,7 @@ static int plan_impl(const hw_attn_desc *d, const int32_t *block_start, const in
   if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
   if (d->n_blocks > 0 && (!block_start || !block_len)) return HW_ERR_INVALID;
   if ((append_block || view_limit) && !tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
+  if (append_block && e4m3(d)) return HW_ERR_UNSUPPORTED;
   if (limited(d) != (view_limit != nullptr)) return view_limit ? HW_ERR_INVALID : HW_ERR_UNSUPPORTED;
   WorkspaceLayout L;
   int max_ctas = 0;
@@ -383,19 +414,21 @@ int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_c
                            size_t workspace_bytes, void *stream) {
   int st = check_desc(d);
   if (st != HW_OK) return st;
-  if (d->n_rows == 0) return HW_OK;
-  if (!q || !out) return HW_ERR_INVALID;
-  if (d->n_blocks > 0 && d->cache_capacity > 0 && (!k_cache || !v_cache)) return HW_ERR_INVALID;
-  WorkspaceLayout L;
-  int max_ctas = 0;
-  st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
+  if (e4m3(d)) return HW_ERR_UNSUPPORTED;  // hw_attn_decode_planned_fp8 takes the scales
+  return planned_impl(d, q, k_cache, v_cache, nullptr, nullptr, out, lse, workspace,
+                      workspace_bytes, stream);
+}
+
+int hw_attn_decode_planned_fp8(const hw_attn_desc *d, const void *q, const void *k_cache,
+                               const void *v_cache, const float *k_scale, const float *v_scale,
+                               void *out, float *lse, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+  int st = check_desc(d);
   if (st != HW_OK) return st;
-  const MetaCopies m = meta_copies(*d, L, workspace);
-  const uint8_t *plan = static_cast<const uint8_t *>(workspace) + L.plan_off;
-  return decode_common(d, q, k_cache, v_cache, m.block_start, m.block_len, m.view_block,
-                       m.view_offset, m.q_pos, m.q_to_kv, plan, out, lse, workspace, L, max_ctas,
-                       stream, nullptr, nullptr, nullptr, nullptr,
-                       limited(d) ? m.view_limit : nullptr);
+  if (!e4m3(d)) return HW_ERR_INVALID;
+  if (d->n_rows > 0 && (!k_scale || !v_scale)) return HW_ERR_INVALID;
+  return planned_impl(d, q, k_cache, v_cache, k_scale, v_scale, out, lse, workspace,
+                      workspace_bytes, stream);
 }
 
 int hw_plan_export(const hw_attn_desc *d, const void *workspace, size_t workspace_bytes,
@@ -429,7 +462,7 @@ int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const vo
                                   void *stream) {
   int st = check_desc(d);
   if (st != HW_OK) return st;
-  if (limited(d)) return HW_ERR_UNSUPPORTED;
+  if (limited(d) || e4m3(d)) return HW_ERR_UNSUPPORTED;
   if (d->n_rows == 0) return HW_OK;
   if (!tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
   if (!q || !out || !k_new || !v_new) return HW_ERR_INVALID;
@@ -455,14 +488,14 @@ static int commit_impl(int32_t dtype, int32_t n_layers, int32_t n_kv_heads, int3
                        int64_t src_capacity, void *k_dst, void *v_dst, int64_t dst_capacity,
                        int32_t n, const int32_t *src_begin, const int32_t *n_tokens,
                        const int32_t *dst_offset, const int32_t *pos_delta, void *stream) {
-  if (dtype != HW_F32 && dtype != HW_BF16) return HW_ERR_INVALID;
+  if (dtype != HW_F32 && dtype != HW_BF16 && dtype != HW_FP8_E4M3) return HW_ERR_INVALID;
   if (n < 0 || n > HW_MAX_COMMITS) return HW_ERR_INVALID;
   if (n > 0 && (!src_begin || !n_tokens || !dst_offset || !pos_delta)) return HW_ERR_INVALID;
   if (n_layers < 0 || n_kv_heads <= 0 || src_capacity < 0 || dst_capacity < 0) return HW_ERR_INVALID;
   for (int c = 0; c < n; ++c)
     if (n_tokens[c] < 0 || src_begin[c] < 0 || dst_offset[c] < 0) return HW_ERR_INVALID;
   if (!(rope_theta > 1.0) || !std::isfinite(rope_theta)) return HW_ERR_INVALID;
-  const int esz = dtype == HW_F32 ? 4 : 2;
+  const int esz = dtype == HW_F32 ? 4 : dtype == HW_FP8_E4M3 ? 1 : 2;
   const int epv = 16 / esz;
   if (head_dim <= 0 || head_dim > 128 || head_dim % (2 * epv) != 0) return HW_ERR_UNSUPPORTED;
   int64_t tokens = 0;

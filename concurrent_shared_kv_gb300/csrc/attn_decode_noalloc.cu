@@ -59,7 +59,8 @@ extern "C" int hw_attn_decode_noalloc(const hw_attn_desc *d, const void *q, cons
                                       const int32_t *q_to_kv, void *out, float *lse,
                                       void *stream) {
   if (!d) return HW_ERR_INVALID;
-  if (d->flags & HW_DESC_VIEW_LIMITS) return HW_ERR_UNSUPPORTED;  // limits come with a plan
+  // view limits and E4M3 caches come with a plan
+  if ((d->flags & HW_DESC_VIEW_LIMITS) || d->dtype == HW_FP8_E4M3) return HW_ERR_UNSUPPORTED;
   size_t need = 0;
   int st = hw_attn_decode_workspace_size(d, &need);
   if (st != HW_OK) return st;

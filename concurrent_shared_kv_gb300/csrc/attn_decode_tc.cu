@@ -26,6 +26,8 @@
 // kernel costs stream time whatever its N, so fewer, wider products pay.)
 #include <cuda.h>
 
+#include <cuda_fp8.h>
+
 #include <cfloat>
 #include <climits>
 
@@ -57,6 +59,32 @@ constexpr uint32_t kSCols = 2 * kN;           // S buffer: S_hi [0,32), S_lo [32
 constexpr uint32_t kTmemCols = 256;           // S0 [0,64)  S1 [64,128)  O0 [128,160)  O1 [160,192)
 constexpr uint32_t kColO = 2 * kSCols;        // segment k accumulates in O[k & 1]
 constexpr float kLazy = 8.f;                  // rescale only when the max grows by > 2^8
+
+// E4M3 caches.  A stage holds the tile's K codes ([128 rows][128 codes],
+// 128-B swizzled; P takes their place once QK has completed), then its V as
+// f16 in the two boxes of the bf16 layout - the V codes land in the upper box
+// and the softmax warps widen them in place.  48 KB a stage, four in the ring
+// (the same 192 KB).  QK runs as kind::f8f6f4 on the codes against the
+// rotated queries split into four E4M3 parts (N = 128: S = S0 + S1/16 +
+// S2/256 + S3/4096, about 16 significant bits, like the bf16 path's hi + lo),
+// PV as kind::f16 on the widened V and an f16 P.  TMEM: S 2 x 128 columns,
+// O 2 x 32 (512 allocated).
+constexpr uint32_t kF8Box = 128 * 128;
+constexpr uint32_t kF8StageBytes = kF8Box + 2 * kBox;
+constexpr int kMaxStages = 4;
+constexpr int kF8Parts = 4;
+template <bool kFp8>
+struct Ring {
+  static constexpr int NS = kFp8 ? kMaxStages : kStages;                 // stages
+  static constexpr uint32_t SB = kFp8 ? kF8StageBytes : kStageBytes;     // bytes per stage
+  static constexpr uint32_t SC = kFp8 ? kF8Parts * kN : kSCols;          // S columns per buffer
+  static constexpr uint32_t CO = 2 * SC;                                 // first O column
+  static constexpr uint32_t VOFF = kFp8 ? kF8Box : 2 * kBox;             // V lo box in a stage
+  static constexpr uint32_t TC = kFp8 ? 512 : kTmemCols;                 // TMEM columns
+};
+static_assert(Ring<true>::NS * Ring<true>::SB <= kStages * kStageBytes, "E4M3 ring");
+static_assert(Ring<true>::CO + 2 * kN <= Ring<true>::TC, "E4M3 TMEM columns");
+static_assert(kF8Parts * kN * 128 <= kQBytes, "E4M3 query parts fit the Q~ buffer");
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
 constexpr int kPre = 4;  // slots of query-side segment metadata
@@ -103,14 +131,17 @@ struct TcSmem {
   float msave[2][kN];     // per segment parity: the reference maxima
   int32_t abort_flag;
   int32_t tiles_done;  // tiles whose P the softmax warps have written (progress only)
-  uint8_t tflags[kStages];  // per stage: the tile starts (1) / ends (2) its segment
+  uint8_t tflags[kMaxStages];  // per stage: the tile starts (1) / ends (2) its segment
   int32_t plan_ok;     // the plan (own or loaded) is usable
   uint32_t tmem_base;
-  alignas(8) uint64_t k_full[kStages];
-  uint64_t v_full[kStages], kv_empty[kStages];
+  float q_mul;         // E4M3: the current segment's score factor (Q~ part scale x k_scale)
+  float v_mul[4];      // E4M3: per segment mod 4, the v_scale of its kv head
+  int32_t qmax[8];     // E4M3: per query-warp maxima |Q~| (ordered ints)
+  alignas(8) uint64_t k_full[kMaxStages];
+  uint64_t v_full[kMaxStages], kv_empty[kMaxStages];
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full[kStages];  // P of the stage's tile written (the softmax may run ahead)
+  uint64_t p_full[kMaxStages];  // P of the stage's tile written (the softmax may run ahead)
   uint64_t p_empty, mma_done;
   uint64_t o_full[2], o_empty[2];  // per O buffer: segment done / epilogue read it
   uint64_t rec_ready[4];           // per segment mod 4: records written, arrivals due
@@ -200,6 +231,35 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&p);
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&p);
+}
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// Two E4M3 codes (low byte first) as f16x2, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -242,11 +302,18 @@ __device__ __forceinline__ TileRef tile_ref(const PlanCore &P, int n_blocks, int
   return t;
 }
 
+template <bool kFp8>
+__device__ __forceinline__ uint8_t *stage_ptr(TcSmem &S, int s) {
+  return S.stage[0] + s * Ring<kFp8>::SB;
+}
+
 // Streams the CTA's tiles through the ring.  The first n_first come decoded
 // from the plan, so that the ring fills without waiting on the unit
 // arithmetic; the others are decoded while their stage is still busy.
+template <bool kFp8>
 __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
                          const CUtensorMap *tv, int64_t u0, int64_t u1, bool appending) {
+  constexpr int NS = Ring<kFp8>::NS;
   const uint64_t pol = policy_evict_first();
   const int n_first = S.cp.n_first;
   // the first tile holding a new token is loaded only once the tokens are
@@ -254,7 +321,7 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
   const int app_tile = appending ? S.cp.app_tile : -1;
   int i = 0;
   for (int64_t u = u0; u < u1; ++u, ++i) {
-    const int s = i % kStages;
+    const int s = i % NS;
     // the tile's coordinates first, so that only the copy waits for the stage
     TileRef t;
     if (i < n_first) {
@@ -264,12 +331,20 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
     } else {
       t = tile_ref(S.ps.plan, a.n_blocks, u, u0, u1);
     }
-    uint8_t *st = S.stage[s];
-    if (i >= kStages && !spin_or_abort(S, a, &S.kv_empty[s], ((i / kStages) & 1) ^ 1)) break;
+    uint8_t *st = stage_ptr<kFp8>(S, s);
+    if (i >= NS && !spin_or_abort(S, a, &S.kv_empty[s], ((i / NS) & 1) ^ 1)) break;
     if (i == app_tile && !spin_or_abort(S, a, &S.app_bar, 0)) break;
     // read by the MMA thread once the stage's copies are seen complete (the
     // arrive below releases this store)
     S.tflags[s] = t.flags;
+    if constexpr (kFp8) {
+      // K codes at the stage's start, V codes into the upper V box
+      mbar_arrive_expect_tx(&S.k_full[s], kF8Box);
+      tma_load_3d(st, tk, &S.k_full[s], 0, t.row, t.h, pol);
+      mbar_arrive_expect_tx(&S.v_full[s], kF8Box);
+      tma_load_3d(st + kF8Box + kBox, tv, &S.v_full[s], 0, t.row, t.h, pol);
+      continue;
+    }
     mbar_arrive_expect_tx(&S.k_full[s], 2 * kBox);
     tma_load_3d(st, tk, &S.k_full[s], 0, t.row, t.h, pol);
     tma_load_3d(st + kBox, tk, &S.k_full[s], 64, t.row, t.h, pol);
@@ -278,9 +353,9 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
     tma_load_3d(st + 3 * kBox, tv, &S.v_full[s], 64, t.row, t.h, pol);
   }
   // no copy may still be landing in shared memory when the CTA retires
-  for (int j = (i > kStages ? i - kStages : 0); j < i; ++j) {
-    mbar_wait(&S.k_full[j % kStages], (j / kStages) & 1);
-    mbar_wait(&S.v_full[j % kStages], (j / kStages) & 1);
+  for (int j = (i > NS ? i - NS : 0); j < i; ++j) {
+    mbar_wait(&S.k_full[j % NS], (j / NS) & 1);
+    mbar_wait(&S.v_full[j % NS], (j / NS) & 1);
   }
 }
 
@@ -292,37 +367,48 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
 // the producer (tflags), and the operand descriptors are a base plus a
 // constant offset per k-step (the start address is the descriptor's low
 // field, 14 bits of address >> 4: shared addresses stay below 2^18).
+template <bool kFp8>
 __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0, int64_t u1) {
-  constexpr uint32_t idesc_qk = idesc_bf16(128, kSCols, 0, 0);  // K tile, [Q~hi; Q~lo]: K-major
-  constexpr uint32_t idesc_pv = idesc_bf16(128, kN, 1, 1);      // V tile, P: both MN-major
+  using R = Ring<kFp8>;
+  constexpr int NS = R::NS;
+  // QK: K tile, [Q~hi; Q~lo] (bf16) or the four E4M3 parts of Q~: K-major.
+  // PV: V tile, P: both MN-major, bf16 or f16.
+  constexpr uint32_t idesc_qk = kFp8 ? idesc_e4m3(128, R::SC, 0, 0) : idesc_bf16(128, R::SC, 0, 0);
+  constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(128, kN, 1, 1) : idesc_bf16(128, kN, 1, 1);
   const int n = static_cast<int>(u1 - u0);
   const uint32_t stage0 = smem_u32(S.stage[0]), qbase = smem_u32(S.q);
   const uint64_t a_qk = smem_desc(stage0, 16, 1024, kSw128);    // + (stage, k-step) offset >> 4
   const uint64_t b_qk = smem_desc(qbase, 16, 1024, kSw128);
-  const uint64_t a_pv = smem_desc(stage0 + 2 * kBox, kBox, 1024, kSw128);
+  const uint64_t a_pv = smem_desc(stage0 + R::VOFF, kBox, 1024, kSw128);
   const uint64_t b_pv = smem_desc(stage0, 512, 512, kSw64);
   int seg_q = -1, seg_p = -1;
   auto qk = [&](int i) {
-    const int s = i % kStages, sb = i & 1;
-    if (!spin_or_abort(S, a, &S.k_full[s], (i / kStages) & 1)) return;
+    const int s = i % NS, sb = i & 1;
+    if (!spin_or_abort(S, a, &S.k_full[s], (i / NS) & 1)) return;
     const uint32_t flags = S.tflags[s];
     if (flags & 1) ++seg_q;
     if (!spin_or_abort(S, a, &S.s_empty[sb], ((i >> 1) & 1) ^ 1)) return;
     if ((flags & 1) && !spin_or_abort(S, a, &S.q_full, seg_q & 1)) return;
     tc_fence_after();
-    const uint64_t as = a_qk + ((s * kStageBytes) >> 4);
+    const uint64_t as = a_qk + ((s * R::SB) >> 4);
+    if constexpr (kFp8) {
 #pragma unroll
-    for (int k8 = 0; k8 < 8; ++k8) {  // 8 k-steps of 16 over d
-      const uint32_t ao = (k8 >> 2) * kBox + (k8 & 3) * 32, bo = (k8 >> 2) * kQHalf + (k8 & 3) * 32;
-      mma_bf16(tmem + sb * kSCols, as + (ao >> 4), b_qk + (bo >> 4), idesc_qk, k8 > 0);
+      for (int k4 = 0; k4 < 4; ++k4)  // 4 k-steps of 32 codes (32 bytes) over d
+        mma_f8(tmem + sb * R::SC, as + ((k4 * 32) >> 4), b_qk + ((k4 * 32) >> 4), idesc_qk, k4 > 0);
+    } else {
+#pragma unroll
+      for (int k8 = 0; k8 < 8; ++k8) {  // 8 k-steps of 16 over d
+        const uint32_t ao = (k8 >> 2) * kBox + (k8 & 3) * 32, bo = (k8 >> 2) * kQHalf + (k8 & 3) * 32;
+        mma_bf16(tmem + sb * R::SC, as + (ao >> 4), b_qk + (bo >> 4), idesc_qk, k8 > 0);
+      }
     }
     mma_commit(&S.s_full[sb]);
     if (flags & 2) mma_commit(&S.q_empty);
   };
   auto pv = [&](int i) {
-    const int s = i % kStages;
-    if (!spin_or_abort(S, a, &S.p_full[s], (i / kStages) & 1)) return;
-    if (!spin_or_abort(S, a, &S.v_full[s], (i / kStages) & 1)) return;
+    const int s = i % NS;
+    if (!spin_or_abort(S, a, &S.p_full[s], (i / NS) & 1)) return;
+    if (!spin_or_abort(S, a, &S.v_full[s], (i / NS) & 1)) return;
     const uint32_t flags = S.tflags[s];
     const bool first = flags & 1;
     if (first) ++seg_p;
@@ -331,10 +417,10 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
     // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart,
     // 8-token groups 1024 B apart.  P^T: MN-major, 32 heads = one 64-B atom,
     // 8-token groups 512 B apart, in the stage's K region.
-    const uint64_t as = a_pv + ((s * kStageBytes) >> 4), bs = b_pv + ((s * kStageBytes) >> 4);
+    const uint64_t as = a_pv + ((s * R::SB) >> 4), bs = b_pv + ((s * R::SB) >> 4);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      mma_bf16(tmem + kColO + (seg_p & 1) * kN, as + ((kk * 2048) >> 4), bs + ((kk * 1024) >> 4),
+      mma_bf16(tmem + R::CO + (seg_p & 1) * kN, as + ((kk * 2048) >> 4), bs + ((kk * 1024) >> 4),
                idesc_pv, !(first && kk == 0));
     mma_commit(&S.kv_empty[s]);
     mma_commit(&S.p_empty);
@@ -444,6 +530,80 @@ __device__ __forceinline__ void store_item(uint32_t qbase, int qi, int c, const 
   st_shared_v4(qbase + kQHalf + kQPart + off, v[3].x, v[3].y, v[3].z, v[3].w);   // lo, d 64-127
 }
 
+// E4M3 caches: the item's 16 rotated values (y[0..7]: d 8c..8c+7, y[8..15]:
+// d 64+8c..), scaled by scale * log2(e), before the segment's part scale is
+// known; the largest magnitude is returned.
+__device__ __forceinline__ float rot_item_f32(const DecodeArgs &a, const TcSmem &S, const QItem &it,
+                                              int c, float (&y)[16]) {
+  const uint32_t lo32[4] = {it.lo.x, it.lo.y, it.lo.z, it.lo.w};
+  const uint32_t hi32[4] = {it.hi.x, it.hi.y, it.hi.z, it.hi.w};
+  float mx = 0.f;
+#pragma unroll
+  for (int e2 = 0; e2 < 4; ++e2) {
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const float x0 = __uint_as_float(h2 ? (lo32[e2] & 0xffff0000u) : (lo32[e2] << 16));
+      const float x1 = __uint_as_float(h2 ? (hi32[e2] & 0xffff0000u) : (hi32[e2] << 16));
+      float cs, sn;
+      rope_cos_sin_fast(it.rel, S.ps.cache.phase[8 * c + 2 * e2 + h2], &cs, &sn);
+      const int j = 2 * e2 + h2;
+      y[j] = (x0 * cs - x1 * sn) * a.scale_log2;
+      y[8 + j] = (x1 * cs + x0 * sn) * a.scale_log2;
+      mx = fmaxf(mx, fmaxf(fabsf(y[j]), fabsf(y[8 + j])));
+    }
+  }
+  return mx;
+}
+
+// The power of two c with max / c < 448 (the largest E4M3 value): the
+// segment's Q~ parts hold y / c.
+__device__ __forceinline__ int part_exponent(float mx) {
+  int e = 0;
+  if (mx > 0.f) frexpf(mx * (1.f / 448.f), &e);
+  return e;
+}
+
+// The item as four E4M3 parts, z = y / c ~ a0 + a1/16 + a2/256 + a3/4096 (each
+// part the residual of the ones before, times 16), into Q~ rows 32 j + qi of
+// part j: 8 codes at byte 8c (d 8c..) and 8 at byte 64 + 8c (d 64 + 8c..),
+// 16-B chunks swizzled by qi % 8 like the bf16 buffer.
+__device__ __forceinline__ void store_item_e4m3(uint32_t qbase, int qi, int c, const float (&y)[16],
+                                                float inv_c) {
+  uint32_t w[kF8Parts][4];
+#pragma unroll
+  for (int j = 0; j < kF8Parts; ++j)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[j][k] = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // value pairs: y[2k], y[2k + 1]
+    float2 z = make_float2(y[2 * k] * inv_c, y[2 * k + 1] * inv_c);
+#pragma unroll
+    for (int j = 0; j < kF8Parts; ++j) {
+      const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(z, __NV_SATFINITE, __NV_E4M3);
+      w[j][k >> 1] |= static_cast<uint32_t>(q) << (16 * (k & 1));
+      if (j + 1 < kF8Parts) {
+        const uint32_t h = e4m3x2_to_f16x2(q);
+        z = make_float2((z.x - f16_lo(h)) * 16.f, (z.y - f16_hi(h)) * 16.f);
+      }
+    }
+  }
+  const uint32_t sub = 8u * (c & 1);
+#pragma unroll
+  for (int j = 0; j < kF8Parts; ++j) {
+    const int row = 32 * j + qi;
+    const uint32_t rb = qbase + row * 128;
+    st_shared_v2(rb + (((c >> 1) ^ (row & 7)) << 4) + sub, w[j][0], w[j][1]);
+    st_shared_v2(rb + (((4 + (c >> 1)) ^ (row & 7)) << 4) + sub, w[j][2], w[j][3]);
+  }
+}
+
+// Max over a warp of a non-negative float.
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // First unit after the segment that holds unit u.
 __device__ __forceinline__ int64_t next_segment(const PlanCore &P, int n_blocks, int64_t u) {
   const UnitPos x = unit_pos(P, n_blocks, u);
@@ -453,7 +613,7 @@ __device__ __forceinline__ int64_t next_segment(const PlanCore &P, int n_blocks,
 // Prologue of warps 2-7 (nt = 192), or of warps 2-5 alone (nt = 128) while warps 6-7
 // write the CTA's new tokens: the metadata of segment 0 (warp 2), then its
 // queries rotated into the Q~ buffer.
-template <bool kPlanned>
+template <bool kPlanned, bool kFp8>
 __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1, int nt) {
   const int t = threadIdx.x - kWarpSoft * 32;  // 0 .. nt-1
   const int w = t >> 5, lane = t & 31;
@@ -478,6 +638,35 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
   QItem q0, q1;
   if (t < n_items) load_item(a, X, t >> 3, t & 7, q0);
   if (t1 < n_items) load_item(a, X, t1 >> 3, t1 & 7, q1);
+  if constexpr (kFp8) {
+    // the segment's head scales, the largest |Q~| over all items, then parts
+    float ks = 1.f, vs = 1.f;
+    if (t == 0) {
+      const int h = unit_pos(S.ps.plan, a.n_blocks, u0).h;
+      ks = __ldg(a.k_scale + h);
+      vs = __ldg(a.v_scale + h);
+    }
+    float y0[16], y1[16], mx = 0.f;
+    if (t < n_items) mx = rot_item_f32(a, S, q0, t & 7, y0);
+    if (t1 < n_items) mx = fmaxf(mx, rot_item_f32(a, S, q1, t1 & 7, y1));
+    mx = warp_max_nonneg(mx);
+    if (lane == 0) S.qmax[w] = __float_as_int(mx);
+    sync();
+    for (int k = 0; k < nt / 32; ++k) mx = fmaxf(mx, __int_as_float(S.qmax[k]));
+    const int e = part_exponent(mx);
+    const float inv_c = ldexpf(1.f, -e);
+    if (t < n_items) store_item_e4m3(qbase, t >> 3, t & 7, y0, inv_c);
+    if (t1 < n_items) store_item_e4m3(qbase, t1 >> 3, t1 & 7, y1, inv_c);
+    if (t == 0) {
+      S.meta_nref = X.m.n_ref;
+      S.q_mul = ldexpf(ks, e);
+      S.v_mul[0] = vs;
+    }
+    fence_proxy_async_smem();
+    sync();
+    if (t == 0) mbar_arrive(&S.q_full);  // phase 0: segment 0
+    return;
+  }
   if (t < n_items) {
     uint4 v[4];
     rot_item(a, S, q0, t & 7, v);
@@ -572,7 +761,7 @@ __device__ void append_tokens(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_
 // warps' record stores sit on the path of the next rotated queries.  Last,
 // the metadata of segment j + 2 goes into the slot segment j - 2 vacated,
 // and its queries are prefetched into L2.
-template <bool kPlanned, bool kLimit>
+template <bool kPlanned, bool kLimit, bool kFp8>
 __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
   const int lane = threadIdx.x & 31, wq = tq >> 5;
@@ -649,17 +838,45 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       if ((tq >> 3) + 8 * k < nq) load_item(a, X, (tq >> 3) + 8 * k, tq & 7, raw[k]);
-    uint4 v[4][4];
+    if constexpr (kFp8) {
+      float ks = 1.f, vs = 1.f;
+      if (tq == 0) {
+        const int h = unit_pos(S.ps.plan, a.n_blocks, u).h;
+        ks = __ldg(a.k_scale + h);
+        vs = __ldg(a.v_scale + h);
+      }
+      float y[4][16], mx = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if ((tq >> 3) + 8 * k < nq) rot_item(a, S, raw[k], tq & 7, v[k]);
-    // The Q~ buffer and the hand-off metadata are free once segment seg-1's
-    // QK products completed and every softmax warp read the hand-off.
-    wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
-    if (tq == 0) S.meta_nref = X.m.n_ref;
+      for (int k = 0; k < 4; ++k)
+        if ((tq >> 3) + 8 * k < nq) mx = fmaxf(mx, rot_item_f32(a, S, raw[k], tq & 7, y[k]));
+      mx = warp_max_nonneg(mx);
+      if (lane == 0) S.qmax[6 + wq] = __float_as_int(mx);
+      sync();
+      mx = fmaxf(__int_as_float(S.qmax[6]), __int_as_float(S.qmax[7]));
+      const int e = part_exponent(mx);
+      const float inv_c = ldexpf(1.f, -e);
+      wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
+      if (tq == 0) {
+        S.meta_nref = X.m.n_ref;
+        S.q_mul = ldexpf(ks, e);
+        S.v_mul[seg & 3] = vs;
+      }
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if ((tq >> 3) + 8 * k < nq) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
+      for (int k = 0; k < 4; ++k)
+        if ((tq >> 3) + 8 * k < nq) store_item_e4m3(qbase, (tq >> 3) + 8 * k, tq & 7, y[k], inv_c);
+    } else {
+      uint4 v[4][4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if ((tq >> 3) + 8 * k < nq) rot_item(a, S, raw[k], tq & 7, v[k]);
+      // The Q~ buffer and the hand-off metadata are free once segment seg-1's
+      // QK products completed and every softmax warp read the hand-off.
+      wait_or_abort(S, a, &S.q_empty, (seg - 1) & 1);
+      if (tq == 0) S.meta_nref = X.m.n_ref;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if ((tq >> 3) + 8 * k < nq) store_item(qbase, (tq >> 3) + 8 * k, tq & 7, v[k]);
+    }
     fence_proxy_async_smem();
     sync();
     if (tq == 0) mbar_arrive(&S.q_full);
@@ -699,19 +916,26 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[kN], int lane) {
 // (m, l) of each query head -> partial records in the workspace.  Runs one
 // tile after the segment's end, when its last P.V product has (nearly always)
 // completed; the arrivals are left to the query warps.
+// (E4M3 caches: O times the v_scale of the segment's kv head.)
+template <bool kFp8>
 __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int seg, int b, int h,
-                                int nq, int ws, int lane, int row, NamedSync<1, 128> sync) {
+                                int nq, int ws, int lane, int row, NamedSync<1, 128> sync,
+                                float vmul) {
   wait_or_abort(S, a, &S.o_full[seg & 1], (seg >> 1) & 1);
   tc_fence_after();
   __syncwarp();
   uint32_t o[32];
-  tmem_ld32(tl + kColO + (seg & 1) * kN, o);
+  tmem_ld32(tl + Ring<kFp8>::CO + (seg & 1) * kN, o);
   tmem_wait_ld();
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(&S.o_empty[seg & 1]);
   sync();  // every warp's lsave of this segment is in place
   const int64_t slot = seg_id(a.n_blocks, b, h) + blockIdx.x;
+  if constexpr (kFp8) {
+#pragma unroll
+    for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * vmul);
+  }
 #pragma unroll
   for (int j = 0; j < kN; ++j)
     if (j < nq) record_ptr(a, slot, j)[row] = __uint_as_float(o[j]);
@@ -725,11 +949,40 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
   if (lane == 0) mbar_arrive(&S.rec_ready[seg & 3]);
 }
 
+// E4M3 V: row `row` of a stage's V codes (in the upper V box) widened to
+// f16 in the two V boxes, in place - the row's codes occupy exactly its row
+// of the upper box and are read whole before anything is written.  Rows past
+// the block end become zeros (their codes may be anything, NaN included).
+__device__ __forceinline__ void widen_v_row(uint32_t vbase, int row, bool keep) {
+  const uint32_t sw = row & 7;
+  const uint32_t src = vbase + kBox + row * 128;
+  uint4 in[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) in[c] = ld_shared_v4(src + ((c ^ sw) << 4));  // codes d 16c..16c+15
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t w[4] = {in[c].x, in[c].y, in[c].z, in[c].w};
+    uint32_t f[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f[2 * k] = keep ? e4m3x2_to_f16x2(w[k]) : 0u;
+      f[2 * k + 1] = keep ? e4m3x2_to_f16x2(w[k] >> 16) : 0u;
+    }
+    // d 16c.. is f16 chunk 2c of the 128 d: box c / 4, chunks (2c) % 8 and (2c + 1) % 8
+    const uint32_t dst = vbase + (c >> 2) * kBox + row * 128;
+    const uint32_t g = (2 * c) & 7;
+    st_shared_v4(dst + ((g ^ sw) << 4), f[0], f[1], f[2], f[3]);
+    st_shared_v4(dst + (((g + 1) ^ sw) << 4), f[4], f[5], f[6], f[7]);
+  }
+}
+
 // kLimit: the plan carries view limits, so a column may attend only part of
-// a block.
-template <bool kLimit>
+// a block.  kFp8: E4M3 caches (three S parts, the V codes widened here, P in
+// f16).
+template <bool kLimit, bool kFp8>
 __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0,
                              int64_t u1) {
+  using R = Ring<kFp8>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ws = warp - kWarpSoft;              // 0..3
   const int qd = warp & 3;                      // TMEM lane quadrant of this warp
@@ -753,6 +1006,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   // view limits of the segment: the fewest tokens a column attends, and the
   // count of column `lane` (broadcast to the others on the tiles that need it)
   int minlim = INT_MAX, lim_mine = INT_MAX;
+  float qmul = 1.f, vmul = 1.f, pend_vmul = 1.f;  // E4M3: score and output factors
   int pend = -1, pend_b = 0, pend_h = 0, pend_nq = 0;  // segment whose records are due
   for (int i = 0; i < n; ++i) {
     const int64_t u = u0 + i;
@@ -762,6 +1016,10 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       ++seg;
       wait_or_abort(S, a, &S.q_full, seg & 1);
       nq = min(S.meta_nref * G, kN);
+      if constexpr (kFp8) {
+        qmul = S.q_mul;
+        vmul = S.v_mul[seg & 3];
+      }
       if constexpr (kLimit) {
         // the segment's metadata stays in its slot until its records are out
         const SegQ &X = S.cp.pre[seg % kPre];
@@ -780,23 +1038,47 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       }
       m_mine = -FLT_MAX;
     }
-    const int sb = i & 1, s = i % kStages;
+    const int sb = i & 1, s = i % R::NS;
+    const int base = x.t * kT;  // the tile's first token in its block
+    const int valid = min(kT, S.ps.plan.len[x.b] - base);
+    const bool tok_ok = row < valid;
+    if constexpr (kFp8) {
+      // this thread's row of the tile's V, widened (fenced for the tensor
+      // cores with P below)
+      wait_or_abort(S, a, &S.v_full[s], (i / R::NS) & 1);
+      widen_v_row(smem_u32(stage_ptr<kFp8>(S, s)) + R::VOFF, row, tok_ok);
+    }
     wait_or_abort(S, a, &S.s_full[sb], (i >> 1) & 1);
     tc_fence_after();
     __syncwarp();
     uint32_t r[32], r2[32];
-    tmem_ld32(tl + sb * kSCols, r);        // S_hi
-    tmem_ld32(tl + sb * kSCols + kN, r2);  // S_lo
+    tmem_ld32(tl + sb * R::SC, r);        // S_hi (E4M3: part 0)
+    tmem_ld32(tl + sb * R::SC + kN, r2);  // S_lo (E4M3: part 1)
     tmem_wait_ld();
+    if constexpr (kFp8) {
+#pragma unroll
+      for (int j = 0; j < kN; ++j)
+        r[j] = __float_as_uint(__fmaf_rn(__uint_as_float(r2[j]), 0.0625f, __uint_as_float(r[j])));
+      tmem_ld32(tl + sb * R::SC + 2 * kN, r2);  // part 2
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < kN; ++j)
+        r[j] = __float_as_uint(__fmaf_rn(__uint_as_float(r2[j]), 0.00390625f, __uint_as_float(r[j])));
+      tmem_ld32(tl + sb * R::SC + 3 * kN, r2);  // part 3
+      tmem_wait_ld();
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.s_empty[sb]);
+    if constexpr (kFp8) {
 #pragma unroll
-    for (int j = 0; j < kN; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+      for (int j = 0; j < kN; ++j)
+        r[j] = __float_as_uint(__fmaf_rn(__uint_as_float(r2[j]), 0.000244140625f, __uint_as_float(r[j])) * qmul);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kN; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+    }
 
-    const int base = x.t * kT;  // the tile's first token in its block
-    const int valid = min(kT, S.ps.plan.len[x.b] - base);
-    const bool tok_ok = row < valid;
     float sc[kN];
     if (!kLimit || base + kT <= minlim) {
 #pragma unroll
@@ -848,11 +1130,11 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
         tc_fence_after();
         __syncwarp();
         uint32_t o[32];
-        tmem_ld32(tl + kColO + (seg & 1) * kN, o);
+        tmem_ld32(tl + R::CO + (seg & 1) * kN, o);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
-        tmem_st32(tl + kColO + (seg & 1) * kN, o);
+        tmem_st32(tl + R::CO + (seg & 1) * kN, o);
         tmem_wait_st();
         tc_fence_before();
       }
@@ -862,15 +1144,21 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     for (int j = 0; j < kN; j += 2) {
       const float p0 = (j < nq) ? ex2(sc[j] - m_run[j]) : 0.f;
       const float p1 = (j + 1 < nq) ? ex2(sc[j + 1] - m_run[j + 1]) : 0.f;
-      pk[j / 2] = pack_bf16(p0, p1);
       // the sum uses the same rounded weights the P.V product sees
-      l_part[j] += __uint_as_float(pk[j / 2] << 16);
-      l_part[j + 1] += __uint_as_float(pk[j / 2] & 0xffff0000u);
+      if constexpr (kFp8) {
+        pk[j / 2] = pack_f16(p0, p1);
+        l_part[j] += f16_lo(pk[j / 2]);
+        l_part[j + 1] += f16_hi(pk[j / 2]);
+      } else {
+        pk[j / 2] = pack_bf16(p0, p1);
+        l_part[j] += __uint_as_float(pk[j / 2] << 16);
+        l_part[j + 1] += __uint_as_float(pk[j / 2] & 0xffff0000u);
+      }
     }
-    if (valid < kT) {
+    if (!kFp8 && valid < kT) {
       // V rows past the block end may hold anything: zero them (p = 0 there,
       // but 0 * NaN would still poison the sum)
-      wait_or_abort(S, a, &S.v_full[s], (i / kStages) & 1);
+      wait_or_abort(S, a, &S.v_full[s], (i / R::NS) & 1);
       if (!tok_ok) {
         const uint32_t v0 = smem_u32(S.stage[s]) + 2 * kBox + row * 128;
 #pragma unroll
@@ -882,7 +1170,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     }
     // P row of this token: 32 heads = four 16-B chunks, 64-B swizzle, in the
     // K region of the tile's stage (QK of this tile has completed: s_full)
-    const uint32_t prow = smem_u32(S.stage[s]) + row * 64;
+    const uint32_t prow = smem_u32(stage_ptr<kFp8>(S, s)) + row * 64;
     const uint32_t swz = (row >> 1) & 3;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -893,7 +1181,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     if (threadIdx.x == kWarpSoft * 32) *reinterpret_cast<volatile int32_t *>(&S.tiles_done) = i + 1;
 
     if (pend >= 0) {  // records of the previous segment, one tile late
-      segment_records(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync);
+      segment_records<kFp8>(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync, pend_vmul);
       pend = -1;
     }
     if (last) {
@@ -908,17 +1196,20 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       pend_b = x.b;
       pend_h = x.h;
       pend_nq = nq;
+      pend_vmul = vmul;
     }
   }
-  if (pend >= 0) segment_records(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync);
+  if (pend >= 0)
+    segment_records<kFp8>(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync, pend_vmul);
 }
 
 // kPlanned: the step's plan is loaded (else built in-kernel); kAppend (with a
 // plan): the layer's new tokens are written first; kLimit (with a plan, no
-// appends): the plan carries view limits.  Each combination is its own
-// kernel, so that no path carries another's code (a second softmax loop in
-// the same kernel, even one never entered, cost the plain path 8 %).
-template <bool kPlanned, bool kAppend, bool kLimit>
+// appends): the plan carries view limits; kFp8 (with a plan alone): E4M3
+// caches with per-kv-head scales.  Each combination is its own kernel, so
+// that no path carries another's code (a second softmax loop in the same
+// kernel, even one never entered, cost the plain path 8 %).
+template <bool kPlanned, bool kAppend, bool kLimit, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
@@ -936,7 +1227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     tma_prefetch_desc(&tm_k);  // (kernel parameters)
     tma_prefetch_desc(&tm_v);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Ring<kFp8>::NS; ++s) {
       mbar_init(&S.p_full[s], 4);  // one per softmax warp
       mbar_init(&S.k_full[s], 1);
       mbar_init(&S.v_full[s], 1);
@@ -969,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
-    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_alloc(&S.tmem_base, Ring<kFp8>::TC);
     tmem_relinquish();
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid is complete
@@ -1036,18 +1327,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (u0 < u1) {
     const bool appending = kAppend && S.cp.app_n > 0;
     if (warp == kWarpTma) {
-      if (lane == 0) producer(a, S, &tm_k, &tm_v, u0, u1, appending);
+      if (lane == 0) producer<kFp8>(a, S, &tm_k, &tm_v, u0, u1, appending);
     } else if (warp == kWarpMma) {
-      if (lane == 0) mma_issuer(a, S, tmem, u0, u1);
+      if (lane == 0) mma_issuer<kFp8>(a, S, tmem, u0, u1);
     } else {
       if (appending && warp >= kWarpQ)
         append_tokens(a, S, u0, u1);
       else
-        query_prologue<kPlanned>(a, S, u0, u1, appending ? 128 : 192);
+        query_prologue<kPlanned, kFp8>(a, S, u0, u1, appending ? 128 : 192);
       if (warp < kWarpQ)
-        softmax_role<kLimit>(a, S, tmem, u0, u1);
+        softmax_role<kLimit, kFp8>(a, S, tmem, u0, u1);
       else
-        qprep<kPlanned, kLimit>(a, S, u0, u1);
+        qprep<kPlanned, kLimit, kFp8>(a, S, u0, u1);
     }
   } else if (!kPlanned) {
     plan_ranks(a, S.ps.cache, warp, lane, 0, 1);  // a CTA without units: ranks for the merge
@@ -1056,7 +1347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == kWarpMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, Ring<kFp8>::TC);
   }
   // the merge scratch lives in the tile buffers: every copy and MMA is done
   static_assert(sizeof(MergeSmem<8>) <= kStageBytes, "merge scratch must fit in a stage");
@@ -1238,12 +1529,13 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const C
   const size_t smem = decode_tc_smem_bytes();
   // planned launches run their own instantiations: without the plan-building
   // (and, without appends, the append) code the kernel is far smaller
-  const int which = !a.plan ? 0 : a.k_new ? 2 : a.view_limit ? 3 : 1;
-  void (*const kernels[4])(DecodeArgs, CUtensorMap, CUtensorMap) = {
-      decode_tc_kernel<false, false, false>, decode_tc_kernel<true, false, false>,
-      decode_tc_kernel<true, true, false>, decode_tc_kernel<true, false, true>};
+  const int which = !a.plan ? 0 : a.k_new ? 2 : a.view_limit ? 3 : a.k_scale ? 4 : 1;
+  void (*const kernels[5])(DecodeArgs, CUtensorMap, CUtensorMap) = {
+      decode_tc_kernel<false, false, false, false>, decode_tc_kernel<true, false, false, false>,
+      decode_tc_kernel<true, true, false, false>, decode_tc_kernel<true, false, true, false>,
+      decode_tc_kernel<true, false, false, true>};
   void (*kernel)(DecodeArgs, CUtensorMap, CUtensorMap) = kernels[which];
-  static bool configured[4] = {false, false, false, false};
+  static bool configured[5] = {false, false, false, false, false};
   if (!configured[which]) {
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));

@@ -9,7 +9,11 @@
 // 16-byte chunk of the first half of a key row and the matching chunk of the
 // second half (RoPE pairs i and i + D/2), so the rotation needs no exchange;
 // V moves as the same two 16-byte chunks.  cos/sin of delta * w_i are made
-// once per CTA in shared memory from the integer phase table.
+// once per CTA in shared memory from the integer phase table.  E4M3 pools are
+// rotated on their codes' values (a head's scale carries over unchanged) and
+// rounded back to the nearest code, saturating at 448.
+#include <cuda_fp8.h>
+
 #include "hw_device.cuh"
 
 namespace hw {
@@ -60,6 +64,38 @@ __device__ __forceinline__ uint4 rotate16<__nv_bfloat16>(const uint4 &lo, const 
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+struct E4M3 {  // storage tag: one E4M3 code
+  uint8_t code;
+};
+
+template <>
+__device__ __forceinline__ uint4 rotate16<E4M3>(const uint4 &lo, const uint4 &hi, const float *cs,
+                                                const float *sn, bool upper) {
+  const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w};
+  const uint32_t wh[4] = {hi.x, hi.y, hi.z, hi.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {  // two e4m3 pairs of the word
+      const __half2 l2(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wl[i] >> (16 * p)), __NV_E4M3));
+      const __half2 h2(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh[i] >> (16 * p)), __NV_E4M3));
+      const float2 xl = __half22float2(l2), xh = __half22float2(h2);
+      const int j = 4 * i + 2 * p;
+      float2 y;
+      y.x = upper ? __fmaf_rn(xh.x, cs[j], __fmul_rn(xl.x, sn[j]))
+                  : __fmaf_rn(xl.x, cs[j], -__fmul_rn(xh.x, sn[j]));
+      y.y = upper ? __fmaf_rn(xh.y, cs[j + 1], __fmul_rn(xl.y, sn[j + 1]))
+                  : __fmaf_rn(xl.y, cs[j + 1], -__fmul_rn(xh.y, sn[j + 1]));
+      const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+      word |= static_cast<uint32_t>(q) << (16 * p);
+    }
+    out[i] = word;
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 // Grid row c (blockIdx.y) commits range c; its CTAs stride over the range's
 // (layer, head, token, chunk) items.
 template <typename T>
@@ -104,7 +140,7 @@ __global__ void __launch_bounds__(kCommitThreads) block_commit_kernel(const __gr
 }
 
 cudaError_t launch_commit(const CommitArgs &a, int dtype, cudaStream_t s) {
-  const int epv = dtype == HW_F32 ? 4 : 8;
+  const int epv = dtype == HW_F32 ? 4 : dtype == HW_FP8_E4M3 ? 16 : 8;
   int64_t work = 0;
   for (int c = 0; c < a.n_commits; ++c)
     work += static_cast<int64_t>(a.n_layers) * a.n_kv_heads * a.n_tokens[c] * ((a.head_dim / 2) / epv);
@@ -118,6 +154,8 @@ cudaError_t launch_commit(const CommitArgs &a, int dtype, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(per > 0 ? per : 1), static_cast<unsigned>(a.n_commits));
   if (dtype == HW_F32)
     block_commit_kernel<float><<<grid, kCommitThreads, 0, s>>>(a);
+  else if (dtype == HW_FP8_E4M3)
+    block_commit_kernel<E4M3><<<grid, kCommitThreads, 0, s>>>(a);
   else
     block_commit_kernel<__nv_bfloat16><<<grid, kCommitThreads, 0, s>>>(a);
   return cudaGetLastError();

@@ -51,6 +51,8 @@ struct DecodeArgs {
   // or null: every entry sees its whole block.  At plan time the caller's
   // array, at decode time the plan's copy.
   const int32_t *view_limit;
+  // E4M3 caches: per kv head, the scale of its K and V codes (null: bf16 caches)
+  const float *k_scale, *v_scale;
   float scale_log2;   // softmax scale * log2(e): scores live in the log2 domain
   // RoPE phase increments: for pair i, the fraction of a turn per position,
   // frac(w_i / 2pi), as an unsigned 0.64 fixed-point number.  The angle of

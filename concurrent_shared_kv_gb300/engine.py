@@ -10,7 +10,8 @@ import torch
 
 from . import api
 
-DTYPES = {torch.float32: api.HW_F32, torch.bfloat16: api.HW_BF16}
+DTYPES = {torch.float32: api.HW_F32, torch.bfloat16: api.HW_BF16,
+          torch.uint8: api.HW_FP8_E4M3, torch.float8_e4m3fn: api.HW_FP8_E4M3}
 
 
 class DecodeSession:
@@ -19,13 +20,16 @@ class DecodeSession:
     def __init__(self, *, n_rows: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
                  n_blocks: int, max_view_blocks: int, capacity: int, dtype: torch.dtype,
                  rope_theta: float, scale: Optional[float] = None, device="cuda",
-                 view_limits: bool = False):
+                 view_limits: bool = False, kv_fp8: bool = False):
         """view_limits: the steps are planned with per-view-entry token limits
-        (plan_limited; decode_planned then applies them)."""
+        (plan_limited; decode_planned then applies them).  kv_fp8: the K and V
+        pools hold E4M3 codes with per-kv-head scales (decode_planned_fp8);
+        dtype is then that of q and out (bf16)."""
         self.device = torch.device(device)
         self.dtype = dtype
         self.desc = api.make_desc(n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks,
-                                  max_view_blocks, capacity, DTYPES[dtype], rope_theta,
+                                  max_view_blocks, capacity,
+                                  api.HW_FP8_E4M3 if kv_fp8 else DTYPES[dtype], rope_theta,
                                   head_dim ** -0.5 if scale is None else scale,
                                   flags=api.HW_DESC_VIEW_LIMITS if view_limits else 0)
         self.ws_bytes = api.attn_decode_workspace_size(self.desc)
@@ -117,6 +121,20 @@ class DecodeSession:
             lse = torch.empty((d.n_rows, d.n_q_heads), dtype=torch.float32, device=self.device)
         api.attn_decode_planned(d, q, k_cache, v_cache, out, lse, self.workspace, self.ws_bytes,
                                 stream=stream)
+        return out, lse
+
+    def decode_planned_fp8(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           k_scale: torch.Tensor, v_scale: torch.Tensor,
+                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           want_lse: bool = True, stream=None):
+        """One layer over E4M3 pools (codes, [Hkv][cap][D]) with float32 scales [Hkv]."""
+        d = self.desc
+        if out is None:
+            out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
+        if lse is None and want_lse:
+            lse = torch.empty((d.n_rows, d.n_q_heads), dtype=torch.float32, device=self.device)
+        api.attn_decode_planned_fp8(d, q, k_cache, v_cache, k_scale, v_scale, out, lse,
+                                    self.workspace, self.ws_bytes, stream=stream)
         return out, lse
 
     def device_flags(self) -> int:

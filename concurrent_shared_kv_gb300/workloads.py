@@ -204,3 +204,41 @@ def draw_device_layer(w: Workload, layer: int, device, poison: float = 0.0):
                 s0 = int(starts[p * (w.n_workers + 1)])
                 k[:, s0] = (k[:, s0].float() * 8.0).to(tdt)
     return q, k, v
+
+
+# ---------------------------------------------------------------------------
+# E4M3 caches: a pool's values packed as 8-bit codes with one scale per kv head
+# ---------------------------------------------------------------------------
+
+def e4m3_pack(pool, lens=None, starts=None):
+    """Pack a [Hkv][capacity][D] pool (float64 numpy or a torch tensor) as E4M3
+    codes with one scale per kv head: scale_h = max |x| over the head's
+    cached rows / 448 (the largest E4M3 value), code = x / scale_h rounded to
+    the nearest E4M3 value by torch's float8_e4m3fn cast.  lens/starts, when
+    given, restrict the maximum to the blocks' rows (slack rows are packed
+    too, clipped into range).  Returns (codes uint8, scales float32 [Hkv]),
+    numpy or torch like the input."""
+    assert torch is not None
+    is_np = isinstance(pool, np.ndarray)
+    t = torch.from_numpy(np.asarray(pool, np.float64)) if is_np else pool.float()
+    Hkv = t.shape[0]
+    if lens is not None:
+        mask = torch.zeros(t.shape[1], dtype=torch.bool, device=t.device)
+        for s, n in zip(starts, lens):
+            mask[int(s):int(s) + int(n)] = True
+        amax = t[:, mask].abs().reshape(Hkv, -1).amax(dim=1) if mask.any() else torch.zeros(Hkv, device=t.device)
+    else:
+        amax = t.abs().reshape(Hkv, -1).amax(dim=1)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).float()
+    z = (t / scale.to(t.dtype)[:, None, None]).clamp(-448.0, 448.0)
+    codes = z.float().to(torch.float8_e4m3fn).view(torch.uint8)
+    if is_np:
+        return codes.numpy(), scale.numpy()
+    return codes, scale
+
+
+def e4m3_values(codes) -> np.ndarray:
+    """Decoded E4M3 codes (float64), by torch's float8_e4m3fn."""
+    assert torch is not None
+    t = torch.from_numpy(np.ascontiguousarray(codes, np.uint8)) if isinstance(codes, np.ndarray) else codes
+    return t.view(torch.float8_e4m3fn).double().cpu().numpy()

@@ -56,7 +56,14 @@ typedef enum {
   HW_ERR_DEVICE = -7       /* device-side metadata check failed (hw_workspace_status) */
 } hw_status;
 
-typedef enum { HW_F32 = 0, HW_BF16 = 1 } hw_dtype;
+/*
+ * HW_FP8_E4M3: the K and V pools hold E4M3 codes (1 byte per element; a
+ * cached value is the code's value times its kv head's scale, k_scale[h] or
+ * v_scale[h]); q and out stay bf16.  head_dim 128; decoded by
+ * hw_attn_plan + hw_attn_decode_planned_fp8 and committed by hw_block_commit
+ * (the other decode calls return HW_ERR_UNSUPPORTED for it).
+ */
+typedef enum { HW_F32 = 0, HW_BF16 = 1, HW_FP8_E4M3 = 2 } hw_dtype;
 
 /* Device-side error bits reported by hw_workspace_status. */
 enum {
@@ -219,6 +226,20 @@ int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_c
  * (copied into the plan).  hw_attn_decode_planned then applies the limits.
  * bf16 with head_dim 128 only (HW_ERR_UNSUPPORTED otherwise).
  */
+/*
+ * hw_attn_decode_planned for HW_FP8_E4M3 caches (the survey's next steps:
+ * E4M3 KV storage with per-head scales): k_cache and v_cache hold E4M3
+ * codes, [Hkv][capacity][128] bytes; k_scale, v_scale (dev, float [Hkv]):
+ * a cached key or value is its code's value times its kv head's scale.  q,
+ * out and lse as in hw_attn_decode; the plan comes from hw_attn_plan with the
+ * same descriptor.  The result is attention over the decoded, scaled cache.
+ * HW_ERR_INVALID for another dtype or null scales.
+ */
+int hw_attn_decode_planned_fp8(const hw_attn_desc *d, const void *q, const void *k_cache,
+                               const void *v_cache, const float *k_scale, const float *v_scale,
+                               void *out, float *lse, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
 int hw_attn_plan_limited(const hw_attn_desc *d, const int32_t *block_start,
                          const int32_t *block_len, const int32_t *view_block,
                          const int32_t *view_offset, const int32_t *view_limit,

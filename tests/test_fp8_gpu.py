@@ -1,0 +1,133 @@
+"""GPU parity of E4M3 KV caches with per-kv-head scales (hw_attn_plan +
+hw_attn_decode_planned_fp8, and hw_block_commit on E4M3 pools, through the C
+ABI) against the float64 oracle on the same codes and scales.  The caches'
+quantisation is part of the inputs - both sides attend the decoded, scaled
+codes - so the bar is the bf16 path's: the kernel's own arithmetic (queries
+in four E4M3 parts, about 16 significant bits; P in f16) is no coarser than
+the bf16 path's (queries in two bf16 parts; P in bf16).  A first build with
+three parts (about 13 bits) missed the lse bar on large queries."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from concurrent_shared_kv_gb300 import api, engine
+from concurrent_shared_kv_gb300 import workloads as wl
+from tests import harness as H
+from tests.test_parity_gpu import small
+
+pytestmark = pytest.mark.gpu
+
+
+class Fp8Case:
+    """A workload's bf16 queries and its caches packed as E4M3 codes."""
+
+    def __init__(self, c: H.Case, q=None, poison_code=None):
+        self.c = c
+        w = c.w
+        self.q = c.q if q is None else q
+        lens, starts = c.block_len, c.block_start
+        self.kc, self.ks = wl.e4m3_pack(c.k, lens, starts)
+        self.vc, self.vs = wl.e4m3_pack(c.v, lens, starts)
+        if poison_code is not None:  # rows outside every block: never read
+            used = torch.zeros(self.kc.shape[1], dtype=torch.bool, device=self.kc.device)
+            for s_, n in zip(starts, lens):
+                used[int(s_):int(s_) + int(n)] = True
+            self.kc[:, ~used] = poison_code
+            self.vc[:, ~used] = poison_code
+
+    def run(self):
+        c, w = self.c, self.c.w
+        s = engine.DecodeSession(n_rows=self.q.shape[0], n_q_heads=w.n_q_heads,
+                                 n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
+                                 n_blocks=len(c.block_len), max_view_blocks=c.view_block.shape[1],
+                                 capacity=c.capacity, dtype=torch.bfloat16, rope_theta=w.rope_theta,
+                                 scale=w.scale, kv_fp8=True)
+        s.set_metadata(c.block_start, c.block_len, c.view_block, c.view_offset, c.q_pos, c.q_to_kv)
+        s.plan()
+        out, lse = s.decode_planned_fp8(self.q, self.kc, self.vc, self.ks, self.vs)
+        torch.cuda.synchronize()
+        assert s.device_flags() == 0
+        return out, lse, s
+
+    def oracle(self, rows=None):
+        c, w = self.c, self.c.w
+        return oracle.get().attn_decode(
+            q=H.to_storage_np(self.q), k_cache=self.kc.cpu().numpy(), v_cache=self.vc.cpu().numpy(),
+            k_scale=self.ks.cpu().numpy(), v_scale=self.vs.cpu().numpy(), block_start=c.block_start,
+            block_len=c.block_len, view_block=c.view_block, view_offset=c.view_offset, q_pos=c.q_pos,
+            n_kv_heads=w.n_kv_heads, rope_theta=w.rope_theta, scale=w.scale, dtype=oracle.FP8,
+            q_to_kv=c.q_to_kv, rows=rows)
+
+    def check(self, what, rows=None):
+        out, lse, s = self.run()
+        ro, rl = self.oracle(rows)
+        H.compare("bf16", out, lse, ro, rl, rows=rows, what=what)
+        return out, lse
+
+
+def test_fp8_small_edges():
+    # ragged tiles (129, 64, 1, 128, 33), an empty block, two problems
+    w = small(P=2, W=3, common=(300, 77), blocks=((129, 64, 1), (128, 0, 33)))
+    Fp8Case(H.host_case(w)).check("fp8 small")
+
+
+def test_fp8_codes_outside_the_blocks_are_never_read():
+    w = small(extra=37, blocks=((129, 64, 10),))
+    Fp8Case(H.host_case(w), poison_code=0x7F).check("fp8 NaN codes in the slack")
+
+
+@pytest.mark.parametrize("qscale", [1e-3, 1.0, 300.0])
+def test_fp8_query_magnitudes(qscale):
+    # the query parts' scale is a power of two per segment: tiny and large
+    # queries, and one q head far smaller than the others of its segment
+    w = small(P=1, W=3, common=(700,), blocks=((129, 64, 40),))
+    c = H.host_case(w)
+    q = (c.q.float() * qscale)
+    q[:, 1] *= 1e-3
+    Fp8Case(c, q=q.to(torch.bfloat16)).check(f"fp8 q x{qscale}")
+
+
+def test_fp8_qwq32b_w4_layer():
+    w = wl.qwq32b_w4()
+    Fp8Case(H.device_case(w, 0)).check("fp8 C3 layer", rows=[0, 1, 2, 3])
+
+
+def test_fp8_serving_ragged_many_segments_per_cta():
+    w = wl.serve_ragged()
+    Fp8Case(H.device_case(w)).check("fp8 serving ragged", rows=list(range(0, 4)) + list(range(60, 64)))
+
+
+def test_fp8_is_deterministic():
+    w = small(P=2, W=3, common=(3000, 77), blocks=((129, 64, 1), (128, 5, 33)))
+    f = Fp8Case(H.host_case(w))
+    o1, l1, _ = f.run()
+    o2, l2, _ = f.run()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+def test_fp8_commit_against_the_oracle():
+    # two layers x 8 heads: 300 tokens rotated by 1000 positions into another
+    # range of the same pool, codes rounded from the fp32 rotation
+    rng = np.random.default_rng(4)
+    L_, Hkv, cap, D = 2, 8, 2000, 128
+    x = rng.standard_normal((L_ * Hkv, cap, D))
+    codes, _ = wl.e4m3_pack(x)
+    k = torch.from_numpy(codes).view(L_, Hkv, cap, D).cuda()
+    v = torch.from_numpy(codes[::-1].copy()).view(L_, Hkv, cap, D).cuda()
+    k0, v0 = k.cpu().numpy().copy(), v.cpu().numpy().copy()
+    engine.block_commit(k, v, 100, 300, k, v, 1500, 1000, 1e6)
+    torch.cuda.synchronize()
+    kg, vg = k.cpu().numpy(), v.cpu().numpy()
+    for l in range(L_):
+        kd, vd = oracle.get().block_commit(dtype=oracle.FP8, rope_theta=1e6, k_src=k0[l], v_src=v0[l],
+                                           src_begin=100, n_tokens=300, k_dst=k0[l], v_dst=v0[l],
+                                           dst_offset=1500, pos_delta=1000)
+        assert np.array_equal(vg[l], vd)
+        same = kg[l] == kd
+        # the kernel rotates in fp32: a value next to a rounding boundary may
+        # land on the neighbouring code; every other code is the oracle's
+        assert same.mean() > 0.995, same.mean()
+        got, want = wl.e4m3_values(kg[l][~same]), wl.e4m3_values(kd[~same])
+        step = np.maximum(np.abs(want), 2.0 ** -6) * 2.0 ** -3
+        assert np.all(np.abs(got - want) <= step * 1.0001)
