@@ -1008,9 +1008,10 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   int minlim = INT_MAX, lim_mine = INT_MAX;
   float qmul = 1.f, vmul = 1.f, pend_vmul = 1.f;  // E4M3: score and output factors
   int pend = -1, pend_b = 0, pend_h = 0, pend_nq = 0;  // segment whose records are due
+  UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u0);  // then advanced unit by unit
   for (int i = 0; i < n; ++i) {
     const int64_t u = u0 + i;
-    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u);
+    if (i > 0) unit_pos_next(S.ps.plan, a.n_blocks, x);
     const bool first = seg_first_unit(x, u, u0), last = seg_last_unit(x, u, u1);
     if (first) {
       ++seg;

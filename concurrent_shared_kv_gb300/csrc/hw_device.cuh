@@ -432,6 +432,25 @@ __device__ __forceinline__ UnitPos unit_pos(const PlanCore &P, int n_blocks, int
   return x;
 }
 
+// unit_pos of u + 1 from that of u (units run block after block, skipping
+// blocks without tiles, then head after head): O(1) where unit_pos costs a
+// division and a binary search over the blocks.
+__device__ __forceinline__ void unit_pos_next(const PlanCore &P, int n_blocks, UnitPos &x) {
+  if (++x.t < x.tiles) return;
+  x.t = 0;
+  int b = x.b + 1;
+  while (b < n_blocks && P.tiles[b] == 0) ++b;
+  if (b == n_blocks) {  // the next head, from its first block with tiles
+    ++x.h;
+    b = 0;
+    while (b < n_blocks && P.tiles[b] == 0) ++b;
+    if (b == n_blocks) b = 0;  // (no units at all: never reached)
+  }
+  x.b = b;
+  x.tiles = P.tiles[b];
+  x.seg_first = static_cast<int64_t>(x.h) * P.UH + P.ubase[b];
+}
+
 // Start weight of unit u (strictly increasing in u).
 __device__ __forceinline__ int64_t unit_weight(const PlanCore &P, int n_blocks, int64_t u) {
   const int h = static_cast<int>(div_nn(u, P.UH));
