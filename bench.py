@@ -507,8 +507,9 @@ def main():
         "worker_tokens_per_s_per_layer": n_rows / per_launch,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": (measured_traffic(kernel, "qwq32b_w4")
-                                 if args.config == "C3" and planned and not fp8 else None),
+                     "traffic": (measured_traffic(kernel, "qwq32b_w4_fp8" if fp8 else "qwq32b_w4")
+                                 if args.config == "C3" and planned and not (append or chunk)
+                                 and args.layout == "combined" else None),
                      "peak_kind": peak_kind,
                      "kernel": f"{'hw_attn_decode_planned' if planned else 'hw_attn_decode'} ({kernel})",
                      "per_launch": "step time / layers per step (the plan launch included)"},
