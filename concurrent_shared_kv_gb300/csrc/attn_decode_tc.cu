@@ -1,6 +1,6 @@
-// attn_decode_tc.cu - concurrent decode attention for bf16 caches with
-// head_dim 128 on the sm_100 tensor cores (tcgen05 + TMEM), K/V tiles staged
-// by TMA.
+// attn_decode_tc.cu - concurrent decode attention for bf16 (or E4M3, see
+// Ring<true>) caches with head_dim 128 on the sm_100 tensor cores (tcgen05 +
+// TMEM), K/V tiles staged by TMA.
 //
 // The path is HBM-bound: every K/V tile is read once and serves every query
 // head that attends it (all workers' view references to the block times the
@@ -23,7 +23,13 @@
 // QK multiplies the K tile with hi and lo stacked as one 64-column operand:
 // one pass of 8 MMAs reads each K slice once, S_hi and S_lo land in separate
 // TMEM columns and the softmax adds them in fp32.  (Each tcgen05.mma of this
-// kernel costs stream time whatever its N, so fewer, wider products pay.)
+// kernel costs stream time whatever its N - about 85 ns for M = 128, measured,
+// and independent accumulators do not shorten it - so fewer, wider products
+// pay.)
+//
+// Variants (template parameters of decode_tc_kernel): a plan loaded or built
+// in-kernel; the step's new tokens written first (appends); per-view-entry
+// token limits (query chunks); E4M3 caches with per-kv-head scales.
 #include <cuda.h>
 
 #include <cuda_fp8.h>
