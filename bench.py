@@ -152,6 +152,25 @@ def measured_traffic(kernel: str, workload_key: str):
     return int(kv["dram_bytes_per_launch"])
 
 
+def max_over_ranks(t: float, device) -> float:
+    """The slowest rank's time (every rank gets it): replicas run the same
+    work, so the job takes as long as its slowest one.  Identity without a
+    process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return t
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def replica_value(units_per_rank: float, t_max: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas: all ranks' units over the
+    slowest rank's time."""
+    return units_per_rank * world / t_max
+
+
 def reference_arm(args):
     """The float64 oracle on the host cores, on the same workload and metric."""
     import numpy as np
@@ -387,10 +406,7 @@ def main():
 
     with ClockSampler(local) as clk:
         t = run_timed(args.steps)
-    if world > 1:
-        tt = torch.tensor([t], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(t, dev)
 
     # algorithmic bytes: E4M3 codes are one byte where bf16 takes two
     div = 2 if fp8 else 1
@@ -400,7 +416,7 @@ def main():
     step_bytes = kv_layer * calls_per_step + commit_bytes
     per_step = t / args.steps
     gbs_rank = step_bytes / per_step / 1e9
-    value = gbs_rank * world  # replicas: every rank streams its own copy
+    value = replica_value(step_bytes / 1e9, per_step, world)  # replicas: each streams its own copy
     per_launch = per_step / calls_per_step
     achieved = kv_layer / per_launch / 1e9
     peaks, peak_kind = measured_peaks()
@@ -468,7 +484,8 @@ def main():
             stream.synchronize()
         t_e2e = (time.perf_counter() - t0) / e2e_steps
         assert torch.isfinite(o_host.float()).all(), "e2e outputs"
-        e2e_gbs = step_bytes / t_e2e / 1e9 * world
+        t_e2e = max_over_ranks(t_e2e, dev)
+        e2e_gbs = replica_value(step_bytes / 1e9, t_e2e, world)
         return {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
                 "how": "per step: metadata + packed queries H2D from pinned memory, the step's "
