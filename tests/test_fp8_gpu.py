@@ -131,3 +131,32 @@ def test_fp8_commit_against_the_oracle():
         got, want = wl.e4m3_values(kg[l][~same]), wl.e4m3_values(kd[~same])
         step = np.maximum(np.abs(want), 2.0 ** -6) * 2.0 ** -3
         assert np.all(np.abs(got - want) <= step * 1.0001)
+
+
+def test_fp8_interleaved_layout():
+    # views [common, own]: each worker block is read for one row only
+    w = small(P=2, W=3, common=(1000, 77), blocks=((129, 64, 1), (128, 5, 33)))
+    c = H.host_case(w, views=api.views("interleaved", w.block_lengths(), w.n_problems, w.n_workers))
+    Fp8Case(c).check("fp8 interleaved")
+
+
+def test_fp8_commit_many_equals_the_commits_in_turn():
+    # three finished steps of one layer committed in one launch
+    rng = np.random.default_rng(6)
+    Hkv, cap, D = 4, 3000, 128
+    codes, _ = wl.e4m3_pack(rng.standard_normal((Hkv, cap, D)))
+    k = torch.from_numpy(codes).cuda()
+    v = torch.from_numpy(codes[:, ::-1].copy()).cuda()
+    k0, v0 = k.cpu().numpy().copy(), v.cpu().numpy().copy()
+    commits = [(0, 200, 1000, 1000), (200, 150, 1200, 1200), (350, 77, 1350, 1350)]
+    engine.block_commit_many(k, v, commits, k, v, 1e6)
+    torch.cuda.synchronize()
+    kd, vd = k0, v0
+    for sb, n, dst, delta in commits:
+        kd, vd = oracle.get().block_commit(dtype=oracle.FP8, rope_theta=1e6, k_src=k0, v_src=v0,
+                                           src_begin=sb, n_tokens=n, k_dst=kd, v_dst=vd,
+                                           dst_offset=dst, pos_delta=delta)
+    kg, vg = k.cpu().numpy(), v.cpu().numpy()
+    assert np.array_equal(vg, vd)
+    same = kg == kd
+    assert same.mean() > 0.998, same.mean()
