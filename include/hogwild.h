@@ -227,8 +227,9 @@ int hw_attn_decode_planned(const hw_attn_desc *d, const void *q, const void *k_c
  * bf16 with head_dim 128 only (HW_ERR_UNSUPPORTED otherwise).
  */
 /*
- * hw_attn_decode_planned for HW_FP8_E4M3 caches (the survey's next steps:
- * E4M3 KV storage with per-head scales): k_cache and v_cache hold E4M3
+ * hw_attn_decode_planned for HW_FP8_E4M3 caches (E4M3 KV storage with
+ * per-head scales; the omica.com.cn article on Hogwild! Inference, section 6,
+ * names FP8 attention as future work): k_cache and v_cache hold E4M3
  * codes, [Hkv][capacity][128] bytes; k_scale, v_scale (dev, float [Hkv]):
  * a cached key or value is its code's value times its kv head's scale.  q,
  * out and lse as in hw_attn_decode; the plan comes from hw_attn_plan with the

@@ -34,8 +34,8 @@
  *  - one max-subtracted softmax over the concatenation of all view blocks;
  *    an empty view gives out = 0 and lse = -inf;
  *  - GQA: q head h reads kv head h / (Hq/Hkv) unless a map is given;
- *  - FP8 caches (the survey's next steps name E4M3 storage with per-head
- *    scales; the pages only mention FP8 attention as future work): K and V
+ *  - FP8 caches (the omica.com.cn article, section 6, only names FP8
+ *    attention as future work; storage as E4M3 with per-head scales): K and V
  *    hold E4M3 codes, a cached element is its decoded value times its kv
  *    head's scale, queries stay bf16.
  *
