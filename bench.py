@@ -152,6 +152,16 @@ def measured_traffic(kernel: str, workload_key: str):
     return int(kv["dram_bytes_per_launch"])
 
 
+def workload_config(w, config: str, layout: str = "combined", layers=None) -> dict:
+    """The keys that name the timed workload, the same in both arms' lines."""
+    if layers is None:
+        layers = w.layers if config != "C5" else 64  # C5: one layer timed x64
+    return {"workload": w.name, "layers_per_step": layers,
+            "problems": w.n_problems, "workers": w.n_workers, "q_heads": w.n_q_heads,
+            "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+            "kv_tokens_per_layer": w.kv_tokens(), "layout": layout}
+
+
 def max_over_ranks(t: float, device) -> float:
     """The slowest rank's time (every rank gets it): replicas run the same
     work, so the job takes as long as its slowest one.  Identity without a
@@ -208,9 +218,10 @@ def reference_arm(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": t_layer * w.layers * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": t_layer * workload_config(w, args.config)["layers_per_step"] * 1e3,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "layers": w.layers},
+        "config": workload_config(w, args.config),
         "worker_tokens_per_s_per_layer": w.n_rows / t_layer,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
@@ -502,11 +513,9 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 kv, bf16 q" if fp8 else w.dtype,
         "data": "synthetic",
         "config": {
-            "workload": w.name, "layers_per_step": calls_per_step, "problems": w.n_problems,
-            "workers": w.n_workers, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
-            "head_dim": w.head_dim, "kv_tokens_per_layer": w.kv_tokens(),
+            **workload_config(w, args.config, args.layout, calls_per_step),
             "kv_bytes_per_step": step_bytes, "commit_bytes_per_step": commit_bytes,
-            "parallelism": f"replicas x{world}", "layout": args.layout, "kv": args.kv,
+            "parallelism": f"replicas x{world}", "kv": args.kv,
             "query_rows": n_rows, "chunk": chunk if chunk > 0 else None,
             "mode": "eager" if graph is None else "cuda-graph",
             "calls": ("hw_attn_plan_append once per step + hw_attn_append_decode_planned per layer "
