@@ -291,3 +291,36 @@ def test_deterministic_and_metadata_reuse():
     assert not torch.equal(a, b)
     ro, rl = c1.run_oracle()
     H.compare("bf16", b, lb, ro, rl, what="layer 1 through a reused session")
+
+
+def test_maximum_sizes():
+    # at the interface's limits at once: 256 blocks in the pool (HW_MAX_BLOCKS),
+    # one row whose view holds 64 of them (HW_MAX_VIEW_BLOCKS, some empty),
+    # 256 query heads over 8 kv heads (HW_MAX_Q_HEADS; G = 32 fills the
+    # tile's 32 columns on every block), planned and unplanned
+    rng = np.random.default_rng(23)
+    nb, V, Hq, Hkv, D = 256, 64, 256, 8, 128
+    lens = rng.integers(0, 90, size=nb).astype(np.int32)
+    lens[[3, 17]] = 0
+    w = wl.Workload("max", "bf16", 1, 1, Hq, Hkv, D, 1e6, 1, [0], [[0]], seed=5)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int32)
+    cap = int(lens.sum()) + 8
+    k = wl.to_storage(rng.standard_normal((Hkv, cap, D)), "bf16")
+    v = wl.to_storage(rng.standard_normal((Hkv, cap, D)), "bf16")
+    q = wl.to_storage(rng.standard_normal((1, Hq, D)), "bf16")
+    chosen = np.sort(rng.choice(nb, size=V, replace=False))
+    chosen[:2] = [3, 17]  # two empty blocks in the view
+    chosen = np.sort(chosen)
+    vb = chosen[None, :].astype(np.int32)
+    vo = np.concatenate([[0], np.cumsum(lens[chosen])[:-1]])[None, :].astype(np.int32)
+    qp = np.array([int(lens[chosen].sum())], np.int32)
+    c = H.Case(w, H.from_storage_np(q, "bf16"), H.from_storage_np(k, "bf16"),
+               H.from_storage_np(v, "bf16"), block_start=starts, block_len=lens, views=(vb, vo, qp))
+    ro, rl = c.run_oracle()
+    out, lse, s = c.run_gpu()
+    assert s.device_flags() == 0
+    H.compare("bf16", out, lse, ro, rl, what="maximum sizes")
+    s.plan()
+    out2, lse2 = s.decode_planned(c.q, c.k, c.v)
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16)) and torch.equal(lse2, lse)
