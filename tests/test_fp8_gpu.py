@@ -160,3 +160,23 @@ def test_fp8_commit_many_equals_the_commits_in_turn():
     assert np.array_equal(vg, vd)
     same = kg == kd
     assert same.mean() > 0.998, same.mean()
+
+
+def test_fp8_full_tile_of_columns():
+    # 256 query heads over 8 kv heads: every block's tile carries 32 columns,
+    # the Q~ buffer all four parts x 32 rows; one row viewing 20 blocks
+    rng = np.random.default_rng(29)
+    nb, Hq, Hkv, D = 20, 256, 8, 128
+    lens = rng.integers(1, 300, size=nb).astype(np.int32)
+    w = wl.Workload("fp8 columns", "bf16", 1, 1, Hq, Hkv, D, 1e6, 1, [0], [[0]], seed=6)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int32)
+    cap = int(lens.sum())
+    k = wl.to_storage(rng.standard_normal((Hkv, cap, D)), "bf16")
+    v = wl.to_storage(rng.standard_normal((Hkv, cap, D)), "bf16")
+    q = wl.to_storage(rng.standard_normal((1, Hq, D)), "bf16")
+    vb = np.arange(nb, dtype=np.int32)[None, :]
+    vo = np.concatenate([[0], np.cumsum(lens)[:-1]])[None, :].astype(np.int32)
+    qp = np.array([cap], np.int32)
+    c = H.Case(w, H.from_storage_np(q, "bf16"), H.from_storage_np(k, "bf16"),
+               H.from_storage_np(v, "bf16"), block_start=starts, block_len=lens, views=(vb, vo, qp))
+    Fp8Case(c).check("fp8 32 columns")
