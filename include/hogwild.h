@@ -166,7 +166,8 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
  * In a decode step every layer attends the same views: the block table,
  * the views and positions are per step, only q, K and V change per layer.
  * hw_attn_plan copies the metadata (same arguments and layouts as
- * hw_attn_decode) into `workspace` and, for the bf16 head_dim-128 kernel,
+ * hw_attn_decode) into `workspace` and, for the tensor-core kernel (bf16 or
+ * E4M3 caches, head_dim 128),
  * precomputes the work split, each CTA's first segments and the merge lists
  * there.  hw_attn_decode_planned then runs one layer against that plan, with
  * results identical to hw_attn_decode on the same metadata.  The plan holds a
@@ -176,6 +177,11 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
  * a missing plan sets HW_DEV_BAD_PLAN, see hw_workspace_status, and leaves
  * out and lse untouched).  Both enqueue work on `stream` only; the plan is
  * seen by calls enqueued after it on the same stream.
+ *
+ * A descriptor with HW_DESC_VIEW_LIMITS is planned by hw_attn_plan_limited
+ * instead (hw_attn_plan returns HW_ERR_UNSUPPORTED for it); HW_FP8_E4M3
+ * caches are planned here and decoded by hw_attn_decode_planned_fp8
+ * (hw_attn_decode_planned returns HW_ERR_UNSUPPORTED for them).
  *
  * Not in the Hogwild! notes, which describe one attention call per layer:
  * this is the usual split of a decode kernel's scheduling from its runs.
