@@ -539,7 +539,8 @@ def main():
                      "peak_kind": peak_kind,
                      "kernel": f"{'hw_attn_decode_planned' if planned else 'hw_attn_decode'} ({kernel})",
                      "per_launch": "step time / layers per step (the plan launch included)"},
-        "gpu_launches": (calls_per_step + (1 if planned else 0) + (1 if commit else 0)) * args.steps,
+        # every rank's launches in the timed region (replicas: the same on each)
+        "gpu_launches": (calls_per_step + (1 if planned else 0) + (1 if commit else 0)) * args.steps * world,
         "clocks": clk.summary(),
         "e2e": e2e,
     }
