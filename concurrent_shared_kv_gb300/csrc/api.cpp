@@ -163,7 +163,8 @@ static int check_desc(const hw_attn_desc *d) {
   if (d->n_q_heads / d->n_kv_heads > kMaxQ) return HW_ERR_UNSUPPORTED;
   if (d->cache_capacity > INT32_MAX) return HW_ERR_UNSUPPORTED;
   if (d->flags & ~HW_DESC_VIEW_LIMITS) return HW_ERR_INVALID;
-  if ((d->flags & HW_DESC_VIEW_LIMITS) && !(d->dtype == HW_BF16 && d->head_dim == 128))
+  if ((d->flags & HW_DESC_VIEW_LIMITS) &&
+      !((d->dtype == HW_BF16 || d->dtype == HW_FP8_E4M3) && d->head_dim == 128))
     return HW_ERR_UNSUPPORTED;
   return HW_OK;
 }

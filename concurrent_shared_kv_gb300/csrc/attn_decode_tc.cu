@@ -1212,8 +1212,8 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
 
 // kPlanned: the step's plan is loaded (else built in-kernel); kAppend (with a
 // plan): the layer's new tokens are written first; kLimit (with a plan, no
-// appends): the plan carries view limits; kFp8 (with a plan alone): E4M3
-// caches with per-kv-head scales.  Each combination is its own kernel, so
+// appends): the plan carries view limits; kFp8 (with a plan, no appends):
+// E4M3 caches with per-kv-head scales.  Each combination is its own kernel, so
 // that no path carries another's code (a second softmax loop in the same
 // kernel, even one never entered, cost the plain path 8 %).
 template <bool kPlanned, bool kAppend, bool kLimit, bool kFp8>
@@ -1536,13 +1536,16 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const C
   const size_t smem = decode_tc_smem_bytes();
   // planned launches run their own instantiations: without the plan-building
   // (and, without appends, the append) code the kernel is far smaller
-  const int which = !a.plan ? 0 : a.k_new ? 2 : a.view_limit ? 3 : a.k_scale ? 4 : 1;
-  void (*const kernels[5])(DecodeArgs, CUtensorMap, CUtensorMap) = {
+  const int which = !a.plan ? 0
+                    : a.k_new ? 2
+                    : a.k_scale ? (a.view_limit ? 5 : 4)
+                    : a.view_limit ? 3 : 1;
+  void (*const kernels[6])(DecodeArgs, CUtensorMap, CUtensorMap) = {
       decode_tc_kernel<false, false, false, false>, decode_tc_kernel<true, false, false, false>,
       decode_tc_kernel<true, true, false, false>, decode_tc_kernel<true, false, true, false>,
-      decode_tc_kernel<true, false, false, true>};
+      decode_tc_kernel<true, false, false, true>, decode_tc_kernel<true, false, true, true>};
   void (*kernel)(DecodeArgs, CUtensorMap, CUtensorMap) = kernels[which];
-  static bool configured[5] = {false, false, false, false, false};
+  static bool configured[6] = {false, false, false, false, false, false};
   if (!configured[which]) {
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));

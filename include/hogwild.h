@@ -100,8 +100,9 @@ typedef struct {
 /*
  * The step's plan carries per-view-entry token limits.  A descriptor with this
  * flag is planned by hw_attn_plan_limited and decoded by
- * hw_attn_decode_planned only (bf16, head_dim 128): the other decode and plan
- * calls return HW_ERR_UNSUPPORTED for it, and hw_attn_plan_limited returns
+ * hw_attn_decode_planned (bf16) or hw_attn_decode_planned_fp8 (HW_FP8_E4M3)
+ * only, head_dim 128: the other decode and plan calls return
+ * HW_ERR_UNSUPPORTED for it, and hw_attn_plan_limited returns
  * HW_ERR_INVALID without it.  (The limits run in their own kernel, so that
  * steps without limits pay nothing for them.)
  */

@@ -43,8 +43,11 @@ def test_fp8_descriptor_is_refused_by_the_other_decode_calls():
     assert status(api.attn_plan_append, d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == -2
     assert status(api.attn_append_decode_planned, d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
                   FAKE, 0) == -2
+    # E4M3 with view limits is planned by hw_attn_plan_limited: the call gets
+    # past the descriptor and argument checks (and stops at the workspace,
+    # which needs a device)
     assert status(api.attn_plan_limited, desc(flags=api.HW_DESC_VIEW_LIMITS), FAKE, FAKE, FAKE,
-                  FAKE, FAKE, FAKE, FAKE, 0) == -2
+                  FAKE, FAKE, FAKE, FAKE, 0) not in (-1, -2)
 
 
 def test_fp8_commit_checks():

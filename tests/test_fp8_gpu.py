@@ -180,3 +180,31 @@ def test_fp8_full_tile_of_columns():
     c = H.Case(w, H.from_storage_np(q, "bf16"), H.from_storage_np(k, "bf16"),
                H.from_storage_np(v, "bf16"), block_start=starts, block_len=lens, views=(vb, vo, qp))
     Fp8Case(c).check("fp8 32 columns")
+
+
+def test_fp8_with_query_chunks():
+    # view limits over E4M3 caches: three-token chunks causal in their own
+    # blocks, against the oracle with the same limits, codes and scales
+    w = small(P=2, W=3, Hq=4, Hkv=2, common=(300, 77), blocks=((129, 64, 3), (130, 5, 256)))
+    vb, vo, vl, qp = api.views_chunked("combined", w.block_lengths(), w.n_problems, w.n_workers, 3)
+    rng = np.random.default_rng(41)
+    _, k, v = wl.draw_host(w, 0)
+    q = wl.to_storage(rng.standard_normal((vb.shape[0], w.n_q_heads, w.head_dim)), "bf16")
+    c = H.Case(w, H.from_storage_np(q, "bf16"), H.from_storage_np(k, "bf16"),
+               H.from_storage_np(v, "bf16"), views=(vb, vo, qp))
+    f = Fp8Case(c)
+    s = engine.DecodeSession(n_rows=vb.shape[0], n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+                             head_dim=w.head_dim, n_blocks=len(c.block_len),
+                             max_view_blocks=vb.shape[1], capacity=c.capacity, dtype=torch.bfloat16,
+                             rope_theta=w.rope_theta, scale=w.scale, kv_fp8=True, view_limits=True)
+    s.set_metadata(c.block_start, c.block_len, vb, vo, qp)
+    s.plan_limited(vl)
+    out, lse = s.decode_planned_fp8(f.q, f.kc, f.vc, f.ks, f.vs)
+    torch.cuda.synchronize()
+    assert s.device_flags() == 0
+    ro, rl = oracle.get().attn_decode(
+        q=H.to_storage_np(f.q), k_cache=f.kc.cpu().numpy(), v_cache=f.vc.cpu().numpy(),
+        k_scale=f.ks.cpu().numpy(), v_scale=f.vs.cpu().numpy(), block_start=c.block_start,
+        block_len=c.block_len, view_block=vb, view_offset=vo, q_pos=qp, n_kv_heads=w.n_kv_heads,
+        rope_theta=w.rope_theta, scale=w.scale, dtype=oracle.FP8, view_limit=vl)
+    H.compare("bf16", out, lse, ro, rl, what="fp8 chunks")
