@@ -263,7 +263,7 @@ def main():
     chunk = args.chunk
     fp8 = args.kv == "fp8"
     if fp8:
-        assert not (args.append or args.unplanned or chunk), "--kv fp8 runs planned decodes"
+        assert not (args.append or args.unplanned), "--kv fp8 runs planned decodes without appends"
         assert w.dtype == "bf16" and w.head_dim == 128, "E4M3 caches: the bf16 head_dim-128 shapes"
     if chunk > 0:
         assert not (args.append or args.unplanned), "--chunk runs planned decodes without appends"
@@ -520,8 +520,9 @@ def main():
             "mode": "eager" if graph is None else "cuda-graph",
             "calls": ("hw_attn_plan_append once per step + hw_attn_append_decode_planned per layer "
                       "(each worker's new token written, then decoded)" if append else
-                      f"hw_attn_plan_limited once per step + hw_attn_decode_planned per layer "
-                      f"({chunk}-token chunks, causal within each worker's own block)" if chunk > 0 else
+                      f"hw_attn_plan_limited once per step + hw_attn_decode_planned{'_fp8' if fp8 else ''} "
+                      f"per layer ({chunk}-token chunks, causal within each worker's own block)"
+                      if chunk > 0 else
                       "hw_attn_plan once per step + hw_attn_decode_planned_fp8 per layer (E4M3 "
                       "K/V codes, per-kv-head scales)" if fp8 else
                       "hw_attn_plan once per step + hw_attn_decode_planned per layer" if planned
