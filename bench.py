@@ -263,7 +263,7 @@ def main():
     chunk = args.chunk
     fp8 = args.kv == "fp8"
     if fp8:
-        assert not (args.append or args.unplanned), "--kv fp8 runs planned decodes without appends"
+        assert not args.unplanned, "--kv fp8 runs planned decodes"
         assert w.dtype == "bf16" and w.head_dim == 128, "E4M3 caches: the bf16 head_dim-128 shapes"
     if chunk > 0:
         assert not (args.append or args.unplanned), "--chunk runs planned decodes without appends"
@@ -343,7 +343,10 @@ def main():
             sess.plan(stream=stream)
         for i in range(calls_per_step):
             l = i % L
-            if append:
+            if append and fp8:
+                sess.append_decode_planned_fp8(qsrc[l], new_k[l], new_v[l], ks[l], vs[l], kscale[l],
+                                               vscale[l], out=osrc[l], lse=lsrc[l], stream=stream)
+            elif append:
                 sess.append_decode_planned(qsrc[l], new_k[l], new_v[l], ks[l], vs[l], out=osrc[l],
                                            lse=lsrc[l], stream=stream)
             elif planned and fp8:
@@ -518,8 +521,9 @@ def main():
             "parallelism": f"replicas x{world}", "kv": args.kv,
             "query_rows": n_rows, "chunk": chunk if chunk > 0 else None,
             "mode": "eager" if graph is None else "cuda-graph",
-            "calls": ("hw_attn_plan_append once per step + hw_attn_append_decode_planned per layer "
-                      "(each worker's new token written, then decoded)" if append else
+            "calls": (f"hw_attn_plan_append once per step + hw_attn_append_decode_planned"
+                      f"{'_fp8' if fp8 else ''} per layer (each worker's new token written, then "
+                      "decoded)" if append else
                       f"hw_attn_plan_limited once per step + hw_attn_decode_planned{'_fp8' if fp8 else ''} "
                       f"per layer ({chunk}-token chunks, causal within each worker's own block)"
                       if chunk > 0 else

@@ -27,6 +27,7 @@ DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMA
 # every symbol the header declares
 EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode",
            "hw_attn_plan", "hw_attn_decode_planned", "hw_attn_decode_planned_fp8", "hw_attn_plan_limited", "hw_attn_plan_append",
+           "hw_attn_append_decode_planned_fp8",
            "hw_attn_append_decode_planned", "hw_plan_export", "hw_attn_decode_noalloc",
            "hw_block_commit", "hw_block_commit_many", "hw_workspace_status", "hw_views_combined",
            "hw_views", "hw_views_chunked", "hw_last_cuda_error", "hw_status_string"]
@@ -81,6 +82,8 @@ def lib(path: Optional[str] = None):
     L.hw_attn_plan_limited.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]
     L.hw_attn_plan_append.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]
     L.hw_attn_append_decode_planned.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]
+    L.hw_attn_append_decode_planned_fp8.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 10 + [
+        ctypes.c_size_t, _P]
     L.hw_plan_export.argtypes = [ctypes.POINTER(AttnDesc), _P, ctypes.c_size_t, _P, ctypes.c_int32,
                                  ctypes.POINTER(ctypes.c_int32), _P]
     L.hw_attn_decode_noalloc.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12
@@ -193,6 +196,19 @@ def attn_decode_planned_fp8(desc: AttnDesc, q, k_cache, v_cache, k_scale, v_scal
                                           _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse),
                                           _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check("hw_attn_decode_planned_fp8", st)
+    return st
+
+
+def attn_append_decode_planned_fp8(desc: AttnDesc, q, k_new, v_new, k_cache, v_cache, k_scale,
+                                   v_scale, out, lse, workspace, workspace_bytes: int,
+                                   stream=None) -> int:
+    """hw_attn_append_decode_planned_fp8: the layer's new tokens written into
+    E4M3 caches (divided by the head scales, rounded), then the layer decoded."""
+    st = lib().hw_attn_append_decode_planned_fp8(
+        ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+        _stream(stream))
+    _check("hw_attn_append_decode_planned_fp8", st)
     return st
 
 

@@ -349,7 +349,6 @@ static int plan_impl(const hw_attn_desc *d, const int32_t *block_start, const in
   if (d->max_view_blocks > 0 && (!view_block || !view_offset)) return HW_ERR_INVALID;
   if (d->n_blocks > 0 && (!block_start || !block_len)) return HW_ERR_INVALID;
   if ((append_block || view_limit) && !tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
-  if (append_block && e4m3(d)) return HW_ERR_UNSUPPORTED;
   if (limited(d) != (view_limit != nullptr)) return view_limit ? HW_ERR_INVALID : HW_ERR_UNSUPPORTED;
   WorkspaceLayout L;
   int max_ctas = 0;
@@ -457,13 +456,11 @@ int hw_plan_export(const hw_attn_desc *d, const void *workspace, size_t workspac
   return HW_OK;
 }
 
-int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const void *k_new,
-                                  const void *v_new, void *k_cache, void *v_cache, void *out,
-                                  float *lse, void *workspace, size_t workspace_bytes,
-                                  void *stream) {
-  int st = check_desc(d);
-  if (st != HW_OK) return st;
-  if (limited(d) || e4m3(d)) return HW_ERR_UNSUPPORTED;
+// hw_attn_append_decode_planned and its E4M3 form, after their own checks.
+static int append_impl(const hw_attn_desc *d, const void *q, const void *k_new, const void *v_new,
+                       void *k_cache, void *v_cache, const float *k_scale, const float *v_scale,
+                       void *out, float *lse, void *workspace, size_t workspace_bytes,
+                       void *stream) {
   if (d->n_rows == 0) return HW_OK;
   if (!tensor_core_path(d)) return HW_ERR_UNSUPPORTED;
   if (!q || !out || !k_new || !v_new) return HW_ERR_INVALID;
@@ -472,13 +469,39 @@ int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const vo
     return HW_ERR_INVALID;  // 16-byte loads of the new rows
   WorkspaceLayout L;
   int max_ctas = 0;
-  st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
+  const int st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
   if (st != HW_OK) return st;
   const MetaCopies m = meta_copies(*d, L, workspace);
   const uint8_t *plan = static_cast<const uint8_t *>(workspace) + L.plan_off;
   return decode_common(d, q, k_cache, v_cache, m.block_start, m.block_len, m.view_block,
                        m.view_offset, m.q_pos, m.q_to_kv, plan, out, lse, workspace, L, max_ctas,
-                       stream, m.append_block, m.append_pos, k_new, v_new);
+                       stream, m.append_block, m.append_pos, k_new, v_new, nullptr, k_scale,
+                       v_scale);
+}
+
+int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const void *k_new,
+                                  const void *v_new, void *k_cache, void *v_cache, void *out,
+                                  float *lse, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+  int st = check_desc(d);
+  if (st != HW_OK) return st;
+  if (limited(d) || e4m3(d)) return HW_ERR_UNSUPPORTED;  // E4M3: the _fp8 form takes the scales
+  return append_impl(d, q, k_new, v_new, k_cache, v_cache, nullptr, nullptr, out, lse, workspace,
+                     workspace_bytes, stream);
+}
+
+int hw_attn_append_decode_planned_fp8(const hw_attn_desc *d, const void *q, const void *k_new,
+                                      const void *v_new, void *k_cache, void *v_cache,
+                                      const float *k_scale, const float *v_scale, void *out,
+                                      float *lse, void *workspace, size_t workspace_bytes,
+                                      void *stream) {
+  int st = check_desc(d);
+  if (st != HW_OK) return st;
+  if (limited(d)) return HW_ERR_UNSUPPORTED;
+  if (!e4m3(d)) return HW_ERR_INVALID;
+  if (d->n_rows > 0 && (!k_scale || !v_scale)) return HW_ERR_INVALID;
+  return append_impl(d, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, out, lse, workspace,
+                     workspace_bytes, stream);
 }
 
 static_assert(kMaxCommits == HW_MAX_COMMITS, "commit table size");

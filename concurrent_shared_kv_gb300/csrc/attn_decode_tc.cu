@@ -695,6 +695,9 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
 // rounded once to bf16, the block commit's arithmetic - and the value copied,
 // into the cache rows that tile's copies will read.  The writes are fenced
 // for the async proxy before the producer is released.
+// (E4M3 caches: the rotated key divided by its head's k_scale, the value by
+// v_scale, each rounded to the nearest code, saturating.)
+template <bool kFp8>
 __device__ void append_tokens(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
   const int lane = tq & 31, wq = tq >> 5;
@@ -704,22 +707,41 @@ __device__ void append_tokens(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_
   const __nv_bfloat16 *vn = static_cast<const __nv_bfloat16 *>(a.v_new);
   __nv_bfloat16 *kc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.k));
   __nv_bfloat16 *vc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.v));
+  uint8_t *kc8 = static_cast<uint8_t *>(const_cast<void *>(a.k));
+  uint8_t *vc8 = static_cast<uint8_t *>(const_cast<void *>(a.v));
+  auto code = [](float x) {  // nearest E4M3 code, ties to even, saturating
+    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+  };
   // one (row, kv head) token by the whole warp: lane l the pairs (l, l + 64)
   // and (l + 32, l + 96)
   auto write_token = [&](int pr, int pos, int row) {
     const int r = pr / Hkv, h = pr - r * Hkv;
     const int64_t s_off = (static_cast<int64_t>(r) * Hkv + h) * 128;
     const int64_t d_off = (static_cast<int64_t>(h) * a.capacity + row) * 128;
+    float kinv = 1.f, vinv = 1.f;
+    if constexpr (kFp8) {
+      kinv = 1.f / __ldg(a.k_scale + h);
+      vinv = 1.f / __ldg(a.v_scale + h);
+    }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int i = lane + 32 * half;
       const float x0 = __bfloat162float(kn[s_off + i]), x1 = __bfloat162float(kn[s_off + i + 64]);
       float cs, sn;
       rope_cos_sin(pos, a.phase[i], &cs, &sn);
-      kc[d_off + i] = __float2bfloat16_rn(__fmaf_rn(x0, cs, -__fmul_rn(x1, sn)));
-      kc[d_off + i + 64] = __float2bfloat16_rn(__fmaf_rn(x1, cs, __fmul_rn(x0, sn)));
-      vc[d_off + i] = vn[s_off + i];
-      vc[d_off + i + 64] = vn[s_off + i + 64];
+      const float y0 = __fmaf_rn(x0, cs, -__fmul_rn(x1, sn));
+      const float y1 = __fmaf_rn(x1, cs, __fmul_rn(x0, sn));
+      if constexpr (kFp8) {
+        kc8[d_off + i] = code(y0 * kinv);
+        kc8[d_off + i + 64] = code(y1 * kinv);
+        vc8[d_off + i] = code(__bfloat162float(vn[s_off + i]) * vinv);
+        vc8[d_off + i + 64] = code(__bfloat162float(vn[s_off + i + 64]) * vinv);
+      } else {
+        kc[d_off + i] = __float2bfloat16_rn(y0);
+        kc[d_off + i + 64] = __float2bfloat16_rn(y1);
+        vc[d_off + i] = vn[s_off + i];
+        vc[d_off + i + 64] = vn[s_off + i + 64];
+      }
     }
   };
   if (S.cp.app_n <= kAppList) {
@@ -1212,8 +1234,8 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
 
 // kPlanned: the step's plan is loaded (else built in-kernel); kAppend (with a
 // plan): the layer's new tokens are written first; kLimit (with a plan, no
-// appends): the plan carries view limits; kFp8 (with a plan, no appends):
-// E4M3 caches with per-kv-head scales.  Each combination is its own kernel, so
+// appends): the plan carries view limits; kFp8 (with a plan): E4M3 caches
+// with per-kv-head scales.  Each combination is its own kernel, so
 // that no path carries another's code (a second softmax loop in the same
 // kernel, even one never entered, cost the plain path 8 %).
 template <bool kPlanned, bool kAppend, bool kLimit, bool kFp8>
@@ -1339,7 +1361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mma_issuer<kFp8>(a, S, tmem, u0, u1);
     } else {
       if (appending && warp >= kWarpQ)
-        append_tokens(a, S, u0, u1);
+        append_tokens<kFp8>(a, S, u0, u1);
       else
         query_prologue<kPlanned, kFp8>(a, S, u0, u1, appending ? 128 : 192);
       if (warp < kWarpQ)
@@ -1537,15 +1559,16 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const C
   // planned launches run their own instantiations: without the plan-building
   // (and, without appends, the append) code the kernel is far smaller
   const int which = !a.plan ? 0
-                    : a.k_new ? 2
+                    : a.k_new ? (a.k_scale ? 6 : 2)
                     : a.k_scale ? (a.view_limit ? 5 : 4)
                     : a.view_limit ? 3 : 1;
-  void (*const kernels[6])(DecodeArgs, CUtensorMap, CUtensorMap) = {
+  void (*const kernels[7])(DecodeArgs, CUtensorMap, CUtensorMap) = {
       decode_tc_kernel<false, false, false, false>, decode_tc_kernel<true, false, false, false>,
       decode_tc_kernel<true, true, false, false>, decode_tc_kernel<true, false, true, false>,
-      decode_tc_kernel<true, false, false, true>, decode_tc_kernel<true, false, true, true>};
+      decode_tc_kernel<true, false, false, true>, decode_tc_kernel<true, false, true, true>,
+      decode_tc_kernel<true, true, false, true>};
   void (*kernel)(DecodeArgs, CUtensorMap, CUtensorMap) = kernels[which];
-  static bool configured[6] = {false, false, false, false, false, false};
+  static bool configured[7] = {false, false, false, false, false, false, false};
   if (!configured[which]) {
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));

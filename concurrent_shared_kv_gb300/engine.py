@@ -137,6 +137,23 @@ class DecodeSession:
                                     self.workspace, self.ws_bytes, stream=stream)
         return out, lse
 
+    def append_decode_planned_fp8(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                  k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  k_scale: torch.Tensor, v_scale: torch.Tensor,
+                                  out: Optional[torch.Tensor] = None,
+                                  lse: Optional[torch.Tensor] = None, want_lse: bool = True,
+                                  stream=None):
+        """One layer over E4M3 pools: its new tokens (bf16, [rows][Hkv][D])
+        written as codes with the head scales, then decoded."""
+        d = self.desc
+        if out is None:
+            out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
+        if lse is None and want_lse:
+            lse = torch.empty((d.n_rows, d.n_q_heads), dtype=torch.float32, device=self.device)
+        api.attn_append_decode_planned_fp8(d, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                           out, lse, self.workspace, self.ws_bytes, stream=stream)
+        return out, lse
+
     def device_flags(self) -> int:
         return api.workspace_status(self.workspace)
 

@@ -181,8 +181,9 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
  *
  * A descriptor with HW_DESC_VIEW_LIMITS is planned by hw_attn_plan_limited
  * instead (hw_attn_plan returns HW_ERR_UNSUPPORTED for it); HW_FP8_E4M3
- * caches are planned here and decoded by hw_attn_decode_planned_fp8
- * (hw_attn_decode_planned returns HW_ERR_UNSUPPORTED for them).
+ * caches are planned here (with appends: hw_attn_plan_append) and decoded by
+ * hw_attn_decode_planned_fp8 (or hw_attn_append_decode_planned_fp8), while
+ * hw_attn_decode_planned returns HW_ERR_UNSUPPORTED for them.
  *
  * Not in the Hogwild! notes, which describe one attention call per layer:
  * this is the usual split of a decode kernel's scheduling from its runs.
@@ -264,6 +265,20 @@ int hw_attn_append_decode_planned(const hw_attn_desc *d, const void *q, const vo
                                   const void *v_new, void *k_cache, void *v_cache, void *out,
                                   float *lse, void *workspace, size_t workspace_bytes,
                                   void *stream);
+
+/*
+ * hw_attn_append_decode_planned for HW_FP8_E4M3 caches: each new token's key
+ * (bf16, rotated at its block-local position in fp32) divided by its kv
+ * head's k_scale and its value divided by v_scale, each rounded to the nearest
+ * E4M3 code (ties to even, saturating at 448), then the layer decoded as
+ * hw_attn_decode_planned_fp8 does.  Planned by hw_attn_plan_append with the
+ * same descriptor.  HW_ERR_INVALID for another dtype or null scales.
+ */
+int hw_attn_append_decode_planned_fp8(const hw_attn_desc *d, const void *q, const void *k_new,
+                                      const void *v_new, void *k_cache, void *v_cache,
+                                      const float *k_scale, const float *v_scale, void *out,
+                                      float *lse, void *workspace, size_t workspace_bytes,
+                                      void *stream);
 
 /*
  * For tests: the work split of the plan in `workspace` (bf16 head_dim-128

@@ -237,6 +237,35 @@ class Oracle:
         return (kd, vd, exact) if want_exact else (kd, vd)
 
 
+def append_tokens_e4m3(o: "Oracle", *, rope_theta: float, k_cache, v_cache, k_new, v_new,
+                       k_scale, v_scale, block_start, append_block, append_pos):
+    """The append into E4M3 caches: row r's new key (bf16 storage, rotated at
+    its block-local position p, in double) divided by its kv head's k_scale and
+    rounded to the nearest E4M3 code (ties to even, saturating at 448); its
+    value divided by v_scale and rounded likewise.  k_new, v_new: [rows][Hkv][D]
+    bf16 storage; caches [Hkv][cap][D] uint8 codes.  Returns (k, v, exact) on
+    copies, exact = {row: ([Hkv][D] key / k_scale, [Hkv][D] value / v_scale)}
+    before rounding."""
+    kd = np.array(k_cache, dtype=np.uint8, copy=True, order="C")
+    vd = np.array(v_cache, dtype=np.uint8, copy=True, order="C")
+    Hkv, _, D = kd.shape
+    bf = lambda a: (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    exact = {}
+    for r in range(len(append_block)):
+        b = int(append_block[r])
+        if b < 0:
+            continue
+        p, row = int(append_pos[r]), int(block_start[b]) + int(append_pos[r])
+        ek = np.stack([o.rope(bf(k_new[r][h]), rope_theta, float(p)) / float(k_scale[h])
+                       for h in range(Hkv)])
+        ev = np.stack([bf(v_new[r][h]) / float(v_scale[h]) for h in range(Hkv)])
+        for h in range(Hkv):
+            kd[h, row] = [o.e4m3_from_double(x) for x in ek[h]]
+            vd[h, row] = [o.e4m3_from_double(x) for x in ev[h]]
+        exact[r] = (ek, ev)
+    return kd, vd, exact
+
+
 _default: Optional[Oracle] = None
 
 

@@ -24,6 +24,14 @@ def status(fn, *args, **kw):
         return e.status
 
 
+def test_fp8_append_entry_checks():
+    call = lambda d, ks=FAKE, vs=FAKE: status(api.attn_append_decode_planned_fp8, d, FAKE, FAKE, FAKE,
+                                              FAKE, FAKE, ks, vs, FAKE, None, FAKE, 0)
+    assert call(desc(), ks=None) == -1
+    assert call(desc(dtype=api.HW_BF16)) == -1
+    assert call(desc(flags=api.HW_DESC_VIEW_LIMITS)) == -2
+
+
 def test_fp8_decode_entry_checks():
     call = lambda d, ks=FAKE, vs=FAKE: status(api.attn_decode_planned_fp8, d, FAKE, FAKE, FAKE, ks, vs,
                                               FAKE, None, FAKE, 0)
@@ -40,7 +48,9 @@ def test_fp8_descriptor_is_refused_by_the_other_decode_calls():
     assert status(api.attn_decode_noalloc, d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                   None) == -2
     assert status(api.attn_decode_planned, d, FAKE, FAKE, FAKE, FAKE, None, FAKE, 0) == -2
-    assert status(api.attn_plan_append, d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == -2
+    # (E4M3 with appends is planned by hw_attn_plan_append: past its checks)
+    assert status(api.attn_plan_append, d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                  0) not in (-1, -2)
     assert status(api.attn_append_decode_planned, d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
                   FAKE, 0) == -2
     # E4M3 with view limits is planned by hw_attn_plan_limited: the call gets
@@ -72,3 +82,32 @@ def test_e4m3_packing_of_the_inputs():
     assert np.all(np.abs(got - z) <= half * 1.0001)
     o = oracle.get()
     assert all(o.e4m3_to_double(int(b)) == g for b, g in zip(codes.ravel()[:500], got.ravel()[:500]))
+
+
+def test_oracle_e4m3_append():
+    # the new token's key rotated at its position, divided by the head scale,
+    # rounded to the nearest code; position 0 and power-of-two scales: the
+    # codes of the scaled raw values; a rotated key decodes (x scale) back,
+    # rotated by -p, to the raw key within E4M3's half-step
+    o = oracle.get()
+    rng = np.random.default_rng(3)
+    Hkv, D = 2, 16
+    raw = rng.standard_normal((2, Hkv, D))
+    kn = wl.to_storage(raw, "bf16")
+    vn = wl.to_storage(raw[::-1].copy(), "bf16")
+    k = np.zeros((Hkv, 40, D), np.uint8)
+    v = np.zeros_like(k)
+    ks, vs = np.array([0.5, 2.0]), np.array([0.25, 1.0])
+    kd, vd, ex = oracle.append_tokens_e4m3(o, rope_theta=1e4, k_cache=k, v_cache=v, k_new=kn,
+                                          v_new=vn, k_scale=ks, v_scale=vs, block_start=[0, 20],
+                                          append_block=[0, 1], append_pos=[0, 9])
+    kb, vb_ = wl.storage_to_f64(kn, "bf16"), wl.storage_to_f64(vn, "bf16")
+    for h in range(Hkv):
+        assert [o.e4m3_from_double(x / ks[h]) for x in kb[0, h]] == kd[h, 0].tolist()
+        assert [o.e4m3_from_double(x / vs[h]) for x in vb_[1, h]] == vd[h, 29].tolist()
+        back = o.rope(wl.e4m3_values(kd[h, 29]) * ks[h], 1e4, -9.0)
+        step = (np.abs(kb[1, h]) + 2.0 ** -6 * ks[h]) * 2.0 ** -3
+        assert np.all(np.abs(back - kb[1, h]) <= np.max(step) * 2)
+    untouched = np.ones(40, bool)
+    untouched[[0, 29]] = False
+    assert not kd[:, untouched].any() and not vd[:, untouched].any()

@@ -208,3 +208,50 @@ def test_fp8_with_query_chunks():
         block_len=c.block_len, view_block=vb, view_offset=vo, q_pos=qp, n_kv_heads=w.n_kv_heads,
         rope_theta=w.rope_theta, scale=w.scale, dtype=oracle.FP8, view_limit=vl)
     H.compare("bf16", out, lse, ro, rl, what="fp8 chunks")
+
+
+def _fp8_append_check(c, what, rows=None):
+    from tests.test_append_gpu import last_position_appends, new_tokens
+    w = c.w
+    f = Fp8Case(c)
+    ab, ap = last_position_appends(c)
+    kn, vn = new_tokens(w, 12)
+    kc0, vc0 = f.kc.cpu().numpy().copy(), f.vc.cpu().numpy().copy()
+    s = engine.DecodeSession(n_rows=w.n_rows, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+                             head_dim=w.head_dim, n_blocks=len(c.block_len),
+                             max_view_blocks=c.view_block.shape[1], capacity=c.capacity,
+                             dtype=torch.bfloat16, rope_theta=w.rope_theta, scale=w.scale,
+                             kv_fp8=True)
+    s.set_metadata(c.block_start, c.block_len, c.view_block, c.view_offset, c.q_pos)
+    s.plan_append(ab, ap)
+    out, lse = s.append_decode_planned_fp8(f.q, kn, vn, f.kc, f.vc, f.ks, f.vs)
+    torch.cuda.synchronize()
+    assert s.device_flags() == 0
+    ks, vs = f.ks.cpu().numpy(), f.vs.cpu().numpy()
+    kd, vd, _ = oracle.append_tokens_e4m3(oracle.get(), rope_theta=w.rope_theta, k_cache=kc0,
+                                          v_cache=vc0, k_new=H.to_storage_np(kn),
+                                          v_new=H.to_storage_np(vn), k_scale=ks, v_scale=vs,
+                                          block_start=c.block_start, append_block=ab, append_pos=ap)
+    kg, vg = f.kc.cpu().numpy(), f.vc.cpu().numpy()
+    # untouched rows bit for bit; the new codes the oracle's, or one code step
+    # away where the fp32 rotation and reciprocal meet a rounding boundary
+    for got, want in ((kg, kd), (vg, vd)):
+        diff = got != want
+        assert diff.mean() < 1e-3, (what, diff.mean())
+        a_, b_ = wl.e4m3_values(got[diff]), wl.e4m3_values(want[diff])
+        assert np.all(np.abs(a_ - b_) <= np.maximum(np.abs(b_), 2.0 ** -6) * 2.0 ** -3 * 1.0001), what
+    ro, rl = oracle.get().attn_decode(
+        q=H.to_storage_np(f.q), k_cache=kg, v_cache=vg, k_scale=ks, v_scale=vs,
+        block_start=c.block_start, block_len=c.block_len, view_block=c.view_block,
+        view_offset=c.view_offset, q_pos=c.q_pos, n_kv_heads=w.n_kv_heads,
+        rope_theta=w.rope_theta, scale=w.scale, dtype=oracle.FP8, rows=rows)
+    H.compare("bf16", out, lse, ro, rl, rows=rows, what=what)
+
+
+def test_fp8_append_small_edges():
+    w = small(P=2, W=3, common=(300, 77), blocks=((129, 64, 1), (128, 0, 33)))
+    _fp8_append_check(H.host_case(w), "fp8 append small")
+
+
+def test_fp8_append_qwq32b_w4_layer():
+    _fp8_append_check(H.device_case(wl.qwq32b_w4(), 0), "fp8 append C3 layer", rows=[0, 1, 2, 3])
