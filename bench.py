@@ -55,6 +55,8 @@ def parse():
     p.add_argument("--unplanned", action="store_true",
                    help="one hw_attn_decode per layer instead of hw_attn_plan once per step "
                         "plus hw_attn_decode_planned per layer")
+    p.add_argument("--no-early", action="store_true",
+                   help="never pass the early-loads promise (HW_DESC_EARLY_LOADS)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     p.add_argument("--layers", type=int, default=0,
@@ -343,19 +345,27 @@ def main():
             sess.plan(stream=stream)
         for i in range(calls_per_step):
             l = i % L
+            # The early-loads promise (HW_DESC_EARLY_LOADS): the call before
+            # this one writes neither its pools nor the plan.  Not for the
+            # first layer (it follows the plan, or the previous step's commit),
+            # nor when the layers repeat one pool that the appends write.
+            early = not args.no_early and i > 0 and not (append and L < calls_per_step)
             if append and fp8:
                 sess.append_decode_planned_fp8(qsrc[l], new_k[l], new_v[l], ks[l], vs[l], kscale[l],
-                                               vscale[l], out=osrc[l], lse=lsrc[l], stream=stream)
+                                               vscale[l], out=osrc[l], lse=lsrc[l], stream=stream,
+                                               early=early)
             elif append:
                 sess.append_decode_planned(qsrc[l], new_k[l], new_v[l], ks[l], vs[l], out=osrc[l],
-                                           lse=lsrc[l], stream=stream)
+                                           lse=lsrc[l], stream=stream, early=early)
             elif planned and fp8:
                 sess.decode_planned_fp8(qsrc[l], ks[l], vs[l], kscale[l], vscale[l], out=osrc[l],
-                                        lse=lsrc[l], stream=stream)
+                                        lse=lsrc[l], stream=stream, early=early)
             elif planned:
-                sess.decode_planned(qsrc[l], ks[l], vs[l], out=osrc[l], lse=lsrc[l], stream=stream)
+                sess.decode_planned(qsrc[l], ks[l], vs[l], out=osrc[l], lse=lsrc[l], stream=stream,
+                                    early=early)
             else:
-                sess.decode(qsrc[l], ks[l], vs[l], out=osrc[l], lse=lsrc[l], stream=stream)
+                sess.decode(qsrc[l], ks[l], vs[l], out=osrc[l], lse=lsrc[l], stream=stream,
+                            early=early)
 
     step_no = [0]
 

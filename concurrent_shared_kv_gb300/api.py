@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libhogwild.so")
 HW_OK = 0
 HW_F32, HW_BF16, HW_FP8_E4M3 = 0, 1, 2
 HW_DESC_VIEW_LIMITS = 1
+HW_DESC_EARLY_LOADS = 2
 STATUS = {0: "HW_OK", -1: "HW_ERR_INVALID", -2: "HW_ERR_UNSUPPORTED", -3: "HW_ERR_WORKSPACE",
           -4: "HW_ERR_CAPACITY", -5: "HW_ERR_OVERLAP", -6: "HW_ERR_CUDA", -7: "HW_ERR_DEVICE"}
 DEV_FLAGS = {1: "HW_DEV_BAD_BLOCK", 2: "HW_DEV_BAD_RANGE", 4: "HW_DEV_BAD_HEADMAP",

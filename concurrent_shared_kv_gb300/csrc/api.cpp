@@ -162,7 +162,7 @@ static int check_desc(const hw_attn_desc *d) {
     return HW_ERR_UNSUPPORTED;
   if (d->n_q_heads / d->n_kv_heads > kMaxQ) return HW_ERR_UNSUPPORTED;
   if (d->cache_capacity > INT32_MAX) return HW_ERR_UNSUPPORTED;
-  if (d->flags & ~HW_DESC_VIEW_LIMITS) return HW_ERR_INVALID;
+  if (d->flags & ~(HW_DESC_VIEW_LIMITS | HW_DESC_EARLY_LOADS)) return HW_ERR_INVALID;
   if ((d->flags & HW_DESC_VIEW_LIMITS) &&
       !((d->dtype == HW_BF16 || d->dtype == HW_FP8_E4M3) && d->head_dim == 128))
     return HW_ERR_UNSUPPORTED;
@@ -215,6 +215,7 @@ static void fill_args(DecodeArgs &a, const hw_attn_desc *d, const WorkspaceLayou
   a.err = reinterpret_cast<int32_t *>(ws + L.err_off);
   a.counters = reinterpret_cast<int32_t *>(ws + L.counters_off);
   a.partials = reinterpret_cast<float *>(ws + L.partials_off);
+  a.early = (d->flags & HW_DESC_EARLY_LOADS) != 0;
   a.n_rows = d->n_rows;
   a.n_q_heads = d->n_q_heads;
   a.n_kv_heads = d->n_kv_heads;

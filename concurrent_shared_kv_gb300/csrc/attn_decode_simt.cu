@@ -226,7 +226,9 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
   }
   __syncthreads();
   merge_phase<T, D, 1>(a, P, S.cache, S.merge, nullptr, nullptr, 0, 0, threadIdx.x, kSimtThreads,
-                    CtaSync(), 2000000000ll);
+                    CtaSync(), 2000000000ll,
+                       merge_rank(P, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x)),
+                       static_cast<int>(gridDim.x));
 }
 
 template <typename T, int D>

@@ -116,6 +116,7 @@ struct alignas(16) CtaPlan {
   SegQ pre[kPre];          // query-side metadata of segment j in pre[j % kPre]
   int32_t mpre[kPreItems][kPreList];  // record lists of its first merge items
   int32_t mpre_n[kPreItems];          // their lengths, or -1 (not built)
+  int32_t mrank;           // its rank among the CTAs by units (merge_ctas: it merges if < nm)
   int32_t trow[kStages];   // its first tiles (the ring's first fill): first cache row,
   uint8_t th[kStages];     // kv head,
   uint8_t tfl[kStages];    // segment flags (see TileRef)
@@ -316,17 +317,23 @@ __device__ __forceinline__ uint8_t *stage_ptr(TcSmem &S, int s) {
 // Streams the CTA's tiles through the ring.  The first n_first come decoded
 // from the plan, so that the ring fills without waiting on the unit
 // arithmetic; the others are decoded while their stage is still busy.
+// The tiles i_begin .. i_end-1 of the range: at entry the first ones into
+// the empty ring (i_begin = 0, i_end at most the ring and before the first
+// tile with a new token), then the others (i_begin = the count issued).
+// Returns the index after the last tile issued.
 template <bool kFp8>
-__device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
-                         const CUtensorMap *tv, int64_t u0, int64_t u1, bool appending) {
+__device__ int producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
+                        const CUtensorMap *tv, int64_t u0, int64_t u1, bool appending,
+                        int i_begin, int64_t i_end) {
   constexpr int NS = Ring<kFp8>::NS;
   const uint64_t pol = policy_evict_first();
   const int n_first = S.cp.n_first;
   // the first tile holding a new token is loaded only once the tokens are
   // written (and fenced for the copy engine)
   const int app_tile = appending ? S.cp.app_tile : -1;
-  int i = 0;
-  for (int64_t u = u0; u < u1; ++u, ++i) {
+  int i = i_begin;
+  const int64_t u_stop = u1 < u0 + i_end ? u1 : u0 + i_end;  // (u1 still decides the flags)
+  for (int64_t u = u0 + i_begin; u < u_stop; ++u, ++i) {
     const int s = i % NS;
     // the tile's coordinates first, so that only the copy waits for the stage
     TileRef t;
@@ -358,8 +365,15 @@ __device__ void producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
     tma_load_3d(st + 2 * kBox, tv, &S.v_full[s], 0, t.row, t.h, pol);
     tma_load_3d(st + 3 * kBox, tv, &S.v_full[s], 64, t.row, t.h, pol);
   }
-  // no copy may still be landing in shared memory when the CTA retires
-  for (int j = (i > NS ? i - NS : 0); j < i; ++j) {
+  return i;
+}
+
+// No copy may still be landing in shared memory when the CTA retires: the
+// last NS of the n issued tiles are waited for.
+template <bool kFp8>
+__device__ void producer_drain(TcSmem &S, int n) {
+  constexpr int NS = Ring<kFp8>::NS;
+  for (int j = (n > NS ? n - NS : 0); j < n; ++j) {
     mbar_wait(&S.k_full[j % NS], (j / NS) & 1);
     mbar_wait(&S.v_full[j % NS], (j / NS) & 1);
   }
@@ -843,11 +857,21 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
           }
         }
         plan_ranks(a, S.ps.cache, wq, lane, 0, 1);
+        {
+          // this CTA's rank by units (which CTAs merge: merge_ctas)
+          int part = units_rank_part(S.ps.plan, a.n_blocks, static_cast<int>(gridDim.x),
+                                     static_cast<int>(blockIdx.x), u1 - u0, tq, 64);
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+          if (lane == 0) S.qmax[6 + wq] = part;
+        }
         sync();
+        if (tq == 0) S.cp.mrank = S.qmax[6] + S.qmax[7];
+        const int nm = merge_ctas(a, static_cast<int>(gridDim.x));
         if (wq == 0 && S.ps.cache.entries_cached) {
-          const int first = merge_rank(S.ps.plan, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
+          const int first = S.qmax[6] + S.qmax[7];
           int n = -1;
-          if (first < a.n_rows * a.n_q_heads) {
+          if (first < nm && first < a.n_rows * a.n_q_heads) {
             n = merge_list(a, S.ps.plan, S.ps.cache, first / a.n_q_heads, first % a.n_q_heads,
                            S.cp.mpre[0], kPreList, nullptr, lane);
             if (n > kPreList) n = -1;
@@ -1249,9 +1273,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Launched as a programmatic dependent of the previous kernel on the
   // stream: this CTA may start while that grid's last CTAs still run (an SM
   // holds one CTA of this kernel, so only SMs they left), and the next
-  // launch may be placed likewise.  Until griddepcontrol.wait nothing here
-  // touches global memory: the previous grid may have written q, the plan,
-  // the caches or this workspace.
+  // launch may be placed likewise.  Before griddepcontrol.wait it writes no
+  // global memory and reads only what cannot be in flight: an L2 prefetch of
+  // q (which never changes a result) and - when the caller promised that the
+  // previous work writes neither (a.early) - its plan or metadata and its
+  // first K/V tiles.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     tma_prefetch_desc(&tm_k);  // (kernel parameters)
@@ -1292,7 +1318,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&S.tmem_base, Ring<kFp8>::TC);
     tmem_relinquish();
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid is complete
   if (tid == 32) {
     // Every CTA warms L2 with its share of q before any K/V tile is asked
     // for: query loads then hit L2 instead of queueing behind the tile
@@ -1324,31 +1349,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (tid == 0) {
+  // The plan: loaded (the shared part and this CTA's record, two bulk
+  // copies) or built in-kernel from the metadata.  Errors it finds are
+  // recorded after griddepcontrol.wait.
+  bool plan_timeout = false;
+  auto get_plan = [&]() {
     if (kPlanned) {
-      // the step's plan: the shared part and this CTA's record
-      mbar_arrive_expect_tx(&S.plan_bar, sizeof(PlanShared) + sizeof(CtaPlan));
-      bulk_g2s(&S.ps, a.plan + kPlanHeaderBytes, sizeof(PlanShared), &S.plan_bar);
-      bulk_g2s(&S.cp, plan_cta_record(a.plan, blockIdx.x), sizeof(CtaPlan), &S.plan_bar);
-      if (!plan_matches(a, a.plan)) S.plan_ok = 0;
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&S.plan_bar, sizeof(PlanShared) + sizeof(CtaPlan));
+        bulk_g2s(&S.ps, a.plan + kPlanHeaderBytes, sizeof(PlanShared), &S.plan_bar);
+        bulk_g2s(&S.cp, plan_cta_record(a.plan, blockIdx.x), sizeof(CtaPlan), &S.plan_bar);
+        if (!plan_matches(a, a.plan)) S.plan_ok = 0;
+      }
+      __syncthreads();  // the barrier is initialised
+      if (!mbar_wait(&S.plan_bar, 0)) {
+        plan_timeout = true;
+        S.plan_ok = 0;
+      }
+      __syncthreads();  // every thread's wait is over: the table may be refreshed
+      if (tid < 64) S.ps.cache.phase[tid] = a.phase[tid];  // this launch's RoPE table
+    } else {
+      // the plan scratch borrows stage 0, which no copy has touched yet
+      build_plan<kT>(a, S.ps.plan, S.ps.cache, *reinterpret_cast<PlanScratch *>(S.stage[0]),
+                     *reinterpret_cast<int64_t(*)[2]>(&S.cp.u0));
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  };
+  const bool early = a.early != 0;
+  int issued = 0;  // tiles the producer issued before griddepcontrol.wait
+  if (early) {
+    get_plan();
+    // the first tiles into the empty ring (not past the first tile that
+    // holds a new token: those are written after the wait)
+    if (tid == 0 && S.plan_ok && S.cp.u0 < S.cp.u1) {
+      int64_t n0 = Ring<kFp8>::NS;
+      if (kAppend && S.cp.app_n > 0 && S.cp.app_tile < n0) n0 = S.cp.app_tile;
+      issued = producer<kFp8>(a, S, &tm_k, &tm_v, S.cp.u0, S.cp.u1, false, 0, n0);
     }
   }
-  if (!kPlanned) {
-    // the plan scratch borrows stage 0, which no copy has touched yet
-    build_plan<kT>(a, S.ps.plan, S.ps.cache, *reinterpret_cast<PlanScratch *>(S.stage[0]),
-                   *reinterpret_cast<int64_t(*)[2]>(&S.cp.u0));
-  } else {
-    __syncthreads();  // the barrier is initialised
-    if (!mbar_wait(&S.plan_bar, 0)) {
-      flag_error(a.err, HW_DEV_TIMEOUT);
-      S.plan_ok = 0;
-    }
-    __syncthreads();  // every thread's wait is over: the table may be refreshed
-    if (tid < 64) S.ps.cache.phase[tid] = a.phase[tid];  // this launch's RoPE table
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid is complete
+  if (!early) get_plan();
+  if (plan_timeout) flag_error(a.err, HW_DEV_TIMEOUT);
   const uint32_t tmem = S.tmem_base;
   const bool ok = S.plan_ok != 0;
   if (!ok && tid == 0 && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_PLAN);
@@ -1356,7 +1399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (u0 < u1) {
     const bool appending = kAppend && S.cp.app_n > 0;
     if (warp == kWarpTma) {
-      if (lane == 0) producer<kFp8>(a, S, &tm_k, &tm_v, u0, u1, appending);
+      if (lane == 0) {
+        const int n = producer<kFp8>(a, S, &tm_k, &tm_v, u0, u1, appending, issued, u1 - u0);
+        producer_drain<kFp8>(S, n);
+      }
     } else if (warp == kWarpMma) {
       if (lane == 0) mma_issuer<kFp8>(a, S, tmem, u0, u1);
     } else {
@@ -1371,6 +1417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (!kPlanned) {
     plan_ranks(a, S.ps.cache, warp, lane, 0, 1);  // a CTA without units: ranks for the merge
+    const int part = units_rank_part(S.ps.plan, a.n_blocks, static_cast<int>(gridDim.x),
+                                     static_cast<int>(blockIdx.x), 0, tid, kThreads);
+    const int rank = __syncthreads_count(part);  // (one CTA per thread at most)
+    if (tid == 0) S.cp.mrank = rank;
   }
   tc_fence_before();
   __syncthreads();
@@ -1380,11 +1430,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // the merge scratch lives in the tile buffers: every copy and MMA is done
   static_assert(sizeof(MergeSmem<8>) <= kStageBytes, "merge scratch must fit in a stage");
+  // Only the merge CTAs (merge_ctas: the ones with the most units) take
+  // items; every other CTA retires here, and the next launch's CTA can take
+  // its SM.
   if (ok)
     merge_phase<__nv_bfloat16, 128, 8>(a, S.ps.plan, S.ps.cache,
                                        *reinterpret_cast<MergeSmem<8> *>(S.stage[0]),
                                        &S.cp.mpre[0][0], S.cp.mpre_n, kPreItems, kPreList, tid,
-                                       kThreads, CtaSync(), kWaitLimit);
+                                       kThreads, CtaSync(), kWaitLimit, S.cp.mrank,
+                                       merge_ctas(a, static_cast<int>(gridDim.x)));
 }
 
 // The plan of one decode step (see "plans" above).  Any grid: CTA c writes
@@ -1449,6 +1503,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       S.cp.tfl[i] = t.flags;
     }
   }
+  {
+    // this CTA's rank by units (which CTAs merge: merge_ctas)
+    const int part = units_rank_part(P, a.n_blocks, static_cast<int>(gridDim.x),
+                                     static_cast<int>(blockIdx.x), S.cp.u1 - S.cp.u0, tid, nt);
+    const int rank = __syncthreads_count(part);  // (one CTA per thread at most)
+    if (tid == 0) S.cp.mrank = rank;
+  }
   __syncthreads();
   if (a.append_block) {
     // the step's new tokens that lie in this CTA's tiles: how many, and the
@@ -1481,12 +1542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const UnitPos x = unit_pos(P, a.n_blocks, S.cp.us[warp]);
     seg_pre<true>(a, P, S.ps.cache, S.cp.pre[warp], x.b, x.h, lane);
   } else if (warp >= kPre && warp < kPre + kPreItems) {
-    // the record lists of the CTA's first merge items (item k: first + k * grid)
+    // the record lists of the CTA's first merge items (item k: rank + k * nm)
     const int k = warp - kPre;
-    const int it = merge_rank(P, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x)) +
-                   k * static_cast<int>(gridDim.x);
+    const int nm = merge_ctas(a, static_cast<int>(gridDim.x));
+    const int it = S.cp.mrank + k * nm;
     int n = -1;
-    if (it < a.n_rows * a.n_q_heads) {
+    if (S.cp.mrank < nm && it < a.n_rows * a.n_q_heads) {
       n = merge_list(a, P, S.ps.cache, it / a.n_q_heads, it % a.n_q_heads, S.cp.mpre[k], kPreList,
                      S.rank_tmp[k], lane);
       if (n > kPreList) n = -1;
@@ -1549,12 +1610,15 @@ cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStr
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  if (o.plan && ctas > kThreads) return cudaErrorInvalidConfiguration;  // (as launch_decode_tc)
   plan_kernel<<<o.plan ? ctas : 1, kThreads, smem, s>>>(a, o);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                              int ctas, cudaStream_t s) {
+  // the merge CTAs are ranked with one CTA per thread (units_rank_part)
+  if (ctas > kThreads) return cudaErrorInvalidConfiguration;
   const size_t smem = decode_tc_smem_bytes();
   // planned launches run their own instantiations: without the plan-building
   // (and, without appends, the append) code the kernel is far smaller
@@ -1575,21 +1639,23 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const C
     if (e != cudaSuccess) return e;
     configured[which] = true;
   }
-  // cooperative: the merge phase waits on other CTAs, so all must be
-  // resident; a programmatic dependent of the previous kernel (see the
-  // kernel's entry)
+  // A programmatic dependent of the previous kernel on the stream (see the
+  // kernel's entry).  Not a cooperative launch: the merge CTAs wait (with a
+  // bound) only for CTAs of this grid, which hold their SMs from their start
+  // and wait for no one, so every CTA this grid waits for is placed - an SM
+  // frees as soon as a CTA of the previous grid, which never waits for this
+  // one, retires.  The CTAs that merge nothing retire early, and the next
+  // launch's CTAs take those SMs at once.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, a, tk, tv);
 }
 

@@ -557,6 +557,28 @@ __device__ __forceinline__ int merge_rank(const PlanCore &P, int c, int grid) {
   return c >= P.C ? c - P.C : c + (grid - P.C);
 }
 
+// Merge CTAs of the tensor-core kernel: the items go to the nm = ceil(items /
+// 2) CTAs with the most units (ties: the lower index first) - the ones that
+// finish their units last, so their wait for the other CTAs' records is
+// short - while every other CTA retires as soon as its records are out.
+__device__ __forceinline__ int merge_ctas(const DecodeArgs &a, int grid) {
+  const int items = a.n_rows * a.n_q_heads;
+  const int nm = (items + 1) / 2;
+  return nm < grid ? nm : grid;
+}
+// This CTA's rank in that order (units u_mine), counted by the threads
+// tid < nt of a group: the CTAs c' = tid, tid + nt, ... that come before it.
+__device__ __forceinline__ int units_rank_part(const PlanCore &P, int n_blocks, int grid, int c,
+                                               int64_t u_mine, int tid, int nt) {
+  int before = 0;
+  for (int c2 = tid; c2 < grid; c2 += nt) {
+    if (c2 == c) continue;
+    const int64_t u2 = cta_unit_begin(P, n_blocks, c2 + 1) - cta_unit_begin(P, n_blocks, c2);
+    before += (u2 > u_mine || (u2 == u_mine && c2 < c)) ? 1 : 0;
+  }
+  return before;
+}
+
 // The record list of merge item (row r, q head hq) in view order, built by
 // one warp: for every view entry, the records that the CTAs c0..c1 touching
 // segment (block, kv head) wrote at column rank * G + gi.  Returns the number
@@ -620,19 +642,19 @@ __device__ __forceinline__ int merge_list(const DecodeArgs &a, const PlanCore &P
 // an item without records gets out = 0, lse = -inf.
 constexpr int kMergeBatch = 4;
 
+// rank / grid: this CTA's position among the nm CTAs that merge (items rank,
+// rank + nm, ...); a rank at or past nm merges nothing.
 template <typename T, int D, int NL, typename Sync>
 __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCache &MC,
                             MergeSmem<NL> &Z, const int32_t *pre_list, const int32_t *pre_n,
                             int n_pre, int pre_stride, int tid, int nt, Sync sync,
-                            long long wait_limit) {
+                            long long wait_limit, int rank, int grid) {
   constexpr int EPL = D / 32;
   constexpr int64_t RS = D + kRecPad;  // record stride in floats
   constexpr int B = kMergeBatch;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
   const int items = a.n_rows * a.n_q_heads;
-  const int grid = static_cast<int>(gridDim.x);
-  const int rank = merge_rank(P, static_cast<int>(blockIdx.x), grid);
-  const int mine = rank < items ? (items - rank + grid - 1) / grid : 0;
+  const int mine = rank >= 0 && rank < grid && rank < items ? (items - rank + grid - 1) / grid : 0;
 
   for (int k0 = 0; k0 < mine; k0 += NL) {
     const int np = min(mine - k0, NL);  // items merged side by side

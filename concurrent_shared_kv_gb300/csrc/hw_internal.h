@@ -39,6 +39,11 @@ struct DecodeArgs {
   int32_t *err;       // workspace error word (HW_DEV_* bits)
   int32_t *counters;  // [n_rows][Hq] merge arrival counters, zero between calls
   float *partials;    // [slots][kMaxQ][D + kRecPad]: o[0..D), m at D, l at D+1
+  // Tensor-core path: nonzero when the caller promises that the work enqueued
+  // just before this call on the stream writes neither the K/V pools nor the
+  // plan (or metadata) this call reads; the kernel then reads them, and starts
+  // its first K/V tiles, before the previous kernel has completed.
+  int32_t early;
   int32_t n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
   int64_t capacity;
   const uint8_t *plan;  // precomputed plan of the tensor-core kernel (hw_attn_plan), or null

@@ -32,6 +32,12 @@ class DecodeSession:
                                   api.HW_FP8_E4M3 if kv_fp8 else DTYPES[dtype], rope_theta,
                                   head_dim ** -0.5 if scale is None else scale,
                                   flags=api.HW_DESC_VIEW_LIMITS if view_limits else 0)
+        # the same description with the early-loads promise (see early= below)
+        self.desc_early = api.make_desc(n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks,
+                                        max_view_blocks, capacity,
+                                        api.HW_FP8_E4M3 if kv_fp8 else DTYPES[dtype], rope_theta,
+                                        head_dim ** -0.5 if scale is None else scale,
+                                        flags=self.desc.flags | api.HW_DESC_EARLY_LOADS)
         self.ws_bytes = api.attn_decode_workspace_size(self.desc)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         api.workspace_init(self.workspace, self.ws_bytes)
@@ -51,8 +57,8 @@ class DecodeSession:
 
     def decode(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-               want_lse: bool = True, stream=None):
-        d = self.desc
+               want_lse: bool = True, stream=None, early: bool = False):
+        d = self.desc_early if early else self.desc
         if out is None:
             out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
         if lse is None and want_lse:
@@ -99,9 +105,9 @@ class DecodeSession:
     def append_decode_planned(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                               k_cache: torch.Tensor, v_cache: torch.Tensor,
                               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                              want_lse: bool = True, stream=None):
+                              want_lse: bool = True, stream=None, early: bool = False):
         """One layer: its new tokens ([rows][Hkv][D]) written, then decoded."""
-        d = self.desc
+        d = self.desc_early if early else self.desc
         if out is None:
             out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
         if lse is None and want_lse:
@@ -112,9 +118,12 @@ class DecodeSession:
 
     def decode_planned(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                       want_lse: bool = True, stream=None):
-        """One layer against the step's plan (see plan())."""
-        d = self.desc
+                       want_lse: bool = True, stream=None, early: bool = False):
+        """One layer against the step's plan (see plan()).  early=True promises
+        that the work enqueued just before this call on the stream writes
+        neither this layer's K/V pools nor the plan (HW_DESC_EARLY_LOADS): true
+        for every layer of a step after the first one that follows the plan."""
+        d = self.desc_early if early else self.desc
         if out is None:
             out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
         if lse is None and want_lse:
@@ -126,9 +135,9 @@ class DecodeSession:
     def decode_planned_fp8(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            k_scale: torch.Tensor, v_scale: torch.Tensor,
                            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                           want_lse: bool = True, stream=None):
+                           want_lse: bool = True, stream=None, early: bool = False):
         """One layer over E4M3 pools (codes, [Hkv][cap][D]) with float32 scales [Hkv]."""
-        d = self.desc
+        d = self.desc_early if early else self.desc
         if out is None:
             out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
         if lse is None and want_lse:
@@ -142,10 +151,10 @@ class DecodeSession:
                                   k_scale: torch.Tensor, v_scale: torch.Tensor,
                                   out: Optional[torch.Tensor] = None,
                                   lse: Optional[torch.Tensor] = None, want_lse: bool = True,
-                                  stream=None):
+                                  stream=None, early: bool = False):
         """One layer over E4M3 pools: its new tokens (bf16, [rows][Hkv][D])
         written as codes with the head scales, then decoded."""
-        d = self.desc
+        d = self.desc_early if early else self.desc
         if out is None:
             out = torch.empty((d.n_rows, d.n_q_heads, d.head_dim), dtype=self.dtype, device=self.device)
         if lse is None and want_lse:

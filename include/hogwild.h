@@ -109,6 +109,21 @@ typedef struct {
 #define HW_DESC_VIEW_LIMITS 1
 
 /*
+ * A promise from the caller about the work enqueued just before this call on
+ * the same stream (a kernel, a copy, or the previous library call): it writes
+ * neither the K/V pools, nor the metadata arrays or plan, that this call
+ * reads.  q, out, lse and the workspace's other contents may be anything.
+ * With the promise, a bf16 or E4M3 head_dim-128 decode starts while that work
+ * finishes: it reads its plan (or builds it from the metadata) and loads its
+ * first K/V tiles before the previous kernel has completed, and only its
+ * reads of q and its writes wait for it.  In a decode step, set it on every
+ * layer after the first one that follows a plan or commit call.  The promise
+ * is not checked; breaking it gives results computed from stale K/V data or
+ * metadata.  Ignored by the fp32 and head_dim-64 kernels.
+ */
+#define HW_DESC_EARLY_LOADS 2
+
+/*
  * Bytes of workspace hw_attn_decode needs for `d` on the current device.
  * Writes the size to *bytes.  The workspace holds the error word, the merge
  * arrival counters and the per-split partial results (max, sum of exp,

@@ -147,3 +147,12 @@ def test_phase_table_source_is_integer_exact():
             ang = (p * w) % (2 * math.pi)
             diff = (turns * 2 * math.pi - ang + math.pi) % (2 * math.pi) - math.pi
             assert abs(diff) < 1e-9, (i, p, diff)
+
+
+
+def test_early_loads_flag_is_accepted_and_unknown_flags_are_not(L):
+    # the flag passes the description checks: the call gets as far as its
+    # null workspace (HW_ERR_WORKSPACE); an unknown bit is an invalid argument
+    assert call_decode(desc(dtype=api.HW_BF16, head_dim=128, flags=api.HW_DESC_EARLY_LOADS)) == -3
+    assert call_decode(desc(flags=api.HW_DESC_EARLY_LOADS)) == -3
+    assert call_decode(desc(flags=64)) == -1
