@@ -117,6 +117,8 @@ struct alignas(16) CtaPlan {
   int32_t mpre[kPreItems][kPreList];  // record lists of its first merge items
   int32_t mpre_n[kPreItems];          // their lengths, or -1 (not built)
   int32_t mrank;           // its rank among the CTAs by units (merge_ctas: it merges if < nm)
+  int32_t c_log;           // the split's CTA index of this work (see "plans": the order of
+                           // the records is by rank, so a launch's CTA b runs rank b)
   int32_t trow[kStages];   // its first tiles (the ring's first fill): first cache row,
   uint8_t th[kStages];     // kv head,
   uint8_t tfl[kStages];    // segment flags (see TileRef)
@@ -983,7 +985,7 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
   __syncwarp();
   if (lane == 0) mbar_arrive(&S.o_empty[seg & 1]);
   sync();  // every warp's lsave of this segment is in place
-  const int64_t slot = seg_id(a.n_blocks, b, h) + blockIdx.x;
+  const int64_t slot = seg_id(a.n_blocks, b, h) + S.cp.c_log;
   if constexpr (kFp8) {
 #pragma unroll
     for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * vmul);
@@ -1309,6 +1311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (with a plan, the bulk copy brings these: no generic store may race it)
     if (!kPlanned) {
       for (int k = 0; k < kPreItems; ++k) S.cp.mpre_n[k] = -1;
+      S.cp.c_log = static_cast<int32_t>(blockIdx.x);
       S.cp.n_first = 0;
       S.cp.app_n = 0;
     }
@@ -1508,7 +1511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = units_rank_part(P, a.n_blocks, static_cast<int>(gridDim.x),
                                      static_cast<int>(blockIdx.x), S.cp.u1 - S.cp.u0, tid, nt);
     const int rank = __syncthreads_count(part);  // (one CTA per thread at most)
-    if (tid == 0) S.cp.mrank = rank;
+    if (tid == 0) {
+      S.cp.mrank = rank;
+      S.cp.c_log = static_cast<int32_t>(blockIdx.x);
+    }
   }
   __syncthreads();
   if (a.append_block) {
@@ -1555,7 +1561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) S.cp.mpre_n[k] = n;
   }
   __syncthreads();
-  copy16(const_cast<uint8_t *>(plan_cta_record(o.plan, blockIdx.x)), &S.cp, sizeof(CtaPlan), tid, nt);
+  // at the position of its rank: a decode launch's CTA b (CTAs are placed in
+  // index order, the low ones on the SMs the previous launch frees first) runs
+  // the b-th heaviest share, so the heaviest shares - which also merge - get
+  // their SMs first and the light ones take the SMs freed last
+  copy16(const_cast<uint8_t *>(plan_cta_record(o.plan, S.cp.mrank)), &S.cp, sizeof(CtaPlan), tid, nt);
   if (blockIdx.x == 0) {
     copy16(o.plan + kPlanHeaderBytes, &S.ps, sizeof(PlanShared), tid, nt);
     if (tid == 0) {
@@ -1585,10 +1595,11 @@ size_t plan_cta_bytes() { return sizeof(CtaPlan); }
 int plan_export_records(const uint8_t *plan_host, int64_t *out, int max_ctas) {
   const PlanHeader &h = *reinterpret_cast<const PlanHeader *>(plan_host);
   if (h.magic != kPlanMagic || h.grid <= 0 || h.grid > max_ctas) return -1;
-  for (int c = 0; c < h.grid; ++c) {
+  for (int b = 0; b < h.grid; ++b) {
     const CtaPlan &cp = *reinterpret_cast<const CtaPlan *>(
-        plan_host + kPlanHeaderBytes + sizeof(PlanShared) + static_cast<size_t>(c) * sizeof(CtaPlan));
-    int64_t *o = out + static_cast<int64_t>(c) * kPlanExportFields;
+        plan_host + kPlanHeaderBytes + sizeof(PlanShared) + static_cast<size_t>(b) * sizeof(CtaPlan));
+    if (cp.c_log < 0 || cp.c_log >= h.grid) return -1;
+    int64_t *o = out + static_cast<int64_t>(cp.c_log) * kPlanExportFields;  // in split order
     o[0] = cp.u0;
     o[1] = cp.u1;
     o[2] = cp.n_first;

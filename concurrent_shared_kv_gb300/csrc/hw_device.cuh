@@ -178,7 +178,7 @@ __device__ __forceinline__ int entry_rank_scan(const DecodeArgs &a, int e, int l
 // three tiles once the records, arrivals and merge wait are counted; the
 // ratio can be made finer through kTileW.
 constexpr int kTileW = 1;
-constexpr int kSegW = 3;
+constexpr int kSegW = 2;
 
 struct PlanCore {
   int32_t tiles[HW_MAX_BLOCKS];      // tiles per kv head (0: block skipped)

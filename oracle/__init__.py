@@ -388,7 +388,7 @@ def chunk_views(layout: str, block_len: Sequence[int], n_problems: int, n_worker
 # ---------------------------------------------------------------------------
 
 def stream_k_split(block_start, block_len, view_block, n_q_heads: int, n_kv_heads: int,
-                   grid: int, seg_weight: int = 3, tile: int = 128, max_cols: int = 32):
+                   grid: int, seg_weight: int = 2, tile: int = 128, max_cols: int = 32):
     """Units are 128-token tiles of one (block, kv head), kv-head-major, then
     block, then tile.  A block takes part when some view references it, it has
     tokens and (references x group size) <= max_cols.  Every unit weighs 1 and
