@@ -184,10 +184,12 @@ def replica_value(units_per_rank: float, t_max: float, world: int) -> float:
 
 
 def reference_arm(args):
-    """The float64 oracle on the host cores, on the same workload and metric."""
-    import numpy as np
+    """The float64 oracle on the host cores, on the same workload and metric:
+    each step runs the oracle over every layer of the step (the 16-problem
+    serving shape: 2 of its 16 problems of its one timed layer, scaled), and
+    ms_per_step is the time the steps actually took.  Nothing here loads the
+    CUDA library: the views come from the oracle's own builder."""
     import oracle
-    from concurrent_shared_kv_gb300 import api
     from concurrent_shared_kv_gb300 import workloads as wl
 
     rank = int(os.environ.get("RANK", "0"))
@@ -196,34 +198,45 @@ def reference_arm(args):
     w = wl.ALL[args.config]()
     o = oracle.get()
     lens, starts = w.block_lengths(), w.block_starts()
-    vb, vo, qp = api.views_combined(lens, w.n_problems, w.n_workers)
+    vb, vo, qp = oracle.combined_views(lens, w.n_problems, w.n_workers)
     cores = len(os.sched_getaffinity(0))
-    # each step: one full layer (all rows, all heads) of the workload; for the
-    # ragged serving shape, 2 of its 16 problems
-    rows = None if args.config != "C5" else list(range(0, 4)) + list(range(60, 64))
+    serving = args.config == "C5"
+    rows = None if not serving else list(range(0, 4)) + list(range(60, 64))
     frac_rows = 1.0 if rows is None else len(rows) / w.n_rows
+    layers = w.layers if not serving else 1
+    if args.layers > 0:
+        layers = min(layers, args.layers)
+    # four distinct layers cycled through the step's calls (64 layers of host
+    # inputs would take gigabytes; the oracle's time does not depend on the values)
+    inputs = [wl.draw_host(w, l) for l in range(min(layers, 4))]
     times = []
-    q, k, v = wl.draw_host(w, 0)
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        o.attn_decode(q=q, k_cache=k, v_cache=v, block_start=starts, block_len=lens,
-                      view_block=vb, view_offset=vo, q_pos=qp, n_kv_heads=w.n_kv_heads,
-                      rope_theta=w.rope_theta, scale=w.scale,
-                      dtype=oracle.F32 if w.dtype == "f32" else oracle.BF16, rows=rows,
-                      n_threads=cores)
+        for l in range(layers):
+            q, k, v = inputs[l % len(inputs)]
+            o.attn_decode(q=q, k_cache=k, v_cache=v, block_start=starts, block_len=lens,
+                          view_block=vb, view_offset=vo, q_pos=qp, n_kv_heads=w.n_kv_heads,
+                          rope_theta=w.rope_theta, scale=w.scale,
+                          dtype=oracle.F32 if w.dtype == "f32" else oracle.BF16, rows=rows,
+                          n_threads=cores)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    t_layer = statistics.median(times) / frac_rows
-    gbs = w.kv_bytes_per_layer() / t_layer / 1e9
-    sample = (f"one layer per step ({'all rows' if rows is None else 'problems 0 and 15, scaled to 16'}),"
-              f" float64 oracle, {cores} threads")
+    t_step = statistics.median(times)
+    done_bytes = w.kv_bytes_per_layer() * layers * frac_rows
+    gbs = done_bytes / t_step / 1e9
+    t_layer = t_step / layers / frac_rows
+    sample = (f"{layers} layer calls per step (4 distinct layers' inputs cycled), all rows and heads, "
+              f"float64 oracle, {cores} threads"
+              if rows is None else
+              f"problems 0 and 15 of the one timed layer per step (2 of 16), float64 oracle, "
+              f"{cores} threads; GB/s of the KV those rows read")
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": t_layer * workload_config(w, args.config)["layers_per_step"] * 1e3,
+        "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, args.config),
+        "config": workload_config(w, args.config, layers=layers),
         "worker_tokens_per_s_per_layer": w.n_rows / t_layer,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
@@ -560,19 +573,24 @@ def main():
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and chunk == 0 and not fp8:
-        line["cpu_baseline"] = timed_oracle(w, qs, ks, vs, starts, lens, vb, vo, qp)
+        line["cpu_baseline"] = timed_oracle(w, qs, ks, vs, starts, lens, args.layout)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def timed_oracle(w, qs, ks, vs, starts, lens, vb, vo, qp, budget_s=12.0):
+def timed_oracle(w, qs, ks, vs, starts, lens, layout, budget_s=12.0):
     """The oracle, as it stands, over whole layers of the same workload on the
     host cores for about budget_s seconds (at least one layer); GB/s of KV."""
     import numpy as np
     import torch
     import oracle
+
+    # the timed step's views, from the oracle's own builders
+    build_views = {"combined": oracle.combined_views, "interleaved": oracle.interleaved_views,
+                   "contiguous": oracle.contiguous_views}[layout]
+    vb, vo, qp = build_views(lens, w.n_problems, w.n_workers)
 
     def host(t):
         t = t.detach().cpu().contiguous()

@@ -31,7 +31,8 @@ EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode
            "hw_attn_append_decode_planned_fp8",
            "hw_attn_append_decode_planned", "hw_plan_export", "hw_attn_decode_noalloc",
            "hw_block_commit", "hw_block_commit_many", "hw_workspace_status", "hw_views_combined",
-           "hw_views", "hw_views_chunked", "hw_last_cuda_error", "hw_status_string"]
+           "hw_views", "hw_views_chunked", "hw_last_cuda_error", "hw_status_string",
+           "hw_test_set_merge_wait_limit", "hw_noalloc_status"]
 HW_LAYOUT_COMBINED, HW_LAYOUT_INTERLEAVED, HW_LAYOUT_CONTIGUOUS = 0, 1, 2
 LAYOUTS = {"combined": HW_LAYOUT_COMBINED, "interleaved": HW_LAYOUT_INTERLEAVED,
            "contiguous": HW_LAYOUT_CONTIGUOUS}
@@ -100,6 +101,8 @@ def lib(path: Optional[str] = None):
     L.hw_views.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
     L.hw_views_chunked.argtypes = [ctypes.c_int32] * 4 + [_P] * 5
     L.hw_last_cuda_error.argtypes = []
+    L.hw_test_set_merge_wait_limit.argtypes = [ctypes.c_int64]
+    L.hw_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int32), _P]
     L.hw_status_string.argtypes = [ctypes.c_int]
     L.hw_status_string.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -356,3 +359,16 @@ def status_string(st: int) -> str:
 
 def last_cuda_error() -> int:
     return int(lib().hw_last_cuda_error())
+
+
+def noalloc_status(stream=None) -> int:
+    """hw_noalloc_status: the no-allocation calls' device error bits (read and cleared)."""
+    f = ctypes.c_int32(0)
+    _check("hw_noalloc_status", lib().hw_noalloc_status(ctypes.byref(f), _stream(stream)))
+    return int(f.value)
+
+
+def test_set_merge_wait_limit(cycles: int):
+    """hw_test_set_merge_wait_limit: the merge's wait bound (SM cycles) for the
+    calls that follow; 0 restores the default."""
+    _check("hw_test_set_merge_wait_limit", lib().hw_test_set_merge_wait_limit(int(cycles)))

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <vector>
+#include <atomic>
 #include <mutex>
 
 #include "hogwild.h"
@@ -16,6 +17,10 @@
 namespace hw {
 
 static thread_local int g_last_cuda_error = 0;
+
+// The merge's wait bound for calls made after hw_test_set_merge_wait_limit.
+constexpr long long kDefaultMergeWait = 2000000000ll;  // ~1 s at 2 GHz
+static std::atomic<long long> g_merge_wait{kDefaultMergeWait};
 
 static int cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -187,6 +192,12 @@ int hw_attn_decode_workspace_size(const hw_attn_desc *d, size_t *bytes) {
   return HW_OK;
 }
 
+int hw_test_set_merge_wait_limit(int64_t cycles) {
+  if (cycles < 0) return HW_ERR_INVALID;
+  g_merge_wait.store(cycles == 0 ? kDefaultMergeWait : static_cast<long long>(cycles));
+  return HW_OK;
+}
+
 int hw_workspace_init(void *workspace, size_t bytes, void *stream) {
   if (!workspace || bytes < 256) return HW_ERR_WORKSPACE;
   const cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream));
@@ -216,6 +227,7 @@ static void fill_args(DecodeArgs &a, const hw_attn_desc *d, const WorkspaceLayou
   a.counters = reinterpret_cast<int32_t *>(ws + L.counters_off);
   a.partials = reinterpret_cast<float *>(ws + L.partials_off);
   a.early = (d->flags & HW_DESC_EARLY_LOADS) != 0;
+  a.wait_limit = g_merge_wait.load();
   a.n_rows = d->n_rows;
   a.n_q_heads = d->n_q_heads;
   a.n_kv_heads = d->n_kv_heads;

@@ -79,3 +79,25 @@ extern "C" int hw_attn_decode_noalloc(const hw_attn_desc *d, const void *q, cons
   return hw_attn_decode(d, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
                         q_pos, q_to_kv, out, lse, scratch, HW_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+// The scratch's error word (its first 4 bytes, like a workspace's): read into
+// host memory and cleared, with plain copies - nothing is allocated.  A device
+// whose scratch was never set up has no error.
+extern "C" int hw_noalloc_status(int32_t *flags, void *stream) {
+  if (!flags) return HW_ERR_INVALID;
+  *flags = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return HW_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return HW_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    scratch = g_scratch_ptr[dev];
+  }
+  if (!scratch) return HW_OK;
+  e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaMemcpy(flags, scratch, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(scratch, 0, sizeof(int32_t));
+  return e == cudaSuccess ? HW_OK : HW_ERR_CUDA;
+}

@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
   }
   __syncthreads();
   merge_phase<T, D, 1>(a, P, S.cache, S.merge, nullptr, nullptr, 0, 0, threadIdx.x, kSimtThreads,
-                    CtaSync(), 2000000000ll,
+                    CtaSync(), a.wait_limit,
                        merge_rank(P, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x)),
                        static_cast<int>(gridDim.x));
 }

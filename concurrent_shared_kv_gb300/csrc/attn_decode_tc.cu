@@ -1440,7 +1440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     merge_phase<__nv_bfloat16, 128, 8>(a, S.ps.plan, S.ps.cache,
                                        *reinterpret_cast<MergeSmem<8> *>(S.stage[0]),
                                        &S.cp.mpre[0][0], S.cp.mpre_n, kPreItems, kPreList, tid,
-                                       kThreads, CtaSync(), kWaitLimit, S.cp.mrank,
+                                       kThreads, CtaSync(), a.wait_limit, S.cp.mrank,
                                        merge_ctas(a, static_cast<int>(gridDim.x)));
 }
 

@@ -44,6 +44,9 @@ struct DecodeArgs {
   // plan (or metadata) this call reads; the kernel then reads them, and starts
   // its first K/V tiles, before the previous kernel has completed.
   int32_t early;
+  // Bound of the merge's wait for an item's records, in SM clock cycles
+  // (hw_test_set_merge_wait_limit; ~1 s by default).
+  int64_t wait_limit;
   int32_t n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
   int64_t capacity;
   const uint8_t *plan;  // precomputed plan of the tensor-core kernel (hw_attn_plan), or null

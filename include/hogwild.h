@@ -28,6 +28,13 @@
  *    D contiguous, element type `dtype`; a block is the token range
  *    [block_start, block_start + block_len) of every head.  Keys are stored
  *    already rotated by RoPE at block-local positions 0 .. len-1.
+ *  - Limits of that layout: every block of a call lives in that one pair of
+ *    pools (the kernels address it through one TMA descriptor per pool), so a
+ *    cache whose blocks are separate allocations - a per-block pointer, as in
+ *    the article's CacheBlock - is laid out in one pool (or copied into one)
+ *    before the call; and block_start, block_len and the capacity are 32-bit:
+ *    at most 2^31 - 1 tokens per head and pool (larger capacities return
+ *    HW_ERR_UNSUPPORTED).
  *  - RoPE pairs element i with element i + D/2 (rotate_half) at frequency
  *    w_i = rope_theta^(-2i/D).
  *  - Every call returns an hw_status.  Argument errors are found on the host
@@ -333,14 +340,26 @@ int hw_plan_export(const hw_attn_desc *d, const void *workspace, size_t workspac
  *    Order them on one stream.
  *  - Returns HW_ERR_WORKSPACE, before enqueuing anything, when `d` needs more
  *    scratch than HW_NOALLOC_SCRATCH_BYTES; use hw_attn_decode then.
- *  - Device-side metadata errors (HW_DEV_*) are not reported: there is no
- *    workspace to read them from.
+ *  - Device-side metadata errors (HW_DEV_*) are recorded in the scratch, in
+ *    place of a workspace: hw_noalloc_status reads and clears them.
+ *  - The array's device address is looked up once per device ordinal and kept:
+ *    calling after cudaDeviceReset (or any reset of the device's primary
+ *    context) in the same process is not supported.
  */
 int hw_attn_decode_noalloc(const hw_attn_desc *d, const void *q, const void *k_cache,
                            const void *v_cache, const int32_t *block_start,
                            const int32_t *block_len, const int32_t *view_block,
                            const int32_t *view_offset, const int32_t *q_pos,
                            const int32_t *q_to_kv, void *out, float *lse, void *stream);
+
+/*
+ * The device error bits (HW_DEV_*, 0 = none) that hw_attn_decode_noalloc calls
+ * on the current device recorded since the last read, into *flags, and
+ * cleared; like hw_workspace_status, for callers that cannot allocate: it
+ * synchronises `stream` and uses plain copies to and from host memory, so it
+ * allocates nothing.  0 when no such call ran on the device yet.
+ */
+int hw_noalloc_status(int32_t *flags, void *stream);
 
 /*
  * Block commit over n_layers layers in one launch (a finished step moves
@@ -436,6 +455,18 @@ int hw_views(int32_t layout, int32_t n_problems, int32_t n_workers, const int32_
 int hw_views_chunked(int32_t layout, int32_t n_problems, int32_t n_workers, int32_t chunk,
                      const int32_t *block_len, int32_t *view_block, int32_t *view_offset,
                      int32_t *view_limit, int32_t *q_pos);
+
+/*
+ * For tests of the bounded waits (the pages have no counterpart).  The merge
+ * step of a decode waits for every partial result of a (row, q head) item
+ * with a bound; past it the call gives up on that item (its out and lse rows
+ * are left as they were), records HW_DEV_TIMEOUT in the workspace and
+ * returns.  This sets that bound, in SM clock cycles, for every decode call
+ * made afterwards in the process; 0 restores the default (about one second).
+ * HW_ERR_INVALID for a negative value.  A workspace whose call timed out is to
+ * be reinitialised (hw_workspace_init) before its next use.
+ */
+int hw_test_set_merge_wait_limit(int64_t cycles);
 
 /* Last CUDA error code seen by this thread's library calls (cudaError_t). */
 int hw_last_cuda_error(void);

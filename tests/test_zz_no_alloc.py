@@ -57,3 +57,22 @@ def test_noalloc_rejects_descriptions_beyond_the_scratch():
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     st = api.lib().hw_attn_decode_noalloc(ctypes.byref(d), *([dummy.data_ptr()] * 12), None)
     assert st == -3  # HW_ERR_WORKSPACE, nothing enqueued
+
+
+def test_noalloc_status_reports_device_errors():
+    # seven workers at five query heads per kv head put 35 query columns on
+    # every block, more than a tile serves: the plan skips the blocks and
+    # records HW_DEV_TOO_MANY_REFS, which the no-allocation status call reads
+    # (and clears) without a workspace
+    w = wl.Workload("wide", "bf16", 1, 7, 40, 8, 128, 1e6, 1, [512], [[64] * 7], seed=21)
+    c = H.device_case(w, 0)
+    s = c.session()
+    m = s.meta
+    api.noalloc_status()  # start from a clear word (earlier calls may have left bits)
+    out = torch.empty((w.n_rows, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.n_rows, w.n_q_heads), device="cuda")
+    api.attn_decode_noalloc(s.desc, c.q, c.k, c.v, m["block_start"], m["block_len"],
+                            m["view_block"], m["view_offset"], m["q_pos"], out, lse,
+                            q_to_kv=m["q_to_kv"])
+    assert api.noalloc_status() & 8  # HW_DEV_TOO_MANY_REFS
+    assert api.noalloc_status() == 0  # read and cleared
