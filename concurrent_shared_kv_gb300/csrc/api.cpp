@@ -124,7 +124,10 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
   const int sms = device_sm_count();
   const size_t plan = kPlanHeaderBytes + plan_shared_bytes() +
                       static_cast<size_t>(sms > 0 ? sms : 0) * plan_cta_bytes();
-  L.total = L.plan_off + up(plan);
+  // hw_attn_decode's own plan (tensor-core path): a second region of the same
+  // size, so that it never overwrites the step's plan of hw_attn_plan
+  L.uplan_off = L.plan_off + up(plan);
+  L.total = L.uplan_off + up(plan);
   return L;
 }
 
@@ -254,9 +257,13 @@ static int decode_common(const hw_attn_desc *d, const void *q, const void *k_cac
                          int max_ctas, void *stream, const int32_t *append_block = nullptr,
                          const int32_t *append_pos = nullptr, const void *k_new = nullptr,
                          const void *v_new = nullptr, const int32_t *view_limit = nullptr,
-                         const float *k_scale = nullptr, const float *v_scale = nullptr) {
+                         const float *k_scale = nullptr, const float *v_scale = nullptr,
+                         bool plan_follows = false) {
   DecodeArgs a;
   fill_args(a, d, L, workspace);
+  // right after its own plan launch, a decode reads that plan only after the
+  // wait: the promise of early loads covers the caller's data, not this plan
+  if (plan_follows) a.early = 0;
   a.view_limit = view_limit;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
@@ -346,6 +353,29 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
   int max_ctas = 0;
   st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
   if (st != HW_OK) return st;
+  if (tensor_core_path(d)) {
+    // Two launches, no host round trip: the plan of this call's metadata
+    // (into the workspace's own region for it, not the step's plan), then the
+    // planned decode over the caller's arrays.  The plan is a programmatic
+    // dependent of the previous kernel (with the early-loads promise it reads
+    // the metadata before that kernel completes) and the decode of the plan.
+    DecodeArgs a;
+    fill_args(a, d, L, workspace);
+    a.block_start = block_start;
+    a.block_len = block_len;
+    a.view_block = view_block;
+    a.view_offset = view_offset;
+    a.q_pos = q_pos;
+    a.q_to_kv = q_to_kv;
+    PlanOut o;
+    std::memset(&o, 0, sizeof o);  // no metadata copies: the decode reads the caller's arrays
+    o.plan = static_cast<uint8_t *>(workspace) + L.uplan_off;
+    const cudaError_t e = launch_plan(a, o, device_sm_count(), static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return decode_common(d, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
+                         q_pos, q_to_kv, o.plan, out, lse, workspace, L, max_ctas, stream, nullptr,
+                         nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, true);
+  }
   return decode_common(d, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
                        q_pos, q_to_kv, nullptr, out, lse, workspace, L, max_ctas, stream);
 }

@@ -1279,8 +1279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // global memory and reads only what cannot be in flight: an L2 prefetch of
   // q (which never changes a result) and - when the caller promised that the
   // previous work writes neither (a.early) - its plan or metadata and its
-  // first K/V tiles.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // first K/V tiles.  The next launch on the stream may start once every CTA
+  // holds its plan (below): a plan launch that follows may then rewrite it.
   if (tid == 0) {
     tma_prefetch_desc(&tm_k);  // (kernel parameters)
     tma_prefetch_desc(&tm_v);
@@ -1384,6 +1384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int issued = 0;  // tiles the producer issued before griddepcontrol.wait
   if (early) {
     get_plan();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the first tiles into the empty ring (not past the first tile that
     // holds a new token: those are written after the wait)
     if (tid == 0 && S.plan_ok && S.cp.u0 < S.cp.u1) {
@@ -1393,7 +1394,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid is complete
-  if (!early) get_plan();
+  if (!early) {
+    get_plan();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  }
   if (plan_timeout) flag_error(a.err, HW_DEV_TIMEOUT);
   const uint32_t tmem = S.tmem_base;
   const bool ok = S.plan_ok != 0;
@@ -1467,7 +1471,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               ~static_cast<uintptr_t>(15));
   const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.n_rows * a.n_view, G = a.n_q_heads / a.n_kv_heads;
-  if (blockIdx.x == 0) {
+  // Launched as a programmatic dependent (hw_attn_decode's own plan, into a
+  // region no other call reads) this kernel may start while the previous one
+  // runs: it reads the caller's metadata before griddepcontrol.wait only
+  // under the early-loads promise, and ends after the wait, so that its
+  // completion implies the previous grid's.  (A plain launch: the wait
+  // returns at once.)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (blockIdx.x == 0 && o.view_block) {
     for (int i = tid; i < E; i += nt) {
       o.view_block[i] = a.view_block[i];
       o.view_offset[i] = a.view_offset[i];
@@ -1484,7 +1496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = tid; i < E; i += nt) o.view_limit[i] = a.view_limit ? a.view_limit[i] : -1;
   }
-  if (!o.plan) return;
+  if (!o.plan) {
+    if (a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
   PlanCore &P = S.ps.plan;
   build_plan<kT>(a, P, S.ps.cache, S.scratch, *reinterpret_cast<int64_t(*)[2]>(&S.cp.u0));
   plan_ranks(a, S.ps.cache, warp, lane, 0, 1);
@@ -1583,6 +1598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<PlanHeader *>(o.plan) = h;
     }
   }
+  if (a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -1612,7 +1628,8 @@ int plan_export_records(const uint8_t *plan_host, int64_t *out, int max_ctas) {
   return h.grid;
 }
 
-cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s) {
+cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s,
+                        bool dependent) {
   const size_t smem = sizeof(PlanSmem) + 16;
   static bool configured = false;
   if (!configured) {
@@ -1622,8 +1639,21 @@ cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStr
     configured = true;
   }
   if (o.plan && ctas > kThreads) return cudaErrorInvalidConfiguration;  // (as launch_decode_tc)
-  plan_kernel<<<o.plan ? ctas : 1, kThreads, smem, s>>>(a, o);
-  return cudaGetLastError();
+  if (!dependent) {
+    plan_kernel<<<o.plan ? ctas : 1, kThreads, smem, s>>>(a, o);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(o.plan ? ctas : 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, a, o);
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,

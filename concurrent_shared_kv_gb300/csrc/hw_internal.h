@@ -71,7 +71,7 @@ struct DecodeArgs {
 // Workspace layout helpers (bytes).  The metadata copies and the plan are
 // written by hw_attn_plan and read by hw_attn_decode_planned.
 struct WorkspaceLayout {
-  size_t err_off, counters_off, partials_off, meta_off, plan_off, total;
+  size_t err_off, counters_off, partials_off, meta_off, plan_off, uplan_off, total;
   int64_t slots;
 };
 constexpr size_t kPlanHeaderBytes = 256;
@@ -100,7 +100,10 @@ struct PlanOut {
   int32_t *append_block, *append_pos;  // -1 / 0 for every row without an append
   int32_t *view_limit;                 // -1 for every entry without a limit
 };
-cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s);
+// dependent: launched as a programmatic dependent of the previous kernel
+// (hw_attn_decode's own plan); otherwise a plain launch (hw_attn_plan).
+cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s,
+                        bool dependent = false);
 int decode_simt_ctas_per_sm(int dtype, int head_dim);
 
 // One launch commits n_commits ranges (kernel grid row c = commit c).
