@@ -36,7 +36,8 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--config", default="C3", choices=["C2", "C3", "C4", "C5"])
+    p.add_argument("--config", default="C3", choices=["C2", "C3", "C4", "C5", "W8"],
+                   help="W8: the C3 shape with eight workers (40 query columns a block)")
     p.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph")
     p.add_argument("--layout", default="combined", choices=["combined", "interleaved", "contiguous"],
                    help="views of the cache layout (the combined layout is the method's own)")
@@ -195,7 +196,7 @@ def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = wl.ALL[args.config]()
+    w = {**wl.ALL, **wl.EXTRA}[args.config]()
     o = oracle.get()
     lens, starts = w.block_lengths(), w.block_starts()
     vb, vo, qp = oracle.combined_views(lens, w.n_problems, w.n_workers)
@@ -265,7 +266,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    w = wl.ALL[args.config]()
+    w = {**wl.ALL, **wl.EXTRA}[args.config]()
     commit_all = args.commit_all and args.config == "C4"
     if commit_all:
         w = dataclasses.replace(w, name=w.name + ", all 4 workers' blocks committed per step",

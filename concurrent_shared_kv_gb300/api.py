@@ -254,9 +254,10 @@ def attn_append_decode_planned(desc: AttnDesc, q, k_new, v_new, k_cache, v_cache
 
 
 def plan_export(desc: AttnDesc, workspace, workspace_bytes: int, max_ctas: int = 1024, stream=None):
-    """hw_plan_export: the plan's per-CTA work split as an int64 array [ctas][12]
-    (u0, u1, n_first, first rows x3, kv heads x3, segment flags x3)."""
-    out = np.zeros((max_ctas, 12), np.int64)
+    """hw_plan_export: the plan's per-CTA work split as an int64 array [ctas][15]
+    (u0, u1, n_first, first rows x3, kv heads x3, segment flags x3, column
+    groups x3)."""
+    out = np.zeros((max_ctas, 15), np.int64)
     n = ctypes.c_int32(0)
     st = lib().hw_plan_export(ctypes.byref(desc), _ptr(workspace), int(workspace_bytes),
                               out.ctypes.data, int(max_ctas), ctypes.byref(n), _stream(stream))

@@ -110,7 +110,12 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
   L.counters_off = 256;
   const size_t counters = static_cast<size_t>(d.n_rows) * d.n_q_heads * sizeof(int32_t);
   L.partials_off = L.counters_off + up(counters);
-  L.slots = static_cast<int64_t>(d.n_blocks) * d.n_kv_heads + max_ctas;
+  // segments per kv head: sum over referenced blocks of ceil(refs / rpg)
+  // column groups <= n_blocks + floor(entries / rpg) (rpg = references a
+  // group holds), then one more slot per CTA
+  const int64_t rpg = kMaxQ / (d.n_q_heads / d.n_kv_heads);
+  const int64_t n_entries = static_cast<int64_t>(d.n_rows) * d.max_view_blocks;
+  L.slots = (d.n_blocks + n_entries / rpg) * d.n_kv_heads + max_ctas;
   const size_t rec = static_cast<size_t>(kMaxQ) * (d.head_dim + kRecPad) * sizeof(float);
   L.meta_off = L.partials_off + up(static_cast<size_t>(L.slots) * rec);
   // metadata copies: view_block, view_offset (rows x V), q_pos, q_to_kv, block_start, block_len,
@@ -671,6 +676,7 @@ int hw_views(int32_t layout, int32_t n_problems, int32_t n_workers, const int32_
       layout != HW_LAYOUT_CONTIGUOUS)
     return HW_ERR_INVALID;
   if (n_problems < 0 || n_workers <= 0) return HW_ERR_INVALID;
+  if (n_workers > HW_MAX_REFS_PER_BLOCK) return HW_ERR_UNSUPPORTED;  // W rows name each block
   if (n_problems == 0) return HW_OK;
   if (!block_len || !view_block || !view_offset || !q_pos) return HW_ERR_INVALID;
   const int W = n_workers, V = n_workers + 1;
@@ -707,6 +713,8 @@ int hw_views_chunked(int32_t layout, int32_t n_problems, int32_t n_workers, int3
                      const int32_t *block_len, int32_t *view_block, int32_t *view_offset,
                      int32_t *view_limit, int32_t *q_pos) {
   if (chunk <= 0 || n_problems < 0 || n_workers <= 0) return HW_ERR_INVALID;
+  // W * chunk rows name each block of a problem
+  if (static_cast<int64_t>(n_workers) * chunk > HW_MAX_REFS_PER_BLOCK) return HW_ERR_UNSUPPORTED;
   if (n_problems == 0) return HW_OK;
   if (!block_len || !view_block || !view_offset || !view_limit || !q_pos) return HW_ERR_INVALID;
   const int W = n_workers, V = n_workers + 1, T = chunk;

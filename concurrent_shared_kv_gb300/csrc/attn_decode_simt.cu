@@ -88,17 +88,17 @@ __device__ __forceinline__ void load_tile(const DecodeArgs &a, SimtSmem<D> &S, i
 }
 
 template <typename T, int D>
-__device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, int t0, int t1) {
+__device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int g, int h, int t0, int t1) {
   PlanCore &P = S.plan;
   SegMeta &M = S.meta;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = a.n_q_heads / a.n_kv_heads;
   if (warp == 0) {
-    gather_refs(a, S.cache, M, b, lane);
+    gather_refs(a, S.cache, M, b, g, lane);
     gather_qheads(a, S.cache, M, h, lane);
   }
   __syncthreads();
-  const int nq = M.n_ref * G;  // <= kMaxQ: blocks with more are skipped by the plan
+  const int nq = M.n_ref * G;  // <= kMaxQ: a column group holds at most that many
 
   // 1. rotated queries: q~ = rho(q, i_q - offset), fp32
   for (int idx = tid; idx < nq * (D / 2); idx += kSimtThreads) {
@@ -189,7 +189,7 @@ __device__ void simt_segment(const DecodeArgs &a, SimtSmem<D> &S, int b, int h, 
   }
 
   // 4. partial records into slot seg + c, then arrival and merges
-  const int64_t slot = seg_id(a.n_blocks, b, h) + blockIdx.x;
+  const int64_t slot = seg_id(P, b, g, h) + blockIdx.x;
 #pragma unroll
   for (int k = 0; k < QPT; ++k) {
     const int qi = qbase + k * QSTEP;
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
   while (u < u_end) {
     const UnitPos x = unit_pos(P, a.n_blocks, u);
     const int64_t seg_stop = min(x.seg_first + x.tiles, u_end);
-    simt_segment<T, D>(a, S, x.b, x.h, static_cast<int>(u - x.seg_first),
+    simt_segment<T, D>(a, S, x.b, x.g, x.h, static_cast<int>(u - x.seg_first),
                        static_cast<int>(seg_stop - x.seg_first));
     u = seg_stop;
   }

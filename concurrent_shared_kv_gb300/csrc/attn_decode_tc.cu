@@ -465,15 +465,15 @@ __device__ __forceinline__ int entry_limit(const int32_t *view_limit, int e, int
   return v >= 0 && v < len ? v : len;
 }
 
-// Query-side metadata of segment (b, h) into X, by one warp (shared memory
+// Query-side metadata of segment (block b, column group g, kv head h) into X, by one warp (shared memory
 // only, except for views beyond the metadata cache), with the fewest tokens
 // any of its columns attends (len when no view limit cuts the block).
 template <bool kLimit>
 __device__ void seg_pre(const DecodeArgs &a, const PlanCore &P, const MetaCache &C, SegQ &X, int b,
-                        int h, int lane) {
+                        int g, int h, int lane) {
   const int len = P.len[b];
   const int G = a.n_q_heads / a.n_kv_heads;
-  gather_refs(a, C, X.m, b, lane);
+  gather_refs(a, C, X.m, b, g, lane);
   gather_qheads(a, C, X.m, h, lane);
   __syncwarp();
   int lim = len;
@@ -648,7 +648,7 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
   };
   if (w == 0 && !kPlanned) {  // a plan brings it ready-made
     const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u0);
-    seg_pre<false>(a, S.ps.plan, S.ps.cache, S.cp.pre[0], x.b, x.h, lane);
+    seg_pre<false>(a, S.ps.plan, S.ps.cache, S.cp.pre[0], x.b, x.g, x.h, lane);
   }
   sync();
   const SegQ &X = S.cp.pre[0];
@@ -775,8 +775,9 @@ __device__ void append_tokens(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_
         if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
           pos = __ldg(a.append_pos + r);
           if (pos >= 0 && pos < P.len[b]) {
-            const int64_t u = static_cast<int64_t>(h) * P.UH + P.ubase[b] + pos / kT;
-            mine = u >= u0 && u < u1;
+            // (every CTA reading the token's tile, for any column group, writes
+            // it - the same bytes - before its own copy of the tile)
+            mine = tile_unit_in(P, b, h, pos / kT, u0, u1) >= 0;
             row = P.start[b] + pos;
           }
         }
@@ -832,7 +833,7 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
     for (int k = 1; k < kPre; ++k) {
       if ((k & 1) == wq && S.cp.us[k] < u1) {
         const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, S.cp.us[k]);
-        seg_pre<kLimit>(a, S.ps.plan, S.ps.cache, S.cp.pre[k], x.b, x.h, lane);
+        seg_pre<kLimit>(a, S.ps.plan, S.ps.cache, S.cp.pre[k], x.b, x.g, x.h, lane);
       }
     }
     sync();
@@ -940,7 +941,7 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
       if (u_prep < u1) {
         const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u_prep);
         SegQ &N = S.cp.pre[(seg + 2) % kPre];
-        if (wq == 0) seg_pre<kLimit>(a, S.ps.plan, S.ps.cache, N, x.b, x.h, lane);
+        if (wq == 0) seg_pre<kLimit>(a, S.ps.plan, S.ps.cache, N, x.b, x.g, x.h, lane);
         u_prep = x.seg_first + x.tiles;
       }
       sync();
@@ -972,7 +973,7 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[kN], int lane) {
 // completed; the arrivals are left to the query warps.
 // (E4M3 caches: O times the v_scale of the segment's kv head.)
 template <bool kFp8>
-__device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int seg, int b, int h,
+__device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int seg, int64_t sid,
                                 int nq, int ws, int lane, int row, NamedSync<1, 128> sync,
                                 float vmul) {
   wait_or_abort(S, a, &S.o_full[seg & 1], (seg >> 1) & 1);
@@ -985,7 +986,7 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
   __syncwarp();
   if (lane == 0) mbar_arrive(&S.o_empty[seg & 1]);
   sync();  // every warp's lsave of this segment is in place
-  const int64_t slot = seg_id(a.n_blocks, b, h) + S.cp.c_log;
+  const int64_t slot = sid + S.cp.c_log;
   if constexpr (kFp8) {
 #pragma unroll
     for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * vmul);
@@ -1061,7 +1062,8 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
   // count of column `lane` (broadcast to the others on the tiles that need it)
   int minlim = INT_MAX, lim_mine = INT_MAX;
   float qmul = 1.f, vmul = 1.f, pend_vmul = 1.f;  // E4M3: score and output factors
-  int pend = -1, pend_b = 0, pend_h = 0, pend_nq = 0;  // segment whose records are due
+  int pend = -1, pend_nq = 0;  // segment whose records are due
+  int64_t pend_sid = 0;        // (its seg_id)
   UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u0);  // then advanced unit by unit
   for (int i = 0; i < n; ++i) {
     const int64_t u = u0 + i;
@@ -1236,7 +1238,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     if (threadIdx.x == kWarpSoft * 32) *reinterpret_cast<volatile int32_t *>(&S.tiles_done) = i + 1;
 
     if (pend >= 0) {  // records of the previous segment, one tile late
-      segment_records<kFp8>(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync, pend_vmul);
+      segment_records<kFp8>(a, S, tl, pend, pend_sid, pend_nq, ws, lane, row, sync, pend_vmul);
       pend = -1;
     }
     if (last) {
@@ -1248,14 +1250,13 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       S.lsave[seg & 1][ws][lane] = v[0];
       if (ws == 0) S.msave[seg & 1][lane] = m_mine;
       pend = seg;
-      pend_b = x.b;
-      pend_h = x.h;
+      pend_sid = seg_id(S.ps.plan, x.b, x.g, x.h);
       pend_nq = nq;
       pend_vmul = vmul;
     }
   }
   if (pend >= 0)
-    segment_records<kFp8>(a, S, tl, pend, pend_b, pend_h, pend_nq, ws, lane, row, sync, pend_vmul);
+    segment_records<kFp8>(a, S, tl, pend, pend_sid, pend_nq, ws, lane, row, sync, pend_vmul);
 }
 
 // kPlanned: the step's plan is loaded (else built in-kernel); kAppend (with a
@@ -1546,8 +1547,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       if (P.tiles[b] == 0) continue;  // a block no view reads takes no part
-      const int64_t u = static_cast<int64_t>(h) * P.UH + P.ubase[b] + pos / kT;
-      if (u >= S.cp.u0 && u < S.cp.u1) {
+      // the first of this CTA's units that read the token's tile (one per
+      // column group): every CTA reading it writes the token - the same bytes
+      const int64_t u = tile_unit_in(P, b, h, pos / kT, S.cp.u0, S.cp.u1);
+      if (u >= 0) {
         const int k = atomicAdd(&S.cp.app_n, 1);
         atomicMin(&S.cp.app_tile, static_cast<int>(u - S.cp.u0));
         if (k < kAppList) {
@@ -1561,7 +1564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp < kPre && S.cp.us[warp] < S.cp.u1) {
     const UnitPos x = unit_pos(P, a.n_blocks, S.cp.us[warp]);
-    seg_pre<true>(a, P, S.ps.cache, S.cp.pre[warp], x.b, x.h, lane);
+    seg_pre<true>(a, P, S.ps.cache, S.cp.pre[warp], x.b, x.g, x.h, lane);
   } else if (warp >= kPre && warp < kPre + kPreItems) {
     // the record lists of the CTA's first merge items (item k: rank + k * nm)
     const int k = warp - kPre;
@@ -1611,6 +1614,7 @@ size_t plan_cta_bytes() { return sizeof(CtaPlan); }
 int plan_export_records(const uint8_t *plan_host, int64_t *out, int max_ctas) {
   const PlanHeader &h = *reinterpret_cast<const PlanHeader *>(plan_host);
   if (h.magic != kPlanMagic || h.grid <= 0 || h.grid > max_ctas) return -1;
+  const PlanCore &P = reinterpret_cast<const PlanShared *>(plan_host + kPlanHeaderBytes)->plan;
   for (int b = 0; b < h.grid; ++b) {
     const CtaPlan &cp = *reinterpret_cast<const CtaPlan *>(
         plan_host + kPlanHeaderBytes + sizeof(PlanShared) + static_cast<size_t>(b) * sizeof(CtaPlan));
@@ -1623,6 +1627,14 @@ int plan_export_records(const uint8_t *plan_host, int64_t *out, int max_ctas) {
       o[3 + i] = cp.trow[i];
       o[6 + i] = cp.th[i];
       o[9 + i] = cp.tfl[i];
+      o[12 + i] = 0;
+      if (i < cp.n_first) {
+        // the tile's column group, from the plan's unit tables
+        const int64_t local = (cp.u0 + i) % P.UH;
+        int b = 0;
+        while (b + 1 < h.n_blocks && P.ubase[b + 1] <= local) ++b;
+        o[12 + i] = P.tiles[b] > 0 ? (local - P.ubase[b]) / P.tiles[b] : -1;
+      }
     }
   }
   return h.grid;
@@ -1663,12 +1675,13 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const C
   const size_t smem = decode_tc_smem_bytes();
   // planned launches run their own instantiations: without the plan-building
   // (and, without appends, the append) code the kernel is far smaller
-  const int which = !a.plan ? 0
-                    : a.k_new ? (a.k_scale ? 6 : 2)
+  // (every decode runs from a plan: hw_attn_decode plans first)
+  if (!a.plan) return cudaErrorInvalidValue;
+  const int which = a.k_new ? (a.k_scale ? 6 : 2)
                     : a.k_scale ? (a.view_limit ? 5 : 4)
                     : a.view_limit ? 3 : 1;
   void (*const kernels[7])(DecodeArgs, CUtensorMap, CUtensorMap) = {
-      decode_tc_kernel<false, false, false, false>, decode_tc_kernel<true, false, false, false>,
+      nullptr, decode_tc_kernel<true, false, false, false>,
       decode_tc_kernel<true, true, false, false>, decode_tc_kernel<true, false, true, false>,
       decode_tc_kernel<true, false, false, true>, decode_tc_kernel<true, false, true, true>,
       decode_tc_kernel<true, true, false, true>};

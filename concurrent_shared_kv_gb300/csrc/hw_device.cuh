@@ -4,20 +4,28 @@
 //
 // Scheduling (omica.com.cn article, section 3.2: the KV cache is split evenly
 // over the SMs and the partial results are merged):
-//   unit      = one tile of `TILE` tokens of one block for one kv head;
-//   units are ordered kv-head-major, then block, then tile (UH units per
-//   head); only blocks that some view references take part.  Head-major
-//   order keeps each head's short worker blocks next to its long common
-//   block, instead of stacking every head's short blocks on the last CTAs.
-//   segment   = the units of one (block, kv head), id seg = h * n_blocks + b,
-//   increasing along the unit order.
+//   column group = up to kMaxQ query columns of one block: the block's
+//   columns are its view references x the GQA group G, and its references,
+//   in view-entry order, form ng = ceil(refs / (kMaxQ / G)) groups of
+//   kMaxQ / G (every worker may attend the common block: a block read by
+//   more rows than one tile serves is read once per group);
+//   unit      = one tile of `TILE` tokens of one (block, group) for one kv
+//   head; units are ordered kv-head-major, then block, then group, then tile
+//   (UH units per head); only blocks that some view references take part.
+//   Head-major order keeps each head's short worker blocks next to its long
+//   common block, instead of stacking every head's short blocks on the last
+//   CTAs.
+//   segment   = the units of one (block, group, kv head), id seg = h * NS +
+//   sord[b] + g (NS segments per head, sord[b] before block b), increasing
+//   along the unit order.
 //   The split is stream-K over a weighted line: every unit weighs kTileW and
 //   every segment start kSegW more (a segment switch costs a record epilogue
 //   and a new set of rotated queries), so a CTA that crosses several short
 //   worker blocks streams fewer tiles than one inside the long common block.
-//   Unit (h, b, t) starts at weight h WH + kTileW (ubase[b] + t) +
-//   kSegW (sord[b] + 1), where sord[b] counts the non-empty blocks before b
-//   and WH = kTileW UH + kSegW NB.  CTA c of C takes the units whose start
+//   Unit (h, b, g, t) starts at weight h WH + kTileW (ubase[b] + g T + t) +
+//   kSegW (sord[b] + g + 1), where T = tiles[b], ubase[b] and sord[b] count
+//   the units and segments of a head before block b, and WH = kTileW UH +
+//   kSegW NS.  CTA c of C takes the units whose start
 //   lies in [floor(c W / C), floor((c+1) W / C)).  C = min(grid,
 //   W / (kSegW + kTileW)): unit starts are at most kSegW + kTileW apart, so
 //   every working CTA owns at least one unit and the CTAs touching a segment
@@ -127,6 +135,7 @@ __device__ __forceinline__ unsigned lanemask_lt(int lane) { return (1u << lane) 
 // ---------------------------------------------------------------------------
 
 constexpr int kCacheEntries = 384;  // view entries (rows x view blocks) held in shared memory
+constexpr int kMaxBlockRefs = HW_MAX_REFS_PER_BLOCK;  // view entries naming one block
 constexpr int kCacheRows = 384;     // q_pos entries held in shared memory
 
 struct MetaCache {
@@ -181,14 +190,19 @@ constexpr int kTileW = 1;
 constexpr int kSegW = 2;
 
 struct PlanCore {
-  int32_t tiles[HW_MAX_BLOCKS];      // tiles per kv head (0: block skipped)
+  int32_t tiles[HW_MAX_BLOCKS];      // tiles of one group for one kv head (0: block skipped)
   int32_t start[HW_MAX_BLOCKS];      // first pool token
   int32_t len[HW_MAX_BLOCKS];        // tokens
   int64_t ubase[HW_MAX_BLOCKS + 1];  // first unit of each block within a head; [n] = UH
-  uint8_t sord[HW_MAX_BLOCKS];       // non-empty blocks before b
+  uint16_t sord[HW_MAX_BLOCKS + 1];  // segments of a head before block b; [n] = NS
   int64_t UH, U, WH, W;              // units per head and in all; weights likewise
-  int32_t NB, C;                     // non-empty blocks; working CTAs
+  int32_t NS, C;                     // segments per head; working CTAs
 };
+
+// Column groups of block b (0 when it takes no part).
+__device__ __forceinline__ int block_groups(const PlanCore &P, int b) { return P.sord[b + 1] - P.sord[b]; }
+// View references a column group holds at most, for GQA group size G.
+__device__ __forceinline__ int refs_per_group(int G) { return kMaxQ / G; }
 
 // Everything the plan derives that every CTA shares (copied as one block).
 struct alignas(16) PlanShared {
@@ -218,15 +232,23 @@ __device__ __forceinline__ int64_t cta_unit_begin(const PlanCore &P, int n_block
   const int h = static_cast<int>(div_nn(w, P.WH));
   const int64_t l = w - static_cast<int64_t>(h) * P.WH;
   // the last block whose weight region [kTileW ubase + kSegW sord, ...) starts
-  // at or before l, then its first unit starting at or after l (one past its
-  // last unit is the next block's first, or the next head's)
+  // at or before l (a block with tiles: an empty one shares its start with
+  // the next, and the last start is WH > l), its group whose region (a start
+  // weight kSegW, then T tiles) holds l, then that group's first unit
+  // starting at or after l (one past its last unit is the next group's
+  // first, the next block's or the next head's)
   int lo = 0, hi = n_blocks - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (kTileW * P.ubase[mid] + static_cast<int64_t>(kSegW) * P.sord[mid] <= l) lo = mid; else hi = mid - 1;
   }
-  const int64_t off = l - (kTileW * P.ubase[lo] + static_cast<int64_t>(kSegW) * P.sord[lo]) - kSegW;
-  return static_cast<int64_t>(h) * P.UH + P.ubase[lo] + (off > 0 ? (off + kTileW - 1) / kTileW : 0);
+  const int64_t T = P.tiles[lo];
+  const int64_t off = l - (kTileW * P.ubase[lo] + static_cast<int64_t>(kSegW) * P.sord[lo]);
+  const int64_t span = kSegW + kTileW * T;
+  const int64_t g = div_nn(off, span);
+  const int64_t rem = off - g * span - kSegW;
+  return static_cast<int64_t>(h) * P.UH + P.ubase[lo] + g * T +
+         (rem > 0 ? (rem + kTileW - 1) / kTileW : 0);
 }
 
 // Loads the metadata into the cache (one round of independent loads), checks
@@ -304,45 +326,53 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanS
       if (S.kv_cnt[h] != G) S.headmap_ok = 0;
     __syncwarp();
     const bool hm_ok = S.headmap_ok != 0;
+    const int rpg = refs_per_group(G);
     int64_t carry = 0;
     int ncarry = 0;
     for (int base = 0; base < a.n_blocks; base += 32) {
       const int b = base + lane;
-      int t = 0;
+      int t = 0, ng = 0;
       if (b < a.n_blocks) {
         const int32_t st = P.start[b], n = P.len[b], refs = S.refs[b];
         if (st < 0 || n < 0 || static_cast<int64_t>(st) + n > a.capacity) {
           if (blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_RANGE);
         } else if (refs > 0 && n > 0) {
-          if (refs * G > kMaxQ) {
+          if (refs > kMaxBlockRefs) {  // (entry ranks are kept in 8 bits)
             if (blockIdx.x == 0) flag_error(a.err, HW_DEV_TOO_MANY_REFS);
           } else {
             t = (n + TILE - 1) / TILE;
+            ng = (refs + rpg - 1) / rpg;
           }
         }
-        if (!hm_ok) t = 0;
+        if (!hm_ok) t = ng = 0;
         P.tiles[b] = t;
       }
-      int64_t incl = t;
+      const int64_t ub = static_cast<int64_t>(t) * ng;  // the block's units per head
+      int64_t incl = ub;
+      int sincl = ng;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        const int z = __shfl_up_sync(0xffffffffu, sincl, o);
+        if (lane >= o) {
+          incl += y;
+          sincl += z;
+        }
       }
-      const unsigned ne = __ballot_sync(0xffffffffu, t > 0);
       if (b < a.n_blocks) {
-        P.ubase[b] = carry + incl - t;
-        P.sord[b] = static_cast<uint8_t>(ncarry + __popc(ne & lanemask_lt(lane)));
+        P.ubase[b] = carry + incl - ub;
+        P.sord[b] = static_cast<uint16_t>(ncarry + sincl - ng);
       }
       carry += __shfl_sync(0xffffffffu, incl, 31);
-      ncarry += __popc(ne);
+      ncarry += __shfl_sync(0xffffffffu, sincl, 31);
     }
     if (lane == 0) {
       if (!hm_ok && blockIdx.x == 0) flag_error(a.err, HW_DEV_BAD_HEADMAP);
       P.ubase[a.n_blocks] = carry;
+      P.sord[a.n_blocks] = static_cast<uint16_t>(ncarry);
       P.UH = carry;
       P.U = carry * a.n_kv_heads;
-      P.NB = ncarry;
+      P.NS = ncarry;
       P.WH = kTileW * carry + static_cast<int64_t>(kSegW) * ncarry;
       P.W = P.WH * a.n_kv_heads;
       const int64_t cmax = P.W / (kSegW + kTileW);
@@ -416,9 +446,10 @@ __device__ __forceinline__ int block_of_unit(const PlanCore &P, int n_blocks, in
   return lo;
 }
 
-// The unit u decoded: block, kv head, tile, and the segment's first unit.
+// The unit u decoded: block, column group, kv head, tile, the tiles of the
+// segment and its first unit.
 struct UnitPos {
-  int b, h, t, tiles;
+  int b, g, h, t, tiles;
   int64_t seg_first;
 };
 __device__ __forceinline__ UnitPos unit_pos(const PlanCore &P, int n_blocks, int64_t u) {
@@ -427,17 +458,24 @@ __device__ __forceinline__ UnitPos unit_pos(const PlanCore &P, int n_blocks, int
   const int64_t local = u - static_cast<int64_t>(x.h) * P.UH;
   x.b = block_of_unit(P, n_blocks, local);
   x.tiles = P.tiles[x.b];
-  x.t = static_cast<int>(local - P.ubase[x.b]);
-  x.seg_first = static_cast<int64_t>(x.h) * P.UH + P.ubase[x.b];
+  const int64_t in_block = local - P.ubase[x.b];
+  x.g = x.tiles > 0 ? static_cast<int>(div_nn(in_block, x.tiles)) : 0;  // (0: u past the units)
+  x.t = static_cast<int>(in_block - static_cast<int64_t>(x.g) * x.tiles);
+  x.seg_first = static_cast<int64_t>(x.h) * P.UH + P.ubase[x.b] + static_cast<int64_t>(x.g) * x.tiles;
   return x;
 }
 
-// unit_pos of u + 1 from that of u (units run block after block, skipping
-// blocks without tiles, then head after head): O(1) where unit_pos costs a
-// division and a binary search over the blocks.
+// unit_pos of u + 1 from that of u (units run group after group, block after
+// block, skipping blocks without tiles, then head after head): O(1) where
+// unit_pos costs a division and a binary search over the blocks.
 __device__ __forceinline__ void unit_pos_next(const PlanCore &P, int n_blocks, UnitPos &x) {
   if (++x.t < x.tiles) return;
   x.t = 0;
+  if (++x.g < block_groups(P, x.b)) {
+    x.seg_first += x.tiles;
+    return;
+  }
+  x.g = 0;
   int b = x.b + 1;
   while (b < n_blocks && P.tiles[b] == 0) ++b;
   if (b == n_blocks) {  // the next head, from its first block with tiles
@@ -456,7 +494,8 @@ __device__ __forceinline__ int64_t unit_weight(const PlanCore &P, int n_blocks, 
   const int h = static_cast<int>(div_nn(u, P.UH));
   const int64_t local = u - static_cast<int64_t>(h) * P.UH;
   const int b = block_of_unit(P, n_blocks, local);
-  return static_cast<int64_t>(h) * P.WH + kTileW * local + static_cast<int64_t>(kSegW) * (P.sord[b] + 1);
+  const int64_t g = P.tiles[b] > 0 ? div_nn(local - P.ubase[b], P.tiles[b]) : 0;
+  return static_cast<int64_t>(h) * P.WH + kTileW * local + static_cast<int64_t>(kSegW) * (P.sord[b] + g + 1);
 }
 
 // The CTA that owns unit u: the largest c with floor(c W / C) <= weight(u).
@@ -464,25 +503,41 @@ __device__ __forceinline__ int cta_of_unit(const PlanCore &P, int n_blocks, int6
   return static_cast<int>(div_nn((unit_weight(P, n_blocks, u) + 1) * P.C - 1, P.W));
 }
 
-__device__ __forceinline__ int64_t seg_id(int n_blocks, int b, int h) {
-  return static_cast<int64_t>(h) * n_blocks + b;
+// The first of the units that read tile t of block b for kv head h (one per
+// column group) at or after u0, or -1 when none of them lies before u1.
+__device__ __forceinline__ int64_t tile_unit_in(const PlanCore &P, int b, int h, int t, int64_t u0,
+                                                int64_t u1) {
+  const int64_t T = P.tiles[b];
+  const int64_t u_g0 = static_cast<int64_t>(h) * P.UH + P.ubase[b] + t;  // column group 0
+  const int64_t g = u0 > u_g0 ? (u0 - u_g0 + T - 1) / T : 0;
+  if (g >= block_groups(P, b)) return -1;
+  const int64_t u = u_g0 + g * T;
+  return u < u1 ? u : -1;
 }
 
-// The view entries referencing block b, in entry order (one warp); an
-// entry's position here is its rank among the block's references.
+// Segment (block b, group g, kv head h): its index along the unit order.
+__device__ __forceinline__ int64_t seg_id(const PlanCore &P, int b, int g, int h) {
+  return static_cast<int64_t>(h) * P.NS + P.sord[b] + g;
+}
+
+// The view entries of column group g of block b (ranks g * rpg .. among the
+// entries referencing b, rpg = refs_per_group(G)), in entry order (one warp);
+// an entry's position here is its rank within the group.
 __device__ __forceinline__ void gather_refs(const DecodeArgs &a, const MetaCache &C, SegMeta &M,
-                                            int b, int lane) {
+                                            int b, int g, int lane) {
   const int E = a.n_rows * a.n_view;
+  const int rpg = refs_per_group(a.n_q_heads / a.n_kv_heads);
+  const int first = g * rpg;
   int cnt = 0;
   for (int base = 0; base < E; base += 32) {
     const int e = base + lane;
     const bool m = e < E && vb_at(a, C, e) == b;
     const unsigned mask = __ballot_sync(0xffffffffu, m);
-    const int pos = cnt + __popc(mask & lanemask_lt(lane));
-    if (m && pos < kMaxQ) M.ref_entry[pos] = e;
+    const int pos = cnt + __popc(mask & lanemask_lt(lane)) - first;
+    if (m && pos >= 0 && pos < rpg) M.ref_entry[pos] = e;
     cnt += __popc(mask);
   }
-  if (lane == 0) M.n_ref = cnt;
+  if (lane == 0) M.n_ref = min(max(cnt - first, 0), rpg);
 }
 
 // The q heads of kv head h, in increasing order (one warp); a q head's
@@ -515,10 +570,10 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
 }
 
 // One arrival on (row, q head) for every view entry referencing the
-// segment's block and every q head of its kv head (M.qhead), one per lane:
-// the whole warp calls it, after the group's record stores were ordered
-// before it (a barrier the writers took part in, or an mbarrier they arrived
-// on).  The plan skips blocks with more than kMaxQ columns, so one warp
+// segment's column group and every q head of its kv head (M.qhead), one per
+// lane: the whole warp calls it, after the group's record stores were
+// ordered before it (a barrier the writers took part in, or an mbarrier they
+// arrived on).  A column group holds at most kMaxQ columns, so one warp
 // covers every arrival; issued together, they cost one trip to L2 instead
 // of one each.
 __device__ __forceinline__ void arrive_segment(const DecodeArgs &a, const SegMeta &M, int lane) {
@@ -580,8 +635,10 @@ __device__ __forceinline__ int units_rank_part(const PlanCore &P, int n_blocks, 
 }
 
 // The record list of merge item (row r, q head hq) in view order, built by
-// one warp: for every view entry, the records that the CTAs c0..c1 touching
-// segment (block, kv head) wrote at column rank * G + gi.  Returns the number
+// one warp: for every view entry (rank k among the references to its block:
+// column group k / rpg, rank k % rpg within it), the records that the CTAs
+// c0..c1 touching segment (block, group, kv head) wrote at column
+// (k % rpg) * G + gi.  Returns the number
 // of records (in every lane); entries at or past `cap` are not written.
 // rank_tmp (HW_MAX_VIEW_BLOCKS ints) is scratch for views beyond the cache.
 __device__ __forceinline__ int merge_list(const DecodeArgs &a, const PlanCore &P,
@@ -605,11 +662,14 @@ __device__ __forceinline__ int merge_list(const DecodeArgs &a, const PlanCore &P
       const int e = r * V + v;
       const int b = vb_at(a, MC, e);
       if (b >= 0 && b < a.n_blocks && P.tiles[b] > 0) {
-        const int64_t s0 = static_cast<int64_t>(h) * P.UH + P.ubase[b];
+        const int rpg = refs_per_group(G);
+        const int k = MC.entries_cached ? MC.rank[e] : rank_tmp[v];
+        const int g = k / rpg;
+        const int64_t s0 = static_cast<int64_t>(h) * P.UH + P.ubase[b] + static_cast<int64_t>(g) * P.tiles[b];
         const int c0 = cta_of_unit(P, a.n_blocks, s0);
         cnt = cta_of_unit(P, a.n_blocks, s0 + P.tiles[b] - 1) - c0 + 1;
-        slot0 = seg_id(a.n_blocks, b, h) + c0;
-        col = (MC.entries_cached ? MC.rank[e] : rank_tmp[v]) * G + gi;
+        slot0 = seg_id(P, b, g, h) + c0;
+        col = (k - g * rpg) * G + gi;
       }
     }
     int incl = cnt;

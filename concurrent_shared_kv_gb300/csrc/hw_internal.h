@@ -78,9 +78,10 @@ constexpr size_t kPlanHeaderBytes = 256;
 size_t plan_shared_bytes();  // the part of a plan every CTA reads
 size_t plan_cta_bytes();     // the part each CTA reads for itself
 // From a host copy of a plan region: kPlanExportFields int64 per CTA (unit
-// range, number of first tiles, their rows, kv heads and segment flags).
-// Returns the plan's grid, or -1 when there is no plan (or it exceeds max_ctas).
-constexpr int kPlanExportFields = 12;
+// range, number of first tiles, their rows, kv heads, segment flags and
+// column groups).  Returns the plan's grid, or -1 when there is no plan (or
+// it exceeds max_ctas).
+constexpr int kPlanExportFields = 15;
 int plan_export_records(const uint8_t *plan_host, int64_t *out, int max_ctas);
 WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas);
 

@@ -118,6 +118,14 @@ def qwq32b_w4() -> Workload:
                     "bf16", 1, 4, 40, 8, 128, 1e6, 64, [16384], [[512, 384, 256, 128]], seed=1003)
 
 
+def qwq32b_w8() -> Workload:
+    """Eight workers on the QwQ-32B shape: 8 view references x G = 5 put 40
+    query columns on the common block and on every worker block."""
+    return Workload("qwq32b-shape bf16 W8 Hq40/Hkv8 D128 common16384 blocks512/384/256/128x2"
+                    " 64 layers", "bf16", 1, 8, 40, 8, 128, 1e6, 64, [16384],
+                    [[512, 384, 256, 128, 512, 384, 256, 128]], seed=1006)
+
+
 def qwen3_8b_w4() -> Workload:
     return Workload("qwen3-8b-shape bf16 W4 Hq32/Hkv8 D128 common32768 blocks1024x4 36 layers"
                     " + commit 1024", "bf16", 1, 4, 32, 8, 128, 1e6, 36, [32768],
@@ -136,6 +144,8 @@ def serve_ragged(n_problems: int = 16, seed: int = 1005) -> Workload:
 
 
 ALL = {"C1": tiny_f32, "C2": qwq32b_w2, "C3": qwq32b_w4, "C4": qwen3_8b_w4, "C5": serve_ragged}
+# wider than one tile's 32 query columns (column groups)
+EXTRA = {"W8": qwq32b_w8}
 
 
 # ---------------------------------------------------------------------------

@@ -77,7 +77,9 @@ enum {
   HW_DEV_BAD_BLOCK = 1,     /* a view names a block id outside [-1, n_blocks) */
   HW_DEV_BAD_RANGE = 2,     /* block_start/len negative or past the pool capacity */
   HW_DEV_BAD_HEADMAP = 4,   /* q_to_kv entry out of range or groups of unequal size */
-  HW_DEV_TOO_MANY_REFS = 8, /* more than HW_MAX_QHEADS_PER_BLOCK query heads on a block */
+  HW_DEV_TOO_MANY_REFS = 8, /* more than HW_MAX_REFS_PER_BLOCK view entries name one block
+                               (it is skipped), or a (row, q head) gathers more partial
+                               results than a merge holds */
   HW_DEV_TIMEOUT = 16,      /* a bounded in-kernel wait expired; results are invalid */
   HW_DEV_BAD_PLAN = 32      /* hw_attn_decode_planned found no plan for this description */
 };
@@ -86,7 +88,12 @@ enum {
 #define HW_MAX_BLOCKS 256          /* blocks per decode call */
 #define HW_MAX_VIEW_BLOCKS 64      /* max_view_blocks */
 #define HW_MAX_VIEW_ENTRIES 4096   /* n_rows * max_view_blocks */
-#define HW_MAX_QHEADS_PER_BLOCK 32 /* (view references to one block) x (Hq/Hkv) */
+/* Query columns one tile serves: a block's columns are (view references to
+ * it) x (Hq/Hkv).  A block with more is split into column groups of
+ * HW_MAX_QHEADS_PER_BLOCK / (Hq/Hkv) references each, in view-entry order,
+ * and each group reads the block's tiles once. */
+#define HW_MAX_QHEADS_PER_BLOCK 32
+#define HW_MAX_REFS_PER_BLOCK 255  /* view entries naming one block */
 #define HW_MAX_Q_HEADS 256         /* n_q_heads */
 
 /* Host-side description of one decode call (all scalars, host memory). */
@@ -304,12 +311,13 @@ int hw_attn_append_decode_planned_fp8(const hw_attn_desc *d, const void *q, cons
 
 /*
  * For tests: the work split of the plan in `workspace` (bf16 head_dim-128
- * kernel; synchronises `stream`).  Per CTA c < *n_ctas, 12 int64 at
- * out[12 c ..]: its unit range [u0, u1) (units: 128-token tiles of one
- * (block, kv head), kv-head-major, then block, then tile), the number of
- * first tiles the plan decodes (min(3, u1 - u0)), their first cache rows,
- * kv heads and segment flags (1: starts its segment within the range, 2:
- * ends it), 3 each.  out holds max_ctas records.  HW_ERR_INVALID when the
+ * kernel; synchronises `stream`).  Per CTA c < *n_ctas, 15 int64 at
+ * out[15 c ..]: its unit range [u0, u1) (units: 128-token tiles of one
+ * (block, column group, kv head), kv-head-major, then block, then group,
+ * then tile; see HW_MAX_QHEADS_PER_BLOCK), the number of first tiles the
+ * plan decodes (min(3, u1 - u0)), their first cache rows, kv heads, segment
+ * flags (1: starts its segment within the range, 2: ends it) and column
+ * groups, 3 each.  out holds max_ctas records.  HW_ERR_INVALID when the
  * workspace holds no plan.
  */
 int hw_plan_export(const hw_attn_desc *d, const void *workspace, size_t workspace_bytes,
@@ -434,7 +442,9 @@ int hw_views_combined(int32_t n_problems, int32_t n_workers, const int32_t *bloc
  *                         ones; the difference is the caller's commit policy.
  * view_offset = tokens before each block in the view; q_pos = the view's
  * total length.  Arrays as in hw_views_combined.  HW_ERR_INVALID for an
- * unknown layout.
+ * unknown layout; HW_ERR_UNSUPPORTED when a block would be named by more
+ * than HW_MAX_REFS_PER_BLOCK rows (n_workers > 255), which the decode calls
+ * skip.
  */
 typedef enum { HW_LAYOUT_COMBINED = 0, HW_LAYOUT_INTERLEAVED = 1, HW_LAYOUT_CONTIGUOUS = 2 } hw_layout;
 int hw_views(int32_t layout, int32_t n_problems, int32_t n_workers, const int32_t *block_len,
@@ -450,7 +460,8 @@ int hw_views(int32_t layout, int32_t n_problems, int32_t n_workers, const int32_
  * entry and -1 (whole block) on the others; q_pos = that token's position in
  * the view.  All arrays host: view_block, view_offset, view_limit
  * [n_problems*W*T][W+1], q_pos [n_problems*W*T].  HW_ERR_INVALID for an
- * unknown layout or a worker block shorter than T.
+ * unknown layout or a worker block shorter than T; HW_ERR_UNSUPPORTED when a
+ * block would be named by more than HW_MAX_REFS_PER_BLOCK rows (W*T > 255).
  */
 int hw_views_chunked(int32_t layout, int32_t n_problems, int32_t n_workers, int32_t chunk,
                      const int32_t *block_len, int32_t *view_block, int32_t *view_offset,

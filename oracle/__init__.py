@@ -389,37 +389,51 @@ def chunk_views(layout: str, block_len: Sequence[int], n_problems: int, n_worker
 
 def stream_k_split(block_start, block_len, view_block, n_q_heads: int, n_kv_heads: int,
                    grid: int, seg_weight: int = 2, tile: int = 128, max_cols: int = 32):
-    """Units are 128-token tiles of one (block, kv head), kv-head-major, then
-    block, then tile.  A block takes part when some view references it, it has
-    tokens and (references x group size) <= max_cols.  Every unit weighs 1 and
-    every segment start (a taking-part block, once per kv head) seg_weight
-    more: unit (h, b, t) starts at weight h*WH + ubase[b] + seg_weight*(sord[b]+1) + t.
+    """The work split of the KV cache over the SMs (omica.com.cn article, §3.2:
+    the cache is divided evenly over the SMs, partial results merged).
+
+    A segment is one column group of one (block, kv head): a block's query
+    columns are its view references x the group size G, and a tile serves at
+    most max_cols of them, so the references of block b, in view-entry order,
+    form ng[b] = ceil(refs[b] / rpg) groups of rpg = max_cols // G (the last
+    one shorter); reference k is in group k // rpg.  A block takes part when
+    some view references it and it has tokens.  Units are 128-token tiles of
+    one segment, ordered kv-head-major, then block, then group, then tile, so
+    every group reads the block's tiles once.  Every unit weighs 1 and every
+    segment start seg_weight more: unit (h, b, g, t) starts at weight
+    h*WH + ubase[b] + g*tiles[b] + t + seg_weight*(sord[b] + g + 1), with
+    ubase/sord the units/segments of the head before block b and
+    WH = UH + seg_weight*NSH (units and segments per head).
     C = min(grid, W // (seg_weight + 1)) CTAs; CTA c < C takes the units whose
     weight lies in [floor(c W / C), floor((c+1) W / C)).
 
-    Returns per CTA c < grid: (u0, u1, n_first, rows[3], heads[3], flags[3])
-    as an int64 array [grid][12], the layout of hw_plan_export.
+    Returns per CTA c < grid: (u0, u1, n_first, rows[3], heads[3], flags[3],
+    groups[3]) as an int64 array [grid][15], the layout of hw_plan_export.
     """
     vb = np.asarray(view_block).ravel()
     G = n_q_heads // n_kv_heads
+    assert 1 <= G <= max_cols
+    rpg = max_cols // G
     nb = len(block_len)
     refs = np.array([(vb == b).sum() for b in range(nb)])
-    tiles = np.array([(int(block_len[b]) + tile - 1) // tile
-                      if refs[b] > 0 and block_len[b] > 0 and refs[b] * G <= max_cols else 0
+    taking = [refs[b] > 0 and block_len[b] > 0 for b in range(nb)]
+    tiles = np.array([(int(block_len[b]) + tile - 1) // tile if taking[b] else 0
                       for b in range(nb)], np.int64)
-    UH = int(tiles.sum())
-    NB = int((tiles > 0).sum())
-    WH = UH + seg_weight * NB
+    ng = np.array([-(-int(refs[b]) // rpg) if taking[b] else 0 for b in range(nb)], np.int64)
+    UH = int((tiles * ng).sum())
+    NSH = int(ng.sum())
+    WH = UH + seg_weight * NSH
     W = WH * n_kv_heads
     C = min(grid, W // (seg_weight + 1))
-    # every unit, brute force: (h, b, t) and its weight
-    units = [(h, b, t) for h in range(n_kv_heads) for b in range(nb) for t in range(int(tiles[b]))]
-    ubase = np.concatenate([[0], np.cumsum(tiles)])
-    sord = np.concatenate([[0], np.cumsum(tiles > 0)])
-    weight = np.array([h * WH + ubase[b] + seg_weight * (sord[b] + 1) + t for (h, b, t) in units],
-                      np.int64)
+    # every unit, brute force: (h, b, g, t) and its weight
+    units = [(h, b, g, t) for h in range(n_kv_heads) for b in range(nb) for g in range(int(ng[b]))
+             for t in range(int(tiles[b]))]
+    ubase = np.concatenate([[0], np.cumsum(tiles * ng)])
+    sord = np.concatenate([[0], np.cumsum(ng)])
+    weight = np.array([h * WH + ubase[b] + g * tiles[b] + t + seg_weight * (sord[b] + g + 1)
+                       for (h, b, g, t) in units], np.int64)
     assert np.all(np.diff(weight) > 0)
-    out = np.zeros((grid, 12), np.int64)
+    out = np.zeros((grid, 15), np.int64)
     for c in range(grid):
         if c < C:
             u0 = int(np.searchsorted(weight, (W * c) // C, side="left"))
@@ -430,10 +444,11 @@ def stream_k_split(block_start, block_len, view_block, n_q_heads: int, n_kv_head
         out[c, 0], out[c, 1], out[c, 2] = u0, u1, nf
         for i in range(nf):
             u = u0 + i
-            h, b, t = units[u]
+            h, b, g, t = units[u]
             first = u == u0 or t == 0
             last = u + 1 == u1 or t == tiles[b] - 1
             out[c, 3 + i] = int(block_start[b]) + t * tile
             out[c, 6 + i] = h
             out[c, 9 + i] = (1 if first else 0) | (2 if last else 0)
+            out[c, 12 + i] = g
     return out

@@ -88,7 +88,7 @@ def test_plan_limited_needs_the_flag_the_limits_and_the_tensor_core_path():
     assert call(desc()) == -1                          # a descriptor without the flag
     assert call(desc(flags=LIM, dtype=api.HW_F32)) == -2
     assert call(desc(flags=LIM, head_dim=64)) == -2
-    assert call(desc(flags=2)) == -1                   # an unknown flag
+    assert call(desc(flags=64)) == -1                  # an unknown flag
 
 
 def test_a_limited_descriptor_is_only_planned_with_limits():
@@ -101,3 +101,17 @@ def test_a_limited_descriptor_is_only_planned_with_limits():
                   FAKE, 0) == -2
     assert status(api.attn_decode_noalloc, d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                   None) == -2
+
+
+def test_views_reject_more_rows_on_a_block_than_a_plan_ranks():
+    # a block named by more than HW_MAX_REFS_PER_BLOCK = 255 view entries is
+    # skipped by the decode; the host builders refuse such tables up front
+    with pytest.raises(api.HwError) as e:
+        api.views_combined(np.full(257, 10, np.int32), 1, 256)  # 256 rows on the common block
+    assert e.value.status == -2
+    with pytest.raises(api.HwError) as e:
+        api.views_chunked("combined", np.full(5, 300, np.int32), 1, 4, 64)  # 4 x 64 rows
+    assert e.value.status == -2
+    # at the limit: 255 rows
+    vb, vo, qp = api.views_combined(np.full(256, 10, np.int32), 1, 255)
+    assert (vb[:, 0] == 0).all()

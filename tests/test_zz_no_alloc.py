@@ -61,9 +61,10 @@ def test_noalloc_rejects_descriptions_beyond_the_scratch():
 
 def test_noalloc_status_reports_device_errors():
     # seven workers at five query heads per kv head put 35 query columns on
-    # every block, more than a tile serves: the plan skips the blocks and
-    # records HW_DEV_TOO_MANY_REFS, which the no-allocation status call reads
-    # (and clears) without a workspace
+    # every block (two column groups): the no-allocation call matches the
+    # oracle and leaves no error bit.  A view naming a block that does not
+    # exist then records HW_DEV_BAD_BLOCK, which the no-allocation status
+    # call reads (and clears) without a workspace.
     w = wl.Workload("wide", "bf16", 1, 7, 40, 8, 128, 1e6, 1, [512], [[64] * 7], seed=21)
     c = H.device_case(w, 0)
     s = c.session()
@@ -74,5 +75,12 @@ def test_noalloc_status_reports_device_errors():
     api.attn_decode_noalloc(s.desc, c.q, c.k, c.v, m["block_start"], m["block_len"],
                             m["view_block"], m["view_offset"], m["q_pos"], out, lse,
                             q_to_kv=m["q_to_kv"])
-    assert api.noalloc_status() & 8  # HW_DEV_TOO_MANY_REFS
+    assert api.noalloc_status() == 0
+    ro, rl = c.run_oracle()
+    H.compare("bf16", out, lse, ro, rl, what="noalloc 35 columns")
+    bad = m["view_block"].clone()
+    bad[0, 1] = w.n_blocks + 5  # no such block
+    api.attn_decode_noalloc(s.desc, c.q, c.k, c.v, m["block_start"], m["block_len"], bad,
+                            m["view_offset"], m["q_pos"], out, lse, q_to_kv=m["q_to_kv"])
+    assert api.noalloc_status() & 1  # HW_DEV_BAD_BLOCK
     assert api.noalloc_status() == 0  # read and cleared
