@@ -328,6 +328,18 @@ def main():
     stream = torch.cuda.Stream(device=dev)
 
     planned = not args.unplanned
+    # hw_attn_decode (unplanned) keeps the plan of the metadata it last saw.
+    # A model's metadata changes every step (positions and lengths grow), so
+    # the steps alternate between this metadata and an equivalent copy with
+    # every view offset and position one higher (i_q - offset, and with it
+    # every result, unchanged): the first layer of each step rebuilds the
+    # plan, like the planned steps' hw_attn_plan.
+    metas = [sess.meta]
+    if not planned:
+        alt = dict(sess.meta)
+        alt["view_offset"] = sess.meta["view_offset"] + 1
+        alt["q_pos"] = sess.meta["q_pos"] + 1
+        metas.append(alt)
 
     append = args.append and planned and kernel == "decode_tc_kernel"
     if append:
@@ -401,24 +413,28 @@ def main():
                             int(starts[0]) + int(w.common_len[0]), int(w.common_len[0]),
                             w.rope_theta, stream=stream)
 
-    def step():
+    def step(k=0):
+        sess.meta = metas[k % len(metas)]
         layer_calls(qs)
         if commit:
             commit_call()
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            step()
+        for k in range(max(args.warmup, 3)):
+            step(k)
     stream.synchronize()
-    graph = None
+    graphs = None
     if not args.eager:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            step()
+        graphs = []
+        for k in range(len(metas)):  # one graph per metadata set, replayed in turn
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(k)
+            graphs.append(g)
         stream.synchronize()
-        for _ in range(2):
-            graph.replay()
+        for k in range(2):
+            graphs[k % len(graphs)].replay()
         stream.synchronize()
     flags = sess.device_flags()
     assert flags == 0, f"device flags {flags}"
@@ -431,11 +447,11 @@ def main():
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             start.record(stream)
-            for _ in range(n):
-                if graph is not None:
-                    graph.replay()
+            for k in range(n):
+                if graphs is not None:
+                    graphs[k % len(graphs)].replay()
                 else:
-                    step()
+                    step(k)
             end.record(stream)
         torch.cuda.synchronize()
         if world > 1:
@@ -474,14 +490,17 @@ def main():
         lses_all = torch.empty((L,) + tuple(lses[0].shape), dtype=lses[0].dtype, device=dev)
         o_host = torch.empty(outs_all.shape, dtype=outs_all.dtype, pin_memory=True)
         l_host = torch.empty(lses_all.shape, dtype=lses_all.dtype, pin_memory=True)
-        meta_host = [torch.from_numpy(np.ascontiguousarray(x, np.int32)).pin_memory()
-                     for x in (starts, lens, vb, vo, qp)]
+        # (unplanned: the steps upload the two equivalent metadata sets in turn)
+        meta_hosts = [[torch.from_numpy(np.ascontiguousarray(x, np.int32)).pin_memory()
+                       for x in (starts, lens, vb, np.asarray(vo) + k, np.asarray(qp) + k)]
+                      for k in range(len(metas))]
+        sess.meta = metas[0]
         meta_dev = [sess.meta[name] for name in ("block_start", "block_len", "view_block",
                                                  "view_offset", "q_pos")]
         if chunk > 0:
-            meta_host.append(torch.from_numpy(np.ascontiguousarray(vl, np.int32)).pin_memory())
+            meta_hosts[0].append(torch.from_numpy(np.ascontiguousarray(vl, np.int32)).pin_memory())
             meta_dev.append(vl_dev)
-        h2d = q_host.numel() * q_host.element_size() + sum(m.numel() * 4 for m in meta_host)
+        h2d = q_host.numel() * q_host.element_size() + sum(m.numel() * 4 for m in meta_hosts[0])
         d2h = o_host.numel() * o_host.element_size() + l_host.numel() * 4
 
         def calls():
@@ -493,15 +512,15 @@ def main():
             calls()
         stream.synchronize()
         g_e2e = None
-        if graph is not None:
+        if graphs is not None:
             g_e2e = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_e2e, stream=stream):
                 calls()
             stream.synchronize()
 
-        def e2e_step():  # noqa: E306
+        def e2e_step(k):  # noqa: E306
             with torch.cuda.stream(stream):
-                for m, md in zip(meta_host, meta_dev):
+                for m, md in zip(meta_hosts[k % len(meta_hosts)], meta_dev):
                     md.copy_(m, non_blocking=True)
                 qdev_all.copy_(q_host, non_blocking=True)
                 if g_e2e is not None:
@@ -511,14 +530,14 @@ def main():
                 o_host.copy_(outs_all, non_blocking=True)
                 l_host.copy_(lses_all, non_blocking=True)
 
-        for _ in range(3):
-            e2e_step()
+        for k in range(3):
+            e2e_step(k)
         stream.synchronize()
         e2e_steps = max(3, min(args.steps, 10))
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            e2e_step()
+        for k in range(e2e_steps):
+            e2e_step(k)
             stream.synchronize()
         t_e2e = (time.perf_counter() - t0) / e2e_steps
         assert torch.isfinite(o_host.float()).all(), "e2e outputs"
@@ -544,7 +563,7 @@ def main():
             "kv_bytes_per_step": step_bytes, "commit_bytes_per_step": commit_bytes,
             "parallelism": f"replicas x{world}", "kv": args.kv,
             "query_rows": n_rows, "chunk": chunk if chunk > 0 else None,
-            "mode": "eager" if graph is None else "cuda-graph",
+            "mode": "eager" if graphs is None else "cuda-graph",
             "calls": (f"hw_attn_plan_append once per step + hw_attn_append_decode_planned"
                       f"{'_fp8' if fp8 else ''} per layer (each worker's new token written, then "
                       "decoded)" if append else

@@ -129,11 +129,19 @@ WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas) {
   const int sms = device_sm_count();
   const size_t plan = kPlanHeaderBytes + plan_shared_bytes() +
                       static_cast<size_t>(sms > 0 ? sms : 0) * plan_cta_bytes();
-  // hw_attn_decode's own plan (tensor-core path): a second region of the same
-  // size, so that it never overwrites the step's plan of hw_attn_plan
-  L.uplan_off = L.plan_off + up(plan);
-  L.total = L.uplan_off + up(plan);
+  // hw_attn_decode's plan cache (tensor-core path; see PlanCacheState): it
+  // never touches the step's plan of hw_attn_plan
+  L.cache_off = L.plan_off + up(plan);
+  L.cache_meta_bytes = up(static_cast<size_t>(plan_cache_meta_words(d.n_rows, d.max_view_blocks,
+                                                                    d.n_q_heads, d.n_blocks)) *
+                          sizeof(int32_t));
+  L.cache_plan_bytes = up(plan);
+  L.total = L.cache_off + kPlanCacheStateBytes + 2 * L.cache_meta_bytes + 2 * L.cache_plan_bytes;
   return L;
+}
+
+WorkspaceLayout decode_workspace_layout(const hw_attn_desc &d) {
+  return workspace_layout(d, max_decode_ctas());
 }
 
 // The metadata copies of a workspace (written by hw_attn_plan).
@@ -245,6 +253,12 @@ static void fill_args(DecodeArgs &a, const hw_attn_desc *d, const WorkspaceLayou
   a.capacity = d->cache_capacity;
   a.scale_log2 = static_cast<float>(static_cast<double>(d->scale) * 1.4426950408889634074);
   rope_phase_table(d->head_dim, d->rope_theta, a.phase);
+  a.cache_meta_bytes = static_cast<int64_t>(L.cache_meta_bytes);  // (the plan cache: use_plan_cache)
+  a.cache_plan_bytes = static_cast<int64_t>(L.cache_plan_bytes);
+}
+
+static void use_plan_cache(DecodeArgs &a, const WorkspaceLayout &L, void *workspace) {
+  a.cache_base = static_cast<uint8_t *>(workspace) + L.cache_off;
 }
 
 static bool tensor_core_path(const hw_attn_desc *d) {
@@ -263,12 +277,10 @@ static int decode_common(const hw_attn_desc *d, const void *q, const void *k_cac
                          const int32_t *append_pos = nullptr, const void *k_new = nullptr,
                          const void *v_new = nullptr, const int32_t *view_limit = nullptr,
                          const float *k_scale = nullptr, const float *v_scale = nullptr,
-                         bool plan_follows = false) {
+                         bool from_cache = false) {
   DecodeArgs a;
   fill_args(a, d, L, workspace);
-  // right after its own plan launch, a decode reads that plan only after the
-  // wait: the promise of early loads covers the caller's data, not this plan
-  if (plan_follows) a.early = 0;
+  if (from_cache) use_plan_cache(a, L, workspace);  // hw_attn_decode: the plan cache
   a.view_limit = view_limit;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
@@ -358,31 +370,13 @@ int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, co
   int max_ctas = 0;
   st = check_workspace(d, workspace, workspace_bytes, &L, &max_ctas);
   if (st != HW_OK) return st;
-  if (tensor_core_path(d)) {
-    // Two launches, no host round trip: the plan of this call's metadata
-    // (into the workspace's own region for it, not the step's plan), then the
-    // planned decode over the caller's arrays.  The plan is a programmatic
-    // dependent of the previous kernel (with the early-loads promise it reads
-    // the metadata before that kernel completes) and the decode of the plan.
-    DecodeArgs a;
-    fill_args(a, d, L, workspace);
-    a.block_start = block_start;
-    a.block_len = block_len;
-    a.view_block = view_block;
-    a.view_offset = view_offset;
-    a.q_pos = q_pos;
-    a.q_to_kv = q_to_kv;
-    PlanOut o;
-    std::memset(&o, 0, sizeof o);  // no metadata copies: the decode reads the caller's arrays
-    o.plan = static_cast<uint8_t *>(workspace) + L.uplan_off;
-    const cudaError_t e = launch_plan(a, o, device_sm_count(), static_cast<cudaStream_t>(stream), true);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return decode_common(d, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
-                         q_pos, q_to_kv, o.plan, out, lse, workspace, L, max_ctas, stream, nullptr,
-                         nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, true);
-  }
+  // the tensor-core kernel runs from the workspace's plan cache: the plan of
+  // the metadata the last call saw, rebuilt by the launch itself when this
+  // call's metadata differs (one launch, no host round trip)
   return decode_common(d, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
-                       q_pos, q_to_kv, nullptr, out, lse, workspace, L, max_ctas, stream);
+                       q_pos, q_to_kv, nullptr, out, lse, workspace, L, max_ctas, stream, nullptr,
+                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                       tensor_core_path(d));
 }
 
 static int plan_impl(const hw_attn_desc *d, const int32_t *block_start, const int32_t *block_len,
@@ -425,7 +419,8 @@ static int plan_impl(const hw_attn_desc *d, const int32_t *block_start, const in
   o.append_block = m.append_block;
   o.append_pos = m.append_pos;
   o.view_limit = m.view_limit;
-  const cudaError_t e = launch_plan(a, o, device_sm_count(), static_cast<cudaStream_t>(stream));
+  o.records = device_sm_count();
+  const cudaError_t e = launch_plan(a, o, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? HW_OK : cuda_fail(e);
 }
 

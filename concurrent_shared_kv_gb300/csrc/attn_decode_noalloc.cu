@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "hogwild.h"
@@ -29,6 +30,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[HW_NOALLOC_SCRA
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {nullptr};
+// the description of each device's last call (the scratch's layout follows it)
+hw_attn_desc g_last_desc[kMaxDevices];
+bool g_have_desc[kMaxDevices] = {false};
 
 // Device address of the scratch on the current device; the first call per
 // device looks it up and zero-fills the whole array (synchronously).
@@ -72,10 +76,31 @@ extern "C" int hw_attn_decode_noalloc(const hw_attn_desc *d, const void *q, cons
   // The error word and the merge counters must start at zero.  Every call
   // leaves the counters at zero again, but a call that gave up on a wait may
   // not have, so they are cleared on the stream before each call.
-  const size_t zero_bytes = hw::workspace_layout(*d, 0).partials_off;
-  const cudaError_t e =
-      cudaMemsetAsync(scratch, 0, zero_bytes, static_cast<cudaStream_t>(stream));
+  const hw::WorkspaceLayout L = hw::decode_workspace_layout(*d);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, L.partials_off, s);
   if (e != cudaSuccess) return HW_ERR_CUDA;
+  // The decode's plan cache lives in the scratch at offsets that follow the
+  // description: after a change of description its state and the header of
+  // its first plan buffer are cleared too, so that the next call rebuilds it
+  // (a workspace would be zeroed again likewise).
+  bool fresh;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HW_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    fresh = !g_have_desc[dev] || std::memcmp(&g_last_desc[dev], d, sizeof *d) != 0;
+    g_last_desc[dev] = *d;
+    g_have_desc[dev] = true;
+  }
+  if (fresh) {
+    unsigned char *base = static_cast<unsigned char *>(scratch) + L.cache_off;
+    e = cudaMemsetAsync(base, 0, hw::kPlanCacheStateBytes, s);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(base + hw::kPlanCacheStateBytes + 2 * L.cache_meta_bytes, 0,
+                          hw::kPlanHeaderBytes, s);
+    if (e != cudaSuccess) return HW_ERR_CUDA;
+  }
   return hw_attn_decode(d, q, k_cache, v_cache, block_start, block_len, view_block, view_offset,
                         q_pos, q_to_kv, out, lse, scratch, HW_NOALLOC_SCRATCH_BYTES, stream);
 }

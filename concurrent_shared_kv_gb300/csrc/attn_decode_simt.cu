@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const __grid_
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem<D> &S = *reinterpret_cast<SimtSmem<D> *>(smem_raw);
   PlanCore &P = S.plan;
-  build_plan<kSimtTile>(a, P, S.cache, S.scratch, S.u_range);
+  build_plan<kSimtTile>(a, P, S.cache, S.scratch, S.u_range, static_cast<int>(gridDim.x));
   plan_ranks(a, S.cache, threadIdx.x >> 5, threadIdx.x & 31, 0, 1);  // read by the merge
   int64_t u = S.u_range[0];
   const int64_t u_end = S.u_range[1];

@@ -141,7 +141,8 @@ struct TcSmem {
   int32_t abort_flag;
   int32_t tiles_done;  // tiles whose P the softmax warps have written (progress only)
   uint8_t tflags[kMaxStages];  // per stage: the tile starts (1) / ends (2) its segment
-  int32_t plan_ok;     // the plan (own or loaded) is usable
+  int32_t plan_ok;     // the loaded plan is usable
+  int32_t cache_cur;   // the plan cache's current buffer (hw_attn_decode)
   uint32_t tmem_base;
   float q_mul;         // E4M3: the current segment's score factor (Q~ part scale x k_scale)
   float v_mul[4];      // E4M3: per segment mod 4, the v_scale of its kv head
@@ -183,13 +184,115 @@ __device__ __forceinline__ const uint8_t *plan_cta_record(const uint8_t *plan, i
   return plan + kPlanHeaderBytes + sizeof(PlanShared) + static_cast<size_t>(c) * sizeof(CtaPlan);
 }
 
+// Does a plan header describe a launch of `grid` CTAs with these arguments?
+__device__ __forceinline__ bool header_matches(const DecodeArgs &a, const PlanHeader &h, int grid) {
+  return h.magic == kPlanMagic && h.grid == grid && h.n_rows == a.n_rows &&
+         h.n_q_heads == a.n_q_heads && h.n_kv_heads == a.n_kv_heads && h.head_dim == a.head_dim &&
+         h.n_blocks == a.n_blocks && h.n_view == a.n_view && h.capacity == a.capacity &&
+         (h.limited != 0) == (a.view_limit != nullptr);
+}
 // Does the plan in global memory describe this launch?
 __device__ __forceinline__ bool plan_matches(const DecodeArgs &a, const uint8_t *plan) {
-  const PlanHeader &h = *reinterpret_cast<const PlanHeader *>(plan);
-  return h.magic == kPlanMagic && h.grid == static_cast<int32_t>(gridDim.x) &&
-         h.n_rows == a.n_rows && h.n_q_heads == a.n_q_heads && h.n_kv_heads == a.n_kv_heads &&
-         h.head_dim == a.head_dim && h.n_blocks == a.n_blocks && h.n_view == a.n_view &&
-         h.capacity == a.capacity && (h.limited != 0) == (a.view_limit != nullptr);
+  return header_matches(a, *reinterpret_cast<const PlanHeader *>(plan), static_cast<int>(gridDim.x));
+}
+
+// The header of a plan through L2 (another launch may have written it).
+__device__ __forceinline__ PlanHeader load_header_cg(const uint8_t *plan) {
+  static_assert(sizeof(PlanHeader) % 4 == 0, "header words");
+  uint32_t w[sizeof(PlanHeader) / 4];
+  for (size_t i = 0; i < sizeof(PlanHeader) / 4; ++i) w[i] = __ldcg(reinterpret_cast<const uint32_t *>(plan) + i);
+  PlanHeader h;
+  memcpy(&h, w, sizeof h);
+  return h;
+}
+
+// ------------------------------------------------------------- plan cache
+//
+// hw_attn_decode plans every call itself, but the layers of a step share
+// their metadata: the workspace keeps the plan of the metadata it last saw,
+// double-buffered (PlanCacheState).  A plan launch compares the call's
+// metadata with the copy beside the current plan; on a match it writes
+// nothing, otherwise it builds the plan and the copy into the other buffer
+// and its last CTA makes that buffer current.  The decode launch after it
+// takes the current buffer: under the early-loads promise, before its wait,
+// when that buffer already matches (the plan launch wrote nothing, or has
+// finished); otherwise after the wait, when the plan launch is complete.
+__device__ __forceinline__ int32_t *cache_state(const DecodeArgs &a) {
+  return reinterpret_cast<int32_t *>(a.cache_base);
+}
+__device__ __forceinline__ int32_t *cache_meta(const DecodeArgs &a, int k) {
+  return reinterpret_cast<int32_t *>(a.cache_base + kPlanCacheStateBytes + k * a.cache_meta_bytes);
+}
+__device__ __forceinline__ uint8_t *cache_plan(const DecodeArgs &a, int k) {
+  return a.cache_base + kPlanCacheStateBytes + 2 * a.cache_meta_bytes + k * a.cache_plan_bytes;
+}
+// The current buffer; acquired, so that its plan and copy read complete.
+__device__ __forceinline__ int cache_current(const DecodeArgs &a) {
+  return ld_acquire_gpu(cache_state(a)) & 1;
+}
+
+// Word j of the caller's metadata in the copy's layout (cache_write_meta).
+__device__ __forceinline__ int32_t caller_meta_word(const DecodeArgs &a, int j) {
+  const int E = a.n_rows * a.n_view, R = a.n_rows, Hq = a.n_q_heads, nb = a.n_blocks;
+  if (j < E) return __ldg(a.view_block + j);
+  if ((j -= E) < E) return __ldg(a.view_offset + j);
+  if ((j -= E) < R) return __ldg(a.q_pos + j);
+  if ((j -= R) < Hq) return a.q_to_kv ? __ldg(a.q_to_kv + j) : j / (Hq / a.n_kv_heads);
+  if ((j -= Hq) < nb) return __ldg(a.block_start + j);
+  return __ldg(a.block_len + j - nb);
+}
+
+// The decode's fetch from the plan cache, in one round of loads: cached plan
+// k (its shared part and this CTA's record, into registers), its header and
+// metadata copy, and the caller's metadata; when they describe this launch
+// the plan goes to shared memory.  Every thread takes part.  Returns whether
+// it matched (the same in every thread).
+__device__ bool cache_fetch(const DecodeArgs &a, int k, PlanShared &ps, CtaPlan &cp, int tid, int nt) {
+  constexpr int kShared = sizeof(PlanShared) / 16, kRec = sizeof(CtaPlan) / 16, kPer = 4;
+  static_assert(kShared <= kPer * 256 && kRec <= 256, "one round of loads of 256 threads");
+  const uint8_t *plan = cache_plan(a, k);
+  const uint4 *src = reinterpret_cast<const uint4 *>(plan + kPlanHeaderBytes);
+  const uint4 *rsrc = reinterpret_cast<const uint4 *>(plan_cta_record(plan, blockIdx.x));
+  uint4 v[kPer], rv = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int r = 0; r < kPer; ++r)
+    if (tid + r * nt < kShared) v[r] = __ldcg(src + tid + r * nt);
+  if (tid < kRec) rv = __ldcg(rsrc + tid);
+  bool same = true;
+  if (tid == 0) same = header_matches(a, load_header_cg(plan), static_cast<int>(gridDim.x));
+  const int words = static_cast<int>(plan_cache_meta_words(a.n_rows, a.n_view, a.n_q_heads, a.n_blocks));
+  const int32_t *m = cache_meta(a, k);
+#pragma unroll 4
+  for (int j = tid; j < words; j += nt) same &= __ldcg(m + j) == caller_meta_word(a, j);
+  same = __syncthreads_and(same);
+  if (same) {
+    uint4 *dst = reinterpret_cast<uint4 *>(&ps);
+#pragma unroll
+    for (int r = 0; r < kPer; ++r)
+      if (tid + r * nt < kShared) dst[tid + r * nt] = v[r];
+    if (tid < kRec) reinterpret_cast<uint4 *>(&cp)[tid] = rv;
+  }
+  return same;
+}
+
+// The caller's metadata into copy k (the layout caller_meta_word reads).
+__device__ void cache_write_meta(const DecodeArgs &a, int k, int tid, int nt) {
+  const int E = a.n_rows * a.n_view, R = a.n_rows, Hq = a.n_q_heads, nb = a.n_blocks;
+  const int G = Hq / a.n_kv_heads;
+  int32_t *m = cache_meta(a, k);
+  for (int i = tid; i < E; i += nt) {
+    m[i] = __ldg(a.view_block + i);
+    m[E + i] = __ldg(a.view_offset + i);
+  }
+  m += 2 * E;
+  for (int i = tid; i < R; i += nt) m[i] = __ldg(a.q_pos + i);
+  m += R;
+  for (int i = tid; i < Hq; i += nt) m[i] = a.q_to_kv ? __ldg(a.q_to_kv + i) : i / G;
+  m += Hq;
+  for (int i = tid; i < nb; i += nt) {
+    m[i] = __ldg(a.block_start + i);
+    m[nb + i] = __ldg(a.block_len + i);
+  }
 }
 
 __device__ __forceinline__ void set_abort(TcSmem &S, const DecodeArgs &a) {
@@ -635,7 +738,7 @@ __device__ __forceinline__ int64_t next_segment(const PlanCore &P, int n_blocks,
 // Prologue of warps 2-7 (nt = 192), or of warps 2-5 alone (nt = 128) while warps 6-7
 // write the CTA's new tokens: the metadata of segment 0 (warp 2), then its
 // queries rotated into the Q~ buffer.
-template <bool kPlanned, bool kFp8>
+template <bool kFp8>
 __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1, int nt) {
   const int t = threadIdx.x - kWarpSoft * 32;  // 0 .. nt-1
   const int w = t >> 5, lane = t & 31;
@@ -646,10 +749,6 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
     else
       asm volatile("bar.sync 3, 128;" ::: "memory");
   };
-  if (w == 0 && !kPlanned) {  // a plan brings it ready-made
-    const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, u0);
-    seg_pre<false>(a, S.ps.plan, S.ps.cache, S.cp.pre[0], x.b, x.g, x.h, lane);
-  }
   sync();
   const SegQ &X = S.cp.pre[0];
   const int nq = min(X.m.n_ref * G, kN);
@@ -806,7 +905,7 @@ __device__ void append_tokens(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_
 // warps' record stores sit on the path of the next rotated queries.  Last,
 // the metadata of segment j + 2 goes into the slot segment j - 2 vacated,
 // and its queries are prefetched into L2.
-template <bool kPlanned, bool kLimit, bool kFp8>
+template <bool kLimit, bool kFp8>
 __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
   const int tq = threadIdx.x - kWarpQ * 32;  // 0..63
   const int lane = threadIdx.x & 31, wq = tq >> 5;
@@ -819,25 +918,6 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
     wait_or_abort(S, a, &S.rec_ready[done & 3], (done >> 2) & 1);
     if (wq == 0) arrive_segment(a, S.cp.pre[done % kPre].m, lane);
   };
-  if (!kPlanned) {
-    // first units and metadata of segments 1 .. kPre-1 (a plan brings them)
-    if (tq == 0) {
-      int64_t u = u0;
-      for (int k = 0; k < kPre; ++k) {
-        S.cp.us[k] = u;
-        if (u < u1) u = next_segment(S.ps.plan, a.n_blocks, u);
-      }
-    }
-    sync();
-#pragma unroll
-    for (int k = 1; k < kPre; ++k) {
-      if ((k & 1) == wq && S.cp.us[k] < u1) {
-        const UnitPos x = unit_pos(S.ps.plan, a.n_blocks, S.cp.us[k]);
-        seg_pre<kLimit>(a, S.ps.plan, S.ps.cache, S.cp.pre[k], x.b, x.g, x.h, lane);
-      }
-    }
-    sync();
-  }
   int64_t u = S.cp.us[1];  // segment 1
   int64_t u_prep = S.cp.us[kPre - 1] < u1 ? next_segment(S.ps.plan, a.n_blocks, S.cp.us[kPre - 1]) : u1;  // segment kPre
   for (int seg = 1;; ++seg) {
@@ -846,42 +926,6 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
       // (a plan brings it): ranks and group indices, and the list of the
       // CTA's first item - once the softmax warps are past their first
       // tiles, so as not to slow them
-      if (!kPlanned) {
-        {
-          // tiles_done only grows; the wait is bounded like every other
-          const int want = static_cast<int>(u1 - u0) < 3 ? static_cast<int>(u1 - u0) : 3;
-          const long long t0 = clock64();
-          while (*reinterpret_cast<volatile int32_t *>(&S.tiles_done) < want && !aborted(S)) {
-            if (clock64() - t0 > kWaitLimit) {
-              set_abort(S, a);
-              break;
-            }
-            __nanosleep(256);
-          }
-        }
-        plan_ranks(a, S.ps.cache, wq, lane, 0, 1);
-        {
-          // this CTA's rank by units (which CTAs merge: merge_ctas)
-          int part = units_rank_part(S.ps.plan, a.n_blocks, static_cast<int>(gridDim.x),
-                                     static_cast<int>(blockIdx.x), u1 - u0, tq, 64);
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-          if (lane == 0) S.qmax[6 + wq] = part;
-        }
-        sync();
-        if (tq == 0) S.cp.mrank = S.qmax[6] + S.qmax[7];
-        const int nm = merge_ctas(a, static_cast<int>(gridDim.x));
-        if (wq == 0 && S.ps.cache.entries_cached) {
-          const int first = S.qmax[6] + S.qmax[7];
-          int n = -1;
-          if (first < nm && first < a.n_rows * a.n_q_heads) {
-            n = merge_list(a, S.ps.plan, S.ps.cache, first / a.n_q_heads, first % a.n_q_heads,
-                           S.cp.mpre[0], kPreList, nullptr, lane);
-            if (n > kPreList) n = -1;
-          }
-          if (lane == 0) S.cp.mpre_n[0] = n;
-        }
-      }
       if (seg >= 2) arrivals(seg - 2);
       arrivals(seg - 1);
       break;
@@ -1259,13 +1303,210 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     segment_records<kFp8>(a, S, tl, pend, pend_sid, pend_nq, ws, lane, row, sync, pend_vmul);
 }
 
-// kPlanned: the step's plan is loaded (else built in-kernel); kAppend (with a
-// plan): the layer's new tokens are written first; kLimit (with a plan, no
-// appends): the plan carries view limits; kFp8 (with a plan): E4M3 caches
-// with per-kv-head scales.  Each combination is its own kernel, so
-// that no path carries another's code (a second softmax loop in the same
-// kernel, even one never entered, cost the plain path 8 %).
-template <bool kPlanned, bool kAppend, bool kLimit, bool kFp8>
+constexpr int kPlanWarps = kThreads / 32;
+
+__device__ __forceinline__ void copy16(uint8_t *dst, const void *src, size_t bytes, int tid, int nt) {
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+  for (size_t i = tid; i < bytes / 16; i += nt) d4[i] = s4[i];
+}
+
+// Record of decode CTA c of R (into cp, and then, unless `plan` is null, at
+// the position of the CTA's rank in `plan`), by a group of nw warps (wi: this
+// warp's index in it; sync: the group's barrier): warp 0 derives the unit
+// range, first tiles, rank and new tokens, then the warps share the first
+// segments' query metadata and the first merge lists.  ubeg: first unit of
+// every decode CTA ([R] = U); rank_tmp: per-warp scratch of merge_list.
+template <typename Sync>
+__device__ void plan_record(const DecodeArgs &a, const PlanShared &ps, const int64_t *ubeg,
+                            CtaPlan &cp, int32_t (*rank_tmp)[HW_MAX_VIEW_BLOCKS], int c, int R,
+                            uint8_t *plan, int wi, int nw, int lane, Sync sync) {
+  const PlanCore &P = ps.plan;
+  const int64_t u0 = ubeg[c], u1 = ubeg[c + 1];
+  if (wi == 0) {
+    if (lane == 0) {
+      cp.u0 = u0;
+      cp.u1 = u1;
+      cp.c_log = c;
+      int64_t u = u0;
+      for (int k = 0; k < kPre; ++k) {
+        cp.us[k] = u;
+        if (u < u1) u = next_segment(P, a.n_blocks, u);
+      }
+    }
+    // the first tiles (the ring's first fill)
+    const int nf = static_cast<int>(min(static_cast<int64_t>(kStages), u1 - u0));
+    if (lane < kStages) {
+      TileRef t = {0, 0, 0};
+      if (lane < nf) t = tile_ref(P, a.n_blocks, u0 + lane, u0, u1);
+      cp.trow[lane] = t.row;
+      cp.th[lane] = static_cast<uint8_t>(t.h);
+      cp.tfl[lane] = t.flags;
+    }
+    if (lane == 0) cp.n_first = static_cast<uint8_t>(nf);
+    // its rank by units (which CTAs merge: merge_ctas): the CTAs with more
+    // units, or as many and a lower index, come first
+    const int64_t mine = u1 - u0;
+    int before = 0;
+    for (int c2 = lane; c2 < R; c2 += 32) {
+      const int64_t u2 = ubeg[c2 + 1] - ubeg[c2];
+      before += c2 != c && (u2 > mine || (u2 == mine && c2 < c)) ? 1 : 0;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    if (lane == 0) cp.mrank = before;
+    // the step's new tokens that lie in its tiles (a token outside its
+    // block is an error and skipped): how many, the first tile that holds
+    // one, and the first kAppList of them
+    int app_n = 0, app_tile = INT_MAX;
+    if (a.append_block) {
+      const int Hkv = a.n_kv_heads, npairs = a.n_rows * Hkv;
+      for (int base = 0; base < npairs; base += 32) {
+        const int pr = base + lane;
+        bool in = false;
+        int row = 0, pos = 0;
+        int64_t u = -1;
+        if (pr < npairs) {
+          const int r = pr / Hkv, h = pr - r * Hkv;
+          const int b = __ldg(a.append_block + r);
+          if (b >= 0) {
+            pos = __ldg(a.append_pos + r);
+            if (b >= a.n_blocks || pos < 0 || pos >= P.len[b]) {
+              if (c == 0 && h == 0) flag_error(a.err, HW_DEV_BAD_RANGE);
+            } else if (P.tiles[b] > 0) {  // (a block no view reads takes no part)
+              // the first of its units that read the token's tile (one per
+              // column group): every CTA reading it writes the token - the
+              // same bytes - before its own copy of the tile
+              u = tile_unit_in(P, b, h, pos / kT, u0, u1);
+              in = u >= 0;
+              row = P.start[b] + pos;
+            }
+          }
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        const int k = app_n + __popc(m & lanemask_lt(lane));
+        if (in && k < kAppList) {
+          cp.app_pair[k] = pr;
+          cp.app_row[k] = row;
+          cp.app_pos[k] = pos;
+        }
+        app_n += __popc(m);
+        if (in) app_tile = min(app_tile, static_cast<int>(u - u0));
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1)
+        app_tile = min(app_tile, __shfl_xor_sync(0xffffffffu, app_tile, o));
+    }
+    if (lane == 0) {
+      cp.app_n = app_n;
+      cp.app_tile = app_tile;
+    }
+  }
+  sync();
+  // the query-side metadata of its first segments, then the record lists of
+  // its first merge items (item k: rank + k * nm), shared by the warps
+  for (int k = wi; k < kPre; k += nw) {
+    if (cp.us[k] < u1) {
+      const UnitPos x = unit_pos(P, a.n_blocks, cp.us[k]);
+      seg_pre<true>(a, P, ps.cache, cp.pre[k], x.b, x.g, x.h, lane);
+    }
+  }
+  const int nm = merge_ctas(a, R), mrank = cp.mrank;
+  for (int k = 0; k < kPreItems; ++k) {
+    if ((kPre + k) % nw != wi) continue;
+    const int it = mrank + k * nm;
+    int n = -1;
+    if (mrank < nm && it < a.n_rows * a.n_q_heads) {
+      n = merge_list(a, P, ps.cache, it / a.n_q_heads, it % a.n_q_heads, cp.mpre[k], kPreList,
+                     rank_tmp[wi], lane);
+      if (n > kPreList) n = -1;
+    }
+    if (lane == 0) cp.mpre_n[k] = n;
+  }
+  sync();
+  // at the position of its rank: a decode launch's CTA b (CTAs are placed in
+  // index order, the low ones on the SMs the previous launch frees first) runs
+  // the b-th heaviest share, so the heaviest shares - which also merge - get
+  // their SMs first and the light ones take the SMs freed last
+  if (plan)
+    copy16(const_cast<uint8_t *>(plan_cta_record(plan, mrank)), &cp, sizeof(CtaPlan),
+           wi * 32 + lane, nw * 32);
+  sync();  // (cp may be the group's next record)
+}
+
+__device__ __forceinline__ void write_plan_header(const DecodeArgs &a, uint8_t *plan, int grid) {
+  PlanHeader h;
+  h.magic = kPlanMagic;
+  h.grid = grid;
+  h.n_rows = a.n_rows;
+  h.n_q_heads = a.n_q_heads;
+  h.n_kv_heads = a.n_kv_heads;
+  h.head_dim = a.head_dim;
+  h.n_blocks = a.n_blocks;
+  h.n_view = a.n_view;
+  h.capacity = a.capacity;
+  h.limited = a.view_limit != nullptr;
+  *reinterpret_cast<PlanHeader *>(plan) = h;
+}
+
+struct WarpSync {
+  __device__ __forceinline__ void operator()() const { __syncwarp(); }
+};
+
+// hw_attn_decode when the plan cache holds another metadata's plan (current
+// buffer `cur`): every CTA builds the plan from the caller's metadata - the
+// shared part, and its own record as CTA c of the split - into shared
+// memory, and writes it into the other buffer for the calls that follow
+// (CTA 0: the shared part, the header and the metadata copy; every CTA: its
+// record at its rank).  The last CTA done makes that buffer current, before
+// it lets the next launch start.  Every thread takes part.
+__device__ __noinline__ void build_cached_plan(const DecodeArgs &a, TcSmem &S, int cur) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = static_cast<int>(gridDim.x);
+  struct Scratch {  // in stage 0, which no copy has touched yet
+    PlanScratch build;
+    int64_t ubeg[kThreads + 1];
+    int32_t rank_tmp[kPlanWarps][HW_MAX_VIEW_BLOCKS];
+  };
+  static_assert(sizeof(Scratch) <= kStageBytes, "plan scratch fits a stage");
+  Scratch &Z = *reinterpret_cast<Scratch *>(S.stage[0]);
+  int64_t unused[2];
+  build_plan<kT>(a, S.ps.plan, S.ps.cache, Z.build, unused, R);
+  plan_ranks(a, S.ps.cache, warp, lane, 0, 1);
+  for (int c = tid; c <= R; c += kThreads) Z.ubeg[c] = cta_unit_begin(S.ps.plan, a.n_blocks, c);
+  __syncthreads();
+  const int target = cur ^ 1;
+  uint8_t *plan = cache_plan(a, target);
+  plan_record(a, S.ps, Z.ubeg, S.cp, Z.rank_tmp, blockIdx.x, R, plan, warp, kPlanWarps, lane,
+              CtaSync());
+  if (blockIdx.x == 0) {
+    copy16(plan + kPlanHeaderBytes, &S.ps, sizeof(PlanShared), tid, kThreads);
+    cache_write_meta(a, target, tid, kThreads);
+    if (tid == 0) write_plan_header(a, plan, R);
+  }
+  // every CTA's stores before its arrival, the arrivals before the switch
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    int32_t *st = cache_state(a);
+    if (atomicAdd(st + 1, 1) == R - 1) {
+      __threadfence();
+      st[1] = 0;
+      asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(st), "r"(target) : "memory");
+      __threadfence();
+    }
+  }
+  __syncthreads();
+}
+
+// Every launch runs from a plan: hw_attn_plan's, or (kCache) hw_attn_decode's
+// plan cache, rebuilt by the launch itself when its metadata differs.
+// kAppend: the layer's new tokens are written first; kLimit (no appends): the
+// plan carries view limits; kFp8: E4M3 caches with per-kv-head scales.  Each
+// combination is its own kernel, so that no path carries another's code (a
+// second softmax loop in the same kernel, even one never entered, cost the
+// plain path 8 %).
+template <bool kAppend, bool kLimit, bool kFp8, bool kCache>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
@@ -1309,13 +1550,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.abort_flag = 0;
     S.tiles_done = 0;
     S.plan_ok = 1;
-    // (with a plan, the bulk copy brings these: no generic store may race it)
-    if (!kPlanned) {
-      for (int k = 0; k < kPreItems; ++k) S.cp.mpre_n[k] = -1;
-      S.cp.c_log = static_cast<int32_t>(blockIdx.x);
-      S.cp.n_first = 0;
-      S.cp.app_n = 0;
-    }
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -1353,12 +1587,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // The plan: loaded (the shared part and this CTA's record, two bulk
-  // copies) or built in-kernel from the metadata.  Errors it finds are
-  // recorded after griddepcontrol.wait.
+  // The plan: the shared part and this CTA's record, into shared memory -
+  // hw_attn_plan's with two bulk copies, or the plan cache's (see "plan
+  // cache") with loads through L2, or built here when the cache holds
+  // another metadata's plan.  Errors it finds are recorded after
+  // griddepcontrol.wait.
   bool plan_timeout = false;
   auto get_plan = [&]() {
-    if (kPlanned) {
+    if constexpr (kCache) {
+      // (the launch before this one, if it rebuilt the cache, switched
+      // buffers before it let this one start)
+      if (tid == 0) S.cache_cur = cache_current(a);
+      __syncthreads();
+      const int k = S.cache_cur;
+      if (!cache_fetch(a, k, S.ps, S.cp, tid, kThreads)) build_cached_plan(a, S, k);
+    } else {
       if (tid == 0) {
         mbar_arrive_expect_tx(&S.plan_bar, sizeof(PlanShared) + sizeof(CtaPlan));
         bulk_g2s(&S.ps, a.plan + kPlanHeaderBytes, sizeof(PlanShared), &S.plan_bar);
@@ -1370,13 +1613,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         plan_timeout = true;
         S.plan_ok = 0;
       }
-      __syncthreads();  // every thread's wait is over: the table may be refreshed
-      if (tid < 64) S.ps.cache.phase[tid] = a.phase[tid];  // this launch's RoPE table
-    } else {
-      // the plan scratch borrows stage 0, which no copy has touched yet
-      build_plan<kT>(a, S.ps.plan, S.ps.cache, *reinterpret_cast<PlanScratch *>(S.stage[0]),
-                     *reinterpret_cast<int64_t(*)[2]>(&S.cp.u0));
     }
+    __syncthreads();  // the plan is in place: the table may be refreshed
+    if (tid < 64) S.ps.cache.phase[tid] = a.phase[tid];  // this launch's RoPE table
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1417,18 +1656,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (appending && warp >= kWarpQ)
         append_tokens<kFp8>(a, S, u0, u1);
       else
-        query_prologue<kPlanned, kFp8>(a, S, u0, u1, appending ? 128 : 192);
+        query_prologue<kFp8>(a, S, u0, u1, appending ? 128 : 192);
       if (warp < kWarpQ)
         softmax_role<kLimit, kFp8>(a, S, tmem, u0, u1);
       else
-        qprep<kPlanned, kLimit, kFp8>(a, S, u0, u1);
+        qprep<kLimit, kFp8>(a, S, u0, u1);
     }
-  } else if (!kPlanned) {
-    plan_ranks(a, S.ps.cache, warp, lane, 0, 1);  // a CTA without units: ranks for the merge
-    const int part = units_rank_part(S.ps.plan, a.n_blocks, static_cast<int>(gridDim.x),
-                                     static_cast<int>(blockIdx.x), 0, tid, kThreads);
-    const int rank = __syncthreads_count(part);  // (one CTA per thread at most)
-    if (tid == 0) S.cp.mrank = rank;
   }
   tc_fence_before();
   __syncthreads();
@@ -1449,21 +1682,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        merge_ctas(a, static_cast<int>(gridDim.x)));
 }
 
-// The plan of one decode step (see "plans" above).  Any grid: CTA c writes
-// the record of decode CTA c, CTA 0 also the metadata copies, the shared part
-// and the header.  With o.plan null only the metadata is copied.
+// The plan of the decode launches of `o.records` CTAs (see "plans" above):
+// every CTA derives the shared part, then its warps write CTA records - one
+// record per warp at a time: warp w of CTA b writes records b + grid w,
+// b + grid (w + 8), ... - each at the position of the CTA's rank.  CTA 0 also writes the
+// metadata copies (hw_attn_plan), the shared part and the header.  With
+// o.plan null and no plan cache only the metadata is copied.
+constexpr int kPlanRecordsPerCta = 2 * kPlanWarps;  // a launch's grid: records / this
 struct PlanSmem {
   PlanShared ps;
-  CtaPlan cp;
   PlanScratch scratch;
-  int32_t rank_tmp[kPreItems][HW_MAX_VIEW_BLOCKS];
+  int64_t ubeg[kThreads + 1];  // first unit of every decode CTA; [records] = U
+  CtaPlan cp[kPlanWarps];      // the record each warp is building
+  int32_t rank_tmp[kPlanWarps][HW_MAX_VIEW_BLOCKS];
 };
-
-__device__ __forceinline__ void copy16(uint8_t *dst, const void *src, size_t bytes, int tid, int nt) {
-  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-  for (size_t i = tid; i < bytes / 16; i += nt) d4[i] = s4[i];
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     plan_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ PlanOut o) {
@@ -1472,14 +1704,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               ~static_cast<uintptr_t>(15));
   const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.n_rows * a.n_view, G = a.n_q_heads / a.n_kv_heads;
-  // Launched as a programmatic dependent (hw_attn_decode's own plan, into a
-  // region no other call reads) this kernel may start while the previous one
-  // runs: it reads the caller's metadata before griddepcontrol.wait only
-  // under the early-loads promise, and ends after the wait, so that its
-  // completion implies the previous grid's.  (A plain launch: the wait
-  // returns at once.)
+  const int R = o.records;
+  // A plain launch, once per decode step.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (!a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  uint8_t *plan = o.plan;
   if (blockIdx.x == 0 && o.view_block) {
     for (int i = tid; i < E; i += nt) {
       o.view_block[i] = a.view_block[i];
@@ -1497,111 +1725,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = tid; i < E; i += nt) o.view_limit[i] = a.view_limit ? a.view_limit[i] : -1;
   }
-  if (!o.plan) {
-    if (a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
-    return;
-  }
+  if (!plan) return;
   PlanCore &P = S.ps.plan;
-  build_plan<kT>(a, P, S.ps.cache, S.scratch, *reinterpret_cast<int64_t(*)[2]>(&S.cp.u0));
+  int64_t unused[2];
+  build_plan<kT>(a, P, S.ps.cache, S.scratch, unused, R);
   plan_ranks(a, S.ps.cache, warp, lane, 0, 1);
-  if (tid == 0) {
-    int64_t u = S.cp.u0;
-    for (int k = 0; k < kPre; ++k) {
-      S.cp.us[k] = u;
-      if (u < S.cp.u1) u = next_segment(P, a.n_blocks, u);
-    }
-    S.cp.app_n = 0;
-    S.cp.app_tile = INT_MAX;
-    const int64_t nf = min(static_cast<int64_t>(kStages), S.cp.u1 - S.cp.u0);
-    S.cp.n_first = static_cast<uint8_t>(nf > 0 ? nf : 0);
-    for (int i = 0; i < kStages; ++i) {
-      TileRef t = {0, 0, 0};
-      if (i < nf) t = tile_ref(P, a.n_blocks, S.cp.u0 + i, S.cp.u0, S.cp.u1);
-      S.cp.trow[i] = t.row;
-      S.cp.th[i] = static_cast<uint8_t>(t.h);
-      S.cp.tfl[i] = t.flags;
-    }
-  }
-  {
-    // this CTA's rank by units (which CTAs merge: merge_ctas)
-    const int part = units_rank_part(P, a.n_blocks, static_cast<int>(gridDim.x),
-                                     static_cast<int>(blockIdx.x), S.cp.u1 - S.cp.u0, tid, nt);
-    const int rank = __syncthreads_count(part);  // (one CTA per thread at most)
-    if (tid == 0) {
-      S.cp.mrank = rank;
-      S.cp.c_log = static_cast<int32_t>(blockIdx.x);
-    }
-  }
+  for (int c = tid; c <= R; c += nt) S.ubeg[c] = cta_unit_begin(P, a.n_blocks, c);
   __syncthreads();
-  if (a.append_block) {
-    // the step's new tokens that lie in this CTA's tiles: how many, and the
-    // first such tile (a token outside its block is an error and skipped)
-    const int Hkv = a.n_kv_heads;
-    for (int pr = tid; pr < a.n_rows * Hkv; pr += nt) {
-      const int r = pr / Hkv, h = pr - r * Hkv;
-      const int b = a.append_block[r];
-      if (b < 0) continue;
-      const int pos = a.append_pos[r];
-      if (b >= a.n_blocks || pos < 0 || pos >= P.len[b]) {
-        if (blockIdx.x == 0 && h == 0) flag_error(a.err, HW_DEV_BAD_RANGE);
-        continue;
-      }
-      if (P.tiles[b] == 0) continue;  // a block no view reads takes no part
-      // the first of this CTA's units that read the token's tile (one per
-      // column group): every CTA reading it writes the token - the same bytes
-      const int64_t u = tile_unit_in(P, b, h, pos / kT, S.cp.u0, S.cp.u1);
-      if (u >= 0) {
-        const int k = atomicAdd(&S.cp.app_n, 1);
-        atomicMin(&S.cp.app_tile, static_cast<int>(u - S.cp.u0));
-        if (k < kAppList) {
-          S.cp.app_pair[k] = pr;
-          S.cp.app_row[k] = P.start[b] + pos;
-          S.cp.app_pos[k] = pos;
-        }
-      }
-    }
-    __syncthreads();
-  }
-  if (warp < kPre && S.cp.us[warp] < S.cp.u1) {
-    const UnitPos x = unit_pos(P, a.n_blocks, S.cp.us[warp]);
-    seg_pre<true>(a, P, S.ps.cache, S.cp.pre[warp], x.b, x.g, x.h, lane);
-  } else if (warp >= kPre && warp < kPre + kPreItems) {
-    // the record lists of the CTA's first merge items (item k: rank + k * nm)
-    const int k = warp - kPre;
-    const int nm = merge_ctas(a, static_cast<int>(gridDim.x));
-    const int it = S.cp.mrank + k * nm;
-    int n = -1;
-    if (S.cp.mrank < nm && it < a.n_rows * a.n_q_heads) {
-      n = merge_list(a, P, S.ps.cache, it / a.n_q_heads, it % a.n_q_heads, S.cp.mpre[k], kPreList,
-                     S.rank_tmp[k], lane);
-      if (n > kPreList) n = -1;
-    }
-    if (lane == 0) S.cp.mpre_n[k] = n;
-  }
-  __syncthreads();
-  // at the position of its rank: a decode launch's CTA b (CTAs are placed in
-  // index order, the low ones on the SMs the previous launch frees first) runs
-  // the b-th heaviest share, so the heaviest shares - which also merge - get
-  // their SMs first and the light ones take the SMs freed last
-  copy16(const_cast<uint8_t *>(plan_cta_record(o.plan, S.cp.mrank)), &S.cp, sizeof(CtaPlan), tid, nt);
+  for (int c = blockIdx.x + gridDim.x * warp; c < R; c += gridDim.x * kPlanWarps)
+    plan_record(a, S.ps, S.ubeg, S.cp[warp], &S.rank_tmp[warp], c, R, plan, 0, 1, lane, WarpSync());
   if (blockIdx.x == 0) {
-    copy16(o.plan + kPlanHeaderBytes, &S.ps, sizeof(PlanShared), tid, nt);
-    if (tid == 0) {
-      PlanHeader h;
-      h.magic = kPlanMagic;
-      h.grid = static_cast<int32_t>(gridDim.x);
-      h.n_rows = a.n_rows;
-      h.n_q_heads = a.n_q_heads;
-      h.n_kv_heads = a.n_kv_heads;
-      h.head_dim = a.head_dim;
-      h.n_blocks = a.n_blocks;
-      h.n_view = a.n_view;
-      h.capacity = a.capacity;
-      h.limited = a.view_limit != nullptr;
-      *reinterpret_cast<PlanHeader *>(o.plan) = h;
-    }
+    copy16(plan + kPlanHeaderBytes, &S.ps, sizeof(PlanShared), tid, nt);
+    if (tid == 0) write_plan_header(a, plan, R);
   }
-  if (a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -1640,8 +1776,7 @@ int plan_export_records(const uint8_t *plan_host, int64_t *out, int max_ctas) {
   return h.grid;
 }
 
-cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s,
-                        bool dependent) {
+cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, cudaStream_t s) {
   const size_t smem = sizeof(PlanSmem) + 16;
   static bool configured = false;
   if (!configured) {
@@ -1650,41 +1785,34 @@ cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStr
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  if (o.plan && ctas > kThreads) return cudaErrorInvalidConfiguration;  // (as launch_decode_tc)
-  if (!dependent) {
-    plan_kernel<<<o.plan ? ctas : 1, kThreads, smem, s>>>(a, o);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(o.plan ? ctas : 1);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, plan_kernel, a, o);
+  // records are the decode launches' CTAs (ranked by one warp's lanes, at
+  // most kThreads of them)
+  if (o.records <= 0 || o.records > kThreads) return cudaErrorInvalidConfiguration;
+  const int grid = o.plan ? (o.records + kPlanRecordsPerCta - 1) / kPlanRecordsPerCta : 1;
+  plan_kernel<<<grid, kThreads, smem, s>>>(a, o);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                              int ctas, cudaStream_t s) {
-  // the merge CTAs are ranked with one CTA per thread (units_rank_part)
+  // a plan holds at most kThreads records (ranked by one warp's lanes)
   if (ctas > kThreads) return cudaErrorInvalidConfiguration;
   const size_t smem = decode_tc_smem_bytes();
   // planned launches run their own instantiations: without the plan-building
   // (and, without appends, the append) code the kernel is far smaller
-  // (every decode runs from a plan: hw_attn_decode plans first)
-  if (!a.plan) return cudaErrorInvalidValue;
-  const int which = a.k_new ? (a.k_scale ? 6 : 2)
+  // every decode runs from a plan: hw_attn_plan's, or the plan cache's (only
+  // for the plain bf16 call, hw_attn_decode)
+  if (a.cache_base ? (a.plan || a.k_new || a.k_scale || a.view_limit) : !a.plan)
+    return cudaErrorInvalidValue;
+  const int which = a.cache_base ? 0
+                    : a.k_new ? (a.k_scale ? 6 : 2)
                     : a.k_scale ? (a.view_limit ? 5 : 4)
                     : a.view_limit ? 3 : 1;
   void (*const kernels[7])(DecodeArgs, CUtensorMap, CUtensorMap) = {
-      nullptr, decode_tc_kernel<true, false, false, false>,
-      decode_tc_kernel<true, true, false, false>, decode_tc_kernel<true, false, true, false>,
-      decode_tc_kernel<true, false, false, true>, decode_tc_kernel<true, false, true, true>,
-      decode_tc_kernel<true, true, false, true>};
+      decode_tc_kernel<false, false, false, true>, decode_tc_kernel<false, false, false, false>,
+      decode_tc_kernel<true, false, false, false>, decode_tc_kernel<false, true, false, false>,
+      decode_tc_kernel<false, false, true, false>, decode_tc_kernel<false, true, true, false>,
+      decode_tc_kernel<true, false, true, false>};
   void (*kernel)(DecodeArgs, CUtensorMap, CUtensorMap) = kernels[which];
   static bool configured[7] = {false, false, false, false, false, false, false};
   if (!configured[which]) {

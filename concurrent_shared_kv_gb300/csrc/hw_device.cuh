@@ -252,13 +252,13 @@ __device__ __forceinline__ int64_t cta_unit_begin(const PlanCore &P, int n_block
 }
 
 // Loads the metadata into the cache (one round of independent loads), checks
-// it and builds the unit prefix and this CTA's unit range [u_range[0],
-// u_range[1]).  Every thread of
-// the CTA takes part (blockDim.x == 256, three __syncthreads inside); one
-// warp does the serial part in a single pass.
+// it and builds the unit prefix of a split over `grid` CTAs and this CTA's
+// unit range [u_range[0], u_range[1]) in it.  Every thread of the CTA takes
+// part (blockDim.x == 256, three __syncthreads inside); one warp does the
+// serial part in a single pass.  Errors are recorded by CTA 0.
 template <int TILE>
 __device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanScratch &S,
-                           int64_t (&u_range)[2]) {
+                           int64_t (&u_range)[2], int grid) {
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads;
   const int E = a.n_rows * a.n_view;
@@ -376,7 +376,7 @@ __device__ void build_plan(const DecodeArgs &a, PlanCore &P, MetaCache &M, PlanS
       P.WH = kTileW * carry + static_cast<int64_t>(kSegW) * ncarry;
       P.W = P.WH * a.n_kv_heads;
       const int64_t cmax = P.W / (kSegW + kTileW);
-      P.C = static_cast<int>(cmax < static_cast<int64_t>(gridDim.x) ? cmax : gridDim.x);
+      P.C = static_cast<int>(cmax < static_cast<int64_t>(grid) ? cmax : grid);
     }
     __syncwarp();
     // lanes 0 and 1: the two ends of this CTA's unit range, side by side
@@ -621,19 +621,6 @@ __device__ __forceinline__ int merge_ctas(const DecodeArgs &a, int grid) {
   const int nm = (items + 1) / 2;
   return nm < grid ? nm : grid;
 }
-// This CTA's rank in that order (units u_mine), counted by the threads
-// tid < nt of a group: the CTAs c' = tid, tid + nt, ... that come before it.
-__device__ __forceinline__ int units_rank_part(const PlanCore &P, int n_blocks, int grid, int c,
-                                               int64_t u_mine, int tid, int nt) {
-  int before = 0;
-  for (int c2 = tid; c2 < grid; c2 += nt) {
-    if (c2 == c) continue;
-    const int64_t u2 = cta_unit_begin(P, n_blocks, c2 + 1) - cta_unit_begin(P, n_blocks, c2);
-    before += (u2 > u_mine || (u2 == u_mine && c2 < c)) ? 1 : 0;
-  }
-  return before;
-}
-
 // The record list of merge item (row r, q head hq) in view order, built by
 // one warp: for every view entry (rank k among the references to its block:
 // column group k / rpg, rank k % rpg within it), the records that the CTAs

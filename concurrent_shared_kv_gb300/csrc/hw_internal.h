@@ -50,6 +50,9 @@ struct DecodeArgs {
   int32_t n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
   int64_t capacity;
   const uint8_t *plan;  // precomputed plan of the tensor-core kernel (hw_attn_plan), or null
+  // hw_attn_decode's plan cache in the workspace (see PlanCache), or null
+  uint8_t *cache_base;
+  int64_t cache_meta_bytes, cache_plan_bytes;
   // The step's appends: at plan time the caller's arrays (null: none); at
   // decode time the plan's copies.  k_new / v_new: this layer's new tokens,
   // [n_rows][Hkv][D], or null (nothing is written; k and v are then only read).
@@ -68,10 +71,27 @@ struct DecodeArgs {
   uint64_t phase[64];
 };
 
+// hw_attn_decode's plan cache: [state: current buffer, arrivals][metadata
+// copy 0][metadata copy 1][plan 0][plan 1].  Buffer `cur` holds the plan of
+// the metadata in copy `cur`; a plan launch whose metadata differs builds
+// into the other buffer and its last CTA makes that one current.  A metadata
+// copy is the effective view_block, view_offset ([rows][V] each), q_pos
+// [rows], q head -> kv head map [Hq], block_start, block_len [blocks].
+struct PlanCacheState {
+  int32_t cur;    // 0 or 1
+  int32_t count;  // CTAs of the building plan launch that are done (0 between launches)
+};
+constexpr size_t kPlanCacheStateBytes = 256;
+inline __host__ __device__ int64_t plan_cache_meta_words(int64_t n_rows, int64_t n_view, int64_t n_q_heads,
+                                                         int64_t n_blocks) {
+  return 2 * n_rows * n_view + n_rows + n_q_heads + 2 * n_blocks;
+}
+
 // Workspace layout helpers (bytes).  The metadata copies and the plan are
 // written by hw_attn_plan and read by hw_attn_decode_planned.
 struct WorkspaceLayout {
-  size_t err_off, counters_off, partials_off, meta_off, plan_off, uplan_off, total;
+  size_t err_off, counters_off, partials_off, meta_off, plan_off, cache_off, total;
+  size_t cache_meta_bytes, cache_plan_bytes;
   int64_t slots;
 };
 constexpr size_t kPlanHeaderBytes = 256;
@@ -84,6 +104,8 @@ size_t plan_cta_bytes();     // the part each CTA reads for itself
 constexpr int kPlanExportFields = 15;
 int plan_export_records(const uint8_t *plan_host, int64_t *out, int max_ctas);
 WorkspaceLayout workspace_layout(const hw_attn_desc &d, int max_ctas);
+// The layout the decode calls use on the current device (their max_ctas).
+WorkspaceLayout decode_workspace_layout(const hw_attn_desc &d);
 
 int device_sm_count();  // SMs of the current device, cached; <= 0 on failure
 
@@ -97,14 +119,12 @@ size_t decode_tc_smem_bytes();
 // tensor-core kernel, the plan (header, shared part, one record per CTA).
 struct PlanOut {
   uint8_t *plan;  // null: copy the metadata only
+  int32_t records;  // CTAs of the decode launches the plan is for
   int32_t *view_block, *view_offset, *q_pos, *q_to_kv, *block_start, *block_len;
   int32_t *append_block, *append_pos;  // -1 / 0 for every row without an append
   int32_t *view_limit;                 // -1 for every entry without a limit
 };
-// dependent: launched as a programmatic dependent of the previous kernel
-// (hw_attn_decode's own plan); otherwise a plain launch (hw_attn_plan).
-cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, int ctas, cudaStream_t s,
-                        bool dependent = false);
+cudaError_t launch_plan(const DecodeArgs &a, const PlanOut &o, cudaStream_t s);
 int decode_simt_ctas_per_sm(int dtype, int head_dim);
 
 // One launch commits n_commits ranges (kernel grid row c = commit c).

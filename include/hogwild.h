@@ -148,7 +148,8 @@ int hw_attn_decode_workspace_size(const hw_attn_desc *d, size_t *bytes);
 /*
  * Zero a workspace (dev, `bytes` long) on `stream`.  Required once before the
  * first hw_attn_decode that uses it; each decode leaves its counters at zero
- * again for the next call.
+ * again for the next call.  A workspace's layout follows its description:
+ * zero it again before using it with another one.
  */
 int hw_workspace_init(void *workspace, size_t bytes, void *stream);
 
