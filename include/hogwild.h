@@ -184,6 +184,17 @@ int hw_workspace_init(void *workspace, size_t bytes, void *stream);
  * The same metadata arrays can serve every layer of a step.  Calls that share
  * a workspace must be ordered on one stream.  Pool slots past a block's
  * length are never used in the result, whatever they hold.
+ *
+ * One launch.  The tensor-core kernel (bf16, head_dim 128) runs from a plan
+ * of the work split that the workspace caches: the plan of the metadata the
+ * last call on the workspace saw, compared word by word with this call's
+ * arrays (contents, not addresses).  A call whose metadata differs - the
+ * first layer of a new step - builds the plan in the kernel and caches it
+ * for the calls after it.  Which call to use: for a step of many layers,
+ * hw_attn_decode on the step's arrays runs within a few percent of
+ * hw_attn_plan + hw_attn_decode_planned (which also lets the caller reuse or
+ * free its arrays after planning); the planned calls are the ones that take
+ * appends, view limits and E4M3 caches.
  */
 int hw_attn_decode(const hw_attn_desc *d, const void *q, const void *k_cache, const void *v_cache,
                    const int32_t *block_start, const int32_t *block_len,
