@@ -32,7 +32,7 @@ EXPORTS = ["hw_attn_decode_workspace_size", "hw_workspace_init", "hw_attn_decode
            "hw_attn_append_decode_planned", "hw_plan_export", "hw_attn_decode_noalloc",
            "hw_block_commit", "hw_block_commit_many", "hw_workspace_status", "hw_views_combined",
            "hw_views", "hw_views_chunked", "hw_last_cuda_error", "hw_status_string",
-           "hw_test_set_merge_wait_limit", "hw_noalloc_status"]
+           "hw_test_set_merge_wait_limit", "hw_noalloc_status", "hw_trace_read", "hw_trace_clear"]
 HW_LAYOUT_COMBINED, HW_LAYOUT_INTERLEAVED, HW_LAYOUT_CONTIGUOUS = 0, 1, 2
 LAYOUTS = {"combined": HW_LAYOUT_COMBINED, "interleaved": HW_LAYOUT_INTERLEAVED,
            "contiguous": HW_LAYOUT_CONTIGUOUS}
@@ -89,6 +89,8 @@ def lib(path: Optional[str] = None):
     L.hw_plan_export.argtypes = [ctypes.POINTER(AttnDesc), _P, ctypes.c_size_t, _P, ctypes.c_int32,
                                  ctypes.POINTER(ctypes.c_int32), _P]
     L.hw_attn_decode_noalloc.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 12
+    L.hw_trace_read.argtypes = [_P]
+    L.hw_trace_clear.argtypes = []
     L.hw_block_commit.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_double, _P, _P, ctypes.c_int64, ctypes.c_int32,
                                   ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32,
@@ -111,6 +113,14 @@ def lib(path: Optional[str] = None):
     if path is None:
         _lib = L
     return L
+
+
+def use_library(path: str):
+    """Make the library at `path` the process's (e.g. the HW_TRACE build);
+    before any other call."""
+    global _lib
+    _lib = lib(path)
+    return _lib
 
 
 def _ptr(x) -> Optional[int]:
@@ -373,3 +383,17 @@ def test_set_merge_wait_limit(cycles: int):
     """hw_test_set_merge_wait_limit: the merge's wait bound (SM cycles) for the
     calls that follow; 0 restores the default."""
     _check("hw_test_set_merge_wait_limit", lib().hw_test_set_merge_wait_limit(int(cycles)))
+
+
+TRACE_SHAPE = (8, 160, 24)  # calls (mod 8), CTAs, points: see hw_trace_read
+
+
+def trace_read() -> np.ndarray:
+    """hw_trace_read: the layer timeline of an HW_TRACE build (uint64 ns)."""
+    out = np.zeros(TRACE_SHAPE, np.uint64)
+    _check("hw_trace_read", lib().hw_trace_read(out.ctypes.data))
+    return out
+
+
+def trace_clear() -> None:
+    _check("hw_trace_clear", lib().hw_trace_clear())

@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libhogwild.so")
+# the layer-timeline build (HW_TRACE: globaltimer stamps, hw_trace_read)
+BUILD_TRACE = os.path.join(PKG, "_build_trace")
+LIB_TRACE = os.path.join(BUILD_TRACE, "libhogwild_trace.so")
 
 SOURCES = ["api.cpp", "attn_decode_simt.cu", "attn_decode_tc.cu", "block_commit.cu",
            "attn_decode_noalloc.cu"]
@@ -51,8 +54,13 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(p) > t for p in [src] + _deps())
 
 
-def build(verbose: bool = False, extra: tuple = ()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra: tuple = (), trace: bool = False) -> str:
+    """Compile libhogwild.so (trace=True: the HW_TRACE build, libhogwild_trace.so
+    in its own folder); returns the library's path."""
+    out_dir, lib_path = (BUILD_TRACE, LIB_TRACE) if trace else (BUILD, LIB)
+    if trace:
+        extra = tuple(extra) + ("-DHW_TRACE",)
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
     jobs = []
     objs = []
@@ -60,9 +68,9 @@ def build(verbose: bool = False, extra: tuple = ()) -> str:
         src = os.path.join(CSRC, s)
         if not os.path.exists(src):
             continue
-        obj = os.path.join(BUILD, s.rsplit(".", 1)[0] + ".o")
+        obj = os.path.join(out_dir, s.rsplit(".", 1)[0] + ".o")
         objs.append(obj)
-        if _stale(obj, src) or extra:
+        if _stale(obj, src) or (extra and not trace):
             cmd = [cc, "-c", src, "-o", obj] + _flags() + list(extra)
             if s.endswith(".cpp"):
                 cmd[1:1] = ["-x", "cu"]
@@ -80,11 +88,11 @@ def build(verbose: bool = False, extra: tuple = ()) -> str:
         for log in ex.map(run, jobs):
             if verbose and log.strip():
                 print(log)
-    if jobs or not os.path.exists(LIB):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if jobs or not os.path.exists(lib_path):
+        tmp = lib_path + f".tmp{os.getpid()}"
         run([cc, "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -243,6 +243,12 @@ static void fill_args(DecodeArgs &a, const hw_attn_desc *d, const WorkspaceLayou
   a.counters = reinterpret_cast<int32_t *>(ws + L.counters_off);
   a.partials = reinterpret_cast<float *>(ws + L.partials_off);
   a.early = (d->flags & HW_DESC_EARLY_LOADS) != 0;
+#ifdef HW_TRACE
+  {
+    static std::atomic<int32_t> calls{0};
+    a.trace_call = calls++;
+  }
+#endif
   a.wait_limit = g_merge_wait.load();
   a.n_rows = d->n_rows;
   a.n_q_heads = d->n_q_heads;

@@ -801,7 +801,10 @@ __device__ void query_prologue(const DecodeArgs &a, TcSmem &S, int64_t u0, int64
   if (t == 0) S.meta_nref = X.m.n_ref;
   fence_proxy_async_smem();
   sync();
-  if (t == 0) mbar_arrive(&S.q_full);  // phase 0: segment 0
+  if (t == 0) {
+    mbar_arrive(&S.q_full);  // phase 0: segment 0
+    HW_TRACE_AT(a, 3);
+  }
 }
 
 // The CTA's new tokens (hw_attn_append_decode_planned), by warps 6-7: for
@@ -917,6 +920,7 @@ __device__ void qprep(const DecodeArgs &a, TcSmem &S, int64_t u0, int64_t u1) {
     // warps keep the same control flow so the named barrier stays balanced.
     wait_or_abort(S, a, &S.rec_ready[done & 3], (done >> 2) & 1);
     if (wq == 0) arrive_segment(a, S.cp.pre[done % kPre].m, lane);
+    if (tq == 0) HW_TRACE_AT(a, 7);
   };
   int64_t u = S.cp.us[1];  // segment 1
   int64_t u_prep = S.cp.us[kPre - 1] < u1 ? next_segment(S.ps.plan, a.n_blocks, S.cp.us[kPre - 1]) : u1;  // segment kPre
@@ -1046,6 +1050,7 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(&S.rec_ready[seg & 3]);
+  if (threadIdx.x == kWarpSoft * 32) HW_TRACE_AT(a, 6);
 }
 
 // E4M3 V: row `row` of a stage's V codes (in the upper V box) widened to
@@ -1150,6 +1155,11 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       widen_v_row(smem_u32(stage_ptr<kFp8>(S, s)) + R::VOFF, row, tok_ok);
     }
     wait_or_abort(S, a, &S.s_full[sb], (i >> 1) & 1);
+    if (threadIdx.x == kWarpSoft * 32 && i == 0) HW_TRACE_AT(a, 4);
+    if (threadIdx.x == kWarpSoft * 32 && i == n - 1) {
+      HW_TRACE_AT(a, 5);
+      HW_TRACE_VAL(a, 21, n);
+    }
     tc_fence_after();
     __syncwarp();
     uint32_t r[32], r2[32];
@@ -1514,6 +1524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   TcSmem &S = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    HW_TRACE_AT(a, 0);
+    unsigned sm;
+    asm("mov.u32 %0, %%smid;" : "=r"(sm));
+    HW_TRACE_VAL(a, 22, sm);
+  }
   // Launched as a programmatic dependent of the previous kernel on the
   // stream: this CTA may start while that grid's last CTAs still run (an SM
   // holds one CTA of this kernel, so only SMs they left), and the next
@@ -1633,7 +1649,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       issued = producer<kFp8>(a, S, &tm_k, &tm_v, S.cp.u0, S.cp.u1, false, 0, n0);
     }
   }
+  if (tid == 0) HW_TRACE_AT(a, 1);
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid is complete
+  if (tid == 0) HW_TRACE_AT(a, 2);
   if (!early) {
     get_plan();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1674,12 +1692,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Only the merge CTAs (merge_ctas: the ones with the most units) take
   // items; every other CTA retires here, and the next launch's CTA can take
   // its SM.
+  if (tid == 0) HW_TRACE_AT(a, 8);
   if (ok)
     merge_phase<__nv_bfloat16, 128, 8>(a, S.ps.plan, S.ps.cache,
                                        *reinterpret_cast<MergeSmem<8> *>(S.stage[0]),
                                        &S.cp.mpre[0][0], S.cp.mpre_n, kPreItems, kPreList, tid,
                                        kThreads, CtaSync(), a.wait_limit, S.cp.mrank,
                                        merge_ctas(a, static_cast<int>(gridDim.x)));
+  if (tid == 0) HW_TRACE_AT(a, 12);
 }
 
 // The plan of the decode launches of `o.records` CTAs (see "plans" above):
@@ -1743,6 +1763,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory of one CTA per SM");
+
+}  // namespace hw
+
+extern "C" int hw_trace_read(uint64_t *dst) {
+#ifdef HW_TRACE
+  if (!dst) return HW_ERR_INVALID;
+  return cudaMemcpyFromSymbol(dst, hw::g_trace, sizeof(hw::g_trace)) == cudaSuccess ? HW_OK : HW_ERR_CUDA;
+#else
+  (void)dst;
+  return HW_ERR_UNSUPPORTED;
+#endif
+}
+
+extern "C" int hw_trace_clear(void) {
+#ifdef HW_TRACE
+  static unsigned long long zero[hw::kTraceCalls][hw::kTraceCtas][hw::kTracePoints];
+  return cudaMemcpyToSymbol(hw::g_trace, zero, sizeof(zero)) == cudaSuccess ? HW_OK : HW_ERR_CUDA;
+#else
+  return HW_ERR_UNSUPPORTED;
+#endif
+}
+
+namespace hw {
 size_t decode_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 size_t plan_shared_bytes() { return sizeof(PlanShared); }
 size_t plan_cta_bytes() { return sizeof(CtaPlan); }

@@ -33,10 +33,13 @@
 //   A CTA emits one partial record per (segment it touched, query head
 //   served) into slot seg + c, unique because seg and c never both stay put
 //   as units advance.  Every delivered record bumps the arrival counter of
-//   its (row, q head).  The launch is cooperative (all CTAs resident): after
-//   its own units, each CTA merges the (row, q head) items given to it - it
-//   waits, with a bound, until the item's counter shows every record, then
-//   combines them with the whole CTA.
+//   its (row, q head).  After its own units, a merging CTA merges the (row,
+//   q head) items given to it - it waits, with a bound, until the item's
+//   counter shows every record, then combines them with the whole CTA.  Every
+//   CTA a merge waits for is resident: the SIMT kernel's launch is
+//   cooperative; the tensor-core kernel's CTAs (one per SM, at most one grid
+//   of them waiting) hold their SMs from their start and wait for no one
+//   before their records are out.
 //
 // The view tables, positions and head map are read from global memory once,
 // in one round of independent loads, into a shared-memory cache (MetaCache);
@@ -57,6 +60,34 @@
 #include "hw_internal.h"
 
 namespace hw {
+
+// Layer timeline (a build with HW_TRACE only; otherwise the points compile to
+// nothing): the globaltimer at point k of CTA c of call n, kept for the last
+// kTraceCalls calls, read by hw_trace_read.  Points (tensor-core kernel):
+// 0 entry, 1 work before griddepcontrol.wait done, 2 wait returned, 3 first
+// queries ready, 4 first scores, 5 last scores, 6 last records stored,
+// 7 last arrivals, 8 merge phase entered, 10 first item's records all
+// there, 11 first item merged, 12 exit; values: 20 items merged, 21 tiles,
+// 22 SM id.
+constexpr int kTraceCalls = 8, kTraceCtas = 160, kTracePoints = 24;
+#ifdef HW_TRACE
+static __device__ unsigned long long g_trace[kTraceCalls][kTraceCtas][kTracePoints];
+__device__ __forceinline__ unsigned long long trace_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define HW_TRACE_VAL(a, k, v)                                                          \
+  do {                                                                                 \
+    if (blockIdx.x < kTraceCtas) g_trace[(a).trace_call % kTraceCalls][blockIdx.x][(k)] = (v); \
+  } while (0)
+#define HW_TRACE_AT(a, k) HW_TRACE_VAL(a, k, trace_now())
+#else
+#define HW_TRACE_VAL(a, k, v) \
+  do {                        \
+  } while (0)
+#define HW_TRACE_AT(a, k) HW_TRACE_VAL(a, k, 0)
+#endif
 
 // ---------------------------------------------------------------------------
 // small helpers
@@ -673,10 +704,12 @@ __device__ __forceinline__ int merge_list(const DecodeArgs &a, const PlanCore &P
   return off;
 }
 
-// The merge phase.  Every thread of every CTA of the (cooperative) grid calls
+// The merge phase.  Every thread of every CTA of the grid calls
 // it once its own units are done.  Work item = (row r, q head hq): all the
 // partial records of that output row, each from one (view entry, CTA) pair.
-// Items go round-robin over the CTAs, those without units first.  A CTA
+// A CTA of rank `rank` among the `grid` merging CTAs takes items rank, rank +
+// grid, ... (the SIMT kernel: every CTA, those without units first; the
+// tensor-core kernel: the merge_ctas CTAs with the most units).  A CTA
 // merges up to NL of its items side by side, its warps split evenly between
 // them.  The first warp of an item's group lists the item's records from the
 // plan (the k-th item of the CTA, k < n_pre, may come with its list
@@ -702,6 +735,7 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
   const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
   const int items = a.n_rows * a.n_q_heads;
   const int mine = rank >= 0 && rank < grid && rank < items ? (items - rank + grid - 1) / grid : 0;
+  if (tid == 0) HW_TRACE_VAL(a, 20, static_cast<unsigned long long>(mine));
 
   for (int k0 = 0; k0 < mine; k0 += NL) {
     const int np = min(mine - k0, NL);  // items merged side by side
@@ -739,6 +773,7 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
           if (!ok) flag_error(a.err, HW_DEV_TIMEOUT);
         }
         Z.n_rec[p] = n;
+        if (k == 0) HW_TRACE_AT(a, 10);
         Z.ok[p] = ok ? 1 : 0;
       }
     }
@@ -824,6 +859,7 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
           a.lse[ob] = any ? (Mx + __log2f(L)) * 0.69314718055994530942f : -INFINITY;
       }
       if (lane == 0) a.counters[it] = 0;  // re-armed for the next call
+      if (lane == 0 && k == 0) HW_TRACE_AT(a, 11);
     }
     sync();  // the scratch is rewritten by the next round
   }

@@ -47,6 +47,9 @@ struct DecodeArgs {
   // Bound of the merge's wait for an item's records, in SM clock cycles
   // (hw_test_set_merge_wait_limit; ~1 s by default).
   int64_t wait_limit;
+#ifdef HW_TRACE
+  int32_t trace_call;  // the call's index in the process (layer-timeline build)
+#endif
   int32_t n_rows, n_q_heads, n_kv_heads, head_dim, n_blocks, n_view;
   int64_t capacity;
   const uint8_t *plan;  // precomputed plan of the tensor-core kernel (hw_attn_plan), or null

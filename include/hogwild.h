@@ -491,6 +491,24 @@ int hw_views_chunked(int32_t layout, int32_t n_problems, int32_t n_workers, int3
  */
 int hw_test_set_merge_wait_limit(int64_t cycles);
 
+/*
+ * Layer timeline, for profiling (the pages have no counterpart).  A library
+ * built with HW_TRACE (concurrent_shared_kv_gb300/build.py, trace=True)
+ * stamps the GPU's global timer (ns) at fixed points of every tensor-core
+ * decode launch: for the last 8 decode calls of the process (call index mod
+ * 8), 160 CTAs and 24 points each - 0 entry, 1 work before the wait on the
+ * previous launch done, 2 that wait returned, 3 first queries ready,
+ * 4 first scores, 5 last scores, 6 last records stored, 7 last arrivals,
+ * 8 merge phase entered, 10 the first item's records all there, 11 first
+ * item merged, 12 exit; and the values 20 items merged, 21 tiles streamed,
+ * 22 SM id (0 where a point was not reached).  hw_trace_read copies the
+ * table into host memory dst (uint64 [8][160][24]; synchronous);
+ * hw_trace_clear zeroes it.  Without HW_TRACE both return
+ * HW_ERR_UNSUPPORTED and the kernels carry no stamps.
+ */
+int hw_trace_read(uint64_t *dst);
+int hw_trace_clear(void);
+
 /* Last CUDA error code seen by this thread's library calls (cudaError_t). */
 int hw_last_cuda_error(void);
 
