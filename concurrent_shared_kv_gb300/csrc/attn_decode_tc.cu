@@ -65,18 +65,25 @@ constexpr uint32_t kSCols = 2 * kN;           // S buffer: S_hi [0,32), S_lo [32
 constexpr uint32_t kTmemCols = 256;           // S0 [0,64)  S1 [64,128)  O0 [128,160)  O1 [160,192)
 constexpr uint32_t kColO = 2 * kSCols;        // segment k accumulates in O[k & 1]
 constexpr float kLazy = 8.f;                  // rescale only when the max grows by > 2^8
+// E4M3 caches: P goes to the tensor cores as E4M3 codes of 2^6 p with p <=
+// 2^2, so 2^6 p <= 256 stays below E4M3's largest value (448) while weights
+// down to 2^-12 of the running max stay normal numbers (>= 2^-6) with their
+// full precision; the factor leaves O and l exactly (a power of two).
+constexpr float kLazyF8 = 2.f;
+constexpr float kPScaleF8 = 64.f, kPUnscaleF8 = 1.f / 64.f;
 
 // E4M3 caches.  A stage holds the tile's K codes ([128 rows][128 codes],
-// 128-B swizzled; P takes their place once QK has completed), then its V as
-// f16 in the two boxes of the bf16 layout - the V codes land in the upper box
-// and the softmax warps widen them in place.  48 KB a stage, four in the ring
-// (the same 192 KB).  QK runs as kind::f8f6f4 on the codes against the
-// rotated queries split into four E4M3 parts (N = 128: S = S0 + S1/16 +
-// S2/256 + S3/4096, about 16 significant bits, like the bf16 path's hi + lo),
-// PV as kind::f16 on the widened V and an f16 P.  TMEM: S 2 x 128 columns,
-// O 2 x 32 (512 allocated).
+// 128-B swizzled; P takes their place once QK has completed), then its V
+// codes in the same layout: 32 KB a stage, four in the ring.  Both products
+// run as kind::f8f6f4 on the codes straight from TMA.  QK against the rotated
+// queries split into four E4M3 parts (N = 128: S = S0 + S1/16 + S2/256 +
+// S3/4096, about 16 significant bits, like the bf16 path's hi + lo).  PV with
+// V^T MN-major (one 128-B atom along d) against P split into two E4M3 parts,
+// the nearest code and the residual times 16, stacked on N (N = 64: O = O_hi
+// + O_lo/16, about 8 significant bits of P, like the bf16 path's bf16 P).
+// TMEM: S 2 x 128 columns, O 2 x 64 (512 allocated).
 constexpr uint32_t kF8Box = 128 * 128;
-constexpr uint32_t kF8StageBytes = kF8Box + 2 * kBox;
+constexpr uint32_t kF8StageBytes = 2 * kF8Box;
 constexpr int kMaxStages = 4;
 constexpr int kF8Parts = 4;
 template <bool kFp8>
@@ -85,11 +92,13 @@ struct Ring {
   static constexpr uint32_t SB = kFp8 ? kF8StageBytes : kStageBytes;     // bytes per stage
   static constexpr uint32_t SC = kFp8 ? kF8Parts * kN : kSCols;          // S columns per buffer
   static constexpr uint32_t CO = 2 * SC;                                 // first O column
-  static constexpr uint32_t VOFF = kFp8 ? kF8Box : 2 * kBox;             // V lo box in a stage
+  static constexpr uint32_t VOFF = kFp8 ? kF8Box : 2 * kBox;             // V (lo box) in a stage
+  static constexpr uint32_t OC = kFp8 ? 2 * kN : kN;                     // O columns per buffer
   static constexpr uint32_t TC = kFp8 ? 512 : kTmemCols;                 // TMEM columns
 };
 static_assert(Ring<true>::NS * Ring<true>::SB <= kStages * kStageBytes, "E4M3 ring");
-static_assert(Ring<true>::CO + 2 * kN <= Ring<true>::TC, "E4M3 TMEM columns");
+static_assert(Ring<true>::CO + 2 * Ring<true>::OC <= Ring<true>::TC, "E4M3 TMEM columns");
+static_assert(Ring<false>::CO + 2 * Ring<false>::OC <= Ring<false>::TC, "bf16 TMEM columns");
 static_assert(kF8Parts * kN * 128 <= kQBytes, "E4M3 query parts fit the Q~ buffer");
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft = 2, kWarpQ = 6;
@@ -343,10 +352,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&p);
 }
 
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  const __half2 p = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&p);
-}
 __device__ __forceinline__ float f16_lo(uint32_t w) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
 }
@@ -456,11 +461,11 @@ __device__ int producer(const DecodeArgs &a, TcSmem &S, const CUtensorMap *tk,
     // arrive below releases this store)
     S.tflags[s] = t.flags;
     if constexpr (kFp8) {
-      // K codes at the stage's start, V codes into the upper V box
+      // K codes at the stage's start, V codes after them
       mbar_arrive_expect_tx(&S.k_full[s], kF8Box);
       tma_load_3d(st, tk, &S.k_full[s], 0, t.row, t.h, pol);
       mbar_arrive_expect_tx(&S.v_full[s], kF8Box);
-      tma_load_3d(st + kF8Box + kBox, tv, &S.v_full[s], 0, t.row, t.h, pol);
+      tma_load_3d(st + Ring<kFp8>::VOFF, tv, &S.v_full[s], 0, t.row, t.h, pol);
       continue;
     }
     mbar_arrive_expect_tx(&S.k_full[s], 2 * kBox);
@@ -497,9 +502,9 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
   using R = Ring<kFp8>;
   constexpr int NS = R::NS;
   // QK: K tile, [Q~hi; Q~lo] (bf16) or the four E4M3 parts of Q~: K-major.
-  // PV: V tile, P: both MN-major, bf16 or f16.
+  // PV: V tile, P (bf16; E4M3: the codes and [P hi, P lo]): both MN-major.
   constexpr uint32_t idesc_qk = kFp8 ? idesc_e4m3(128, R::SC, 0, 0) : idesc_bf16(128, R::SC, 0, 0);
-  constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(128, kN, 1, 1) : idesc_bf16(128, kN, 1, 1);
+  constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3(128, R::OC, 1, 1) : idesc_bf16(128, kN, 1, 1);
   const int n = static_cast<int>(u1 - u0);
   const uint32_t stage0 = smem_u32(S.stage[0]), qbase = smem_u32(S.q);
   const uint64_t a_qk = smem_desc(stage0, 16, 1024, kSw128);    // + (stage, k-step) offset >> 4
@@ -539,14 +544,22 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
     if (first) ++seg_p;
     if (first && !spin_or_abort(S, a, &S.o_empty[seg_p & 1], ((seg_p >> 1) & 1) ^ 1)) return;
     tc_fence_after();
-    // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart,
-    // 8-token groups 1024 B apart.  P^T: MN-major, 32 heads = one 64-B atom,
+    // V^T: MN-major, d 0-63 and 64-127 in two 128-B swizzle atoms kBox apart
+    // (E4M3: all 128 d in one atom), 8-token groups 1024 B apart.  P^T:
+    // MN-major, 32 heads (E4M3: the 32 hi and 32 lo codes) = one 64-B atom,
     // 8-token groups 512 B apart, in the stage's K region.
     const uint64_t as = a_pv + ((s * R::SB) >> 4), bs = b_pv + ((s * R::SB) >> 4);
+    if constexpr (kFp8) {
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-      mma_bf16(tmem + R::CO + (seg_p & 1) * kN, as + ((kk * 2048) >> 4), bs + ((kk * 1024) >> 4),
+      for (int kk = 0; kk < 4; ++kk)  // 4 k-steps of 32 tokens
+        mma_f8(tmem + R::CO + (seg_p & 1) * R::OC, as + ((kk * 4096) >> 4), bs + ((kk * 2048) >> 4),
                idesc_pv, !(first && kk == 0));
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // 8 k-steps of 16 tokens
+        mma_bf16(tmem + R::CO + (seg_p & 1) * R::OC, as + ((kk * 2048) >> 4),
+                 bs + ((kk * 1024) >> 4), idesc_pv, !(first && kk == 0));
+    }
     mma_commit(&S.kv_empty[s]);
     mma_commit(&S.p_empty);
     if (flags & 2) mma_commit(&S.o_full[seg_p & 1]);
@@ -1019,17 +1032,30 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[kN], int lane) {
 // (m, l) of each query head -> partial records in the workspace.  Runs one
 // tile after the segment's end, when its last P.V product has (nearly always)
 // completed; the arrivals are left to the query warps.
-// (E4M3 caches: O times the v_scale of the segment's kv head.)
+// (E4M3 caches: O = O_hi + O_lo / 16, times the v_scale of the segment's kv
+// head.)
 template <bool kFp8>
 __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int seg, int64_t sid,
                                 int nq, int ws, int lane, int row, NamedSync<1, 128> sync,
                                 float vmul) {
+  using R = Ring<kFp8>;
   wait_or_abort(S, a, &S.o_full[seg & 1], (seg >> 1) & 1);
   tc_fence_after();
   __syncwarp();
   uint32_t o[32];
-  tmem_ld32(tl + Ring<kFp8>::CO + (seg & 1) * kN, o);
+  tmem_ld32(tl + R::CO + (seg & 1) * R::OC, o);
   tmem_wait_ld();
+  if constexpr (kFp8) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // O_lo, 16 columns at a time
+      uint32_t t[16];
+      tmem_ld16(tl + R::CO + (seg & 1) * R::OC + kN + 16 * h, t);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        o[16 * h + j] = __float_as_uint(__fmaf_rn(__uint_as_float(t[j]), 0.0625f, __uint_as_float(o[16 * h + j])));
+    }
+  }
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(&S.o_empty[seg & 1]);
@@ -1053,40 +1079,13 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
   if (threadIdx.x == kWarpSoft * 32) HW_TRACE_AT(a, 6);
 }
 
-// E4M3 V: row `row` of a stage's V codes (in the upper V box) widened to
-// f16 in the two V boxes, in place - the row's codes occupy exactly its row
-// of the upper box and are read whole before anything is written.  Rows past
-// the block end become zeros (their codes may be anything, NaN included).
-__device__ __forceinline__ void widen_v_row(uint32_t vbase, int row, bool keep) {
-  const uint32_t sw = row & 7;
-  const uint32_t src = vbase + kBox + row * 128;
-  uint4 in[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) in[c] = ld_shared_v4(src + ((c ^ sw) << 4));  // codes d 16c..16c+15
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t w[4] = {in[c].x, in[c].y, in[c].z, in[c].w};
-    uint32_t f[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      f[2 * k] = keep ? e4m3x2_to_f16x2(w[k]) : 0u;
-      f[2 * k + 1] = keep ? e4m3x2_to_f16x2(w[k] >> 16) : 0u;
-    }
-    // d 16c.. is f16 chunk 2c of the 128 d: box c / 4, chunks (2c) % 8 and (2c + 1) % 8
-    const uint32_t dst = vbase + (c >> 2) * kBox + row * 128;
-    const uint32_t g = (2 * c) & 7;
-    st_shared_v4(dst + ((g ^ sw) << 4), f[0], f[1], f[2], f[3]);
-    st_shared_v4(dst + (((g + 1) ^ sw) << 4), f[4], f[5], f[6], f[7]);
-  }
-}
-
 // kLimit: the plan carries view limits, so a column may attend only part of
-// a block.  kFp8: E4M3 caches (three S parts, the V codes widened here, P in
-// f16).
+// a block.  kFp8: E4M3 caches (four S parts; P as two E4M3 parts).
 template <bool kLimit, bool kFp8>
 __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_t u0,
                              int64_t u1) {
   using R = Ring<kFp8>;
+  constexpr float lazy = kFp8 ? kLazyF8 : kLazy;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ws = warp - kWarpSoft;              // 0..3
   const int qd = warp & 3;                      // TMEM lane quadrant of this warp
@@ -1124,7 +1123,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       nq = min(S.meta_nref * G, kN);
       if constexpr (kFp8) {
         qmul = S.q_mul;
-        vmul = S.v_mul[seg & 3];
+        vmul = S.v_mul[seg & 3] * kPUnscaleF8;  // (O is 2^6 times too large)
       }
       if constexpr (kLimit) {
         // the segment's metadata stays in its slot until its records are out
@@ -1148,12 +1147,6 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     const int base = x.t * kT;  // the tile's first token in its block
     const int valid = min(kT, S.ps.plan.len[x.b] - base);
     const bool tok_ok = row < valid;
-    if constexpr (kFp8) {
-      // this thread's row of the tile's V, widened (fenced for the tensor
-      // cores with P below)
-      wait_or_abort(S, a, &S.v_full[s], (i / R::NS) & 1);
-      widen_v_row(smem_u32(stage_ptr<kFp8>(S, s)) + R::VOFF, row, tok_ok);
-    }
     wait_or_abort(S, a, &S.s_full[sb], (i >> 1) & 1);
     if (threadIdx.x == kWarpSoft * 32 && i == 0) HW_TRACE_AT(a, 4);
     if (threadIdx.x == kWarpSoft * 32 && i == n - 1) {
@@ -1205,13 +1198,13 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     }
 
     // Lazy rescaling: the reference max m_run moves only when some score
-    // exceeds it by more than kLazy (log2 units), so p <= 2^kLazy and O is
+    // exceeds it by more than kLazy (log2 units; E4M3: kLazyF8), so p <= 2^kLazy and O is
     // rarely touched.  The common case needs only this one CTA-group vote;
     // exact column maxima are taken on the rare tiles that need them (the
     // first tile of a segment always does: m_run starts at -inf).
     bool exceed = false;
 #pragma unroll
-    for (int j = 0; j < kN; ++j) exceed |= (j < nq) && (sc[j] > m_run[j] + kLazy);
+    for (int j = 0; j < kN; ++j) exceed |= (j < nq) && (sc[j] > m_run[j] + lazy);
     if (bar_red_or_128(exceed)) {
       float(*red)[4] = S.red[i & 1];
       float v[kN];
@@ -1226,7 +1219,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       const float4 t4 = *reinterpret_cast<const float4 *>(red[lane]);
       const float tmax = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
       const float m_old = m_mine;
-      if (lane < nq && tmax > m_old + kLazy) m_mine = tmax;
+      if (lane < nq && tmax > m_old + lazy) m_mine = tmax;
       const float a_mine = (m_mine == m_old) ? 1.f : ex2(m_old - m_mine);
       float alpha[kN];
 #pragma unroll
@@ -1240,47 +1233,73 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
         wait_or_abort(S, a, &S.p_empty, (i - 1) & 1);
         tc_fence_after();
         __syncwarp();
-        uint32_t o[32];
-        tmem_ld32(tl + R::CO + (seg & 1) * kN, o);
-        tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
-        tmem_st32(tl + R::CO + (seg & 1) * kN, o);
-        tmem_wait_st();
+        for (int h = 0; h < (kFp8 ? 2 : 1); ++h) {  // (E4M3: O_hi, then O_lo)
+          uint32_t o[32];
+          tmem_ld32(tl + R::CO + (seg & 1) * R::OC + h * kN, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
+          tmem_st32(tl + R::CO + (seg & 1) * R::OC + h * kN, o);
+          tmem_wait_st();
+        }
         tc_fence_before();
       }
     }
-    uint32_t pk[kN / 2];
+    // P row of this token: 64 bytes (bf16: 32 heads; E4M3: the 32 hi codes,
+    // then the 32 lo codes) = four 16-B chunks.  The sum uses the same
+    // rounded weights the P.V product sees.
+    uint32_t pk[16];
+    if constexpr (kFp8) {
 #pragma unroll
-    for (int j = 0; j < kN; j += 2) {
-      const float p0 = (j < nq) ? ex2(sc[j] - m_run[j]) : 0.f;
-      const float p1 = (j + 1 < nq) ? ex2(sc[j + 1] - m_run[j + 1]) : 0.f;
-      // the sum uses the same rounded weights the P.V product sees
-      if constexpr (kFp8) {
-        pk[j / 2] = pack_f16(p0, p1);
-        l_part[j] += f16_lo(pk[j / 2]);
-        l_part[j + 1] += f16_hi(pk[j / 2]);
-      } else {
+      for (int k = 0; k < 16; ++k) pk[k] = 0;
+#pragma unroll
+      for (int j = 0; j < kN; j += 2) {
+        const float p0 = (j < nq) ? ex2(sc[j] - m_run[j]) : 0.f;
+        const float p1 = (j + 1 < nq) ? ex2(sc[j + 1] - m_run[j + 1]) : 0.f;
+        // 2^6 p (see kPScaleF8, <= 256 < 448) as hi + lo / 16: hi its
+        // nearest code, lo that of the residual times 16 (E4M3's grid,
+        // subnormals included: about 8 significant bits in all, like the
+        // bf16 path's P).  l sums the values of the codes the product sees.
+        // (The conversion instructions: splitting with floating-point
+        // arithmetic instead - Veltkamp's split - took ~40 % more per tile.)
+        const float s0 = p0 * kPScaleF8, s1 = p1 * kPScaleF8;
+        const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(s0, s1), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hf = e4m3x2_to_f16x2(h);
+        const float h0 = f16_lo(hf), h1 = f16_hi(hf);
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2((s0 - h0) * 16.f, (s1 - h1) * 16.f), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t lf = e4m3x2_to_f16x2(lo);
+        l_part[j] += __fmaf_rn(f16_lo(lf), 0.0625f, h0);
+        l_part[j + 1] += __fmaf_rn(f16_hi(lf), 0.0625f, h1);
+        pk[j >> 2] |= static_cast<uint32_t>(h) << (16 * ((j >> 1) & 1));
+        pk[8 + (j >> 2)] |= static_cast<uint32_t>(lo) << (16 * ((j >> 1) & 1));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kN; j += 2) {
+        const float p0 = (j < nq) ? ex2(sc[j] - m_run[j]) : 0.f;
+        const float p1 = (j + 1 < nq) ? ex2(sc[j + 1] - m_run[j + 1]) : 0.f;
         pk[j / 2] = pack_bf16(p0, p1);
         l_part[j] += __uint_as_float(pk[j / 2] << 16);
         l_part[j + 1] += __uint_as_float(pk[j / 2] & 0xffff0000u);
       }
     }
-    if (!kFp8 && valid < kT) {
+    if (valid < kT) {
       // V rows past the block end may hold anything: zero them (p = 0 there,
       // but 0 * NaN would still poison the sum)
       wait_or_abort(S, a, &S.v_full[s], (i / R::NS) & 1);
       if (!tok_ok) {
-        const uint32_t v0 = smem_u32(S.stage[s]) + 2 * kBox + row * 128;
+        const uint32_t v0 = smem_u32(stage_ptr<kFp8>(S, s)) + R::VOFF + row * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           st_shared_v4(v0 + c * 16, 0, 0, 0, 0);
-          st_shared_v4(v0 + kBox + c * 16, 0, 0, 0, 0);
+          if (!kFp8) st_shared_v4(v0 + kBox + c * 16, 0, 0, 0, 0);
         }
       }
     }
-    // P row of this token: 32 heads = four 16-B chunks, 64-B swizzle, in the
-    // K region of the tile's stage (QK of this tile has completed: s_full)
+    // in the K region of the tile's stage (QK of this tile has completed:
+    // s_full), 64-B swizzle
     const uint32_t prow = smem_u32(stage_ptr<kFp8>(S, s)) + row * 64;
     const uint32_t swz = (row >> 1) & 3;
 #pragma unroll
@@ -1299,7 +1318,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       // hand over (m, l) of every query head; the records follow one tile later
       float v[kN];
 #pragma unroll
-      for (int j = 0; j < kN; ++j) v[j] = l_part[j];
+      for (int j = 0; j < kN; ++j) v[j] = kFp8 ? l_part[j] * kPUnscaleF8 : l_part[j];
       transpose_reduce<false>(v, lane);
       S.lsave[seg & 1][ws][lane] = v[0];
       if (ws == 0) S.msave[seg & 1][lane] = m_mine;
