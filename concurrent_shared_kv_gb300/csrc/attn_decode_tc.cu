@@ -359,6 +359,19 @@ __device__ __forceinline__ float f16_hi(uint32_t w) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 
+// Elements j, j + 1 of a register array as one float pair, and back: the
+// paired fp32 instructions of sm_100 (__ffma2_rn and the like: two
+// correctly rounded operations in one) then halve the softmax's arithmetic
+// instructions with results identical to the scalar ones.
+__device__ __forceinline__ float2 pair_at(const uint32_t (&r)[32], int j) {
+  return make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+}
+__device__ __forceinline__ void pair_put(uint32_t (&r)[32], int j, float2 v) {
+  r[j] = __float_as_uint(v.x);
+  r[j + 1] = __float_as_uint(v.y);
+}
+__device__ __forceinline__ float2 fpair(float a) { return make_float2(a, a); }
+
 // Two E4M3 codes (low byte first) as f16x2, exactly.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
@@ -1161,13 +1174,13 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     tmem_wait_ld();
     if constexpr (kFp8) {
 #pragma unroll
-      for (int j = 0; j < kN; ++j)
-        r[j] = __float_as_uint(__fmaf_rn(__uint_as_float(r2[j]), 0.0625f, __uint_as_float(r[j])));
+      for (int j = 0; j < kN; j += 2)
+        pair_put(r, j, __ffma2_rn(pair_at(r2, j), fpair(0.0625f), pair_at(r, j)));
       tmem_ld32(tl + sb * R::SC + 2 * kN, r2);  // part 2
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < kN; ++j)
-        r[j] = __float_as_uint(__fmaf_rn(__uint_as_float(r2[j]), 0.00390625f, __uint_as_float(r[j])));
+      for (int j = 0; j < kN; j += 2)
+        pair_put(r, j, __ffma2_rn(pair_at(r2, j), fpair(0.00390625f), pair_at(r, j)));
       tmem_ld32(tl + sb * R::SC + 3 * kN, r2);  // part 3
       tmem_wait_ld();
     }
@@ -1176,17 +1189,22 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     if (lane == 0) mbar_arrive(&S.s_empty[sb]);
     if constexpr (kFp8) {
 #pragma unroll
-      for (int j = 0; j < kN; ++j)
-        r[j] = __float_as_uint(__fmaf_rn(__uint_as_float(r2[j]), 0.000244140625f, __uint_as_float(r[j])) * qmul);
+      for (int j = 0; j < kN; j += 2)
+        pair_put(r, j, __fmul2_rn(__ffma2_rn(pair_at(r2, j), fpair(0.000244140625f), pair_at(r, j)),
+                                  fpair(qmul)));
     } else {
 #pragma unroll
-      for (int j = 0; j < kN; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+      for (int j = 0; j < kN; j += 2) pair_put(r, j, __fadd2_rn(pair_at(r, j), pair_at(r2, j)));
     }
 
     float sc[kN];
     if (!kLimit || base + kT <= minlim) {
 #pragma unroll
-      for (int j = 0; j < kN; ++j) sc[j] = tok_ok ? __uint_as_float(r[j]) : -INFINITY;
+      for (int j = 0; j < kN; ++j) sc[j] = __uint_as_float(r[j]);
+      if (!tok_ok) {  // (a row past the block end: a ragged tile only)
+#pragma unroll
+        for (int j = 0; j < kN; ++j) sc[j] = -INFINITY;
+      }
     } else {
       // some column's view limit ends in this tile (a chunk's own tokens);
       // limits never exceed the block, so they cover valid too
@@ -1255,34 +1273,41 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       for (int k = 0; k < 16; ++k) pk[k] = 0;
 #pragma unroll
       for (int j = 0; j < kN; j += 2) {
-        const float p0 = (j < nq) ? ex2(sc[j] - m_run[j]) : 0.f;
-        const float p1 = (j + 1 < nq) ? ex2(sc[j + 1] - m_run[j + 1]) : 0.f;
+        const float2 d = __fadd2_rn(make_float2(sc[j], sc[j + 1]), make_float2(-m_run[j], -m_run[j + 1]));
+        const float p0 = (j < nq) ? ex2(d.x) : 0.f;
+        const float p1 = (j + 1 < nq) ? ex2(d.y) : 0.f;
         // 2^6 p (see kPScaleF8, <= 256 < 448) as hi + lo / 16: hi its
         // nearest code, lo that of the residual times 16 (E4M3's grid,
         // subnormals included: about 8 significant bits in all, like the
         // bf16 path's P).  l sums the values of the codes the product sees.
         // (The conversion instructions: splitting with floating-point
         // arithmetic instead - Veltkamp's split - took ~40 % more per tile.)
-        const float s0 = p0 * kPScaleF8, s1 = p1 * kPScaleF8;
-        const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(s0, s1), __NV_SATFINITE, __NV_E4M3);
+        const float2 sv = __fmul2_rn(make_float2(p0, p1), fpair(kPScaleF8));
+        const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(sv, __NV_SATFINITE, __NV_E4M3);
         const uint32_t hf = e4m3x2_to_f16x2(h);
-        const float h0 = f16_lo(hf), h1 = f16_hi(hf);
+        const float2 hv = make_float2(f16_lo(hf), f16_hi(hf));
         const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-            make_float2((s0 - h0) * 16.f, (s1 - h1) * 16.f), __NV_SATFINITE, __NV_E4M3);
+            __fmul2_rn(__fadd2_rn(sv, make_float2(-hv.x, -hv.y)), fpair(16.f)), __NV_SATFINITE, __NV_E4M3);
         const uint32_t lf = e4m3x2_to_f16x2(lo);
-        l_part[j] += __fmaf_rn(f16_lo(lf), 0.0625f, h0);
-        l_part[j + 1] += __fmaf_rn(f16_hi(lf), 0.0625f, h1);
+        const float2 lsum = __fadd2_rn(make_float2(l_part[j], l_part[j + 1]),
+                                       __ffma2_rn(make_float2(f16_lo(lf), f16_hi(lf)), fpair(0.0625f), hv));
+        l_part[j] = lsum.x;
+        l_part[j + 1] = lsum.y;
         pk[j >> 2] |= static_cast<uint32_t>(h) << (16 * ((j >> 1) & 1));
         pk[8 + (j >> 2)] |= static_cast<uint32_t>(lo) << (16 * ((j >> 1) & 1));
       }
     } else {
 #pragma unroll
       for (int j = 0; j < kN; j += 2) {
-        const float p0 = (j < nq) ? ex2(sc[j] - m_run[j]) : 0.f;
-        const float p1 = (j + 1 < nq) ? ex2(sc[j + 1] - m_run[j + 1]) : 0.f;
+        const float2 d = __fadd2_rn(make_float2(sc[j], sc[j + 1]), make_float2(-m_run[j], -m_run[j + 1]));
+        const float p0 = (j < nq) ? ex2(d.x) : 0.f;
+        const float p1 = (j + 1 < nq) ? ex2(d.y) : 0.f;
         pk[j / 2] = pack_bf16(p0, p1);
-        l_part[j] += __uint_as_float(pk[j / 2] << 16);
-        l_part[j + 1] += __uint_as_float(pk[j / 2] & 0xffff0000u);
+        const float2 lsum = __fadd2_rn(make_float2(l_part[j], l_part[j + 1]),
+                                       make_float2(__uint_as_float(pk[j / 2] << 16),
+                                                   __uint_as_float(pk[j / 2] & 0xffff0000u)));
+        l_part[j] = lsum.x;
+        l_part[j + 1] = lsum.y;
       }
     }
     if (valid < kT) {
