@@ -2,9 +2,9 @@
 // Ring<true>) caches with head_dim 128 on the sm_100 tensor cores (tcgen05 +
 // TMEM), K/V tiles staged by TMA.
 //
-// The path is HBM-bound: every K/V tile is read once and serves every query
-// head that attends it (all workers' view references to the block times the
-// GQA group, up to 32).  At 16-20 flop per KV byte the CUDA cores would be
+// The path is HBM-bound: every K/V tile is read once per column group and
+// serves every query head of the group that attends it (view references to
+// the block times the GQA group, up to 32 a group; hw_device.cuh).  At 16-20 flop per KV byte the CUDA cores would be
 // the ceiling, so the two small products run on the tensor cores:
 //   S^T [128 tokens x 64]      = K_tile [128 x 128] . [Q~hi; Q~lo]^T   (TMEM, fp32)
 //   O^T [128 d x 32 heads]     += V_tile^T [128 x 128 tokens] . P^T
@@ -17,7 +17,8 @@
 //   warp 1     MMA issuer (one thread) and TMEM owner
 //   warps 2-5  softmax: S from TMEM, running max / sum, P (bf16) into smem;
 //              segment epilogue: O from TMEM -> partial records
-// then all eight warps take part in the grid-wide merge phase (hw_device.cuh).
+// then all eight warps of the CTAs that merge (the ones with the most units)
+// take part in the merge phase (hw_device.cuh).
 //   warps 6-7  rotated queries of the next segment: fp32, scale folded in,
 //              split into bf16 hi + lo parts so that S keeps ~16 mantissa bits.
 // QK multiplies the K tile with hi and lo stacked as one 64-column operand:
@@ -27,9 +28,12 @@
 // and independent accumulators do not shorten it - so fewer, wider products
 // pay.)
 //
-// Variants (template parameters of decode_tc_kernel): a plan loaded or built
-// in-kernel; the step's new tokens written first (appends); per-view-entry
-// token limits (query chunks); E4M3 caches with per-kv-head scales.
+// Variants (template parameters of decode_tc_kernel): the step's new tokens
+// written first (appends); per-view-entry token limits (query chunks); E4M3
+// caches with per-kv-head scales; hw_attn_decode's plan cache (the plan of the
+// metadata the last call saw, rebuilt in the kernel when the metadata
+// differs) in place of hw_attn_plan's plan.  Consecutive launches overlap
+// (programmatic dependent launch, see the kernel's entry).
 #include <cuda.h>
 
 #include <cuda_fp8.h>

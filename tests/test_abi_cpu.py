@@ -156,3 +156,11 @@ def test_early_loads_flag_is_accepted_and_unknown_flags_are_not(L):
     assert call_decode(desc(dtype=api.HW_BF16, head_dim=128, flags=api.HW_DESC_EARLY_LOADS)) == -3
     assert call_decode(desc(flags=api.HW_DESC_EARLY_LOADS)) == -3
     assert call_decode(desc(flags=64)) == -1
+
+
+def test_trace_calls_are_absent_from_the_normal_build(L):
+    # the layer timeline needs the HW_TRACE build; the normal library carries
+    # no stamps and says so before touching the device
+    dst = np.zeros((8, 160, 24), np.uint64)
+    assert L.hw_trace_read(dst.ctypes.data) == -2   # HW_ERR_UNSUPPORTED
+    assert L.hw_trace_clear() == -2
