@@ -85,7 +85,10 @@ constexpr float kPScaleF8 = 64.f, kPUnscaleF8 = 1.f / 64.f;
 // V^T MN-major (one 128-B atom along d) against P split into two E4M3 parts,
 // the nearest code and the residual times 16, stacked on N (N = 64: O = O_hi
 // + O_lo/16, about 8 significant bits of P, like the bf16 path's bf16 P).
-// TMEM: S 2 x 128 columns, O 2 x 64 (512 allocated).
+// The sums l of the P columns come from the tensor cores too: the same P
+// against a constant tile of E4M3 ones (in the ring's unused fifth 32 KB),
+// so each of the 128 result rows holds every column's sum.  TMEM: S 2 x 128
+// columns, O 2 x 64, L 2 x 64 (512 allocated).
 constexpr uint32_t kF8Box = 128 * 128;
 constexpr uint32_t kF8StageBytes = 2 * kF8Box;
 constexpr int kMaxStages = 4;
@@ -98,8 +101,13 @@ struct Ring {
   static constexpr uint32_t CO = 2 * SC;                                 // first O column
   static constexpr uint32_t VOFF = kFp8 ? kF8Box : 2 * kBox;             // V (lo box) in a stage
   static constexpr uint32_t OC = kFp8 ? 2 * kN : kN;                     // O columns per buffer
+  static constexpr uint32_t LC = CO + 2 * OC;                            // E4M3: first L column
   static constexpr uint32_t TC = kFp8 ? 512 : kTmemCols;                 // TMEM columns
 };
+// E4M3: the ones tile's offset in the ring ([128 rows][128 ones], 16 KB)
+constexpr uint32_t kOnesOff = Ring<true>::NS * Ring<true>::SB;
+static_assert(kOnesOff + kF8Box <= kStages * kStageBytes, "E4M3 ones tile fits the ring");
+static_assert(Ring<true>::LC + 2 * Ring<true>::OC <= Ring<true>::TC, "E4M3 L columns");
 static_assert(Ring<true>::NS * Ring<true>::SB <= kStages * kStageBytes, "E4M3 ring");
 static_assert(Ring<true>::CO + 2 * Ring<true>::OC <= Ring<true>::TC, "E4M3 TMEM columns");
 static_assert(Ring<false>::CO + 2 * Ring<false>::OC <= Ring<false>::TC, "bf16 TMEM columns");
@@ -376,6 +384,20 @@ __device__ __forceinline__ void pair_put(uint32_t (&r)[32], int j, float2 v) {
 }
 __device__ __forceinline__ float2 fpair(float a) { return make_float2(a, a); }
 
+// The E4M3 codes (low byte first) of 16 (s - h) for the pair s, where h is
+// the f16x2 value of s's codes: s goes to f16 (11 bits), the residual is
+// exact there, and its codes are the nearest (saturating).
+__device__ __forceinline__ uint16_t e4m3x2_residual(float2 s, uint32_t h) {
+  uint32_t sh, rh;
+  uint16_t lo;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(sh) : "f"(s.y), "f"(s.x));  // (s.x in the low half)
+  asm("{\n\t.reg .b32 t;\n\tsub.rn.f16x2 t, %1, %2;\n\tmul.rn.f16x2 %0, t, %3;\n\t}"
+      : "=r"(rh)
+      : "r"(sh), "r"(h), "r"(0x4C004C00u));  // 16.0 in both halves
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lo) : "r"(rh));
+  return lo;
+}
+
 // Two E4M3 codes (low byte first) as f16x2, exactly.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
@@ -527,6 +549,7 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
   const uint64_t a_qk = smem_desc(stage0, 16, 1024, kSw128);    // + (stage, k-step) offset >> 4
   const uint64_t b_qk = smem_desc(qbase, 16, 1024, kSw128);
   const uint64_t a_pv = smem_desc(stage0 + R::VOFF, kBox, 1024, kSw128);
+  const uint64_t a_ones = smem_desc(stage0 + kOnesOff, kBox, 1024, kSw128);  // (E4M3)
   const uint64_t b_pv = smem_desc(stage0, 512, 512, kSw64);
   int seg_q = -1, seg_p = -1;
   auto qk = [&](int i) {
@@ -571,6 +594,11 @@ __device__ void mma_issuer(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int64_
       for (int kk = 0; kk < 4; ++kk)  // 4 k-steps of 32 tokens
         mma_f8(tmem + R::CO + (seg_p & 1) * R::OC, as + ((kk * 4096) >> 4), bs + ((kk * 2048) >> 4),
                idesc_pv, !(first && kk == 0));
+      // the column sums of P: ones^T . P^T (the ones tile in V's layout)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f8(tmem + R::LC + (seg_p & 1) * R::OC, a_ones + ((kk * 4096) >> 4),
+               bs + ((kk * 2048) >> 4), idesc_pv, !(first && kk == 0));
     } else {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)  // 8 k-steps of 16 tokens
@@ -1073,6 +1101,25 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
         o[16 * h + j] = __float_as_uint(__fmaf_rn(__uint_as_float(t[j]), 0.0625f, __uint_as_float(o[16 * h + j])));
     }
   }
+  // E4M3: l of column `lane` from the L buffer (every TMEM row holds every
+  // column's sum), L_hi + L_lo / 16, without the 2^6 of P
+  // (lane 0's row, through lsave, which E4M3 does not use otherwise)
+  float l_col = 0.f;
+  if (kFp8 && ws == 0) {
+    float(*ls)[kN] = S.lsave[seg & 1];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // L_hi 0-15, 16-31, L_lo 0-15, 16-31
+      uint32_t t[16];
+      tmem_ld16(tl + R::LC + (seg & 1) * R::OC + (q >> 1) * kN + 16 * (q & 1), t);
+      tmem_wait_ld();
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) ls[q >> 1][16 * (q & 1) + c] = __uint_as_float(t[c]);
+      }
+    }
+    __syncwarp();
+    l_col = __fmaf_rn(ls[1][lane], 0.0625f, ls[0][lane]) * kPUnscaleF8;
+  }
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(&S.o_empty[seg & 1]);
@@ -1089,7 +1136,7 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
     float *rec = record_ptr(a, slot, lane);
     const float(*ls)[kN] = S.lsave[seg & 1];
     rec[128] = S.msave[seg & 1][lane];
-    rec[129] = ls[0][lane] + ls[1][lane] + ls[2][lane] + ls[3][lane];
+    rec[129] = kFp8 ? l_col : ls[0][lane] + ls[1][lane] + ls[2][lane] + ls[3][lane];
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(&S.rec_ready[seg & 3]);
@@ -1248,7 +1295,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
       for (int j = 0; j < kN; ++j) {
         m_run[j] = __shfl_sync(0xffffffffu, m_mine, j);
         alpha[j] = __shfl_sync(0xffffffffu, a_mine, j);
-        l_part[j] *= alpha[j];
+        if (!kFp8) l_part[j] *= alpha[j];
       }
       if (!first) {
         // O must hold every earlier tile before it is rescaled
@@ -1256,13 +1303,14 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
         tc_fence_after();
         __syncwarp();
 #pragma unroll
-        for (int h = 0; h < (kFp8 ? 2 : 1); ++h) {  // (E4M3: O_hi, then O_lo)
+        for (int h = 0; h < (kFp8 ? 4 : 1); ++h) {  // (E4M3: O_hi, O_lo, L_hi, L_lo)
+          const uint32_t col = (h < 2 ? R::CO : R::LC) + (seg & 1) * R::OC + (h & 1) * kN;
           uint32_t o[32];
-          tmem_ld32(tl + R::CO + (seg & 1) * R::OC + h * kN, o);
+          tmem_ld32(tl + col, o);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
-          tmem_st32(tl + R::CO + (seg & 1) * R::OC + h * kN, o);
+          tmem_st32(tl + col, o);
           tmem_wait_st();
         }
         tc_fence_before();
@@ -1281,22 +1329,15 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
         const float p0 = (j < nq) ? ex2(d.x) : 0.f;
         const float p1 = (j + 1 < nq) ? ex2(d.y) : 0.f;
         // 2^6 p (see kPScaleF8, <= 256 < 448) as hi + lo / 16: hi its
-        // nearest code, lo that of the residual times 16 (E4M3's grid,
-        // subnormals included: about 8 significant bits in all, like the
-        // bf16 path's P).  l sums the values of the codes the product sees.
-        // (The conversion instructions: splitting with floating-point
-        // arithmetic instead - Veltkamp's split - took ~40 % more per tile.)
+        // nearest code, lo that of the residual of its f16 value times 16
+        // (E4M3's grid, subnormals included: about 8 significant bits in all,
+        // like the bf16 path's P).  l is the tensor cores' sum of these very
+        // codes (the ones product).  (The conversion instructions: splitting
+        // with fp32 arithmetic instead - Veltkamp's split - took ~40 % more
+        // per tile.)
         const float2 sv = __fmul2_rn(make_float2(p0, p1), fpair(kPScaleF8));
         const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(sv, __NV_SATFINITE, __NV_E4M3);
-        const uint32_t hf = e4m3x2_to_f16x2(h);
-        const float2 hv = make_float2(f16_lo(hf), f16_hi(hf));
-        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-            __fmul2_rn(__fadd2_rn(sv, make_float2(-hv.x, -hv.y)), fpair(16.f)), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t lf = e4m3x2_to_f16x2(lo);
-        const float2 lsum = __fadd2_rn(make_float2(l_part[j], l_part[j + 1]),
-                                       __ffma2_rn(make_float2(f16_lo(lf), f16_hi(lf)), fpair(0.0625f), hv));
-        l_part[j] = lsum.x;
-        l_part[j + 1] = lsum.y;
+        const uint16_t lo = e4m3x2_residual(sv, e4m3x2_to_f16x2(h));
         pk[j >> 2] |= static_cast<uint32_t>(h) << (16 * ((j >> 1) & 1));
         pk[8 + (j >> 2)] |= static_cast<uint32_t>(lo) << (16 * ((j >> 1) & 1));
       }
@@ -1345,11 +1386,13 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     }
     if (last) {
       // hand over (m, l) of every query head; the records follow one tile later
-      float v[kN];
+      if constexpr (!kFp8) {  // (E4M3: l comes from TMEM with the records)
+        float v[kN];
 #pragma unroll
-      for (int j = 0; j < kN; ++j) v[j] = kFp8 ? l_part[j] * kPUnscaleF8 : l_part[j];
-      transpose_reduce<false>(v, lane);
-      S.lsave[seg & 1][ws][lane] = v[0];
+        for (int j = 0; j < kN; ++j) v[j] = l_part[j];
+        transpose_reduce<false>(v, lane);
+        S.lsave[seg & 1][ws][lane] = v[0];
+      }
       if (ws == 0) S.msave[seg & 1][lane] = m_mine;
       pend = seg;
       pend_sid = seg_id(S.ps.plan, x.b, x.g, x.h);
@@ -1651,6 +1694,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if constexpr (kFp8) {
+    // the ones tile of the l product (E4M3 1.0 = 0x38 in every byte, so its
+    // swizzle is moot), seen by the tensor cores after the barrier below
+    uint4 *ones = reinterpret_cast<uint4 *>(S.stage[0] + kOnesOff);
+    for (int i = tid; i < static_cast<int>(kF8Box / 16); i += kThreads)
+      ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+    fence_proxy_async_smem();
+  }
   // The plan: the shared part and this CTA's record, into shared memory -
   // hw_attn_plan's with two bulk copies, or the plan cache's (see "plan
   // cache") with loads through L2, or built here when the cache holds
