@@ -616,6 +616,33 @@ __device__ __forceinline__ void arrive_segment(const DecodeArgs &a, const SegMet
   }
 }
 
+// EPL consecutive output elements of a lane: one vector store where the row
+// is aligned for it (the output rows start at multiples of D elements, so
+// this depends only on the caller's base pointer), else one store each.
+template <typename T, int EPL>
+__device__ __forceinline__ void store_row_part(T *dst, const T (&v)[EPL]) {
+  constexpr int kBytes = EPL * static_cast<int>(sizeof(T));
+  static_assert(kBytes == 4 || kBytes == 8 || kBytes == 16, "vector width");
+  if ((reinterpret_cast<uintptr_t>(dst) & (kBytes - 1)) == 0) {
+    if constexpr (kBytes == 16) {
+      uint4 w;
+      memcpy(&w, v, 16);
+      *reinterpret_cast<uint4 *>(dst) = w;
+    } else if constexpr (kBytes == 8) {
+      uint2 w;
+      memcpy(&w, v, 8);
+      *reinterpret_cast<uint2 *>(dst) = w;
+    } else {
+      uint32_t w;
+      memcpy(&w, v, 4);
+      *reinterpret_cast<uint32_t *>(dst) = w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) dst[e] = v[e];
+  }
+}
+
 // (m, l) of two partial softmaxes in the log2 domain, combined.
 __device__ __forceinline__ void lse_combine(float &M, float &L, float m, float l) {
   if (m == -INFINITY) return;  // nothing to add (and -inf - -inf would be NaN)
@@ -797,8 +824,9 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
           for (int e = 0; e < EPL; ++e) x[b][e] = 0.f;
           if (kk < n_rec) {
             const float *rec = a.partials + static_cast<int64_t>(list[kk]) * RS;
-            m[b] = __ldcg(rec + D);
-            l[b] = __ldcg(rec + D + 1);
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(rec + D));
+            m[b] = ml.x;
+            l[b] = ml.y;
             if constexpr (EPL == 4) {
               const float4 v = __ldcg(reinterpret_cast<const float4 *>(rec + lane * EPL));
               x[b][0] = v.x; x[b][1] = v.y; x[b][2] = v.z; x[b][3] = v.w;
@@ -853,8 +881,10 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
         }
         // L = 0: view limits left the row no token (its partials are empty)
         const bool any = L > 0.f;
+        T ov[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) orow[e] = from_f32<T>(any ? sum[e] / L : 0.f);
+        for (int e = 0; e < EPL; ++e) ov[e] = from_f32<T>(any ? sum[e] / L : 0.f);
+        store_row_part(orow, ov);
         if (lane == 0 && a.lse)
           a.lse[ob] = any ? (Mx + __log2f(L)) * 0.69314718055994530942f : -INFINITY;
       }
