@@ -205,6 +205,13 @@ __device__ __forceinline__ const uint8_t *plan_cta_record(const uint8_t *plan, i
   return plan + kPlanHeaderBytes + sizeof(PlanShared) + static_cast<size_t>(c) * sizeof(CtaPlan);
 }
 
+// The launch's RoPE table (MetaCache::phase, the first field of the shared
+// part's metadata) is written into shared memory at the kernel's entry: the
+// plan copies skip those bytes.
+constexpr uint32_t kPhaseOff = offsetof(PlanShared, cache) + offsetof(MetaCache, phase);
+constexpr uint32_t kPhaseBytes = sizeof(MetaCache::phase);
+static_assert(kPhaseOff % 16 == 0 && kPhaseBytes % 16 == 0, "the phase table is a whole number of 16-B chunks");
+
 // Does a plan header describe a launch of `grid` CTAs with these arguments?
 __device__ __forceinline__ bool header_matches(const DecodeArgs &a, const PlanHeader &h, int grid) {
   return h.magic == kPlanMagic && h.grid == grid && h.n_rows == a.n_rows &&
@@ -212,9 +219,21 @@ __device__ __forceinline__ bool header_matches(const DecodeArgs &a, const PlanHe
          h.n_blocks == a.n_blocks && h.n_view == a.n_view && h.capacity == a.capacity &&
          (h.limited != 0) == (a.view_limit != nullptr);
 }
-// Does the plan in global memory describe this launch?
-__device__ __forceinline__ bool plan_matches(const DecodeArgs &a, const uint8_t *plan) {
-  return header_matches(a, *reinterpret_cast<const PlanHeader *>(plan), static_cast<int>(gridDim.x));
+
+// hw_attn_plan's plan into shared memory with bulk copies completing on
+// plan_bar: the header (into the query buffer, idle until the queries are
+// rotated; checked once it lands), the shared part around the RoPE table,
+// and this CTA's record.
+__device__ __forceinline__ void issue_plan_copies(const DecodeArgs &a, TcSmem &S) {
+  constexpr uint32_t kHdr = (sizeof(PlanHeader) + 15) & ~15u;
+  constexpr uint32_t kTail = sizeof(PlanShared) - kPhaseOff - kPhaseBytes;
+  const uint8_t *src = a.plan + kPlanHeaderBytes;
+  uint8_t *dst = reinterpret_cast<uint8_t *>(&S.ps);
+  mbar_arrive_expect_tx(&S.plan_bar, kHdr + kPhaseOff + kTail + sizeof(CtaPlan));
+  bulk_g2s(S.q, a.plan, kHdr, &S.plan_bar);
+  bulk_g2s(dst, src, kPhaseOff, &S.plan_bar);
+  bulk_g2s(dst + kPhaseOff + kPhaseBytes, src + kPhaseOff + kPhaseBytes, kTail, &S.plan_bar);
+  bulk_g2s(&S.cp, plan_cta_record(a.plan, blockIdx.x), sizeof(CtaPlan), &S.plan_bar);
 }
 
 // The header of a plan through L2 (another launch may have written it).
@@ -288,9 +307,12 @@ __device__ bool cache_fetch(const DecodeArgs &a, int k, PlanShared &ps, CtaPlan 
   same = __syncthreads_and(same);
   if (same) {
     uint4 *dst = reinterpret_cast<uint4 *>(&ps);
+    constexpr int kP0 = kPhaseOff / 16, kP1 = (kPhaseOff + kPhaseBytes) / 16;  // (the launch's table)
 #pragma unroll
-    for (int r = 0; r < kPer; ++r)
-      if (tid + r * nt < kShared) dst[tid + r * nt] = v[r];
+    for (int r = 0; r < kPer; ++r) {
+      const int i = tid + r * nt;
+      if (i < kShared && (i < kP0 || i >= kP1)) dst[i] = v[r];
+    }
     if (tid < kRec) reinterpret_cast<uint4 *>(&cp)[tid] = rv;
   }
   return same;
@@ -1643,6 +1665,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // first K/V tiles.  The next launch on the stream may start once every CTA
   // holds its plan (below): a plan launch that follows may then rewrite it.
   if (tid == 0) {
+    // the plan's barrier first: under the early-loads promise its copies are
+    // issued before the other set-up
+    mbar_init(&S.plan_bar, 1);
+    fence_mbar_init();
+    if (!kCache && a.early) issue_plan_copies(a, S);
     tma_prefetch_desc(&tm_k);  // (kernel parameters)
     tma_prefetch_desc(&tm_v);
     for (int s = 0; s < Ring<kFp8>::NS; ++s) {
@@ -1664,13 +1691,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 4; ++b) mbar_init(&S.rec_ready[b], 4);  // one per softmax warp
     mbar_init(&S.mma_done, 1);
-    mbar_init(&S.plan_bar, 1);
     mbar_init(&S.app_bar, 1);
     S.abort_flag = 0;
     S.tiles_done = 0;
     S.plan_ok = 1;
     fence_mbar_init();
   }
+  // this launch's RoPE table (no plan copy writes these bytes)
+  if (tid >= kThreads - 64) S.ps.cache.phase[tid - (kThreads - 64)] = a.phase[tid - (kThreads - 64)];
   if (warp == kWarpMma) {
     tmem_alloc(&S.tmem_base, Ring<kFp8>::TC);
     tmem_relinquish();
@@ -1729,20 +1757,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k = S.cache_cur;
       if (!cache_fetch(a, k, S.ps, S.cp, tid, kThreads)) build_cached_plan(a, S, k);
     } else {
-      if (tid == 0) {
-        mbar_arrive_expect_tx(&S.plan_bar, sizeof(PlanShared) + sizeof(CtaPlan));
-        bulk_g2s(&S.ps, a.plan + kPlanHeaderBytes, sizeof(PlanShared), &S.plan_bar);
-        bulk_g2s(&S.cp, plan_cta_record(a.plan, blockIdx.x), sizeof(CtaPlan), &S.plan_bar);
-        if (!plan_matches(a, a.plan)) S.plan_ok = 0;
-      }
-      __syncthreads();  // the barrier is initialised
+      if (tid == 0 && !a.early) issue_plan_copies(a, S);
+      __syncthreads();  // the barriers are initialised
       if (!mbar_wait(&S.plan_bar, 0)) {
         plan_timeout = true;
         S.plan_ok = 0;
       }
+      if (tid == 0 &&
+          !header_matches(a, *reinterpret_cast<const PlanHeader *>(S.q), static_cast<int>(gridDim.x)))
+        S.plan_ok = 0;
     }
-    __syncthreads();  // the plan is in place: the table may be refreshed
-    if (tid < 64) S.ps.cache.phase[tid] = a.phase[tid];  // this launch's RoPE table
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -169,7 +169,7 @@ constexpr int kCacheEntries = 384;  // view entries (rows x view blocks) held in
 constexpr int kMaxBlockRefs = HW_MAX_REFS_PER_BLOCK;  // view entries naming one block
 constexpr int kCacheRows = 384;     // q_pos entries held in shared memory
 
-struct MetaCache {
+struct alignas(16) MetaCache {
   uint64_t phase[64];           // RoPE phase increments (the kernel argument's table)
   int32_t vb[kCacheEntries];    // view_block
   int32_t voff[kCacheEntries];  // view_offset
