@@ -1096,7 +1096,7 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[kN], int lane) {
 template <bool kFp8>
 __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int seg, int64_t sid,
                                 int nq, int ws, int lane, int row, NamedSync<1, 128> sync,
-                                float vmul) {
+                                float vmul, bool fin) {
   using R = Ring<kFp8>;
   wait_or_abort(S, a, &S.o_full[seg & 1], (seg >> 1) & 1);
   tc_fence_after();
@@ -1143,16 +1143,33 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
 #pragma unroll
     for (int j = 0; j < kN; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * vmul);
   }
-  // 16-byte stores: a 4 x 4 transpose within each group of four lanes gives
-  // lane 4q + r the elements d = 4q .. 4q+3 (of the warp's 32) of column
-  // 4b + r, for each block b of four columns - 8 store instructions instead
-  // of 32.  (Inside this kernel the tail's cost follows its count of global
-  // store instructions: the 32 scalar stores took ~0.86 us, measured with
-  // globaltimer stamps.)
+  // 16-byte stores, 8 instructions a thread instead of 32 scalar ones (the
+  // tail's cost follows its count of global store instructions: the scalar
+  // stores took ~0.86 us, measured with globaltimer stamps).  The CTA's last
+  // records (fin: every copy and product is done, the ring is idle) go
+  // through stage 0; the others by a 4 x 4 transpose within each group of
+  // four lanes, which gives lane 4q + r the elements d = 4q .. 4q+3 (of the
+  // warp's 32) of column 4b + r, for each block b of four columns.
+  if (fin) {
+    float *stg = reinterpret_cast<float *>(S.stage[0]);
+    constexpr int kPitch = 132;  // floats a column: 16-B rows, conflict-free
+#pragma unroll
+    for (int j = 0; j < kN; ++j) stg[j * kPitch + row] = __uint_as_float(o[j]);
+    sync();
+    const int t = threadIdx.x - kWarpSoft * 32;  // 0..127
+#pragma unroll
+    for (int k = 0; k < kN * 128 / 4 / 128; ++k) {
+      const int f4 = k * 128 + t, j = f4 >> 5, c = f4 & 31;  // column j, chunk c of 32
+      if (j < nq)
+        *reinterpret_cast<float4 *>(record_ptr(a, slot, j) + 4 * c) =
+            *reinterpret_cast<const float4 *>(stg + j * kPitch + 4 * c);
+    }
+  }
   const int r4 = lane & 3;
   const int d0 = row - r4;  // first element of the lane's group
 #pragma unroll
   for (int b = 0; b < kN / 4; ++b) {
+    if (fin) break;
     float v0 = __uint_as_float(o[4 * b]), v1 = __uint_as_float(o[4 * b + 1]);
     float v2 = __uint_as_float(o[4 * b + 2]), v3 = __uint_as_float(o[4 * b + 3]);
     const bool odd = lane & 1, hi = lane & 2;
@@ -1415,7 +1432,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     if (threadIdx.x == kWarpSoft * 32) *reinterpret_cast<volatile int32_t *>(&S.tiles_done) = i + 1;
 
     if (pend >= 0) {  // records of the previous segment, one tile late
-      segment_records<kFp8>(a, S, tl, pend, pend_sid, pend_nq, ws, lane, row, sync, pend_vmul);
+      segment_records<kFp8>(a, S, tl, pend, pend_sid, pend_nq, ws, lane, row, sync, pend_vmul, false);
       pend = -1;
     }
     if (last) {
@@ -1435,7 +1452,7 @@ __device__ void softmax_role(const DecodeArgs &a, TcSmem &S, uint32_t tmem, int6
     }
   }
   if (pend >= 0)
-    segment_records<kFp8>(a, S, tl, pend, pend_sid, pend_nq, ws, lane, row, sync, pend_vmul);
+    segment_records<kFp8>(a, S, tl, pend, pend_sid, pend_nq, ws, lane, row, sync, pend_vmul, true);
 }
 
 constexpr int kPlanWarps = kThreads / 32;

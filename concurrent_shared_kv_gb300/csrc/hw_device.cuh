@@ -866,18 +866,32 @@ __device__ void merge_phase(const DecodeArgs &a, const PlanCore &P, const MetaCa
         for (int e = 0; e < EPL; ++e) orow[e] = from_f32<T>(0.f);
         if (lane == 0 && a.lse) a.lse[ob] = -INFINITY;
       } else if (ok) {
+        // the g <= 8 warps' partials unrolled over all 8 (indexes wrapped
+        // into the arrays, the terms past g skipped): the loads and scale
+        // factors are independent of one another, and the sums keep the warp
+        // order of a plain loop
+        constexpr int kW = 8;
+        static_assert(sizeof(Z.wm) / sizeof(Z.wm[0]) == kW, "one partial per warp");
         const int w0 = p * g;
+        float wm[kW], wl[kW];
+#pragma unroll
+        for (int w2 = 0; w2 < kW; ++w2) {
+          wm[w2] = w2 < g ? Z.wm[(w0 + w2) & (kW - 1)] : -INFINITY;
+          wl[w2] = Z.wl[(w0 + w2) & (kW - 1)];
+        }
         float Mx = -INFINITY;
-        for (int w2 = 0; w2 < g; ++w2) Mx = fmaxf(Mx, Z.wm[w0 + w2]);
+#pragma unroll
+        for (int w2 = 0; w2 < kW; ++w2) Mx = fmaxf(Mx, wm[w2]);
         float L = 0.f, sum[EPL];
 #pragma unroll
         for (int e = 0; e < EPL; ++e) sum[e] = 0.f;
-        for (int w2 = 0; w2 < g; ++w2) {
-          if (Z.wm[w0 + w2] == -INFINITY) continue;
-          const float f = ex2(Z.wm[w0 + w2] - Mx);
-          L += Z.wl[w0 + w2] * f;
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) sum[e] += Z.acc[w0 + w2][lane * EPL + e] * f;
+        for (int w2 = 0; w2 < kW; ++w2) {
+          if (wm[w2] == -INFINITY) continue;
+          const float f = ex2(wm[w2] - Mx);
+          L += wl[w2] * f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) sum[e] += Z.acc[(w0 + w2) & (kW - 1)][lane * EPL + e] * f;
         }
         // L = 0: view limits left the row no token (its partials are empty)
         const bool any = L > 0.f;
