@@ -176,7 +176,8 @@ int hw_workspace_init(void *workspace, size_t bytes, void *stream);
  *                     that row's view (any int32; the rotation uses i_q - offset)
  *  q_pos        dev   int32 [n_rows], i_q: the query's position in its view
  *  q_to_kv      dev   int32 [Hq] or NULL (grouped heads, hq / (Hq/Hkv))
- *  out          dev   [n_rows][Hq][D] dtype
+ *  out          dev   [n_rows][Hq][D] dtype, any element-aligned address (rows
+ *                     are written with vector stores when the address allows)
  *  lse          dev   float [n_rows][Hq] or NULL
  *  workspace    dev   >= hw_attn_decode_workspace_size bytes, 256-byte aligned,
  *                     zeroed once with hw_workspace_init; one call at a time
