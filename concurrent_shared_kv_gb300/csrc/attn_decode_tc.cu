@@ -65,9 +65,10 @@ constexpr uint32_t kQBytes = 2 * kQHalf;
 constexpr uint32_t kPBytes = kT * kN * 2;     // [128 tokens][32 heads], 64-B swizzled; it
                                               // lives in the stage's K region, free once
                                               // the tile's QK product has completed
+static_assert(kPBytes <= 2 * kBox, "P fits the K region of a stage");
 constexpr uint32_t kSCols = 2 * kN;           // S buffer: S_hi [0,32), S_lo [32,64)
-constexpr uint32_t kTmemCols = 256;           // S0 [0,64)  S1 [64,128)  O0 [128,160)  O1 [160,192)
-constexpr uint32_t kColO = 2 * kSCols;        // segment k accumulates in O[k & 1]
+constexpr uint32_t kTmemCols = 256;           // S0 [0,64)  S1 [64,128)  O0 [128,160)  O1 [160,192);
+                                              // segment k accumulates in O[k & 1]
 constexpr float kLazy = 8.f;                  // rescale only when the max grows by > 2^8
 // E4M3 caches: P goes to the tensor cores as E4M3 codes of 2^6 p with p <=
 // 2^2, so 2^6 p <= 256 stays below E4M3's largest value (448) while weights
@@ -360,13 +361,6 @@ __device__ __forceinline__ bool seg_last_unit(const UnitPos &x, int64_t u, int64
   return u + 1 == u1 || u + 1 == x.seg_first + x.tiles;
 }
 
-// order-preserving float <-> int map for integer max reductions
-__device__ __forceinline__ int f2ord(float f) {
-  const int i = __float_as_int(f);
-  return i >= 0 ? i : i ^ 0x7fffffff;
-}
-__device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
-
 // Named barrier 1 over the 128 softmax threads, returning the OR of `pred`.
 __device__ __forceinline__ bool bar_red_or_128(bool pred) {
   uint32_t out;
@@ -474,7 +468,7 @@ __device__ __forceinline__ TileRef tile_ref(const PlanCore &P, int n_blocks, int
 
 template <bool kFp8>
 __device__ __forceinline__ uint8_t *stage_ptr(TcSmem &S, int s) {
-  return S.stage[0] + s * Ring<kFp8>::SB;
+  return &S.stage[0][0] + s * Ring<kFp8>::SB;  // (the ring as one byte array)
 }
 
 // Streams the CTA's tiles through the ring.  The first n_first come decoded
@@ -1164,25 +1158,25 @@ __device__ void segment_records(const DecodeArgs &a, TcSmem &S, uint32_t tl, int
         *reinterpret_cast<float4 *>(record_ptr(a, slot, j) + 4 * c) =
             *reinterpret_cast<const float4 *>(stg + j * kPitch + 4 * c);
     }
-  }
-  const int r4 = lane & 3;
-  const int d0 = row - r4;  // first element of the lane's group
+  } else {
+    const int r4 = lane & 3;
+    const int d0 = row - r4;  // first element of the lane's group
 #pragma unroll
-  for (int b = 0; b < kN / 4; ++b) {
-    if (fin) break;
-    float v0 = __uint_as_float(o[4 * b]), v1 = __uint_as_float(o[4 * b + 1]);
-    float v2 = __uint_as_float(o[4 * b + 2]), v3 = __uint_as_float(o[4 * b + 3]);
-    const bool odd = lane & 1, hi = lane & 2;
-    float t = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-    if (odd) v0 = t; else v1 = t;
-    t = __shfl_xor_sync(0xffffffffu, odd ? v2 : v3, 1);
-    if (odd) v2 = t; else v3 = t;
-    t = __shfl_xor_sync(0xffffffffu, hi ? v0 : v2, 2);
-    if (hi) v0 = t; else v2 = t;
-    t = __shfl_xor_sync(0xffffffffu, hi ? v1 : v3, 2);
-    if (hi) v1 = t; else v3 = t;
-    const int j = 4 * b + r4;
-    if (j < nq) *reinterpret_cast<float4 *>(record_ptr(a, slot, j) + d0) = make_float4(v0, v1, v2, v3);
+    for (int b = 0; b < kN / 4; ++b) {
+      float v0 = __uint_as_float(o[4 * b]), v1 = __uint_as_float(o[4 * b + 1]);
+      float v2 = __uint_as_float(o[4 * b + 2]), v3 = __uint_as_float(o[4 * b + 3]);
+      const bool odd = lane & 1, hi = lane & 2;
+      float t = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+      if (odd) v0 = t; else v1 = t;
+      t = __shfl_xor_sync(0xffffffffu, odd ? v2 : v3, 1);
+      if (odd) v2 = t; else v3 = t;
+      t = __shfl_xor_sync(0xffffffffu, hi ? v0 : v2, 2);
+      if (hi) v0 = t; else v2 = t;
+      t = __shfl_xor_sync(0xffffffffu, hi ? v1 : v3, 2);
+      if (hi) v1 = t; else v3 = t;
+      const int j = 4 * b + r4;
+      if (j < nq) *reinterpret_cast<float4 *>(record_ptr(a, slot, j) + d0) = make_float4(v0, v1, v2, v3);
+    }
   }
   if (ws == 0 && lane < nq) {
     const float(*ls)[kN] = S.lsave[seg & 1];
@@ -1754,7 +1748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (kFp8) {
     // the ones tile of the l product (E4M3 1.0 = 0x38 in every byte, so its
     // swizzle is moot), seen by the tensor cores after the barrier below
-    uint4 *ones = reinterpret_cast<uint4 *>(S.stage[0] + kOnesOff);
+    uint4 *ones = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(S.stage) + kOnesOff);
     for (int i = tid; i < static_cast<int>(kF8Box / 16); i += kThreads)
       ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
     fence_proxy_async_smem();
